@@ -1,0 +1,404 @@
+#!/usr/bin/env python3
+"""Benchmark: MoE expert-parallel dispatch + combine on one GB300.
+
+A step is one whole pass of the path over one batch of N simulated ranks' tokens:
+routing layout (histogram, scans, placements) -> dispatch send (pack + per-peer write) ->
+dispatch recv (grouped expert rows) -> identity expert -> combine send (reverse shuffle +
+per-peer write back) -> combine recv (fp32 weighted sum -> bf16).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1] [--impl reference]
+
+Prints one JSON line (rank 0). `value` is tokens/s over all GPUs: (N*T tokens per
+simulated group) x (GPUs) / (step time, max over ranks), timed with CUDA events on the
+launching stream, inputs resident in HBM, L2 flushed (a write of 2x the L2 size) before
+every timed step. With --gpus > 1 each GPU runs an independent replica of the whole
+simulated group (the one-GPU path has no cross-GPU exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "dispatch+combine tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+KERNELS = ["route_count", "layout_maps", "quant_fp8", "pack", "scatter", "unpack", "expert",
+           "combine_pack", "combine_scatter", "combine_reduce"]
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--config", type=int, default=1, help="workload index (1: EP8 T128 H7168 E256 R8 bf16)")
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--mover", choices=["tma", "ldg"], default="tma")
+    p.add_argument("--tma-stages", type=int, default=0)
+    p.add_argument("--ctas-per-sm", type=int, default=0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work for the oracle baseline")
+    return p.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------- distributed helpers
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+    ws, rank, _ = dist_env()
+    if ws > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend, rank=rank, world_size=ws)
+    return dist if ws > 1 else None
+
+
+def max_over_ranks(value: float, dist, device=None) -> float:
+    """Max of a float over all ranks (identity on one rank)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ---------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampled every 20 ms while running; summarised on stop()."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"moe_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)  # let it emit its first sample
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.05)
+        self.proc.terminate()
+        self.proc.wait()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[3:]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for n, v in zip(names[1:], r[3][1:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        loaded = [r for r in rows if r[2] > 0.25 * max(x[2] for x in rows)] or rows
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------- byte accounting
+
+def algorithmic_bytes(wl: workloads.Workload, P: int, Pk: int) -> dict:
+    """Bytes each kernel must move per launch: payload reads + writes (index, weight and layout
+    traffic is under 1% for the data kernels and is counted only for the layout kernels).
+    P = routed pairs, Pk = pairs kept in the grouped buffers (P unless capacity dropped some)."""
+    N, T, H, E, R, L = wl.N, wl.T, wl.H, wl.E, wl.R, wl.L
+    B, cap, RB = wl.row_bytes, wl.cap_eff, wl.RB
+    tok = N * T
+    P_all = tok * R
+    return {
+        "route_count": 8 * P_all + 4 * N * E * 5,
+        "layout_maps": 32 * P_all + 4 * E * cap + 4 * N * RB,
+        "quant_fp8": tok * 2 * H + tok * B,
+        "pack": tok * B + P * B,
+        "scatter": 2 * P * B,
+        "unpack": 2 * P * B,
+        "expert": Pk * (H + H // 32) + Pk * 2 * H if wl.payload == "fp8" else 2 * Pk * 2 * H,
+        "combine_pack": 2 * Pk * 2 * H,
+        "combine_scatter": 2 * Pk * 2 * H,
+        "combine_reduce": Pk * 2 * H + tok * 2 * H,
+    }
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        if d.get("hbm_gbs"):
+            return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "combine_routing_count_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on these sources."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path))
+    if d.get("source_sha") != kernel_source_sha():
+        return None
+    return d.get("workloads", {}).get(workload, {}).get(kernel)
+
+
+# ---------------------------------------------------------------------------- CPU oracle baseline
+
+def cpu_baseline(wl, inp, seconds: float) -> dict:
+    import oracle
+    b = oracle.alloc_step(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, wl.payload)
+    oracle.run_step(b, inp["x"], inp["idx"], inp["w"])   # first touch of the buffers, untimed
+    times = []
+    t_end = time.perf_counter() + seconds
+    while len(times) < 3 or time.perf_counter() < t_end:
+        t0 = time.perf_counter()
+        oracle.run_step(b, inp["x"], inp["idx"], inp["w"])
+        times.append(time.perf_counter() - t0)
+    med = statistics.median(times)
+    return {"value": wl.N * wl.T / med, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{len(times)} whole steps of {wl.name} (all {wl.N} simulated ranks), median "
+                      f"{med * 1e3:.1f} ms, single-threaded C",
+            "out": b["out"]}
+
+
+# ---------------------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import torch
+    from combine_routing_count_gb300 import KERNEL_NAMES, MoeEP, MoeProf, build, lib
+    build.build()
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = dist_init("nccl")
+
+    wl = workloads.config(args.config)
+    inp = workloads.make_inputs(wl)
+    ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, wl.payload, alias_buffers=(wl.payload == "bf16"),
+               flags=1 if args.mover == "ldg" else 0, tma_stages=args.tma_stages, ctas_per_sm=args.ctas_per_sm)
+    x = torch.from_numpy(inp["x"]).view(torch.bfloat16).to(device)
+    idx = torch.from_numpy(inp["idx"]).to(device)
+    w = torch.from_numpy(inp["w"]).to(device)
+    stream = torch.cuda.current_stream()
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=device)
+
+    def step():
+        ep.forward(x, idx, w)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    code, bits = ep.status()
+    if code != 0:
+        raise RuntimeError(f"device status {code} bits {bits:#x}")
+    lay = ep.layout_arrays()
+    P = int(lay["rtot"].sum().item())
+    Pk = int((lay["slot"] >= 0).sum().item())
+
+    # per-step, per-kernel events through the library's profiling hook
+    K = args.steps
+    profs = []
+    for _ in range(K):
+        pr = MoeProf()
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(KERNEL_NAMES))]
+        for i, e in enumerate(evs):
+            e.record(stream)
+            pr.events[i] = e.cuda_event
+        profs.append((pr, evs))
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    torch.cuda.synchronize()
+
+    vis = [v.strip() for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+    sampler = ClockSampler(vis[local] if local < len(vis) else local)
+    sampler.start()
+    barrier(dist, device)
+    torch.cuda.synchronize()
+    n0 = lib().moe_launch_count()
+    for i in range(K):
+        flush.zero_()
+        pr, _ = profs[i]
+        pr.n = 0
+        ep.layout.prof = ctypes.pointer(pr)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(dist, device)
+    launches = lib().moe_launch_count() - n0
+    clocks = sampler.stop()
+    ep.layout.prof = None
+    code, bits = ep.status()
+    if code != 0:
+        raise RuntimeError(f"device status {code} bits {bits:#x}")
+
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    per_kernel = {}
+    for pr, evs in profs:
+        for j in range(pr.n):
+            name = KERNEL_NAMES[pr.kernel[j]]
+            per_kernel.setdefault(name, []).append(evs[2 * j].elapsed_time(evs[2 * j + 1]))
+    mean_ms = statistics.fmean(step_ms)
+    mean_ms_all = max_over_ranks(mean_ms, dist, device)
+    tokens = wl.N * wl.T * ws
+    value = tokens / (mean_ms_all * 1e-3)
+
+    peak, peak_kind = measured_peak()
+    ab = algorithmic_bytes(wl, P, Pk)
+    kernels = {}
+    for name, ts in per_kernel.items():
+        us = statistics.fmean(ts) * 1e3 / 1.0
+        launches_per_step = len(ts) / K
+        gbs = ab[name] / (us * 1e-6) / 1e9
+        kernels[name] = {"us": round(us, 2), "launches_per_step": launches_per_step, "bytes": ab[name],
+                         "gbs": round(gbs, 1), "frac": round(gbs / peak, 3)}
+    dom = max(kernels, key=lambda k: kernels[k]["us"] * kernels[k]["launches_per_step"])
+    step_bytes = sum(ab[k] * kernels[k]["launches_per_step"] for k in kernels)
+
+    # end to end through the C ABI with host buffers: H2D inputs, the pass, D2H output
+    h_x = torch.from_numpy(inp["x"]).view(torch.bfloat16).pin_memory()
+    h_idx = torch.from_numpy(inp["idx"]).pin_memory()
+    h_w = torch.from_numpy(inp["w"]).pin_memory()
+    h_out = torch.empty((wl.N, wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
+    for _ in range(3):
+        ep.forward_host(h_x, h_idx, h_w, h_out, x, idx, w)
+    torch.cuda.synchronize()
+    e_start = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    e_end = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for i in range(K):
+        flush.zero_()
+        e_start[i].record(stream)
+        ep.forward_host(h_x, h_idx, h_w, h_out, x, idx, w)
+        e_end[i].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(statistics.fmean(s.elapsed_time(e) for s, e in zip(e_start, e_end)), dist, device)
+    h2d = inp["x"].nbytes + inp["idx"].nbytes + inp["w"].nbytes
+    d2h = wl.N * wl.T * wl.H * 2
+
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(mean_ms_all, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8+bf16" if wl.payload == "fp8" else "bf16",
+        "data": "synthetic (seeded; DeepSeek-V3/Kimi-K2-shaped routing, identity experts)",
+        "config": {"workload": wl.name, "N_ranks_simulated": wl.N, "T": wl.T, "H": wl.H, "E": wl.E, "R": wl.R,
+                   "payload": wl.payload, "routing": wl.routing, "seed": wl.seed, "mover": args.mover,
+                   "l2": "flushed before every timed step (write of 2x L2)",
+                   "parallelism": f"{ws} independent replica(s) of the {wl.N}-rank group"},
+        "hbm_gbs": round(step_bytes / (mean_ms * 1e-3) / 1e9, 1),
+        "hbm_frac": round(step_bytes / (mean_ms * 1e-3) / 1e9 / peak, 3),
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["gbs"], "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": kernels[dom]["frac"],
+                     "bytes_per_launch": ab[dom], "traffic": ncu_traffic(dom, wl.name)},
+        "kernels": kernels,
+        "e2e": {"value": round(tokens / (e2e_ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(e2e_ms, 4),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "path": "moe_forward_host (C ABI)"},
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cb = cpu_baseline(wl, inp, args.cpu_seconds)
+        gpu_out = ep.out.cpu().view(torch.int16).numpy().view(np.uint16)
+        out["parity"] = {"out_bit_exact_vs_oracle": bool(np.array_equal(gpu_out, cb.pop("out")))}
+        out["cpu_baseline"] = cb
+    if dist is not None:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+# ---------------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The oracle, as it stands, timed on the host cores: K whole steps of the same workload."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    wl = workloads.config(args.config)
+    inp = workloads.make_inputs(wl)
+    b = oracle.alloc_step(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, wl.payload)
+    oracle.run_step(b, inp["x"], inp["idx"], inp["w"])   # first touch
+    for _ in range(max(0, args.warmup - 1)):
+        oracle.run_step(b, inp["x"], inp["idx"], inp["w"])
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.run_step(b, inp["x"], inp["idx"], inp["w"])
+        times.append(time.perf_counter() - t0)
+    mean = statistics.fmean(times)
+    value = wl.N * wl.T / mean
+    sample = f"{args.steps} whole steps of {wl.name} (all {wl.N} simulated ranks), single-threaded C oracle"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8+bf16" if wl.payload == "fp8" else "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "N_ranks_simulated": wl.N, "T": wl.T, "H": wl.H, "E": wl.E, "R": wl.R,
+                   "payload": wl.payload, "routing": wl.routing, "seed": wl.seed},
+        "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

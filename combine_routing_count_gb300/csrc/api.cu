@@ -1,0 +1,362 @@
+// C ABI of libmoe_ep (declared in include/moe_ep.h): argument checks, workspace carving and
+// the kernel sequence of each dispatch/combine step. No allocation, no synchronisation
+// (except moe_status_sync), no fallback: every step runs in this library's kernels.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+namespace moe {
+
+std::atomic<uint64_t> g_launches{0};
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxE = 1536;
+constexpr int64_t kMaxScanInts = 56832;  // N*E + N*N ints staged in shared memory
+constexpr int64_t kI32 = 0x7fffffff;
+
+struct DevInfo {
+  int num_sms = 0;
+  int smem_optin = 0;
+  int smem_per_sm = 0;
+};
+DevInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status make_geo(const moe_dims* d, Geo& g) {
+  if (!d) return MOE_ERR_INVALID_ARG;
+  if (d->N < 1 || d->T < 0 || d->E < 1 || d->R < 1 || d->cap < 0 || d->H < 8) return MOE_ERR_INVALID_ARG;
+  if (d->E % d->N != 0 || d->H % 8 != 0) return MOE_ERR_INVALID_ARG;
+  if (d->payload != MOE_PAYLOAD_BF16 && d->payload != MOE_PAYLOAD_FP8_E4M3_B128) return MOE_ERR_INVALID_ARG;
+  if (d->payload == MOE_PAYLOAD_FP8_E4M3_B128 && d->H % 128 != 0) return MOE_ERR_INVALID_ARG;
+  if (d->E > kMaxE) return MOE_ERR_INVALID_ARG;
+  const int64_t N = d->N, T = d->T, E = d->E, R = d->R, L = E / N;
+  if (N * E + N * N > kMaxScanInts) return MOE_ERR_INVALID_ARG;
+  const int64_t cap = d->cap > 0 ? d->cap : N * T;  // 0 only when there are no tokens
+  const int64_t RB = N * T * (R > L ? R : L);
+  if (N * T * R > kI32 || N * RB > kI32 || E * cap > kI32 || N * T * (int64_t)d->H > (int64_t)1 << 40)
+    return MOE_ERR_INVALID_ARG;
+  g.N = d->N;
+  g.T = d->T;
+  g.H = d->H;
+  g.E = d->E;
+  g.R = d->R;
+  g.L = (int)L;
+  g.cap = (int)cap;
+  g.payload = d->payload;
+  g.TR = T * R;
+  g.RB = RB;
+  g.P = N * T * R;
+  g.B = d->payload == MOE_PAYLOAD_FP8_E4M3_B128 ? (int64_t)d->H + 4 * (int64_t)(d->H / 128) : 2 * (int64_t)d->H;
+  return MOE_OK;
+}
+
+moe_status make_ctx(const moe_layout_t* lay, void* stream, Ctx& c) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DevInfo& di = g_dev[dev];
+    if (di.num_sms == 0) {
+      if (cudaDeviceGetAttribute(&di.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&di.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&di.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess) {
+        di.num_sms = 0;
+        return MOE_ERR_CUDA;
+      }
+    }
+    c.num_sms = di.num_sms;
+    c.smem_optin = di.smem_optin;
+    c.smem_per_sm = di.smem_per_sm;
+  }
+  c.device = dev;
+  c.stream = static_cast<cudaStream_t>(stream);
+  c.prof = lay->prof;
+  c.flags = lay->flags;
+  c.tma_stages = lay->tma_stages;
+  c.ctas_per_sm = lay->ctas_per_sm;
+  c.status = lay->status;
+  return MOE_OK;
+}
+
+bool layout_ok(const moe_layout_t* l) {
+  if (!l) return false;
+  const void* ps[] = {l->cnt, l->C,        l->soff,     l->roff,  l->rtot,  l->ecnt,  l->eoff,   l->pos,
+                      l->rrow, l->slot,    l->slot_src, l->recv_src, l->gsend, l->grecv, l->gslot, l->status,
+                      l->scratch};
+  for (const void* p : ps)
+    if (!p) return false;
+  return true;
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// Byte sizes of the workspace arrays, in carving order.
+struct WsPlan {
+  size_t n[18];
+  size_t total;
+};
+
+size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+WsPlan ws_plan(const Geo& g) {
+  WsPlan w;
+  const size_t N = g.N, E = g.E, P = g.P;
+  const size_t sizes[] = {N * E,           // cnt
+                          N * N,           // C
+                          N * E,           // soff
+                          N * N,           // roff
+                          N,               // rtot
+                          E,               // ecnt
+                          E * N,           // eoff
+                          P,               // pos
+                          P,               // rrow
+                          P,               // slot
+                          E * g.cap,       // slot_src
+                          N * g.RB,        // recv_src
+                          P,               // gsend
+                          P,               // grecv
+                          P,               // gslot
+                          16,              // status
+                          16};             // scratch
+  w.total = 0;
+  for (int i = 0; i < 17; ++i) {
+    w.n[i] = al256(4 * sizes[i]);
+    w.total += w.n[i];
+  }
+  return w;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+moe_status moe_check_dims(const moe_dims* dims) {
+  Geo g;
+  return make_geo(dims, g);
+}
+
+size_t moe_recv_capacity_rows(const moe_dims* dims) {
+  Geo g;
+  return make_geo(dims, g) == MOE_OK ? (size_t)g.RB : 0;
+}
+
+size_t moe_row_bytes(const moe_dims* dims) {
+  Geo g;
+  return make_geo(dims, g) == MOE_OK ? (size_t)g.B : 0;
+}
+
+int32_t moe_capacity(const moe_dims* dims) {
+  Geo g;
+  return make_geo(dims, g) == MOE_OK ? g.cap : 0;
+}
+
+size_t moe_layout_workspace_bytes(const moe_dims* dims) {
+  Geo g;
+  if (make_geo(dims, g) != MOE_OK) return 0;
+  return ws_plan(g).total;
+}
+
+moe_status moe_layout_init(const moe_dims* dims, void* d_ws, size_t ws_bytes, moe_layout_t* out, void* stream) {
+  Geo g;
+  moe_status st = make_geo(dims, g);
+  if (st != MOE_OK) return st;
+  if (!out || !d_ws || (reinterpret_cast<uintptr_t>(d_ws) & 255u)) return MOE_ERR_INVALID_ARG;
+  const WsPlan w = ws_plan(g);
+  if (ws_bytes < w.total) return MOE_ERR_INVALID_ARG;
+  uint8_t* p = static_cast<uint8_t*>(d_ws);
+  int32_t** slots[] = {&out->cnt,  &out->C,        &out->soff,     &out->roff,  &out->rtot,  &out->ecnt,
+                       &out->eoff, &out->pos,      &out->rrow,     &out->slot,  &out->slot_src, &out->recv_src,
+                       &out->gsend, &out->grecv,   &out->gslot,    &out->status, &out->scratch};
+  for (int i = 0; i < 17; ++i) {
+    *slots[i] = reinterpret_cast<int32_t*>(p);
+    p += w.n[i];
+  }
+  out->flags = 0;
+  out->prof = nullptr;
+  out->tma_stages = 0;
+  out->ctas_per_sm = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(out->status, 0, 64, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(out->scratch, 0, 64, s) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_layout(const moe_dims* dims, const int32_t* d_idx, const moe_layout_t* lay, void* stream) {
+  Geo g;
+  moe_status st = make_geo(dims, g);
+  if (st != MOE_OK) return st;
+  if (!layout_ok(lay) || (!d_idx && g.P > 0)) return MOE_ERR_INVALID_ARG;
+  Ctx c;
+  if ((st = make_ctx(lay, stream, c)) != MOE_OK) return st;
+  if ((int)layout_smem_bytes(g) > c.smem_optin) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_layout(g, d_idx, lay, c));
+}
+
+moe_status moe_quantize_fp8_b128(const moe_dims* dims, const uint16_t* d_x, uint8_t* d_xq, const moe_layout_t* lay,
+                                 void* stream) {
+  Geo g;
+  moe_status st = make_geo(dims, g);
+  if (st != MOE_OK) return st;
+  if ((int64_t)g.N * g.T == 0) return layout_ok(lay) ? MOE_OK : MOE_ERR_INVALID_ARG;  // nothing to move
+  if (g.payload != MOE_PAYLOAD_FP8_E4M3_B128 || !layout_ok(lay) || !d_x || !d_xq || !aligned16(d_x) ||
+      !aligned16(d_xq))
+    return MOE_ERR_INVALID_ARG;
+  Ctx c;
+  if ((st = make_ctx(lay, stream, c)) != MOE_OK) return st;
+  return cuda_status(launch_quant_fp8(g, d_x, d_xq, c));
+}
+
+moe_status moe_dispatch_send(const moe_dims* dims, const moe_layout_t* lay, const void* d_x, void* d_send,
+                             void* d_recv, void* stream) {
+  Geo g;
+  moe_status st = make_geo(dims, g);
+  if (st != MOE_OK) return st;
+  if ((int64_t)g.N * g.T == 0) return layout_ok(lay) ? MOE_OK : MOE_ERR_INVALID_ARG;  // nothing to move
+  if (!layout_ok(lay) || !d_x || !d_send || !d_recv || !aligned16(d_x) || !aligned16(d_send) || !aligned16(d_recv))
+    return MOE_ERR_INVALID_ARG;
+  Ctx c;
+  if ((st = make_ctx(lay, stream, c)) != MOE_OK) return st;
+  cudaError_t e = launch_move(kMovePack, g, lay, d_x, d_send, nullptr, c);
+  if (e == cudaSuccess) e = launch_move(kMoveScatter, g, lay, d_send, d_recv, nullptr, c);
+  return cuda_status(e);
+}
+
+moe_status moe_dispatch_recv(const moe_dims* dims, const moe_layout_t* lay, const void* d_recv, void* d_expert_x,
+                             float* d_expert_scale, void* stream) {
+  Geo g;
+  moe_status st = make_geo(dims, g);
+  if (st != MOE_OK) return st;
+  if ((int64_t)g.N * g.T == 0) return layout_ok(lay) ? MOE_OK : MOE_ERR_INVALID_ARG;  // nothing to move
+  const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
+  if (!layout_ok(lay) || !d_recv || !d_expert_x || !aligned16(d_recv) || !aligned16(d_expert_x))
+    return MOE_ERR_INVALID_ARG;
+  if (fp8 && (!d_expert_scale || !aligned16(d_expert_scale))) return MOE_ERR_INVALID_ARG;
+  Ctx c;
+  if ((st = make_ctx(lay, stream, c)) != MOE_OK) return st;
+  return cuda_status(launch_move(kMoveUnpack, g, lay, d_recv, d_expert_x, fp8 ? d_expert_scale : nullptr, c));
+}
+
+moe_status moe_expert_identity(const moe_dims* dims, const moe_layout_t* lay, const void* d_expert_x,
+                               const float* d_expert_scale, uint16_t* d_expert_y, void* stream) {
+  Geo g;
+  moe_status st = make_geo(dims, g);
+  if (st != MOE_OK) return st;
+  if ((int64_t)g.N * g.T == 0) return layout_ok(lay) ? MOE_OK : MOE_ERR_INVALID_ARG;  // nothing to move
+  const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
+  if (!layout_ok(lay) || !d_expert_x || !d_expert_y || !aligned16(d_expert_x) || !aligned16(d_expert_y))
+    return MOE_ERR_INVALID_ARG;
+  if (fp8 && (!d_expert_scale || !aligned16(d_expert_scale))) return MOE_ERR_INVALID_ARG;
+  Ctx c;
+  if ((st = make_ctx(lay, stream, c)) != MOE_OK) return st;
+  if (fp8)
+    return cuda_status(launch_dequant_fp8(g, lay, static_cast<const uint8_t*>(d_expert_x), d_expert_scale,
+                                          d_expert_y, c));
+  if (static_cast<const void*>(d_expert_y) == d_expert_x) return MOE_OK;  // identity by aliasing
+  return cuda_status(launch_move(kMoveCopyEx, g, lay, d_expert_x, d_expert_y, nullptr, c));
+}
+
+moe_status moe_combine_send(const moe_dims* dims, const moe_layout_t* lay, const uint16_t* d_expert_y,
+                            uint16_t* d_csend, uint16_t* d_crecv, void* stream) {
+  Geo g;
+  moe_status st = make_geo(dims, g);
+  if (st != MOE_OK) return st;
+  if ((int64_t)g.N * g.T == 0) return layout_ok(lay) ? MOE_OK : MOE_ERR_INVALID_ARG;  // nothing to move
+  if (!layout_ok(lay) || !d_expert_y || !d_csend || !d_crecv || !aligned16(d_expert_y) || !aligned16(d_csend) ||
+      !aligned16(d_crecv))
+    return MOE_ERR_INVALID_ARG;
+  Ctx c;
+  if ((st = make_ctx(lay, stream, c)) != MOE_OK) return st;
+  cudaError_t e = launch_move(kMoveCPack, g, lay, d_expert_y, d_csend, nullptr, c);
+  if (e == cudaSuccess) e = launch_move(kMoveCScatter, g, lay, d_csend, d_crecv, nullptr, c);
+  return cuda_status(e);
+}
+
+moe_status moe_combine_recv(const moe_dims* dims, const moe_layout_t* lay, const uint16_t* d_crecv, const float* d_w,
+                            uint16_t* d_out, void* stream) {
+  Geo g;
+  moe_status st = make_geo(dims, g);
+  if (st != MOE_OK) return st;
+  if ((int64_t)g.N * g.T == 0) return layout_ok(lay) ? MOE_OK : MOE_ERR_INVALID_ARG;  // nothing to move
+  if (!layout_ok(lay) || !d_crecv || !d_w || !d_out || !aligned16(d_crecv) || !aligned16(d_out))
+    return MOE_ERR_INVALID_ARG;
+  Ctx c;
+  if ((st = make_ctx(lay, stream, c)) != MOE_OK) return st;
+  return cuda_status(launch_combine_reduce(g, lay, d_crecv, d_w, d_out, c));
+}
+
+moe_status moe_forward(const moe_dims* dims, const moe_layout_t* lay, const moe_buffers_t* b, void* stream) {
+  if (!b) return MOE_ERR_INVALID_ARG;
+  Geo g;
+  moe_status st = make_geo(dims, g);
+  if (st != MOE_OK) return st;
+  const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
+  if ((st = moe_layout(dims, b->idx, lay, stream)) != MOE_OK) return st;
+  const void* xin = b->x;
+  if (fp8) {
+    if ((st = moe_quantize_fp8_b128(dims, b->x, b->xq, lay, stream)) != MOE_OK) return st;
+    xin = b->xq;
+  }
+  if ((st = moe_dispatch_send(dims, lay, xin, b->send, b->recv, stream)) != MOE_OK) return st;
+  if ((st = moe_dispatch_recv(dims, lay, b->recv, b->expert_x, b->expert_scale, stream)) != MOE_OK) return st;
+  if ((st = moe_expert_identity(dims, lay, b->expert_x, b->expert_scale, b->expert_y, stream)) != MOE_OK) return st;
+  if ((st = moe_combine_send(dims, lay, b->expert_y, b->csend, b->crecv, stream)) != MOE_OK) return st;
+  return moe_combine_recv(dims, lay, b->crecv, b->w, b->out, stream);
+}
+
+moe_status moe_forward_host(const moe_dims* dims, const moe_layout_t* lay, const moe_buffers_t* b, const uint16_t* h_x,
+                            const int32_t* h_idx, const float* h_w, uint16_t* h_out, void* stream) {
+  if (!b) return MOE_ERR_INVALID_ARG;
+  Geo g;
+  moe_status st = make_geo(dims, g);
+  if (st != MOE_OK) return st;
+  const size_t xb = (size_t)g.N * g.T * g.H * 2, pb = (size_t)g.P * 4;
+  if ((xb && (!h_x || !h_out || !b->x || !b->out)) || (pb && (!h_idx || !h_w || !b->idx || !b->w)))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (xb && cudaMemcpyAsync(b->x, h_x, xb, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (pb && cudaMemcpyAsync(b->idx, h_idx, pb, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (pb && cudaMemcpyAsync(b->w, h_w, pb, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if ((st = moe_forward(dims, lay, b, stream)) != MOE_OK) return st;
+  if (xb && cudaMemcpyAsync(h_out, b->out, xb, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_status_sync(const moe_layout_t* lay, void* stream, uint32_t* bits_out) {
+  if (!lay || !lay->status) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  uint32_t bits = 0;
+  if (cudaMemcpy(&bits, lay->status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(lay->status, 0, 4, s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (bits_out) *bits_out = bits;
+  for (int code = MOE_ERR_EXPERT_RANGE; code <= MOE_ERR_TIMEOUT; ++code)
+    if (bits & (1u << code)) return static_cast<moe_status>(code);
+  return MOE_OK;
+}
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_EXPERT_RANGE: return "expert id out of range (pair skipped)";
+    case MOE_ERR_CAPACITY: return "expert capacity exceeded (pairs dropped)";
+    case MOE_ERR_RECV_BOUND: return "receive bound N*T*max(R,E/N) exceeded";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "bounded in-kernel wait timed out";
+  }
+  return "unknown status";
+}
+
+uint64_t moe_launch_count(void) { return g_launches.load(); }
+
+}  // extern "C"

@@ -1,0 +1,82 @@
+// Host-side internals of libmoe_ep: launch context, per-kernel profiling scope and the
+// launchers each translation unit provides.
+#pragma once
+
+#include <atomic>
+
+#include "common.cuh"
+
+namespace moe {
+
+// Everything a launcher needs besides its operands.
+struct Ctx {
+  cudaStream_t stream;
+  moe_prof_t* prof;
+  int device;
+  int num_sms;
+  int smem_optin;     // max dynamic shared memory per block (opt-in), bytes
+  int smem_per_sm;    // shared memory per SM, bytes
+  uint32_t flags;
+  int tma_stages;     // 0 = automatic
+  int ctas_per_sm;    // 0 = automatic
+  int32_t* status;
+};
+
+extern std::atomic<uint64_t> g_launches;
+
+// Brackets one kernel launch with the caller's profiling events (if any) and counts it.
+struct LaunchScope {
+  Ctx& c;
+  int slot = -1;
+  LaunchScope(Ctx& ctx, moe_kernel_id id) : c(ctx) {
+    if (c.prof && c.prof->n < MOE_PROF_MAX) {
+      slot = c.prof->n++;
+      c.prof->kernel[slot] = id;
+      cudaEventRecord(static_cast<cudaEvent_t>(c.prof->events[2 * slot]), c.stream);
+    }
+  }
+  ~LaunchScope() {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (slot >= 0) cudaEventRecord(static_cast<cudaEvent_t>(c.prof->events[2 * slot + 1]), c.stream);
+  }
+};
+
+// Raises a kernel's dynamic shared memory limit to `bytes` (needed above 48 KB) once per
+// device; `cache` holds the largest value set so far for each of 64 devices.
+template <typename K>
+inline cudaError_t ensure_dyn_smem(K kernel, int device, size_t bytes, std::atomic<int>* cache) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  std::atomic<int>& c = cache[device & 63];
+  if (c.load() >= (int)bytes) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return e;
+  int cur = c.load();
+  while (cur < (int)bytes && !c.compare_exchange_weak(cur, (int)bytes)) {
+  }
+  return cudaSuccess;
+}
+
+// layout.cu
+cudaError_t launch_layout(const Geo& g, const int32_t* idx, const moe_layout_t* lay, Ctx& c);
+size_t layout_smem_bytes(const Geo& g);
+
+// movers.cu: row movement kernels.
+enum MoveKind : int {
+  kMovePack = 0,      // token rows -> R send rows
+  kMoveScatter = 1,   // send rows -> receive rows of the owner rank
+  kMoveUnpack = 2,    // receive rows -> grouped expert rows (fp8: codes + scales)
+  kMoveCPack = 3,     // grouped expert output rows -> receive order (combine send buffer)
+  kMoveCScatter = 4,  // combine send rows -> the source rank's combine receive rows
+  kMoveCopyEx = 5,    // grouped rows -> grouped rows (bf16 identity expert, distinct output)
+};
+cudaError_t launch_move(MoveKind kind, const Geo& g, const moe_layout_t* lay, const void* src, void* dst,
+                        void* dst2, Ctx& c);
+
+// numerics.cu
+cudaError_t launch_quant_fp8(const Geo& g, const uint16_t* x, uint8_t* xq, Ctx& c);
+cudaError_t launch_dequant_fp8(const Geo& g, const moe_layout_t* lay, const uint8_t* exq, const float* exs,
+                               uint16_t* ey, Ctx& c);
+cudaError_t launch_combine_reduce(const Geo& g, const moe_layout_t* lay, const uint16_t* crecv, const float* w,
+                                  uint16_t* out, Ctx& c);
+
+}  // namespace moe

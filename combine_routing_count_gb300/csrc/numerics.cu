@@ -1,0 +1,213 @@
+// Kernels that compute on the payload: block-scaled fp8 quantisation of the dispatch rows,
+// the fp8 identity expert (dequantisation to bf16), and the combine reduction.
+//
+// "Enabling trillion-parameter models on AWS EFA" (Perplexity), section "Evaluation":
+// block-scaled fp8 dispatch and bf16 combine; section "Dispatch and combine": combine
+// accumulates the tokens from the receive buffer into the output tensor, a weighted
+// average over each token's experts, on the receiving side only.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// Half a warp per 128-element block: each lane holds 8 bf16 values (one 16-byte load).
+// amax over the block by xor-shuffles inside the half warp; scale = amax / 448 (IEEE fp32
+// division; 1 when amax is 0); codes = e4m3(x / scale), round to nearest even, saturating.
+// Output row: H codes, then H/128 fp32 scales. 4-byte stores (rows are 4-byte aligned).
+__global__ void __launch_bounds__(256) k_quant_fp8(Geo g, const uint16_t* __restrict__ x, uint8_t* __restrict__ xq) {
+  const int nb = g.H / 128;
+  const int64_t nblk = (int64_t)g.N * g.T * nb;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane & 15;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t b0 = warp * 2; b0 < nblk; b0 += nwarps * 2) {  // warp-uniform trip count
+    const int64_t blk = b0 + (lane >> 4);
+    const bool act = blk < nblk;
+    const int64_t row = act ? blk / nb : 0;
+    const int b = act ? (int)(blk - row * nb) : 0;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (act) v = ld_stream16(x + row * g.H + b * 128 + sub * 8);
+    float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                  bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o, 16));
+    const float scale = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+    uint32_t w[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+          make_float2(__fdiv_rn(f[4 * i + 0], scale), __fdiv_rn(f[4 * i + 1], scale)), __NV_SATFINITE, __NV_E4M3);
+      const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+          make_float2(__fdiv_rn(f[4 * i + 2], scale), __fdiv_rn(f[4 * i + 3], scale)), __NV_SATFINITE, __NV_E4M3);
+      w[i] = (uint32_t)lo | ((uint32_t)hi << 16);
+    }
+    if (act) {
+      uint8_t* qr = xq + row * g.B;
+      uint32_t* dst = reinterpret_cast<uint32_t*>(qr + b * 128 + sub * 8);
+      dst[0] = w[0];
+      dst[1] = w[1];
+      if (sub == 0) *reinterpret_cast<float*>(qr + g.H + 4 * b) = scale;
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+  const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+  return a | (b << 16);
+}
+
+// y = bf16(float(code) * scale) for two codes (low byte first).
+__device__ __forceinline__ uint32_t dequant2(uint16_t codes, float scale) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(codes, __NV_E4M3);
+  const float lo = __half2float(__half(__half_raw{h.x}));
+  const float hi = __half2float(__half(__half_raw{h.y}));
+  return pack_bf16x2(__fmul_rn(lo, scale), __fmul_rn(hi, scale));
+}
+
+// Identity expert for the fp8 payload: one warp per used grouped row (found through the
+// pairs' gslot), 16 codes per lane per step.
+__global__ void __launch_bounds__(256) k_dequant_fp8(Geo g, const int32_t* __restrict__ gslot,
+                                                     const uint8_t* __restrict__ exq, const float* __restrict__ exs,
+                                                     uint16_t* __restrict__ ey) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int nvec = g.H / 16;
+  for (int64_t q = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; q < g.P; q += nwarps) {
+    const int gl = __ldg(gslot + q);
+    if (gl < 0) continue;
+    const uint8_t* qr = exq + (int64_t)gl * g.H;
+    const float* sr = exs + (int64_t)gl * (g.H / 128);
+    uint16_t* yr = ey + (int64_t)gl * g.H;
+    for (int v = lane; v < nvec; v += 32) {
+      const uint4 c = ld_stream16(qr + v * 16);
+      const float sc = __ldg(sr + (v * 16) / 128);
+      uint4 o0, o1;
+      o0.x = dequant2((uint16_t)(c.x & 0xffffu), sc);
+      o0.y = dequant2((uint16_t)(c.x >> 16), sc);
+      o0.z = dequant2((uint16_t)(c.y & 0xffffu), sc);
+      o0.w = dequant2((uint16_t)(c.y >> 16), sc);
+      o1.x = dequant2((uint16_t)(c.z & 0xffffu), sc);
+      o1.y = dequant2((uint16_t)(c.z >> 16), sc);
+      o1.z = dequant2((uint16_t)(c.w & 0xffffu), sc);
+      o1.w = dequant2((uint16_t)(c.w >> 16), sc);
+      st16(yr + v * 16, o0);
+      st16(yr + v * 16 + 8, o1);
+    }
+  }
+}
+
+// Combine receive. Block (token u, column tile); a thread owns 8 bf16 columns (16 bytes).
+// Lane j of each warp loads pair j's send row and weight and shares them by shuffle; the
+// R rows are gathered with up to 8 loads in flight; fp32 products and sums are rounded
+// separately in slot order; dropped or invalid pairs are skipped.
+constexpr int kReduceThreads = 128;
+
+__global__ void __launch_bounds__(kReduceThreads) k_combine_reduce(Geo g, const int32_t* __restrict__ gsend,
+                                                                   const int32_t* __restrict__ gslot,
+                                                                   const float* __restrict__ w,
+                                                                   const uint16_t* __restrict__ crecv,
+                                                                   uint16_t* __restrict__ out) {
+  const int64_t u = blockIdx.x;
+  const int col = blockIdx.y * kReduceThreads + threadIdx.x;
+  const int ncol = g.H / 8;
+  const bool act = col < ncol;
+  const int lane = threadIdx.x & 31;
+  const int64_t q0 = u * g.R;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+  for (int k0 = 0; k0 < g.R; k0 += 32) {
+    int myrow = -1;
+    float myw = 0.0f;
+    if (k0 + lane < g.R) {
+      const int gs = __ldg(gsend + q0 + k0 + lane);
+      const int gl = __ldg(gslot + q0 + k0 + lane);
+      if (gs >= 0 && gl >= 0) {
+        myrow = gs;
+        myw = __ldg(w + q0 + k0 + lane);
+      }
+    }
+    const int kn = min(32, g.R - k0);
+    for (int j0 = 0; j0 < kn; j0 += 8) {
+      int rk[8];
+      float wk[8];
+      uint4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        rk[j] = __shfl_sync(kFull, myrow, (j0 + j) & 31);
+        wk[j] = __shfl_sync(kFull, myw, (j0 + j) & 31);
+        if (j0 + j >= kn) rk[j] = -1;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        v[j] = make_uint4(0, 0, 0, 0);
+        if (act && rk[j] >= 0) v[j] = ld_stream16(crecv + (int64_t)rk[j] * g.H + col * 8);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (rk[j] < 0) continue;
+        const float f[8] = {bf16_lo(v[j].x), bf16_hi(v[j].x), bf16_lo(v[j].y), bf16_hi(v[j].y),
+                            bf16_lo(v[j].z), bf16_hi(v[j].z), bf16_lo(v[j].w), bf16_hi(v[j].w)};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(wk[j], f[i]));
+      }
+    }
+  }
+  if (act) {
+    uint4 o;
+    o.x = pack_bf16x2(acc[0], acc[1]);
+    o.y = pack_bf16x2(acc[2], acc[3]);
+    o.z = pack_bf16x2(acc[4], acc[5]);
+    o.w = pack_bf16x2(acc[6], acc[7]);
+    st16(out + u * g.H + col * 8, o);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_quant_fp8(const Geo& g, const uint16_t* x, uint8_t* xq, Ctx& c) {
+  const int64_t nblk = (int64_t)g.N * g.T * (g.H / 128);
+  if (nblk == 0) return cudaSuccess;
+  int64_t blocks = (nblk + 15) / 16;  // 8 warps x 2 blocks per CTA
+  const int64_t maxb = (int64_t)c.num_sms * 8;
+  if (blocks > maxb) blocks = maxb;
+  LaunchScope ls(c, MOE_K_QUANT_FP8);
+  k_quant_fp8<<<(unsigned)blocks, 256, 0, c.stream>>>(g, x, xq);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_fp8(const Geo& g, const moe_layout_t* lay, const uint8_t* exq, const float* exs,
+                               uint16_t* ey, Ctx& c) {
+  if (g.P == 0) return cudaSuccess;
+  int64_t blocks = (g.P + 7) / 8;
+  const int64_t maxb = (int64_t)c.num_sms * 8;
+  if (blocks > maxb) blocks = maxb;
+  LaunchScope ls(c, MOE_K_EXPERT);
+  k_dequant_fp8<<<(unsigned)blocks, 256, 0, c.stream>>>(g, lay->gslot, exq, exs, ey);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_reduce(const Geo& g, const moe_layout_t* lay, const uint16_t* crecv, const float* w,
+                                  uint16_t* out, Ctx& c) {
+  const int64_t tokens = (int64_t)g.N * g.T;
+  if (tokens == 0) return cudaSuccess;
+  const int ncol = g.H / 8;
+  dim3 grid((unsigned)tokens, (unsigned)((ncol + kReduceThreads - 1) / kReduceThreads));
+  LaunchScope ls(c, MOE_K_COMBINE_REDUCE);
+  k_combine_reduce<<<grid, kReduceThreads, 0, c.stream>>>(g, lay->gsend, lay->gslot, w, crecv, out);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,276 @@
+/*
+ * moe_ep.h — C ABI of the GB300 (sm_103a) MoE expert-parallel dispatch/combine library.
+ *
+ * The method is the one of "Enabling trillion-parameter models on AWS EFA" (Perplexity,
+ * 2025-11-04). N expert-parallel ranks each hold T tokens of hidden size H; every token
+ * is routed to R of E experts, expert e living on rank owner(e) = e / L, L = E / N.
+ *   dispatch: count tokens per (source rank, expert), scan the counts into collision-free
+ *             contiguous offsets, pack each (token, expert) pair into the source rank's
+ *             send buffer, write each destination's slice into that rank's receive buffer,
+ *             and shuffle the received rows into per-expert grouped rows [L, cap, H];
+ *   combine:  send expert outputs back with one write per peer and take, per token, the
+ *             fp32 weighted sum of its R expert outputs, stored as bf16.
+ * On one GPU all N simulated ranks live in one HBM: a rank is an address range of each
+ * buffer, and a peer "RDMA write" is a device copy into the peer's receive region.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named d_* are DEVICE pointers, h_* HOST pointers. Every device buffer must be
+ *    16-byte aligned; MOE_ERR_INVALID_ARG otherwise.
+ *  - The caller allocates and owns all memory and streams. The library never allocates,
+ *    frees or synchronises, except moe_status_sync. `stream` is a cudaStream_t (NULL = the
+ *    legacy default stream). All calls are asynchronous on that stream; a buffer may be
+ *    reused once the stream has passed its consumer (the buffer-reuse barrier between
+ *    dispatch and combine of the page's section "Dispatch and combine" is stream order).
+ *  - Host-checkable argument errors return MOE_ERR_INVALID_ARG before anything is launched.
+ *    Data-dependent errors (bad expert id, expert capacity exceeded) never trap: kernels
+ *    skip the affected pairs and OR a bit into a sticky device status word that
+ *    moe_status_sync reads and clears. A failed launch returns MOE_ERR_CUDA.
+ *  - Row layouts are row-major and dense; simulated rank r's part of every [N, ...] buffer
+ *    starts at r * (product of the remaining dimensions).
+ */
+#ifndef MOE_EP_H_
+#define MOE_EP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,  /* bad dims, NULL or misaligned pointer, workspace too small */
+    MOE_ERR_EXPERT_RANGE = 2, /* an expert id outside [0, E); its pair was left out */
+    MOE_ERR_CAPACITY = 3,     /* an expert got more than cap pairs; the excess was dropped */
+    MOE_ERR_RECV_BOUND = 4,   /* a rank received more than N*T*max(R,E/N) rows (cannot
+                                 happen with in-range ids; checked defensively) */
+    MOE_ERR_CUDA = 5,         /* a CUDA call or launch failed */
+    MOE_ERR_TIMEOUT = 6       /* a bounded wait inside a kernel ran out; work was skipped */
+} moe_status;
+
+typedef enum {
+    MOE_PAYLOAD_BF16 = 0,          /* rows of H bf16 values, B = 2H bytes */
+    MOE_PAYLOAD_FP8_E4M3_B128 = 1  /* rows of H e4m3 codes then H/128 fp32 scales,
+                                      B = H + 4*(H/128) bytes (section "Evaluation":
+                                      block-scaled fp8 dispatch, bf16 combine) */
+} moe_payload;
+
+/* Problem size, in the page's notation (section "Send and receive buffers": N ranks each
+ * dispatch T tokens, each routed to R of E experts). */
+typedef struct {
+    int32_t N;       /* simulated expert-parallel ranks, >= 1 */
+    int32_t T;       /* tokens per rank, >= 0 */
+    int32_t H;       /* hidden size: multiple of 8 (bf16), of 128 (fp8) */
+    int32_t E;       /* experts in total, multiple of N; E/N local experts per rank */
+    int32_t R;       /* experts per token, >= 1 */
+    int32_t cap;     /* rows per expert in the grouped buffers; 0 means N*T */
+    int32_t payload; /* moe_payload of the dispatched rows */
+} moe_dims;
+
+/* Kernel ids reported through moe_prof_t. */
+typedef enum {
+    MOE_K_ROUTE_COUNT = 0,     /* routing-count histogram + stable pair ranks + scans */
+    MOE_K_LAYOUT_MAPS = 1,     /* per-pair placements and inverse maps */
+    MOE_K_QUANT_FP8 = 2,       /* block-scaled fp8 quantisation */
+    MOE_K_PACK = 3,            /* dispatch send: token rows -> send rows */
+    MOE_K_SCATTER = 4,         /* dispatch "RDMA write": send slices -> peers' receive rows */
+    MOE_K_UNPACK = 5,          /* dispatch recv: receive rows -> grouped expert rows */
+    MOE_K_EXPERT = 6,          /* identity expert (fp8 dequantisation or bf16 copy) */
+    MOE_K_COMBINE_PACK = 7,    /* combine send: grouped rows -> receive order */
+    MOE_K_COMBINE_SCATTER = 8, /* combine "RDMA write": back to the source ranks */
+    MOE_K_COMBINE_REDUCE = 9,  /* combine recv: weighted sum over R -> bf16 */
+    MOE_K_NUM = 10
+} moe_kernel_id;
+
+/* Optional per-kernel timing. When moe_layout_t.prof is non-NULL, every kernel the library
+ * launches is bracketed by cudaEventRecord(events[2n]) and cudaEventRecord(events[2n+1]) on
+ * the call's stream, kernel[n] receives its moe_kernel_id and n is incremented, until n
+ * reaches MOE_PROF_MAX. The caller creates the events (cudaEvent_t cast to void*) and
+ * resets n. */
+#define MOE_PROF_MAX 32
+typedef struct {
+    void *events[2 * MOE_PROF_MAX];
+    int32_t kernel[MOE_PROF_MAX];
+    int32_t n;
+} moe_prof_t;
+
+/* moe_layout_t.flags */
+#define MOE_FLAG_LDG_MOVER 0x1u /* move rows with 16-byte register loads/stores instead of
+                                   TMA bulk copies (always used where rows are not 16-byte
+                                   multiples, e.g. fp8 with H % 512 != 0) */
+
+/*
+ * Routing layout. Device arrays carved by moe_layout_init from one caller workspace, filled
+ * by moe_layout, read by every later call (section "Send and receive buffers": per-expert
+ * counts are exchanged first, so every rank knows where its writes go and at which offset
+ * it receives from each rank; section "Dispatch and combine": the receiver computes the
+ * offsets needed for dispatch and combine). int32, row-major:
+ *   cnt  [N][E]   tokens rank s routes to expert e
+ *   C    [N][N]   C[s][d]: rows rank s sends to rank d
+ *   soff [N][E]   exclusive scan of cnt[s][.] over e: send offsets
+ *   roff [N][N]   roff[d][s]: exclusive scan of C[.][d] over s: receive offsets
+ *   rtot [N]      rows rank d receives (<= N*T*max(R,E/N))
+ *   ecnt [N][L]   rows expert l of rank d receives
+ *   eoff [N][L][N] eoff[d][l][s]: exclusive scan of cnt[.][d*L+l] over s
+ *   pos  [N][T][R] send row of pair (s,t,k): soff[s][e] + rk, rk = number of earlier
+ *                  (t',k') of rank s with the same expert; -1 for a bad expert id
+ *   rrow [N][T][R] receive row of the pair in rank owner(e); -1 for a bad id
+ *   slot [N][T][R] grouped row of the pair in expert e: eoff[d][l][s] + rk; -1 if >= cap
+ *   slot_src [N][L][cap] pair id (s*T+t)*R+k of each grouped row, -1 if unused
+ *   recv_src [N][RB]     pair id of each receive row, -1 if unused (RB = N*T*max(R,E/N))
+ *   gsend [N*T*R]  global send row of each pair, s*T*R + pos (row of d_send), or -1
+ *   grecv [N*T*R]  global receive row, owner(e)*RB + rrow (row of d_recv), or -1
+ *   gslot [N*T*R]  global grouped row, e*cap + slot (row of d_expert_x), or -1 when the
+ *                  pair's expert id is bad or the pair was dropped for capacity
+ *   status   [1]         sticky error bits, bit (1 << moe_status)
+ * Host-side fields (set by the caller after moe_layout_init, read at each call):
+ *   flags, prof, tma_stages (0 = automatic, else 1..32 stages per TMA mover CTA),
+ *   ctas_per_sm (0 = automatic, else mover CTAs per SM).
+ */
+typedef struct {
+    int32_t *cnt, *C, *soff, *roff, *rtot, *ecnt, *eoff;
+    int32_t *pos, *rrow, *slot, *slot_src, *recv_src;
+    int32_t *gsend, *grecv, *gslot;
+    int32_t *status;
+    int32_t *scratch; /* internal: completion counter of the routing-count kernel */
+    uint32_t flags;
+    moe_prof_t *prof;
+    int32_t tma_stages;
+    int32_t ctas_per_sm;
+} moe_layout_t;
+
+/* Device buffers of one whole pass (moe_forward). Shapes, with B = row bytes,
+ * RB = N*T*max(R,E/N), L = E/N:
+ *   x        [N][T][H]  bf16 tokens (input)
+ *   xq       [N][T][B]  fp8 rows (fp8 payload only; written by the pass)
+ *   idx      [N][T][R]  int32 expert ids (input)
+ *   w        [N][T][R]  fp32 router weights (input)
+ *   send     [N][T*R][B]
+ *   recv     [N][RB][B]
+ *   expert_x [N][L][cap][B] (bf16) or [N][L][cap][H] e4m3 codes (fp8)
+ *   expert_scale [N][L][cap][H/128] fp32 (fp8 only, else NULL)
+ *   expert_y [N][L][cap][H] bf16; for bf16 it may equal expert_x (identity by aliasing)
+ *   csend    [N][RB][H] bf16 (may alias recv when B == 2H)
+ *   crecv    [N][T*R][H] bf16 (may alias send when B == 2H)
+ *   out      [N][T][H]  bf16 (output) */
+typedef struct {
+    uint16_t *x;
+    uint8_t *xq;
+    int32_t *idx;
+    float *w;
+    void *send;
+    void *recv;
+    void *expert_x;
+    float *expert_scale;
+    uint16_t *expert_y;
+    uint16_t *csend;
+    uint16_t *crecv;
+    uint16_t *out;
+} moe_buffers_t;
+
+/* Validates dims: N >= 1, T >= 0, E % N == 0, R >= 1, cap >= 0, H % 8 == 0 (bf16) or
+ * H % 128 == 0 (fp8), and the library's limits (E <= 1536, N*E + N*N <= 56832, all row
+ * counts below 2^31). MOE_OK or MOE_ERR_INVALID_ARG. */
+moe_status moe_check_dims(const moe_dims *dims);
+
+/* N*T*max(R, E/N): the receive rows one rank can need (section "Send and receive
+ * buffers": with all tokens routed to one rank, it receives at most N*T*max(R,E/N)). */
+size_t moe_recv_capacity_rows(const moe_dims *dims);
+
+/* Bytes per dispatched row: 2H (bf16) or H + 4*(H/128) (fp8). 0 for invalid dims. */
+size_t moe_row_bytes(const moe_dims *dims);
+
+/* Effective per-expert capacity (cap, or N*T when cap is 0). */
+int32_t moe_capacity(const moe_dims *dims);
+
+/* Bytes of device workspace moe_layout_init needs (every array above, 256-byte aligned). */
+size_t moe_layout_workspace_bytes(const moe_dims *dims);
+
+/* Carves the layout arrays out of d_ws (ws_bytes >= moe_layout_workspace_bytes) into *out,
+ * zeroes the status word and the internal counter on `stream`, and sets the host-side
+ * fields to their defaults (flags 0, prof NULL, automatic tuning). */
+moe_status moe_layout_init(const moe_dims *dims, void *d_ws, size_t ws_bytes, moe_layout_t *out,
+                           void *stream);
+
+/* Dispatch-send step 1-2 and the receiver's offsets (section "Dispatch and combine":
+ * aggregate the routing in shared memory into per-expert token counts, then their
+ * cumulative sums as send offsets; the receiver centralises all ranks' routing and
+ * computes the offsets for dispatch and combine). Reads d_idx [N][T][R] int32, fills every
+ * array of *lay. Two kernels. */
+moe_status moe_layout(const moe_dims *dims, const int32_t *d_idx, const moe_layout_t *lay, void *stream);
+
+/* Block-scaled fp8 quantisation of the dispatch payload (section "Evaluation"): for each
+ * 128-element block of each token row of d_x [N][T][H] bf16, scale = amax/448 (1 if amax is
+ * 0) and q = e4m3(x/scale), round to nearest even, saturating. Writes d_xq [N][T][B]: the
+ * H codes of a row, then its H/128 fp32 scales. dims->payload must be fp8. */
+moe_status moe_quantize_fp8_b128(const moe_dims *dims, const uint16_t *d_x, uint8_t *d_xq,
+                                 const moe_layout_t *lay, void *stream);
+
+/* Dispatch send (section "Dispatch and combine": pack every token into the send buffer at
+ * its offsets; then one write per peer, the TransferEngine "scatter" of section "MoE
+ * routing with TransferEngine"): send[s][pos[s][t][k]] = x[s][t], then
+ * recv[d][roff[d][s] + j] = send[s][soff[s][d*L] + j] for j < C[s][d].
+ * d_x [N][T][B] (bf16 tokens, or fp8 rows from moe_quantize_fp8_b128), d_send [N][T*R][B],
+ * d_recv [N][RB][B]. Receive rows at or beyond rtot[d] are not written. Two kernels. */
+moe_status moe_dispatch_send(const moe_dims *dims, const moe_layout_t *lay, const void *d_x, void *d_send,
+                             void *d_recv, void *stream);
+
+/* Dispatch receive (section "Dispatch and combine": shuffle tokens from the receive buffer
+ * into the tensor handed to the grouped GEMM): every receive row of rank d goes to row
+ * slot of its expert l. bf16: d_expert_x [N][L][cap][H] bf16, d_expert_scale unused.
+ * fp8: d_expert_x [N][L][cap][H] e4m3 codes, d_expert_scale [N][L][cap][H/128] fp32.
+ * Rows j >= ecnt[d][l] are not written. One kernel. */
+moe_status moe_dispatch_recv(const moe_dims *dims, const moe_layout_t *lay, const void *d_recv,
+                             void *d_expert_x, float *d_expert_scale, void *stream);
+
+/* Identity expert standing in for the grouped GEMM (not a step of the paper's kernels):
+ * fp8: y = bf16(float(q) * scale) on every used grouped row; bf16: y = x, no launch when
+ * d_expert_y == d_expert_x, else a copy of the used rows. d_expert_y [N][L][cap][H] bf16. */
+moe_status moe_expert_identity(const moe_dims *dims, const moe_layout_t *lay, const void *d_expert_x,
+                               const float *d_expert_scale, uint16_t *d_expert_y, void *stream);
+
+/* Combine send (section "Dispatch and combine": routing is already known, tokens go back
+ * with a single write per peer): the reverse receive shuffle
+ * csend[d][rrow(s,t,k)] = expert_y[d][l][slot(s,t,k)], then the write back
+ * crecv[s][soff[s][d*L] + j] = csend[d][roff[d][s] + j]. d_expert_y [N][L][cap][H] bf16,
+ * d_csend [N][RB][H] bf16, d_crecv [N][T*R][H] bf16. Pairs dropped for capacity are
+ * skipped (their crecv rows are not written). Two kernels. */
+moe_status moe_combine_send(const moe_dims *dims, const moe_layout_t *lay, const uint16_t *d_expert_y,
+                            uint16_t *d_csend, uint16_t *d_crecv, void *stream);
+
+/* Combine receive (section "Dispatch and combine": accumulate the tokens from the receive
+ * buffer into the output tensor; accumulation happens on the receiving side only, section
+ * "Evaluation"): out[s][t] = bf16(sum_k w[s][t][k] * crecv[s][pos[s][t][k]]), fp32 products
+ * and sums rounded separately, k ascending, dropped or invalid pairs skipped.
+ * d_crecv [N][T*R][H] bf16, d_w [N][T][R] fp32, d_out [N][T][H] bf16. One kernel. */
+moe_status moe_combine_recv(const moe_dims *dims, const moe_layout_t *lay, const uint16_t *d_crecv,
+                            const float *d_w, uint16_t *d_out, void *stream);
+
+/* One whole pass on device-resident buffers: moe_layout, [moe_quantize_fp8_b128],
+ * moe_dispatch_send, moe_dispatch_recv, moe_expert_identity, moe_combine_send,
+ * moe_combine_recv. Returns the first error. */
+moe_status moe_forward(const moe_dims *dims, const moe_layout_t *lay, const moe_buffers_t *bufs, void *stream);
+
+/* moe_forward with host inputs and output: cudaMemcpyAsync of h_x [N][T][H] bf16,
+ * h_idx [N][T][R] and h_w [N][T][R] into bufs->x/idx/w, the pass, then cudaMemcpyAsync of
+ * bufs->out into h_out [N][T][H]. Asynchronous: the caller synchronises `stream` before
+ * reading h_out; host buffers should be pinned. */
+moe_status moe_forward_host(const moe_dims *dims, const moe_layout_t *lay, const moe_buffers_t *bufs,
+                            const uint16_t *h_x, const int32_t *h_idx, const float *h_w, uint16_t *h_out,
+                            void *stream);
+
+/* Synchronises `stream`, reads and clears the device status word. Returns MOE_OK or the
+ * lowest-numbered error whose bit is set; *bits_out (may be NULL) receives all bits. */
+moe_status moe_status_sync(const moe_layout_t *lay, void *stream, uint32_t *bits_out);
+
+/* Static string for a status code. */
+const char *moe_status_string(moe_status s);
+
+/* Number of kernels this library has launched in this process (all devices). */
+uint64_t moe_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_EP_H_ */

@@ -232,3 +232,63 @@ def forward(N, T, H, E, R, cap, payload, x: np.ndarray, idx: np.ndarray, w: np.n
     out, out64 = combine_recv(N, T, R, H, crecv, w, lay)
     res["out"], res["out64"] = out, out64
     return res
+
+
+def alloc_step(N, T, H, E, R, cap, payload) -> dict:
+    """Buffers for run_step, allocated once (np.empty: pages are touched only where written)."""
+    L = E // N
+    cap = cap if cap > 0 else N * T
+    RB = recv_rows(N, T, E, R)
+    B = H + 4 * (H // 128) if payload == "fp8" else 2 * H
+    b = {"dims": (N, T, H, E, R, cap, payload), "B": B}
+    for k in ("cnt", "soff"):
+        b[k] = np.empty((N, E), np.int32)
+    b["C"], b["roff"] = np.empty((N, N), np.int32), np.empty((N, N), np.int32)
+    b["rtot"], b["ecnt"], b["eoff"] = np.empty(N, np.int32), np.empty((N, L), np.int32), np.empty((N, L, N), np.int32)
+    for k in ("pos", "rrow", "slot"):
+        b[k] = np.empty((N, T, R), np.int32)
+    b["slot_src"], b["recv_src"] = np.empty((N, L, cap), np.int32), np.empty((N, RB), np.int32)
+    b["xq"] = np.empty((N, T, B), np.uint8) if payload == "fp8" else None
+    b["send"], b["recv"] = np.empty((N, T * R, B), np.uint8), np.empty((N, RB, B), np.uint8)
+    if payload == "fp8":
+        b["exq"], b["exs"] = np.empty((N, L, cap, H), np.uint8), np.empty((N, L, cap, H // 128), np.float32)
+        b["ey"] = np.empty((N, L, cap, H), np.uint16)
+    else:
+        b["ex"] = np.empty((N, L, cap, B), np.uint8)
+    b["csend"], b["crecv"] = np.empty((N, RB, H), np.uint16), np.empty((N, T * R, H), np.uint16)
+    b["out"], b["out64"] = np.empty((N, T, H), np.uint16), np.empty((N, T, H), np.float64)
+    return b
+
+
+def run_step(b: dict, x: np.ndarray, idx: np.ndarray, w: np.ndarray) -> int:
+    """One whole pass into preallocated buffers (same arithmetic as forward()); returns the status bits."""
+    N, T, H, E, R, cap, payload = b["dims"]
+    L_ = lib()
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    st = L_.orc_layout(N, T, E, R, cap, _i32(idx), *[_i32(b[k]) for k in
+                       ("cnt", "C", "soff", "roff", "rtot", "ecnt", "eoff", "pos", "rrow", "slot", "slot_src",
+                        "recv_src")])
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    if payload == "fp8":
+        L_.orc_quantize_fp8(N, T, H, _ptr(x, c_uint16), _ptr(b["xq"], c_uint8))
+        xrows = b["xq"]
+    else:
+        xrows = x.view(np.uint8)
+    L_.orc_dispatch_send(N, T, E, R, b["B"], _ptr(xrows, c_uint8), _i32(b["pos"]), _i32(b["C"]), _i32(b["soff"]),
+                         _i32(b["roff"]), _ptr(b["send"], c_uint8), _ptr(b["recv"], c_uint8))
+    if payload == "fp8":
+        L_.orc_dispatch_recv(N, T, E, R, cap, b["B"], H, _ptr(b["recv"], c_uint8), _i32(b["cnt"]), _i32(b["soff"]),
+                             _i32(b["roff"]), _i32(b["eoff"]), _ptr(b["exq"], c_uint8), _ptr(b["exs"], c_float))
+        L_.orc_expert_dequant(N, E // N, cap, H, _i32(b["ecnt"]), _ptr(b["exq"], c_uint8), _ptr(b["exs"], c_float),
+                              _ptr(b["ey"], c_uint16))
+        ey = b["ey"]
+    else:
+        L_.orc_dispatch_recv(N, T, E, R, cap, b["B"], 0, _ptr(b["recv"], c_uint8), _i32(b["cnt"]), _i32(b["soff"]),
+                             _i32(b["roff"]), _i32(b["eoff"]), _ptr(b["ex"], c_uint8), None)
+        ey = b["ex"]
+    L_.orc_combine_send(N, T, E, R, cap, H, ey.ctypes.data_as(POINTER(c_uint16)), _i32(b["cnt"]), _i32(b["C"]),
+                        _i32(b["soff"]), _i32(b["roff"]), _i32(b["eoff"]), _ptr(b["csend"], c_uint16),
+                        _ptr(b["crecv"], c_uint16))
+    L_.orc_combine_recv(N, T, R, H, _ptr(b["crecv"], c_uint16), _ptr(np.ascontiguousarray(w, np.float32), c_float),
+                        _i32(b["pos"]), _i32(b["slot"]), _ptr(b["out"], c_uint16), _ptr(b["out64"], c_double))
+    return int(st)

@@ -1,0 +1,169 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, element by element."""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from tests.gpu_util import compare_all, run_gpu, to_dev, u8, u16
+
+pytestmark = pytest.mark.gpu
+
+W = workloads.Workload
+# Sizes the oracle finishes in seconds that still span many CTAs and end in ragged tails.
+CASES = [
+    workloads.config(0),
+    W("ragged-bf16-H7168", 4, 37, 7168, 32, 8, "bf16", "uniform", 101),
+    W("zipf-bf16-H4096", 6, 23, 4096, 48, 8, "bf16", "zipf", 102),
+    W("skew-bf16-H2048", 8, 19, 2048, 64, 8, "bf16", "skew0", 103),
+    W("fp8-H7168", 8, 9, 7168, 48, 8, "fp8", "uniform", 104),
+    W("fp8-H384-unaligned", 3, 11, 384, 12, 3, "fp8", "uniform", 105),     # rows of 396 bytes
+    W("R1-bf16", 5, 13, 1024, 10, 1, "bf16", "uniform", 106),
+    W("R3-E-small", 2, 40, 136, 4, 3, "bf16", "uniform", 107),              # H not a multiple of 16
+    W("cap-overflow", 4, 16, 512, 8, 2, "bf16", "uniform", 108, cap=5),
+]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from combine_routing_count_gb300 import build
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+@pytest.mark.parametrize("flags", [0, 1], ids=["tma", "ldg"])
+@pytest.mark.parametrize("wl", CASES, ids=lambda w: w.name)
+def test_path_matches_oracle(orc, wl, flags):
+    inp = workloads.make_inputs(wl)
+    _, res = run_gpu(wl, inp, flags=flags)
+    compare_all(orc, wl, inp, res)
+
+
+@pytest.mark.parametrize("flags", [0, 1], ids=["tma", "ldg"])
+def test_duplicates_and_bad_ids(orc, flags):
+    wl = W("dups", 3, 21, 256, 12, 4, "bf16", "uniform", 110)
+    inp = workloads.make_inputs(wl)
+    rng = np.random.default_rng(0)
+    idx = rng.integers(0, wl.E, size=(wl.N, wl.T, wl.R)).astype(np.int32)   # duplicates allowed
+    idx[0, 3, 1] = -1
+    idx[2, 5, 0] = wl.E
+    idx[1, 7, 3] = 1 << 30
+    inp["idx"] = idx
+    _, res = run_gpu(wl, inp, flags=flags)
+    assert res["status_code"] == 2                      # MOE_ERR_EXPERT_RANGE, no trap
+    compare_all(orc, wl, inp, res)
+
+
+def test_random_tiny_layouts_bit_exact(orc):
+    from combine_routing_count_gb300 import MoeEP
+    rng = np.random.default_rng(1234)
+    for i in range(40):
+        N = int(rng.integers(1, 6))
+        L = int(rng.integers(1, 7))
+        E, T, R = N * L, int(rng.integers(0, 40)), int(rng.integers(1, 9))
+        cap = int(rng.integers(1, N * T + 1)) if (T and rng.random() < 0.3) else 0
+        idx = rng.integers(0, E, size=(N, T, R)).astype(np.int32)
+        ep = MoeEP(N, T, 64, E, R, cap)
+        ep.layout_step(to_dev(idx))
+        code, bits = ep.status()
+        got = {k: v.cpu().numpy() for k, v in ep.layout_arrays().items()}
+        o = orc.layout(N, T, E, R, cap, idx)
+        for k in ("cnt", "C", "soff", "roff", "rtot", "ecnt", "eoff", "pos", "rrow", "slot", "slot_src", "recv_src"):
+            np.testing.assert_array_equal(got[k], o[k], err_msg=f"case {i} {k}")
+        assert bits == o["status"]
+
+
+def test_large_pairs_per_rank_layout(orc):
+    """T*R well above one 1024-pair chunk per rank (prefill-sized), with duplicates."""
+    from combine_routing_count_gb300 import MoeEP
+    rng = np.random.default_rng(5)
+    N, T, E, R = 4, 1500, 64, 6
+    idx = rng.integers(0, E, size=(N, T, R)).astype(np.int32)
+    ep = MoeEP(N, T, 64, E, R, 0)
+    ep.layout_step(to_dev(idx))
+    ep.status()
+    got = {k: v.cpu().numpy() for k, v in ep.layout_arrays().items()}
+    o = orc.layout(N, T, E, R, 0, idx)
+    for k in ("cnt", "soff", "roff", "rtot", "ecnt", "eoff", "pos", "rrow", "slot", "slot_src", "recv_src"):
+        np.testing.assert_array_equal(got[k], o[k], err_msg=k)
+
+
+def test_empty_batch():
+    from combine_routing_count_gb300 import MoeEP, lib
+    ep = MoeEP(4, 0, 256, 8, 2)
+    x = torch.empty((4, 0, 256), dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty((4, 0, 2), dtype=torch.int32, device="cuda")
+    w = torch.empty((4, 0, 2), dtype=torch.float32, device="cuda")
+    ep.forward(x, idx, w)
+    code, bits = ep.status()
+    assert code == 0 and bits == 0
+    assert (ep.layout_arrays()["cnt"] == 0).all()
+
+
+def test_invalid_arguments_launch_nothing():
+    import ctypes
+    from combine_routing_count_gb300 import MoeEP, lib
+    ep = MoeEP(2, 4, 128, 4, 2)
+    L = lib()
+    n0 = L.moe_launch_count()
+    x = torch.zeros((2, 4, 128), dtype=torch.bfloat16, device="cuda")
+    # misaligned pointer
+    rc = L.moe_dispatch_send(ctypes.byref(ep.dims), ctypes.byref(ep.layout), x.data_ptr() + 2,
+                             ep.send.data_ptr(), ep.recv.data_ptr(), None)
+    assert rc == 1
+    rc = L.moe_combine_recv(ctypes.byref(ep.dims), ctypes.byref(ep.layout), None, None, None, None)
+    assert rc == 1
+    assert L.moe_launch_count() == n0
+
+
+def test_forward_host_matches_device_path(orc):
+    wl = W("host-e2e", 4, 29, 2048, 16, 4, "bf16", "zipf", 120)
+    inp = workloads.make_inputs(wl)
+    from combine_routing_count_gb300 import MoeEP
+    ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, alias_buffers=True)
+    h_x = torch.from_numpy(inp["x"]).view(torch.bfloat16).pin_memory()
+    h_idx = torch.from_numpy(inp["idx"]).pin_memory()
+    h_w = torch.from_numpy(inp["w"]).pin_memory()
+    h_out = torch.empty((wl.N, wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
+    x = torch.empty_like(h_x, device="cuda")
+    idx = torch.empty_like(h_idx, device="cuda")
+    w = torch.empty_like(h_w, device="cuda")
+    for _ in range(2):
+        ep.forward_host(h_x, h_idx, h_w, h_out, x, idx, w)
+        code, _ = ep.status()
+        assert code == 0
+        o = orc.forward(wl.N, wl.T, wl.H, wl.E, wl.R, 0, "bf16", inp["x"], inp["idx"], inp["w"])
+        np.testing.assert_array_equal(u16(h_out), o["out"])
+
+
+def test_launch_counter_counts_kernels():
+    from combine_routing_count_gb300 import MoeEP, lib
+    wl = workloads.config(0)
+    inp = workloads.make_inputs(wl)
+    ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R)
+    n0 = lib().moe_launch_count()
+    ep.forward(to_dev(inp["x"]).view(torch.bfloat16), to_dev(inp["idx"]), to_dev(inp["w"]))
+    torch.cuda.synchronize()
+    # layout (2) + pack + scatter + unpack + combine pack + combine scatter + reduce; bf16 identity aliases
+    assert lib().moe_launch_count() - n0 == 8
+
+
+def test_profiling_events_bracket_each_kernel():
+    import ctypes
+    from combine_routing_count_gb300 import MoeEP, MoeProf, KERNEL_NAMES
+    wl = W("prof", 4, 16, 1024, 16, 4, "fp8", "uniform", 130)
+    inp = workloads.make_inputs(wl)
+    ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, payload="fp8")
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(64)]
+    prof = MoeProf()
+    for i, e in enumerate(evs):
+        e.record()  # materialise the handle
+        prof.events[i] = e.cuda_event
+    prof.n = 0
+    ep.layout.prof = ctypes.pointer(prof)
+    ep.forward(to_dev(inp["x"]).view(torch.bfloat16), to_dev(inp["idx"]), to_dev(inp["w"]))
+    torch.cuda.synchronize()
+    names = [KERNEL_NAMES[prof.kernel[i]] for i in range(prof.n)]
+    assert names == ["route_count", "layout_maps", "quant_fp8", "pack", "scatter", "unpack", "expert",
+                     "combine_pack", "combine_scatter", "combine_reduce"]
+    for i in range(prof.n):
+        assert evs[2 * i].elapsed_time(evs[2 * i + 1]) >= 0.0

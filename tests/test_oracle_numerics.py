@@ -286,3 +286,14 @@ def test_combine_skips_dropped_and_invalid_pairs(orc):
             keep = [(k) for k in range(2) if lay["pos"][s, t, k] >= 0 and lay["slot"][s, t, k] >= 0]
             want = sum(np.float32(0.5) * x[s, t] for _ in keep) if keep else np.zeros(wl.H, np.float32)
             np.testing.assert_array_equal(out[s, t], from_bf16_bits(to_bf16_bits(np.asarray(want, np.float32))))
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
+def test_run_step_equals_forward(orc, wl):
+    inp = workloads.make_inputs(wl)
+    r = orc.forward(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, wl.payload, inp["x"], inp["idx"], inp["w"])
+    b = orc.alloc_step(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, wl.payload)
+    st = orc.run_step(b, inp["x"], inp["idx"], inp["w"])
+    assert st == r["layout"]["status"]
+    np.testing.assert_array_equal(b["out"], r["out"])
+    np.testing.assert_array_equal(b["out64"], r["out64"])
