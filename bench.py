@@ -45,6 +45,8 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--config", type=int, default=1, help="workload index (1: EP8 T128 H7168 E256 R8 bf16)")
+    p.add_argument("--shape", default="", help="custom workload N,T,H,E,R[,payload[,cap]] (uniform routing, "
+                   "seed 11) instead of --config, e.g. for profiling a smaller footprint")
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--mover", choices=["tma", "ldg"], default="tma")
     p.add_argument("--tma-stages", type=int, default=0)
@@ -55,6 +57,17 @@ def parse_args(argv=None):
 
 
 # ---------------------------------------------------------------------------- distributed helpers
+
+def workload_of(args) -> workloads.Workload:
+    if not args.shape:
+        return workloads.config(args.config)
+    f = args.shape.split(",")
+    N, T, H, E, R = (int(v) for v in f[:5])
+    payload = f[5] if len(f) > 5 else "bf16"
+    cap = int(f[6]) if len(f) > 6 else 0
+    return workloads.Workload(f"custom-N{N}-T{T}-H{H}-E{E}-R{R}-{payload}-cap{cap}", N, T, H, E, R, payload,
+                              "uniform", 11, cap=cap)
+
 
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
@@ -223,7 +236,7 @@ def run_ours(args):
     device = torch.device("cuda", local)
     dist = dist_init("nccl")
 
-    wl = workloads.config(args.config)
+    wl = workload_of(args)
     inp = workloads.make_inputs(wl)
     ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, wl.payload, alias_buffers=(wl.payload == "bf16"),
                flags=1 if args.mover == "ldg" else 0, tma_stages=args.tma_stages, ctas_per_sm=args.ctas_per_sm)
@@ -366,7 +379,7 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle
-    wl = workloads.config(args.config)
+    wl = workload_of(args)
     inp = workloads.make_inputs(wl)
     b = oracle.alloc_step(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, wl.payload)
     oracle.run_step(b, inp["x"], inp["idx"], inp["w"])   # first touch
