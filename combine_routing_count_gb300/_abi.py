@@ -79,6 +79,7 @@ def lib():
             "moe_layout": (c_int32, [D, c_void_p, Lp, c_void_p]),
             "moe_quantize_fp8_b128": (c_int32, [D, c_void_p, c_void_p, Lp, c_void_p]),
             "moe_dispatch_send": (c_int32, [D, Lp, c_void_p, c_void_p, c_void_p, c_void_p]),
+            "moe_dispatch_send_noalloc": (c_int32, [D, Lp, c_void_p, c_void_p, c_void_p]),
             "moe_dispatch_recv": (c_int32, [D, Lp, c_void_p, c_void_p, c_void_p, c_void_p]),
             "moe_expert_identity": (c_int32, [D, Lp, c_void_p, c_void_p, c_void_p, c_void_p]),
             "moe_combine_send": (c_int32, [D, Lp, c_void_p, c_void_p, c_void_p, c_void_p]),
@@ -109,6 +110,6 @@ def check(code: int, what: str) -> None:
 # Names a symbol-export test checks against include/moe_ep.h.
 EXPORTED = ("moe_check_dims", "moe_recv_capacity_rows", "moe_row_bytes", "moe_capacity",
             "moe_layout_workspace_bytes", "moe_layout_init", "moe_layout", "moe_quantize_fp8_b128",
-            "moe_dispatch_send", "moe_dispatch_recv", "moe_expert_identity", "moe_combine_send",
+            "moe_dispatch_send", "moe_dispatch_send_noalloc", "moe_dispatch_recv", "moe_expert_identity", "moe_combine_send",
             "moe_combine_recv", "moe_forward", "moe_forward_host", "moe_status_sync", "moe_status_string",
             "moe_launch_count")

@@ -216,6 +216,22 @@ moe_status moe_quantize_fp8_b128(const moe_dims *dims, const uint16_t *d_x, uint
 moe_status moe_dispatch_send(const moe_dims *dims, const moe_layout_t *lay, const void *d_x, void *d_send,
                              void *d_recv, void *stream);
 
+/* Dispatch send that allocates nothing, for callers that cannot call cudaMalloc (code
+ * under a fixed memory plan made before serving, allocator hooks that must not re-enter the
+ * allocator, hosts that only pass in tensors they already own). The page has no counterpart:
+ * it is an interface variant of moe_dispatch_send, with the same results in d_recv, whose
+ * send buffer lives in a file-scope device array of the library (64 MiB) instead of a
+ * caller buffer. Arguments are those of moe_dispatch_send without d_send.
+ *  - Sizes: N*T*R*B must be at most 64 MiB (B = row bytes), else MOE_ERR_INVALID_ARG.
+ *  - The first call on a device looks the array's address up (cudaGetSymbolAddress) with
+ *    that device current; make that first call before any stream capture.
+ *  - The array is shared by every call and keeps the last call's rows; calls that overlap
+ *    on the GPU (other streams or threads) race on it. Every GPU that loads the library
+ *    holds the 64 MiB until the process exits.
+ *  - Calls no allocating routine (no cudaMalloc, cudaFree or library allocator). */
+moe_status moe_dispatch_send_noalloc(const moe_dims *dims, const moe_layout_t *lay, const void *d_x,
+                                     void *d_recv, void *stream);
+
 /* Dispatch receive (section "Dispatch and combine": shuffle tokens from the receive buffer
  * into the tensor handed to the grouped GEMM): every receive row of rank d goes to row
  * slot of its expert l. bf16: d_expert_x [N][L][cap][H] bf16, d_expert_scale unused.
