@@ -36,7 +36,7 @@ import workloads  # noqa: E402
 
 METRIC = "dispatch+combine tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 KERNELS = ["route_count", "layout_maps", "quant_fp8", "pack", "scatter", "unpack", "expert",
-           "combine_pack", "combine_scatter", "combine_reduce"]
+           "combine_pack", "combine_scatter", "combine_reduce", "route_scan", "pack_push", "combine_push"]
 
 
 def parse_args(argv=None):
@@ -48,9 +48,10 @@ def parse_args(argv=None):
     p.add_argument("--shape", default="", help="custom workload N,T,H,E,R[,payload[,cap]] (uniform routing, "
                    "seed 11) instead of --config, e.g. for profiling a smaller footprint")
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--mover", choices=["tma", "ldg"], default="tma")
+    p.add_argument("--mover", choices=["auto", "tma", "ldg"], default="auto")
     p.add_argument("--tma-stages", type=int, default=0)
     p.add_argument("--ctas-per-sm", type=int, default=0)
+    p.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work for the oracle baseline")
     return p.parse_args(argv)
@@ -165,8 +166,9 @@ def algorithmic_bytes(wl: workloads.Workload, P: int, Pk: int) -> dict:
     tok = N * T
     P_all = tok * R
     return {
-        "route_count": 8 * P_all + 4 * N * E * 5,
-        "layout_maps": 32 * P_all + 4 * E * cap + 4 * N * RB,
+        "route_count": 8 * P_all + 4 * N * E * ((T * R + 255) // 256),
+        "route_scan": 4 * N * E * (2 * ((T * R + 255) // 256) + 5) + 4 * 3 * N * N,
+        "layout_maps": 36 * P_all + 4 * E * cap + 4 * N * RB,
         "quant_fp8": tok * 2 * H + tok * B,
         "pack": tok * B + P * B,
         "scatter": 2 * P * B,
@@ -175,6 +177,8 @@ def algorithmic_bytes(wl: workloads.Workload, P: int, Pk: int) -> dict:
         "combine_pack": 2 * Pk * 2 * H,
         "combine_scatter": 2 * Pk * 2 * H,
         "combine_reduce": Pk * 2 * H + tok * 2 * H,
+        "pack_push": tok * B + P * B,
+        "combine_push": 2 * Pk * 2 * H,
     }
 
 
@@ -239,7 +243,8 @@ def run_ours(args):
     wl = workload_of(args)
     inp = workloads.make_inputs(wl)
     ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, wl.payload, alias_buffers=(wl.payload == "bf16"),
-               flags=1 if args.mover == "ldg" else 0, tma_stages=args.tma_stages, ctas_per_sm=args.ctas_per_sm)
+               flags={"auto": 0, "ldg": 1, "tma": 4}[args.mover] | (2 if args.no_pdl else 0), tma_stages=args.tma_stages,
+               ctas_per_sm=args.ctas_per_sm)
     x = torch.from_numpy(inp["x"]).view(torch.bfloat16).to(device)
     idx = torch.from_numpy(inp["idx"]).to(device)
     w = torch.from_numpy(inp["w"]).to(device)
@@ -247,8 +252,25 @@ def run_ours(args):
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     flush = torch.empty(2 * l2, dtype=torch.uint8, device=device)
 
+    fp8 = wl.payload == "fp8"
+
     def step():
         ep.forward(x, idx, w)
+
+    def step_split(e0, e1, e2, e3):
+        """One pass with events around the identity expert (the grouped-GEMM stand-in), so
+        its time can be left out of the step as the scope's tokens/s definition asks."""
+        e0.record(stream)
+        ep.layout_step(idx)
+        ep.quantize(x)
+        ep.dispatch_send(ep.xq)
+        ep.dispatch_recv()
+        e1.record(stream)
+        ep.expert_identity()
+        e2.record(stream)
+        ep.combine_send()
+        ep.combine_recv(w)
+        e3.record(stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -276,34 +298,61 @@ def run_ours(args):
 
     vis = [v.strip() for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
     sampler = ClockSampler(vis[local] if local < len(vis) else local)
-    sampler.start()
-    barrier(dist, device)
-    torch.cuda.synchronize()
-    n0 = lib().moe_launch_count()
-    for i in range(K):
-        flush.zero_()
-        pr, _ = profs[i]
-        pr.n = 0
-        ep.layout.prof = ctypes.pointer(pr)
-        starts[i].record(stream)
-        step()
-        ends[i].record(stream)
-    torch.cuda.synchronize()
-    barrier(dist, device)
-    launches = lib().moe_launch_count() - n0
-    clocks = sampler.stop()
-    ep.layout.prof = None
-    code, bits = ep.status()
-    if code != 0:
-        raise RuntimeError(f"device status {code} bits {bits:#x}")
+    def kernel_region():
+        """Timed region: per-kernel CUDA events (the library records one pair around each of
+        its launches on this stream) give each kernel's duration for the roofline."""
+        barrier(dist, device)
+        torch.cuda.synchronize()
+        for i in range(K):
+            flush.zero_()
+            pr, _ = profs[i]
+            pr.n = 0
+            ep.layout.prof = ctypes.pointer(pr)
+            step()
+        torch.cuda.synchronize()
+        ep.layout.prof = None
+        per_kernel = {}
+        for pr, evs in profs:
+            for j in range(pr.n):
+                name = KERNEL_NAMES[pr.kernel[j]]
+                per_kernel.setdefault(name, []).append(evs[2 * j].elapsed_time(evs[2 * j + 1]))
+        return per_kernel
 
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    per_kernel = {}
-    for pr, evs in profs:
-        for j in range(pr.n):
-            name = KERNEL_NAMES[pr.kernel[j]]
-            per_kernel.setdefault(name, []).append(evs[2 * j].elapsed_time(evs[2 * j + 1]))
-    mean_ms = statistics.fmean(step_ms)
+    def step_region():
+        """Timed region: whole steps only (no events between the kernels, so consecutive
+        kernels overlap launch and drain as they do in use); gives the step time."""
+        barrier(dist, device)
+        torch.cuda.synchronize()
+        n0 = lib().moe_launch_count()
+        if fp8:
+            mids = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+            for i in range(K):
+                flush.zero_()
+                step_split(starts[i], mids[i][0], mids[i][1], ends[i])
+        else:
+            for i in range(K):
+                flush.zero_()
+                starts[i].record(stream)
+                step()
+                ends[i].record(stream)
+        torch.cuda.synchronize()
+        barrier(dist, device)
+        launches = lib().moe_launch_count() - n0
+        code, bits = ep.status()
+        if code != 0:
+            raise RuntimeError(f"device status {code} bits {bits:#x}")
+        step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        expert_ms = None
+        if fp8:
+            ex = [m0.elapsed_time(m1) for m0, m1 in mids]
+            step_ms = [t - x_ for t, x_ in zip(step_ms, ex)]
+            expert_ms = statistics.fmean(ex)
+        return statistics.fmean(step_ms), expert_ms, launches
+
+    sampler.start()
+    per_kernel = kernel_region()
+    mean_ms, expert_ms, launches = step_region()
+    clocks = sampler.stop()
     mean_ms_all = max_over_ranks(mean_ms, dist, device)
     tokens = wl.N * wl.T * ws
     value = tokens / (mean_ms_all * 1e-3)
@@ -312,6 +361,8 @@ def run_ours(args):
     ab = algorithmic_bytes(wl, P, Pk)
     kernels = {}
     for name, ts in per_kernel.items():
+        if name == "expert":
+            continue  # the identity expert stands in for the grouped GEMM; reported separately
         us = statistics.fmean(ts) * 1e3 / 1.0
         launches_per_step = len(ts) / K
         gbs = ab[name] / (us * 1e-6) / 1e9
@@ -319,6 +370,25 @@ def run_ours(args):
                          "gbs": round(gbs, 1), "frac": round(gbs / peak, 3)}
     dom = max(kernels, key=lambda k: kernels[k]["us"] * kernels[k]["launches_per_step"])
     step_bytes = sum(ab[k] * kernels[k]["launches_per_step"] for k in kernels)
+
+    # The same step in direct-push mode (the pack writes into the owners' receive rows and
+    # the combine send into the sources' rows, fusing away both per-peer write steps).
+    ep.layout.flags |= 8
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    pk_push = kernel_region()
+    push_ms, _, _ = step_region()
+    ep.layout.flags &= ~8
+    push_kernels = {}
+    for name, ts in pk_push.items():
+        if name == "expert":
+            continue
+        us = statistics.fmean(ts) * 1e3
+        push_kernels[name] = {"us": round(us, 2), "gbs": round(ab[name] / (us * 1e-6) / 1e9, 1),
+                              "frac": round(ab[name] / (us * 1e-6) / 1e9 / peak, 3)}
+    push_bytes = sum(ab[k] for k in push_kernels)
+    push_ms_all = max_over_ranks(push_ms, dist, device)
 
     # end to end through the C ABI with host buffers: H2D inputs, the pass, D2H output
     h_x = torch.from_numpy(inp["x"]).view(torch.bfloat16).pin_memory()
@@ -347,6 +417,7 @@ def run_ours(args):
         "data": "synthetic (seeded; DeepSeek-V3/Kimi-K2-shaped routing, identity experts)",
         "config": {"workload": wl.name, "N_ranks_simulated": wl.N, "T": wl.T, "H": wl.H, "E": wl.E, "R": wl.R,
                    "payload": wl.payload, "routing": wl.routing, "seed": wl.seed, "mover": args.mover,
+                   "pdl": not args.no_pdl,
                    "l2": "flushed before every timed step (write of 2x L2)",
                    "parallelism": f"{ws} independent replica(s) of the {wl.N}-rank group"},
         "hbm_gbs": round(step_bytes / (mean_ms * 1e-3) / 1e9, 1),
@@ -355,8 +426,18 @@ def run_ours(args):
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": kernels[dom]["frac"],
                      "bytes_per_launch": ab[dom], "traffic": ncu_traffic(dom, wl.name)},
         "kernels": kernels,
+        "direct_push": {"value": round(tokens / (push_ms_all * 1e-3), 1), "unit": "tokens/s",
+                        "ms_per_step": round(push_ms_all, 4),
+                        "hbm_gbs": round(push_bytes / (push_ms * 1e-3) / 1e9, 1),
+                        "hbm_frac": round(push_bytes / (push_ms * 1e-3) / 1e9 / peak, 3),
+                        "kernels": push_kernels,
+                        "note": "same results; pack and combine send write straight into the peers' "
+                                "receive regions, so the two per-peer write kernels are fused away"},
         "e2e": {"value": round(tokens / (e2e_ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "path": "moe_forward_host (C ABI)"},
+        "identity_expert": None if expert_ms is None else {
+            "ms_per_step": round(expert_ms, 4), "kernel_us": round(statistics.fmean(per_kernel["expert"]) * 1e3, 2),
+            "note": "fp8 dequantisation standing in for the grouped GEMM; excluded from ms_per_step and value"},
         "gpu_launches": int(launches),
         "clocks": clocks,
     }

@@ -19,10 +19,13 @@ MOE_PAYLOAD_BF16 = 0
 MOE_PAYLOAD_FP8_E4M3_B128 = 1
 
 MOE_FLAG_LDG_MOVER = 0x1
+MOE_FLAG_NO_PDL = 0x2
+MOE_FLAG_TMA_MOVER = 0x4
+MOE_FLAG_DIRECT_PUSH = 0x8
 MOE_PROF_MAX = 32
 
 KERNEL_NAMES = ["route_count", "layout_maps", "quant_fp8", "pack", "scatter", "unpack", "expert",
-                "combine_pack", "combine_scatter", "combine_reduce"]
+                "combine_pack", "combine_scatter", "combine_reduce", "route_scan", "pack_push", "combine_push"]
 
 LAYOUT_FIELDS = ("cnt", "C", "soff", "roff", "rtot", "ecnt", "eoff", "pos", "rrow", "slot", "slot_src",
                  "recv_src", "gsend", "grecv", "gslot", "status", "scratch")

@@ -15,7 +15,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxE = 1536;
-constexpr int64_t kMaxScanInts = 56832;  // N*E + N*N ints staged in shared memory
+constexpr int64_t kMaxScanInts = 56832;  // N*(E|1) + N*(N|1) ints staged in shared memory
 constexpr int64_t kI32 = 0x7fffffff;
 
 struct DevInfo {
@@ -36,7 +36,7 @@ moe_status make_geo(const moe_dims* d, Geo& g) {
   if (d->payload == MOE_PAYLOAD_FP8_E4M3_B128 && d->H % 128 != 0) return MOE_ERR_INVALID_ARG;
   if (d->E > kMaxE) return MOE_ERR_INVALID_ARG;
   const int64_t N = d->N, T = d->T, E = d->E, R = d->R, L = E / N;
-  if (N * E + N * N > kMaxScanInts) return MOE_ERR_INVALID_ARG;
+  if (N * (E | 1) + N * (N | 1) > kMaxScanInts) return MOE_ERR_INVALID_ARG;
   const int64_t cap = d->cap > 0 ? d->cap : N * T;  // 0 only when there are no tokens
   const int64_t RB = N * T * (R > L ? R : L);
   if (N * T * R > kI32 || N * RB > kI32 || E * cap > kI32 || N * T * (int64_t)d->H > (int64_t)1 << 40)
@@ -123,7 +123,7 @@ WsPlan ws_plan(const Geo& g) {
                           P,               // grecv
                           P,               // gslot
                           16,              // status
-                          16};             // scratch
+                          (size_t)N * layout_chunks(g) * E + 16};  // scratch: chunk table
   w.total = 0;
   for (int i = 0; i < 17; ++i) {
     w.n[i] = al256(4 * sizes[i]);
@@ -186,7 +186,6 @@ moe_status moe_layout_init(const moe_dims* dims, void* d_ws, size_t ws_bytes, mo
   out->ctas_per_sm = 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(out->status, 0, 64, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (cudaMemsetAsync(out->scratch, 0, 64, s) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }
 
@@ -197,7 +196,7 @@ moe_status moe_layout(const moe_dims* dims, const int32_t* d_idx, const moe_layo
   if (!layout_ok(lay) || (!d_idx && g.P > 0)) return MOE_ERR_INVALID_ARG;
   Ctx c;
   if ((st = make_ctx(lay, stream, c)) != MOE_OK) return st;
-  if ((int)layout_smem_bytes(g) > c.smem_optin) return MOE_ERR_INVALID_ARG;
+  if (layout_smem_bytes(g) + 1024 > (size_t)c.smem_optin) return MOE_ERR_INVALID_ARG;
   return cuda_status(launch_layout(g, d_idx, lay, c));
 }
 
@@ -221,10 +220,13 @@ moe_status moe_dispatch_send(const moe_dims* dims, const moe_layout_t* lay, cons
   moe_status st = make_geo(dims, g);
   if (st != MOE_OK) return st;
   if ((int64_t)g.N * g.T == 0) return layout_ok(lay) ? MOE_OK : MOE_ERR_INVALID_ARG;  // nothing to move
-  if (!layout_ok(lay) || !d_x || !d_send || !d_recv || !aligned16(d_x) || !aligned16(d_send) || !aligned16(d_recv))
+  const bool push = lay && (lay->flags & MOE_FLAG_DIRECT_PUSH);
+  if (!layout_ok(lay) || !d_x || !d_recv || !aligned16(d_x) || !aligned16(d_recv) ||
+      (!push && (!d_send || !aligned16(d_send))))
     return MOE_ERR_INVALID_ARG;
   Ctx c;
   if ((st = make_ctx(lay, stream, c)) != MOE_OK) return st;
+  if (push) return cuda_status(launch_move(kMovePackPush, g, lay, d_x, d_recv, nullptr, c));
   cudaError_t e = launch_move(kMovePack, g, lay, d_x, d_send, nullptr, c);
   if (e == cudaSuccess) e = launch_move(kMoveScatter, g, lay, d_send, d_recv, nullptr, c);
   return cuda_status(e);
@@ -270,11 +272,13 @@ moe_status moe_combine_send(const moe_dims* dims, const moe_layout_t* lay, const
   moe_status st = make_geo(dims, g);
   if (st != MOE_OK) return st;
   if ((int64_t)g.N * g.T == 0) return layout_ok(lay) ? MOE_OK : MOE_ERR_INVALID_ARG;  // nothing to move
-  if (!layout_ok(lay) || !d_expert_y || !d_csend || !d_crecv || !aligned16(d_expert_y) || !aligned16(d_csend) ||
-      !aligned16(d_crecv))
+  const bool push = lay && (lay->flags & MOE_FLAG_DIRECT_PUSH);
+  if (!layout_ok(lay) || !d_expert_y || !d_crecv || !aligned16(d_expert_y) || !aligned16(d_crecv) ||
+      (!push && (!d_csend || !aligned16(d_csend))))
     return MOE_ERR_INVALID_ARG;
   Ctx c;
   if ((st = make_ctx(lay, stream, c)) != MOE_OK) return st;
+  if (push) return cuda_status(launch_move(kMoveCPush, g, lay, d_expert_y, d_crecv, nullptr, c));
   cudaError_t e = launch_move(kMoveCPack, g, lay, d_expert_y, d_csend, nullptr, c);
   if (e == cudaSuccess) e = launch_move(kMoveCScatter, g, lay, d_csend, d_crecv, nullptr, c);
   return cuda_status(e);

@@ -41,6 +41,18 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ---- programmatic dependent launch (sm_90+) ------------------------------------------
+// Every kernel of the library waits for the grids it depends on before its first global
+// memory access, so a kernel launched with programmatic stream serialization may be
+// scheduled while its predecessor drains without changing stream-order semantics.
+// Without that launch attribute both instructions are no-ops.
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the next kernel in the stream launch once every CTA of this grid has called it
+// (or exited). It still waits in pdl_wait() for this grid to complete.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // ---- mbarrier -----------------------------------------------------------------------
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

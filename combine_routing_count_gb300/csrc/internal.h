@@ -3,6 +3,7 @@
 #pragma once
 
 #include <atomic>
+#include <utility>
 
 #include "common.cuh"
 
@@ -23,6 +24,24 @@ struct Ctx {
 };
 
 extern std::atomic<uint64_t> g_launches;
+
+// Launches `kernel` on c.stream, with programmatic stream serialization unless
+// MOE_FLAG_NO_PDL is set (every kernel calls pdl_wait() before touching memory).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, const Ctx& c,
+                                 Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = (c.flags & MOE_FLAG_NO_PDL) ? 0 : 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Brackets one kernel launch with the caller's profiling events (if any) and counts it.
 struct LaunchScope {
@@ -59,6 +78,7 @@ inline cudaError_t ensure_dyn_smem(K kernel, int device, size_t bytes, std::atom
 // layout.cu
 cudaError_t launch_layout(const Geo& g, const int32_t* idx, const moe_layout_t* lay, Ctx& c);
 size_t layout_smem_bytes(const Geo& g);
+int layout_chunks(const Geo& g);
 
 // movers.cu: row movement kernels.
 enum MoveKind : int {
@@ -68,6 +88,8 @@ enum MoveKind : int {
   kMoveCPack = 3,     // grouped expert output rows -> receive order (combine send buffer)
   kMoveCScatter = 4,  // combine send rows -> the source rank's combine receive rows
   kMoveCopyEx = 5,    // grouped rows -> grouped rows (bf16 identity expert, distinct output)
+  kMovePackPush = 6,  // direct push: token rows -> R receive rows of the owner ranks
+  kMoveCPush = 7,     // direct push: grouped expert output rows -> source ranks' combine rows
 };
 cudaError_t launch_move(MoveKind kind, const Geo& g, const moe_layout_t* lay, const void* src, void* dst,
                         void* dst2, Ctx& c);

@@ -8,16 +8,17 @@
 // the grouped-GEMM input; combine runs the same moves backwards.
 //
 // Two implementations, same results:
-//  - k_move_tma: one warp per CTA; lane j owns pipeline stage j (one row of shared memory
-//    and one mbarrier). Each lane plans its next row's addresses while its current row
-//    streams in through a 1-D TMA bulk copy (cp.async.bulk global->shared, completion on
-//    the mbarrier), then issues bulk stores shared->global to the row's destination(s):
-//    R of them for pack, codes + scales for the fp8 receive shuffle. A row is read from
-//    HBM once however many destinations it has.
-//  - k_move_ldg: one warp per row with 16-byte (or, for rows that are not 16-byte
+//  - k_move_tma: kIssuers independent issuer warps per CTA. Lane 0 of each warp runs its
+//    own ring of S row stages in shared memory: a 1-D TMA bulk copy (cp.async.bulk
+//    global->shared, completion counted on the stage's mbarrier) brings a row in, and bulk
+//    stores shared->global write it to its destination(s): R of them for pack, codes +
+//    scales for the fp8 receive shuffle. A row is read from HBM once however many
+//    destinations it has. While the oldest stage drains, S-1 loads stay in flight, and the
+//    indices of the next row to load are fetched one refill ahead.
+//  - k_move_ldg: one warp per unit with 16-byte (or, for rows that are not 16-byte
 //    multiples, 4-byte) register loads and stores; also the path for misaligned shapes.
-// Units are tokens (pack) or (token, expert) pairs (everything else); each CTA takes a
-// contiguous range of units, so skewed routing spreads evenly over the grid.
+// Units are (token, column chunk) for pack and (token, expert) pairs for the rest; units
+// are dealt round-robin over all issuers / warps, so skewed routing spreads evenly.
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -34,10 +35,13 @@ struct MoveArgs {
   const int32_t* gsend;   // per pair: global send row, or -1
   const int32_t* grecv;   // per pair: global receive row, or -1
   const int32_t* gslot;   // per pair: global grouped row, or -1
+  const int32_t* fan;     // pack: per pair, the destination row (gsend, or grecv for direct push)
   int32_t* status;
   int64_t units;
   uint32_t stage_bytes;
   int stages;
+  int chunks;             // pack: column chunks per token row (1 elsewhere)
+  uint32_t chunk_bytes;   // pack: bytes per chunk (B / chunks)
 };
 
 struct Plan {
@@ -45,24 +49,34 @@ struct Plan {
   uint8_t* dst;
   uint8_t* dst2;
   int64_t tok;                 // pack: token index s*T+t
+  int32_t coff;                // pack: byte offset of the chunk in the row
   int32_t p[kPackPrefetch];    // pack: global send rows of the token's pairs
 };
 
 template <int KIND>
 __host__ __device__ __forceinline__ uint32_t load_bytes(const Geo& g) {
-  if (KIND == kMovePack || KIND == kMoveScatter || KIND == kMoveUnpack) return (uint32_t)g.B;
+  if (KIND == kMovePack || KIND == kMovePackPush || KIND == kMoveScatter || KIND == kMoveUnpack)
+    return (uint32_t)g.B;
   return (uint32_t)(2 * g.H);
+}
+
+// Bytes one unit moves per destination: a chunk for pack, a whole row otherwise.
+template <int KIND>
+__host__ __device__ __forceinline__ uint32_t unit_bytes(const Geo& g, const MoveArgs& a) {
+  return (KIND == kMovePack || KIND == kMovePackPush) ? a.chunk_bytes : load_bytes<KIND>(g);
 }
 
 // Fills `pl` for unit u; false when the unit moves nothing (bad expert id or dropped pair).
 template <int KIND, bool FP8>
 __device__ __forceinline__ bool make_plan(const Geo& g, const MoveArgs& a, int64_t u, Plan& pl) {
   const int64_t H2 = 2 * (int64_t)g.H;
-  if (KIND == kMovePack) {
-    pl.tok = u;
-    pl.src = a.src + u * g.B;
+  if (KIND == kMovePack || KIND == kMovePackPush) {
+    const int64_t tok = u / a.chunks;
+    pl.tok = tok;
+    pl.coff = (int32_t)((u - tok * a.chunks) * a.chunk_bytes);
+    pl.src = a.src + tok * g.B + pl.coff;
 #pragma unroll
-    for (int k = 0; k < kPackPrefetch; ++k) pl.p[k] = (k < g.R) ? __ldg(a.gsend + u * g.R + k) : -1;
+    for (int k = 0; k < kPackPrefetch; ++k) pl.p[k] = (k < g.R) ? __ldg(a.fan + tok * g.R + k) : -1;
     return true;
   }
   if (KIND == kMoveScatter) {
@@ -99,6 +113,13 @@ __device__ __forceinline__ bool make_plan(const Geo& g, const MoveArgs& a, int64
     pl.dst = a.dst + (int64_t)gr * H2;
     return true;
   }
+  if (KIND == kMoveCPush) {
+    const int gs = __ldg(a.gsend + u);
+    if (gl < 0) return false;
+    pl.src = a.src + (int64_t)gl * H2;
+    pl.dst = a.dst + (int64_t)gs * H2;
+    return true;
+  }
   // kMoveCScatter
   const int gs = __ldg(a.gsend + u);
   if (gl < 0) return false;
@@ -111,13 +132,13 @@ __device__ __forceinline__ bool make_plan(const Geo& g, const MoveArgs& a, int64
 template <int KIND, bool FP8>
 __device__ __forceinline__ void issue_stores(const Geo& g, const MoveArgs& a, const Plan& pl, const uint8_t* stage,
                                              uint32_t bytes) {
-  if (KIND == kMovePack) {
+  if (KIND == kMovePack || KIND == kMovePackPush) {
 #pragma unroll
     for (int k = 0; k < kPackPrefetch; ++k)
-      if (pl.p[k] >= 0) bulk_s2g(a.dst + (int64_t)pl.p[k] * g.B, stage, bytes);
+      if (pl.p[k] >= 0) bulk_s2g(a.dst + (int64_t)pl.p[k] * g.B + pl.coff, stage, bytes);
     for (int k = kPackPrefetch; k < g.R; ++k) {
-      const int p = __ldg(a.gsend + pl.tok * g.R + k);
-      if (p >= 0) bulk_s2g(a.dst + (int64_t)p * g.B, stage, bytes);
+      const int p = __ldg(a.fan + pl.tok * g.R + k);
+      if (p >= 0) bulk_s2g(a.dst + (int64_t)p * g.B + pl.coff, stage, bytes);
     }
   } else if (KIND == kMoveUnpack && FP8) {
     bulk_s2g(pl.dst, stage, (uint32_t)g.H);
@@ -127,46 +148,95 @@ __device__ __forceinline__ void issue_stores(const Geo& g, const MoveArgs& a, co
   }
 }
 
+constexpr int kIssuers = 4;          // issuer warps per CTA
+constexpr int kMaxStages = 8;        // stages per issuer
+constexpr int kTmaHeader = kIssuers * kMaxStages * (8 + 128);  // mbarriers + plan slots
+
+// One stage's plan, kept in shared memory until its stores are issued.
+struct StagePlan {
+  uint8_t* dst;
+  uint8_t* dst2;
+  int64_t tok;
+  int32_t coff;
+  int32_t p[kPackPrefetch];
+};
+
+__device__ __forceinline__ void bulk_wait_read_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
 template <int KIND, bool FP8>
-__global__ void __launch_bounds__(32) k_move_tma(Geo g, MoveArgs a) {
+__global__ void __launch_bounds__(kIssuers * 32) k_move_tma(Geo g, MoveArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
-  const int lane = threadIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = a.stages;
-  uint8_t* stage = smem + 256 + (size_t)lane * a.stage_bytes;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem) + warp * kMaxStages;
+  StagePlan* sp = reinterpret_cast<StagePlan*>(smem + kIssuers * kMaxStages * 8) + warp * kMaxStages;
+  uint8_t* ring = smem + kTmaHeader + (size_t)warp * S * a.stage_bytes;
   if (lane < S) mbar_init(&bar[lane], 1);
   fence_mbar_init();
   __syncwarp();
-
-  const int64_t u0 = a.units * blockIdx.x / gridDim.x;
-  const int64_t u1 = a.units * (blockIdx.x + 1) / gridDim.x;
-  const uint32_t bytes = load_bytes<KIND>(g);
-  uint32_t phase = 0;
-  bool alive = lane < S;
-
-  Plan nxt;
-  bool has_nxt = alive && (u0 + lane < u1) && make_plan<KIND, FP8>(g, a, u0 + lane, nxt);
-  for (int64_t base = u0; base < u1; base += S) {
-    const Plan cur = nxt;
-    const bool has = has_nxt && alive;
-    bulk_wait_read_all();  // the stage's previous stores have read it
-    if (has) {
-      mbar_arrive_expect_tx(&bar[lane], bytes);
-      bulk_g2s(stage, cur.src, bytes, &bar[lane]);
-    }
-    const int64_t un = base + S + lane;
-    has_nxt = alive && (un < u1) && make_plan<KIND, FP8>(g, a, un, nxt);
-    if (has) {
-      if (mbar_wait_bounded(&bar[lane], phase, a.status)) {
-        phase ^= 1u;
-        issue_stores<KIND, FP8>(g, a, cur, stage, bytes);
-        bulk_commit();
-      } else {
-        alive = false;  // status carries the timeout; stop issuing
+  pdl_wait();
+  if (lane == 0) {
+    const int64_t G = (int64_t)gridDim.x * kIssuers;
+    const int64_t gi = (int64_t)blockIdx.x * kIssuers + warp;
+    const int64_t n = a.units > gi ? (a.units - gi + G - 1) / G : 0;   // this issuer's units
+    const uint32_t bytes = unit_bytes<KIND>(g, a);
+    uint32_t vbits = 0, pbits = 0;   // per stage: a load is in flight; the barrier's parity
+    Plan pl;
+    for (int k = 0; k < S && k < n; ++k) {
+      const bool ok = make_plan<KIND, FP8>(g, a, gi + k * G, pl);
+      sp[k] = StagePlan{pl.dst, pl.dst2, pl.tok, pl.coff, {}};
+      if (KIND == kMovePack || KIND == kMovePackPush)
+        for (int r = 0; r < kPackPrefetch; ++r) sp[k].p[r] = pl.p[r];
+      if (ok) {
+        mbar_arrive_expect_tx(&bar[k], bytes);
+        bulk_g2s(ring + (size_t)k * a.stage_bytes, pl.src, bytes, &bar[k]);
+        vbits |= 1u << k;
       }
     }
+    Plan nx;
+    bool nx_ok = (S < n) && make_plan<KIND, FP8>(g, a, gi + S * G, nx);
+    for (int64_t j = 0; j < n; ++j) {
+      const int k = (int)(j % S);
+      bool stored = false;
+      if (vbits & (1u << k)) {
+        if (!mbar_wait_bounded(&bar[k], (pbits >> k) & 1u, a.status)) break;  // status has the timeout
+        pbits ^= 1u << k;
+        Plan cur;
+        cur.dst = sp[k].dst;
+        cur.dst2 = sp[k].dst2;
+        cur.tok = sp[k].tok;
+        cur.coff = sp[k].coff;
+        if (KIND == kMovePack || KIND == kMovePackPush)
+          for (int r = 0; r < kPackPrefetch; ++r) cur.p[r] = sp[k].p[r];
+        issue_stores<KIND, FP8>(g, a, cur, ring + (size_t)k * a.stage_bytes, bytes);
+        bulk_commit();
+        stored = true;
+      }
+      // Refill the stage of unit j-1 with unit j-1+S once its stores have read it.
+      const int64_t jr = j - 1 + S;
+      if (j >= 1 && jr < n) {
+        const int kp = (int)((j - 1) % S);
+        if (stored)
+          bulk_wait_read_1();
+        else
+          bulk_wait_read_all();
+        vbits &= ~(1u << kp);
+        sp[kp] = StagePlan{nx.dst, nx.dst2, nx.tok, nx.coff, {}};
+        if (KIND == kMovePack || KIND == kMovePackPush)
+          for (int r = 0; r < kPackPrefetch; ++r) sp[kp].p[r] = nx.p[r];
+        if (nx_ok) {
+          mbar_arrive_expect_tx(&bar[kp], bytes);
+          bulk_g2s(ring + (size_t)kp * a.stage_bytes, nx.src, bytes, &bar[kp]);
+          vbits |= 1u << kp;
+        }
+        nx_ok = (jr + 1 < n) && make_plan<KIND, FP8>(g, a, gi + (jr + 1) * G, nx);
+      }
+    }
+    pdl_trigger();
+    bulk_wait_all();
   }
-  bulk_wait_all();
 }
 
 template <typename V>
@@ -188,8 +258,9 @@ __global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
   constexpr int W = (int)sizeof(V);
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  const int64_t nel = load_bytes<KIND>(g) / W;
+  const int64_t nel = unit_bytes<KIND>(g, a) / W;
   const int64_t split = (KIND == kMoveUnpack && FP8) ? g.H / W : nel;
+  pdl_wait();
   for (int64_t u = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < a.units; u += nwarps) {
     Plan pl;
     if (!make_plan<KIND, FP8>(g, a, u, pl)) continue;
@@ -204,13 +275,13 @@ __global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
       for (int j = 0; j < U; ++j) {
         const int64_t v = v0 + 32 * j;
         if (v >= nel) continue;
-        if (KIND == kMovePack) {
+        if (KIND == kMovePack || KIND == kMovePackPush) {
 #pragma unroll
           for (int k = 0; k < kPackPrefetch; ++k)
-            if (pl.p[k] >= 0) st_vec(a.dst + (int64_t)pl.p[k] * g.B + v * W, r[j]);
+            if (pl.p[k] >= 0) st_vec(a.dst + (int64_t)pl.p[k] * g.B + pl.coff + v * W, r[j]);
           for (int k = kPackPrefetch; k < g.R; ++k) {
-            const int p = __ldg(a.gsend + pl.tok * g.R + k);
-            if (p >= 0) st_vec(a.dst + (int64_t)p * g.B + v * W, r[j]);
+            const int p = __ldg(a.fan + pl.tok * g.R + k);
+            if (p >= 0) st_vec(a.dst + (int64_t)p * g.B + pl.coff + v * W, r[j]);
           }
         } else if (KIND == kMoveUnpack && FP8) {
           if (v < split)
@@ -223,28 +294,34 @@ __global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
       }
     }
   }
+  pdl_trigger();
 }
 
 // Largest dynamic shared memory limit set so far, per TMA instantiation and device.
-std::atomic<int> g_tma_smem[6][2][64];
+std::atomic<int> g_tma_smem[8][2][64];
 
-// Stages per CTA and CTAs per SM: two CTAs per SM when each still holds >= 8 row stages,
-// else one CTA with as many stages as shared memory allows (at most 32, one per lane).
-// Each CTA also pays 1 KB of reserved shared memory and 256 bytes of mbarriers.
+// Stages per issuer and CTAs per SM: as many CTAs as fit with 3 stages per issuer (at
+// most 8 CTAs), then as many stages as the shared memory of each CTA holds (2..8). Each
+// CTA also pays 1 KB of reserved shared memory and its mbarrier/plan header.
 template <int KIND, bool FP8>
 cudaError_t run_tma(const Geo& g, MoveArgs a, Ctx& c) {
-  const uint32_t row = load_bytes<KIND>(g);
-  const int stage_bytes = (int)((row + 127u) & ~127u);
-  const int per_cta_extra = 1024 + 256;
+  const uint32_t bytes = unit_bytes<KIND>(g, a);
+  const int stage_bytes = (int)((bytes + 127u) & ~127u);
+  const int per_cta_extra = 1024 + kTmaHeader;
   int cps = c.ctas_per_sm;
-  if (cps <= 0) cps = ((c.smem_per_sm / 2 - per_cta_extra) / stage_bytes >= 8) ? 2 : 1;
-  int S = (c.smem_per_sm / cps - per_cta_extra) / stage_bytes;
-  const int S_blk = (c.smem_optin - 256) / stage_bytes;
+  if (cps <= 0) {
+    cps = c.smem_per_sm / (kIssuers * 3 * stage_bytes + per_cta_extra);
+    if (cps > 8) cps = 8;
+    if (cps < 1) cps = 1;
+  }
+  while (cps > 1 && (c.smem_per_sm / cps - per_cta_extra) / (kIssuers * stage_bytes) < 2) --cps;
+  int S = (c.smem_per_sm / cps - per_cta_extra) / (kIssuers * stage_bytes);
+  const int S_blk = (c.smem_optin - kTmaHeader) / (kIssuers * stage_bytes);
   if (S > S_blk) S = S_blk;
-  if (S > 32) S = 32;
+  if (S > kMaxStages) S = kMaxStages;
   if (c.tma_stages > 0 && c.tma_stages < S) S = c.tma_stages;
-  if (S < 1) return cudaErrorInvalidValue;
-  const size_t smem = 256 + (size_t)S * stage_bytes;
+  if (S < 2) return cudaErrorInvalidValue;
+  const size_t smem = kTmaHeader + (size_t)kIssuers * S * stage_bytes;
   {
     cudaError_t e = ensure_dyn_smem(k_move_tma<KIND, FP8>, c.device, smem, g_tma_smem[KIND][FP8 ? 1 : 0]);
     if (e != cudaSuccess) return e;
@@ -252,9 +329,9 @@ cudaError_t run_tma(const Geo& g, MoveArgs a, Ctx& c) {
   a.stages = S;
   a.stage_bytes = stage_bytes;
   int64_t grid = (int64_t)c.num_sms * cps;
-  if (grid > a.units) grid = a.units;
-  k_move_tma<KIND, FP8><<<(unsigned)grid, 32, smem, c.stream>>>(g, a);
-  return cudaGetLastError();
+  const int64_t need = (a.units + kIssuers - 1) / kIssuers;
+  if (grid > need) grid = need;
+  return launch_kernel(k_move_tma<KIND, FP8>, dim3((unsigned)grid), dim3(kIssuers * 32), smem, c, g, a);
 }
 
 template <int KIND, bool FP8, typename V>
@@ -262,13 +339,32 @@ cudaError_t run_ldg(const Geo& g, const MoveArgs& a, Ctx& c) {
   int64_t blocks = (a.units + 7) / 8;
   const int64_t maxb = (int64_t)c.num_sms * 4;
   if (blocks > maxb) blocks = maxb;
-  k_move_ldg<KIND, FP8, V><<<(unsigned)blocks, 256, 0, c.stream>>>(g, a);
-  return cudaGetLastError();
+  return launch_kernel(k_move_ldg<KIND, FP8, V>, dim3((unsigned)blocks), dim3(256), 0, c, g, a);
+}
+
+// True when two stages per issuer fit in one CTA's shared memory.
+template <int KIND>
+bool tma_fits(const Geo& g, const MoveArgs& a, const Ctx& c) {
+  const int stage_bytes = (int)((unit_bytes<KIND>(g, a) + 127u) & ~127u);
+  return (c.smem_optin - kTmaHeader) / (kIssuers * stage_bytes) >= 2;
+}
+
+// Default choice (measured on GB300): the TMA ring streams one-to-one moves at 95-98% of
+// the copy bandwidth once every issuer has >= 20 rows, but its stages are held until the
+// bulk stores have read them, which costs it the ramp on small problems and pack's R-fold
+// stores; there the register mover, whose stores free their registers at issue, is faster.
+template <int KIND>
+bool tma_default(const MoveArgs& a, const Ctx& c) {
+  if (KIND == kMovePack || KIND == kMovePackPush) return false;
+  return a.units >= 20LL * kIssuers * c.num_sms;
 }
 
 template <int KIND, bool FP8>
 cudaError_t run_kind(const Geo& g, const MoveArgs& a, Ctx& c, bool row16) {
-  if (row16 && !(c.flags & MOE_FLAG_LDG_MOVER)) return run_tma<KIND, FP8>(g, a, c);
+  const bool want_tma = (c.flags & MOE_FLAG_TMA_MOVER) ? true
+                        : (c.flags & MOE_FLAG_LDG_MOVER) ? false
+                                                          : tma_default<KIND>(a, c);
+  if (row16 && want_tma && tma_fits<KIND>(g, a, c)) return run_tma<KIND, FP8>(g, a, c);
   if (row16) return run_ldg<KIND, FP8, uint4>(g, a, c);
   return run_ldg<KIND, FP8, uint32_t>(g, a, c);
 }
@@ -284,15 +380,30 @@ cudaError_t launch_move(MoveKind kind, const Geo& g, const moe_layout_t* lay, co
   a.gsend = lay->gsend;
   a.grecv = lay->grecv;
   a.gslot = lay->gslot;
+  a.fan = kind == kMovePackPush ? lay->grecv : lay->gsend;
   a.status = lay->status;
-  a.units = (kind == kMovePack) ? (int64_t)g.N * g.T : g.P;
   a.stages = 0;
   a.stage_bytes = 0;
-  if (a.units == 0) return cudaSuccess;
+  a.chunks = 1;
+  a.chunk_bytes = (uint32_t)g.B;
   const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
   const bool rowB16 = (g.B % 16) == 0;  // bf16 rows always; fp8 rows when H % 512 == 0
-  static const moe_kernel_id ids[] = {MOE_K_PACK, MOE_K_SCATTER, MOE_K_UNPACK, MOE_K_COMBINE_PACK,
-                                      MOE_K_COMBINE_SCATTER, MOE_K_EXPERT};
+  if (kind == kMovePack || kind == kMovePackPush) {
+    // Split token rows into column chunks until there are ~16 units per SM (chunks of at
+    // least 1 KB, 16-byte multiples), so that pack has parallelism beyond one unit per token.
+    const int64_t tokens = (int64_t)g.N * g.T;
+    while (a.chunks < 8 && tokens * a.chunks < 16LL * c.num_sms && g.B % (16 * 2 * a.chunks) == 0 &&
+           g.B / (2 * a.chunks) >= 1024)
+      a.chunks *= 2;
+    a.chunk_bytes = (uint32_t)(g.B / a.chunks);
+    a.units = tokens * a.chunks;
+  } else {
+    a.units = g.P;
+  }
+  if (a.units == 0) return cudaSuccess;
+  static const moe_kernel_id ids[] = {MOE_K_PACK,         MOE_K_SCATTER,         MOE_K_UNPACK,
+                                      MOE_K_COMBINE_PACK, MOE_K_COMBINE_SCATTER, MOE_K_EXPERT,
+                                      MOE_K_PACK_PUSH,    MOE_K_COMBINE_PUSH};
   LaunchScope ls(c, ids[kind]);
   switch (kind) {
     case kMovePack:
@@ -307,6 +418,10 @@ cudaError_t launch_move(MoveKind kind, const Geo& g, const moe_layout_t* lay, co
       return run_kind<kMoveCScatter, false>(g, a, c, true);
     case kMoveCopyEx:
       return run_kind<kMoveCopyEx, false>(g, a, c, true);
+    case kMovePackPush:
+      return run_kind<kMovePackPush, false>(g, a, c, rowB16);
+    case kMoveCPush:
+      return run_kind<kMoveCPush, false>(g, a, c, true);
   }
   return cudaErrorInvalidValue;
 }

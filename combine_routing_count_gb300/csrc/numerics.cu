@@ -21,6 +21,9 @@ constexpr unsigned kFull = 0xffffffffu;
 // amax over the block by xor-shuffles inside the half warp; scale = amax / 448 (IEEE fp32
 // division; 1 when amax is 0); codes = e4m3(x / scale), round to nearest even, saturating.
 // Output row: H codes, then H/128 fp32 scales. 4-byte stores (rows are 4-byte aligned).
+// A warp takes kQuantUnroll pairs of blocks per trip and issues all their loads first.
+constexpr int kQuantUnroll = 4;
+
 __global__ void __launch_bounds__(256) k_quant_fp8(Geo g, const uint16_t* __restrict__ x, uint8_t* __restrict__ xq) {
   const int nb = g.H / 128;
   const int64_t nblk = (int64_t)g.N * g.T * nb;
@@ -28,38 +31,50 @@ __global__ void __launch_bounds__(256) k_quant_fp8(Geo g, const uint16_t* __rest
   const int sub = lane & 15;
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t b0 = warp * 2; b0 < nblk; b0 += nwarps * 2) {  // warp-uniform trip count
-    const int64_t blk = b0 + (lane >> 4);
-    const bool act = blk < nblk;
-    const int64_t row = act ? blk / nb : 0;
-    const int b = act ? (int)(blk - row * nb) : 0;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (act) v = ld_stream16(x + row * g.H + b * 128 + sub * 8);
-    float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                  bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
-    float amax = 0.0f;
+  pdl_wait();
+  for (int64_t b0 = warp * 2 * kQuantUnroll; b0 < nblk; b0 += nwarps * 2 * kQuantUnroll) {  // warp-uniform
+    uint4 v[kQuantUnroll];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
-#pragma unroll
-    for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o, 16));
-    const float scale = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
-    uint32_t w[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
-          make_float2(__fdiv_rn(f[4 * i + 0], scale), __fdiv_rn(f[4 * i + 1], scale)), __NV_SATFINITE, __NV_E4M3);
-      const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-          make_float2(__fdiv_rn(f[4 * i + 2], scale), __fdiv_rn(f[4 * i + 3], scale)), __NV_SATFINITE, __NV_E4M3);
-      w[i] = (uint32_t)lo | ((uint32_t)hi << 16);
+    for (int j = 0; j < kQuantUnroll; ++j) {
+      const int64_t blk = b0 + 2 * j + (lane >> 4);
+      v[j] = make_uint4(0, 0, 0, 0);
+      if (blk < nblk) {
+        const int64_t row = blk / nb;
+        v[j] = ld_stream16(x + row * g.H + (blk - row * nb) * 128 + sub * 8);
+      }
     }
-    if (act) {
-      uint8_t* qr = xq + row * g.B;
-      uint32_t* dst = reinterpret_cast<uint32_t*>(qr + b * 128 + sub * 8);
-      dst[0] = w[0];
-      dst[1] = w[1];
-      if (sub == 0) *reinterpret_cast<float*>(qr + g.H + 4 * b) = scale;
+#pragma unroll
+    for (int j = 0; j < kQuantUnroll; ++j) {
+      const int64_t blk = b0 + 2 * j + (lane >> 4);
+      const float f[8] = {bf16_lo(v[j].x), bf16_hi(v[j].x), bf16_lo(v[j].y), bf16_hi(v[j].y),
+                          bf16_lo(v[j].z), bf16_hi(v[j].z), bf16_lo(v[j].w), bf16_hi(v[j].w)};
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+      for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o, 16));
+      const float scale = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+      uint32_t w[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+            make_float2(__fdiv_rn(f[4 * i + 0], scale), __fdiv_rn(f[4 * i + 1], scale)), __NV_SATFINITE, __NV_E4M3);
+        const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+            make_float2(__fdiv_rn(f[4 * i + 2], scale), __fdiv_rn(f[4 * i + 3], scale)), __NV_SATFINITE, __NV_E4M3);
+        w[i] = (uint32_t)lo | ((uint32_t)hi << 16);
+      }
+      if (blk < nblk) {
+        const int64_t row = blk / nb;
+        const int b = (int)(blk - row * nb);
+        uint8_t* qr = xq + row * g.B;
+        uint32_t* dst = reinterpret_cast<uint32_t*>(qr + b * 128 + sub * 8);
+        dst[0] = w[0];
+        dst[1] = w[1];
+        if (sub == 0) *reinterpret_cast<float*>(qr + g.H + 4 * b) = scale;
+      }
     }
   }
+  pdl_trigger();
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -77,35 +92,52 @@ __device__ __forceinline__ uint32_t dequant2(uint16_t codes, float scale) {
 }
 
 // Identity expert for the fp8 payload: one warp per used grouped row (found through the
-// pairs' gslot), 16 codes per lane per step.
+// pairs' gslot), 16 codes per lane per load, kDequantUnroll loads in flight per lane.
+constexpr int kDequantUnroll = 4;
+
 __global__ void __launch_bounds__(256) k_dequant_fp8(Geo g, const int32_t* __restrict__ gslot,
                                                      const uint8_t* __restrict__ exq, const float* __restrict__ exs,
                                                      uint16_t* __restrict__ ey) {
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int nvec = g.H / 16;
+  pdl_wait();
   for (int64_t q = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; q < g.P; q += nwarps) {
     const int gl = __ldg(gslot + q);
     if (gl < 0) continue;
     const uint8_t* qr = exq + (int64_t)gl * g.H;
     const float* sr = exs + (int64_t)gl * (g.H / 128);
     uint16_t* yr = ey + (int64_t)gl * g.H;
-    for (int v = lane; v < nvec; v += 32) {
-      const uint4 c = ld_stream16(qr + v * 16);
-      const float sc = __ldg(sr + (v * 16) / 128);
-      uint4 o0, o1;
-      o0.x = dequant2((uint16_t)(c.x & 0xffffu), sc);
-      o0.y = dequant2((uint16_t)(c.x >> 16), sc);
-      o0.z = dequant2((uint16_t)(c.y & 0xffffu), sc);
-      o0.w = dequant2((uint16_t)(c.y >> 16), sc);
-      o1.x = dequant2((uint16_t)(c.z & 0xffffu), sc);
-      o1.y = dequant2((uint16_t)(c.z >> 16), sc);
-      o1.z = dequant2((uint16_t)(c.w & 0xffffu), sc);
-      o1.w = dequant2((uint16_t)(c.w >> 16), sc);
-      st16(yr + v * 16, o0);
-      st16(yr + v * 16 + 8, o1);
+    for (int v0 = lane; v0 < nvec; v0 += 32 * kDequantUnroll) {
+      uint4 c[kDequantUnroll];
+      float sc[kDequantUnroll];
+#pragma unroll
+      for (int j = 0; j < kDequantUnroll; ++j) {
+        const int v = v0 + 32 * j;
+        if (v < nvec) {
+          c[j] = ld_stream16(qr + v * 16);
+          sc[j] = __ldg(sr + (v * 16) / 128);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kDequantUnroll; ++j) {
+        const int v = v0 + 32 * j;
+        if (v >= nvec) continue;
+        uint4 o0, o1;
+        o0.x = dequant2((uint16_t)(c[j].x & 0xffffu), sc[j]);
+        o0.y = dequant2((uint16_t)(c[j].x >> 16), sc[j]);
+        o0.z = dequant2((uint16_t)(c[j].y & 0xffffu), sc[j]);
+        o0.w = dequant2((uint16_t)(c[j].y >> 16), sc[j]);
+        o1.x = dequant2((uint16_t)(c[j].z & 0xffffu), sc[j]);
+        o1.y = dequant2((uint16_t)(c[j].z >> 16), sc[j]);
+        o1.z = dequant2((uint16_t)(c[j].w & 0xffffu), sc[j]);
+        o1.w = dequant2((uint16_t)(c[j].w >> 16), sc[j]);
+        st16(yr + v * 16, o0);
+        st16(yr + v * 16 + 8, o1);
+      }
     }
   }
+  pdl_trigger();
 }
 
 // Combine receive. Block (token u, column tile); a thread owns 8 bf16 columns (16 bytes).
@@ -128,6 +160,7 @@ __global__ void __launch_bounds__(kReduceThreads) k_combine_reduce(Geo g, const 
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+  pdl_wait();
   for (int k0 = 0; k0 < g.R; k0 += 32) {
     int myrow = -1;
     float myw = 0.0f;
@@ -173,6 +206,7 @@ __global__ void __launch_bounds__(kReduceThreads) k_combine_reduce(Geo g, const 
     o.w = pack_bf16x2(acc[6], acc[7]);
     st16(out + u * g.H + col * 8, o);
   }
+  pdl_trigger();
 }
 
 }  // namespace
@@ -180,12 +214,11 @@ __global__ void __launch_bounds__(kReduceThreads) k_combine_reduce(Geo g, const 
 cudaError_t launch_quant_fp8(const Geo& g, const uint16_t* x, uint8_t* xq, Ctx& c) {
   const int64_t nblk = (int64_t)g.N * g.T * (g.H / 128);
   if (nblk == 0) return cudaSuccess;
-  int64_t blocks = (nblk + 15) / 16;  // 8 warps x 2 blocks per CTA
+  int64_t blocks = (nblk + 16 * kQuantUnroll - 1) / (16 * kQuantUnroll);  // 8 warps x 2 x unroll blocks per CTA
   const int64_t maxb = (int64_t)c.num_sms * 8;
   if (blocks > maxb) blocks = maxb;
   LaunchScope ls(c, MOE_K_QUANT_FP8);
-  k_quant_fp8<<<(unsigned)blocks, 256, 0, c.stream>>>(g, x, xq);
-  return cudaGetLastError();
+  return launch_kernel(k_quant_fp8, dim3((unsigned)blocks), dim3(256), 0, c, g, x, xq);
 }
 
 cudaError_t launch_dequant_fp8(const Geo& g, const moe_layout_t* lay, const uint8_t* exq, const float* exs,
@@ -195,8 +228,8 @@ cudaError_t launch_dequant_fp8(const Geo& g, const moe_layout_t* lay, const uint
   const int64_t maxb = (int64_t)c.num_sms * 8;
   if (blocks > maxb) blocks = maxb;
   LaunchScope ls(c, MOE_K_EXPERT);
-  k_dequant_fp8<<<(unsigned)blocks, 256, 0, c.stream>>>(g, lay->gslot, exq, exs, ey);
-  return cudaGetLastError();
+  return launch_kernel(k_dequant_fp8, dim3((unsigned)blocks), dim3(256), 0, c, g, (const int32_t*)lay->gslot, exq,
+                       exs, ey);
 }
 
 cudaError_t launch_combine_reduce(const Geo& g, const moe_layout_t* lay, const uint16_t* crecv, const float* w,
@@ -206,8 +239,8 @@ cudaError_t launch_combine_reduce(const Geo& g, const moe_layout_t* lay, const u
   const int ncol = g.H / 8;
   dim3 grid((unsigned)tokens, (unsigned)((ncol + kReduceThreads - 1) / kReduceThreads));
   LaunchScope ls(c, MOE_K_COMBINE_REDUCE);
-  k_combine_reduce<<<grid, kReduceThreads, 0, c.stream>>>(g, lay->gsend, lay->gslot, w, crecv, out);
-  return cudaGetLastError();
+  return launch_kernel(k_combine_reduce, grid, dim3(kReduceThreads), 0, c, g, (const int32_t*)lay->gsend,
+                       (const int32_t*)lay->gslot, w, crecv, out);
 }
 
 }  // namespace moe

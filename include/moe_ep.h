@@ -70,7 +70,7 @@ typedef struct {
 
 /* Kernel ids reported through moe_prof_t. */
 typedef enum {
-    MOE_K_ROUTE_COUNT = 0,     /* routing-count histogram + stable pair ranks + scans */
+    MOE_K_ROUTE_COUNT = 0,     /* routing-count histogram per 256-pair chunk + stable ranks */
     MOE_K_LAYOUT_MAPS = 1,     /* per-pair placements and inverse maps */
     MOE_K_QUANT_FP8 = 2,       /* block-scaled fp8 quantisation */
     MOE_K_PACK = 3,            /* dispatch send: token rows -> send rows */
@@ -80,7 +80,10 @@ typedef enum {
     MOE_K_COMBINE_PACK = 7,    /* combine send: grouped rows -> receive order */
     MOE_K_COMBINE_SCATTER = 8, /* combine "RDMA write": back to the source ranks */
     MOE_K_COMBINE_REDUCE = 9,  /* combine recv: weighted sum over R -> bf16 */
-    MOE_K_NUM = 10
+    MOE_K_ROUTE_SCAN = 10,     /* per-rank totals and every exclusive scan */
+    MOE_K_PACK_PUSH = 11,      /* direct push: token rows -> owners' receive rows */
+    MOE_K_COMBINE_PUSH = 12,   /* direct push: grouped rows -> sources' combine rows */
+    MOE_K_NUM = 13
 } moe_kernel_id;
 
 /* Optional per-kernel timing. When moe_layout_t.prof is non-NULL, every kernel the library
@@ -96,9 +99,23 @@ typedef struct {
 } moe_prof_t;
 
 /* moe_layout_t.flags */
-#define MOE_FLAG_LDG_MOVER 0x1u /* move rows with 16-byte register loads/stores instead of
-                                   TMA bulk copies (always used where rows are not 16-byte
-                                   multiples, e.g. fp8 with H % 512 != 0) */
+/* Row movers. By default each launch picks one: TMA bulk copies for the one-to-one moves
+ * when every issuer warp has at least 20 rows to stream, 16-byte register loads/stores for
+ * pack (one row to R destinations) and for small problems. Rows that are not 16-byte
+ * multiples (fp8 with H % 512 != 0) always take the register path. */
+#define MOE_FLAG_LDG_MOVER 0x1u /* force the register mover for every move */
+#define MOE_FLAG_TMA_MOVER 0x4u /* force the TMA mover wherever rows allow it */
+/* Direct push: the send halves write straight into the destination's buffer, the way the
+ * page's intra-node path pushes tokens over NVLink into peers' mapped receive buffers
+ * (sections "MoE all-to-all over EFA" and "Dispatch and combine"). moe_dispatch_send packs
+ * each pair into its owner's receive row (d_send is not used and may be NULL), and
+ * moe_combine_send writes each expert output into its source's combine row (d_csend is
+ * not used and may be NULL). The receive, grouped and combine buffers hold exactly what
+ * they hold without the flag; the per-peer write step is fused away. */
+#define MOE_FLAG_DIRECT_PUSH 0x8u
+#define MOE_FLAG_NO_PDL 0x2u    /* launch without programmatic dependent launch (by default
+                                   each kernel may be scheduled while its predecessor in the
+                                   stream drains; it waits for it before touching memory) */
 
 /*
  * Routing layout. Device arrays carved by moe_layout_init from one caller workspace, filled
@@ -124,6 +141,7 @@ typedef struct {
  *   gslot [N*T*R]  global grouped row, e*cap + slot (row of d_expert_x), or -1 when the
  *                  pair's expert id is bad or the pair was dropped for capacity
  *   status   [1]         sticky error bits, bit (1 << moe_status)
+ *   scratch  [N][ceil(T*R/256)][E]  internal: per-chunk counts, then chunk offsets
  * Host-side fields (set by the caller after moe_layout_init, read at each call):
  *   flags, prof, tma_stages (0 = automatic, else 1..32 stages per TMA mover CTA),
  *   ctas_per_sm (0 = automatic, else mover CTAs per SM).
@@ -133,7 +151,7 @@ typedef struct {
     int32_t *pos, *rrow, *slot, *slot_src, *recv_src;
     int32_t *gsend, *grecv, *gslot;
     int32_t *status;
-    int32_t *scratch; /* internal: completion counter of the routing-count kernel */
+    int32_t *scratch; /* internal: chunk count table of the routing-count kernels */
     uint32_t flags;
     moe_prof_t *prof;
     int32_t tma_stages;
@@ -170,7 +188,8 @@ typedef struct {
 } moe_buffers_t;
 
 /* Validates dims: N >= 1, T >= 0, E % N == 0, R >= 1, cap >= 0, H % 8 == 0 (bf16) or
- * H % 128 == 0 (fp8), and the library's limits (E <= 1536, N*E + N*N <= 56832, all row
+ * H % 128 == 0 (fp8), and the library's limits (E <= 1536, N*E' + N*N' <= 56832 with E', N'
+ * the odd numbers E|1, N|1, all row
  * counts below 2^31). MOE_OK or MOE_ERR_INVALID_ARG. */
 moe_status moe_check_dims(const moe_dims *dims);
 

@@ -58,8 +58,9 @@ def u16(t: torch.Tensor) -> np.ndarray:
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-def compare_all(orc, wl, inp, res, check_poison=True):
-    """Bit-exact comparison of every buffer's used rows with the oracle; padding untouched."""
+def compare_all(orc, wl, inp, res, check_poison=True, push=False):
+    """Bit-exact comparison of every buffer's used rows with the oracle; padding untouched.
+    With push (direct-push mode) the send and combine-send buffers must stay untouched."""
     N, T, H, E, R, L = wl.N, wl.T, wl.H, wl.E, wl.R, wl.L
     o = orc.forward(N, T, H, E, R, wl.cap, wl.payload, inp["x"], inp["idx"], inp["w"])
     lay_o = o["layout"]
@@ -75,7 +76,9 @@ def compare_all(orc, wl, inp, res, check_poison=True):
         np.testing.assert_array_equal(u8(res["xq"]), o["xq"], err_msg="fp8 quantised rows")
     # send rows of every valid pair
     send = u8(res["send"])
-    for s in range(N):
+    if push:
+        assert (send == POISON).all(), "direct push wrote the send buffer"
+    for s in ([] if push else range(N)):
         rows = pos[s][valid[s]]
         np.testing.assert_array_equal(send[s][rows], o["send"][s][rows], err_msg="send")
         if check_poison:
@@ -117,7 +120,9 @@ def compare_all(orc, wl, inp, res, check_poison=True):
                 np.testing.assert_array_equal(ey[d, l, :n], o["ex"][d, l, :n], err_msg="identity expert copy")
     csend = u16(res["csend"])
     crecv = u16(res["crecv"])
-    for d in range(N):
+    if push:
+        assert (csend.view(np.uint8) == POISON).all(), "direct push wrote the combine send buffer"
+    for d in ([] if push else range(N)):
         rows = lay_o["rrow"][kept & (np.asarray(inp["idx"]) // L == d)] if L > 0 else []
         np.testing.assert_array_equal(csend[d][rows], o["csend"][d][rows], err_msg="combine send rows")
     for s in range(N):

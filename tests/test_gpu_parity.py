@@ -30,7 +30,7 @@ def _built():
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
 
 
-@pytest.mark.parametrize("flags", [0, 1], ids=["tma", "ldg"])
+@pytest.mark.parametrize("flags", [0, 1, 4, 6], ids=["auto", "ldg", "tma", "tma-nopdl"])
 @pytest.mark.parametrize("wl", CASES, ids=lambda w: w.name)
 def test_path_matches_oracle(orc, wl, flags):
     inp = workloads.make_inputs(wl)
@@ -38,7 +38,17 @@ def test_path_matches_oracle(orc, wl, flags):
     compare_all(orc, wl, inp, res)
 
 
-@pytest.mark.parametrize("flags", [0, 1], ids=["tma", "ldg"])
+@pytest.mark.parametrize("flags", [8, 9, 12], ids=["push-auto", "push-ldg", "push-tma"])
+@pytest.mark.parametrize("wl", CASES, ids=lambda w: w.name)
+def test_direct_push_matches_oracle(orc, wl, flags):
+    """Direct push (pack into the owners' receive rows, combine into the sources' rows)
+    leaves exactly the canonical receive, grouped and combine contents."""
+    inp = workloads.make_inputs(wl)
+    _, res = run_gpu(wl, inp, flags=flags)
+    compare_all(orc, wl, inp, res, push=True)
+
+
+@pytest.mark.parametrize("flags", [1, 4, 12], ids=["ldg", "tma", "push-tma"])
 def test_duplicates_and_bad_ids(orc, flags):
     wl = W("dups", 3, 21, 256, 12, 4, "bf16", "uniform", 110)
     inp = workloads.make_inputs(wl)
@@ -50,7 +60,7 @@ def test_duplicates_and_bad_ids(orc, flags):
     inp["idx"] = idx
     _, res = run_gpu(wl, inp, flags=flags)
     assert res["status_code"] == 2                      # MOE_ERR_EXPERT_RANGE, no trap
-    compare_all(orc, wl, inp, res)
+    compare_all(orc, wl, inp, res, push=bool(flags & 8))
 
 
 def test_random_tiny_layouts_bit_exact(orc):
@@ -143,8 +153,8 @@ def test_launch_counter_counts_kernels():
     n0 = lib().moe_launch_count()
     ep.forward(to_dev(inp["x"]).view(torch.bfloat16), to_dev(inp["idx"]), to_dev(inp["w"]))
     torch.cuda.synchronize()
-    # layout (2) + pack + scatter + unpack + combine pack + combine scatter + reduce; bf16 identity aliases
-    assert lib().moe_launch_count() - n0 == 8
+    # layout (3) + pack + scatter + unpack + combine pack + combine scatter + reduce; bf16 identity aliases
+    assert lib().moe_launch_count() - n0 == 9
 
 
 def test_profiling_events_bracket_each_kernel():
@@ -163,7 +173,7 @@ def test_profiling_events_bracket_each_kernel():
     ep.forward(to_dev(inp["x"]).view(torch.bfloat16), to_dev(inp["idx"]), to_dev(inp["w"]))
     torch.cuda.synchronize()
     names = [KERNEL_NAMES[prof.kernel[i]] for i in range(prof.n)]
-    assert names == ["route_count", "layout_maps", "quant_fp8", "pack", "scatter", "unpack", "expert",
-                     "combine_pack", "combine_scatter", "combine_reduce"]
+    assert names == ["route_count", "route_scan", "layout_maps", "quant_fp8", "pack", "scatter", "unpack",
+                     "expert", "combine_pack", "combine_scatter", "combine_reduce"]
     for i in range(prof.n):
         assert evs[2 * i].elapsed_time(evs[2 * i + 1]) >= 0.0
