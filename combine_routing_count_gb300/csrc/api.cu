@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "internal.h"
 
@@ -15,7 +17,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxE = 1536;
-constexpr int64_t kMaxScanInts = 56832;  // N*(E|1) + N*(N|1) ints staged in shared memory
+constexpr int64_t kMaxN = 2048;           // ranks: the scan CTAs stage up to 64*33 per-rank values
 constexpr int64_t kI32 = 0x7fffffff;
 
 struct DevInfo {
@@ -36,7 +38,7 @@ moe_status make_geo(const moe_dims* d, Geo& g) {
   if (d->payload == MOE_PAYLOAD_FP8_E4M3_B128 && d->H % 128 != 0) return MOE_ERR_INVALID_ARG;
   if (d->E > kMaxE) return MOE_ERR_INVALID_ARG;
   const int64_t N = d->N, T = d->T, E = d->E, R = d->R, L = E / N;
-  if (N * (E | 1) + N * (N | 1) > kMaxScanInts) return MOE_ERR_INVALID_ARG;
+  if (N > kMaxN) return MOE_ERR_INVALID_ARG;
   const int64_t cap = d->cap > 0 ? d->cap : N * T;  // 0 only when there are no tokens
   const int64_t RB = N * T * (R > L ? R : L);
   if (N * T * R > kI32 || N * RB > kI32 || E * cap > kI32 || N * T * (int64_t)d->H > (int64_t)1 << 40)
@@ -123,7 +125,7 @@ WsPlan ws_plan(const Geo& g) {
                           P,               // grecv
                           P,               // gslot
                           16,              // status
-                          (size_t)N * layout_chunks(g) * E + 16};  // scratch: chunk table
+                          (size_t)layout_scratch_done_offset(g) + N + 16};  // scratch: chunk table + counters
   w.total = 0;
   for (int i = 0; i < 17; ++i) {
     w.n[i] = al256(4 * sizes[i]);
@@ -186,6 +188,8 @@ moe_status moe_layout_init(const moe_dims* dims, void* d_ws, size_t ws_bytes, mo
   out->ctas_per_sm = 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(out->status, 0, 64, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(out->scratch + layout_scratch_done_offset(g), 0, 4 * (size_t)g.N, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
   return MOE_OK;
 }
 
@@ -196,7 +200,6 @@ moe_status moe_layout(const moe_dims* dims, const int32_t* d_idx, const moe_layo
   if (!layout_ok(lay) || (!d_idx && g.P > 0)) return MOE_ERR_INVALID_ARG;
   Ctx c;
   if ((st = make_ctx(lay, stream, c)) != MOE_OK) return st;
-  if (layout_smem_bytes(g) + 1024 > (size_t)c.smem_optin) return MOE_ERR_INVALID_ARG;
   return cuda_status(launch_layout(g, d_idx, lay, c));
 }
 

@@ -77,8 +77,8 @@ inline cudaError_t ensure_dyn_smem(K kernel, int device, size_t bytes, std::atom
 
 // layout.cu
 cudaError_t launch_layout(const Geo& g, const int32_t* idx, const moe_layout_t* lay, Ctx& c);
-size_t layout_smem_bytes(const Geo& g);
 int layout_chunks(const Geo& g);
+int64_t layout_scratch_done_offset(const Geo& g);  // ints from the scratch start to the counters
 
 // movers.cu: row movement kernels.
 enum MoveKind : int {

@@ -26,7 +26,6 @@ namespace moe {
 namespace {
 
 constexpr int kChunk = 256;          // pairs per histogram CTA (= its threads)
-constexpr int kScanThreads = 1024;   // threads of the scan CTA
 constexpr unsigned kFull = 0xffffffffu;
 
 struct LayoutArgs {
@@ -36,6 +35,7 @@ struct LayoutArgs {
   int32_t *gsend, *grecv, *gslot;
   int32_t* status;
   int32_t* ccnt;    // [N][nch][E]: per-chunk counts
+  int32_t* done;    // [N]: chunk CTAs of each rank that have finished (reset by the last one)
   int nch;          // chunks per rank, ceil(T*R / kChunk)
 };
 
@@ -48,103 +48,138 @@ __device__ __forceinline__ int warp_inclusive_scan(int v, int lane) {
   return v;
 }
 
-// Exclusive scans over the full count table; run by the last CTA of k_route_count.
-// The table is staged in shared memory with odd row strides (E|1, N|1) so that the
-// column walks below are free of bank conflicts; every scan runs one warp per row with
-// lanes along the scanned dimension, so the global stores are coalesced.
-__device__ __forceinline__ void layout_scans(const Geo& g, const LayoutArgs& a, int32_t* sm) {
-  const int N = g.N, E = g.E, L = g.L;
-  const int E1 = E | 1, N1 = N | 1;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  constexpr int kWarps = kScanThreads / 32;
-  int32_t* scnt = sm;               // [N][E1]
-  int32_t* sC = sm + N * E1;        // [N][N1], sC[s*N1 + d] = C[s][d]
+// The scans, as one grid of independent CTAs (kScanThreads threads each), by role:
+//   [0, N)              row CTA s:    soff[s][.] = exclusive scan of cnt[s][.] over experts,
+//                                     C[s][d] = sum of cnt[s][.] over d's experts;
+//   [N, N + ceil(E/32)) column CTA:   for 32 experts e, eoff[e][.] = exclusive scan of
+//                                     cnt[.][e] over source ranks, ecnt[e] = its total;
+//   [.., + N)           dest CTA d:   roff[d][.] = exclusive scan of C[.][d] over source
+//                                     ranks, rtot[d] = its total.
+// Every CTA reads the per-rank totals cnt[][] written by the counting kernel; lanes run
+// along the scanned dimension, so global stores are coalesced.
+constexpr int kScanThreads = 256;
 
-  // cnt[s][e] = sum of the chunk counts, read kColBatch columns at a time so that their
-  // loads are in flight together.
-  constexpr int kColBatch = 8;
-  const int nch = a.nch;
-  const int NE = N * E;
-  for (int i0 = tid; i0 < NE; i0 += kScanThreads * kColBatch) {
-    int run[kColBatch];
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int incl = warp_inclusive_scan(v, lane);
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int t = lane < kScanThreads / 32 ? warp_tot[lane] : 0;
+    const int ti = warp_inclusive_scan(t, lane);
+    if (lane < kScanThreads / 32) warp_tot[lane] = ti - t;
+    if (lane == 31) warp_tot[kScanThreads / 32] = ti;
+  }
+  __syncthreads();
+  total = warp_tot[kScanThreads / 32];
+  const int r = warp_tot[warp] + incl - v;
+  __syncthreads();
+  return r;
+}
+
+// cnt[i], or 0 when there are no tokens (no counting kernel ran; the row CTAs write the 0s).
+__device__ __forceinline__ int cnt_at(const LayoutArgs& a, int64_t i) {
+  return a.nch > 0 ? __ldcg(a.cnt + i) : 0;
+}
+
+__global__ void __launch_bounds__(kScanThreads) k_route_scan(Geo g, LayoutArgs a) {
+  __shared__ int warp_tot[kScanThreads / 32 + 1];
+  __shared__ int tile[64 * 33];
+  const int N = g.N, E = g.E, L = g.L;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n_col = (E + 31) / 32;
+  const int b = blockIdx.x;
+  pdl_wait();
+  if (b < N) {
+    // ---- row CTA: soff[s][.] and C[s][.]
+    const int s = b;
+    const int k = (E + kScanThreads - 1) / kScanThreads;      // experts per thread, <= 6
+    const int e0 = tid * k;
+    int vals[6];
+    int sum = 0;
 #pragma unroll
-    for (int j = 0; j < kColBatch; ++j) run[j] = 0;
-    for (int c = 0; c < nch; ++c) {
-      int v[kColBatch];
+    for (int j = 0; j < 6; ++j) {
+      vals[j] = (j < k && e0 + j < E) ? cnt_at(a, (int64_t)s * E + e0 + j) : 0;
+      sum += vals[j];
+    }
+    int total;
+    int run = block_exclusive_scan(sum, warp_tot, total);
 #pragma unroll
-      for (int j = 0; j < kColBatch; ++j) {
-        const int i = i0 + j * kScanThreads;
-        v[j] = 0;
-        if (i < NE) {
-          const int s = i / E;
-          v[j] = __ldcg(a.ccnt + ((int64_t)s * nch + c) * E + (i - s * E));
+    for (int j = 0; j < 6; ++j)
+      if (j < k && e0 + j < E) {
+        a.soff[(int64_t)s * E + e0 + j] = run;
+        run += vals[j];
+        if (a.nch == 0) a.cnt[(int64_t)s * E + e0 + j] = 0;
+      }
+    for (int d = warp; d < N; d += kScanThreads / 32) {   // C[s][d]: lanes along d's experts
+      int c = 0;
+      for (int l = lane; l < L; l += 32) c += cnt_at(a, (int64_t)s * E + d * L + l);
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
+      if (lane == 0) a.C[s * N + d] = c;
+    }
+  } else if (b < N + n_col) {
+    // ---- column CTA: eoff[e][.] and ecnt[e] for experts e0 .. e0+31. Tiles of 64 ranks
+    // x 32 experts are staged in shared memory (coalesced rows, odd stride); warp w scans
+    // experts w, w+8, w+16, w+24 down the ranks, carrying their totals across tiles.
+    const int e0 = (b - N) * 32;
+    int carry[4] = {0, 0, 0, 0};
+    for (int s0 = 0; s0 < N; s0 += 64) {
+      const int ns = N - s0 < 64 ? N - s0 : 64;
+      for (int i = tid; i < ns * 32; i += kScanThreads) {
+        const int ss = i >> 5, ee = i & 31;
+        tile[ss * 33 + ee] = (e0 + ee < E) ? cnt_at(a, (int64_t)(s0 + ss) * E + e0 + ee) : 0;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int ee = warp + 8 * j, e = e0 + ee;
+        for (int sc = 0; sc < ns; sc += 32) {
+          const int sl = sc + lane;
+          const int v = sl < ns ? tile[sl * 33 + ee] : 0;
+          const int incl = warp_inclusive_scan(v, lane);
+          if (sl < ns && e < E) a.eoff[(int64_t)e * N + s0 + sl] = carry[j] + incl - v;
+          carry[j] += __shfl_sync(kFull, incl, 31);
         }
       }
-#pragma unroll
-      for (int j = 0; j < kColBatch; ++j) run[j] += v[j];
+      __syncthreads();
     }
 #pragma unroll
-    for (int j = 0; j < kColBatch; ++j) {
-      const int i = i0 + j * kScanThreads;
-      if (i < NE) {
-        const int s = i / E;
-        scnt[s * E1 + (i - s * E)] = run[j];
-        a.cnt[i] = run[j];
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + warp + 8 * j;
+      if (lane == 0 && e < E) {
+        a.ecnt[e] = carry[j];
+        if (carry[j] > g.cap) set_status(a.status, kBitCapacity);
+      }
+    }
+  } else {
+    // ---- destination CTA: roff[d][.] and rtot[d]
+    const int d = b - N - n_col;
+    int* cd = tile;   // cd[s] = C[s][d], N <= 64*33
+    for (int s = warp; s < N; s += kScanThreads / 32) {
+      int c = 0;
+      for (int l = lane; l < L; l += 32) c += cnt_at(a, (int64_t)s * E + d * L + l);
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
+      if (lane == 0) cd[s] = c;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int carry = 0;
+      for (int sc = 0; sc < N; sc += 32) {
+        const int s = sc + lane;
+        const int v = s < N ? cd[s] : 0;
+        const int incl = warp_inclusive_scan(v, lane);
+        if (s < N) a.roff[d * N + s] = carry + incl - v;
+        carry += __shfl_sync(kFull, incl, 31);
+      }
+      if (lane == 0) {
+        a.rtot[d] = carry;
+        if ((int64_t)carry > g.RB) set_status(a.status, kBitRecvBound);
       }
     }
   }
-  __syncthreads();
-
-  // C[s][d] = sum over d's experts of cnt[s][.]
-  for (int i = tid; i < N * N; i += kScanThreads) {
-    const int s = i / N, d = i - s * N;
-    int c = 0;
-    for (int l = 0; l < L; ++l) c += scnt[s * E1 + d * L + l];
-    sC[s * N1 + d] = c;
-    a.C[i] = c;
-  }
-  // soff[s][e]: scan over experts, one warp per source rank
-  for (int s = warp; s < N; s += kWarps) {
-    int carry = 0;
-    for (int e0 = 0; e0 < E; e0 += 32) {
-      const int e = e0 + lane;
-      const int v = e < E ? scnt[s * E1 + e] : 0;
-      const int incl = warp_inclusive_scan(v, lane);
-      if (e < E) a.soff[(int64_t)s * E + e] = carry + incl - v;
-      carry += __shfl_sync(kFull, incl, 31);
-    }
-  }
-  // eoff[d][l][s] (= eoff[e][s]) and ecnt[e]: scan over source ranks, one warp per expert
-  for (int e = warp; e < E; e += kWarps) {
-    int carry = 0;
-    for (int s0 = 0; s0 < N; s0 += 32) {
-      const int s = s0 + lane;
-      const int v = s < N ? scnt[s * E1 + e] : 0;
-      const int incl = warp_inclusive_scan(v, lane);
-      if (s < N) a.eoff[(int64_t)e * N + s] = carry + incl - v;
-      carry += __shfl_sync(kFull, incl, 31);
-    }
-    if (lane == 0) {
-      a.ecnt[e] = carry;
-      if (carry > g.cap) set_status(a.status, kBitCapacity);
-    }
-  }
-  __syncthreads();
-  // roff[d][s] and rtot[d]: scan of C[.][d] over source ranks, one warp per destination
-  for (int d = warp; d < N; d += kWarps) {
-    int carry = 0;
-    for (int s0 = 0; s0 < N; s0 += 32) {
-      const int s = s0 + lane;
-      const int v = s < N ? sC[s * N1 + d] : 0;
-      const int incl = warp_inclusive_scan(v, lane);
-      if (s < N) a.roff[d * N + s] = carry + incl - v;
-      carry += __shfl_sync(kFull, incl, 31);
-    }
-    if (lane == 0) {
-      a.rtot[d] = carry;
-      if ((int64_t)carry > g.RB) set_status(a.status, kBitRecvBound);
-    }
-  }
+  pdl_trigger();
 }
 
 // One CTA per (chunk c, source rank s): the chunk's 256 pairs in (t,k) order, one per
@@ -182,14 +217,30 @@ __global__ void __launch_bounds__(kChunk) k_route_count(Geo g, LayoutArgs a) {
   }
   __syncthreads();
   if (in) a.pos[q] = ok ? wtab[warp * E + e] + lrank : -1;
-  pdl_trigger();
-}
 
-// One CTA: per-rank totals and every scan (see layout_scans).
-__global__ void __launch_bounds__(kScanThreads, 1) k_route_scan(Geo g, LayoutArgs a) {
-  extern __shared__ int32_t sm[];
-  pdl_wait();
-  layout_scans(g, a, sm);
+  // The last chunk CTA of rank s to finish sums the rank's chunk rows into cnt[s][.]
+  // (completion counter per rank; no CTA waits for another).
+  __shared__ int is_last;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) is_last = (atomicAdd(a.done + s, 1) == a.nch - 1);
+  __syncthreads();
+  if (is_last) {
+    __threadfence();
+    const int32_t* base = a.ccnt + (int64_t)s * a.nch * E;
+    for (int ee = tid; ee < E; ee += kChunk) {
+      int r = 0;
+      int cc = 0;
+      for (; cc + 4 <= a.nch; cc += 4) {   // four independent loads in flight
+        const int v0 = __ldcg(base + (int64_t)cc * E + ee), v1 = __ldcg(base + (int64_t)(cc + 1) * E + ee);
+        const int v2 = __ldcg(base + (int64_t)(cc + 2) * E + ee), v3 = __ldcg(base + (int64_t)(cc + 3) * E + ee);
+        r += v0 + v1 + v2 + v3;
+      }
+      for (; cc < a.nch; ++cc) r += __ldcg(base + (int64_t)cc * E + ee);
+      a.cnt[(int64_t)s * E + ee] = r;
+    }
+    if (tid == 0) a.done[s] = 0;  // ready for the next call
+  }
   pdl_trigger();
 }
 
@@ -255,15 +306,13 @@ __global__ void __launch_bounds__(kMapThreads) k_layout_maps(Geo g, LayoutArgs a
   pdl_trigger();
 }
 
-std::atomic<int> g_scan_smem[64];
 
 }  // namespace
 
 int layout_chunks(const Geo& g) { return (int)((g.TR + kChunk - 1) / kChunk); }
 
-size_t layout_smem_bytes(const Geo& g) {
-  return 4 * ((size_t)g.N * (g.E | 1) + (size_t)g.N * (g.N | 1));
-}
+int64_t layout_scratch_done_offset(const Geo& g) { return (int64_t)g.N * layout_chunks(g) * g.E; }
+
 
 cudaError_t launch_layout(const Geo& g, const int32_t* idx, const moe_layout_t* lay, Ctx& c) {
   LayoutArgs a;
@@ -284,13 +333,11 @@ cudaError_t launch_layout(const Geo& g, const int32_t* idx, const moe_layout_t* 
   a.grecv = lay->grecv;
   a.gslot = lay->gslot;
   a.status = lay->status;
-  a.ccnt = lay->scratch;
   a.nch = layout_chunks(g);
+  a.ccnt = lay->scratch;
+  a.done = lay->scratch + layout_scratch_done_offset(g);
 
-  const size_t scan_smem = layout_smem_bytes(g);
-  if (scan_smem + 1024 > (size_t)c.smem_optin) return cudaErrorInvalidValue;
-  cudaError_t e = ensure_dyn_smem(k_route_scan, c.device, scan_smem, g_scan_smem);
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
   if (a.nch > 0) {
     LaunchScope ls(c, MOE_K_ROUTE_COUNT);
     e = launch_kernel(k_route_count, dim3(a.nch, g.N), dim3(kChunk), (size_t)4 * (kChunk / 32) * g.E, c, g, a);
@@ -298,7 +345,7 @@ cudaError_t launch_layout(const Geo& g, const int32_t* idx, const moe_layout_t* 
   }
   {
     LaunchScope ls(c, MOE_K_ROUTE_SCAN);
-    e = launch_kernel(k_route_scan, dim3(1), dim3(kScanThreads), scan_smem, c, g, a);
+    e = launch_kernel(k_route_scan, dim3(2 * g.N + (g.E + 31) / 32), dim3(kScanThreads), 0, c, g, a);
   }
   if (e != cudaSuccess) return e;
   const int pair_blocks = (int)((g.P + kMapThreads - 1) / kMapThreads);

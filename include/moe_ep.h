@@ -188,8 +188,7 @@ typedef struct {
 } moe_buffers_t;
 
 /* Validates dims: N >= 1, T >= 0, E % N == 0, R >= 1, cap >= 0, H % 8 == 0 (bf16) or
- * H % 128 == 0 (fp8), and the library's limits (E <= 1536, N*E' + N*N' <= 56832 with E', N'
- * the odd numbers E|1, N|1, all row
+ * H % 128 == 0 (fp8), and the library's limits (E <= 1536, N <= 2048, all row
  * counts below 2^31). MOE_OK or MOE_ERR_INVALID_ARG. */
 moe_status moe_check_dims(const moe_dims *dims);
 

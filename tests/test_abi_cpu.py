@@ -40,7 +40,7 @@ def test_dims_validation(L):
     ok = _dims()
     assert L.moe_check_dims(ctypes.byref(ok)) == 0
     bad = [_dims(E=255), _dims(N=0), _dims(T=-1), _dims(H=7170), _dims(R=0), _dims(cap=-1),
-           _dims(H=200, payload=1), _dims(payload=2), _dims(E=2048, N=8), _dims(N=256, E=512)]
+           _dims(H=200, payload=1), _dims(payload=2), _dims(E=2048, N=8), _dims(N=4096, E=4096)]
     for d in bad:
         assert L.moe_check_dims(ctypes.byref(d)) == 1, (d.N, d.T, d.H, d.E, d.R, d.cap, d.payload)
     assert L.moe_check_dims(None) == 1
