@@ -60,10 +60,11 @@ __host__ __device__ __forceinline__ uint32_t load_bytes(const Geo& g) {
   return (uint32_t)(2 * g.H);
 }
 
-// Bytes one unit moves per destination: a chunk for pack, a whole row otherwise.
+// Bytes one unit moves per destination: one column chunk of a row (the whole row when
+// the move is not chunked).
 template <int KIND>
 __host__ __device__ __forceinline__ uint32_t unit_bytes(const Geo& g, const MoveArgs& a) {
-  return (KIND == kMovePack || KIND == kMovePackPush) ? a.chunk_bytes : load_bytes<KIND>(g);
+  return a.chunk_bytes;
 }
 
 // Fills `pl` for unit u; false when the unit moves nothing (bad expert id or dropped pair).
@@ -79,52 +80,56 @@ __device__ __forceinline__ bool make_plan(const Geo& g, const MoveArgs& a, int64
     for (int k = 0; k < kPackPrefetch; ++k) pl.p[k] = (k < g.R) ? __ldg(a.fan + tok * g.R + k) : -1;
     return true;
   }
+  // Non-pack kinds: unit u is column chunk (u % chunks) of pair u / chunks.
+  const int64_t cq = u / a.chunks;
+  const int64_t coff = (u - cq * a.chunks) * (int64_t)a.chunk_bytes;
+  u = cq;
   if (KIND == kMoveScatter) {
     const int gs = __ldg(a.gsend + u);
     const int gr = __ldg(a.grecv + u);
     if (gs < 0) return false;
-    pl.src = a.src + (int64_t)gs * g.B;
-    pl.dst = a.dst + (int64_t)gr * g.B;
+    pl.src = a.src + (int64_t)gs * g.B + coff;
+    pl.dst = a.dst + (int64_t)gr * g.B + coff;
     return true;
   }
   if (KIND == kMoveCopyEx) {
     const int gl = __ldg(a.gslot + u);
     if (gl < 0) return false;
-    pl.src = a.src + (int64_t)gl * H2;
-    pl.dst = a.dst + (int64_t)gl * H2;
+    pl.src = a.src + (int64_t)gl * H2 + coff;
+    pl.dst = a.dst + (int64_t)gl * H2 + coff;
     return true;
   }
   const int gl = __ldg(a.gslot + u);
   const int gr = __ldg(a.grecv + u);
   if (KIND == kMoveUnpack) {
     if (gl < 0) return false;
-    pl.src = a.src + (int64_t)gr * g.B;
+    pl.src = a.src + (int64_t)gr * g.B + coff;
     if (FP8) {
       pl.dst = a.dst + (int64_t)gl * g.H;
       pl.dst2 = a.dst2 + (int64_t)gl * (g.H / 32);
     } else {
-      pl.dst = a.dst + (int64_t)gl * g.B;
+      pl.dst = a.dst + (int64_t)gl * g.B + coff;
     }
     return true;
   }
   if (KIND == kMoveCPack) {
     if (gl < 0) return false;
-    pl.src = a.src + (int64_t)gl * H2;
-    pl.dst = a.dst + (int64_t)gr * H2;
+    pl.src = a.src + (int64_t)gl * H2 + coff;
+    pl.dst = a.dst + (int64_t)gr * H2 + coff;
     return true;
   }
   if (KIND == kMoveCPush) {
     const int gs = __ldg(a.gsend + u);
     if (gl < 0) return false;
-    pl.src = a.src + (int64_t)gl * H2;
-    pl.dst = a.dst + (int64_t)gs * H2;
+    pl.src = a.src + (int64_t)gl * H2 + coff;
+    pl.dst = a.dst + (int64_t)gs * H2 + coff;
     return true;
   }
   // kMoveCScatter
   const int gs = __ldg(a.gsend + u);
   if (gl < 0) return false;
-  pl.src = a.src + (int64_t)gr * H2;
-  pl.dst = a.dst + (int64_t)gs * H2;
+  pl.src = a.src + (int64_t)gr * H2 + coff;
+  pl.dst = a.dst + (int64_t)gs * H2 + coff;
   return true;
 }
 
@@ -350,13 +355,14 @@ bool tma_fits(const Geo& g, const MoveArgs& a, const Ctx& c) {
 }
 
 // Default choice (measured on GB300): the TMA ring streams one-to-one moves at 95-98% of
-// the copy bandwidth once every issuer has >= 20 rows, but its stages are held until the
-// bulk stores have read them, which costs it the ramp on small problems and pack's R-fold
-// stores; there the register mover, whose stores free their registers at issue, is faster.
+// the copy bandwidth once every issuer has >= 40 rows (32K+ pairs), but its stages are held
+// until the bulk stores have read them, which costs it the ramp on smaller problems and
+// pack's R-fold stores; there the register mover, whose stores free their registers at
+// issue, is as fast or faster.
 template <int KIND>
 bool tma_default(const MoveArgs& a, const Ctx& c) {
   if (KIND == kMovePack || KIND == kMovePackPush) return false;
-  return a.units >= 20LL * kIssuers * c.num_sms;
+  return a.units / a.chunks >= 40LL * kIssuers * c.num_sms;
 }
 
 template <int KIND, bool FP8>
@@ -398,7 +404,14 @@ cudaError_t launch_move(MoveKind kind, const Geo& g, const moe_layout_t* lay, co
     a.chunk_bytes = (uint32_t)(g.B / a.chunks);
     a.units = tokens * a.chunks;
   } else {
-    a.units = g.P;
+    // One-to-one moves: halve rows of >= 8 KB when there are fewer than 32 pairs per issuer
+    // slot of the TMA ring, so that each issuer keeps more (smaller) rows in flight. The
+    // fp8 receive split (codes | scales) is never chunked.
+    const int64_t rowb = (kind == kMoveScatter || kind == kMoveUnpack) ? g.B : 2 * (int64_t)g.H;
+    const bool splittable = !(kind == kMoveUnpack && fp8) && rowb >= 8192 && rowb % 32 == 0;
+    if (splittable && g.P < 32LL * 4 * c.num_sms) a.chunks = 2;
+    a.chunk_bytes = (uint32_t)(rowb / a.chunks);
+    a.units = g.P * a.chunks;
   }
   if (a.units == 0) return cudaSuccess;
   static const moe_kernel_id ids[] = {MOE_K_PACK,         MOE_K_SCATTER,         MOE_K_UNPACK,

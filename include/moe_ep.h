@@ -100,8 +100,8 @@ typedef struct {
 
 /* moe_layout_t.flags */
 /* Row movers. By default each launch picks one: TMA bulk copies for the one-to-one moves
- * when every issuer warp has at least 20 rows to stream, 16-byte register loads/stores for
- * pack (one row to R destinations) and for small problems. Rows that are not 16-byte
+ * when every issuer warp has at least 40 rows to stream, 16-byte register loads/stores for
+ * pack (one row to R destinations) and for smaller problems. Rows that are not 16-byte
  * multiples (fp8 with H % 512 != 0) always take the register path. */
 #define MOE_FLAG_LDG_MOVER 0x1u /* force the register mover for every move */
 #define MOE_FLAG_TMA_MOVER 0x4u /* force the TMA mover wherever rows allow it */
