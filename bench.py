@@ -36,7 +36,8 @@ import workloads  # noqa: E402
 
 METRIC = "dispatch+combine tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 KERNELS = ["route_count", "layout_maps", "quant_fp8", "pack", "scatter", "unpack", "expert",
-           "combine_pack", "combine_scatter", "combine_reduce", "route_scan", "pack_push", "combine_push"]
+           "combine_pack", "combine_scatter", "combine_reduce", "route_scan", "pack_push", "combine_push",
+           "combine_partial", "combine_sum"]
 
 
 def parse_args(argv=None):
@@ -298,7 +299,18 @@ def run_ours(args):
 
     vis = [v.strip() for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
     sampler = ClockSampler(vis[local] if local < len(vis) else local)
-    def kernel_region():
+    def step_partial():
+        ep.layout_step(idx)
+        if fp8:
+            ep.quantize(x)
+            ep.dispatch_send(ep.xq)
+        else:
+            ep.dispatch_send(x)
+        ep.dispatch_recv()
+        ep.expert_identity()
+        ep.combine_partial(w)
+
+    def kernel_region(step=step):
         """Timed region: per-kernel CUDA events (the library records one pair around each of
         its launches on this stream) give each kernel's duration for the roofline."""
         barrier(dist, device)
@@ -318,13 +330,14 @@ def run_ours(args):
                 per_kernel.setdefault(name, []).append(evs[2 * j].elapsed_time(evs[2 * j + 1]))
         return per_kernel
 
-    def step_region():
+    def step_region(step=step):
         """Timed region: whole steps only (no events between the kernels, so consecutive
         kernels overlap launch and drain as they do in use); gives the step time."""
         barrier(dist, device)
         torch.cuda.synchronize()
         n0 = lib().moe_launch_count()
-        if fp8:
+        split = fp8 and step is not step_partial
+        if split:
             mids = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
             for i in range(K):
                 flush.zero_()
@@ -343,7 +356,7 @@ def run_ours(args):
             raise RuntimeError(f"device status {code} bits {bits:#x}")
         step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
         expert_ms = None
-        if fp8:
+        if split:
             ex = [m0.elapsed_time(m1) for m0, m1 in mids]
             step_ms = [t - x_ for t, x_ in zip(step_ms, ex)]
             expert_ms = statistics.fmean(ex)
@@ -390,6 +403,29 @@ def run_ours(args):
     push_bytes = sum(ab[k] for k in push_kernels)
     push_ms_all = max_over_ranks(push_ms, dist, device)
 
+    # The same step with the combine's weighted sum started on the expert side: one row per
+    # (token, destination rank) group instead of one per (token, expert) pair.
+    slot_np = lay["slot"].cpu().numpy().reshape(-1, wl.R)
+    own = np.where(slot_np >= 0, inp["idx"].reshape(-1, wl.R) // wl.L, -1)
+    G = int(sum(len(set(r[r >= 0].tolist())) for r in own))
+    ab["combine_partial"] = Pk * 2 * wl.H + G * 2 * wl.H
+    ab["combine_sum"] = G * 2 * wl.H + wl.N * wl.T * 2 * wl.H
+    for _ in range(args.warmup):
+        flush.zero_()
+        step_partial()
+    pk_part = kernel_region(step_partial)
+    part_ms, _, _ = step_region(step_partial)
+    if fp8:   # the identity expert is inside this step; take it out as for the main step
+        part_ms -= expert_ms
+    part_kernels = {}
+    for name, ts in pk_part.items():
+        if name == "expert":
+            continue
+        us = statistics.fmean(ts) * 1e3
+        part_kernels[name] = {"us": round(us, 2), "gbs": round(ab[name] / (us * 1e-6) / 1e9, 1),
+                              "frac": round(ab[name] / (us * 1e-6) / 1e9 / peak, 3)}
+    part_ms_all = max_over_ranks(part_ms, dist, device)
+
     # end to end through the C ABI with host buffers: H2D inputs, the pass, D2H output
     h_x = torch.from_numpy(inp["x"]).view(torch.bfloat16).pin_memory()
     h_idx = torch.from_numpy(inp["idx"]).pin_memory()
@@ -433,6 +469,11 @@ def run_ours(args):
                         "kernels": push_kernels,
                         "note": "same results; pack and combine send write straight into the peers' "
                                 "receive regions, so the two per-peer write kernels are fused away"},
+        "sender_side_combine": {"value": round(tokens / (part_ms_all * 1e-3), 1), "unit": "tokens/s",
+                                "ms_per_step": round(part_ms_all, 4), "groups": G, "pairs": Pk,
+                                "kernels": {k: v for k, v in part_kernels.items() if k.startswith("combine")},
+                                "note": "combine sums each token's experts per destination rank on the "
+                                        "expert side (bf16 partial rows), then over ranks on the source"},
         "e2e": {"value": round(tokens / (e2e_ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "path": "moe_forward_host (C ABI)"},
         "identity_expert": None if expert_ms is None else {

@@ -125,6 +125,21 @@ class MoeEP:
         check(lib().moe_combine_recv(ctypes.byref(self.dims), ctypes.byref(self.layout), self.crecv.data_ptr(),
                                      w.data_ptr(), self.out.data_ptr(), _stream(stream)), "moe_combine_recv")
 
+    def combine_partial(self, w: torch.Tensor, stream=None) -> torch.Tensor:
+        """Combine with expert-side partial sums (one row per token and destination rank):
+        moe_combine_send_partial into self.cpart, then moe_combine_recv_partial into self.out."""
+        if getattr(self, "cpart", None) is None:
+            J = min(self.R, self.N)
+            self.cpart = torch.empty((self.N, self.T, J, self.H), dtype=torch.bfloat16, device=self.out.device)
+        self.w = w
+        check(lib().moe_combine_send_partial(ctypes.byref(self.dims), ctypes.byref(self.layout),
+                                             self.expert_y.data_ptr(), w.data_ptr(), self.cpart.data_ptr(),
+                                             _stream(stream)), "moe_combine_send_partial")
+        check(lib().moe_combine_recv_partial(ctypes.byref(self.dims), ctypes.byref(self.layout),
+                                             self.cpart.data_ptr(), self.out.data_ptr(), _stream(stream)),
+              "moe_combine_recv_partial")
+        return self.out
+
     def buffers(self, x, idx, w) -> MoeBuffers:
         b = MoeBuffers()
         b.x, b.xq, b.idx, b.w = _ptr(x), _ptr(self.xq), _ptr(idx), _ptr(w)

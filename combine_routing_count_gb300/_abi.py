@@ -25,7 +25,8 @@ MOE_FLAG_DIRECT_PUSH = 0x8
 MOE_PROF_MAX = 32
 
 KERNEL_NAMES = ["route_count", "layout_maps", "quant_fp8", "pack", "scatter", "unpack", "expert",
-                "combine_pack", "combine_scatter", "combine_reduce", "route_scan", "pack_push", "combine_push"]
+                "combine_pack", "combine_scatter", "combine_reduce", "route_scan", "pack_push", "combine_push",
+                "combine_partial", "combine_sum"]
 
 LAYOUT_FIELDS = ("cnt", "C", "soff", "roff", "rtot", "ecnt", "eoff", "pos", "rrow", "slot", "slot_src",
                  "recv_src", "gsend", "grecv", "gslot", "status", "scratch")
@@ -87,6 +88,8 @@ def lib():
             "moe_expert_identity": (c_int32, [D, Lp, c_void_p, c_void_p, c_void_p, c_void_p]),
             "moe_combine_send": (c_int32, [D, Lp, c_void_p, c_void_p, c_void_p, c_void_p]),
             "moe_combine_recv": (c_int32, [D, Lp, c_void_p, c_void_p, c_void_p, c_void_p]),
+            "moe_combine_send_partial": (c_int32, [D, Lp, c_void_p, c_void_p, c_void_p, c_void_p]),
+            "moe_combine_recv_partial": (c_int32, [D, Lp, c_void_p, c_void_p, c_void_p]),
             "moe_forward": (c_int32, [D, Lp, B, c_void_p]),
             "moe_forward_host": (c_int32, [D, Lp, B, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
             "moe_status_sync": (c_int32, [Lp, c_void_p, POINTER(c_uint32)]),
@@ -114,5 +117,5 @@ def check(code: int, what: str) -> None:
 EXPORTED = ("moe_check_dims", "moe_recv_capacity_rows", "moe_row_bytes", "moe_capacity",
             "moe_layout_workspace_bytes", "moe_layout_init", "moe_layout", "moe_quantize_fp8_b128",
             "moe_dispatch_send", "moe_dispatch_send_noalloc", "moe_dispatch_recv", "moe_expert_identity", "moe_combine_send",
-            "moe_combine_recv", "moe_forward", "moe_forward_host", "moe_status_sync", "moe_status_string",
+            "moe_combine_recv", "moe_combine_send_partial", "moe_combine_recv_partial", "moe_forward", "moe_forward_host", "moe_status_sync", "moe_status_string",
             "moe_launch_count")

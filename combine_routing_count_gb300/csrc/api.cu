@@ -125,7 +125,8 @@ WsPlan ws_plan(const Geo& g) {
                           P,               // grecv
                           P,               // gslot
                           16,              // status
-                          (size_t)layout_scratch_done_offset(g) + N + 16};  // scratch: chunk table + counters
+                          (size_t)layout_scratch_tgroups_offset(g) + N * g.T + 16};  // scratch: chunk table,
+                                                                                  // counters, token groups
   w.total = 0;
   for (int i = 0; i < 17; ++i) {
     w.n[i] = al256(4 * sizes[i]);
@@ -298,6 +299,33 @@ moe_status moe_combine_recv(const moe_dims* dims, const moe_layout_t* lay, const
   Ctx c;
   if ((st = make_ctx(lay, stream, c)) != MOE_OK) return st;
   return cuda_status(launch_combine_reduce(g, lay, d_crecv, d_w, d_out, c));
+}
+
+moe_status moe_combine_send_partial(const moe_dims* dims, const moe_layout_t* lay, const uint16_t* d_expert_y,
+                                    const float* d_w, uint16_t* d_cpart, void* stream) {
+  Geo g;
+  moe_status st = make_geo(dims, g);
+  if (st != MOE_OK) return st;
+  if ((int64_t)g.N * g.T == 0) return layout_ok(lay) ? MOE_OK : MOE_ERR_INVALID_ARG;  // nothing to move
+  if (!layout_ok(lay) || !d_expert_y || !d_w || !d_cpart || !aligned16(d_expert_y) || !aligned16(d_cpart) ||
+      g.R > 32)
+    return MOE_ERR_INVALID_ARG;
+  Ctx c;
+  if ((st = make_ctx(lay, stream, c)) != MOE_OK) return st;
+  return cuda_status(launch_combine_partial(g, lay, d_expert_y, d_w, d_cpart, c));
+}
+
+moe_status moe_combine_recv_partial(const moe_dims* dims, const moe_layout_t* lay, const uint16_t* d_cpart,
+                                    uint16_t* d_out, void* stream) {
+  Geo g;
+  moe_status st = make_geo(dims, g);
+  if (st != MOE_OK) return st;
+  if ((int64_t)g.N * g.T == 0) return layout_ok(lay) ? MOE_OK : MOE_ERR_INVALID_ARG;  // nothing to move
+  if (!layout_ok(lay) || !d_cpart || !d_out || !aligned16(d_cpart) || !aligned16(d_out) || g.R > 32)
+    return MOE_ERR_INVALID_ARG;
+  Ctx c;
+  if ((st = make_ctx(lay, stream, c)) != MOE_OK) return st;
+  return cuda_status(launch_combine_sum(g, lay, d_cpart, d_out, c));
 }
 
 moe_status moe_forward(const moe_dims* dims, const moe_layout_t* lay, const moe_buffers_t* b, void* stream) {

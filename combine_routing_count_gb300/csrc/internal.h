@@ -79,6 +79,7 @@ inline cudaError_t ensure_dyn_smem(K kernel, int device, size_t bytes, std::atom
 cudaError_t launch_layout(const Geo& g, const int32_t* idx, const moe_layout_t* lay, Ctx& c);
 int layout_chunks(const Geo& g);
 int64_t layout_scratch_done_offset(const Geo& g);  // ints from the scratch start to the counters
+int64_t layout_scratch_tgroups_offset(const Geo& g);  // ... to the per-token group counts
 
 // movers.cu: row movement kernels.
 enum MoveKind : int {
@@ -98,6 +99,10 @@ cudaError_t launch_move(MoveKind kind, const Geo& g, const moe_layout_t* lay, co
 cudaError_t launch_quant_fp8(const Geo& g, const uint16_t* x, uint8_t* xq, Ctx& c);
 cudaError_t launch_dequant_fp8(const Geo& g, const moe_layout_t* lay, const uint8_t* exq, const float* exs,
                                uint16_t* ey, Ctx& c);
+cudaError_t launch_combine_partial(const Geo& g, const moe_layout_t* lay, const uint16_t* ey, const float* w,
+                                   uint16_t* cpart, Ctx& c);
+cudaError_t launch_combine_sum(const Geo& g, const moe_layout_t* lay, const uint16_t* cpart, uint16_t* out,
+                               Ctx& c);
 cudaError_t launch_combine_reduce(const Geo& g, const moe_layout_t* lay, const uint16_t* crecv, const float* w,
                                   uint16_t* out, Ctx& c);
 

@@ -313,6 +313,8 @@ int layout_chunks(const Geo& g) { return (int)((g.TR + kChunk - 1) / kChunk); }
 
 int64_t layout_scratch_done_offset(const Geo& g) { return (int64_t)g.N * layout_chunks(g) * g.E; }
 
+int64_t layout_scratch_tgroups_offset(const Geo& g) { return layout_scratch_done_offset(g) + g.N; }
+
 
 cudaError_t launch_layout(const Geo& g, const int32_t* idx, const moe_layout_t* lay, Ctx& c) {
   LayoutArgs a;

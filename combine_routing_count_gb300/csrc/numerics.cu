@@ -209,7 +209,201 @@ __global__ void __launch_bounds__(kReduceThreads) k_combine_reduce(Geo g, const 
   pdl_trigger();
 }
 
+// ---- combine with expert-side partial sums --------------------------------------------
+// A token's kept pairs are grouped by destination rank d = grecv / RB; groups are numbered
+// in ascending d. Lane k of a warp describes pair k (k < R <= 32).
+struct PairGroups {
+  int row;      // global grouped row (gslot) of this lane's pair, or -1
+  float w;      // its weight
+  int j;        // its group number
+  int ngroups;  // groups of the token (same in every lane)
+};
+
+__device__ __forceinline__ PairGroups token_groups(const Geo& g, const int32_t* gslot, const int32_t* grecv,
+                                                   const float* w, int64_t q0, int lane) {
+  PairGroups pg;
+  int d = 0x7fffffff;
+  pg.row = -1;
+  pg.w = 0.0f;
+  if (lane < g.R) {
+    const int gl = __ldg(gslot + q0 + lane);
+    if (gl >= 0) {
+      pg.row = gl;
+      pg.w = w ? __ldg(w + q0 + lane) : 0.0f;
+      d = (int)(__ldg(grecv + q0 + lane) / g.RB);
+    }
+  }
+  const bool kept = pg.row >= 0;
+  const unsigned peers = __match_any_sync(kFull, d);
+  const bool first = kept && (__ffs(peers) - 1 == lane);
+  const unsigned firsts = __ballot_sync(kFull, first);
+  pg.ngroups = __popc(firsts);
+  int j = 0;
+  for (unsigned f = firsts; f; f &= f - 1) {
+    const int l = __ffs(f) - 1;
+    const int dl = __shfl_sync(kFull, d, l);   // every lane runs the same trip count
+    j += dl < d;
+  }
+  pg.j = j;
+  return pg;
+}
+
+// Expert side: for each token and each group, cpart[s][t][j] = bf16(sum of w*y over the
+// group's pairs, k ascending, fp32 with separate rounding). Block (token, 1024 columns).
+// With R <= 8 all of a token's rows are gathered at once and summed group by group from
+// registers; larger R gathers each group's rows in batches of 8. The token's group count
+// goes to tgroups[token] for the source side.
+__global__ void __launch_bounds__(kReduceThreads) k_combine_partial(Geo g, const int32_t* __restrict__ gslot,
+                                                                    const int32_t* __restrict__ grecv,
+                                                                    const float* __restrict__ w,
+                                                                    const uint16_t* __restrict__ ey,
+                                                                    uint16_t* __restrict__ cpart,
+                                                                    int32_t* __restrict__ tgroups) {
+  const int64_t u = blockIdx.x;
+  const int col = blockIdx.y * kReduceThreads + threadIdx.x;
+  const int ncol = g.H / 8;
+  const bool act = col < ncol;
+  const int lane = threadIdx.x & 31;
+  const int J = g.R < g.N ? g.R : g.N;
+  pdl_wait();
+  const PairGroups pg = token_groups(g, gslot, grecv, w, u * g.R, lane);
+  if (blockIdx.y == 0 && threadIdx.x == 0) tgroups[u] = pg.ngroups;
+  uint16_t* out0 = cpart + (u * J) * g.H + col * 8;
+  const int nb = g.R <= 8 ? 1 : pg.ngroups;   // gather rounds: one, or one per group
+  for (int round = 0; round < nb; ++round) {
+    const int jsel = g.R <= 8 ? -1 : round;   // -1: gather every kept row
+    float acc[8];
+    int jcur = g.R <= 8 ? 0 : round;
+    for (int k0 = 0; k0 < g.R; k0 += 8) {
+      int rk[8], jk[8];
+      float wk[8];
+      uint4 v[8];
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const int k = (k0 + m) & 31;
+        const int row = __shfl_sync(kFull, pg.row, k);
+        jk[m] = __shfl_sync(kFull, pg.j, k);
+        wk[m] = __shfl_sync(kFull, pg.w, k);
+        rk[m] = (k0 + m < g.R && row >= 0 && (jsel < 0 || jk[m] == jsel)) ? row : -1;
+      }
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        v[m] = make_uint4(0, 0, 0, 0);
+        if (act && rk[m] >= 0) v[m] = ld_stream16(ey + (int64_t)rk[m] * g.H + col * 8);
+      }
+      // Sum group by group (all groups when every row is in registers, else this round's).
+      const int jlo = jsel < 0 ? 0 : jsel, jhi = jsel < 0 ? pg.ngroups : jsel + 1;
+      for (int j = jlo; j < jhi; ++j) {
+        if (jsel < 0 || k0 == 0) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+        }
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          if (rk[m] < 0 || jk[m] != j) continue;
+          const float f[8] = {bf16_lo(v[m].x), bf16_hi(v[m].x), bf16_lo(v[m].y), bf16_hi(v[m].y),
+                              bf16_lo(v[m].z), bf16_hi(v[m].z), bf16_lo(v[m].w), bf16_hi(v[m].w)};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(wk[m], f[i]));
+        }
+        if (jsel < 0 && act) {   // every row of group j is in: store it
+          uint4 o;
+          o.x = pack_bf16x2(acc[0], acc[1]);
+          o.y = pack_bf16x2(acc[2], acc[3]);
+          o.z = pack_bf16x2(acc[4], acc[5]);
+          o.w = pack_bf16x2(acc[6], acc[7]);
+          st16(out0 + (int64_t)j * g.H, o);
+        }
+      }
+    }
+    if (jsel >= 0 && act) {
+      uint4 o;
+      o.x = pack_bf16x2(acc[0], acc[1]);
+      o.y = pack_bf16x2(acc[2], acc[3]);
+      o.z = pack_bf16x2(acc[4], acc[5]);
+      o.w = pack_bf16x2(acc[6], acc[7]);
+      st16(out0 + (int64_t)jcur * g.H, o);
+    }
+  }
+  pdl_trigger();
+}
+
+// Source side: out[s][t] = bf16(sum over the token's groups j ascending of cpart[s][t][j]).
+// Block (token, 2048 columns): each thread sums two 16-byte column vectors.
+__global__ void __launch_bounds__(kReduceThreads) k_combine_sum(Geo g, const int32_t* __restrict__ tgroups,
+                                                                const uint16_t* __restrict__ cpart,
+                                                                uint16_t* __restrict__ out) {
+  const int64_t u = blockIdx.x;
+  const int ncol = g.H / 8;
+  const int J = g.R < g.N ? g.R : g.N;
+  pdl_wait();
+  const int ng = __ldg(tgroups + u);
+  const uint16_t* in0 = cpart + (u * J) * g.H;
+  int cols[2];
+  float acc[2][8];
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    cols[c] = blockIdx.y * 2 * kReduceThreads + c * kReduceThreads + threadIdx.x;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[c][i] = 0.0f;
+  }
+  for (int j0 = 0; j0 < ng; j0 += 4) {
+    uint4 v[4][2];
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        v[m][c] = make_uint4(0, 0, 0, 0);
+        if (j0 + m < ng && cols[c] < ncol) v[m][c] = ld_stream16(in0 + (int64_t)(j0 + m) * g.H + cols[c] * 8);
+      }
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      if (j0 + m >= ng) continue;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const float f[8] = {bf16_lo(v[m][c].x), bf16_hi(v[m][c].x), bf16_lo(v[m][c].y), bf16_hi(v[m][c].y),
+                            bf16_lo(v[m][c].z), bf16_hi(v[m][c].z), bf16_lo(v[m][c].w), bf16_hi(v[m][c].w)};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[c][i] = __fadd_rn(acc[c][i], f[i]);
+      }
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    if (cols[c] >= ncol) continue;
+    uint4 o;
+    o.x = pack_bf16x2(acc[c][0], acc[c][1]);
+    o.y = pack_bf16x2(acc[c][2], acc[c][3]);
+    o.z = pack_bf16x2(acc[c][4], acc[c][5]);
+    o.w = pack_bf16x2(acc[c][6], acc[c][7]);
+    st16(out + u * g.H + cols[c] * 8, o);
+  }
+  pdl_trigger();
+}
+
 }  // namespace
+
+cudaError_t launch_combine_partial(const Geo& g, const moe_layout_t* lay, const uint16_t* ey, const float* w,
+                                   uint16_t* cpart, Ctx& c) {
+  const int64_t tokens = (int64_t)g.N * g.T;
+  if (tokens == 0) return cudaSuccess;
+  const int ncol = g.H / 8;
+  dim3 grid((unsigned)tokens, (unsigned)((ncol + kReduceThreads - 1) / kReduceThreads));
+  LaunchScope ls(c, MOE_K_COMBINE_PARTIAL);
+  return launch_kernel(k_combine_partial, grid, dim3(kReduceThreads), 0, c, g, (const int32_t*)lay->gslot,
+                       (const int32_t*)lay->grecv, w, ey, cpart, lay->scratch + layout_scratch_tgroups_offset(g));
+}
+
+cudaError_t launch_combine_sum(const Geo& g, const moe_layout_t* lay, const uint16_t* cpart, uint16_t* out,
+                               Ctx& c) {
+  const int64_t tokens = (int64_t)g.N * g.T;
+  if (tokens == 0) return cudaSuccess;
+  const int ncol = g.H / 8;
+  dim3 grid((unsigned)tokens, (unsigned)((ncol + 2 * kReduceThreads - 1) / (2 * kReduceThreads)));
+  LaunchScope ls(c, MOE_K_COMBINE_SUM);
+  return launch_kernel(k_combine_sum, grid, dim3(kReduceThreads), 0, c, g,
+                       (const int32_t*)(lay->scratch + layout_scratch_tgroups_offset(g)), cpart, out);
+}
 
 cudaError_t launch_quant_fp8(const Geo& g, const uint16_t* x, uint8_t* xq, Ctx& c) {
   const int64_t nblk = (int64_t)g.N * g.T * (g.H / 128);

@@ -83,7 +83,9 @@ typedef enum {
     MOE_K_ROUTE_SCAN = 10,     /* per-rank totals and every exclusive scan */
     MOE_K_PACK_PUSH = 11,      /* direct push: token rows -> owners' receive rows */
     MOE_K_COMBINE_PUSH = 12,   /* direct push: grouped rows -> sources' combine rows */
-    MOE_K_NUM = 13
+    MOE_K_COMBINE_PARTIAL = 13, /* expert-side partial sums, one row per (token, rank) */
+    MOE_K_COMBINE_SUM = 14,    /* source-side sum of the partial rows -> bf16 */
+    MOE_K_NUM = 15
 } moe_kernel_id;
 
 /* Optional per-kernel timing. When moe_layout_t.prof is non-NULL, every kernel the library
@@ -141,7 +143,8 @@ typedef struct {
  *   gslot [N*T*R]  global grouped row, e*cap + slot (row of d_expert_x), or -1 when the
  *                  pair's expert id is bad or the pair was dropped for capacity
  *   status   [1]         sticky error bits, bit (1 << moe_status)
- *   scratch  [N][ceil(T*R/256)][E]  internal: per-chunk counts, then chunk offsets
+ *   scratch  internal: per-chunk counts [N][ceil(T*R/256)][E], per-rank counters [N] and
+ *            per-token group counts of the partial combine [N][T]
  * Host-side fields (set by the caller after moe_layout_init, read at each call):
  *   flags, prof, tma_stages (0 = automatic, else 1..32 stages per TMA mover CTA),
  *   ctas_per_sm (0 = automatic, else mover CTAs per SM).
@@ -280,6 +283,24 @@ moe_status moe_combine_send(const moe_dims *dims, const moe_layout_t *lay, const
  * d_crecv [N][T*R][H] bf16, d_w [N][T][R] fp32, d_out [N][T][H] bf16. One kernel. */
 moe_status moe_combine_recv(const moe_dims *dims, const moe_layout_t *lay, const uint16_t *d_crecv,
                             const float *d_w, uint16_t *d_out, void *stream);
+
+/* Combine with the weighted sum started on the expert side (section "Evaluation": DeepEP
+ * accumulates on the sender side to send less data, at some accuracy cost; this library's
+ * default combine accumulates on the receiving side only, as the page's kernels do).
+ * For token (s,t) the pairs kept in the grouped buffers are grouped by destination rank
+ * d = owner(e), groups numbered j = 0, 1, ... in ascending d; J = min(R, N).
+ *  moe_combine_send_partial: each expert rank writes, straight into the source's buffer,
+ *    d_cpart[s][t][j] = bf16(sum over the group's pairs, k ascending, of w * y), fp32 with
+ *    products and sums rounded separately. d_expert_y [N][L][cap][H] bf16, d_w [N][T][R]
+ *    fp32, d_cpart [N][T][J][H] bf16; rows j >= the token's group count are not written.
+ *  moe_combine_recv_partial: d_out[s][t] = bf16(sum over j ascending of d_cpart[s][t][j]),
+ *    fp32, with the group counts the send half left in the layout's scratch: call it after
+ *    moe_combine_send_partial on the same layout. Every token moves one row per group
+ *    instead of one per expert. */
+moe_status moe_combine_send_partial(const moe_dims *dims, const moe_layout_t *lay, const uint16_t *d_expert_y,
+                                    const float *d_w, uint16_t *d_cpart, void *stream);
+moe_status moe_combine_recv_partial(const moe_dims *dims, const moe_layout_t *lay, const uint16_t *d_cpart,
+                                    uint16_t *d_out, void *stream);
 
 /* One whole pass on device-resident buffers: moe_layout, [moe_quantize_fp8_b128],
  * moe_dispatch_send, moe_dispatch_recv, moe_expert_identity, moe_combine_send,

@@ -72,6 +72,10 @@ def lib():
         L.orc_combine_send.restype = None
         L.orc_combine_recv.argtypes = [c_int] * 4 + [_P(c_uint16), _P(c_float), i32p, i32p, _P(c_uint16), _P(c_double)]
         L.orc_combine_recv.restype = None
+        L.orc_combine_partial_send.argtypes = [c_int] * 6 + [_P(c_uint16), _P(c_float), i32p, i32p, _P(c_uint16)]
+        L.orc_combine_partial_send.restype = None
+        L.orc_combine_partial_recv.argtypes = [c_int] * 4 + [i32p, i32p, c_int, _P(c_uint16), _P(c_uint16)]
+        L.orc_combine_partial_recv.restype = None
         _lib = L
     return _lib
 
@@ -292,3 +296,19 @@ def run_step(b: dict, x: np.ndarray, idx: np.ndarray, w: np.ndarray) -> int:
     L_.orc_combine_recv(N, T, R, H, _ptr(b["crecv"], c_uint16), _ptr(np.ascontiguousarray(w, np.float32), c_float),
                         _i32(b["pos"]), _i32(b["slot"]), _ptr(b["out"], c_uint16), _ptr(b["out64"], c_double))
     return int(st)
+
+
+def combine_partial(N, T, E, R, cap, H, ey: np.ndarray, w: np.ndarray, idx: np.ndarray, lay: dict, fill: int = 0):
+    """Expert-side partial sums then source-side sum -> (cpart uint16 [N,T,J,H], out uint16 [N,T,H])."""
+    cap = cap if cap > 0 else N * T
+    J = min(R, N)
+    ey = np.ascontiguousarray(ey, dtype=np.uint16)
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    cpart = np.full((N, T, J, H), fill, np.uint16)
+    out = np.zeros((N, T, H), np.uint16)
+    lib().orc_combine_partial_send(N, T, E, R, cap, H, _ptr(ey, c_uint16), _ptr(w, c_float), _i32(idx),
+                                   _i32(lay["slot"]), _ptr(cpart, c_uint16))
+    lib().orc_combine_partial_recv(N, T, E, R, _i32(idx), _i32(lay["slot"]), H, _ptr(cpart, c_uint16),
+                                   _ptr(out, c_uint16))
+    return cpart, out

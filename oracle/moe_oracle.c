@@ -426,3 +426,73 @@ void orc_combine_recv(int N, int T, int R, int H, const uint16_t *crecv, const f
                 if (out64) out64[((int64_t)s * T + t) * H + h] = acc64;
             }
 }
+
+/* ---------------------------------------------------------------- combine with partial sums */
+
+/*
+ * Combine with the weighted sum started on the expert side (section "Evaluation": DeepEP
+ * accumulates on the sender side to send less data, possibly at some accuracy cost).
+ * Reading: for token (s,t) the kept pairs (slot >= 0) are grouped by destination rank
+ * d = e / L; the groups are numbered j = 0, 1, ... in ascending d. Group j's partial
+ *   cpart[s][t][j] = bf16( sum_{k in group, k ascending} w[s][t][k] * y_k ),
+ *   y_k = ey[d][e % L][slot[s][t][k]],
+ * fp32 with multiply and add rounded separately; rows j >= number of groups are untouched.
+ * cpart [N][T][J][H] with J = min(R, N).
+ */
+void orc_combine_partial_send(int N, int T, int E, int R, int cap, int H, const uint16_t *ey,
+                              const float *w, const int32_t *idx, const int32_t *slot,
+                              uint16_t *cpart) {
+    const int L = E / N;
+    const int J = R < N ? R : N;
+    float *acc = (float *)malloc(sizeof(float) * (size_t)H);
+    for (int s = 0; s < N; s++)
+        for (int t = 0; t < T; t++) {
+            int64_t q0 = ((int64_t)s * T + t) * R;
+            int j = 0;
+            for (int d = 0; d < N; d++) {
+                int any = 0;
+                for (int h = 0; h < H; h++) acc[h] = 0.0f;
+                for (int k = 0; k < R; k++) {
+                    int e = idx[q0 + k];
+                    if (e < 0 || e >= E || slot[q0 + k] < 0 || e / L != d) continue;
+                    any = 1;
+                    const uint16_t *y = ey + (((int64_t)d * L + e % L) * cap + slot[q0 + k]) * H;
+                    for (int h = 0; h < H; h++) {
+                        float prod = w[q0 + k] * orc_bf16_to_f32(y[h]);
+                        acc[h] = acc[h] + prod;
+                    }
+                }
+                if (!any) continue;
+                uint16_t *row = cpart + (((int64_t)s * T + t) * J + j) * H;
+                for (int h = 0; h < H; h++) row[h] = orc_f32_to_bf16(acc[h]);
+                j++;
+            }
+        }
+    free(acc);
+}
+
+/* out[s][t] = bf16( sum_{j < groups(s,t), j ascending} float(cpart[s][t][j]) ), fp32. */
+void orc_combine_partial_recv(int N, int T, int E, int R, const int32_t *idx, const int32_t *slot,
+                              int H, const uint16_t *cpart, uint16_t *out) {
+    const int L = E / N;
+    const int J = R < N ? R : N;
+    for (int s = 0; s < N; s++)
+        for (int t = 0; t < T; t++) {
+            int64_t q0 = ((int64_t)s * T + t) * R;
+            int groups = 0;
+            for (int d = 0; d < N; d++) {
+                int any = 0;
+                for (int k = 0; k < R; k++) {
+                    int e = idx[q0 + k];
+                    if (e >= 0 && e < E && slot[q0 + k] >= 0 && e / L == d) any = 1;
+                }
+                groups += any;
+            }
+            for (int h = 0; h < H; h++) {
+                float acc = 0.0f;
+                for (int j = 0; j < groups; j++)
+                    acc = acc + orc_bf16_to_f32(cpart[(((int64_t)s * T + t) * J + j) * H + h]);
+                out[((int64_t)s * T + t) * H + h] = orc_f32_to_bf16(acc);
+            }
+        }
+}

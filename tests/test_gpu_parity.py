@@ -20,6 +20,7 @@ CASES = [
     W("R1-bf16", 5, 13, 1024, 10, 1, "bf16", "uniform", 106),
     W("R3-E-small", 2, 40, 136, 4, 3, "bf16", "uniform", 107),              # H not a multiple of 16
     W("cap-overflow", 4, 16, 512, 8, 2, "bf16", "uniform", 108, cap=5),
+    W("R12-gather-batches", 4, 9, 512, 32, 12, "bf16", "uniform", 109),  # R > 8: gathers in batches
 ]
 
 
@@ -177,3 +178,20 @@ def test_profiling_events_bracket_each_kernel():
                      "expert", "combine_pack", "combine_scatter", "combine_reduce"]
     for i in range(prof.n):
         assert evs[2 * i].elapsed_time(evs[2 * i + 1]) >= 0.0
+
+
+@pytest.mark.parametrize("wl", CASES + [workloads.config(4).replace(T=24, H=1024, seed=140)], ids=lambda w: w.name)
+def test_partial_combine_matches_oracle(orc, wl):
+    """Expert-side partial sums (one row per token and destination rank) and the source-side
+    sum, bit for bit against the oracle."""
+    inp = workloads.make_inputs(wl)
+    ep, res = run_gpu(wl, inp)
+    ep.cpart = torch.full((wl.N, wl.T, min(wl.R, wl.N), wl.H), -1.0, dtype=torch.bfloat16, device="cuda")
+    poison = u16(ep.cpart[:1, :1, :1].cpu())[0, 0, 0, 0]
+    ep.combine_partial(to_dev(inp["w"]))
+    code, _ = ep.status()
+    o = orc.forward(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, wl.payload, inp["x"], inp["idx"], inp["w"])
+    cpart_o, out_o = orc.combine_partial(wl.N, wl.T, wl.E, wl.R, wl.cap, wl.H, o["ey"], inp["w"], inp["idx"],
+                                         o["layout"], fill=poison)
+    np.testing.assert_array_equal(u16(ep.cpart.cpu()), cpart_o)
+    np.testing.assert_array_equal(u16(ep.out.cpu()), out_o)

@@ -297,3 +297,55 @@ def test_run_step_equals_forward(orc, wl):
     assert st == r["layout"]["status"]
     np.testing.assert_array_equal(b["out"], r["out"])
     np.testing.assert_array_equal(b["out64"], r["out64"])
+
+
+# ---------------------------------------------------------------- combine with expert-side partial sums
+
+
+def _partial(orc, wl, inp, r):
+    L = wl.L
+    lay = r["layout"]
+    return orc.combine_partial(wl.N, wl.T, wl.E, wl.R, wl.cap, wl.H, r["ey"], inp["w"], inp["idx"], lay,
+                               fill=0x7FFF)
+
+
+@pytest.mark.parametrize("wl", [SMALL[3], workloads.config(4).replace(T=24, H=256, seed=44),
+                                workloads.Workload("r1", 4, 9, 256, 12, 1, "bf16", "uniform", 45)],
+                         ids=["skew-small", "skew-cfg4-shape", "R1"])
+def test_partial_combine_equals_canonical_with_one_group_per_token(orc, wl):
+    """When all of a token's experts sit on one rank there is one partial per token: it is
+    the canonical fp32 sum rounded once, so both combines agree bit for bit."""
+    inp, r = _fwd(orc, wl)
+    cpart, out = _partial(orc, wl, inp, r)
+    np.testing.assert_array_equal(out, r["out"])
+    np.testing.assert_array_equal(cpart[:, :, 0], r["out"])
+    if cpart.shape[2] > 1:
+        assert (cpart[:, :, 1:] == 0x7FFF).all()          # rows past the groups are untouched
+
+
+@pytest.mark.parametrize("wl", SMALL[:3] + [workloads.config(1).replace(T=6, H=256, seed=46)], ids=lambda w: w.name)
+def test_partial_combine_within_tolerance_and_restated(orc, wl):
+    inp, r = _fwd(orc, wl)
+    cpart, out = _partial(orc, wl, inp, r)
+    x = from_bf16_bits(inp["x"]).astype(np.float64)
+    # one bf16 rounding per group plus one of the sum: within 2^-7 max|x| of the exact sum
+    assert np.abs(from_bf16_bits(out) - r["out64"]).max() <= 2.0 ** -7 * np.abs(x).max()
+    # independent restatement: group pairs by owner rank with numpy, fp32 scalar arithmetic
+    lay = r["layout"]
+    ey = from_bf16_bits(r["ey"])
+    N, T, R, L = wl.N, wl.T, wl.R, wl.L
+    for s in range(N):
+        for t in range(T):
+            ks = [k for k in range(R) if lay["slot"][s, t, k] >= 0]
+            owners = sorted({int(inp["idx"][s, t, k]) // L for k in ks})
+            total = np.zeros(wl.H, np.float32)
+            for j, d in enumerate(owners):
+                acc = np.zeros(wl.H, np.float32)
+                for k in ks:
+                    e = int(inp["idx"][s, t, k])
+                    if e // L == d:
+                        acc = (acc + np.float32(inp["w"][s, t, k]) * ey[d, e % L, lay["slot"][s, t, k]]).astype(np.float32)
+                p = to_bf16_bits(acc)
+                np.testing.assert_array_equal(cpart[s, t, j], p)
+                total = (total + from_bf16_bits(p)).astype(np.float32)
+            np.testing.assert_array_equal(out[s, t], to_bf16_bits(total))
