@@ -230,7 +230,7 @@ __device__ __forceinline__ PairGroups token_groups(const Geo& g, const int32_t* 
     if (gl >= 0) {
       pg.row = gl;
       pg.w = w ? __ldg(w + q0 + lane) : 0.0f;
-      d = (int)(__ldg(grecv + q0 + lane) / g.RB);
+      d = __ldg(grecv + q0 + lane) / (int)g.RB;   // grecv = d*RB + row, all below 2^31
     }
   }
   const bool kept = pg.row >= 0;
@@ -248,11 +248,32 @@ __device__ __forceinline__ PairGroups token_groups(const Geo& g, const int32_t* 
   return pg;
 }
 
+// Sums the 16-byte column vector `v` of a pair into acc with weight wm (fp32, separate
+// rounding of product and sum).
+__device__ __forceinline__ void acc_pair(float (&acc)[8], const uint4& v, float wm) {
+  const float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                      bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(wm, f[i]));
+}
+
+__device__ __forceinline__ void store_bf16x8(uint16_t* p, const float (&acc)[8]) {
+  uint4 o;
+  o.x = pack_bf16x2(acc[0], acc[1]);
+  o.y = pack_bf16x2(acc[2], acc[3]);
+  o.z = pack_bf16x2(acc[4], acc[5]);
+  o.w = pack_bf16x2(acc[6], acc[7]);
+  st16(p, o);
+}
+
 // Expert side: for each token and each group, cpart[s][t][j] = bf16(sum of w*y over the
 // group's pairs, k ascending, fp32 with separate rounding). Block (token, 1024 columns).
-// With R <= 8 all of a token's rows are gathered at once and summed group by group from
-// registers; larger R gathers each group's rows in batches of 8. The token's group count
-// goes to tgroups[token] for the source side.
+// kSmall (R <= 8): a token's rows are gathered once into registers and summed group by
+// group; a pair's row, weight and group are re-read by shuffle instead of being kept in
+// arrays, which keeps the register count (and so the occupancy) close to the plain reduce.
+// Otherwise each group's rows are gathered in batches of 8. The token's group count goes
+// to tgroups[token] for the source side.
+template <bool kSmall>
 __global__ void __launch_bounds__(kReduceThreads) k_combine_partial(Geo g, const int32_t* __restrict__ gslot,
                                                                     const int32_t* __restrict__ grecv,
                                                                     const float* __restrict__ w,
@@ -269,60 +290,80 @@ __global__ void __launch_bounds__(kReduceThreads) k_combine_partial(Geo g, const
   const PairGroups pg = token_groups(g, gslot, grecv, w, u * g.R, lane);
   if (blockIdx.y == 0 && threadIdx.x == 0) tgroups[u] = pg.ngroups;
   uint16_t* out0 = cpart + (u * J) * g.H + col * 8;
-  const int nb = g.R <= 8 ? 1 : pg.ngroups;   // gather rounds: one, or one per group
-  for (int round = 0; round < nb; ++round) {
-    const int jsel = g.R <= 8 ? -1 : round;   // -1: gather every kept row
+  const uint16_t* y0 = ey + col * 8;
+  if (kSmall) {
+    // Warp 0 lays the kept pairs out in group order (k ascending inside a group) in shared
+    // memory; every thread then makes one pass over them, storing at each group's end.
+    __shared__ int s_row[8], s_last[8], s_n;
+    __shared__ float s_w[8];
+    if (threadIdx.x < 32) {
+      const int d = pg.row >= 0 ? pg.j : 0x7fffffff;   // group number orders like the rank
+      const unsigned peers = __match_any_sync(kFull, d);
+      const unsigned firsts = __ballot_sync(kFull, pg.row >= 0 && (__ffs(peers) - 1 == lane));
+      int before = 0;   // kept pairs in groups before this lane's group
+      for (unsigned f = firsts; f; f &= f - 1) {
+        const int l = __ffs(f) - 1;
+        const int jl = __shfl_sync(kFull, pg.j, l);
+        const unsigned pl = __shfl_sync(kFull, peers, l);
+        before += (jl < pg.j) ? __popc(pl) : 0;
+      }
+      if (pg.row >= 0) {
+        const int p = before + __popc(peers & ((1u << lane) - 1u));
+        s_row[p] = pg.row;
+        s_w[p] = pg.w;
+        s_last[p] = (32 - __clz(peers)) - 1 == lane;   // highest lane of the group
+      }
+      const unsigned kept = __ballot_sync(kFull, pg.row >= 0);
+      if (lane == 0) s_n = __popc(kept);
+    }
+    __syncthreads();
+    const int n = s_n;
+    uint4 v[8];
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+      v[p] = make_uint4(0, 0, 0, 0);
+      if (act && p < n) v[p] = ld_stream16(y0 + (int64_t)s_row[p] * g.H);
+    }
     float acc[8];
-    int jcur = g.R <= 8 ? 0 : round;
-    for (int k0 = 0; k0 < g.R; k0 += 8) {
-      int rk[8], jk[8];
-      float wk[8];
-      uint4 v[8];
 #pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const int k = (k0 + m) & 31;
-        const int row = __shfl_sync(kFull, pg.row, k);
-        jk[m] = __shfl_sync(kFull, pg.j, k);
-        wk[m] = __shfl_sync(kFull, pg.w, k);
-        rk[m] = (k0 + m < g.R && row >= 0 && (jsel < 0 || jk[m] == jsel)) ? row : -1;
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    int j = 0;
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+      if (p >= n) break;
+      acc_pair(acc, v[p], s_w[p]);
+      if (s_last[p]) {
+        if (act) store_bf16x8(out0 + (int64_t)j * g.H, acc);
+        ++j;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
       }
+    }
+  } else {
+    for (int j = 0; j < pg.ngroups; ++j) {
+      float acc[8];
 #pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        v[m] = make_uint4(0, 0, 0, 0);
-        if (act && rk[m] >= 0) v[m] = ld_stream16(ey + (int64_t)rk[m] * g.H + col * 8);
-      }
-      // Sum group by group (all groups when every row is in registers, else this round's).
-      const int jlo = jsel < 0 ? 0 : jsel, jhi = jsel < 0 ? pg.ngroups : jsel + 1;
-      for (int j = jlo; j < jhi; ++j) {
-        if (jsel < 0 || k0 == 0) {
+      for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+      for (int k0 = 0; k0 < g.R; k0 += 8) {
+        uint4 v[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+        for (int m = 0; m < 8; ++m) {
+          const int k = (k0 + m) & 31;
+          const int row = __shfl_sync(kFull, pg.row, k);
+          const int jm = __shfl_sync(kFull, pg.j, k);
+          v[m] = make_uint4(0, 0, 0, 0);
+          if (act && k0 + m < g.R && row >= 0 && jm == j) v[m] = ld_stream16(y0 + (int64_t)row * g.H);
         }
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
-          if (rk[m] < 0 || jk[m] != j) continue;
-          const float f[8] = {bf16_lo(v[m].x), bf16_hi(v[m].x), bf16_lo(v[m].y), bf16_hi(v[m].y),
-                              bf16_lo(v[m].z), bf16_hi(v[m].z), bf16_lo(v[m].w), bf16_hi(v[m].w)};
-#pragma unroll
-          for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(wk[m], f[i]));
-        }
-        if (jsel < 0 && act) {   // every row of group j is in: store it
-          uint4 o;
-          o.x = pack_bf16x2(acc[0], acc[1]);
-          o.y = pack_bf16x2(acc[2], acc[3]);
-          o.z = pack_bf16x2(acc[4], acc[5]);
-          o.w = pack_bf16x2(acc[6], acc[7]);
-          st16(out0 + (int64_t)j * g.H, o);
+          const int k = (k0 + m) & 31;
+          const int row = __shfl_sync(kFull, pg.row, k);
+          const int jm = __shfl_sync(kFull, pg.j, k);
+          const float wm = __shfl_sync(kFull, pg.w, k);
+          if (k0 + m < g.R && row >= 0 && jm == j) acc_pair(acc, v[m], wm);
         }
       }
-    }
-    if (jsel >= 0 && act) {
-      uint4 o;
-      o.x = pack_bf16x2(acc[0], acc[1]);
-      o.y = pack_bf16x2(acc[2], acc[3]);
-      o.z = pack_bf16x2(acc[4], acc[5]);
-      o.w = pack_bf16x2(acc[6], acc[7]);
-      st16(out0 + (int64_t)jcur * g.H, o);
+      if (act) store_bf16x8(out0 + (int64_t)j * g.H, acc);
     }
   }
   pdl_trigger();
@@ -390,8 +431,12 @@ cudaError_t launch_combine_partial(const Geo& g, const moe_layout_t* lay, const 
   const int ncol = g.H / 8;
   dim3 grid((unsigned)tokens, (unsigned)((ncol + kReduceThreads - 1) / kReduceThreads));
   LaunchScope ls(c, MOE_K_COMBINE_PARTIAL);
-  return launch_kernel(k_combine_partial, grid, dim3(kReduceThreads), 0, c, g, (const int32_t*)lay->gslot,
-                       (const int32_t*)lay->grecv, w, ey, cpart, lay->scratch + layout_scratch_tgroups_offset(g));
+  int32_t* tg = lay->scratch + layout_scratch_tgroups_offset(g);
+  if (g.R <= 8)
+    return launch_kernel(k_combine_partial<true>, grid, dim3(kReduceThreads), 0, c, g, (const int32_t*)lay->gslot,
+                         (const int32_t*)lay->grecv, w, ey, cpart, tg);
+  return launch_kernel(k_combine_partial<false>, grid, dim3(kReduceThreads), 0, c, g, (const int32_t*)lay->gslot,
+                       (const int32_t*)lay->grecv, w, ey, cpart, tg);
 }
 
 cudaError_t launch_combine_sum(const Geo& g, const moe_layout_t* lay, const uint16_t* cpart, uint16_t* out,
