@@ -266,6 +266,39 @@ __global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
   const int64_t nel = unit_bytes<KIND>(g, a) / W;
   const int64_t split = (KIND == kMoveUnpack && FP8) ? g.H / W : nel;
   pdl_wait();
+  if (KIND == kMovePack || KIND == kMovePackPush) {
+    // Pack: lane k holds the destination row of the token's pair k and broadcasts it by
+    // shuffle, so a warp keeps only its U loaded vectors live while it writes R copies.
+    for (int64_t u = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < a.units; u += nwarps) {
+      const int64_t tok = u / a.chunks;
+      const int64_t coff = (u - tok * a.chunks) * (int64_t)a.chunk_bytes;
+      const uint8_t* src = a.src + tok * g.B + coff;
+      uint8_t* dst0 = a.dst + coff;
+      const int32_t* fan = a.fan + tok * g.R;
+      const int myp = lane < g.R ? __ldg(fan + lane) : -1;   // pairs 0..31 (R > 32: see below)
+      for (int64_t v0 = lane; v0 < nel; v0 += 32 * U) {
+        V r[U];
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+          const int64_t v = v0 + 32 * j;
+          if (v < nel) r[j] = ld_vec<V>(src + v * W);
+        }
+#pragma unroll 1
+        for (int k = 0; k < g.R; ++k) {
+          const int p = k < 32 ? __shfl_sync(0xffffffffu, myp, k) : __ldg(fan + k);
+          if (p < 0) continue;
+          uint8_t* d = dst0 + (int64_t)p * g.B;
+#pragma unroll
+          for (int j = 0; j < U; ++j) {
+            const int64_t v = v0 + 32 * j;
+            if (v < nel) st_vec(d + v * W, r[j]);
+          }
+        }
+      }
+    }
+    pdl_trigger();
+    return;
+  }
   for (int64_t u = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < a.units; u += nwarps) {
     Plan pl;
     if (!make_plan<KIND, FP8>(g, a, u, pl)) continue;
@@ -280,15 +313,7 @@ __global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
       for (int j = 0; j < U; ++j) {
         const int64_t v = v0 + 32 * j;
         if (v >= nel) continue;
-        if (KIND == kMovePack || KIND == kMovePackPush) {
-#pragma unroll
-          for (int k = 0; k < kPackPrefetch; ++k)
-            if (pl.p[k] >= 0) st_vec(a.dst + (int64_t)pl.p[k] * g.B + pl.coff + v * W, r[j]);
-          for (int k = kPackPrefetch; k < g.R; ++k) {
-            const int p = __ldg(a.fan + pl.tok * g.R + k);
-            if (p >= 0) st_vec(a.dst + (int64_t)p * g.B + pl.coff + v * W, r[j]);
-          }
-        } else if (KIND == kMoveUnpack && FP8) {
+        if (KIND == kMoveUnpack && FP8) {
           if (v < split)
             st_vec(pl.dst + v * W, r[j]);
           else
@@ -341,8 +366,19 @@ cudaError_t run_tma(const Geo& g, MoveArgs a, Ctx& c) {
 
 template <int KIND, bool FP8, typename V>
 cudaError_t run_ldg(const Geo& g, const MoveArgs& a, Ctx& c) {
+  // Four waves of the CTAs the SMs hold at once (registers decide): warps that finish early
+  // take later units, which measured faster on GB300 than one wave of grid-stride loops.
+  static std::atomic<int> resident{0};
+  int per_sm = resident.load(std::memory_order_relaxed);
+  if (per_sm == 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_move_ldg<KIND, FP8, V>, 256, 0) != cudaSuccess ||
+        per_sm < 1)
+      per_sm = 1;
+    resident.store(per_sm, std::memory_order_relaxed);
+  }
+  per_sm = c.ctas_per_sm > 0 ? c.ctas_per_sm : 4 * per_sm;   // tuning override, else 4 waves
   int64_t blocks = (a.units + 7) / 8;
-  const int64_t maxb = (int64_t)c.num_sms * 4;
+  const int64_t maxb = (int64_t)c.num_sms * per_sm;
   if (blocks > maxb) blocks = maxb;
   return launch_kernel(k_move_ldg<KIND, FP8, V>, dim3((unsigned)blocks), dim3(256), 0, c, g, a);
 }

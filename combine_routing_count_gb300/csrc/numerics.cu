@@ -140,10 +140,42 @@ __global__ void __launch_bounds__(256) k_dequant_fp8(Geo g, const int32_t* __res
   pdl_trigger();
 }
 
+// acc (eight fp32 sums as four packed pairs) += w * v, v a 16-byte vector of eight bf16;
+// product and sum are rounded separately in each lane (RN), as in the scalar definition.
+__device__ __forceinline__ void acc_pair(uint64_t (&acc)[4], const uint4& v, uint64_t w2) {
+  acc[0] = f2_add(acc[0], f2_mul(w2, f2_from_bf16x2(v.x)));
+  acc[1] = f2_add(acc[1], f2_mul(w2, f2_from_bf16x2(v.y)));
+  acc[2] = f2_add(acc[2], f2_mul(w2, f2_from_bf16x2(v.z)));
+  acc[3] = f2_add(acc[3], f2_mul(w2, f2_from_bf16x2(v.w)));
+}
+
+// acc += v (no weight).
+__device__ __forceinline__ void acc_add(uint64_t (&acc)[4], const uint4& v) {
+  acc[0] = f2_add(acc[0], f2_from_bf16x2(v.x));
+  acc[1] = f2_add(acc[1], f2_from_bf16x2(v.y));
+  acc[2] = f2_add(acc[2], f2_from_bf16x2(v.z));
+  acc[3] = f2_add(acc[3], f2_from_bf16x2(v.w));
+}
+
+__device__ __forceinline__ void acc_zero(uint64_t (&acc)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc[i] = 0ull;
+}
+
+__device__ __forceinline__ void store_bf16x8(uint16_t* p, const uint64_t (&acc)[4]) {
+  uint4 o;
+  o.x = pack_bf16x2(f2_lo(acc[0]), f2_hi(acc[0]));
+  o.y = pack_bf16x2(f2_lo(acc[1]), f2_hi(acc[1]));
+  o.z = pack_bf16x2(f2_lo(acc[2]), f2_hi(acc[2]));
+  o.w = pack_bf16x2(f2_lo(acc[3]), f2_hi(acc[3]));
+  st16(p, o);
+}
+
 // Combine receive. Block (token u, column tile); a thread owns 8 bf16 columns (16 bytes).
 // Lane j of each warp loads pair j's send row and weight and shares them by shuffle; the
 // R rows are gathered with up to 8 loads in flight; fp32 products and sums are rounded
-// separately in slot order; dropped or invalid pairs are skipped.
+// separately in slot order (packed f32x2 pairs, each lane rounded as the scalar op);
+// dropped or invalid pairs are skipped.
 constexpr int kReduceThreads = 128;
 
 __global__ void __launch_bounds__(kReduceThreads) k_combine_reduce(Geo g, const int32_t* __restrict__ gsend,
@@ -157,9 +189,8 @@ __global__ void __launch_bounds__(kReduceThreads) k_combine_reduce(Geo g, const 
   const bool act = col < ncol;
   const int lane = threadIdx.x & 31;
   const int64_t q0 = u * g.R;
-  float acc[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+  uint64_t acc[4];
+  acc_zero(acc);
   pdl_wait();
   for (int k0 = 0; k0 < g.R; k0 += 32) {
     int myrow = -1;
@@ -189,23 +220,11 @@ __global__ void __launch_bounds__(kReduceThreads) k_combine_reduce(Geo g, const 
         if (act && rk[j] >= 0) v[j] = ld_stream16(crecv + (int64_t)rk[j] * g.H + col * 8);
       }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (rk[j] < 0) continue;
-        const float f[8] = {bf16_lo(v[j].x), bf16_hi(v[j].x), bf16_lo(v[j].y), bf16_hi(v[j].y),
-                            bf16_lo(v[j].z), bf16_hi(v[j].z), bf16_lo(v[j].w), bf16_hi(v[j].w)};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(wk[j], f[i]));
-      }
+      for (int j = 0; j < 8; ++j)
+        if (rk[j] >= 0) acc_pair(acc, v[j], f2_splat(wk[j]));
     }
   }
-  if (act) {
-    uint4 o;
-    o.x = pack_bf16x2(acc[0], acc[1]);
-    o.y = pack_bf16x2(acc[2], acc[3]);
-    o.z = pack_bf16x2(acc[4], acc[5]);
-    o.w = pack_bf16x2(acc[6], acc[7]);
-    st16(out + u * g.H + col * 8, o);
-  }
+  if (act) store_bf16x8(out + u * g.H + col * 8, acc);
   pdl_trigger();
 }
 
@@ -246,24 +265,6 @@ __device__ __forceinline__ PairGroups token_groups(const Geo& g, const int32_t* 
   }
   pg.j = j;
   return pg;
-}
-
-// Sums the 16-byte column vector `v` of a pair into acc with weight wm (fp32, separate
-// rounding of product and sum).
-__device__ __forceinline__ void acc_pair(float (&acc)[8], const uint4& v, float wm) {
-  const float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                      bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
-#pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(wm, f[i]));
-}
-
-__device__ __forceinline__ void store_bf16x8(uint16_t* p, const float (&acc)[8]) {
-  uint4 o;
-  o.x = pack_bf16x2(acc[0], acc[1]);
-  o.y = pack_bf16x2(acc[2], acc[3]);
-  o.z = pack_bf16x2(acc[4], acc[5]);
-  o.w = pack_bf16x2(acc[6], acc[7]);
-  st16(p, o);
 }
 
 // Expert side: for each token and each group, cpart[s][t][j] = bf16(sum of w*y over the
@@ -324,26 +325,23 @@ __global__ void __launch_bounds__(kReduceThreads) k_combine_partial(Geo g, const
       v[p] = make_uint4(0, 0, 0, 0);
       if (act && p < n) v[p] = ld_stream16(y0 + (int64_t)s_row[p] * g.H);
     }
-    float acc[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    uint64_t acc[4];
+    acc_zero(acc);
     int j = 0;
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
       if (p >= n) break;
-      acc_pair(acc, v[p], s_w[p]);
+      acc_pair(acc, v[p], f2_splat(s_w[p]));
       if (s_last[p]) {
         if (act) store_bf16x8(out0 + (int64_t)j * g.H, acc);
         ++j;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+        acc_zero(acc);
       }
     }
   } else {
     for (int j = 0; j < pg.ngroups; ++j) {
-      float acc[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+      uint64_t acc[4];
+      acc_zero(acc);
       for (int k0 = 0; k0 < g.R; k0 += 8) {
         uint4 v[8];
 #pragma unroll
@@ -360,7 +358,7 @@ __global__ void __launch_bounds__(kReduceThreads) k_combine_partial(Geo g, const
           const int row = __shfl_sync(kFull, pg.row, k);
           const int jm = __shfl_sync(kFull, pg.j, k);
           const float wm = __shfl_sync(kFull, pg.w, k);
-          if (k0 + m < g.R && row >= 0 && jm == j) acc_pair(acc, v[m], wm);
+          if (k0 + m < g.R && row >= 0 && jm == j) acc_pair(acc, v[m], f2_splat(wm));
         }
       }
       if (act) store_bf16x8(out0 + (int64_t)j * g.H, acc);
@@ -381,12 +379,11 @@ __global__ void __launch_bounds__(kReduceThreads) k_combine_sum(Geo g, const int
   const int ng = __ldg(tgroups + u);
   const uint16_t* in0 = cpart + (u * J) * g.H;
   int cols[2];
-  float acc[2][8];
+  uint64_t acc[2][4];
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
     cols[c] = blockIdx.y * 2 * kReduceThreads + c * kReduceThreads + threadIdx.x;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[c][i] = 0.0f;
+    acc_zero(acc[c]);
   }
   for (int j0 = 0; j0 < ng; j0 += 4) {
     uint4 v[4][2];
@@ -401,24 +398,12 @@ __global__ void __launch_bounds__(kReduceThreads) k_combine_sum(Geo g, const int
     for (int m = 0; m < 4; ++m) {
       if (j0 + m >= ng) continue;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const float f[8] = {bf16_lo(v[m][c].x), bf16_hi(v[m][c].x), bf16_lo(v[m][c].y), bf16_hi(v[m][c].y),
-                            bf16_lo(v[m][c].z), bf16_hi(v[m][c].z), bf16_lo(v[m][c].w), bf16_hi(v[m][c].w)};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[c][i] = __fadd_rn(acc[c][i], f[i]);
-      }
+      for (int c = 0; c < 2; ++c) acc_add(acc[c], v[m][c]);
     }
   }
 #pragma unroll
-  for (int c = 0; c < 2; ++c) {
-    if (cols[c] >= ncol) continue;
-    uint4 o;
-    o.x = pack_bf16x2(acc[c][0], acc[c][1]);
-    o.y = pack_bf16x2(acc[c][2], acc[c][3]);
-    o.z = pack_bf16x2(acc[c][4], acc[c][5]);
-    o.w = pack_bf16x2(acc[c][6], acc[c][7]);
-    st16(out + u * g.H + cols[c] * 8, o);
-  }
+  for (int c = 0; c < 2; ++c)
+    if (cols[c] < ncol) store_bf16x8(out + u * g.H + cols[c] * 8, acc[c]);
   pdl_trigger();
 }
 
