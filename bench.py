@@ -37,7 +37,7 @@ import workloads  # noqa: E402
 METRIC = "dispatch+combine tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 KERNELS = ["route_count", "layout_maps", "quant_fp8", "pack", "scatter", "unpack", "expert",
            "combine_pack", "combine_scatter", "combine_reduce", "route_scan", "pack_push", "combine_push",
-           "combine_partial", "combine_sum"]
+           "combine_partial", "combine_sum", "dispatch_split"]
 
 
 def parse_args(argv=None):
@@ -180,6 +180,7 @@ def algorithmic_bytes(wl: workloads.Workload, P: int, Pk: int) -> dict:
         "combine_reduce": Pk * 2 * H + tok * 2 * H,
         "pack_push": tok * B + P * B,
         "combine_push": 2 * Pk * 2 * H,
+        "dispatch_split": tok * B + P * B + 2 * Pk * B,
     }
 
 
@@ -258,6 +259,8 @@ def run_ours(args):
     def step():
         ep.forward(x, idx, w)
 
+    step_default = step
+
     def step_split(e0, e1, e2, e3):
         """One pass with events around the identity expert (the grouped-GEMM stand-in), so
         its time can be left out of the step as the scope's tokens/s definition asks."""
@@ -310,6 +313,17 @@ def run_ours(args):
         ep.expert_identity()
         ep.combine_partial(w)
 
+    def step_splitphase():
+        ep.layout_step(idx)
+        if fp8:
+            ep.quantize(x)
+            ep.dispatch_split(ep.xq)
+        else:
+            ep.dispatch_split(x)
+        ep.expert_identity()
+        ep.combine_send()
+        ep.combine_recv(w)
+
     def kernel_region(step=step):
         """Timed region: per-kernel CUDA events (the library records one pair around each of
         its launches on this stream) give each kernel's duration for the roofline."""
@@ -336,7 +350,7 @@ def run_ours(args):
         barrier(dist, device)
         torch.cuda.synchronize()
         n0 = lib().moe_launch_count()
-        split = fp8 and step is not step_partial
+        split = fp8 and step is step_default
         if split:
             mids = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
             for i in range(K):
@@ -426,6 +440,26 @@ def run_ours(args):
                               "frac": round(ab[name] / (us * 1e-6) / 1e9 / peak, 3)}
     part_ms_all = max_over_ranks(part_ms, dist, device)
 
+    # The direct-push step with dispatch as one split-phase launch: every CTA pushes its
+    # share of rows and signals per slice, then waits for each pair's slice and shuffles it.
+    ep.layout.flags |= 8
+    for _ in range(args.warmup):
+        flush.zero_()
+        step_splitphase()
+    pk_sp = kernel_region(step_splitphase)
+    sp_ms, _, _ = step_region(step_splitphase)
+    ep.layout.flags &= ~8
+    if fp8:
+        sp_ms -= expert_ms
+    sp_kernels = {}
+    for name, ts in pk_sp.items():
+        if name == "expert":
+            continue
+        us = statistics.fmean(ts) * 1e3
+        sp_kernels[name] = {"us": round(us, 2), "gbs": round(ab[name] / (us * 1e-6) / 1e9, 1),
+                            "frac": round(ab[name] / (us * 1e-6) / 1e9 / peak, 3)}
+    sp_ms_all = max_over_ranks(sp_ms, dist, device)
+
     # end to end through the C ABI with host buffers: H2D inputs, the pass, D2H output
     h_x = torch.from_numpy(inp["x"]).view(torch.bfloat16).pin_memory()
     h_idx = torch.from_numpy(inp["idx"]).pin_memory()
@@ -474,6 +508,12 @@ def run_ours(args):
                                 "kernels": {k: v for k, v in part_kernels.items() if k.startswith("combine")},
                                 "note": "combine sums each token's experts per destination rank on the "
                                         "expert side (bf16 partial rows), then over ranks on the source"},
+        "split_phase_dispatch": {"value": round(tokens / (sp_ms_all * 1e-3), 1), "unit": "tokens/s",
+                                 "ms_per_step": round(sp_ms_all, 4),
+                                 "kernels": {k: v for k, v in sp_kernels.items() if k == "dispatch_split"},
+                                 "note": "direct-push step whose dispatch is one cooperative launch: "
+                                         "push rows, signal per (destination, source) slice, wait "
+                                         "(bounded), shuffle into the grouped rows"},
         "e2e": {"value": round(tokens / (e2e_ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "path": "moe_forward_host (C ABI)"},
         "identity_expert": None if expert_ms is None else {

@@ -105,6 +105,14 @@ class MoeEP:
                                       self.send.data_ptr(), self.recv.data_ptr(), _stream(stream)),
               "moe_dispatch_send")
 
+    def dispatch_split(self, x: torch.Tensor, withhold_slice: int = -1, stream=None):
+        """Split-phase dispatch: receive rows and grouped expert rows in one launch.
+        withhold_slice (tests only) names a slice d*N + s whose arrival signals are not sent."""
+        self.x = x
+        check(lib().moe_dispatch_split(ctypes.byref(self.dims), ctypes.byref(self.layout), x.data_ptr(),
+                                       self.recv.data_ptr(), self.expert_x.data_ptr(), _ptr(self.expert_scale),
+                                       int(withhold_slice), _stream(stream)), "moe_dispatch_split")
+
     def dispatch_recv(self, stream=None):
         check(lib().moe_dispatch_recv(ctypes.byref(self.dims), ctypes.byref(self.layout), self.recv.data_ptr(),
                                       self.expert_x.data_ptr(), _ptr(self.expert_scale), _stream(stream)),

@@ -315,6 +315,8 @@ int64_t layout_scratch_done_offset(const Geo& g) { return (int64_t)g.N * layout_
 
 int64_t layout_scratch_tgroups_offset(const Geo& g) { return layout_scratch_done_offset(g) + g.N; }
 
+int64_t layout_scratch_arrive_offset(const Geo& g) { return layout_scratch_tgroups_offset(g) + (int64_t)g.N * g.T; }
+
 
 cudaError_t launch_layout(const Geo& g, const int32_t* idx, const moe_layout_t* lay, Ctx& c) {
   LayoutArgs a;

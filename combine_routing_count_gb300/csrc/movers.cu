@@ -276,7 +276,9 @@ __global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
       uint8_t* dst0 = a.dst + coff;
       const int32_t* fan = a.fan + tok * g.R;
       const int myp = lane < g.R ? __ldg(fan + lane) : -1;   // pairs 0..31 (R > 32: see below)
-      for (int64_t v0 = lane; v0 < nel; v0 += 32 * U) {
+      // The trip count is the same for every lane: the shuffles below need the whole warp.
+      for (int64_t b0 = 0; b0 < nel; b0 += 32 * U) {
+        const int64_t v0 = b0 + lane;
         V r[U];
 #pragma unroll
         for (int j = 0; j < U; ++j) {

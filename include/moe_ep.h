@@ -85,7 +85,8 @@ typedef enum {
     MOE_K_COMBINE_PUSH = 12,   /* direct push: grouped rows -> sources' combine rows */
     MOE_K_COMBINE_PARTIAL = 13, /* expert-side partial sums, one row per (token, rank) */
     MOE_K_COMBINE_SUM = 14,    /* source-side sum of the partial rows -> bf16 */
-    MOE_K_NUM = 15
+    MOE_K_DISPATCH_SPLIT = 15, /* split-phase dispatch: push, signal, wait, shuffle in one launch */
+    MOE_K_NUM = 16
 } moe_kernel_id;
 
 /* Optional per-kernel timing. When moe_layout_t.prof is non-NULL, every kernel the library
@@ -252,6 +253,27 @@ moe_status moe_dispatch_send(const moe_dims *dims, const moe_layout_t *lay, cons
  *  - Calls no allocating routine (no cudaMalloc, cudaFree or library allocator). */
 moe_status moe_dispatch_send_noalloc(const moe_dims *dims, const moe_layout_t *lay, const void *d_x,
                                      void *d_recv, void *stream);
+
+/* Split-phase dispatch (section "Dispatch and combine": dispatch is split into a sender half
+ * that fills the peers' buffers and signals, and a receiver half that waits for every transfer
+ * of its peers and then shuffles the tokens into the grouped-GEMM input; section "MoE
+ * all-to-all over EFA": inside a node the sender writes straight into the peers' buffers).
+ * Results are those of moe_dispatch_send with MOE_FLAG_DIRECT_PUSH followed by
+ * moe_dispatch_recv: d_recv [N][RB][B] holds every receive row, d_expert_x / d_expert_scale
+ * the grouped rows (same layouts as moe_dispatch_recv).
+ * One cooperative launch: every CTA first pushes its share of token rows into the owners'
+ * receive rows and increments, per row, the arrival counter of the slice (d, s) it belongs
+ * to; it then takes pairs, waits until the counter of the pair's slice reaches C[s][d] row
+ * pieces, and copies the row into its expert's slot. Each wait is bounded (1 s): on expiry
+ * the status word gets the MOE_ERR_TIMEOUT bit, later waits of the call give up at once,
+ * the grouped rows of unfinished slices are left unwritten, and the call still completes.
+ * The counters live in the layout workspace, start at zero and are zeroed again by the
+ * call; calls that share a layout must not overlap on the GPU.
+ * withhold_slice: failure injection for tests; the signals of slice d*N + s are never sent,
+ * so its waits time out. Pass -1 in normal use; other negative values and values >= N*N
+ * are MOE_ERR_INVALID_ARG, and so is R > 32. */
+moe_status moe_dispatch_split(const moe_dims *dims, const moe_layout_t *lay, const void *d_x, void *d_recv,
+                              void *d_expert_x, float *d_expert_scale, int32_t withhold_slice, void *stream);
 
 /* Dispatch receive (section "Dispatch and combine": shuffle tokens from the receive buffer
  * into the tensor handed to the grouped GEMM): every receive row of rank d goes to row

@@ -17,8 +17,11 @@ def to_dev(a: np.ndarray, dtype=None) -> torch.Tensor:
     return t.cuda()
 
 
-def run_gpu(wl: workloads.Workload, inp: dict, flags: int = 0, poison: bool = True, **kw):
-    """Runs every step separately on the GPU; returns (MoeEP, host copies of every buffer)."""
+def run_gpu(wl: workloads.Workload, inp: dict, flags: int = 0, poison: bool = True, split: bool = False,
+            withhold_slice: int = -1, **kw):
+    """Runs every step separately on the GPU; returns (MoeEP, host copies of every buffer).
+    With split, dispatch is the one-launch split-phase dispatch (direct push) instead of
+    dispatch send + receive; withhold_slice is passed to it."""
     from combine_routing_count_gb300 import MoeEP
     ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, wl.payload, flags=flags, separate_expert_y=True, **kw)
     if poison:
@@ -33,10 +36,12 @@ def run_gpu(wl: workloads.Workload, inp: dict, flags: int = 0, poison: bool = Tr
     res = {}
     if wl.payload == "fp8":
         ep.quantize(x)
-        ep.dispatch_send(ep.xq)
+        x = ep.xq
+    if split:
+        ep.dispatch_split(x, withhold_slice)
     else:
         ep.dispatch_send(x)
-    ep.dispatch_recv()
+        ep.dispatch_recv()
     ep.expert_identity()
     ep.combine_send()
     ep.combine_recv(w)

@@ -195,3 +195,65 @@ def test_partial_combine_matches_oracle(orc, wl):
                                          o["layout"], fill=poison)
     np.testing.assert_array_equal(u16(ep.cpart.cpu()), cpart_o)
     np.testing.assert_array_equal(u16(ep.out.cpu()), out_o)
+
+
+@pytest.mark.parametrize("wl", CASES + [workloads.config(1).replace(T=16, seed=150)], ids=lambda w: w.name)
+def test_split_dispatch_matches_oracle(orc, wl):
+    """Split-phase dispatch (push, per-slice arrival counters, bounded waits, shuffle in one
+    cooperative launch) leaves exactly the receive and grouped rows of the two-step path."""
+    inp = workloads.make_inputs(wl)
+    _, res = run_gpu(wl, inp, flags=8, split=True)
+    compare_all(orc, wl, inp, res, push=True)
+
+
+def test_split_dispatch_withheld_slice_times_out_and_recovers(orc):
+    """A slice whose arrival signals never come: its waits end after the bound with the
+    timeout status, every other row is still placed, and the next call on the same layout
+    (counters reset by the call itself) is exact again."""
+    wl = W("split-timeout", 4, 33, 1024, 16, 4, "bf16", "uniform", 151)
+    inp = workloads.make_inputs(wl)
+    o = orc.forward(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, wl.payload, inp["x"], inp["idx"], inp["w"])
+    lay_o = o["layout"]
+    s, d = 1, 2
+    assert lay_o["C"][s, d] > 0
+    ep, res = run_gpu(wl, inp, flags=8, split=True, withhold_slice=d * wl.N + s)
+    assert res["status_code"] == 6                      # MOE_ERR_TIMEOUT
+    recv = u8(res["recv"])
+    for dd in range(wl.N):
+        n = lay_o["rtot"][dd]
+        np.testing.assert_array_equal(recv[dd, :n], o["recv"][dd, :n], err_msg="recv")
+    # grouped rows: those of slice (d, s) are unwritten, every other one is exact
+    ex = u16(res["expert_x"])
+    slot_src = lay_o["slot_src"].reshape(wl.E, -1)
+    TR = wl.T * wl.R
+    for e in range(wl.E):
+        dd, l = divmod(e, wl.L)
+        for j in range(min(lay_o["ecnt"][dd, l], lay_o["cap"])):
+            src = slot_src[e, j] // TR
+            if dd == d and src == s:
+                assert (ex[dd, l, j].view(np.uint8) == 0xA5).all(), "withheld row was written"
+            else:
+                np.testing.assert_array_equal(ex[dd, l, j], o["ex"][dd, l, j])
+    # the context is still usable and the counters start from zero again
+    ep.expert_x.view(torch.uint8).fill_(0xA5)
+    ep.dispatch_split(ep.x)
+    code, bits = ep.status()
+    assert code == 0 and bits == 0
+    ex = u16(ep.expert_x.cpu())
+    ecnt = np.minimum(lay_o["ecnt"], lay_o["cap"])
+    for dd in range(wl.N):
+        for l in range(wl.L):
+            np.testing.assert_array_equal(ex[dd, l, :ecnt[dd, l]], o["ex"][dd, l, :ecnt[dd, l]])
+
+
+def test_split_dispatch_rejects_bad_withhold_slice():
+    import ctypes
+    from combine_routing_count_gb300 import MoeEP, lib
+    ep = MoeEP(2, 4, 128, 4, 2)
+    x = torch.zeros((2, 4, 128), dtype=torch.bfloat16, device="cuda")
+    n0 = lib().moe_launch_count()
+    for bad in (-2, 4):
+        rc = lib().moe_dispatch_split(ctypes.byref(ep.dims), ctypes.byref(ep.layout), x.data_ptr(),
+                                      ep.recv.data_ptr(), ep.expert_x.data_ptr(), None, bad, None)
+        assert rc == 1
+    assert lib().moe_launch_count() == n0
