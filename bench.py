@@ -37,7 +37,7 @@ import workloads  # noqa: E402
 METRIC = "dispatch+combine tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 KERNELS = ["route_count", "layout_maps", "quant_fp8", "pack", "scatter", "unpack", "expert",
            "combine_pack", "combine_scatter", "combine_reduce", "route_scan", "pack_push", "combine_push",
-           "combine_partial", "combine_sum", "dispatch_split"]
+           "combine_partial", "combine_sum", "dispatch_split", "quant_pack"]
 
 
 def parse_args(argv=None):
@@ -53,6 +53,8 @@ def parse_args(argv=None):
     p.add_argument("--tma-stages", type=int, default=0)
     p.add_argument("--ctas-per-sm", type=int, default=0)
     p.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
+    p.add_argument("--staged-quant", action="store_true",
+                   help="fp8: quantise into a staging buffer, then pack (two kernels) instead of inside the pack")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work for the oracle baseline")
     return p.parse_args(argv)
@@ -179,6 +181,7 @@ def algorithmic_bytes(wl: workloads.Workload, P: int, Pk: int) -> dict:
         "combine_scatter": 2 * Pk * 2 * H,
         "combine_reduce": Pk * 2 * H + tok * 2 * H,
         "pack_push": tok * B + P * B,
+        "quant_pack": tok * 2 * H + P * B,
         "combine_push": 2 * Pk * 2 * H,
         "dispatch_split": tok * B + P * B + 2 * Pk * B,
     }
@@ -245,7 +248,8 @@ def run_ours(args):
     wl = workload_of(args)
     inp = workloads.make_inputs(wl)
     ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, wl.payload, alias_buffers=(wl.payload == "bf16"),
-               flags={"auto": 0, "ldg": 1, "tma": 4}[args.mover] | (2 if args.no_pdl else 0), tma_stages=args.tma_stages,
+               flags={"auto": 0, "ldg": 1, "tma": 4}[args.mover] | (2 if args.no_pdl else 0) |
+               (0x10 if args.staged_quant else 0), tma_stages=args.tma_stages,
                ctas_per_sm=args.ctas_per_sm)
     x = torch.from_numpy(inp["x"]).view(torch.bfloat16).to(device)
     idx = torch.from_numpy(inp["idx"]).to(device)
@@ -261,13 +265,20 @@ def run_ours(args):
 
     step_default = step
 
+    def quant_dispatch_send():
+        """fp8 dispatch send as moe_forward does it: quantisation inside the pack, or staged."""
+        if args.staged_quant:
+            ep.quantize(x)
+            ep.dispatch_send(ep.xq)
+        else:
+            ep.quantize_dispatch_send(x)
+
     def step_split(e0, e1, e2, e3):
         """One pass with events around the identity expert (the grouped-GEMM stand-in), so
         its time can be left out of the step as the scope's tokens/s definition asks."""
         e0.record(stream)
         ep.layout_step(idx)
-        ep.quantize(x)
-        ep.dispatch_send(ep.xq)
+        quant_dispatch_send()
         ep.dispatch_recv()
         e1.record(stream)
         ep.expert_identity()
@@ -305,8 +316,7 @@ def run_ours(args):
     def step_partial():
         ep.layout_step(idx)
         if fp8:
-            ep.quantize(x)
-            ep.dispatch_send(ep.xq)
+            quant_dispatch_send()
         else:
             ep.dispatch_send(x)
         ep.dispatch_recv()
@@ -487,7 +497,7 @@ def run_ours(args):
         "data": "synthetic (seeded; DeepSeek-V3/Kimi-K2-shaped routing, identity experts)",
         "config": {"workload": wl.name, "N_ranks_simulated": wl.N, "T": wl.T, "H": wl.H, "E": wl.E, "R": wl.R,
                    "payload": wl.payload, "routing": wl.routing, "seed": wl.seed, "mover": args.mover,
-                   "pdl": not args.no_pdl,
+                   "pdl": not args.no_pdl, "fp8_quant": ("staged" if args.staged_quant else "inside the pack") if fp8 else None,
                    "l2": "flushed before every timed step (write of 2x L2)",
                    "parallelism": f"{ws} independent replica(s) of the {wl.N}-rank group"},
         "hbm_gbs": round(step_bytes / (mean_ms * 1e-3) / 1e9, 1),

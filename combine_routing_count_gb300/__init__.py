@@ -14,12 +14,13 @@ import ctypes
 import torch
 
 from . import _abi
-from ._abi import (MOE_FLAG_DIRECT_PUSH, MOE_FLAG_LDG_MOVER, MOE_FLAG_NO_PDL, MOE_FLAG_TMA_MOVER, MOE_PAYLOAD_BF16, MOE_PAYLOAD_FP8_E4M3_B128, KERNEL_NAMES, MoeBuffers,
+from ._abi import (MOE_FLAG_DIRECT_PUSH, MOE_FLAG_LDG_MOVER, MOE_FLAG_NO_PDL, MOE_FLAG_STAGED_QUANT,
+                   MOE_FLAG_TMA_MOVER, MOE_PAYLOAD_BF16, MOE_PAYLOAD_FP8_E4M3_B128, KERNEL_NAMES, MoeBuffers,
                    MoeDims, MoeError, MoeLayout, MoeProf, check, lib)
 
 __all__ = ["MoeEP", "MoeDims", "MoeLayout", "MoeBuffers", "MoeProf", "MoeError", "lib", "check",
            "MOE_FLAG_LDG_MOVER", "MOE_FLAG_NO_PDL", "MOE_FLAG_TMA_MOVER", "MOE_FLAG_DIRECT_PUSH",
-           "KERNEL_NAMES"]
+           "MOE_FLAG_STAGED_QUANT", "KERNEL_NAMES"]
 
 
 def _ptr(t) -> int | None:
@@ -104,6 +105,13 @@ class MoeEP:
         check(lib().moe_dispatch_send(ctypes.byref(self.dims), ctypes.byref(self.layout), x.data_ptr(),
                                       self.send.data_ptr(), self.recv.data_ptr(), _stream(stream)),
               "moe_dispatch_send")
+
+    def quantize_dispatch_send(self, x: torch.Tensor, stream=None):
+        """fp8 payload: quantise the bf16 token rows x [N,T,H] inside the pack (xq is not written)."""
+        self.x = x
+        check(lib().moe_quantize_dispatch_send(ctypes.byref(self.dims), ctypes.byref(self.layout), x.data_ptr(),
+                                               self.send.data_ptr(), self.recv.data_ptr(), _stream(stream)),
+              "moe_quantize_dispatch_send")
 
     def dispatch_split(self, x: torch.Tensor, withhold_slice: int = -1, stream=None):
         """Split-phase dispatch: receive rows and grouped expert rows in one launch.

@@ -239,6 +239,25 @@ moe_status moe_dispatch_send(const moe_dims* dims, const moe_layout_t* lay, cons
   return cuda_status(e);
 }
 
+moe_status moe_quantize_dispatch_send(const moe_dims* dims, const moe_layout_t* lay, const uint16_t* d_x,
+                                      void* d_send, void* d_recv, void* stream) {
+  Geo g;
+  moe_status st = make_geo(dims, g);
+  if (st != MOE_OK) return st;
+  if (g.payload != MOE_PAYLOAD_FP8_E4M3_B128) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)g.N * g.T == 0) return layout_ok(lay) ? MOE_OK : MOE_ERR_INVALID_ARG;  // nothing to move
+  const bool push = lay && (lay->flags & MOE_FLAG_DIRECT_PUSH);
+  if (!layout_ok(lay) || !d_x || !d_recv || !aligned16(d_x) || !aligned16(d_recv) ||
+      (!push && (!d_send || !aligned16(d_send))))
+    return MOE_ERR_INVALID_ARG;
+  Ctx c;
+  if ((st = make_ctx(lay, stream, c)) != MOE_OK) return st;
+  if (push) return cuda_status(launch_quant_pack(g, lay->grecv, d_x, static_cast<uint8_t*>(d_recv), c));
+  cudaError_t e = launch_quant_pack(g, lay->gsend, d_x, static_cast<uint8_t*>(d_send), c);
+  if (e == cudaSuccess) e = launch_move(kMoveScatter, g, lay, d_send, d_recv, nullptr, c);
+  return cuda_status(e);
+}
+
 moe_status moe_dispatch_split(const moe_dims* dims, const moe_layout_t* lay, const void* d_x, void* d_recv,
                               void* d_expert_x, float* d_expert_scale, int32_t withhold_slice, void* stream) {
   Geo g;
@@ -356,12 +375,16 @@ moe_status moe_forward(const moe_dims* dims, const moe_layout_t* lay, const moe_
   if (st != MOE_OK) return st;
   const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
   if ((st = moe_layout(dims, b->idx, lay, stream)) != MOE_OK) return st;
-  const void* xin = b->x;
-  if (fp8) {
-    if ((st = moe_quantize_fp8_b128(dims, b->x, b->xq, lay, stream)) != MOE_OK) return st;
-    xin = b->xq;
+  if (fp8 && !(lay->flags & MOE_FLAG_STAGED_QUANT)) {
+    if ((st = moe_quantize_dispatch_send(dims, lay, b->x, b->send, b->recv, stream)) != MOE_OK) return st;
+  } else {
+    const void* xin = b->x;
+    if (fp8) {
+      if ((st = moe_quantize_fp8_b128(dims, b->x, b->xq, lay, stream)) != MOE_OK) return st;
+      xin = b->xq;
+    }
+    if ((st = moe_dispatch_send(dims, lay, xin, b->send, b->recv, stream)) != MOE_OK) return st;
   }
-  if ((st = moe_dispatch_send(dims, lay, xin, b->send, b->recv, stream)) != MOE_OK) return st;
   if ((st = moe_dispatch_recv(dims, lay, b->recv, b->expert_x, b->expert_scale, stream)) != MOE_OK) return st;
   if ((st = moe_expert_identity(dims, lay, b->expert_x, b->expert_scale, b->expert_y, stream)) != MOE_OK) return st;
   if ((st = moe_combine_send(dims, lay, b->expert_y, b->csend, b->crecv, stream)) != MOE_OK) return st;

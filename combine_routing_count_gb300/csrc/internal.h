@@ -102,6 +102,8 @@ cudaError_t launch_move(MoveKind kind, const Geo& g, const moe_layout_t* lay, co
 
 // numerics.cu
 cudaError_t launch_quant_fp8(const Geo& g, const uint16_t* x, uint8_t* xq, Ctx& c);
+// Quantise bf16 token rows and write each one's fp8 row into dst rows fan[token][k] (k < R).
+cudaError_t launch_quant_pack(const Geo& g, const int32_t* fan, const uint16_t* x, uint8_t* dst, Ctx& c);
 cudaError_t launch_dequant_fp8(const Geo& g, const moe_layout_t* lay, const uint8_t* exq, const float* exs,
                                uint16_t* ey, Ctx& c);
 cudaError_t launch_combine_partial(const Geo& g, const moe_layout_t* lay, const uint16_t* ey, const float* w,

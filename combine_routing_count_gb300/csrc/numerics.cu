@@ -7,7 +7,6 @@
 // average over each token's experts, on the receiving side only.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
-#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -21,56 +20,250 @@ constexpr unsigned kFull = 0xffffffffu;
 // amax over the block by xor-shuffles inside the half warp; scale = amax / 448 (IEEE fp32
 // division; 1 when amax is 0); codes = e4m3(x / scale), round to nearest even, saturating.
 // Output row: H codes, then H/128 fp32 scales. 4-byte stores (rows are 4-byte aligned).
-// A warp takes kQuantUnroll pairs of blocks per trip and issues all their loads first.
+// A warp takes kQuantUnroll pairs of blocks of one row per trip (one index division per
+// trip) and issues all their loads first.
 constexpr int kQuantUnroll = 4;
+
+// Two fp32 values to two e4m3 codes, round to nearest even, saturating to +-448; lo goes to
+// the low byte (the conversion puts its first source operand in the upper byte).
+__device__ __forceinline__ uint32_t e4m3x2_rn_sat(float lo, float hi) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// Two e4m3 codes (low byte first) to two f16 values (exact: every e4m3 value is an f16 value).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t c) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(c));
+  return d;
+}
+
+__device__ __forceinline__ float e4m3_value(uint32_t c) {
+  return __half2float(__ushort_as_half((unsigned short)(e4m3x2_to_f16x2((uint16_t)c) & 0xffffu)));
+}
+
+// Four e4m3 codes (low byte first) of four fp32 values.
+__device__ __forceinline__ uint32_t e4m3x4_rn_sat(float a, float b, float c, float d) {
+  uint32_t w;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(w) : "f"(a), "f"(b), "f"(c), "f"(d));
+  return w;
+}
+
+// The code of RN(x / scale) for a value whose bracket (below) gave the two adjacent codes cl and
+// ch, values a and b, with the e4m3 rounding boundary m = (a + b) / 2 between them. m has at most
+// five significant bits, so it is even in fp32 and RN(x / scale) == m (a tie, rounded to the even
+// code) exactly when |x / scale - m| <= ulp(m) / 2, that is when |x - m * scale| <= t with
+// t = ulp(m) / 2 * scale; otherwise the quotient lies on the side of m that x - m * scale has.
+// d = fma(-m, scale, x) is that difference rounded once (exact for scale >= 2^-90): it has the
+// exact sign and decides the comparison unless it lands on t itself, where the quotient is
+// divided.
+__device__ __forceinline__ uint32_t e4m3_resolve(float x, float scale, uint32_t cl, uint32_t ch) {
+  const float a = e4m3_value(cl), b = e4m3_value(ch);
+  const float m = __fmul_rn(__fadd_rn(a, b), 0.5f);
+  const float d = __fmaf_rn(-m, scale, x);
+  const float t = __fmul_rn(__fmul_rn(__uint_as_float(__float_as_uint(m) & 0x7f800000u), 0x1p-24f), scale);
+  const float ad = fabsf(d);
+  if (ad < t) return (cl & 1u) ? ch : cl;
+  if (ad > t) return ((d > 0.0f) == (a > b)) ? cl : ch;
+  return e4m3x2_rn_sat(__fdiv_rn(x, scale), 0.0f) & 0xffu;
+}
+
+// scale = RN(amax / 448) of a block's amax (a bf16 value), 1 for amax 0. Above 2^-100 without a
+// division: q0 = RN(amax * c) with c = RN(1/448), the remainder amax - 448 * q0 (exact, one
+// fma), and Markstein's correction RN(q0 + remainder * c). That this equals the correctly
+// rounded quotient was checked, with exact rational arithmetic, for every bf16 value from
+// 2^-100 up to the largest finite one.
+__device__ __forceinline__ float block_scale(float amax) {
+  if (amax == 0.0f) return 1.0f;
+  if (amax < 0x1p-100f) return __fdiv_rn(amax, 448.0f);
+  constexpr float c = 1.0f / 448.0f;
+  const float q0 = __fmul_rn(amax, c);
+  return __fmaf_rn(__fmaf_rn(-q0, 448.0f, amax), c, q0);
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Bit k of the result: byte k of d is nonzero.
+__device__ __forceinline__ uint32_t nonzero_bytes(uint32_t d) {
+  d |= d >> 4;
+  d |= d >> 2;
+  d |= d >> 1;
+  return ((d & 0x01010101u) * 0x01020408u) >> 24;
+}
+
+// Codes of q = RN(x / scale) without a division per value. With r an approximate 1 / scale
+// (relative error at most 2^-23), lo = RN(x * RN(r * (1 - 2^-19))) and hi = RN(x * RN(r * (1 +
+// 2^-19))) bracket q strictly: r and the three roundings move a value by well under 2^-19
+// together. Rounding to e4m3 is monotonic, so where lo and hi get the same code, q gets it too.
+__device__ __forceinline__ void bracket_rcp(float scale, float& rlo, float& rhi) {
+  const float r = rcp_approx(scale);
+  rlo = __fmul_rn(r, 1.0f - 0x1p-19f);
+  rhi = __fmul_rn(r, 1.0f + 0x1p-19f);
+}
+
+// The code of RN(x / scale) for one value, exactly: the bracket, and where its ends differ,
+// e4m3_resolve; a tiny or subnormal scale divides.
+__device__ __forceinline__ uint32_t e4m3_code_exact(float x, float scale) {
+  if (scale < 0x1p-90f) return e4m3x2_rn_sat(__fdiv_rn(x, scale), 0.0f) & 0xffu;
+  float rlo, rhi;
+  bracket_rcp(scale, rlo, rhi);
+  const uint32_t cl = e4m3x2_rn_sat(__fmul_rn(x, rlo), 0.0f) & 0xffu;
+  const uint32_t ch = e4m3x2_rn_sat(__fmul_rn(x, rhi), 0.0f) & 0xffu;
+  return cl == ch ? cl : e4m3_resolve(x, scale, cl, ch);
+}
+
+// One warp unit of a row: lane (half h, sub) loads blocks bbase + 2j (bbase already holds h)
+// and quantises its 8 values of each; codes[j] are its codes, scale[j] its block's scale.
+// Blocks at or past nb read as zeros. The codes come from the lower end of the quotient
+// bracket; the values whose bracket ends disagree (about 1 in 200 for bf16 data, mostly exact
+// ties) are flagged and settled afterwards, one by one, by e4m3_code_exact, which keeps that
+// code out of the unrolled main path.
+__device__ __forceinline__ void quant_unit(const uint16_t* xr, int bbase, int nb, uint32_t (&codes)[kQuantUnroll][2],
+                                           float (&scale)[kQuantUnroll]) {
+  uint4 v[kQuantUnroll];
+#pragma unroll
+  for (int j = 0; j < kQuantUnroll; ++j) {
+    const int b = bbase + 2 * j;
+    v[j] = b < nb ? ld_stream16(xr + b * 128) : make_uint4(0, 0, 0, 0);
+  }
+  uint32_t diff[kQuantUnroll][2];   // bytes where the bracket ends disagree
+  uint32_t any = 0;
+#pragma unroll
+  for (int j = 0; j < kQuantUnroll; ++j) {
+    const float f[8] = {bf16_lo(v[j].x), bf16_hi(v[j].x), bf16_lo(v[j].y), bf16_hi(v[j].y),
+                        bf16_lo(v[j].z), bf16_hi(v[j].z), bf16_lo(v[j].w), bf16_hi(v[j].w)};
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o, 16));
+    const float sc = block_scale(amax);
+    scale[j] = sc;
+    const bool tiny = sc < 0x1p-90f;
+    float rlo, rhi;
+    bracket_rcp(tiny ? 1.0f : sc, rlo, rhi);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float* fi = f + 4 * i;
+      const uint32_t wl = e4m3x4_rn_sat(__fmul_rn(fi[0], rlo), __fmul_rn(fi[1], rlo), __fmul_rn(fi[2], rlo),
+                                        __fmul_rn(fi[3], rlo));
+      const uint32_t wh = e4m3x4_rn_sat(__fmul_rn(fi[0], rhi), __fmul_rn(fi[1], rhi), __fmul_rn(fi[2], rhi),
+                                        __fmul_rn(fi[3], rhi));
+      codes[j][i] = wl;
+      diff[j][i] = tiny ? 0xffffffffu : (wl ^ wh);
+      any |= diff[j][i];
+    }
+  }
+  if (!any) return;
+  uint32_t pend = 0;   // bit 8j + 4i + e: value e of word i of block j to settle
+#pragma unroll
+  for (int j = 0; j < kQuantUnroll; ++j)
+#pragma unroll
+    for (int i = 0; i < 2; ++i) pend |= nonzero_bytes(diff[j][i]) << (8 * j + 4 * i);
+  while (pend) {
+    const int bit = __ffs(pend) - 1;
+    pend &= pend - 1;
+    const int j = bit >> 3, w = bit >> 2, e = bit & 3;
+    const int q = 2 * (w & 1) + (e >> 1);   // component of v[j] holding the value
+    float sc = scale[0];
+    uint32_t pair = v[0].x;
+#pragma unroll
+    for (int jj = 0; jj < kQuantUnroll; ++jj) {
+      sc = j == jj ? scale[jj] : sc;
+      pair = (j == jj && q == 0) ? v[jj].x : pair;
+      pair = (j == jj && q == 1) ? v[jj].y : pair;
+      pair = (j == jj && q == 2) ? v[jj].z : pair;
+      pair = (j == jj && q == 3) ? v[jj].w : pair;
+    }
+    const uint32_t c = e4m3_code_exact((e & 1) ? bf16_hi(pair) : bf16_lo(pair), sc);
+#pragma unroll
+    for (int jj = 0; jj < kQuantUnroll; ++jj)
+#pragma unroll
+      for (int ii = 0; ii < 2; ++ii)
+        if (w == 2 * jj + ii) codes[jj][ii] = (codes[jj][ii] & ~(0xffu << (8 * e))) | (c << (8 * e));
+  }
+}
 
 __global__ void __launch_bounds__(256) k_quant_fp8(Geo g, const uint16_t* __restrict__ x, uint8_t* __restrict__ xq) {
   const int nb = g.H / 128;
-  const int64_t nblk = (int64_t)g.N * g.T * nb;
+  const int upr = (nb + 2 * kQuantUnroll - 1) / (2 * kQuantUnroll);   // warp units per row
+  const int64_t units = (int64_t)g.N * g.T * upr;
   const int lane = threadIdx.x & 31;
   const int sub = lane & 15;
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   pdl_wait();
-  for (int64_t b0 = warp * 2 * kQuantUnroll; b0 < nblk; b0 += nwarps * 2 * kQuantUnroll) {  // warp-uniform
-    uint4 v[kQuantUnroll];
+  for (int64_t u = warp; u < units; u += nwarps) {   // warp-uniform
+    const int64_t row = units <= INT32_MAX ? (int64_t)((uint32_t)u / (uint32_t)upr) : u / upr;
+    const int bbase = (int)(u - row * upr) * 2 * kQuantUnroll + (lane >> 4);   // block of j = 0
+    uint32_t codes[kQuantUnroll][2];
+    float scale[kQuantUnroll];
+    quant_unit(x + row * g.H + sub * 8, bbase, nb, codes, scale);
+    uint8_t* qr = xq + row * g.B;
 #pragma unroll
     for (int j = 0; j < kQuantUnroll; ++j) {
-      const int64_t blk = b0 + 2 * j + (lane >> 4);
-      v[j] = make_uint4(0, 0, 0, 0);
-      if (blk < nblk) {
-        const int64_t row = blk / nb;
-        v[j] = ld_stream16(x + row * g.H + (blk - row * nb) * 128 + sub * 8);
+      const int b = bbase + 2 * j;
+      if (b < nb) {
+        uint32_t* dst = reinterpret_cast<uint32_t*>(qr + b * 128 + sub * 8);
+        dst[0] = codes[j][0];
+        dst[1] = codes[j][1];
+        if (sub == 0) *reinterpret_cast<float*>(qr + g.H + 4 * b) = scale[j];
       }
     }
+  }
+  pdl_trigger();
+}
+
+// Quantisation fused into the pack: a warp unit quantises its blocks of a token row once, in
+// registers, and writes them into the R rows fan[token][k] of dst (send rows, or receive rows
+// when pushing), so the fp8 rows are never staged in HBM. The bytes each row gets are those
+// moe_quantize_fp8_b128 writes. W8: rows are 8-byte aligned (8-byte code stores).
+template <bool W8>
+__global__ void __launch_bounds__(256) k_quant_pack(Geo g, const uint16_t* __restrict__ x,
+                                                    const int32_t* __restrict__ fan, uint8_t* __restrict__ dst) {
+  const int nb = g.H / 128;
+  const int upr = (nb + 2 * kQuantUnroll - 1) / (2 * kQuantUnroll);
+  const int64_t units = (int64_t)g.N * g.T * upr;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane & 15;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  pdl_wait();
+  for (int64_t u = warp; u < units; u += nwarps) {   // warp-uniform
+    const int64_t row = units <= INT32_MAX ? (int64_t)((uint32_t)u / (uint32_t)upr) : u / upr;
+    const int bbase = (int)(u - row * upr) * 2 * kQuantUnroll + (lane >> 4);
+    const int32_t* fr = fan + row * g.R;
+    const int myp = lane < g.R ? __ldg(fr + lane) : -1;   // rows of pairs 0..31 (R > 32: loaded)
+    uint32_t codes[kQuantUnroll][2];
+    float scale[kQuantUnroll];
+    quant_unit(x + row * g.H + sub * 8, bbase, nb, codes, scale);
+#pragma unroll 1
+    for (int k = 0; k < g.R; ++k) {
+      const int p = k < 32 ? __shfl_sync(kFull, myp, k) : __ldg(fr + k);
+      if (p < 0) continue;
+      uint8_t* dr = dst + (int64_t)p * g.B;
 #pragma unroll
-    for (int j = 0; j < kQuantUnroll; ++j) {
-      const int64_t blk = b0 + 2 * j + (lane >> 4);
-      const float f[8] = {bf16_lo(v[j].x), bf16_hi(v[j].x), bf16_lo(v[j].y), bf16_hi(v[j].y),
-                          bf16_lo(v[j].z), bf16_hi(v[j].z), bf16_lo(v[j].w), bf16_hi(v[j].w)};
-      float amax = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
-#pragma unroll
-      for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o, 16));
-      const float scale = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
-      uint32_t w[2];
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
-            make_float2(__fdiv_rn(f[4 * i + 0], scale), __fdiv_rn(f[4 * i + 1], scale)), __NV_SATFINITE, __NV_E4M3);
-        const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-            make_float2(__fdiv_rn(f[4 * i + 2], scale), __fdiv_rn(f[4 * i + 3], scale)), __NV_SATFINITE, __NV_E4M3);
-        w[i] = (uint32_t)lo | ((uint32_t)hi << 16);
-      }
-      if (blk < nblk) {
-        const int64_t row = blk / nb;
-        const int b = (int)(blk - row * nb);
-        uint8_t* qr = xq + row * g.B;
-        uint32_t* dst = reinterpret_cast<uint32_t*>(qr + b * 128 + sub * 8);
-        dst[0] = w[0];
-        dst[1] = w[1];
-        if (sub == 0) *reinterpret_cast<float*>(qr + g.H + 4 * b) = scale;
+      for (int j = 0; j < kQuantUnroll; ++j) {
+        const int b = bbase + 2 * j;
+        if (b < nb) {
+          uint8_t* c = dr + b * 128 + sub * 8;
+          if (W8) {
+            *reinterpret_cast<uint2*>(c) = make_uint2(codes[j][0], codes[j][1]);
+          } else {
+            reinterpret_cast<uint32_t*>(c)[0] = codes[j][0];
+            reinterpret_cast<uint32_t*>(c)[1] = codes[j][1];
+          }
+          if (sub == 0) *reinterpret_cast<float*>(dr + g.H + 4 * b) = scale[j];
+        }
       }
     }
   }
@@ -85,9 +278,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 // y = bf16(float(code) * scale) for two codes (low byte first).
 __device__ __forceinline__ uint32_t dequant2(uint16_t codes, float scale) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(codes, __NV_E4M3);
-  const float lo = __half2float(__half(__half_raw{h.x}));
-  const float hi = __half2float(__half(__half_raw{h.y}));
+  const uint32_t h = e4m3x2_to_f16x2(codes);
+  const float lo = __half2float(__ushort_as_half((unsigned short)(h & 0xffffu)));
+  const float hi = __half2float(__ushort_as_half((unsigned short)(h >> 16)));
   return pack_bf16x2(__fmul_rn(lo, scale), __fmul_rn(hi, scale));
 }
 
@@ -436,13 +629,27 @@ cudaError_t launch_combine_sum(const Geo& g, const moe_layout_t* lay, const uint
 }
 
 cudaError_t launch_quant_fp8(const Geo& g, const uint16_t* x, uint8_t* xq, Ctx& c) {
-  const int64_t nblk = (int64_t)g.N * g.T * (g.H / 128);
-  if (nblk == 0) return cudaSuccess;
-  int64_t blocks = (nblk + 16 * kQuantUnroll - 1) / (16 * kQuantUnroll);  // 8 warps x 2 x unroll blocks per CTA
+  const int64_t upr = (g.H / 128 + 2 * kQuantUnroll - 1) / (2 * kQuantUnroll);
+  const int64_t units = (int64_t)g.N * g.T * upr;   // one warp unit: 2 x kQuantUnroll blocks of a row
+  if (units == 0) return cudaSuccess;
+  int64_t blocks = (units + 7) / 8;                 // 8 warps per CTA
   const int64_t maxb = (int64_t)c.num_sms * 8;
   if (blocks > maxb) blocks = maxb;
   LaunchScope ls(c, MOE_K_QUANT_FP8);
   return launch_kernel(k_quant_fp8, dim3((unsigned)blocks), dim3(256), 0, c, g, x, xq);
+}
+
+cudaError_t launch_quant_pack(const Geo& g, const int32_t* fan, const uint16_t* x, uint8_t* dst, Ctx& c) {
+  const int64_t upr = (g.H / 128 + 2 * kQuantUnroll - 1) / (2 * kQuantUnroll);
+  const int64_t units = (int64_t)g.N * g.T * upr;
+  if (units == 0) return cudaSuccess;
+  int64_t blocks = (units + 7) / 8;
+  const int64_t maxb = (int64_t)c.num_sms * 8;
+  if (blocks > maxb) blocks = maxb;
+  LaunchScope ls(c, MOE_K_QUANT_PACK);
+  if (g.B % 8 == 0)
+    return launch_kernel(k_quant_pack<true>, dim3((unsigned)blocks), dim3(256), 0, c, g, x, fan, dst);
+  return launch_kernel(k_quant_pack<false>, dim3((unsigned)blocks), dim3(256), 0, c, g, x, fan, dst);
 }
 
 cudaError_t launch_dequant_fp8(const Geo& g, const moe_layout_t* lay, const uint8_t* exq, const float* exs,

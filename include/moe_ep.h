@@ -86,7 +86,8 @@ typedef enum {
     MOE_K_COMBINE_PARTIAL = 13, /* expert-side partial sums, one row per (token, rank) */
     MOE_K_COMBINE_SUM = 14,    /* source-side sum of the partial rows -> bf16 */
     MOE_K_DISPATCH_SPLIT = 15, /* split-phase dispatch: push, signal, wait, shuffle in one launch */
-    MOE_K_NUM = 16
+    MOE_K_QUANT_PACK = 16,     /* fp8 quantisation fused into the pack */
+    MOE_K_NUM = 17
 } moe_kernel_id;
 
 /* Optional per-kernel timing. When moe_layout_t.prof is non-NULL, every kernel the library
@@ -116,6 +117,10 @@ typedef struct {
  * not used and may be NULL). The receive, grouped and combine buffers hold exactly what
  * they hold without the flag; the per-peer write step is fused away. */
 #define MOE_FLAG_DIRECT_PUSH 0x8u
+/* fp8 payload in moe_forward: quantise into d_xq with moe_quantize_fp8_b128 and dispatch
+ * those rows (two kernels), instead of the default moe_quantize_dispatch_send, which
+ * quantises inside the pack and leaves d_xq unwritten. Same receive and grouped contents. */
+#define MOE_FLAG_STAGED_QUANT 0x10u
 #define MOE_FLAG_NO_PDL 0x2u    /* launch without programmatic dependent launch (by default
                                    each kernel may be scheduled while its predecessor in the
                                    stream drains; it waits for it before touching memory) */
@@ -237,6 +242,17 @@ moe_status moe_quantize_fp8_b128(const moe_dims *dims, const uint16_t *d_x, uint
  * d_recv [N][RB][B]. Receive rows at or beyond rtot[d] are not written. Two kernels. */
 moe_status moe_dispatch_send(const moe_dims *dims, const moe_layout_t *lay, const void *d_x, void *d_send,
                              void *d_recv, void *stream);
+
+/* Quantisation fused into dispatch send (section "Evaluation": block-scaled fp8 dispatch;
+ * section "Dispatch and combine": the sender packs tokens for single writes per peer):
+ * for an fp8 payload, each bf16 token row of d_x [N][T][H] is quantised once in registers
+ * (the rule of moe_quantize_fp8_b128) and its B-byte fp8 row written to the send rows of
+ * its pairs, then scattered as by moe_dispatch_send; with MOE_FLAG_DIRECT_PUSH it is
+ * written straight into the owners' receive rows (d_send unused, may be NULL). d_recv
+ * ends up byte-identical to moe_quantize_fp8_b128 followed by moe_dispatch_send; no
+ * quantised copy of d_x is kept. A bf16 payload is MOE_ERR_INVALID_ARG. */
+moe_status moe_quantize_dispatch_send(const moe_dims *dims, const moe_layout_t *lay, const uint16_t *d_x,
+                                      void *d_send, void *d_recv, void *stream);
 
 /* Dispatch send that allocates nothing, for callers that cannot call cudaMalloc (code
  * under a fixed memory plan made before serving, allocator hooks that must not re-enter the

@@ -18,10 +18,11 @@ def to_dev(a: np.ndarray, dtype=None) -> torch.Tensor:
 
 
 def run_gpu(wl: workloads.Workload, inp: dict, flags: int = 0, poison: bool = True, split: bool = False,
-            withhold_slice: int = -1, **kw):
+            withhold_slice: int = -1, fused_quant: bool = False, **kw):
     """Runs every step separately on the GPU; returns (MoeEP, host copies of every buffer).
     With split, dispatch is the one-launch split-phase dispatch (direct push) instead of
-    dispatch send + receive; withhold_slice is passed to it."""
+    dispatch send + receive; withhold_slice is passed to it. With fused_quant (fp8), the
+    quantisation runs inside the pack (the quantised token rows are not kept)."""
     from combine_routing_count_gb300 import MoeEP
     ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, wl.payload, flags=flags, separate_expert_y=True, **kw)
     if poison:
@@ -34,14 +35,18 @@ def run_gpu(wl: workloads.Workload, inp: dict, flags: int = 0, poison: bool = Tr
     w = to_dev(inp["w"])
     ep.layout_step(idx)
     res = {}
-    if wl.payload == "fp8":
-        ep.quantize(x)
-        x = ep.xq
-    if split:
-        ep.dispatch_split(x, withhold_slice)
-    else:
-        ep.dispatch_send(x)
+    if fused_quant:
+        ep.quantize_dispatch_send(x)
         ep.dispatch_recv()
+    else:
+        if wl.payload == "fp8":
+            ep.quantize(x)
+            x = ep.xq
+        if split:
+            ep.dispatch_split(x, withhold_slice)
+        else:
+            ep.dispatch_send(x)
+            ep.dispatch_recv()
     ep.expert_identity()
     ep.combine_send()
     ep.combine_recv(w)
@@ -63,7 +68,7 @@ def u16(t: torch.Tensor) -> np.ndarray:
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-def compare_all(orc, wl, inp, res, check_poison=True, push=False):
+def compare_all(orc, wl, inp, res, check_poison=True, push=False, fused_quant=False):
     """Bit-exact comparison of every buffer's used rows with the oracle; padding untouched.
     With push (direct-push mode) the send and combine-send buffers must stay untouched."""
     N, T, H, E, R, L = wl.N, wl.T, wl.H, wl.E, wl.R, wl.L
@@ -77,7 +82,7 @@ def compare_all(orc, wl, inp, res, check_poison=True, push=False):
     pos, slot = lay_o["pos"], lay_o["slot"]
     valid = pos >= 0
     kept = slot >= 0
-    if wl.payload == "fp8":
+    if wl.payload == "fp8" and not fused_quant:
         np.testing.assert_array_equal(u8(res["xq"]), o["xq"], err_msg="fp8 quantised rows")
     # send rows of every valid pair
     send = u8(res["send"])

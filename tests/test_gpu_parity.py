@@ -174,7 +174,7 @@ def test_profiling_events_bracket_each_kernel():
     ep.forward(to_dev(inp["x"]).view(torch.bfloat16), to_dev(inp["idx"]), to_dev(inp["w"]))
     torch.cuda.synchronize()
     names = [KERNEL_NAMES[prof.kernel[i]] for i in range(prof.n)]
-    assert names == ["route_count", "route_scan", "layout_maps", "quant_fp8", "pack", "scatter", "unpack",
+    assert names == ["route_count", "route_scan", "layout_maps", "quant_pack", "scatter", "unpack",
                      "expert", "combine_pack", "combine_scatter", "combine_reduce"]
     for i in range(prof.n):
         assert evs[2 * i].elapsed_time(evs[2 * i + 1]) >= 0.0
@@ -257,3 +257,87 @@ def test_split_dispatch_rejects_bad_withhold_slice():
                                       ep.recv.data_ptr(), ep.expert_x.data_ptr(), None, bad, None)
         assert rc == 1
     assert lib().moe_launch_count() == n0
+
+
+def _quant_boundary_rows(H: int) -> np.ndarray:
+    """bf16 rows whose 128-blocks put x / scale on the e4m3 rounding boundaries: exact ties at
+    the normal-range midpoints and at the subnormal-range odd multiples of 2^-10 (scales 1.5
+    and 1.25, exact in fp32, so the quotients are exact), their e4m3 neighbours, zeros of
+    both signs, subnormal scales, and a wide log-normal spread of magnitudes."""
+    rng = np.random.default_rng(77)
+    mids = [(1 + (2 * j + 1) / 16) * 2.0 ** e for e in range(-6, 9) for j in range(8)]
+    mids += [(2 * k + 1) * 2.0 ** -10 for k in range(8)]                       # subnormal-range ties
+    vals = mids + [(1 + j / 8) * 2.0 ** e for e in range(-6, 9) for j in range(8)] + [m * 2.0 ** -9 for m in range(8)]
+    rows = []
+    for scale in (1.5, 1.25):
+        cand = np.array([s * v * scale for v in vals for s in (1.0, -1.0)], np.float32)
+        cand = cand[np.abs(cand) <= 448 * scale]
+        exact = workloads.from_bf16_bits(workloads.to_bf16_bits(cand)) == cand
+        cand = cand[exact]
+        nblk = -(-len(cand) // 127)
+        blocks = np.zeros((nblk, 128), np.float32)
+        flat = np.concatenate([cand, np.zeros(nblk * 127 - len(cand), np.float32)])
+        blocks[:, 1:] = flat.reshape(nblk, 127)
+        blocks[:, 0] = 448 * scale                                              # amax -> this scale
+        rows.append(blocks.reshape(-1))
+    z = np.zeros(128, np.float32)
+    z[::2] = -0.0
+    rows.append(z)                                                              # amax 0 -> scale 1
+    tiny = (rng.standard_normal(128 * 4) * 1e-37).astype(np.float32)            # subnormal scales
+    rows.append(tiny)
+    spread = rng.standard_normal(128 * 2048) * np.exp(rng.normal(0, 12, size=(2048, 1))).repeat(128, 1).reshape(-1)
+    rows.append(np.clip(spread, -3e38, 3e38).astype(np.float32))
+    flat = np.concatenate(rows)
+    flat = np.concatenate([flat, np.zeros(-len(flat) % H, np.float32)])
+    return workloads.to_bf16_bits(flat).reshape(1, -1, H)
+
+
+def test_quantize_fp8_rounding_boundaries(orc):
+    from combine_routing_count_gb300 import MoeEP
+    H = 1024
+    xb = _quant_boundary_rows(H)
+    T = xb.shape[1]
+    ep = MoeEP(1, T, H, 2, 1, payload="fp8")
+    ep.quantize(to_dev(xb).view(torch.bfloat16))
+    code, _ = ep.status()
+    assert code == 0
+    np.testing.assert_array_equal(u8(ep.xq.cpu()), orc.quantize_fp8(xb))
+
+
+FP8_CASES = [c for c in CASES if c.payload == "fp8"] + [
+    W("fp8-H1152-R12", 5, 17, 1152, 20, 12, "fp8", "zipf", 160),           # 9 blocks: a ragged warp unit
+    W("fp8-skew", 4, 40, 2048, 32, 8, "fp8", "skew0", 161),
+]
+
+
+@pytest.mark.parametrize("flags", [0, 8], ids=["scatter", "push"])
+@pytest.mark.parametrize("wl", FP8_CASES, ids=lambda w: w.name)
+def test_fused_quantize_dispatch_matches_oracle(orc, wl, flags):
+    """Quantisation inside the pack: send, receive and grouped rows (codes and scales) are
+    those of the staged path, bit for bit."""
+    inp = workloads.make_inputs(wl)
+    _, res = run_gpu(wl, inp, flags=flags, fused_quant=True)
+    compare_all(orc, wl, inp, res, push=bool(flags & 8), fused_quant=True)
+
+
+def test_fused_quantize_rejects_bf16_payload():
+    import ctypes
+    from combine_routing_count_gb300 import MoeEP, lib
+    ep = MoeEP(2, 4, 128, 4, 2)
+    x = torch.zeros((2, 4, 128), dtype=torch.bfloat16, device="cuda")
+    rc = lib().moe_quantize_dispatch_send(ctypes.byref(ep.dims), ctypes.byref(ep.layout), x.data_ptr(),
+                                          ep.send.data_ptr(), ep.recv.data_ptr(), None)
+    assert rc == 1
+
+
+def test_forward_fp8_staged_and_fused_agree(orc):
+    wl = W("fp8-forward", 8, 24, 7168, 64, 8, "fp8", "uniform", 162)
+    inp = workloads.make_inputs(wl)
+    from combine_routing_count_gb300 import MoeEP
+    o = orc.forward(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, wl.payload, inp["x"], inp["idx"], inp["w"])
+    for flags in (0, 0x10, 0x18):
+        ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, payload="fp8", flags=flags)
+        ep.forward(to_dev(inp["x"]).view(torch.bfloat16), to_dev(inp["idx"]), to_dev(inp["w"]))
+        code, _ = ep.status()
+        assert code == 0
+        np.testing.assert_array_equal(u16(ep.out.cpu()), o["out"], err_msg=f"flags {flags:#x}")
