@@ -15,9 +15,11 @@
 //    __match_any_sync groups plus a per-warp table in shared memory give each pair its
 //    rank among the chunk's pairs of the same expert in (token, slot) order —
 //    deterministic, unlike an atomic slot grab;
-//  - one CTA then turns the chunk table into chunk offsets and totals and runs every
-//    scan; the maps kernel adds a pair's chunk offset to its chunk-local rank. The three
-//    kernels chain with programmatic dependent launch.
+//  - the last chunk CTA of each source rank to finish (a completion counter, no waiting)
+//    sums that rank's chunk counts into cnt[s][.]; a grid of independent scan CTAs (one
+//    per source row, per 32-expert column tile and per destination) then runs every
+//    scan, and the maps kernel adds a pair's earlier-chunk counts to its chunk-local rank.
+//    The three kernels chain with programmatic dependent launch.
 #include <cuda_runtime.h>
 
 #include "internal.h"

@@ -17,8 +17,9 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 
 // Half a warp per 128-element block: each lane holds 8 bf16 values (one 16-byte load).
-// amax over the block by xor-shuffles inside the half warp; scale = amax / 448 (IEEE fp32
-// division; 1 when amax is 0); codes = e4m3(x / scale), round to nearest even, saturating.
+// amax over the block by xor-shuffles inside the half warp; scale = RN(amax / 448) (1 when
+// amax is 0); codes = e4m3(RN(x / scale)), round to nearest even, saturating: bit for bit the
+// fp32 division, computed without dividing (block_scale, quant_unit below).
 // Output row: H codes, then H/128 fp32 scales. 4-byte stores (rows are 4-byte aligned).
 // A warp takes kQuantUnroll pairs of blocks of one row per trip (one index division per
 // trip) and issues all their loads first.
