@@ -475,18 +475,27 @@ def run_ours(args):
     h_idx = torch.from_numpy(inp["idx"]).pin_memory()
     h_w = torch.from_numpy(inp["w"]).pin_memory()
     h_out = torch.empty((wl.N, wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
-    for _ in range(3):
-        ep.forward_host(h_x, h_idx, h_w, h_out, x, idx, w)
-    torch.cuda.synchronize()
-    e_start = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    e_end = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    for i in range(K):
-        flush.zero_()
-        e_start[i].record(stream)
-        ep.forward_host(h_x, h_idx, h_w, h_out, x, idx, w)
-        e_end[i].record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(statistics.fmean(s.elapsed_time(e) for s, e in zip(e_start, e_end)), dist, device)
+    def e2e_region():
+        for _ in range(3):
+            ep.forward_host(h_x, h_idx, h_w, h_out, x, idx, w)
+        torch.cuda.synchronize()
+        e_start = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        e_end = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        for i in range(K):
+            flush.zero_()
+            e_start[i].record(stream)
+            ep.forward_host(h_x, h_idx, h_w, h_out, x, idx, w)
+            e_end[i].record(stream)
+        torch.cuda.synchronize()
+        ok = bool(np.array_equal(h_out.view(torch.int16).numpy(), ep.out.cpu().view(torch.int16).numpy()))
+        return max_over_ranks(statistics.fmean(s.elapsed_time(e) for s, e in zip(e_start, e_end)), dist, device), ok
+
+    # Default: the kernels read the pinned host inputs and write the host output directly
+    # (NVLink-C2C); then the same with copy engines staging through device buffers.
+    e2e_ms, e2e_same = e2e_region()
+    ep.layout.flags |= 0x20
+    e2e_copy_ms, _ = e2e_region()
+    ep.layout.flags &= ~0x20
     h2d = inp["x"].nbytes + inp["idx"].nbytes + inp["w"].nbytes
     d2h = wl.N * wl.T * wl.H * 2
 
@@ -525,7 +534,12 @@ def run_ours(args):
                                          "push rows, signal per (destination, source) slice, wait "
                                          "(bounded), shuffle into the grouped rows"},
         "e2e": {"value": round(tokens / (e2e_ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(e2e_ms, 4),
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "path": "moe_forward_host (C ABI)"},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "path": "moe_forward_host (C ABI): kernels read pinned host inputs and write the host output "
+                        "over the host link",
+                "out_equals_device_path": e2e_same,
+                "copy_engine": {"value": round(tokens / (e2e_copy_ms * 1e-3), 1), "ms_per_step": round(e2e_copy_ms, 4),
+                                "path": "MOE_FLAG_HOST_STAGED: cudaMemcpyAsync in and out around the pass"}},
         "identity_expert": None if expert_ms is None else {
             "ms_per_step": round(expert_ms, 4), "kernel_us": round(statistics.fmean(per_kernel["expert"]) * 1e3, 2),
             "note": "fp8 dequantisation standing in for the grouped GEMM; excluded from ms_per_step and value"},

@@ -135,6 +135,20 @@ WsPlan ws_plan(const Geo& g) {
   return w;
 }
 
+// The device address of pinned host memory p (cudaHostAlloc / cudaHostRegister), if the
+// current device can address it.
+bool host_mapped(const void* p, void** dev) {
+  if (!p) return false;
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+    cudaGetLastError();   // not a CUDA-known pointer: clear the error
+    return false;
+  }
+  if (attr.type != cudaMemoryTypeHost || !attr.devicePointer) return false;
+  *dev = attr.devicePointer;
+  return true;
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -400,6 +414,19 @@ moe_status moe_forward_host(const moe_dims* dims, const moe_layout_t* lay, const
   const size_t xb = (size_t)g.N * g.T * g.H * 2, pb = (size_t)g.P * 4;
   if ((xb && (!h_x || !h_out || !b->x || !b->out)) || (pb && (!h_idx || !h_w || !b->idx || !b->w)))
     return MOE_ERR_INVALID_ARG;
+  if (!layout_ok(lay)) return MOE_ERR_INVALID_ARG;
+  if (!(lay->flags & MOE_FLAG_HOST_STAGED)) {
+    // Device-accessible host memory: run the pass on it directly.
+    void *dx = nullptr, *didx = nullptr, *dw = nullptr, *dout = nullptr;
+    if (host_mapped(h_x, &dx) && host_mapped(h_idx, &didx) && host_mapped(h_w, &dw) && host_mapped(h_out, &dout)) {
+      moe_buffers_t m = *b;
+      m.x = static_cast<uint16_t*>(dx);
+      m.idx = static_cast<int32_t*>(didx);
+      m.w = static_cast<float*>(dw);
+      m.out = static_cast<uint16_t*>(dout);
+      return moe_forward(dims, lay, &m, stream);
+    }
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (xb && cudaMemcpyAsync(b->x, h_x, xb, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (pb && cudaMemcpyAsync(b->idx, h_idx, pb, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;

@@ -433,12 +433,18 @@ cudaError_t launch_move(MoveKind kind, const Geo& g, const moe_layout_t* lay, co
   const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
   const bool rowB16 = (g.B % 16) == 0;  // bf16 rows always; fp8 rows when H % 512 == 0
   if (kind == kMovePack || kind == kMovePackPush) {
-    // Split token rows into column chunks until there are ~16 units per SM (chunks of at
-    // least 1 KB, 16-byte multiples), so that pack has parallelism beyond one unit per token.
+    // Split token rows into column chunks (16-byte multiples, at most 8 per row) of at least
+    // 2 KB, or 1 KB while there are fewer than ~16 units per SM: smaller units balance the
+    // warps better (measured: 3.5 KB chunks of 14 KB rows and 2 KB chunks of 8 KB rows were
+    // the fastest) and give small batches parallelism beyond one unit per token.
     const int64_t tokens = (int64_t)g.N * g.T;
-    while (a.chunks < 8 && tokens * a.chunks < 16LL * c.num_sms && g.B % (16 * 2 * a.chunks) == 0 &&
-           g.B / (2 * a.chunks) >= 1024)
-      a.chunks *= 2;
+    while (a.chunks < 8 && g.B % (16 * 2 * a.chunks) == 0) {
+      const int64_t half = g.B / (2 * a.chunks);
+      if (half >= 2048 || (half >= 1024 && tokens * a.chunks < 16LL * c.num_sms))
+        a.chunks *= 2;
+      else
+        break;
+    }
     a.chunk_bytes = (uint32_t)(g.B / a.chunks);
     a.units = tokens * a.chunks;
   } else {

@@ -121,6 +121,9 @@ typedef struct {
  * those rows (two kernels), instead of the default moe_quantize_dispatch_send, which
  * quantises inside the pack and leaves d_xq unwritten. Same receive and grouped contents. */
 #define MOE_FLAG_STAGED_QUANT 0x10u
+/* moe_forward_host: copy host inputs into the device buffers and the output back with copy
+ * engines, even when the host buffers are device-accessible. */
+#define MOE_FLAG_HOST_STAGED 0x20u
 #define MOE_FLAG_NO_PDL 0x2u    /* launch without programmatic dependent launch (by default
                                    each kernel may be scheduled while its predecessor in the
                                    stream drains; it waits for it before touching memory) */
@@ -340,15 +343,20 @@ moe_status moe_combine_send_partial(const moe_dims *dims, const moe_layout_t *la
 moe_status moe_combine_recv_partial(const moe_dims *dims, const moe_layout_t *lay, const uint16_t *d_cpart,
                                     uint16_t *d_out, void *stream);
 
-/* One whole pass on device-resident buffers: moe_layout, [moe_quantize_fp8_b128],
- * moe_dispatch_send, moe_dispatch_recv, moe_expert_identity, moe_combine_send,
- * moe_combine_recv. Returns the first error. */
+/* One whole pass: moe_layout, moe_quantize_dispatch_send (fp8; or moe_quantize_fp8_b128 +
+ * moe_dispatch_send with MOE_FLAG_STAGED_QUANT) or moe_dispatch_send (bf16),
+ * moe_dispatch_recv, moe_expert_identity, moe_combine_send, moe_combine_recv. Returns the
+ * first error. bufs->x, idx, w and out may also be device-accessible host memory. */
 moe_status moe_forward(const moe_dims *dims, const moe_layout_t *lay, const moe_buffers_t *bufs, void *stream);
 
-/* moe_forward with host inputs and output: cudaMemcpyAsync of h_x [N][T][H] bf16,
- * h_idx [N][T][R] and h_w [N][T][R] into bufs->x/idx/w, the pass, then cudaMemcpyAsync of
- * bufs->out into h_out [N][T][H]. Asynchronous: the caller synchronises `stream` before
- * reading h_out; host buffers should be pinned. */
+/* moe_forward with host inputs h_x [N][T][H] bf16, h_idx [N][T][R], h_w [N][T][R] and host
+ * output h_out [N][T][H]. When all four are pinned host memory that the device can address
+ * (cudaHostAlloc / cudaHostRegister; over NVLink-C2C on Grace-Blackwell), the kernels read
+ * the inputs and write the output there directly: each input byte crosses the host link
+ * once, when the kernel that needs it loads it, and bufs->x/idx/w/out are not used.
+ * Otherwise, or with MOE_FLAG_HOST_STAGED, cudaMemcpyAsync copies the inputs into
+ * bufs->x/idx/w, the pass runs, and bufs->out is copied into h_out. Asynchronous: the caller
+ * synchronises `stream` before reading h_out. */
 moe_status moe_forward_host(const moe_dims *dims, const moe_layout_t *lay, const moe_buffers_t *bufs,
                             const uint16_t *h_x, const int32_t *h_idx, const float *h_w, uint16_t *h_out,
                             void *stream);

@@ -126,15 +126,21 @@ def test_invalid_arguments_launch_nothing():
     assert L.moe_launch_count() == n0
 
 
-def test_forward_host_matches_device_path(orc):
-    wl = W("host-e2e", 4, 29, 2048, 16, 4, "bf16", "zipf", 120)
+@pytest.mark.parametrize("mode", ["mapped", "staged", "pageable"])
+@pytest.mark.parametrize("payload", ["bf16", "fp8"])
+def test_forward_host_matches_device_path(orc, mode, payload):
+    """Host inputs and output: pinned memory read and written by the kernels directly
+    (default), copied by copy engines (MOE_FLAG_HOST_STAGED), or pageable (copied)."""
+    wl = W("host-e2e", 4, 29, 2048, 16, 4, payload, "zipf", 120)
     inp = workloads.make_inputs(wl)
     from combine_routing_count_gb300 import MoeEP
-    ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, alias_buffers=True)
-    h_x = torch.from_numpy(inp["x"]).view(torch.bfloat16).pin_memory()
-    h_idx = torch.from_numpy(inp["idx"]).pin_memory()
-    h_w = torch.from_numpy(inp["w"]).pin_memory()
-    h_out = torch.empty((wl.N, wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
+    ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, payload=payload, alias_buffers=(payload == "bf16"),
+               flags=0x20 if mode == "staged" else 0)
+    pin = (lambda t: t) if mode == "pageable" else (lambda t: t.pin_memory())
+    h_x = pin(torch.from_numpy(inp["x"]).view(torch.bfloat16))
+    h_idx = pin(torch.from_numpy(inp["idx"]))
+    h_w = pin(torch.from_numpy(inp["w"]))
+    h_out = pin(torch.empty((wl.N, wl.T, wl.H), dtype=torch.bfloat16))
     x = torch.empty_like(h_x, device="cuda")
     idx = torch.empty_like(h_idx, device="cuda")
     w = torch.empty_like(h_w, device="cuda")
@@ -142,7 +148,7 @@ def test_forward_host_matches_device_path(orc):
         ep.forward_host(h_x, h_idx, h_w, h_out, x, idx, w)
         code, _ = ep.status()
         assert code == 0
-        o = orc.forward(wl.N, wl.T, wl.H, wl.E, wl.R, 0, "bf16", inp["x"], inp["idx"], inp["w"])
+        o = orc.forward(wl.N, wl.T, wl.H, wl.E, wl.R, 0, payload, inp["x"], inp["idx"], inp["w"])
         np.testing.assert_array_equal(u16(h_out), o["out"])
 
 
