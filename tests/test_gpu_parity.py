@@ -347,3 +347,34 @@ def test_forward_fp8_staged_and_fused_agree(orc):
         code, _ = ep.status()
         assert code == 0
         np.testing.assert_array_equal(u16(ep.out.cpu()), o["out"], err_msg=f"flags {flags:#x}")
+
+
+@pytest.mark.parametrize("flags", [0, 4, 8], ids=["auto", "tma", "push"])
+@pytest.mark.parametrize("payload", ["bf16", "fp8"])
+def test_forward_replays_under_cuda_graph(orc, flags, payload):
+    """The whole pass captures into a CUDA graph (no synchronisation or allocation on the
+    path; programmatic dependent launches become graph edges) and replays on new inputs
+    written into the captured tensors."""
+    from combine_routing_count_gb300 import MoeEP
+    wl = W("graph", 4, 64, 2048, 32, 8, payload, "uniform", 170)
+    ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, payload=payload, alias_buffers=(payload == "bf16"), flags=flags)
+    inp = workloads.make_inputs(wl)
+    x, idx, w = to_dev(inp["x"]).view(torch.bfloat16), to_dev(inp["idx"]), to_dev(inp["w"])
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        ep.forward(x, idx, w)          # first launches set kernel attributes outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        ep.forward(x, idx, w)
+    for seed in (171, 172):
+        inp = workloads.make_inputs(wl.replace(seed=seed))
+        x.copy_(to_dev(inp["x"]).view(torch.bfloat16))
+        idx.copy_(to_dev(inp["idx"]))
+        w.copy_(to_dev(inp["w"]))
+        graph.replay()
+        code, _ = ep.status()
+        assert code == 0
+        o = orc.forward(wl.N, wl.T, wl.H, wl.E, wl.R, 0, payload, inp["x"], inp["idx"], inp["w"])
+        np.testing.assert_array_equal(u16(ep.out.cpu()), o["out"], err_msg=f"seed {seed}")
