@@ -64,7 +64,7 @@ struct LaunchScope {
 // device; `cache` holds the largest value set so far for each of 64 devices.
 template <typename K>
 inline cudaError_t ensure_dyn_smem(K kernel, int device, size_t bytes, std::atomic<int>* cache) {
-  if (bytes <= 48 * 1024) return cudaSuccess;
+  if (bytes + 1024 <= 48 * 1024) return cudaSuccess;   // room for up to 1 KB of static shared memory
   std::atomic<int>& c = cache[device & 63];
   if (c.load() >= (int)bytes) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);

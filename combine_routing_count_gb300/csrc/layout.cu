@@ -320,6 +320,8 @@ int64_t layout_scratch_tgroups_offset(const Geo& g) { return layout_scratch_done
 int64_t layout_scratch_arrive_offset(const Geo& g) { return layout_scratch_tgroups_offset(g) + (int64_t)g.N * g.T; }
 
 
+std::atomic<int> g_count_smem[64];   // per device: dynamic shared memory k_route_count is set up for
+
 cudaError_t launch_layout(const Geo& g, const int32_t* idx, const moe_layout_t* lay, Ctx& c) {
   LayoutArgs a;
   a.idx = idx;
@@ -345,8 +347,10 @@ cudaError_t launch_layout(const Geo& g, const int32_t* idx, const moe_layout_t* 
 
   cudaError_t e = cudaSuccess;
   if (a.nch > 0) {
+    const size_t smem = (size_t)4 * (kChunk / 32) * g.E;   // per-warp tables: 48 KB at E = 1536
+    if ((e = ensure_dyn_smem(k_route_count, c.device, smem, g_count_smem)) != cudaSuccess) return e;
     LaunchScope ls(c, MOE_K_ROUTE_COUNT);
-    e = launch_kernel(k_route_count, dim3(a.nch, g.N), dim3(kChunk), (size_t)4 * (kChunk / 32) * g.E, c, g, a);
+    e = launch_kernel(k_route_count, dim3(a.nch, g.N), dim3(kChunk), smem, c, g, a);
     if (e != cudaSuccess) return e;
   }
   {

@@ -378,3 +378,19 @@ def test_forward_replays_under_cuda_graph(orc, flags, payload):
         assert code == 0
         o = orc.forward(wl.N, wl.T, wl.H, wl.E, wl.R, 0, payload, inp["x"], inp["idx"], inp["w"])
         np.testing.assert_array_equal(u16(ep.out.cpu()), o["out"], err_msg=f"seed {seed}")
+
+
+LIMIT_CASES = [
+    W("E1536-max", 8, 64, 256, 1536, 8, "bf16", "uniform", 180),      # largest E: 48 KB count tables
+    W("N1536-L1", 1536, 2, 128, 1536, 2, "bf16", "uniform", 181),     # 1536 ranks, one expert each
+    W("R40", 4, 16, 256, 64, 40, "bf16", "uniform", 182),             # R > 32: pair data past one warp
+    W("fp8-E1536-zipf", 8, 32, 1024, 1536, 8, "fp8", "zipf", 183),
+]
+
+
+@pytest.mark.parametrize("flags", [0, 8], ids=["auto", "push"])
+@pytest.mark.parametrize("wl", LIMIT_CASES, ids=lambda w: w.name)
+def test_limits_match_oracle(orc, wl, flags):
+    inp = workloads.make_inputs(wl)
+    _, res = run_gpu(wl, inp, flags=flags)
+    compare_all(orc, wl, inp, res, push=bool(flags & 8))
