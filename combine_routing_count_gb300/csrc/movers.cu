@@ -53,13 +53,6 @@ struct Plan {
   int32_t p[kPackPrefetch];    // pack: global send rows of the token's pairs
 };
 
-template <int KIND>
-__host__ __device__ __forceinline__ uint32_t load_bytes(const Geo& g) {
-  if (KIND == kMovePack || KIND == kMovePackPush || KIND == kMoveScatter || KIND == kMoveUnpack)
-    return (uint32_t)g.B;
-  return (uint32_t)(2 * g.H);
-}
-
 // Bytes one unit moves per destination: one column chunk of a row (the whole row when
 // the move is not chunked).
 template <int KIND>
