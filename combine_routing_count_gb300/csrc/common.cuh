@@ -145,28 +145,4 @@ __device__ __forceinline__ void st16(void* p, const uint4& v) {
 __device__ __forceinline__ float bf16_lo(uint32_t packed) { return __uint_as_float(packed << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t packed) { return __uint_as_float(packed & 0xffff0000u); }
 
-// ---- packed fp32 pairs (sm_100+ f32x2): each lane rounded exactly as the scalar op ------
-
-// {lo, hi} as one 64-bit operand.
-__device__ __forceinline__ uint64_t f2_make(uint32_t lo_bits, uint32_t hi_bits) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo_bits), "r"(hi_bits));
-  return r;
-}
-__device__ __forceinline__ uint64_t f2_splat(float x) { return f2_make(__float_as_uint(x), __float_as_uint(x)); }
-// Two bf16 values packed low-first in a 32-bit word -> their exact fp32 pair.
-__device__ __forceinline__ uint64_t f2_from_bf16x2(uint32_t w) { return f2_make(w << 16, w & 0xffff0000u); }
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ float f2_lo(uint64_t a) { return __uint_as_float((uint32_t)a); }
-__device__ __forceinline__ float f2_hi(uint64_t a) { return __uint_as_float((uint32_t)(a >> 32)); }
-
 }  // namespace moe

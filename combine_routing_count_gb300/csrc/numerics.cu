@@ -334,34 +334,40 @@ __global__ void __launch_bounds__(256) k_dequant_fp8(Geo g, const int32_t* __res
   pdl_trigger();
 }
 
-// acc (eight fp32 sums as four packed pairs) += w * v, v a 16-byte vector of eight bf16;
-// product and sum are rounded separately in each lane (RN), as in the scalar definition.
-__device__ __forceinline__ void acc_pair(uint64_t (&acc)[4], const uint4& v, uint64_t w2) {
-  acc[0] = f2_add(acc[0], f2_mul(w2, f2_from_bf16x2(v.x)));
-  acc[1] = f2_add(acc[1], f2_mul(w2, f2_from_bf16x2(v.y)));
-  acc[2] = f2_add(acc[2], f2_mul(w2, f2_from_bf16x2(v.z)));
-  acc[3] = f2_add(acc[3], f2_mul(w2, f2_from_bf16x2(v.w)));
+// acc (eight fp32 sums) += w * v, v a 16-byte vector of eight bf16: the product and the sum
+// rounded separately (RN), as in the definition. Scalar __fmul_rn / __fadd_rn, which are
+// never contracted into a fused multiply-add (the packed f32x2 multiply-then-add pair is:
+// measured on sm_103a, it gave the fma result).
+__device__ __forceinline__ void acc_pair(float (&acc)[8], const uint4& v, float w) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    acc[2 * i] = __fadd_rn(acc[2 * i], __fmul_rn(w, bf16_lo(u[i])));
+    acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __fmul_rn(w, bf16_hi(u[i])));
+  }
 }
 
 // acc += v (no weight).
-__device__ __forceinline__ void acc_add(uint64_t (&acc)[4], const uint4& v) {
-  acc[0] = f2_add(acc[0], f2_from_bf16x2(v.x));
-  acc[1] = f2_add(acc[1], f2_from_bf16x2(v.y));
-  acc[2] = f2_add(acc[2], f2_from_bf16x2(v.z));
-  acc[3] = f2_add(acc[3], f2_from_bf16x2(v.w));
-}
-
-__device__ __forceinline__ void acc_zero(uint64_t (&acc)[4]) {
+__device__ __forceinline__ void acc_add(float (&acc)[8], const uint4& v) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-  for (int i = 0; i < 4; ++i) acc[i] = 0ull;
+  for (int i = 0; i < 4; ++i) {
+    acc[2 * i] = __fadd_rn(acc[2 * i], bf16_lo(u[i]));
+    acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], bf16_hi(u[i]));
+  }
 }
 
-__device__ __forceinline__ void store_bf16x8(uint16_t* p, const uint64_t (&acc)[4]) {
+__device__ __forceinline__ void acc_zero(float (&acc)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+}
+
+__device__ __forceinline__ void store_bf16x8(uint16_t* p, const float (&acc)[8]) {
   uint4 o;
-  o.x = pack_bf16x2(f2_lo(acc[0]), f2_hi(acc[0]));
-  o.y = pack_bf16x2(f2_lo(acc[1]), f2_hi(acc[1]));
-  o.z = pack_bf16x2(f2_lo(acc[2]), f2_hi(acc[2]));
-  o.w = pack_bf16x2(f2_lo(acc[3]), f2_hi(acc[3]));
+  o.x = pack_bf16x2(acc[0], acc[1]);
+  o.y = pack_bf16x2(acc[2], acc[3]);
+  o.z = pack_bf16x2(acc[4], acc[5]);
+  o.w = pack_bf16x2(acc[6], acc[7]);
   st16(p, o);
 }
 
@@ -383,7 +389,7 @@ __global__ void __launch_bounds__(kReduceThreads) k_combine_reduce(Geo g, const 
   const bool act = col < ncol;
   const int lane = threadIdx.x & 31;
   const int64_t q0 = u * g.R;
-  uint64_t acc[4];
+  float acc[8];
   acc_zero(acc);
   pdl_wait();
   for (int k0 = 0; k0 < g.R; k0 += 32) {
@@ -415,7 +421,7 @@ __global__ void __launch_bounds__(kReduceThreads) k_combine_reduce(Geo g, const 
       }
 #pragma unroll
       for (int j = 0; j < 8; ++j)
-        if (rk[j] >= 0) acc_pair(acc, v[j], f2_splat(wk[j]));
+        if (rk[j] >= 0) acc_pair(acc, v[j], wk[j]);
     }
   }
   if (act) store_bf16x8(out + u * g.H + col * 8, acc);
@@ -519,13 +525,13 @@ __global__ void __launch_bounds__(kReduceThreads) k_combine_partial(Geo g, const
       v[p] = make_uint4(0, 0, 0, 0);
       if (act && p < n) v[p] = ld_stream16(y0 + (int64_t)s_row[p] * g.H);
     }
-    uint64_t acc[4];
+    float acc[8];
     acc_zero(acc);
     int j = 0;
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
       if (p >= n) break;
-      acc_pair(acc, v[p], f2_splat(s_w[p]));
+      acc_pair(acc, v[p], s_w[p]);
       if (s_last[p]) {
         if (act) store_bf16x8(out0 + (int64_t)j * g.H, acc);
         ++j;
@@ -534,7 +540,7 @@ __global__ void __launch_bounds__(kReduceThreads) k_combine_partial(Geo g, const
     }
   } else {
     for (int j = 0; j < pg.ngroups; ++j) {
-      uint64_t acc[4];
+      float acc[8];
       acc_zero(acc);
       for (int k0 = 0; k0 < g.R; k0 += 8) {
         uint4 v[8];
@@ -552,7 +558,7 @@ __global__ void __launch_bounds__(kReduceThreads) k_combine_partial(Geo g, const
           const int row = __shfl_sync(kFull, pg.row, k);
           const int jm = __shfl_sync(kFull, pg.j, k);
           const float wm = __shfl_sync(kFull, pg.w, k);
-          if (k0 + m < g.R && row >= 0 && jm == j) acc_pair(acc, v[m], f2_splat(wm));
+          if (k0 + m < g.R && row >= 0 && jm == j) acc_pair(acc, v[m], wm);
         }
       }
       if (act) store_bf16x8(out0 + (int64_t)j * g.H, acc);
@@ -573,7 +579,7 @@ __global__ void __launch_bounds__(kReduceThreads) k_combine_sum(Geo g, const int
   const int ng = __ldg(tgroups + u);
   const uint16_t* in0 = cpart + (u * J) * g.H;
   int cols[2];
-  uint64_t acc[2][4];
+  float acc[2][8];
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
     cols[c] = blockIdx.y * 2 * kReduceThreads + c * kReduceThreads + threadIdx.x;

@@ -11,6 +11,7 @@ function against brute force, invariants, closed forms and the OCP FP8 definitio
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import subprocess
@@ -27,13 +28,20 @@ BIT_CAPACITY = 1 << 3
 BIT_RECV_BOUND = 1 << 4
 
 
+def compile_source(src: str, out: str) -> str:
+    """gcc the C source file src into the shared library out (no FMA contraction, no
+    fast-math)."""
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", "-O2", "-std=c99", "-ffp-contract=off", "-fno-fast-math",
+                           "-fPIC", "-shared", src, "-o", tmp, "-lm"])
+    os.replace(tmp, out)
+    return out
+
+
 def build(force: bool = False) -> str:
-    """Compile moe_oracle.c with gcc (no FMA contraction, no fast-math)."""
+    """Compile moe_oracle.c."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
-        tmp = _LIB + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-std=c99", "-ffp-contract=off", "-fno-fast-math",
-                               "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"])
-        os.replace(tmp, _LIB)
+        compile_source(_SRC, _LIB)
     return _LIB
 
 
@@ -44,40 +52,56 @@ def _P(t):
     return POINTER(t)
 
 
+@contextlib.contextmanager
+def library(path: str):
+    """Runs every function of this module on another build of moe_oracle.c (the tests that
+    plant a mistake in a copy of the oracle, to show that its pins catch it)."""
+    global _lib
+    saved = _lib
+    _lib = _load(path)
+    try:
+        yield
+    finally:
+        _lib = saved
+
+
 def lib():
     global _lib
     if _lib is None:
-        build()
-        L = ctypes.CDLL(_LIB)
-        i32p = _P(ctypes.c_int32)
-        L.orc_bf16_to_f32.argtypes = [c_uint16]
-        L.orc_bf16_to_f32.restype = c_float
-        L.orc_f32_to_bf16.argtypes = [c_float]
-        L.orc_f32_to_bf16.restype = c_uint16
-        L.orc_e4m3_decode.argtypes = [c_uint8]
-        L.orc_e4m3_decode.restype = c_double
-        L.orc_e4m3_encode.argtypes = [c_float]
-        L.orc_e4m3_encode.restype = c_uint8
-        L.orc_layout.argtypes = [c_int] * 5 + [i32p] * 13
-        L.orc_layout.restype = c_uint32
-        L.orc_quantize_fp8.argtypes = [c_int, c_int, c_int, _P(c_uint16), _P(c_uint8)]
-        L.orc_quantize_fp8.restype = None
-        L.orc_dispatch_send.argtypes = [c_int] * 4 + [c_int64, _P(c_uint8)] + [i32p] * 4 + [_P(c_uint8)] * 2
-        L.orc_dispatch_send.restype = None
-        L.orc_dispatch_recv.argtypes = [c_int] * 5 + [c_int64, c_int, _P(c_uint8)] + [i32p] * 4 + [_P(c_uint8), _P(c_float)]
-        L.orc_dispatch_recv.restype = None
-        L.orc_expert_dequant.argtypes = [c_int] * 4 + [i32p, _P(c_uint8), _P(c_float), _P(c_uint16)]
-        L.orc_expert_dequant.restype = None
-        L.orc_combine_send.argtypes = [c_int] * 6 + [_P(c_uint16)] + [i32p] * 5 + [_P(c_uint16)] * 2
-        L.orc_combine_send.restype = None
-        L.orc_combine_recv.argtypes = [c_int] * 4 + [_P(c_uint16), _P(c_float), i32p, i32p, _P(c_uint16), _P(c_double)]
-        L.orc_combine_recv.restype = None
-        L.orc_combine_partial_send.argtypes = [c_int] * 6 + [_P(c_uint16), _P(c_float), i32p, i32p, _P(c_uint16)]
-        L.orc_combine_partial_send.restype = None
-        L.orc_combine_partial_recv.argtypes = [c_int] * 4 + [i32p, i32p, c_int, _P(c_uint16), _P(c_uint16)]
-        L.orc_combine_partial_recv.restype = None
-        _lib = L
+        _lib = _load(build())
     return _lib
+
+
+def _load(path: str):
+    L = ctypes.CDLL(path)
+    i32p = _P(ctypes.c_int32)
+    L.orc_bf16_to_f32.argtypes = [c_uint16]
+    L.orc_bf16_to_f32.restype = c_float
+    L.orc_f32_to_bf16.argtypes = [c_float]
+    L.orc_f32_to_bf16.restype = c_uint16
+    L.orc_e4m3_decode.argtypes = [c_uint8]
+    L.orc_e4m3_decode.restype = c_double
+    L.orc_e4m3_encode.argtypes = [c_float]
+    L.orc_e4m3_encode.restype = c_uint8
+    L.orc_layout.argtypes = [c_int] * 5 + [i32p] * 13
+    L.orc_layout.restype = c_uint32
+    L.orc_quantize_fp8.argtypes = [c_int, c_int, c_int, _P(c_uint16), _P(c_uint8)]
+    L.orc_quantize_fp8.restype = None
+    L.orc_dispatch_send.argtypes = [c_int] * 4 + [c_int64, _P(c_uint8)] + [i32p] * 4 + [_P(c_uint8)] * 2
+    L.orc_dispatch_send.restype = None
+    L.orc_dispatch_recv.argtypes = [c_int] * 5 + [c_int64, c_int, _P(c_uint8)] + [i32p] * 4 + [_P(c_uint8), _P(c_float)]
+    L.orc_dispatch_recv.restype = None
+    L.orc_expert_dequant.argtypes = [c_int] * 4 + [i32p, _P(c_uint8), _P(c_float), _P(c_uint16)]
+    L.orc_expert_dequant.restype = None
+    L.orc_combine_send.argtypes = [c_int] * 6 + [_P(c_uint16)] + [i32p] * 5 + [_P(c_uint16)] * 2
+    L.orc_combine_send.restype = None
+    L.orc_combine_recv.argtypes = [c_int] * 4 + [_P(c_uint16), _P(c_float), i32p, i32p, _P(c_uint16), _P(c_double)]
+    L.orc_combine_recv.restype = None
+    L.orc_combine_partial_send.argtypes = [c_int] * 6 + [_P(c_uint16), _P(c_float), i32p, i32p, _P(c_uint16)]
+    L.orc_combine_partial_send.restype = None
+    L.orc_combine_partial_recv.argtypes = [c_int] * 4 + [i32p, i32p, c_int, _P(c_uint16), _P(c_uint16)]
+    L.orc_combine_partial_recv.restype = None
+    return L
 
 
 def _ptr(a: np.ndarray, t):

@@ -394,3 +394,49 @@ def test_limits_match_oracle(orc, wl, flags):
     inp = workloads.make_inputs(wl)
     _, res = run_gpu(wl, inp, flags=flags)
     compare_all(orc, wl, inp, res, push=bool(flags & 8))
+
+
+RANDOM_EXPERT_CASES = [CASES[1], CASES[2], CASES[4], CASES[8], CASES[9],
+                       W("dups-bad-ids", 3, 21, 256, 12, 4, "bf16", "uniform", 190)]
+
+
+@pytest.mark.parametrize("flags", [0, 1, 4, 8], ids=["auto", "ldg", "tma", "push"])
+@pytest.mark.parametrize("wl", RANDOM_EXPERT_CASES, ids=lambda w: w.name)
+def test_combine_with_random_expert_outputs(orc, wl, flags):
+    """Experts that return their own random rows (not the identity), so every pair of a
+    token brings a different row: combine rows, output, and the partial combine must
+    match the oracle on the same expert outputs bit for bit."""
+    from workloads import to_bf16_bits
+    inp = workloads.make_inputs(wl)
+    if wl.name == "dups-bad-ids":
+        rng0 = np.random.default_rng(191)
+        inp["idx"] = rng0.integers(0, wl.E, size=(wl.N, wl.T, wl.R)).astype(np.int32)
+        inp["idx"][1, 4, 2] = -3
+    ep, _ = run_gpu(wl, inp, flags=flags)
+    lay_o = orc.layout(wl.N, wl.T, wl.E, wl.R, wl.cap, inp["idx"])
+    cap = lay_o["cap"]
+    ey = to_bf16_bits(np.random.default_rng(192).standard_normal((wl.N, wl.L, cap, wl.H)).astype(np.float32))
+    ep.expert_y.copy_(to_dev(ey).view(torch.bfloat16))
+    w = to_dev(inp["w"])
+    ep.combine_send()
+    ep.combine_recv(w)
+    ep.status()
+    _, crecv_o = orc.combine_send(wl.N, wl.T, wl.E, wl.R, cap, wl.H, ey, lay_o)
+    out_o, _ = orc.combine_recv(wl.N, wl.T, wl.R, wl.H, crecv_o, inp["w"], lay_o)
+    np.testing.assert_array_equal(u16(ep.out.cpu()), out_o, err_msg="combine output")
+    crecv = u16(ep.crecv.cpu())
+    for s in range(wl.N):
+        rows = lay_o["pos"][s][lay_o["slot"][s] >= 0]
+        np.testing.assert_array_equal(crecv[s][rows], crecv_o[s][rows], err_msg="combine rows")
+    if wl.R <= 32:
+        ep.combine_partial(w)
+        ep.status()
+        cpart_o, pout_o = orc.combine_partial(wl.N, wl.T, wl.E, wl.R, cap, wl.H, ey, inp["w"], inp["idx"], lay_o)
+        np.testing.assert_array_equal(u16(ep.out.cpu()), pout_o, err_msg="partial combine output")
+        ngroups = [[len({int(inp["idx"][s, t, k]) // wl.L for k in range(wl.R) if lay_o["slot"][s, t, k] >= 0})
+                    for t in range(wl.T)] for s in range(wl.N)]
+        cpart = u16(ep.cpart.cpu())
+        for s in range(wl.N):
+            for t in range(wl.T):
+                g = ngroups[s][t]
+                np.testing.assert_array_equal(cpart[s, t, :g], cpart_o[s, t, :g], err_msg="partial rows")

@@ -281,11 +281,16 @@ def test_combine_skips_dropped_and_invalid_pairs(orc):
     assert lay["status"] == orc.BIT_EXPERT_RANGE | orc.BIT_CAPACITY
     x = from_bf16_bits(inp["x"])
     out = from_bf16_bits(r["out"])
-    for s in range(2):
-        for t in range(4):
-            keep = [(k) for k in range(2) if lay["pos"][s, t, k] >= 0 and lay["slot"][s, t, k] >= 0]
-            want = sum(np.float32(0.5) * x[s, t] for _ in keep) if keep else np.zeros(wl.H, np.float32)
-            np.testing.assert_array_equal(out[s, t], from_bf16_bits(to_bf16_bits(np.asarray(want, np.float32))))
+    # the combine rows of dropped pairs are never written; fill them with 1.0 so that a
+    # combine which read them would differ
+    _, crecv1 = orc.combine_send(wl.N, wl.T, wl.E, wl.R, lay["cap"], wl.H, r["ey"], lay, fill=0x3F80)
+    out1, _ = orc.combine_recv(wl.N, wl.T, wl.R, wl.H, crecv1, w, lay)
+    for o in (out, from_bf16_bits(out1)):
+        for s in range(2):
+            for t in range(4):
+                keep = [(k) for k in range(2) if lay["pos"][s, t, k] >= 0 and lay["slot"][s, t, k] >= 0]
+                want = sum(np.float32(0.5) * x[s, t] for _ in keep) if keep else np.zeros(wl.H, np.float32)
+                np.testing.assert_array_equal(o[s, t], from_bf16_bits(to_bf16_bits(np.asarray(want, np.float32))))
 
 
 @pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
@@ -348,4 +353,74 @@ def test_partial_combine_within_tolerance_and_restated(orc, wl):
                 p = to_bf16_bits(acc)
                 np.testing.assert_array_equal(cpart[s, t, j], p)
                 total = (total + from_bf16_bits(p)).astype(np.float32)
+            np.testing.assert_array_equal(out[s, t], to_bf16_bits(total))
+
+
+# ---------------------------------------------------------------- combine with distinct expert outputs
+
+def _random_expert_rows(wl, cap, seed):
+    rng = np.random.default_rng(seed)
+    return to_bf16_bits(rng.standard_normal((wl.N, wl.L, cap, wl.H)).astype(np.float32))
+
+
+DISTINCT = [SMALL[1], SMALL[2], workloads.Workload("dup-cap", 3, 10, 128, 6, 4, "bf16", "uniform", 47, cap=7)]
+
+
+@pytest.mark.parametrize("wl", DISTINCT, ids=lambda w: w.name)
+def test_combine_with_distinct_expert_outputs_restated(orc, wl):
+    """Every expert returns its own rows, so each (token, expert) pair brings a different row:
+    combine must pair weight k with the row of expert idx[k] at slot[k]. Restated per pair
+    from idx, slot and the weights alone (fp32, k ascending, separate rounding), bit for bit;
+    the fp64 variant against an exact sum."""
+    inp = workloads.make_inputs(wl)
+    if wl.name == "dup-cap":   # duplicates within tokens, bad ids, and capacity drops
+        rng = np.random.default_rng(48)
+        inp["idx"] = rng.integers(0, wl.E, size=(wl.N, wl.T, wl.R)).astype(np.int32)
+        inp["idx"][0, 2, 1] = -1
+    lay = orc.layout(wl.N, wl.T, wl.E, wl.R, wl.cap, inp["idx"])
+    cap, L = lay["cap"], wl.L
+    ey = _random_expert_rows(wl, cap, 49)
+    csend, crecv = orc.combine_send(wl.N, wl.T, wl.E, wl.R, cap, wl.H, ey, lay)
+    out, out64 = orc.combine_recv(wl.N, wl.T, wl.R, wl.H, crecv, inp["w"], lay)
+    y = from_bf16_bits(ey)
+    for s in range(wl.N):
+        for t in range(wl.T):
+            acc = np.zeros(wl.H, np.float32)
+            terms = []
+            for k in range(wl.R):
+                e, j = int(inp["idx"][s, t, k]), int(lay["slot"][s, t, k])
+                if 0 <= e < wl.E and j >= 0:
+                    row = y[e // L, e % L, j]
+                    acc = (acc + (np.float32(inp["w"][s, t, k]) * row).astype(np.float32)).astype(np.float32)
+                    terms.append(np.float64(inp["w"][s, t, k]) * row.astype(np.float64))
+            np.testing.assert_array_equal(out[s, t], to_bf16_bits(acc), err_msg=f"token ({s},{t})")
+            if terms:
+                exact = np.array([math.fsum(c) for c in np.stack(terms).T])
+                assert np.abs(out64[s, t] - exact).max() <= wl.R * 2.0 ** -52 * np.abs(np.stack(terms)).sum(0).max()
+
+
+@pytest.mark.parametrize("wl", DISTINCT[:2], ids=lambda w: w.name)
+def test_partial_combine_with_distinct_expert_outputs_restated(orc, wl):
+    """Sender-side partial combine with per-expert rows: groups by owner rank ascending,
+    weights paired with their own expert's row, restated per pair."""
+    inp = workloads.make_inputs(wl)
+    lay = orc.layout(wl.N, wl.T, wl.E, wl.R, wl.cap, inp["idx"])
+    cap, L = lay["cap"], wl.L
+    ey = _random_expert_rows(wl, cap, 50)
+    cpart, out = orc.combine_partial(wl.N, wl.T, wl.E, wl.R, cap, wl.H, ey, inp["w"], inp["idx"], lay, fill=0x7FFF)
+    y = from_bf16_bits(ey)
+    for s in range(wl.N):
+        for t in range(wl.T):
+            ks = [k for k in range(wl.R) if lay["slot"][s, t, k] >= 0]
+            owners = sorted({int(inp["idx"][s, t, k]) // L for k in ks})
+            total = np.zeros(wl.H, np.float32)
+            for jg, d in enumerate(owners):
+                acc = np.zeros(wl.H, np.float32)
+                for k in ks:
+                    e = int(inp["idx"][s, t, k])
+                    if e // L == d:
+                        acc = (acc + (np.float32(inp["w"][s, t, k]) * y[d, e % L, lay["slot"][s, t, k]])
+                               .astype(np.float32)).astype(np.float32)
+                np.testing.assert_array_equal(cpart[s, t, jg], to_bf16_bits(acc))
+                total = (total + from_bf16_bits(to_bf16_bits(acc))).astype(np.float32)
             np.testing.assert_array_equal(out[s, t], to_bf16_bits(total))
