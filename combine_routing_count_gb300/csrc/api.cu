@@ -125,8 +125,8 @@ WsPlan ws_plan(const Geo& g) {
                           P,               // grecv
                           P,               // gslot
                           16,              // status
-                          (size_t)layout_scratch_lrank_offset(g) + (size_t)g.P + 16};  // scratch: chunk table,
-                                                         // counters, token groups, arrivals, ranks
+                          (size_t)layout_scratch_arrive_offset(g) + N * N + 16};  // scratch: chunk table,
+                                                                      // counters, token groups, arrivals
   w.total = 0;
   for (int i = 0; i < 17; ++i) {
     w.n[i] = al256(4 * sizes[i]);

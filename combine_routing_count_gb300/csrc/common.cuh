@@ -145,25 +145,4 @@ __device__ __forceinline__ void st16(void* p, const uint4& v) {
 __device__ __forceinline__ float bf16_lo(uint32_t packed) { return __uint_as_float(packed << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t packed) { return __uint_as_float(packed & 0xffff0000u); }
 
-// A pair's send row from per-rank layout data only (no receiver-side scan): for pair q of
-// rank s with expert e, s*TR + soff[s][e] + (pairs of e in earlier 256-pair chunks of s) +
-// (its rank among its chunk's pairs of e). -1 for an expert id outside [0, E).
-struct LocalRows {
-  const int32_t* idx;     // [N][T][R]
-  const int32_t* lrank;   // [N][T*R]: rank inside the pair's chunk
-  const int32_t* cpre;    // [N][nch][E]: pairs of each expert in earlier chunks
-  const int32_t* soff;    // [N][E]
-  int nch;
-};
-constexpr int kLayoutChunk = 256;   // pairs per counting chunk
-__device__ __forceinline__ int local_send_row(const Geo& g, const LocalRows& lr, int64_t q) {
-  const int e = __ldg(lr.idx + q);
-  if (e < 0 || e >= g.E) return -1;
-  const int s = (int)(q / g.TR);
-  const int64_t pl = q - (int64_t)s * g.TR;
-  const int c = (int)(pl / kLayoutChunk);
-  return (int)((int64_t)s * g.TR + __ldcg(lr.soff + (int64_t)s * g.E + e) +
-               __ldcg(lr.cpre + ((int64_t)s * lr.nch + c) * g.E + e) + __ldcg(lr.lrank + q));
-}
-
 }  // namespace moe

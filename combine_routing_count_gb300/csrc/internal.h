@@ -81,7 +81,6 @@ int layout_chunks(const Geo& g);
 int64_t layout_scratch_done_offset(const Geo& g);  // ints from the scratch start to the counters
 int64_t layout_scratch_tgroups_offset(const Geo& g);  // ... to the per-token group counts
 int64_t layout_scratch_arrive_offset(const Geo& g);   // ... to the split-dispatch counters [N*N + 2]
-int64_t layout_scratch_lrank_offset(const Geo& g);    // ... to the pairs' chunk-local ranks [P]
 
 // split.cu
 cudaError_t launch_dispatch_split(const Geo& g, const moe_layout_t* lay, const void* x, void* recv, void* ex,

@@ -27,7 +27,7 @@
 namespace moe {
 namespace {
 
-constexpr int kChunk = kLayoutChunk;   // pairs per histogram CTA (= its threads)
+constexpr int kChunk = 256;          // pairs per histogram CTA (= its threads)
 constexpr unsigned kFull = 0xffffffffu;
 
 struct LayoutArgs {
@@ -36,8 +36,7 @@ struct LayoutArgs {
   int32_t *pos, *rrow, *slot, *slot_src, *recv_src;
   int32_t *gsend, *grecv, *gslot;
   int32_t* status;
-  int32_t* ccnt;    // [N][nch][E]: per-chunk counts, turned into exclusive prefixes over chunks
-  int32_t* lrank;   // [N][T*R]: each pair's rank among its chunk's pairs of the same expert
+  int32_t* ccnt;    // [N][nch][E]: per-chunk counts
   int32_t* done;    // [N]: chunk CTAs of each rank that have finished (reset by the last one)
   int nch;          // chunks per rank, ceil(T*R / kChunk)
 };
@@ -51,19 +50,16 @@ __device__ __forceinline__ int warp_inclusive_scan(int v, int lane) {
   return v;
 }
 
-// The scans. Per source rank (row_scan): soff[s][.] = exclusive scan of cnt[s][.] over
-// experts and C[s][d] = sum of cnt[s][.] over d's experts; the counting kernel's last CTA
-// of each rank runs it. The rest is one grid of independent CTAs (kScanThreads threads
-// each), by role:
-//   [0, rows)               row CTA s (only with no tokens, when no counting kernel ran);
-//   [rows, rows + ceil(E/32)) column CTA: for 32 experts e, eoff[e][.] = exclusive scan of
+// The scans, as one grid of independent CTAs (kScanThreads threads each), by role:
+//   [0, N)              row CTA s:    soff[s][.] = exclusive scan of cnt[s][.] over experts,
+//                                     C[s][d] = sum of cnt[s][.] over d's experts;
+//   [N, N + ceil(E/32)) column CTA:   for 32 experts e, eoff[e][.] = exclusive scan of
 //                                     cnt[.][e] over source ranks, ecnt[e] = its total;
-//   [.., + N)               dest CTA d:   roff[d][.] = exclusive scan of C[.][d] over source
+//   [.., + N)           dest CTA d:   roff[d][.] = exclusive scan of C[.][d] over source
 //                                     ranks, rtot[d] = its total.
 // Every CTA reads the per-rank totals cnt[][] written by the counting kernel; lanes run
 // along the scanned dimension, so global stores are coalesced.
 constexpr int kScanThreads = 256;
-static_assert(kScanThreads == kChunk, "the counting kernel's last CTA runs the row scan");
 
 __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -88,37 +84,6 @@ __device__ __forceinline__ int cnt_at(const LayoutArgs& a, int64_t i) {
   return a.nch > 0 ? __ldcg(a.cnt + i) : 0;
 }
 
-// soff[s][.] and C[s][.] for source rank s, by the whole CTA (kScanThreads threads).
-__device__ __forceinline__ void row_scan(const Geo& g, const LayoutArgs& a, int s, int* warp_tot) {
-  const int N = g.N, E = g.E, L = g.L;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int k = (E + kScanThreads - 1) / kScanThreads;      // experts per thread, <= 6
-  const int e0 = tid * k;
-  int vals[6];
-  int sum = 0;
-#pragma unroll
-  for (int j = 0; j < 6; ++j) {
-    vals[j] = (j < k && e0 + j < E) ? cnt_at(a, (int64_t)s * E + e0 + j) : 0;
-    sum += vals[j];
-  }
-  int total;
-  int run = block_exclusive_scan(sum, warp_tot, total);
-#pragma unroll
-  for (int j = 0; j < 6; ++j)
-    if (j < k && e0 + j < E) {
-      a.soff[(int64_t)s * E + e0 + j] = run;
-      run += vals[j];
-      if (a.nch == 0) a.cnt[(int64_t)s * E + e0 + j] = 0;
-    }
-  for (int d = warp; d < N; d += kScanThreads / 32) {   // C[s][d]: lanes along d's experts
-    int c = 0;
-    for (int l = lane; l < L; l += 32) c += cnt_at(a, (int64_t)s * E + d * L + l);
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
-    if (lane == 0) a.C[s * N + d] = c;
-  }
-}
-
 __global__ void __launch_bounds__(kScanThreads) k_route_scan(Geo g, LayoutArgs a) {
   __shared__ int warp_tot[kScanThreads / 32 + 1];
   __shared__ int tile[64 * 33];
@@ -127,14 +92,39 @@ __global__ void __launch_bounds__(kScanThreads) k_route_scan(Geo g, LayoutArgs a
   const int n_col = (E + 31) / 32;
   const int b = blockIdx.x;
   pdl_wait();
-  const int rows = a.nch == 0 ? N : 0;
-  if (b < rows) {
-    row_scan(g, a, b, warp_tot);
-  } else if (b < rows + n_col) {
+  if (b < N) {
+    // ---- row CTA: soff[s][.] and C[s][.]
+    const int s = b;
+    const int k = (E + kScanThreads - 1) / kScanThreads;      // experts per thread, <= 6
+    const int e0 = tid * k;
+    int vals[6];
+    int sum = 0;
+#pragma unroll
+    for (int j = 0; j < 6; ++j) {
+      vals[j] = (j < k && e0 + j < E) ? cnt_at(a, (int64_t)s * E + e0 + j) : 0;
+      sum += vals[j];
+    }
+    int total;
+    int run = block_exclusive_scan(sum, warp_tot, total);
+#pragma unroll
+    for (int j = 0; j < 6; ++j)
+      if (j < k && e0 + j < E) {
+        a.soff[(int64_t)s * E + e0 + j] = run;
+        run += vals[j];
+        if (a.nch == 0) a.cnt[(int64_t)s * E + e0 + j] = 0;
+      }
+    for (int d = warp; d < N; d += kScanThreads / 32) {   // C[s][d]: lanes along d's experts
+      int c = 0;
+      for (int l = lane; l < L; l += 32) c += cnt_at(a, (int64_t)s * E + d * L + l);
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
+      if (lane == 0) a.C[s * N + d] = c;
+    }
+  } else if (b < N + n_col) {
     // ---- column CTA: eoff[e][.] and ecnt[e] for experts e0 .. e0+31. Tiles of 64 ranks
     // x 32 experts are staged in shared memory (coalesced rows, odd stride); warp w scans
     // experts w, w+8, w+16, w+24 down the ranks, carrying their totals across tiles.
-    const int e0 = (b - rows) * 32;
+    const int e0 = (b - N) * 32;
     int carry[4] = {0, 0, 0, 0};
     for (int s0 = 0; s0 < N; s0 += 64) {
       const int ns = N - s0 < 64 ? N - s0 : 64;
@@ -166,7 +156,7 @@ __global__ void __launch_bounds__(kScanThreads) k_route_scan(Geo g, LayoutArgs a
     }
   } else {
     // ---- destination CTA: roff[d][.] and rtot[d]
-    const int d = b - rows - n_col;
+    const int d = b - N - n_col;
     int* cd = tile;   // cd[s] = C[s][d], N <= 64*33
     for (int s = warp; s < N; s += kScanThreads / 32) {
       int c = 0;
@@ -195,11 +185,8 @@ __global__ void __launch_bounds__(kScanThreads) k_route_scan(Geo g, LayoutArgs a
 }
 
 // One CTA per (chunk c, source rank s): the chunk's 256 pairs in (t,k) order, one per
-// thread. Writes each pair's rank among the chunk's pairs of the same expert into lrank[]
+// thread. Writes each pair's rank among the chunk's pairs of the same expert into pos[]
 // (-1 for an id outside [0,E)) and the chunk's count of every expert into ccnt[s][c][.].
-// The last CTA of rank s to finish turns the rank's chunk counts into exclusive prefixes
-// over chunks, sums them into cnt[s][.] and runs the rank's row scan (soff, C): after this
-// kernel a pair's send row needs no other rank's data (local_send_row).
 __global__ void __launch_bounds__(kChunk) k_route_count(Geo g, LayoutArgs a) {
   extern __shared__ int32_t wtab[];  // [kChunk/32][E]: per-warp counts, then exclusive offsets
   constexpr int kW = kChunk / 32;
@@ -231,40 +218,29 @@ __global__ void __launch_bounds__(kChunk) k_route_count(Geo g, LayoutArgs a) {
     crow[ee] = r;
   }
   __syncthreads();
-  if (in) a.lrank[q] = ok ? wtab[warp * E + e] + lrank : -1;
+  if (in) a.pos[q] = ok ? wtab[warp * E + e] + lrank : -1;
 
-  // The last chunk CTA of rank s to finish (completion counter per rank; no CTA waits for
-  // another) works on the rank's chunk rows.
+  // The last chunk CTA of rank s to finish sums the rank's chunk rows into cnt[s][.]
+  // (completion counter per rank; no CTA waits for another).
   __shared__ int is_last;
-  __shared__ int warp_tot[kScanThreads / 32 + 1];
   __threadfence();
   __syncthreads();
   if (tid == 0) is_last = (atomicAdd(a.done + s, 1) == a.nch - 1);
   __syncthreads();
   if (is_last) {
     __threadfence();
-    int32_t* base = a.ccnt + (int64_t)s * a.nch * E;
+    const int32_t* base = a.ccnt + (int64_t)s * a.nch * E;
     for (int ee = tid; ee < E; ee += kChunk) {
       int r = 0;
       int cc = 0;
       for (; cc + 4 <= a.nch; cc += 4) {   // four independent loads in flight
         const int v0 = __ldcg(base + (int64_t)cc * E + ee), v1 = __ldcg(base + (int64_t)(cc + 1) * E + ee);
         const int v2 = __ldcg(base + (int64_t)(cc + 2) * E + ee), v3 = __ldcg(base + (int64_t)(cc + 3) * E + ee);
-        base[(int64_t)cc * E + ee] = r;
-        base[(int64_t)(cc + 1) * E + ee] = r + v0;
-        base[(int64_t)(cc + 2) * E + ee] = r + v0 + v1;
-        base[(int64_t)(cc + 3) * E + ee] = r + v0 + v1 + v2;
         r += v0 + v1 + v2 + v3;
       }
-      for (; cc < a.nch; ++cc) {
-        const int v = __ldcg(base + (int64_t)cc * E + ee);
-        base[(int64_t)cc * E + ee] = r;
-        r += v;
-      }
+      for (; cc < a.nch; ++cc) r += __ldcg(base + (int64_t)cc * E + ee);
       a.cnt[(int64_t)s * E + ee] = r;
     }
-    __syncthreads();   // cnt[s][.] complete for the whole CTA
-    row_scan(g, a, s, warp_tot);
     if (tid == 0) a.done[s] = 0;  // ready for the next call
   }
   pdl_trigger();
@@ -283,8 +259,7 @@ __global__ void __launch_bounds__(kMapThreads) k_layout_maps(Geo g, LayoutArgs a
     const int q = b * kMapThreads + threadIdx.x;
     if (q < g.P) {
       const int e = __ldg(a.idx + q);
-      if (e < 0 || e >= g.E) {
-        a.pos[q] = -1;
+      if (e < 0 || e >= g.E) {  // pos[q] is already -1
         a.rrow[q] = -1;
         a.slot[q] = -1;
         a.gsend[q] = -1;
@@ -294,7 +269,9 @@ __global__ void __launch_bounds__(kMapThreads) k_layout_maps(Geo g, LayoutArgs a
         const int TR = (int)g.TR;
         const int s = q / TR;
         const int c = (q - s * TR) / kChunk;
-        const int rk = __ldg(a.lrank + q) + __ldg(a.ccnt + ((int64_t)s * a.nch + c) * g.E + e);
+        const int32_t* col = a.ccnt + (int64_t)s * a.nch * g.E + e;
+        int rk = a.pos[q];
+        for (int cc = 0; cc < c; ++cc) rk += col[(int64_t)cc * g.E];   // pairs of e in earlier chunks
         const int d = e / g.L;
         const int p = a.soff[s * g.E + e] + rk;
         const int rr = a.roff[d * g.N + s] + p - a.soff[s * g.E + d * g.L];
@@ -342,8 +319,6 @@ int64_t layout_scratch_tgroups_offset(const Geo& g) { return layout_scratch_done
 
 int64_t layout_scratch_arrive_offset(const Geo& g) { return layout_scratch_tgroups_offset(g) + (int64_t)g.N * g.T; }
 
-int64_t layout_scratch_lrank_offset(const Geo& g) { return layout_scratch_arrive_offset(g) + (int64_t)g.N * g.N + 2; }
-
 
 std::atomic<int> g_count_smem[64];   // per device: dynamic shared memory k_route_count is set up for
 
@@ -368,7 +343,6 @@ cudaError_t launch_layout(const Geo& g, const int32_t* idx, const moe_layout_t* 
   a.status = lay->status;
   a.nch = layout_chunks(g);
   a.ccnt = lay->scratch;
-  a.lrank = lay->scratch + layout_scratch_lrank_offset(g);
   a.done = lay->scratch + layout_scratch_done_offset(g);
 
   cudaError_t e = cudaSuccess;
@@ -381,8 +355,7 @@ cudaError_t launch_layout(const Geo& g, const int32_t* idx, const moe_layout_t* 
   }
   {
     LaunchScope ls(c, MOE_K_ROUTE_SCAN);
-    const int rows = a.nch == 0 ? g.N : 0;   // row scans run in the counting kernel when it runs
-    e = launch_kernel(k_route_scan, dim3(rows + (g.E + 31) / 32 + g.N), dim3(kScanThreads), 0, c, g, a);
+    e = launch_kernel(k_route_scan, dim3(2 * g.N + (g.E + 31) / 32), dim3(kScanThreads), 0, c, g, a);
   }
   if (e != cudaSuccess) return e;
   const int pair_blocks = (int)((g.P + kMapThreads - 1) / kMapThreads);
