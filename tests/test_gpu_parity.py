@@ -336,17 +336,25 @@ def test_fused_quantize_rejects_bf16_payload():
     assert rc == 1
 
 
-def test_forward_fp8_staged_and_fused_agree(orc):
-    wl = W("fp8-forward", 8, 24, 7168, 64, 8, "fp8", "uniform", 162)
+@pytest.mark.parametrize("payload", ["bf16", "fp8"])
+def test_forward_variants_agree(orc, payload):
+    """moe_forward by default, with staged fp8 quantisation, and pushed: the same output and
+    layout, twice in a row on the same layout workspace."""
+    wl = W("forward-variants", 8, 24, 7168, 64, 8, payload, "uniform", 162)
     inp = workloads.make_inputs(wl)
     from combine_routing_count_gb300 import MoeEP
     o = orc.forward(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, wl.payload, inp["x"], inp["idx"], inp["w"])
-    for flags in (0, 0x10, 0x18):
-        ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, payload="fp8", flags=flags)
-        ep.forward(to_dev(inp["x"]).view(torch.bfloat16), to_dev(inp["idx"]), to_dev(inp["w"]))
-        code, _ = ep.status()
-        assert code == 0
-        np.testing.assert_array_equal(u16(ep.out.cpu()), o["out"], err_msg=f"flags {flags:#x}")
+    for flags in (0, 0x10, 0x18, 0x8):
+        ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, payload=payload, flags=flags)
+        for _ in range(2):
+            ep.out.fill_(0)
+            ep.forward(to_dev(inp["x"]).view(torch.bfloat16), to_dev(inp["idx"]), to_dev(inp["w"]))
+            code, _ = ep.status()
+            assert code == 0
+            np.testing.assert_array_equal(u16(ep.out.cpu()), o["out"], err_msg=f"flags {flags:#x}")
+            got = {k: v.cpu().numpy() for k, v in ep.layout_arrays().items()}
+            for k in ("pos", "rrow", "slot", "slot_src", "recv_src", "soff", "roff", "eoff"):
+                np.testing.assert_array_equal(got[k], o["layout"][k], err_msg=f"flags {flags:#x} {k}")
 
 
 @pytest.mark.parametrize("flags", [0, 4, 8], ids=["auto", "tma", "push"])
