@@ -152,8 +152,9 @@ typedef struct {
  *   gslot [N*T*R]  global grouped row, e*cap + slot (row of d_expert_x), or -1 when the
  *                  pair's expert id is bad or the pair was dropped for capacity
  *   status   [1]         sticky error bits, bit (1 << moe_status)
- *   scratch  internal: per-chunk counts [N][ceil(T*R/256)][E], per-rank counters [N] and
- *            per-token group counts of the partial combine [N][T]
+ *   scratch  internal: per-chunk counts [N][ceil(T*R/256)][E], per-rank counters [N],
+ *            per-token group counts of the partial combine [N][T] and the split-phase
+ *            arrival counters [N][N] (+ 2)
  * Host-side fields (set by the caller after moe_layout_init, read at each call):
  *   flags, prof, tma_stages (0 = automatic, else 1..32 stages per TMA mover CTA),
  *   ctas_per_sm (0 = automatic, else mover CTAs per SM).
