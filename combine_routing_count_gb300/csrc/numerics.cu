@@ -568,7 +568,10 @@ __global__ void __launch_bounds__(kReduceThreads) k_combine_partial(Geo g, const
 }
 
 // Source side: out[s][t] = bf16(sum over the token's groups j ascending of cpart[s][t][j]).
-// Block (token, 2048 columns): each thread sums two 16-byte column vectors.
+// Block (token, kSumVec * kReduceThreads * 8 columns): each thread sums kSumVec 16-byte
+// column vectors, two groups' loads in flight at a time.
+constexpr int kSumVec = 4;
+
 __global__ void __launch_bounds__(kReduceThreads) k_combine_sum(Geo g, const int32_t* __restrict__ tgroups,
                                                                 const uint16_t* __restrict__ cpart,
                                                                 uint16_t* __restrict__ out) {
@@ -578,31 +581,31 @@ __global__ void __launch_bounds__(kReduceThreads) k_combine_sum(Geo g, const int
   pdl_wait();
   const int ng = __ldg(tgroups + u);
   const uint16_t* in0 = cpart + (u * J) * g.H;
-  int cols[2];
-  float acc[2][8];
+  int cols[kSumVec];
+  float acc[kSumVec][8];
 #pragma unroll
-  for (int c = 0; c < 2; ++c) {
-    cols[c] = blockIdx.y * 2 * kReduceThreads + c * kReduceThreads + threadIdx.x;
+  for (int c = 0; c < kSumVec; ++c) {
+    cols[c] = blockIdx.y * kSumVec * kReduceThreads + c * kReduceThreads + threadIdx.x;
     acc_zero(acc[c]);
   }
-  for (int j0 = 0; j0 < ng; j0 += 4) {
-    uint4 v[4][2];
+  for (int j0 = 0; j0 < ng; j0 += 2) {
+    uint4 v[2][kSumVec];
 #pragma unroll
-    for (int m = 0; m < 4; ++m)
+    for (int m = 0; m < 2; ++m)
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < kSumVec; ++c) {
         v[m][c] = make_uint4(0, 0, 0, 0);
         if (j0 + m < ng && cols[c] < ncol) v[m][c] = ld_stream16(in0 + (int64_t)(j0 + m) * g.H + cols[c] * 8);
       }
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
+    for (int m = 0; m < 2; ++m) {
       if (j0 + m >= ng) continue;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) acc_add(acc[c], v[m][c]);
+      for (int c = 0; c < kSumVec; ++c) acc_add(acc[c], v[m][c]);
     }
   }
 #pragma unroll
-  for (int c = 0; c < 2; ++c)
+  for (int c = 0; c < kSumVec; ++c)
     if (cols[c] < ncol) store_bf16x8(out + u * g.H + cols[c] * 8, acc[c]);
   pdl_trigger();
 }
@@ -629,7 +632,7 @@ cudaError_t launch_combine_sum(const Geo& g, const moe_layout_t* lay, const uint
   const int64_t tokens = (int64_t)g.N * g.T;
   if (tokens == 0) return cudaSuccess;
   const int ncol = g.H / 8;
-  dim3 grid((unsigned)tokens, (unsigned)((ncol + 2 * kReduceThreads - 1) / (2 * kReduceThreads)));
+  dim3 grid((unsigned)tokens, (unsigned)((ncol + kSumVec * kReduceThreads - 1) / (kSumVec * kReduceThreads)));
   LaunchScope ls(c, MOE_K_COMBINE_SUM);
   return launch_kernel(k_combine_sum, grid, dim3(kReduceThreads), 0, c, g,
                        (const int32_t*)(lay->scratch + layout_scratch_tgroups_offset(g)), cpart, out);
