@@ -448,3 +448,43 @@ def test_combine_with_random_expert_outputs(orc, wl, flags):
             for t in range(wl.T):
                 g = ngroups[s][t]
                 np.testing.assert_array_equal(cpart[s, t, :g], cpart_o[s, t, :g], err_msg="partial rows")
+
+
+def test_concurrent_passes_on_two_streams(orc):
+    """Two host threads, each with its own stream and layout, run whole passes at the same
+    time (different workloads, TMA and register movers, bf16 and fp8): the library keeps
+    no per-call state outside the caller's layout and buffers."""
+    import threading
+    from combine_routing_count_gb300 import MoeEP
+    cases = [(W("conc-a", 8, 64, 4096, 64, 8, "bf16", "uniform", 210), 4),
+             (W("conc-b", 4, 48, 2048, 32, 6, "fp8", "zipf", 211), 0)]
+    results, errors = {}, []
+
+    def run(wl, flags):
+        try:
+            stream = torch.cuda.Stream()
+            with torch.cuda.stream(stream):
+                inp = workloads.make_inputs(wl)
+                ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, payload=wl.payload, flags=flags)
+                x, idx, w = to_dev(inp["x"]).view(torch.bfloat16), to_dev(inp["idx"]), to_dev(inp["w"])
+                outs = []
+                for _ in range(6):
+                    ep.forward(x, idx, w)
+                    code, _ = ep.status()
+                    assert code == 0
+                    outs.append(u16(ep.out.cpu()))
+                results[wl.name] = (inp, outs)
+        except Exception as e:   # reported by the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=run, args=c) for c in cases]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for wl, _ in cases:
+        inp, outs = results[wl.name]
+        o = orc.forward(wl.N, wl.T, wl.H, wl.E, wl.R, 0, wl.payload, inp["x"], inp["idx"], inp["w"])
+        for out in outs:
+            np.testing.assert_array_equal(out, o["out"], err_msg=wl.name)
