@@ -37,7 +37,7 @@ import workloads  # noqa: E402
 METRIC = "dispatch+combine tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 KERNELS = ["route_count", "layout_maps", "quant_fp8", "pack", "scatter", "unpack", "expert",
            "combine_pack", "combine_scatter", "combine_reduce", "route_scan", "pack_push", "combine_push",
-           "combine_partial", "combine_sum", "dispatch_split", "quant_pack"]
+           "combine_partial", "combine_sum", "dispatch_split", "quant_pack", "dispatch_dedicated"]
 
 
 def parse_args(argv=None):
@@ -184,6 +184,7 @@ def algorithmic_bytes(wl: workloads.Workload, P: int, Pk: int) -> dict:
         "quant_pack": tok * 2 * H + P * B,
         "combine_push": 2 * Pk * 2 * H,
         "dispatch_split": tok * B + P * B + 2 * Pk * B,
+        "dispatch_dedicated": tok * B + P * B + 2 * Pk * B,
     }
 
 
@@ -334,6 +335,19 @@ def run_ours(args):
         ep.combine_send()
         ep.combine_recv(w)
 
+    DED_K = 16   # dedicated rows per (receiver, sender)
+
+    def step_dedicated():
+        ep.layout_step(idx)
+        if fp8:
+            ep.quantize(x)
+            ep.dispatch_dedicated(ep.xq, idx, DED_K)
+        else:
+            ep.dispatch_dedicated(x, idx, DED_K)
+        ep.expert_identity()
+        ep.combine_send()
+        ep.combine_recv(w)
+
     def kernel_region(step=step):
         """Timed region: per-kernel CUDA events (the library records one pair around each of
         its launches on this stream) give each kernel's duration for the roofline."""
@@ -470,6 +484,24 @@ def run_ours(args):
                             "frac": round(ab[name] / (us * 1e-6) / 1e9 / peak, 3)}
     sp_ms_all = max_over_ranks(sp_ms, dist, device)
 
+    # Split-phase dispatch with per-sender dedicated space and piggybacked routing counts.
+    ep.layout.flags |= 8
+    for _ in range(args.warmup):
+        flush.zero_()
+        step_dedicated()
+    pk_ded = kernel_region(step_dedicated)
+    ded_ms, _, _ = step_region(step_dedicated)
+    ep.layout.flags &= ~8
+    if fp8:
+        ded_ms -= expert_ms
+    ded_kernels = {}
+    for name, ts in pk_ded.items():
+        if name == "dispatch_dedicated":
+            us = statistics.fmean(ts) * 1e3
+            ded_kernels[name] = {"us": round(us, 2), "gbs": round(ab[name] / (us * 1e-6) / 1e9, 1),
+                                 "frac": round(ab[name] / (us * 1e-6) / 1e9 / peak, 3)}
+    ded_ms_all = max_over_ranks(ded_ms, dist, device)
+
     # end to end through the C ABI with host buffers: H2D inputs, the pass, D2H output
     h_x = torch.from_numpy(inp["x"]).view(torch.bfloat16).pin_memory()
     h_idx = torch.from_numpy(inp["idx"]).pin_memory()
@@ -533,6 +565,12 @@ def run_ours(args):
                                  "note": "direct-push step whose dispatch is one cooperative launch: "
                                          "push rows, signal per (destination, source) slice, wait "
                                          "(bounded), shuffle into the grouped rows"},
+        "split_phase_dedicated": {"value": round(tokens / (ded_ms_all * 1e-3), 1), "unit": "tokens/s",
+                                  "ms_per_step": round(ded_ms_all, 4), "dedicated_rows": DED_K,
+                                  "kernels": ded_kernels,
+                                  "note": "direct-push step whose dispatch is one cooperative launch with "
+                                          "per-sender dedicated rows and the routing counts piggybacked; "
+                                          "receivers compute their offsets from the reported counts"},
         "e2e": {"value": round(tokens / (e2e_ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "path": "moe_forward_host (C ABI): kernels read pinned host inputs and write the host output "

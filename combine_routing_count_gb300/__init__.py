@@ -121,6 +121,21 @@ class MoeEP:
                                        self.recv.data_ptr(), self.expert_x.data_ptr(), _ptr(self.expert_scale),
                                        int(withhold_slice), _stream(stream)), "moe_dispatch_split")
 
+    def dispatch_dedicated(self, x: torch.Tensor, idx: torch.Tensor, K: int, withhold_slice: int = -1, stream=None):
+        """Split-phase dispatch with K dedicated rows per (receiver, sender) and the routing
+        counts piggybacked on the first writes. The shared region is self.recv; the
+        dedicated rows are self.ded [N,N,K,B]. withhold_slice (tests only) names a slice
+        d*N + s whose row signals are not sent."""
+        self.x = x
+        if getattr(self, "ded", None) is None or self.ded.shape[2] != K:
+            self.ded = torch.empty((self.N, self.N, max(K, 1), self.B), dtype=torch.uint8, device=self.recv.device)
+            nbytes = lib().moe_dedicated_exchange_bytes(ctypes.byref(self.dims))
+            self.xchg = torch.empty(nbytes, dtype=torch.uint8, device=self.recv.device)
+        check(lib().moe_dispatch_dedicated(ctypes.byref(self.dims), ctypes.byref(self.layout), idx.data_ptr(),
+                                           x.data_ptr(), int(K), self.ded.data_ptr(), self.xchg.data_ptr(),
+                                           self.recv.data_ptr(), self.expert_x.data_ptr(), _ptr(self.expert_scale),
+                                           int(withhold_slice), _stream(stream)), "moe_dispatch_dedicated")
+
     def dispatch_recv(self, stream=None):
         check(lib().moe_dispatch_recv(ctypes.byref(self.dims), ctypes.byref(self.layout), self.recv.data_ptr(),
                                       self.expert_x.data_ptr(), _ptr(self.expert_scale), _stream(stream)),

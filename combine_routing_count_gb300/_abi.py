@@ -28,7 +28,7 @@ MOE_PROF_MAX = 32
 
 KERNEL_NAMES = ["route_count", "layout_maps", "quant_fp8", "pack", "scatter", "unpack", "expert",
                 "combine_pack", "combine_scatter", "combine_reduce", "route_scan", "pack_push", "combine_push",
-                "combine_partial", "combine_sum", "dispatch_split", "quant_pack"]
+                "combine_partial", "combine_sum", "dispatch_split", "quant_pack", "dispatch_dedicated"]
 
 LAYOUT_FIELDS = ("cnt", "C", "soff", "roff", "rtot", "ecnt", "eoff", "pos", "rrow", "slot", "slot_src",
                  "recv_src", "gsend", "grecv", "gslot", "status", "scratch")
@@ -87,6 +87,9 @@ def lib():
             "moe_dispatch_send": (c_int32, [D, Lp, c_void_p, c_void_p, c_void_p, c_void_p]),
             "moe_dispatch_send_noalloc": (c_int32, [D, Lp, c_void_p, c_void_p, c_void_p]),
             "moe_quantize_dispatch_send": (c_int32, [D, Lp, c_void_p, c_void_p, c_void_p, c_void_p]),
+            "moe_dedicated_exchange_bytes": (c_size_t, [D]),
+            "moe_dispatch_dedicated": (c_int32, [D, Lp, c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_void_p,
+                                                 c_void_p, c_void_p, c_int32, c_void_p]),
             "moe_dispatch_split": (c_int32, [D, Lp, c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_void_p]),
             "moe_dispatch_recv": (c_int32, [D, Lp, c_void_p, c_void_p, c_void_p, c_void_p]),
             "moe_expert_identity": (c_int32, [D, Lp, c_void_p, c_void_p, c_void_p, c_void_p]),
@@ -120,7 +123,8 @@ def check(code: int, what: str) -> None:
 # Names a symbol-export test checks against include/moe_ep.h.
 EXPORTED = ("moe_check_dims", "moe_recv_capacity_rows", "moe_row_bytes", "moe_capacity",
             "moe_layout_workspace_bytes", "moe_layout_init", "moe_layout", "moe_quantize_fp8_b128",
-            "moe_dispatch_send", "moe_dispatch_send_noalloc", "moe_quantize_dispatch_send", "moe_dispatch_split", "moe_dispatch_recv",
+            "moe_dispatch_send", "moe_dispatch_send_noalloc", "moe_quantize_dispatch_send", "moe_dispatch_split",
+            "moe_dedicated_exchange_bytes", "moe_dispatch_dedicated", "moe_dispatch_recv",
             "moe_expert_identity", "moe_combine_send", "moe_combine_recv", "moe_combine_send_partial",
             "moe_combine_recv_partial", "moe_forward", "moe_forward_host", "moe_status_sync",
             "moe_status_string", "moe_launch_count")

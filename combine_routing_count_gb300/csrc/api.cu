@@ -290,6 +290,32 @@ moe_status moe_dispatch_split(const moe_dims* dims, const moe_layout_t* lay, con
                                            withhold_slice, c));
 }
 
+size_t moe_dedicated_exchange_bytes(const moe_dims* dims) {
+  Geo g;
+  if (make_geo(dims, g) != MOE_OK) return 0;
+  return dedicated_exchange_bytes(g);
+}
+
+moe_status moe_dispatch_dedicated(const moe_dims* dims, const moe_layout_t* lay, const int32_t* d_idx,
+                                  const void* d_x, int32_t K, void* d_ded, void* d_xchg, void* d_main,
+                                  void* d_expert_x, float* d_expert_scale, int32_t withhold_slice, void* stream) {
+  Geo g;
+  moe_status st = make_geo(dims, g);
+  if (st != MOE_OK) return st;
+  if (K < 0 || withhold_slice < -1 || withhold_slice >= (int64_t)g.N * g.N || g.R > 32) return MOE_ERR_INVALID_ARG;
+  const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
+  if (!layout_ok(lay) || !d_xchg || !aligned16(d_xchg)) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)g.N * g.T > 0 &&
+      (!d_idx || !d_x || !d_main || !d_expert_x || !aligned16(d_x) || !aligned16(d_main) ||
+       !aligned16(d_expert_x) || (K > 0 && (!d_ded || !aligned16(d_ded))) ||
+       (fp8 && (!d_expert_scale || !aligned16(d_expert_scale)))))
+    return MOE_ERR_INVALID_ARG;
+  Ctx c;
+  if ((st = make_ctx(lay, stream, c)) != MOE_OK) return st;
+  return cuda_status(launch_dispatch_dedicated(g, lay, d_idx, d_x, K, d_ded, d_xchg, d_main, d_expert_x,
+                                               fp8 ? d_expert_scale : nullptr, withhold_slice, c));
+}
+
 moe_status moe_dispatch_recv(const moe_dims* dims, const moe_layout_t* lay, const void* d_recv, void* d_expert_x,
                              float* d_expert_scale, void* stream) {
   Geo g;

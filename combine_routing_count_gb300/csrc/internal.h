@@ -82,6 +82,12 @@ int64_t layout_scratch_done_offset(const Geo& g);  // ints from the scratch star
 int64_t layout_scratch_tgroups_offset(const Geo& g);  // ... to the per-token group counts
 int64_t layout_scratch_arrive_offset(const Geo& g);   // ... to the split-dispatch counters [N*N + 2]
 
+// dedicated.cu
+size_t dedicated_exchange_bytes(const Geo& g);
+cudaError_t launch_dispatch_dedicated(const Geo& g, const moe_layout_t* lay, const int32_t* idx, const void* x,
+                                      int K, void* ded, void* xchg, void* main, void* ex, float* exs,
+                                      int drop_slice, Ctx& c);
+
 // split.cu
 cudaError_t launch_dispatch_split(const Geo& g, const moe_layout_t* lay, const void* x, void* recv, void* ex,
                                   float* exs, int drop_slice, Ctx& c);

@@ -87,7 +87,8 @@ typedef enum {
     MOE_K_COMBINE_SUM = 14,    /* source-side sum of the partial rows -> bf16 */
     MOE_K_DISPATCH_SPLIT = 15, /* split-phase dispatch: push, signal, wait, shuffle in one launch */
     MOE_K_QUANT_PACK = 16,     /* fp8 quantisation fused into the pack */
-    MOE_K_NUM = 17
+    MOE_K_DISPATCH_DEDICATED = 17, /* split-phase dispatch with dedicated space and piggybacked routing */
+    MOE_K_NUM = 18
 } moe_kernel_id;
 
 /* Optional per-kernel timing. When moe_layout_t.prof is non-NULL, every kernel the library
@@ -294,6 +295,31 @@ moe_status moe_dispatch_send_noalloc(const moe_dims *dims, const moe_layout_t *l
  * are MOE_ERR_INVALID_ARG, and so is R > 32. */
 moe_status moe_dispatch_split(const moe_dims *dims, const moe_layout_t *lay, const void *d_x, void *d_recv,
                               void *d_expert_x, float *d_expert_scale, int32_t withhold_slice, void *stream);
+
+/* Split-phase dispatch with per-sender dedicated space and the routing information
+ * piggybacked on the first writes (section "Send and receive buffers": each receiver
+ * reserves a small dedicated space per sender; the sender dispatches part of its tokens
+ * together with the routing-information write, and after the routes are exchanged the
+ * remaining tokens go with one write per peer; section "Dispatch and combine": the receiver
+ * centralises its peers' routing, computes its offsets, waits for every transfer and
+ * shuffles the tokens into the grouped-GEMM input).
+ * Senders use only their own routing from *lay (cnt, soff, pos, filled by moe_layout);
+ * receivers compute their offsets only from the counts the senders report. Buffers:
+ *   d_ded  [N][N][K][B]: rank d's dedicated rows for sender s: rows j < K of the slice
+ *          (d, s) (the rows s sends to d, in s's send order);
+ *   d_main [N][RB][B]: rank d's shared region: rows j >= K of each slice, sender after
+ *          sender (the slice of s at place sum over s' < s of max(C[s'][d] - K, 0));
+ *   d_xchg moe_dedicated_exchange_bytes(dims) bytes: the reported counts, the receivers'
+ *          offsets and the flags (zeroed by the call);
+ *   d_expert_x / d_expert_scale: the grouped rows, as moe_dispatch_recv writes them.
+ * One cooperative launch (after a memset of the flags); every wait bounded (1 s, then
+ * MOE_ERR_TIMEOUT and the call still completes). K >= 0 (K = 0: no dedicated rows).
+ * withhold_slice: failure injection for tests (the row signals of slice d*N + s are never
+ * sent); -1 in normal use. MOE_ERR_INVALID_ARG for R > 32, K < 0 or a bad withhold_slice. */
+size_t moe_dedicated_exchange_bytes(const moe_dims *dims);
+moe_status moe_dispatch_dedicated(const moe_dims *dims, const moe_layout_t *lay, const int32_t *d_idx,
+                                  const void *d_x, int32_t K, void *d_ded, void *d_xchg, void *d_main,
+                                  void *d_expert_x, float *d_expert_scale, int32_t withhold_slice, void *stream);
 
 /* Dispatch receive (section "Dispatch and combine": shuffle tokens from the receive buffer
  * into the tensor handed to the grouped GEMM): every receive row of rank d goes to row
