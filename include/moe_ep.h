@@ -229,7 +229,8 @@ moe_status moe_layout_init(const moe_dims *dims, void *d_ws, size_t ws_bytes, mo
  * aggregate the routing in shared memory into per-expert token counts, then their
  * cumulative sums as send offsets; the receiver centralises all ranks' routing and
  * computes the offsets for dispatch and combine). Reads d_idx [N][T][R] int32, fills every
- * array of *lay. Two kernels. */
+ * array of *lay. Three kernels: per-chunk counts and ranks (the last CTA of each source
+ * rank sums its chunks), the scans, the per-pair maps. */
 moe_status moe_layout(const moe_dims *dims, const int32_t *d_idx, const moe_layout_t *lay, void *stream);
 
 /* Block-scaled fp8 quantisation of the dispatch payload (section "Evaluation"): for each
@@ -244,7 +245,8 @@ moe_status moe_quantize_fp8_b128(const moe_dims *dims, const uint16_t *d_x, uint
  * routing with TransferEngine"): send[s][pos[s][t][k]] = x[s][t], then
  * recv[d][roff[d][s] + j] = send[s][soff[s][d*L] + j] for j < C[s][d].
  * d_x [N][T][B] (bf16 tokens, or fp8 rows from moe_quantize_fp8_b128), d_send [N][T*R][B],
- * d_recv [N][RB][B]. Receive rows at or beyond rtot[d] are not written. Two kernels. */
+ * d_recv [N][RB][B]. Receive rows at or beyond rtot[d] are not written. Two kernels (one
+ * with MOE_FLAG_DIRECT_PUSH). */
 moe_status moe_dispatch_send(const moe_dims *dims, const moe_layout_t *lay, const void *d_x, void *d_send,
                              void *d_recv, void *stream);
 
@@ -340,7 +342,7 @@ moe_status moe_expert_identity(const moe_dims *dims, const moe_layout_t *lay, co
  * csend[d][rrow(s,t,k)] = expert_y[d][l][slot(s,t,k)], then the write back
  * crecv[s][soff[s][d*L] + j] = csend[d][roff[d][s] + j]. d_expert_y [N][L][cap][H] bf16,
  * d_csend [N][RB][H] bf16, d_crecv [N][T*R][H] bf16. Pairs dropped for capacity are
- * skipped (their crecv rows are not written). Two kernels. */
+ * skipped (their crecv rows are not written). Two kernels (one with MOE_FLAG_DIRECT_PUSH). */
 moe_status moe_combine_send(const moe_dims *dims, const moe_layout_t *lay, const uint16_t *d_expert_y,
                             uint16_t *d_csend, uint16_t *d_crecv, void *stream);
 
