@@ -575,3 +575,31 @@ def test_dedicated_dispatch_withheld_slice_times_out_and_recovers(orc):
     code, _ = ep.status()
     assert code == 0
     _check_dedicated(orc, wl, inp, ep, 5)
+
+
+def _fuzz_cases(n, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        fp8 = rng.random() < 0.35
+        N = int(rng.integers(1, 9))
+        L = int(rng.integers(1, 13))
+        E = N * L
+        R = int(rng.integers(1, min(E, 12) + 1))
+        T = int(rng.integers(0, 40))
+        H = int(rng.choice([128, 256, 384, 1024, 1152])) if fp8 else int(8 * rng.integers(1, 160))
+        routing = str(rng.choice(["uniform", "zipf"] + (["skew0"] if R <= L else [])))
+        cap = int(rng.integers(1, N * T + 1)) if (T and rng.random() < 0.3) else 0
+        flags = int(rng.choice([0, 1, 4, 2, 8, 9, 12]))
+        out.append((W(f"fuzz{i}", N, T, H, E, R, "fp8" if fp8 else "bf16", routing, 300 + i, cap=cap), flags))
+    return out
+
+
+@pytest.mark.parametrize("wl,flags", _fuzz_cases(120, 31), ids=lambda v: v.name if hasattr(v, "name") else f"f{v}")
+def test_fuzz_shapes_and_flags(orc, wl, flags):
+    """Seeded random shapes (ranks, tokens incl. none, hidden sizes incl. rows that are not
+    16-byte multiples, experts, R, capacity, routing) and launch options (movers, no PDL,
+    direct push): every buffer bit for bit against the oracle."""
+    inp = workloads.make_inputs(wl)
+    _, res = run_gpu(wl, inp, flags=flags)
+    compare_all(orc, wl, inp, res, push=bool(flags & 8))
