@@ -24,6 +24,7 @@ MOE_FLAG_TMA_MOVER = 0x4
 MOE_FLAG_DIRECT_PUSH = 0x8
 MOE_FLAG_STAGED_QUANT = 0x10
 MOE_FLAG_HOST_STAGED = 0x20
+MOE_FLAG_HOST_ONE_BATCH = 0x40
 MOE_PROF_MAX = 32
 
 KERNEL_NAMES = ["route_count", "layout_maps", "quant_fp8", "pack", "scatter", "unpack", "expert",

@@ -24,9 +24,47 @@ struct DevInfo {
   int num_sms = 0;
   int smem_optin = 0;
   int smem_per_sm = 0;
+  // The host pass's second stream (highest priority) and its fork and join events, created
+  // on first use and kept until exit; fork_mu makes a fork (record, then wait) atomic.
+  cudaStream_t aux = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  std::mutex fork_mu;
 };
 DevInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
+
+DevInfo* aux_for(int dev) {
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevInfo& di = g_dev[dev];
+  if (!di.aux) {
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return nullptr;
+    cudaStream_t s = nullptr;
+    cudaEvent_t f = nullptr, j = nullptr;
+    if (cudaStreamCreateWithPriority(&s, cudaStreamNonBlocking, greatest) != cudaSuccess) return nullptr;
+    if (cudaEventCreateWithFlags(&f, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&j, cudaEventDisableTiming) != cudaSuccess) {
+      if (f) cudaEventDestroy(f);
+      cudaStreamDestroy(s);
+      return nullptr;
+    }
+    di.aux = s;
+    di.fork = f;
+    di.join = j;
+  }
+  return &di;
+}
+
+// The auxiliary stream starts after everything issued so far on `main`.
+bool fork_to(DevInfo* di, cudaStream_t main) {
+  std::lock_guard<std::mutex> lk(di->fork_mu);
+  return cudaEventRecord(di->fork, main) == cudaSuccess && cudaStreamWaitEvent(di->aux, di->fork, 0) == cudaSuccess;
+}
+
+// `main` continues after everything issued so far on the auxiliary stream.
+bool join_from(DevInfo* di, cudaStream_t main) {
+  return cudaEventRecord(di->join, di->aux) == cudaSuccess && cudaStreamWaitEvent(main, di->join, 0) == cudaSuccess;
+}
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -431,6 +469,56 @@ moe_status moe_forward(const moe_dims* dims, const moe_layout_t* lay, const moe_
   return moe_combine_recv(dims, lay, b->crecv, b->w, b->out, stream);
 }
 
+// The whole pass in two token batches (tokens [0, T/2) and [T/2, T) of every rank) so that
+// the host-link-bound kernels of one batch overlap the HBM-bound moves of the other: the
+// pack of batch B (reading tokens over the host link) runs while batch A is scattered and
+// unpacked on the second stream, and the reduce of batch A (writing the output over the
+// link) runs there while batch B's combine send runs. The two batches touch disjoint rows
+// of every buffer (also when the combine buffers alias the dispatch ones).
+moe_status forward_two_batches(const Geo& g, const moe_dims* dims, const moe_layout_t* lay, const moe_buffers_t* b,
+                               void* stream) {
+  const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
+  if (!layout_ok(lay) || !b->x || !b->idx || !b->w || !b->send || !b->recv || !b->expert_x || !b->expert_y ||
+      !b->csend || !b->crecv || !b->out || !aligned16(b->x) || !aligned16(b->send) || !aligned16(b->recv) ||
+      !aligned16(b->expert_x) || !aligned16(b->expert_y) || !aligned16(b->csend) || !aligned16(b->crecv) ||
+      !aligned16(b->out) || (fp8 && (!b->expert_scale || !aligned16(b->expert_scale))))
+    return MOE_ERR_INVALID_ARG;
+  moe_status st = moe_layout(dims, b->idx, lay, stream);
+  if (st != MOE_OK) return st;
+  Ctx c;
+  if ((st = make_ctx(lay, stream, c)) != MOE_OK) return st;
+  DevInfo* di = aux_for(c.device);
+  if (!di) return MOE_ERR_CUDA;
+  Ctx ca = c;
+  ca.stream = di->aux;
+  const int ta = g.T / 2, tb = g.T - ta;
+  auto pack = [&](int t0, int nt) {
+    return fp8 ? launch_quant_pack(g, lay->gsend, b->x, static_cast<uint8_t*>(b->send), c, t0, nt)
+               : launch_move_range(kMovePack, g, lay, b->x, b->send, nullptr, t0, nt, c);
+  };
+  auto recv_half = [&](int t0, int nt, Ctx& cc) {
+    cudaError_t e = launch_move_range(kMoveScatter, g, lay, b->send, b->recv, nullptr, t0, nt, cc);
+    if (e == cudaSuccess)
+      e = launch_move_range(kMoveUnpack, g, lay, b->recv, b->expert_x, fp8 ? b->expert_scale : nullptr, t0, nt, cc);
+    return e;
+  };
+  auto combine_send_half = [&](int t0, int nt) {
+    cudaError_t e = launch_move_range(kMoveCPack, g, lay, b->expert_y, b->csend, nullptr, t0, nt, c);
+    if (e == cudaSuccess) e = launch_move_range(kMoveCScatter, g, lay, b->csend, b->crecv, nullptr, t0, nt, c);
+    return e;
+  };
+  if (pack(0, ta) != cudaSuccess || !fork_to(di, c.stream) || pack(ta, tb) != cudaSuccess ||
+      recv_half(0, ta, ca) != cudaSuccess || recv_half(ta, tb, c) != cudaSuccess || !join_from(di, c.stream))
+    return MOE_ERR_CUDA;
+  if ((st = moe_expert_identity(dims, lay, b->expert_x, b->expert_scale, b->expert_y, stream)) != MOE_OK) return st;
+  if (combine_send_half(0, ta) != cudaSuccess || !fork_to(di, c.stream) ||
+      launch_combine_reduce(g, lay, b->crecv, b->w, b->out, ca, 0, ta) != cudaSuccess ||
+      combine_send_half(ta, tb) != cudaSuccess ||
+      launch_combine_reduce(g, lay, b->crecv, b->w, b->out, c, ta, tb) != cudaSuccess || !join_from(di, c.stream))
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
 moe_status moe_forward_host(const moe_dims* dims, const moe_layout_t* lay, const moe_buffers_t* b, const uint16_t* h_x,
                             const int32_t* h_idx, const float* h_w, uint16_t* h_out, void* stream) {
   if (!b) return MOE_ERR_INVALID_ARG;
@@ -450,7 +538,9 @@ moe_status moe_forward_host(const moe_dims* dims, const moe_layout_t* lay, const
       m.idx = static_cast<int32_t*>(didx);
       m.w = static_cast<float*>(dw);
       m.out = static_cast<uint16_t*>(dout);
-      return moe_forward(dims, lay, &m, stream);
+      const bool two = g.T >= 2 && !(lay->flags & (MOE_FLAG_HOST_ONE_BATCH | MOE_FLAG_DIRECT_PUSH)) &&
+                       !(g.payload == MOE_PAYLOAD_FP8_E4M3_B128 && (lay->flags & MOE_FLAG_STAGED_QUANT));
+      return two ? forward_two_batches(g, dims, lay, &m, stream) : moe_forward(dims, lay, &m, stream);
     }
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);

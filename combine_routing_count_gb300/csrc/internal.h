@@ -105,11 +105,17 @@ enum MoveKind : int {
 };
 cudaError_t launch_move(MoveKind kind, const Geo& g, const moe_layout_t* lay, const void* src, void* dst,
                         void* dst2, Ctx& c);
+// The same move over the token range [t0, t0 + nt) of every rank only (its tokens for a
+// pack, its pairs otherwise).
+cudaError_t launch_move_range(MoveKind kind, const Geo& g, const moe_layout_t* lay, const void* src, void* dst,
+                              void* dst2, int t0, int nt, Ctx& c);
 
 // numerics.cu
 cudaError_t launch_quant_fp8(const Geo& g, const uint16_t* x, uint8_t* xq, Ctx& c);
 // Quantise bf16 token rows and write each one's fp8 row into dst rows fan[token][k] (k < R).
-cudaError_t launch_quant_pack(const Geo& g, const int32_t* fan, const uint16_t* x, uint8_t* dst, Ctx& c);
+// t0, nt: only the token range [t0, t0 + nt) of every rank (nt < 0: all tokens).
+cudaError_t launch_quant_pack(const Geo& g, const int32_t* fan, const uint16_t* x, uint8_t* dst, Ctx& c, int t0 = 0,
+                              int nt = -1);
 cudaError_t launch_dequant_fp8(const Geo& g, const moe_layout_t* lay, const uint8_t* exq, const float* exs,
                                uint16_t* ey, Ctx& c);
 cudaError_t launch_combine_partial(const Geo& g, const moe_layout_t* lay, const uint16_t* ey, const float* w,
@@ -117,6 +123,6 @@ cudaError_t launch_combine_partial(const Geo& g, const moe_layout_t* lay, const 
 cudaError_t launch_combine_sum(const Geo& g, const moe_layout_t* lay, const uint16_t* cpart, uint16_t* out,
                                Ctx& c);
 cudaError_t launch_combine_reduce(const Geo& g, const moe_layout_t* lay, const uint16_t* crecv, const float* w,
-                                  uint16_t* out, Ctx& c);
+                                  uint16_t* out, Ctx& c, int t0 = 0, int nt = -1);   // t0, nt as launch_quant_pack
 
 }  // namespace moe

@@ -36,6 +36,7 @@ struct MoveArgs {
   const int32_t* grecv;   // per pair: global receive row, or -1
   const int32_t* gslot;   // per pair: global grouped row, or -1
   const int32_t* fan;     // pack: per pair, the destination row (gsend, or grecv for direct push)
+  int t0, nt;             // token range [t0, t0 + nt) of every rank that the move covers
   int32_t* status;
   int64_t units;
   uint32_t stage_bytes;
@@ -61,13 +62,25 @@ __host__ __device__ __forceinline__ uint32_t unit_bytes(const Geo& g, const Move
 }
 
 // Fills `pl` for unit u; false when the unit moves nothing (bad expert id or dropped pair).
-template <int KIND, bool FP8>
+// The global index (token for per = 1, pair for per = R) of item v of the token range
+// [t0, t0 + nt) of every rank, items rank-major. RANGED is a compile-time choice, so moves
+// over all tokens compile to the identity.
+template <bool RANGED>
+__device__ __forceinline__ int64_t range_item(const Geo& g, const MoveArgs& a, int64_t v, int per) {
+  if (!RANGED) return v;
+  const int64_t span = (int64_t)a.nt * per;
+  const int64_t s = v / span;
+  return (s * g.T + a.t0) * per + (v - s * span);
+}
+
+template <int KIND, bool FP8, bool RANGED>
 __device__ __forceinline__ bool make_plan(const Geo& g, const MoveArgs& a, int64_t u, Plan& pl) {
   const int64_t H2 = 2 * (int64_t)g.H;
   if (KIND == kMovePack || KIND == kMovePackPush) {
-    const int64_t tok = u / a.chunks;
+    const int64_t tv = u / a.chunks;
+    const int64_t tok = range_item<RANGED>(g, a, tv, 1);
     pl.tok = tok;
-    pl.coff = (int32_t)((u - tok * a.chunks) * a.chunk_bytes);
+    pl.coff = (int32_t)((u - tv * a.chunks) * a.chunk_bytes);
     pl.src = a.src + tok * g.B + pl.coff;
 #pragma unroll
     for (int k = 0; k < kPackPrefetch; ++k) pl.p[k] = (k < g.R) ? __ldg(a.fan + tok * g.R + k) : -1;
@@ -76,7 +89,7 @@ __device__ __forceinline__ bool make_plan(const Geo& g, const MoveArgs& a, int64
   // Non-pack kinds: unit u is column chunk (u % chunks) of pair u / chunks.
   const int64_t cq = u / a.chunks;
   const int64_t coff = (u - cq * a.chunks) * (int64_t)a.chunk_bytes;
-  u = cq;
+  u = range_item<RANGED>(g, a, cq, g.R);
   if (KIND == kMoveScatter) {
     const int gs = __ldg(a.gsend + u);
     const int gr = __ldg(a.grecv + u);
@@ -163,7 +176,7 @@ __device__ __forceinline__ void bulk_wait_read_1() {
   asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 
-template <int KIND, bool FP8>
+template <int KIND, bool FP8, bool RANGED>
 __global__ void __launch_bounds__(kIssuers * 32) k_move_tma(Geo g, MoveArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -183,7 +196,7 @@ __global__ void __launch_bounds__(kIssuers * 32) k_move_tma(Geo g, MoveArgs a) {
     uint32_t vbits = 0, pbits = 0;   // per stage: a load is in flight; the barrier's parity
     Plan pl;
     for (int k = 0; k < S && k < n; ++k) {
-      const bool ok = make_plan<KIND, FP8>(g, a, gi + k * G, pl);
+      const bool ok = make_plan<KIND, FP8, RANGED>(g, a, gi + k * G, pl);
       sp[k] = StagePlan{pl.dst, pl.dst2, pl.tok, pl.coff, {}};
       if (KIND == kMovePack || KIND == kMovePackPush)
         for (int r = 0; r < kPackPrefetch; ++r) sp[k].p[r] = pl.p[r];
@@ -194,7 +207,7 @@ __global__ void __launch_bounds__(kIssuers * 32) k_move_tma(Geo g, MoveArgs a) {
       }
     }
     Plan nx;
-    bool nx_ok = (S < n) && make_plan<KIND, FP8>(g, a, gi + S * G, nx);
+    bool nx_ok = (S < n) && make_plan<KIND, FP8, RANGED>(g, a, gi + S * G, nx);
     for (int64_t j = 0; j < n; ++j) {
       const int k = (int)(j % S);
       bool stored = false;
@@ -229,7 +242,7 @@ __global__ void __launch_bounds__(kIssuers * 32) k_move_tma(Geo g, MoveArgs a) {
           bulk_g2s(ring + (size_t)kp * a.stage_bytes, nx.src, bytes, &bar[kp]);
           vbits |= 1u << kp;
         }
-        nx_ok = (jr + 1 < n) && make_plan<KIND, FP8>(g, a, gi + (jr + 1) * G, nx);
+        nx_ok = (jr + 1 < n) && make_plan<KIND, FP8, RANGED>(g, a, gi + (jr + 1) * G, nx);
       }
     }
     pdl_trigger();
@@ -250,7 +263,7 @@ __device__ __forceinline__ uint32_t ld_vec<uint32_t>(const uint8_t* p) {
 __device__ __forceinline__ void st_vec(uint8_t* p, const uint4& v) { st16(p, v); }
 __device__ __forceinline__ void st_vec(uint8_t* p, const uint32_t& v) { *reinterpret_cast<uint32_t*>(p) = v; }
 
-template <int KIND, bool FP8, typename V>
+template <int KIND, bool FP8, typename V, bool RANGED>
 __global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
   constexpr int U = 8;
   constexpr int W = (int)sizeof(V);
@@ -263,8 +276,9 @@ __global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
     // Pack: lane k holds the destination row of the token's pair k and broadcasts it by
     // shuffle, so a warp keeps only its U loaded vectors live while it writes R copies.
     for (int64_t u = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < a.units; u += nwarps) {
-      const int64_t tok = u / a.chunks;
-      const int64_t coff = (u - tok * a.chunks) * (int64_t)a.chunk_bytes;
+      const int64_t tv = u / a.chunks;
+      const int64_t tok = range_item<RANGED>(g, a, tv, 1);
+      const int64_t coff = (u - tv * a.chunks) * (int64_t)a.chunk_bytes;
       const uint8_t* src = a.src + tok * g.B + coff;
       uint8_t* dst0 = a.dst + coff;
       const int32_t* fan = a.fan + tok * g.R;
@@ -296,7 +310,7 @@ __global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
   }
   for (int64_t u = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < a.units; u += nwarps) {
     Plan pl;
-    if (!make_plan<KIND, FP8>(g, a, u, pl)) continue;
+    if (!make_plan<KIND, FP8, RANGED>(g, a, u, pl)) continue;
     for (int64_t v0 = lane; v0 < nel; v0 += 32 * U) {
       V r[U];
 #pragma unroll
@@ -323,12 +337,12 @@ __global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
 }
 
 // Largest dynamic shared memory limit set so far, per TMA instantiation and device.
-std::atomic<int> g_tma_smem[8][2][64];
+std::atomic<int> g_tma_smem[8][2][2][64];
 
 // Stages per issuer and CTAs per SM: as many CTAs as fit with 3 stages per issuer (at
 // most 8 CTAs), then as many stages as the shared memory of each CTA holds (2..8). Each
 // CTA also pays 1 KB of reserved shared memory and its mbarrier/plan header.
-template <int KIND, bool FP8>
+template <int KIND, bool FP8, bool RANGED>
 cudaError_t run_tma(const Geo& g, MoveArgs a, Ctx& c) {
   const uint32_t bytes = unit_bytes<KIND>(g, a);
   const int stage_bytes = (int)((bytes + 127u) & ~127u);
@@ -348,7 +362,8 @@ cudaError_t run_tma(const Geo& g, MoveArgs a, Ctx& c) {
   if (S < 2) return cudaErrorInvalidValue;
   const size_t smem = kTmaHeader + (size_t)kIssuers * S * stage_bytes;
   {
-    cudaError_t e = ensure_dyn_smem(k_move_tma<KIND, FP8>, c.device, smem, g_tma_smem[KIND][FP8 ? 1 : 0]);
+    cudaError_t e = ensure_dyn_smem(k_move_tma<KIND, FP8, RANGED>, c.device, smem,
+                                    g_tma_smem[KIND][FP8 ? 1 : 0][RANGED ? 1 : 0]);
     if (e != cudaSuccess) return e;
   }
   a.stages = S;
@@ -356,17 +371,17 @@ cudaError_t run_tma(const Geo& g, MoveArgs a, Ctx& c) {
   int64_t grid = (int64_t)c.num_sms * cps;
   const int64_t need = (a.units + kIssuers - 1) / kIssuers;
   if (grid > need) grid = need;
-  return launch_kernel(k_move_tma<KIND, FP8>, dim3((unsigned)grid), dim3(kIssuers * 32), smem, c, g, a);
+  return launch_kernel(k_move_tma<KIND, FP8, RANGED>, dim3((unsigned)grid), dim3(kIssuers * 32), smem, c, g, a);
 }
 
-template <int KIND, bool FP8, typename V>
+template <int KIND, bool FP8, typename V, bool RANGED>
 cudaError_t run_ldg(const Geo& g, const MoveArgs& a, Ctx& c) {
   // Four waves of the CTAs the SMs hold at once (registers decide): warps that finish early
   // take later units, which measured faster on GB300 than one wave of grid-stride loops.
   static std::atomic<int> resident{0};
   int per_sm = resident.load(std::memory_order_relaxed);
   if (per_sm == 0) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_move_ldg<KIND, FP8, V>, 256, 0) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_move_ldg<KIND, FP8, V, RANGED>, 256, 0) != cudaSuccess ||
         per_sm < 1)
       per_sm = 1;
     resident.store(per_sm, std::memory_order_relaxed);
@@ -375,7 +390,7 @@ cudaError_t run_ldg(const Geo& g, const MoveArgs& a, Ctx& c) {
   int64_t blocks = (a.units + 7) / 8;
   const int64_t maxb = (int64_t)c.num_sms * per_sm;
   if (blocks > maxb) blocks = maxb;
-  return launch_kernel(k_move_ldg<KIND, FP8, V>, dim3((unsigned)blocks), dim3(256), 0, c, g, a);
+  return launch_kernel(k_move_ldg<KIND, FP8, V, RANGED>, dim3((unsigned)blocks), dim3(256), 0, c, g, a);
 }
 
 // True when two stages per issuer fit in one CTA's shared memory.
@@ -396,20 +411,52 @@ bool tma_default(const MoveArgs& a, const Ctx& c) {
   return a.units / a.chunks >= 40LL * kIssuers * c.num_sms;
 }
 
-template <int KIND, bool FP8>
+template <int KIND, bool FP8, bool RANGED>
 cudaError_t run_kind(const Geo& g, const MoveArgs& a, Ctx& c, bool row16) {
   const bool want_tma = (c.flags & MOE_FLAG_TMA_MOVER) ? true
                         : (c.flags & MOE_FLAG_LDG_MOVER) ? false
                                                           : tma_default<KIND>(a, c);
-  if (row16 && want_tma && tma_fits<KIND>(g, a, c)) return run_tma<KIND, FP8>(g, a, c);
-  if (row16) return run_ldg<KIND, FP8, uint4>(g, a, c);
-  return run_ldg<KIND, FP8, uint32_t>(g, a, c);
+  if (row16 && want_tma && tma_fits<KIND>(g, a, c)) return run_tma<KIND, FP8, RANGED>(g, a, c);
+  if (row16) return run_ldg<KIND, FP8, uint4, RANGED>(g, a, c);
+  return run_ldg<KIND, FP8, uint32_t, RANGED>(g, a, c);
+}
+
+}  // namespace
+
+namespace {
+
+template <bool R>
+cudaError_t run_move(MoveKind kind, const Geo& g, const MoveArgs& a, Ctx& c, bool fp8, bool rowB16) {
+  switch (kind) {
+    case kMovePack:
+      return run_kind<kMovePack, false, R>(g, a, c, rowB16);
+    case kMoveScatter:
+      return run_kind<kMoveScatter, false, R>(g, a, c, rowB16);
+    case kMoveUnpack:
+      return fp8 ? run_kind<kMoveUnpack, true, R>(g, a, c, rowB16) : run_kind<kMoveUnpack, false, R>(g, a, c, rowB16);
+    case kMoveCPack:
+      return run_kind<kMoveCPack, false, R>(g, a, c, true);
+    case kMoveCScatter:
+      return run_kind<kMoveCScatter, false, R>(g, a, c, true);
+    case kMoveCopyEx:
+      return run_kind<kMoveCopyEx, false, R>(g, a, c, true);
+    case kMovePackPush:
+      return run_kind<kMovePackPush, false, R>(g, a, c, rowB16);
+    case kMoveCPush:
+      return run_kind<kMoveCPush, false, R>(g, a, c, true);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
 cudaError_t launch_move(MoveKind kind, const Geo& g, const moe_layout_t* lay, const void* src, void* dst, void* dst2,
                         Ctx& c) {
+  return launch_move_range(kind, g, lay, src, dst, dst2, 0, g.T, c);
+}
+
+cudaError_t launch_move_range(MoveKind kind, const Geo& g, const moe_layout_t* lay, const void* src, void* dst,
+                              void* dst2, int t0, int nt, Ctx& c) {
   MoveArgs a;
   a.src = static_cast<const uint8_t*>(src);
   a.dst = static_cast<uint8_t*>(dst);
@@ -418,6 +465,8 @@ cudaError_t launch_move(MoveKind kind, const Geo& g, const moe_layout_t* lay, co
   a.grecv = lay->grecv;
   a.gslot = lay->gslot;
   a.fan = kind == kMovePackPush ? lay->grecv : lay->gsend;
+  a.t0 = 0;
+  a.nt = g.T;
   a.status = lay->status;
   a.stages = 0;
   a.stage_bytes = 0;
@@ -450,30 +499,17 @@ cudaError_t launch_move(MoveKind kind, const Geo& g, const moe_layout_t* lay, co
     a.chunk_bytes = (uint32_t)(rowb / a.chunks);
     a.units = g.P * a.chunks;
   }
+  if (nt != g.T) {   // a token range of every rank: its tokens, or its pairs
+    a.t0 = t0;
+    a.nt = nt;
+    a.units = (int64_t)g.N * nt * (kind == kMovePack || kind == kMovePackPush ? 1 : g.R) * a.chunks;
+  }
   if (a.units == 0) return cudaSuccess;
   static const moe_kernel_id ids[] = {MOE_K_PACK,         MOE_K_SCATTER,         MOE_K_UNPACK,
                                       MOE_K_COMBINE_PACK, MOE_K_COMBINE_SCATTER, MOE_K_EXPERT,
                                       MOE_K_PACK_PUSH,    MOE_K_COMBINE_PUSH};
   LaunchScope ls(c, ids[kind]);
-  switch (kind) {
-    case kMovePack:
-      return run_kind<kMovePack, false>(g, a, c, rowB16);
-    case kMoveScatter:
-      return run_kind<kMoveScatter, false>(g, a, c, rowB16);
-    case kMoveUnpack:
-      return fp8 ? run_kind<kMoveUnpack, true>(g, a, c, rowB16) : run_kind<kMoveUnpack, false>(g, a, c, rowB16);
-    case kMoveCPack:
-      return run_kind<kMoveCPack, false>(g, a, c, true);
-    case kMoveCScatter:
-      return run_kind<kMoveCScatter, false>(g, a, c, true);
-    case kMoveCopyEx:
-      return run_kind<kMoveCopyEx, false>(g, a, c, true);
-    case kMovePackPush:
-      return run_kind<kMovePackPush, false>(g, a, c, rowB16);
-    case kMoveCPush:
-      return run_kind<kMoveCPush, false>(g, a, c, true);
-  }
-  return cudaErrorInvalidValue;
+  return nt != g.T ? run_move<true>(kind, g, a, c, fp8, rowB16) : run_move<false>(kind, g, a, c, fp8, rowB16);
 }
 
 }  // namespace moe

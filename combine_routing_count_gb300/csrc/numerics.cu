@@ -228,20 +228,23 @@ __global__ void __launch_bounds__(256) k_quant_fp8(Geo g, const uint16_t* __rest
 // registers, and writes them into the R rows fan[token][k] of dst (send rows, or receive rows
 // when pushing), so the fp8 rows are never staged in HBM. The bytes each row gets are those
 // moe_quantize_fp8_b128 writes. W8: rows are 8-byte aligned (8-byte code stores).
-template <bool W8>
+// RANGED: only the token range [t0, t0 + nt) of every rank (else every token; t0, nt unused).
+template <bool W8, bool RANGED>
 __global__ void __launch_bounds__(256) k_quant_pack(Geo g, const uint16_t* __restrict__ x,
-                                                    const int32_t* __restrict__ fan, uint8_t* __restrict__ dst) {
+                                                    const int32_t* __restrict__ fan, uint8_t* __restrict__ dst,
+                                                    int t0, int nt) {
   const int nb = g.H / 128;
   const int upr = (nb + 2 * kQuantUnroll - 1) / (2 * kQuantUnroll);
-  const int64_t units = (int64_t)g.N * g.T * upr;
+  const int64_t units = (int64_t)g.N * (RANGED ? nt : g.T) * upr;
   const int lane = threadIdx.x & 31;
   const int sub = lane & 15;
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   pdl_wait();
   for (int64_t u = warp; u < units; u += nwarps) {   // warp-uniform
-    const int64_t row = units <= INT32_MAX ? (int64_t)((uint32_t)u / (uint32_t)upr) : u / upr;
-    const int bbase = (int)(u - row * upr) * 2 * kQuantUnroll + (lane >> 4);
+    const int64_t rv = units <= INT32_MAX ? (int64_t)((uint32_t)u / (uint32_t)upr) : u / upr;
+    const int bbase = (int)(u - rv * upr) * 2 * kQuantUnroll + (lane >> 4);
+    const int64_t row = RANGED ? (rv / nt) * g.T + t0 + rv % nt : rv;   // token
     const int32_t* fr = fan + row * g.R;
     const int myp = lane < g.R ? __ldg(fr + lane) : -1;   // rows of pairs 0..31 (R > 32: loaded)
     uint32_t codes[kQuantUnroll][2];
@@ -376,14 +379,17 @@ __device__ __forceinline__ void store_bf16x8(uint16_t* p, const float (&acc)[8])
 // R rows are gathered with up to 8 loads in flight; fp32 products and sums are rounded
 // separately in slot order (packed f32x2 pairs, each lane rounded as the scalar op);
 // dropped or invalid pairs are skipped.
+// RANGED: block x covers token x of the range [t0, t0 + nt) of every rank, rank-major (else
+// token x; t0, nt unused).
 constexpr int kReduceThreads = 128;
 
+template <bool RANGED>
 __global__ void __launch_bounds__(kReduceThreads) k_combine_reduce(Geo g, const int32_t* __restrict__ gsend,
                                                                    const int32_t* __restrict__ gslot,
                                                                    const float* __restrict__ w,
                                                                    const uint16_t* __restrict__ crecv,
-                                                                   uint16_t* __restrict__ out) {
-  const int64_t u = blockIdx.x;
+                                                                   uint16_t* __restrict__ out, int t0, int nt) {
+  const int64_t u = RANGED ? (int64_t)(blockIdx.x / nt) * g.T + t0 + blockIdx.x % nt : (int64_t)blockIdx.x;
   const int col = blockIdx.y * kReduceThreads + threadIdx.x;
   const int ncol = g.H / 8;
   const bool act = col < ncol;
@@ -649,17 +655,20 @@ cudaError_t launch_quant_fp8(const Geo& g, const uint16_t* x, uint8_t* xq, Ctx& 
   return launch_kernel(k_quant_fp8, dim3((unsigned)blocks), dim3(256), 0, c, g, x, xq);
 }
 
-cudaError_t launch_quant_pack(const Geo& g, const int32_t* fan, const uint16_t* x, uint8_t* dst, Ctx& c) {
+cudaError_t launch_quant_pack(const Geo& g, const int32_t* fan, const uint16_t* x, uint8_t* dst, Ctx& c, int t0,
+                              int nt) {
+  if (nt < 0) nt = g.T;
   const int64_t upr = (g.H / 128 + 2 * kQuantUnroll - 1) / (2 * kQuantUnroll);
-  const int64_t units = (int64_t)g.N * g.T * upr;
+  const int64_t units = (int64_t)g.N * nt * upr;
   if (units == 0) return cudaSuccess;
   int64_t blocks = (units + 7) / 8;
   const int64_t maxb = (int64_t)c.num_sms * 8;
   if (blocks > maxb) blocks = maxb;
   LaunchScope ls(c, MOE_K_QUANT_PACK);
-  if (g.B % 8 == 0)
-    return launch_kernel(k_quant_pack<true>, dim3((unsigned)blocks), dim3(256), 0, c, g, x, fan, dst);
-  return launch_kernel(k_quant_pack<false>, dim3((unsigned)blocks), dim3(256), 0, c, g, x, fan, dst);
+  const bool ranged = nt != g.T;
+  auto k = g.B % 8 == 0 ? (ranged ? k_quant_pack<true, true> : k_quant_pack<true, false>)
+                        : (ranged ? k_quant_pack<false, true> : k_quant_pack<false, false>);
+  return launch_kernel(k, dim3((unsigned)blocks), dim3(256), 0, c, g, x, fan, dst, t0, nt);
 }
 
 cudaError_t launch_dequant_fp8(const Geo& g, const moe_layout_t* lay, const uint8_t* exq, const float* exs,
@@ -674,14 +683,16 @@ cudaError_t launch_dequant_fp8(const Geo& g, const moe_layout_t* lay, const uint
 }
 
 cudaError_t launch_combine_reduce(const Geo& g, const moe_layout_t* lay, const uint16_t* crecv, const float* w,
-                                  uint16_t* out, Ctx& c) {
-  const int64_t tokens = (int64_t)g.N * g.T;
+                                  uint16_t* out, Ctx& c, int t0, int nt) {
+  if (nt < 0) nt = g.T;
+  const int64_t tokens = (int64_t)g.N * nt;
   if (tokens == 0) return cudaSuccess;
   const int ncol = g.H / 8;
   dim3 grid((unsigned)tokens, (unsigned)((ncol + kReduceThreads - 1) / kReduceThreads));
   LaunchScope ls(c, MOE_K_COMBINE_REDUCE);
-  return launch_kernel(k_combine_reduce, grid, dim3(kReduceThreads), 0, c, g, (const int32_t*)lay->gsend,
-                       (const int32_t*)lay->gslot, w, crecv, out);
+  return launch_kernel(nt != g.T ? k_combine_reduce<true> : k_combine_reduce<false>, grid, dim3(kReduceThreads), 0, c,
+                       g, (const int32_t*)lay->gsend,
+                       (const int32_t*)lay->gslot, w, crecv, out, t0, nt);
 }
 
 }  // namespace moe

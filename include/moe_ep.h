@@ -125,6 +125,11 @@ typedef struct {
 /* moe_forward_host: copy host inputs into the device buffers and the output back with copy
  * engines, even when the host buffers are device-accessible. */
 #define MOE_FLAG_HOST_STAGED 0x20u
+/* moe_forward_host on device-accessible host memory: run the pass as one batch on the
+ * caller's stream, instead of the default two token batches whose host-link-bound kernels
+ * (the pack reading the tokens, the reduce writing the output) overlap the other batch's
+ * HBM-bound moves on a second stream of the library. */
+#define MOE_FLAG_HOST_ONE_BATCH 0x40u
 #define MOE_FLAG_NO_PDL 0x2u    /* launch without programmatic dependent launch (by default
                                    each kernel may be scheduled while its predecessor in the
                                    stream drains; it waits for it before touching memory) */
@@ -382,7 +387,13 @@ moe_status moe_forward(const moe_dims *dims, const moe_layout_t *lay, const moe_
  * output h_out [N][T][H]. When all four are pinned host memory that the device can address
  * (cudaHostAlloc / cudaHostRegister; over NVLink-C2C on Grace-Blackwell), the kernels read
  * the inputs and write the output there directly: each input byte crosses the host link
- * once, when the kernel that needs it loads it, and bufs->x/idx/w/out are not used.
+ * once, when the kernel that needs it loads it, and bufs->x/idx/w/out are not used. With
+ * T >= 2 (and neither direct push, staged fp8 quantisation nor MOE_FLAG_HOST_ONE_BATCH)
+ * the pass runs in two token batches, the second stream of the library (created on the
+ * first such call per device with two events, kept until exit) taking the scatter and
+ * unpack of the first batch and its reduce while the caller's stream packs and sends the
+ * second; the caller's stream waits for it before the call returns, so `stream` orders
+ * everything as usual (and the pass can be captured into a CUDA graph).
  * Otherwise, or with MOE_FLAG_HOST_STAGED, cudaMemcpyAsync copies the inputs into
  * bufs->x/idx/w, the pass runs, and bufs->out is copied into h_out. Asynchronous: the caller
  * synchronises `stream` before reading h_out. */

@@ -126,16 +126,18 @@ def test_invalid_arguments_launch_nothing():
     assert L.moe_launch_count() == n0
 
 
-@pytest.mark.parametrize("mode", ["mapped", "staged", "pageable"])
+@pytest.mark.parametrize("mode", ["mapped", "mapped-one-batch", "mapped-cap", "staged", "pageable"])
 @pytest.mark.parametrize("payload", ["bf16", "fp8"])
 def test_forward_host_matches_device_path(orc, mode, payload):
-    """Host inputs and output: pinned memory read and written by the kernels directly
-    (default), copied by copy engines (MOE_FLAG_HOST_STAGED), or pageable (copied)."""
-    wl = W("host-e2e", 4, 29, 2048, 16, 4, payload, "zipf", 120)
+    """Host inputs and output: pinned memory read and written by the kernels directly, in
+    two token batches on two streams (default) or one (MOE_FLAG_HOST_ONE_BATCH), copied by
+    copy engines (MOE_FLAG_HOST_STAGED), or pageable (copied); an odd token count with
+    capacity drops for the batched pass."""
+    wl = W("host-e2e", 4, 29, 2048, 16, 4, payload, "zipf", 120, cap=(9 if mode == "mapped-cap" else 0))
     inp = workloads.make_inputs(wl)
     from combine_routing_count_gb300 import MoeEP
-    ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, payload=payload, alias_buffers=(payload == "bf16"),
-               flags=0x20 if mode == "staged" else 0)
+    ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, payload=payload, alias_buffers=(payload == "bf16"),
+               flags={"staged": 0x20, "mapped-one-batch": 0x40}.get(mode, 0))
     pin = (lambda t: t) if mode == "pageable" else (lambda t: t.pin_memory())
     h_x = pin(torch.from_numpy(inp["x"]).view(torch.bfloat16))
     h_idx = pin(torch.from_numpy(inp["idx"]))
@@ -145,10 +147,11 @@ def test_forward_host_matches_device_path(orc, mode, payload):
     idx = torch.empty_like(h_idx, device="cuda")
     w = torch.empty_like(h_w, device="cuda")
     for _ in range(2):
+        h_out.view(torch.int16).fill_(-1)
         ep.forward_host(h_x, h_idx, h_w, h_out, x, idx, w)
         code, _ = ep.status()
-        assert code == 0
-        o = orc.forward(wl.N, wl.T, wl.H, wl.E, wl.R, 0, payload, inp["x"], inp["idx"], inp["w"])
+        assert code in (0, 3)   # 3: capacity drops of the mapped-cap case
+        o = orc.forward(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, payload, inp["x"], inp["idx"], inp["w"])
         np.testing.assert_array_equal(u16(h_out), o["out"])
 
 
