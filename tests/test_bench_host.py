@@ -70,3 +70,15 @@ def test_reference_arm_other_ranks_exit_quietly():
                         "--steps", "2", "--warmup", "1"], capture_output=True, text=True, timeout=300, cwd=ROOT,
                        env=env)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_cpu_baseline_reports_single_thread_and_all_cores():
+    wl = workloads.config(0)
+    inp = workloads.make_inputs(wl)
+    cb = bench.cpu_baseline(wl, inp, 0.2)
+    out = cb.pop("out")
+    assert out.shape == (wl.N, wl.T, wl.H)
+    assert cb["cores"] == 1 and cb["value"] > 0
+    ac = cb["all_cores"]
+    assert ac["kind"] == "oracle" and ac["cores"] >= 1 and ac["value"] > 0
+    assert f"{ac['cores']} threads" in ac["sample"]
