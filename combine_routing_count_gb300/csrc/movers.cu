@@ -73,8 +73,9 @@ __device__ __forceinline__ int64_t range_item(const Geo& g, const MoveArgs& a, i
   return (s * g.T + a.t0) * per + (v - s * span);
 }
 
-template <int KIND, bool FP8, bool RANGED>
+template <int KIND, bool FP8, bool RANGED, bool REV>
 __device__ __forceinline__ bool make_plan(const Geo& g, const MoveArgs& a, int64_t u, Plan& pl) {
+  if (REV) u = a.units - 1 - u;
   const int64_t H2 = 2 * (int64_t)g.H;
   if (KIND == kMovePack || KIND == kMovePackPush) {
     const int64_t tv = u / a.chunks;
@@ -176,7 +177,7 @@ __device__ __forceinline__ void bulk_wait_read_1() {
   asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 
-template <int KIND, bool FP8, bool RANGED>
+template <int KIND, bool FP8, bool RANGED, bool REV>
 __global__ void __launch_bounds__(kIssuers * 32) k_move_tma(Geo g, MoveArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -196,7 +197,7 @@ __global__ void __launch_bounds__(kIssuers * 32) k_move_tma(Geo g, MoveArgs a) {
     uint32_t vbits = 0, pbits = 0;   // per stage: a load is in flight; the barrier's parity
     Plan pl;
     for (int k = 0; k < S && k < n; ++k) {
-      const bool ok = make_plan<KIND, FP8, RANGED>(g, a, gi + k * G, pl);
+      const bool ok = make_plan<KIND, FP8, RANGED, REV>(g, a, gi + k * G, pl);
       sp[k] = StagePlan{pl.dst, pl.dst2, pl.tok, pl.coff, {}};
       if (KIND == kMovePack || KIND == kMovePackPush)
         for (int r = 0; r < kPackPrefetch; ++r) sp[k].p[r] = pl.p[r];
@@ -207,7 +208,7 @@ __global__ void __launch_bounds__(kIssuers * 32) k_move_tma(Geo g, MoveArgs a) {
       }
     }
     Plan nx;
-    bool nx_ok = (S < n) && make_plan<KIND, FP8, RANGED>(g, a, gi + S * G, nx);
+    bool nx_ok = (S < n) && make_plan<KIND, FP8, RANGED, REV>(g, a, gi + S * G, nx);
     for (int64_t j = 0; j < n; ++j) {
       const int k = (int)(j % S);
       bool stored = false;
@@ -242,7 +243,7 @@ __global__ void __launch_bounds__(kIssuers * 32) k_move_tma(Geo g, MoveArgs a) {
           bulk_g2s(ring + (size_t)kp * a.stage_bytes, nx.src, bytes, &bar[kp]);
           vbits |= 1u << kp;
         }
-        nx_ok = (jr + 1 < n) && make_plan<KIND, FP8, RANGED>(g, a, gi + (jr + 1) * G, nx);
+        nx_ok = (jr + 1 < n) && make_plan<KIND, FP8, RANGED, REV>(g, a, gi + (jr + 1) * G, nx);
       }
     }
     pdl_trigger();
@@ -263,7 +264,7 @@ __device__ __forceinline__ uint32_t ld_vec<uint32_t>(const uint8_t* p) {
 __device__ __forceinline__ void st_vec(uint8_t* p, const uint4& v) { st16(p, v); }
 __device__ __forceinline__ void st_vec(uint8_t* p, const uint32_t& v) { *reinterpret_cast<uint32_t*>(p) = v; }
 
-template <int KIND, bool FP8, typename V, bool RANGED>
+template <int KIND, bool FP8, typename V, bool RANGED, bool REV>
 __global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
   constexpr int U = 8;
   constexpr int W = (int)sizeof(V);
@@ -275,7 +276,8 @@ __global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
   if (KIND == kMovePack || KIND == kMovePackPush) {
     // Pack: lane k holds the destination row of the token's pair k and broadcasts it by
     // shuffle, so a warp keeps only its U loaded vectors live while it writes R copies.
-    for (int64_t u = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < a.units; u += nwarps) {
+    for (int64_t u0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u0 < a.units; u0 += nwarps) {
+      const int64_t u = REV ? a.units - 1 - u0 : u0;
       const int64_t tv = u / a.chunks;
       const int64_t tok = range_item<RANGED>(g, a, tv, 1);
       const int64_t coff = (u - tv * a.chunks) * (int64_t)a.chunk_bytes;
@@ -310,7 +312,7 @@ __global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
   }
   for (int64_t u = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < a.units; u += nwarps) {
     Plan pl;
-    if (!make_plan<KIND, FP8, RANGED>(g, a, u, pl)) continue;
+    if (!make_plan<KIND, FP8, RANGED, REV>(g, a, u, pl)) continue;
     for (int64_t v0 = lane; v0 < nel; v0 += 32 * U) {
       V r[U];
 #pragma unroll
@@ -337,12 +339,12 @@ __global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
 }
 
 // Largest dynamic shared memory limit set so far, per TMA instantiation and device.
-std::atomic<int> g_tma_smem[8][2][2][64];
+std::atomic<int> g_tma_smem[8][2][2][2][64];
 
 // Stages per issuer and CTAs per SM: as many CTAs as fit with 3 stages per issuer (at
 // most 8 CTAs), then as many stages as the shared memory of each CTA holds (2..8). Each
 // CTA also pays 1 KB of reserved shared memory and its mbarrier/plan header.
-template <int KIND, bool FP8, bool RANGED>
+template <int KIND, bool FP8, bool RANGED, bool REV>
 cudaError_t run_tma(const Geo& g, MoveArgs a, Ctx& c) {
   const uint32_t bytes = unit_bytes<KIND>(g, a);
   const int stage_bytes = (int)((bytes + 127u) & ~127u);
@@ -362,8 +364,8 @@ cudaError_t run_tma(const Geo& g, MoveArgs a, Ctx& c) {
   if (S < 2) return cudaErrorInvalidValue;
   const size_t smem = kTmaHeader + (size_t)kIssuers * S * stage_bytes;
   {
-    cudaError_t e = ensure_dyn_smem(k_move_tma<KIND, FP8, RANGED>, c.device, smem,
-                                    g_tma_smem[KIND][FP8 ? 1 : 0][RANGED ? 1 : 0]);
+    cudaError_t e = ensure_dyn_smem(k_move_tma<KIND, FP8, RANGED, REV>, c.device, smem,
+                                    g_tma_smem[KIND][FP8 ? 1 : 0][RANGED ? 1 : 0][REV ? 1 : 0]);
     if (e != cudaSuccess) return e;
   }
   a.stages = S;
@@ -371,17 +373,17 @@ cudaError_t run_tma(const Geo& g, MoveArgs a, Ctx& c) {
   int64_t grid = (int64_t)c.num_sms * cps;
   const int64_t need = (a.units + kIssuers - 1) / kIssuers;
   if (grid > need) grid = need;
-  return launch_kernel(k_move_tma<KIND, FP8, RANGED>, dim3((unsigned)grid), dim3(kIssuers * 32), smem, c, g, a);
+  return launch_kernel(k_move_tma<KIND, FP8, RANGED, REV>, dim3((unsigned)grid), dim3(kIssuers * 32), smem, c, g, a);
 }
 
-template <int KIND, bool FP8, typename V, bool RANGED>
+template <int KIND, bool FP8, typename V, bool RANGED, bool REV>
 cudaError_t run_ldg(const Geo& g, const MoveArgs& a, Ctx& c) {
   // Four waves of the CTAs the SMs hold at once (registers decide): warps that finish early
   // take later units, which measured faster on GB300 than one wave of grid-stride loops.
   static std::atomic<int> resident{0};
   int per_sm = resident.load(std::memory_order_relaxed);
   if (per_sm == 0) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_move_ldg<KIND, FP8, V, RANGED>, 256, 0) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_move_ldg<KIND, FP8, V, RANGED, REV>, 256, 0) != cudaSuccess ||
         per_sm < 1)
       per_sm = 1;
     resident.store(per_sm, std::memory_order_relaxed);
@@ -390,7 +392,7 @@ cudaError_t run_ldg(const Geo& g, const MoveArgs& a, Ctx& c) {
   int64_t blocks = (a.units + 7) / 8;
   const int64_t maxb = (int64_t)c.num_sms * per_sm;
   if (blocks > maxb) blocks = maxb;
-  return launch_kernel(k_move_ldg<KIND, FP8, V, RANGED>, dim3((unsigned)blocks), dim3(256), 0, c, g, a);
+  return launch_kernel(k_move_ldg<KIND, FP8, V, RANGED, REV>, dim3((unsigned)blocks), dim3(256), 0, c, g, a);
 }
 
 // True when two stages per issuer fit in one CTA's shared memory.
@@ -411,14 +413,32 @@ bool tma_default(const MoveArgs& a, const Ctx& c) {
   return a.units / a.chunks >= 40LL * kIssuers * c.num_sms;
 }
 
-template <int KIND, bool FP8, bool RANGED>
+template <int KIND, bool FP8, bool RANGED, bool REV>
 cudaError_t run_kind(const Geo& g, const MoveArgs& a, Ctx& c, bool row16) {
   const bool want_tma = (c.flags & MOE_FLAG_TMA_MOVER) ? true
                         : (c.flags & MOE_FLAG_LDG_MOVER) ? false
                                                           : tma_default<KIND>(a, c);
-  if (row16 && want_tma && tma_fits<KIND>(g, a, c)) return run_tma<KIND, FP8, RANGED>(g, a, c);
-  if (row16) return run_ldg<KIND, FP8, uint4, RANGED>(g, a, c);
-  return run_ldg<KIND, FP8, uint32_t, RANGED>(g, a, c);
+  if (row16 && want_tma && tma_fits<KIND>(g, a, c)) return run_tma<KIND, FP8, RANGED, REV>(g, a, c);
+  if (row16) return run_ldg<KIND, FP8, uint4, RANGED, REV>(g, a, c);
+  return run_ldg<KIND, FP8, uint32_t, RANGED, REV>(g, a, c);
+}
+
+// Traversal direction. Each intermediate buffer of the pass is written by one move and read
+// once by the next; a move that runs in the opposite unit order to its producer starts on
+// the rows the producer wrote last, which are still in L2 (at 8K pairs of 14 KB rows,
+// about 117 MB a buffer against 129 MB of L2). Pair-ordered moves therefore alternate:
+// pack forward, scatter backward, unpack forward, identity expert forward, combine pack
+// backward, combine scatter forward. With direct push the pack writes the receive rows
+// forward, so the unpack and the identity expert run backward and the combine push forward.
+// Only the order in which independent rows are copied changes, never a value.
+template <int KIND, bool FP8, bool RANGED>
+cudaError_t run_dir(const Geo& g, const MoveArgs& a, Ctx& c, bool row16) {
+  if constexpr (KIND == kMoveUnpack || KIND == kMoveCopyEx) {
+    if (c.flags & MOE_FLAG_DIRECT_PUSH) return run_kind<KIND, FP8, RANGED, true>(g, a, c, row16);
+    return run_kind<KIND, FP8, RANGED, false>(g, a, c, row16);
+  } else {
+    return run_kind<KIND, FP8, RANGED, KIND == kMoveScatter || KIND == kMoveCPack>(g, a, c, row16);
+  }
 }
 
 }  // namespace
@@ -429,21 +449,21 @@ template <bool R>
 cudaError_t run_move(MoveKind kind, const Geo& g, const MoveArgs& a, Ctx& c, bool fp8, bool rowB16) {
   switch (kind) {
     case kMovePack:
-      return run_kind<kMovePack, false, R>(g, a, c, rowB16);
+      return run_dir<kMovePack, false, R>(g, a, c, rowB16);
     case kMoveScatter:
-      return run_kind<kMoveScatter, false, R>(g, a, c, rowB16);
+      return run_dir<kMoveScatter, false, R>(g, a, c, rowB16);
     case kMoveUnpack:
-      return fp8 ? run_kind<kMoveUnpack, true, R>(g, a, c, rowB16) : run_kind<kMoveUnpack, false, R>(g, a, c, rowB16);
+      return fp8 ? run_dir<kMoveUnpack, true, R>(g, a, c, rowB16) : run_dir<kMoveUnpack, false, R>(g, a, c, rowB16);
     case kMoveCPack:
-      return run_kind<kMoveCPack, false, R>(g, a, c, true);
+      return run_dir<kMoveCPack, false, R>(g, a, c, true);
     case kMoveCScatter:
-      return run_kind<kMoveCScatter, false, R>(g, a, c, true);
+      return run_dir<kMoveCScatter, false, R>(g, a, c, true);
     case kMoveCopyEx:
-      return run_kind<kMoveCopyEx, false, R>(g, a, c, true);
+      return run_dir<kMoveCopyEx, false, R>(g, a, c, true);
     case kMovePackPush:
-      return run_kind<kMovePackPush, false, R>(g, a, c, rowB16);
+      return run_dir<kMovePackPush, false, R>(g, a, c, rowB16);
     case kMoveCPush:
-      return run_kind<kMoveCPush, false, R>(g, a, c, true);
+      return run_dir<kMoveCPush, false, R>(g, a, c, true);
   }
   return cudaErrorInvalidValue;
 }

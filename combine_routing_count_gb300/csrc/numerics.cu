@@ -290,8 +290,11 @@ __device__ __forceinline__ uint32_t dequant2(uint16_t codes, float scale) {
 
 // Identity expert for the fp8 payload: one warp per used grouped row (found through the
 // pairs' gslot), 16 codes per lane per load, kDequantUnroll loads in flight per lane.
+// REV: pairs in descending order, for grouped rows that the unpack wrote in that order
+// (direct push), so that the rows written last, still in L2, are read first.
 constexpr int kDequantUnroll = 4;
 
+template <bool REV>
 __global__ void __launch_bounds__(256) k_dequant_fp8(Geo g, const int32_t* __restrict__ gslot,
                                                      const uint8_t* __restrict__ exq, const float* __restrict__ exs,
                                                      uint16_t* __restrict__ ey) {
@@ -299,7 +302,8 @@ __global__ void __launch_bounds__(256) k_dequant_fp8(Geo g, const int32_t* __res
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int nvec = g.H / 16;
   pdl_wait();
-  for (int64_t q = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; q < g.P; q += nwarps) {
+  for (int64_t q0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; q0 < g.P; q0 += nwarps) {
+    const int64_t q = REV ? g.P - 1 - q0 : q0;
     const int gl = __ldg(gslot + q);
     if (gl < 0) continue;
     const uint8_t* qr = exq + (int64_t)gl * g.H;
@@ -678,8 +682,8 @@ cudaError_t launch_dequant_fp8(const Geo& g, const moe_layout_t* lay, const uint
   const int64_t maxb = (int64_t)c.num_sms * 8;
   if (blocks > maxb) blocks = maxb;
   LaunchScope ls(c, MOE_K_EXPERT);
-  return launch_kernel(k_dequant_fp8, dim3((unsigned)blocks), dim3(256), 0, c, g, (const int32_t*)lay->gslot, exq,
-                       exs, ey);
+  return launch_kernel((c.flags & MOE_FLAG_DIRECT_PUSH) ? k_dequant_fp8<true> : k_dequant_fp8<false>,
+                       dim3((unsigned)blocks), dim3(256), 0, c, g, (const int32_t*)lay->gslot, exq, exs, ey);
 }
 
 cudaError_t launch_combine_reduce(const Geo& g, const moe_layout_t* lay, const uint16_t* crecv, const float* w,
