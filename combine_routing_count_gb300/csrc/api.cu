@@ -3,6 +3,7 @@
 // (except moe_status_sync), no fallback: every step runs in this library's kernels.
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <mutex>
 #include <utility>
 #include <vector>
@@ -16,6 +17,7 @@ std::atomic<uint64_t> g_launches{0};
 namespace {
 
 constexpr int kMaxDevices = 64;
+constexpr int kMaxHostBatches = 16;
 constexpr int64_t kMaxE = 1536;
 constexpr int64_t kMaxN = 2048;           // ranks: the scan CTAs stage up to 64*33 per-rank values
 constexpr int64_t kI32 = 0x7fffffff;
@@ -29,6 +31,13 @@ struct DevInfo {
   cudaStream_t aux = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
   std::mutex fork_mu;
+  // The copy-engine pipeline of the host pass: a stream for host-to-device and one for
+  // device-to-host copies, with their events; pipe_mu makes one pass's enqueue atomic.
+  bool pipe_ready = false;
+  cudaStream_t cin = nullptr, cout = nullptr;
+  cudaEvent_t p_start = nullptr, p_idx = nullptr, p_done = nullptr;
+  cudaEvent_t p_in[kMaxHostBatches] = {}, p_dev[kMaxHostBatches] = {};
+  std::mutex pipe_mu;
 };
 DevInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -51,6 +60,22 @@ DevInfo* aux_for(int dev) {
     di.aux = s;
     di.fork = f;
     di.join = j;
+  }
+  return &di;
+}
+
+DevInfo* pipe_for(int dev) {
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevInfo& di = g_dev[dev];
+  if (!di.pipe_ready) {
+    auto ev = [](cudaEvent_t* e) { return *e || cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess; };
+    if ((!di.cin && cudaStreamCreateWithFlags(&di.cin, cudaStreamNonBlocking) != cudaSuccess) ||
+        (!di.cout && cudaStreamCreateWithFlags(&di.cout, cudaStreamNonBlocking) != cudaSuccess) ||
+        !ev(&di.p_start) || !ev(&di.p_idx) || !ev(&di.p_done))
+      return nullptr;
+    for (int i = 0; i < kMaxHostBatches; ++i)
+      if (!ev(&di.p_in[i]) || !ev(&di.p_dev[i])) return nullptr;
+    di.pipe_ready = true;
   }
   return &di;
 }
@@ -192,6 +217,166 @@ bool host_mapped(const void* p, void** dev) {
 
 using namespace moe;
 
+namespace moe {
+namespace {
+
+// The whole pass in two token batches (tokens [0, T/2) and [T/2, T) of every rank) so that
+// the host-link-bound kernels of one batch overlap the HBM-bound moves of the other: the
+// pack of batch B (reading tokens over the host link) runs while batch A is scattered and
+// unpacked on the second stream, and the reduce of batch A (writing the output over the
+// link) runs there while batch B's combine send runs. The two batches touch disjoint rows
+// of every buffer (also when the combine buffers alias the dispatch ones).
+moe_status forward_two_batches(const Geo& g, const moe_dims* dims, const moe_layout_t* lay, const moe_buffers_t* b,
+                               void* stream) {
+  const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
+  if (!layout_ok(lay) || !b->x || !b->idx || !b->w || !b->send || !b->recv || !b->expert_x || !b->expert_y ||
+      !b->csend || !b->crecv || !b->out || !aligned16(b->x) || !aligned16(b->send) || !aligned16(b->recv) ||
+      !aligned16(b->expert_x) || !aligned16(b->expert_y) || !aligned16(b->csend) || !aligned16(b->crecv) ||
+      !aligned16(b->out) || (fp8 && (!b->expert_scale || !aligned16(b->expert_scale))))
+    return MOE_ERR_INVALID_ARG;
+  moe_status st = moe_layout(dims, b->idx, lay, stream);
+  if (st != MOE_OK) return st;
+  Ctx c;
+  if ((st = make_ctx(lay, stream, c)) != MOE_OK) return st;
+  DevInfo* di = aux_for(c.device);
+  if (!di) return MOE_ERR_CUDA;
+  Ctx ca = c;
+  ca.stream = di->aux;
+  const int ta = g.T / 2, tb = g.T - ta;
+  auto pack = [&](int t0, int nt) {
+    return fp8 ? launch_quant_pack(g, lay->gsend, b->x, static_cast<uint8_t*>(b->send), c, t0, nt)
+               : launch_move_range(kMovePack, g, lay, b->x, b->send, nullptr, t0, nt, c);
+  };
+  auto recv_half = [&](int t0, int nt, Ctx& cc) {
+    cudaError_t e = launch_move_range(kMoveScatter, g, lay, b->send, b->recv, nullptr, t0, nt, cc);
+    if (e == cudaSuccess)
+      e = launch_move_range(kMoveUnpack, g, lay, b->recv, b->expert_x, fp8 ? b->expert_scale : nullptr, t0, nt, cc);
+    return e;
+  };
+  auto combine_send_half = [&](int t0, int nt) {
+    cudaError_t e = launch_move_range(kMoveCPack, g, lay, b->expert_y, b->csend, nullptr, t0, nt, c);
+    if (e == cudaSuccess) e = launch_move_range(kMoveCScatter, g, lay, b->csend, b->crecv, nullptr, t0, nt, c);
+    return e;
+  };
+  if (pack(0, ta) != cudaSuccess || !fork_to(di, c.stream) || pack(ta, tb) != cudaSuccess ||
+      recv_half(0, ta, ca) != cudaSuccess || recv_half(ta, tb, c) != cudaSuccess || !join_from(di, c.stream))
+    return MOE_ERR_CUDA;
+  if ((st = moe_expert_identity(dims, lay, b->expert_x, b->expert_scale, b->expert_y, stream)) != MOE_OK) return st;
+  if (combine_send_half(0, ta) != cudaSuccess || !fork_to(di, c.stream) ||
+      launch_combine_reduce(g, lay, b->crecv, b->w, b->out, ca, 0, ta) != cudaSuccess ||
+      combine_send_half(ta, tb) != cudaSuccess ||
+      launch_combine_reduce(g, lay, b->crecv, b->w, b->out, c, ta, tb) != cudaSuccess || !join_from(di, c.stream))
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+// Device work of one token batch [t0, t0 + nt) of every rank: dispatch send and recv, the
+// identity expert and the combine, each on only the batch's tokens or pairs.
+cudaError_t batch_chain(const Geo& g, const moe_layout_t* lay, const moe_buffers_t* b, int t0, int nt, Ctx& c) {
+  const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
+  const bool push = (c.flags & MOE_FLAG_DIRECT_PUSH) != 0;
+  cudaError_t e;
+  if (push) {
+    e = fp8 ? launch_quant_pack(g, lay->grecv, b->x, static_cast<uint8_t*>(b->recv), c, t0, nt)
+            : launch_move_range(kMovePackPush, g, lay, b->x, b->recv, nullptr, t0, nt, c);
+  } else {
+    e = fp8 ? launch_quant_pack(g, lay->gsend, b->x, static_cast<uint8_t*>(b->send), c, t0, nt)
+            : launch_move_range(kMovePack, g, lay, b->x, b->send, nullptr, t0, nt, c);
+    if (e == cudaSuccess) e = launch_move_range(kMoveScatter, g, lay, b->send, b->recv, nullptr, t0, nt, c);
+  }
+  if (e == cudaSuccess)
+    e = launch_move_range(kMoveUnpack, g, lay, b->recv, b->expert_x, fp8 ? b->expert_scale : nullptr, t0, nt, c);
+  if (e == cudaSuccess) {
+    if (fp8)
+      e = launch_dequant_fp8(g, lay, static_cast<const uint8_t*>(b->expert_x), b->expert_scale, b->expert_y, c, t0,
+                             nt);
+    else if (static_cast<const void*>(b->expert_y) != b->expert_x)
+      e = launch_move_range(kMoveCopyEx, g, lay, b->expert_x, b->expert_y, nullptr, t0, nt, c);
+  }
+  if (e == cudaSuccess) {
+    if (push) {
+      e = launch_move_range(kMoveCPush, g, lay, b->expert_y, b->crecv, nullptr, t0, nt, c);
+    } else {
+      e = launch_move_range(kMoveCPack, g, lay, b->expert_y, b->csend, nullptr, t0, nt, c);
+      if (e == cudaSuccess) e = launch_move_range(kMoveCScatter, g, lay, b->csend, b->crecv, nullptr, t0, nt, c);
+    }
+  }
+  if (e == cudaSuccess) e = launch_combine_reduce(g, lay, b->crecv, b->w, b->out, c, t0, nt);
+  return e;
+}
+
+// Token batches of the copy-engine pipeline: the caller's choice, else about the square root
+// of the token rows' MB. The first copy in and the last copy out are what no device work
+// hides (X / nb each, X the token bytes), while every batch adds its launches' ramp and
+// tail (about c); X / nb + c * nb is least at nb = sqrt(X / c), and c near 1 MB of link
+// time fitted the measured optimum (4 batches at 14.7 MB, 8 at 59-67 MB) on GB300.
+int host_batch_count(const Geo& g, const moe_layout_t* lay) {
+  if (lay->flags & MOE_FLAG_HOST_ONE_BATCH) return 1;
+  if (g.payload == MOE_PAYLOAD_FP8_E4M3_B128 && (lay->flags & MOE_FLAG_STAGED_QUANT)) return 1;
+  int nb = lay->host_batches;
+  if (nb <= 0) nb = (int)std::lround(std::sqrt((double)g.N * g.T * g.H * 2 / 1e6));
+  if (nb > kMaxHostBatches) nb = kMaxHostBatches;
+  if (nb > g.T) nb = (int)g.T;
+  return nb < 1 ? 1 : nb;
+}
+
+// The host pass as a pipeline over nb token batches (tokens [t0, t0 + nt) of every rank):
+// the library's input stream copies idx, w and then each batch's token rows into the device
+// buffers; the caller's stream runs the layout once idx is there, then each batch's device
+// work once its rows are there; the output stream copies each finished batch's output rows
+// back. Copy engines move the host bytes, so batch j's copies in and out overlap the device
+// work of its neighbours without taking SMs from it. The caller's stream waits for the last
+// copy before the call returns.
+moe_status forward_host_pipelined(const Geo& g, const moe_dims* dims, const moe_layout_t* lay,
+                                  const moe_buffers_t* b, const uint16_t* h_x, const int32_t* h_idx,
+                                  const float* h_w, uint16_t* h_out, int nb, void* stream) {
+  const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
+  if (!b->send || !b->recv || !b->expert_x || !b->expert_y || !b->csend || !b->crecv || !aligned16(b->x) ||
+      !aligned16(b->send) || !aligned16(b->recv) || !aligned16(b->expert_x) || !aligned16(b->expert_y) ||
+      !aligned16(b->csend) || !aligned16(b->crecv) || !aligned16(b->out) ||
+      (fp8 && (!b->expert_scale || !aligned16(b->expert_scale))))
+    return MOE_ERR_INVALID_ARG;
+  Ctx c;
+  moe_status st = make_ctx(lay, stream, c);
+  if (st != MOE_OK) return st;
+  DevInfo* di = pipe_for(c.device);
+  if (!di) return MOE_ERR_CUDA;
+  const size_t pitch = (size_t)g.T * g.H * 2, pb = (size_t)g.P * 4;
+  std::lock_guard<std::mutex> lk(di->pipe_mu);
+  // Nothing is overwritten before the caller's earlier work on `stream` is done with it.
+  if (cudaEventRecord(di->p_start, c.stream) != cudaSuccess || cudaStreamWaitEvent(di->cin, di->p_start, 0) ||
+      cudaStreamWaitEvent(di->cout, di->p_start, 0))
+    return MOE_ERR_CUDA;
+  if (cudaMemcpyAsync(b->idx, h_idx, pb, cudaMemcpyHostToDevice, di->cin) != cudaSuccess ||
+      cudaEventRecord(di->p_idx, di->cin) != cudaSuccess ||
+      cudaMemcpyAsync(b->w, h_w, pb, cudaMemcpyHostToDevice, di->cin) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  for (int j = 0; j < nb; ++j) {
+    const int t0 = (int)((int64_t)j * g.T / nb), nt = (int)((int64_t)(j + 1) * g.T / nb) - t0;
+    if (cudaMemcpy2DAsync(b->x + (size_t)t0 * g.H, pitch, h_x + (size_t)t0 * g.H, pitch, (size_t)nt * g.H * 2, g.N,
+                          cudaMemcpyHostToDevice, di->cin) != cudaSuccess ||
+        cudaEventRecord(di->p_in[j], di->cin) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  if (cudaStreamWaitEvent(c.stream, di->p_idx, 0) != cudaSuccess) return MOE_ERR_CUDA;
+  if ((st = moe_layout(dims, b->idx, lay, stream)) != MOE_OK) return st;
+  for (int j = 0; j < nb; ++j) {
+    const int t0 = (int)((int64_t)j * g.T / nb), nt = (int)((int64_t)(j + 1) * g.T / nb) - t0;
+    if (cudaStreamWaitEvent(c.stream, di->p_in[j], 0) != cudaSuccess) return MOE_ERR_CUDA;
+    if (batch_chain(g, lay, b, t0, nt, c) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaEventRecord(di->p_dev[j], c.stream) != cudaSuccess || cudaStreamWaitEvent(di->cout, di->p_dev[j], 0) ||
+        cudaMemcpy2DAsync(h_out + (size_t)t0 * g.H, pitch, b->out + (size_t)t0 * g.H, pitch, (size_t)nt * g.H * 2,
+                          g.N, cudaMemcpyDeviceToHost, di->cout) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  if (cudaEventRecord(di->p_done, di->cout) != cudaSuccess || cudaStreamWaitEvent(c.stream, di->p_done, 0))
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
 extern "C" {
 
 moe_status moe_check_dims(const moe_dims* dims) {
@@ -239,6 +424,7 @@ moe_status moe_layout_init(const moe_dims* dims, void* d_ws, size_t ws_bytes, mo
   out->prof = nullptr;
   out->tma_stages = 0;
   out->ctas_per_sm = 0;
+  out->host_batches = 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(out->status, 0, 64, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemsetAsync(out->scratch + layout_scratch_done_offset(g), 0, 4 * (size_t)g.N, s) != cudaSuccess)
@@ -469,56 +655,6 @@ moe_status moe_forward(const moe_dims* dims, const moe_layout_t* lay, const moe_
   return moe_combine_recv(dims, lay, b->crecv, b->w, b->out, stream);
 }
 
-// The whole pass in two token batches (tokens [0, T/2) and [T/2, T) of every rank) so that
-// the host-link-bound kernels of one batch overlap the HBM-bound moves of the other: the
-// pack of batch B (reading tokens over the host link) runs while batch A is scattered and
-// unpacked on the second stream, and the reduce of batch A (writing the output over the
-// link) runs there while batch B's combine send runs. The two batches touch disjoint rows
-// of every buffer (also when the combine buffers alias the dispatch ones).
-moe_status forward_two_batches(const Geo& g, const moe_dims* dims, const moe_layout_t* lay, const moe_buffers_t* b,
-                               void* stream) {
-  const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
-  if (!layout_ok(lay) || !b->x || !b->idx || !b->w || !b->send || !b->recv || !b->expert_x || !b->expert_y ||
-      !b->csend || !b->crecv || !b->out || !aligned16(b->x) || !aligned16(b->send) || !aligned16(b->recv) ||
-      !aligned16(b->expert_x) || !aligned16(b->expert_y) || !aligned16(b->csend) || !aligned16(b->crecv) ||
-      !aligned16(b->out) || (fp8 && (!b->expert_scale || !aligned16(b->expert_scale))))
-    return MOE_ERR_INVALID_ARG;
-  moe_status st = moe_layout(dims, b->idx, lay, stream);
-  if (st != MOE_OK) return st;
-  Ctx c;
-  if ((st = make_ctx(lay, stream, c)) != MOE_OK) return st;
-  DevInfo* di = aux_for(c.device);
-  if (!di) return MOE_ERR_CUDA;
-  Ctx ca = c;
-  ca.stream = di->aux;
-  const int ta = g.T / 2, tb = g.T - ta;
-  auto pack = [&](int t0, int nt) {
-    return fp8 ? launch_quant_pack(g, lay->gsend, b->x, static_cast<uint8_t*>(b->send), c, t0, nt)
-               : launch_move_range(kMovePack, g, lay, b->x, b->send, nullptr, t0, nt, c);
-  };
-  auto recv_half = [&](int t0, int nt, Ctx& cc) {
-    cudaError_t e = launch_move_range(kMoveScatter, g, lay, b->send, b->recv, nullptr, t0, nt, cc);
-    if (e == cudaSuccess)
-      e = launch_move_range(kMoveUnpack, g, lay, b->recv, b->expert_x, fp8 ? b->expert_scale : nullptr, t0, nt, cc);
-    return e;
-  };
-  auto combine_send_half = [&](int t0, int nt) {
-    cudaError_t e = launch_move_range(kMoveCPack, g, lay, b->expert_y, b->csend, nullptr, t0, nt, c);
-    if (e == cudaSuccess) e = launch_move_range(kMoveCScatter, g, lay, b->csend, b->crecv, nullptr, t0, nt, c);
-    return e;
-  };
-  if (pack(0, ta) != cudaSuccess || !fork_to(di, c.stream) || pack(ta, tb) != cudaSuccess ||
-      recv_half(0, ta, ca) != cudaSuccess || recv_half(ta, tb, c) != cudaSuccess || !join_from(di, c.stream))
-    return MOE_ERR_CUDA;
-  if ((st = moe_expert_identity(dims, lay, b->expert_x, b->expert_scale, b->expert_y, stream)) != MOE_OK) return st;
-  if (combine_send_half(0, ta) != cudaSuccess || !fork_to(di, c.stream) ||
-      launch_combine_reduce(g, lay, b->crecv, b->w, b->out, ca, 0, ta) != cudaSuccess ||
-      combine_send_half(ta, tb) != cudaSuccess ||
-      launch_combine_reduce(g, lay, b->crecv, b->w, b->out, c, ta, tb) != cudaSuccess || !join_from(di, c.stream))
-    return MOE_ERR_CUDA;
-  return MOE_OK;
-}
-
 moe_status moe_forward_host(const moe_dims* dims, const moe_layout_t* lay, const moe_buffers_t* b, const uint16_t* h_x,
                             const int32_t* h_idx, const float* h_w, uint16_t* h_out, void* stream) {
   if (!b) return MOE_ERR_INVALID_ARG;
@@ -529,7 +665,7 @@ moe_status moe_forward_host(const moe_dims* dims, const moe_layout_t* lay, const
   if ((xb && (!h_x || !h_out || !b->x || !b->out)) || (pb && (!h_idx || !h_w || !b->idx || !b->w)))
     return MOE_ERR_INVALID_ARG;
   if (!layout_ok(lay)) return MOE_ERR_INVALID_ARG;
-  if (!(lay->flags & MOE_FLAG_HOST_STAGED)) {
+  if (lay->flags & MOE_FLAG_HOST_MAPPED) {
     // Device-accessible host memory: run the pass on it directly.
     void *dx = nullptr, *didx = nullptr, *dw = nullptr, *dout = nullptr;
     if (host_mapped(h_x, &dx) && host_mapped(h_idx, &didx) && host_mapped(h_w, &dw) && host_mapped(h_out, &dout)) {
@@ -543,6 +679,8 @@ moe_status moe_forward_host(const moe_dims* dims, const moe_layout_t* lay, const
       return two ? forward_two_batches(g, dims, lay, &m, stream) : moe_forward(dims, lay, &m, stream);
     }
   }
+  const int nb = moe_host_batches(dims, lay);
+  if (nb > 1) return forward_host_pipelined(g, dims, lay, b, h_x, h_idx, h_w, h_out, nb, stream);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (xb && cudaMemcpyAsync(b->x, h_x, xb, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (pb && cudaMemcpyAsync(b->idx, h_idx, pb, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -550,6 +688,12 @@ moe_status moe_forward_host(const moe_dims* dims, const moe_layout_t* lay, const
   if ((st = moe_forward(dims, lay, b, stream)) != MOE_OK) return st;
   if (xb && cudaMemcpyAsync(h_out, b->out, xb, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+int32_t moe_host_batches(const moe_dims* dims, const moe_layout_t* lay) {
+  Geo g;
+  if (make_geo(dims, g) != MOE_OK || !lay) return 0;
+  return (int64_t)g.N * g.T > 0 ? host_batch_count(g, lay) : 1;
 }
 
 moe_status moe_status_sync(const moe_layout_t* lay, void* stream, uint32_t* bits_out) {

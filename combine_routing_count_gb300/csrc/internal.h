@@ -117,7 +117,7 @@ cudaError_t launch_quant_fp8(const Geo& g, const uint16_t* x, uint8_t* xq, Ctx& 
 cudaError_t launch_quant_pack(const Geo& g, const int32_t* fan, const uint16_t* x, uint8_t* dst, Ctx& c, int t0 = 0,
                               int nt = -1);
 cudaError_t launch_dequant_fp8(const Geo& g, const moe_layout_t* lay, const uint8_t* exq, const float* exs,
-                               uint16_t* ey, Ctx& c);
+                               uint16_t* ey, Ctx& c, int t0 = 0, int nt = -1);   // t0, nt as launch_quant_pack
 cudaError_t launch_combine_partial(const Geo& g, const moe_layout_t* lay, const uint16_t* ey, const float* w,
                                    uint16_t* cpart, Ctx& c);
 cudaError_t launch_combine_sum(const Geo& g, const moe_layout_t* lay, const uint16_t* cpart, uint16_t* out,

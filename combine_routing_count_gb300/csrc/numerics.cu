@@ -291,19 +291,24 @@ __device__ __forceinline__ uint32_t dequant2(uint16_t codes, float scale) {
 // Identity expert for the fp8 payload: one warp per used grouped row (found through the
 // pairs' gslot), 16 codes per lane per load, kDequantUnroll loads in flight per lane.
 // REV: pairs in descending order, for grouped rows that the unpack wrote in that order
-// (direct push), so that the rows written last, still in L2, are read first.
+// (direct push), so that the rows written last, still in L2, are read first. RANGED: only
+// the pairs of tokens [t0, t0 + nt) of every rank (np = N * nt * R of them).
 constexpr int kDequantUnroll = 4;
 
-template <bool REV>
+template <bool REV, bool RANGED>
 __global__ void __launch_bounds__(256) k_dequant_fp8(Geo g, const int32_t* __restrict__ gslot,
                                                      const uint8_t* __restrict__ exq, const float* __restrict__ exs,
-                                                     uint16_t* __restrict__ ey) {
+                                                     uint16_t* __restrict__ ey, int t0, int nt, int64_t np) {
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int nvec = g.H / 16;
   pdl_wait();
-  for (int64_t q0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; q0 < g.P; q0 += nwarps) {
-    const int64_t q = REV ? g.P - 1 - q0 : q0;
+  for (int64_t q0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; q0 < np; q0 += nwarps) {
+    int64_t q = REV ? np - 1 - q0 : q0;
+    if (RANGED) {
+      const int64_t span = (int64_t)nt * g.R, s = q / span;
+      q = (s * g.T + t0) * g.R + (q - s * span);
+    }
     const int gl = __ldg(gslot + q);
     if (gl < 0) continue;
     const uint8_t* qr = exq + (int64_t)gl * g.H;
@@ -676,14 +681,19 @@ cudaError_t launch_quant_pack(const Geo& g, const int32_t* fan, const uint16_t* 
 }
 
 cudaError_t launch_dequant_fp8(const Geo& g, const moe_layout_t* lay, const uint8_t* exq, const float* exs,
-                               uint16_t* ey, Ctx& c) {
-  if (g.P == 0) return cudaSuccess;
-  int64_t blocks = (g.P + 7) / 8;
+                               uint16_t* ey, Ctx& c, int t0, int nt) {
+  if (nt < 0) nt = g.T;
+  const int64_t np = (int64_t)g.N * nt * g.R;
+  if (np == 0) return cudaSuccess;
+  int64_t blocks = (np + 7) / 8;
   const int64_t maxb = (int64_t)c.num_sms * 8;
   if (blocks > maxb) blocks = maxb;
   LaunchScope ls(c, MOE_K_EXPERT);
-  return launch_kernel((c.flags & MOE_FLAG_DIRECT_PUSH) ? k_dequant_fp8<true> : k_dequant_fp8<false>,
-                       dim3((unsigned)blocks), dim3(256), 0, c, g, (const int32_t*)lay->gslot, exq, exs, ey);
+  const bool rev = (c.flags & MOE_FLAG_DIRECT_PUSH) != 0, ranged = nt != g.T;
+  auto k = rev ? (ranged ? k_dequant_fp8<true, true> : k_dequant_fp8<true, false>)
+               : (ranged ? k_dequant_fp8<false, true> : k_dequant_fp8<false, false>);
+  return launch_kernel(k, dim3((unsigned)blocks), dim3(256), 0, c, g, (const int32_t*)lay->gslot, exq, exs, ey, t0,
+                       nt, np);
 }
 
 cudaError_t launch_combine_reduce(const Geo& g, const moe_layout_t* lay, const uint16_t* crecv, const float* w,

@@ -122,13 +122,13 @@ typedef struct {
  * those rows (two kernels), instead of the default moe_quantize_dispatch_send, which
  * quantises inside the pack and leaves d_xq unwritten. Same receive and grouped contents. */
 #define MOE_FLAG_STAGED_QUANT 0x10u
-/* moe_forward_host: copy host inputs into the device buffers and the output back with copy
- * engines, even when the host buffers are device-accessible. */
-#define MOE_FLAG_HOST_STAGED 0x20u
-/* moe_forward_host on device-accessible host memory: run the pass as one batch on the
- * caller's stream, instead of the default two token batches whose host-link-bound kernels
- * (the pack reading the tokens, the reduce writing the output) overlap the other batch's
- * HBM-bound moves on a second stream of the library. */
+/* moe_forward_host with device-accessible host buffers: run the kernels on the host memory
+ * itself (the pack reads the tokens and the reduce writes the output over the host link)
+ * instead of the default copy-engine pipeline. */
+#define MOE_FLAG_HOST_MAPPED 0x20u
+/* moe_forward_host: run the pass as one token batch on the caller's stream (copies, then
+ * the pass, then the copy back; or, with MOE_FLAG_HOST_MAPPED, the pass alone) instead of
+ * the default pipeline of token batches. */
 #define MOE_FLAG_HOST_ONE_BATCH 0x40u
 #define MOE_FLAG_NO_PDL 0x2u    /* launch without programmatic dependent launch (by default
                                    each kernel may be scheduled while its predecessor in the
@@ -163,7 +163,8 @@ typedef struct {
  *            arrival counters [N][N] (+ 2)
  * Host-side fields (set by the caller after moe_layout_init, read at each call):
  *   flags, prof, tma_stages (0 = automatic, else 1..32 stages per TMA mover CTA),
- *   ctas_per_sm (0 = automatic, else mover CTAs per SM).
+ *   ctas_per_sm (0 = automatic, else mover CTAs per SM), host_batches (token batches of
+ *   moe_forward_host's copy-engine pipeline: 0 = automatic, else 1..16).
  */
 typedef struct {
     int32_t *cnt, *C, *soff, *roff, *rtot, *ecnt, *eoff;
@@ -175,6 +176,7 @@ typedef struct {
     moe_prof_t *prof;
     int32_t tma_stages;
     int32_t ctas_per_sm;
+    int32_t host_batches;
 } moe_layout_t;
 
 /* Device buffers of one whole pass (moe_forward). Shapes, with B = row bytes,
@@ -384,22 +386,34 @@ moe_status moe_combine_recv_partial(const moe_dims *dims, const moe_layout_t *la
 moe_status moe_forward(const moe_dims *dims, const moe_layout_t *lay, const moe_buffers_t *bufs, void *stream);
 
 /* moe_forward with host inputs h_x [N][T][H] bf16, h_idx [N][T][R], h_w [N][T][R] and host
- * output h_out [N][T][H]. When all four are pinned host memory that the device can address
+ * output h_out [N][T][H] (pinned for the copies to be asynchronous; pageable works too).
+ * Default: a pipeline over nb token batches (tokens [j*T/nb, (j+1)*T/nb) of every rank;
+ * nb = lay->host_batches, or automatically about sqrt(token-row MB), at most 16 and T).
+ * A copy-engine stream of the library copies h_idx and h_w into bufs->idx/w, then each
+ * batch's token rows into bufs->x; the caller's stream runs the layout as soon as idx is
+ * there, then each batch's dispatch, identity expert and combine once its rows are there;
+ * a second copy-engine stream copies each finished batch's rows of bufs->out into h_out.
+ * The copies of one batch overlap the device work of the others without taking SMs from
+ * it. The two streams and their events are created on the first such call per device and
+ * kept until exit; the caller's stream waits for the last copy before the call returns, so
+ * `stream` orders everything as usual (and the pass can be captured into a CUDA graph).
+ * With MOE_FLAG_HOST_ONE_BATCH (or fp8 with MOE_FLAG_STAGED_QUANT): copies in, moe_forward,
+ * copy out, all on `stream`.
+ * With MOE_FLAG_HOST_MAPPED and all four buffers pinned memory the device can address
  * (cudaHostAlloc / cudaHostRegister; over NVLink-C2C on Grace-Blackwell), the kernels read
- * the inputs and write the output there directly: each input byte crosses the host link
- * once, when the kernel that needs it loads it, and bufs->x/idx/w/out are not used. With
+ * the inputs and write the output there directly and bufs->x/idx/w/out are not used; with
  * T >= 2 (and neither direct push, staged fp8 quantisation nor MOE_FLAG_HOST_ONE_BATCH)
- * the pass runs in two token batches, the second stream of the library (created on the
- * first such call per device with two events, kept until exit) taking the scatter and
- * unpack of the first batch and its reduce while the caller's stream packs and sends the
- * second; the caller's stream waits for it before the call returns, so `stream` orders
- * everything as usual (and the pass can be captured into a CUDA graph).
- * Otherwise, or with MOE_FLAG_HOST_STAGED, cudaMemcpyAsync copies the inputs into
- * bufs->x/idx/w, the pass runs, and bufs->out is copied into h_out. Asynchronous: the caller
- * synchronises `stream` before reading h_out. */
+ * that pass runs in two token batches, the library's high-priority stream taking the
+ * scatter and unpack of the first batch and its reduce while the caller's stream packs and
+ * sends the second. Asynchronous: the caller synchronises `stream` before reading h_out. */
 moe_status moe_forward_host(const moe_dims *dims, const moe_layout_t *lay, const moe_buffers_t *bufs,
                             const uint16_t *h_x, const int32_t *h_idx, const float *h_w, uint16_t *h_out,
                             void *stream);
+
+/* Token batches moe_forward_host's copy-engine pipeline uses for these dims and layout
+ * settings (lay->host_batches, lay->flags): 1 means one batch (no pipeline); 0 for bad
+ * arguments. Host only, no CUDA call. */
+int32_t moe_host_batches(const moe_dims *dims, const moe_layout_t *lay);
 
 /* Synchronises `stream`, reads and clears the device status word. Returns MOE_OK or the
  * lowest-numbered error whose bit is set; *bits_out (may be NULL) receives all bits. */

@@ -91,3 +91,38 @@ def test_library_never_calls_exit(L):
     r = subprocess.run(["nm", "-D", "--undefined-only", build.LIB], capture_output=True, text=True, check=True)
     imported = {line.split()[-1].split("@")[0] for line in r.stdout.splitlines() if line.strip()}
     assert not ({"exit", "abort", "_exit"} & imported), sorted({"exit", "abort", "_exit"} & imported)
+
+
+def test_library_exports_only_the_abi(L):
+    """Every C-linkage symbol the library defines is one of the header's moe_* entry points
+    (internal helpers stay out of the dynamic symbol table)."""
+    import subprocess
+    from combine_routing_count_gb300 import build
+    from combine_routing_count_gb300._abi import EXPORTED
+    r = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True, text=True, check=True)
+    c_syms = {line.split()[-1].split("@")[0] for line in r.stdout.splitlines()
+              if line.strip() and line.split()[-2] in ("T", "W") and not line.split()[-1].startswith("_Z")}
+    assert c_syms == set(EXPORTED), sorted(c_syms ^ set(EXPORTED))
+
+
+def test_host_batch_count_rule(L):
+    """The copy-engine pipeline's token batches: about sqrt(token-row MiB) by default, the
+    caller's count when set (capped at 16 and at T), one for the one-batch flag and for the
+    staged fp8 quantiser; 0 for bad dims. Host only."""
+    from combine_routing_count_gb300 import MoeLayout
+    def nb(N, T, H, E, R, payload=0, flags=0, host_batches=0):
+        lay = MoeLayout()
+        lay.flags, lay.host_batches = flags, host_batches
+        return L.moe_host_batches(ctypes.byref(_dims(N, T, H, E, R, 0, payload)), ctypes.byref(lay))
+    assert nb(8, 128, 7168, 256, 8) == 4        # 14.7 MB of token rows
+    assert nb(32, 128, 7168, 384, 8) == 8       # 58.7 MB
+    assert nb(16, 512, 4096, 128, 8) == 8       # 67.1 MB
+    assert nb(64, 32, 7168, 384, 8, 1) == 5     # 29.4 MB (fp8 payload, bf16 tokens)
+    assert nb(2, 16, 128, 8, 2) == 1            # 8 KB: no pipeline
+    assert nb(8, 128, 7168, 256, 8, host_batches=7) == 7
+    assert nb(8, 3, 7168, 256, 8, host_batches=16) == 3
+    assert nb(8, 128, 7168, 256, 8, host_batches=40) == 16
+    assert nb(8, 128, 7168, 256, 8, flags=0x40) == 1
+    assert nb(64, 32, 7168, 384, 8, 1, flags=0x10) == 1
+    assert nb(8, 0, 7168, 256, 8) == 1
+    assert nb(8, 128, 7168, 250, 8) == 0        # E not a multiple of N

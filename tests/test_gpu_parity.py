@@ -126,19 +126,36 @@ def test_invalid_arguments_launch_nothing():
     assert L.moe_launch_count() == n0
 
 
-@pytest.mark.parametrize("mode", ["mapped", "mapped-one-batch", "mapped-cap", "staged", "pageable"])
+# mode: (flags, host_batches, capacity, pinned, identity expert by aliasing)
+HOST_MODES = {
+    "pipelined": (0, 0, 0, True, True),              # copy-engine pipeline, automatic batches
+    "pipelined-7": (0, 7, 0, True, True),            # 7 uneven batches of 29 tokens
+    "pipelined-29": (0, 29, 0, True, True),          # one token per batch
+    "pipelined-cap": (0, 5, 9, True, True),          # capacity drops
+    "pipelined-copy-expert": (0, 3, 0, True, False), # ranged identity expert into its own buffer
+    "pipelined-push": (0x8, 4, 0, True, True),       # direct push in every batch
+    "one-batch": (0x40, 0, 0, True, True),
+    "pageable": (0, 4, 0, False, True),
+    "mapped": (0x20, 0, 0, True, True),              # kernels on the pinned memory, two batches
+    "mapped-one-batch": (0x60, 0, 0, True, True),
+    "mapped-cap": (0x20, 0, 9, True, True),
+}
+
+
+@pytest.mark.parametrize("mode", list(HOST_MODES))
 @pytest.mark.parametrize("payload", ["bf16", "fp8"])
 def test_forward_host_matches_device_path(orc, mode, payload):
-    """Host inputs and output: pinned memory read and written by the kernels directly, in
-    two token batches on two streams (default) or one (MOE_FLAG_HOST_ONE_BATCH), copied by
-    copy engines (MOE_FLAG_HOST_STAGED), or pageable (copied); an odd token count with
-    capacity drops for the batched pass."""
-    wl = W("host-e2e", 4, 29, 2048, 16, 4, payload, "zipf", 120, cap=(9 if mode == "mapped-cap" else 0))
+    """Host inputs and output: copied by the copy-engine pipeline in token batches (default;
+    several batch counts, pageable memory too), in one batch (MOE_FLAG_HOST_ONE_BATCH), or
+    read and written by the kernels directly (MOE_FLAG_HOST_MAPPED); an odd token count,
+    with and without capacity drops."""
+    flags, nb, cap, pinned, alias = HOST_MODES[mode]
+    wl = W("host-e2e", 4, 29, 2048, 16, 4, payload, "zipf", 120, cap=cap)
     inp = workloads.make_inputs(wl)
     from combine_routing_count_gb300 import MoeEP
-    ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, payload=payload, alias_buffers=(payload == "bf16"),
-               flags={"staged": 0x20, "mapped-one-batch": 0x40}.get(mode, 0))
-    pin = (lambda t: t) if mode == "pageable" else (lambda t: t.pin_memory())
+    ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, payload=payload, alias_buffers=(payload == "bf16" and alias),
+               separate_expert_y=(payload == "bf16" and not alias), flags=flags, host_batches=nb)
+    pin = (lambda t: t.pin_memory()) if pinned else (lambda t: t)
     h_x = pin(torch.from_numpy(inp["x"]).view(torch.bfloat16))
     h_idx = pin(torch.from_numpy(inp["idx"]))
     h_w = pin(torch.from_numpy(inp["w"]))
@@ -150,7 +167,7 @@ def test_forward_host_matches_device_path(orc, mode, payload):
         h_out.view(torch.int16).fill_(-1)
         ep.forward_host(h_x, h_idx, h_w, h_out, x, idx, w)
         code, _ = ep.status()
-        assert code in (0, 3)   # 3: capacity drops of the mapped-cap case
+        assert code == (3 if cap else 0)   # 3: capacity drops
         o = orc.forward(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, payload, inp["x"], inp["idx"], inp["w"])
         np.testing.assert_array_equal(u16(h_out), o["out"])
 
