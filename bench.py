@@ -206,15 +206,17 @@ def kernel_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on these sources."""
+def ncu_traffic(kernel: str, workload: str, mode: str = "cold"):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on these sources:
+    mode "cold" (ncu's default cache control, L2 flushed before the kernel) or "warm_l2"
+    (L2 carried over from the previous kernel, as in the step)."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(path):
         return None
     d = json.load(open(path))
     if d.get("source_sha") != kernel_source_sha():
         return None
-    return d.get("workloads", {}).get(workload, {}).get(kernel)
+    return d.get("workloads", {}).get(workload, {}).get(mode, {}).get(kernel)
 
 
 # ---------------------------------------------------------------------------- CPU oracle baseline
@@ -607,7 +609,8 @@ def run_ours(args):
         "hbm_frac": round(step_bytes / (mean_ms * 1e-3) / 1e9 / peak, 3),
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["gbs"], "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": kernels[dom]["frac"],
-                     "bytes_per_launch": ab[dom], "traffic": ncu_traffic(dom, wl.name)},
+                     "bytes_per_launch": ab[dom], "traffic": ncu_traffic(dom, wl.name),
+                     "traffic_warm_l2": ncu_traffic(dom, wl.name, "warm_l2")},
         "kernels": kernels,
         "direct_push": {"value": round(tokens / (push_ms_all * 1e-3), 1), "unit": "tokens/s",
                         "ms_per_step": round(push_ms_all, 4),
