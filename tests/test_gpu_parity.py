@@ -510,6 +510,94 @@ def test_concurrent_passes_on_two_streams(orc):
             np.testing.assert_array_equal(out, o["out"], err_msg=wl.name)
 
 
+def _host_tensors(inp, wl):
+    h_x = torch.from_numpy(inp["x"]).view(torch.bfloat16).pin_memory()
+    h_idx = torch.from_numpy(inp["idx"]).pin_memory()
+    h_w = torch.from_numpy(inp["w"]).pin_memory()
+    h_out = torch.empty((wl.N, wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
+    return h_x, h_idx, h_w, h_out
+
+
+def test_forward_host_concurrent_callers(orc):
+    """Two host threads, each with its own stream, layout and pinned buffers, run host passes
+    at the same time through the library's shared copy streams (pipelines of 3 and 4 batches)
+    and, in a third thread, the pass on mapped host memory: every output is the oracle's."""
+    import threading
+    from combine_routing_count_gb300 import MoeEP
+    cases = [(W("hconc-a", 8, 40, 2048, 64, 8, "bf16", "uniform", 214), 0, 3),
+             (W("hconc-b", 4, 33, 2048, 32, 6, "fp8", "zipf", 215), 0, 4),
+             (W("hconc-c", 4, 20, 1024, 16, 4, "bf16", "zipf", 216), 0x20, 0)]
+    results, errors = {}, []
+
+    def run(wl, flags, nb):
+        try:
+            stream = torch.cuda.Stream()
+            with torch.cuda.stream(stream):
+                inp = workloads.make_inputs(wl)
+                ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, payload=wl.payload, alias_buffers=(wl.payload == "bf16"),
+                           flags=flags, host_batches=nb)
+                h_x, h_idx, h_w, h_out = _host_tensors(inp, wl)
+                x = torch.empty_like(h_x, device="cuda")
+                idx = torch.empty_like(h_idx, device="cuda")
+                w = torch.empty_like(h_w, device="cuda")
+                outs = []
+                for _ in range(6):
+                    h_out.view(torch.int16).fill_(-1)
+                    ep.forward_host(h_x, h_idx, h_w, h_out, x, idx, w)
+                    code, _ = ep.status()
+                    assert code == 0
+                    outs.append(u16(h_out).copy())
+                results[wl.name] = (inp, outs)
+        except Exception as e:   # reported by the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=run, args=c) for c in cases]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for wl, _, _ in cases:
+        inp, outs = results[wl.name]
+        o = orc.forward(wl.N, wl.T, wl.H, wl.E, wl.R, 0, wl.payload, inp["x"], inp["idx"], inp["w"])
+        for out in outs:
+            np.testing.assert_array_equal(out, o["out"], err_msg=wl.name)
+
+
+@pytest.mark.parametrize("payload", ["bf16", "fp8"])
+def test_forward_host_pipeline_replays_under_cuda_graph(orc, payload):
+    """The copy-engine pipeline (its two library streams fork from and join back into the
+    caller's stream) captures into a CUDA graph and replays on new host inputs written into
+    the captured pinned tensors."""
+    from combine_routing_count_gb300 import MoeEP
+    wl = W("hgraph", 4, 24, 2048, 16, 4, payload, "uniform", 217)
+    ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, payload=payload, alias_buffers=(payload == "bf16"), host_batches=3)
+    inp = workloads.make_inputs(wl)
+    h_x, h_idx, h_w, h_out = _host_tensors(inp, wl)
+    x = torch.empty_like(h_x, device="cuda")
+    idx = torch.empty_like(h_idx, device="cuda")
+    w = torch.empty_like(h_w, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        ep.forward_host(h_x, h_idx, h_w, h_out, x, idx, w)   # streams, events, attributes set up here
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        ep.forward_host(h_x, h_idx, h_w, h_out, x, idx, w)
+    for seed in (218, 219):
+        inp = workloads.make_inputs(wl.replace(seed=seed))
+        h_x.copy_(torch.from_numpy(inp["x"]).view(torch.bfloat16))
+        h_idx.copy_(torch.from_numpy(inp["idx"]))
+        h_w.copy_(torch.from_numpy(inp["w"]))
+        h_out.view(torch.int16).fill_(-1)
+        graph.replay()
+        code, _ = ep.status()
+        assert code == 0
+        o = orc.forward(wl.N, wl.T, wl.H, wl.E, wl.R, 0, payload, inp["x"], inp["idx"], inp["w"])
+        np.testing.assert_array_equal(u16(h_out), o["out"], err_msg=f"seed {seed}")
+
+
 def _run_dedicated(orc, wl, inp, K, withhold=-1):
     from combine_routing_count_gb300 import MoeEP
     ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, wl.payload)
