@@ -26,6 +26,7 @@ struct DevInfo {
   int num_sms = 0;
   int smem_optin = 0;
   int smem_per_sm = 0;
+  int l2_bytes = 0;
   // The host pass's second stream (highest priority) and its fork and join events, created
   // on first use and kept until exit; fork_mu makes a fork (record, then wait) atomic.
   cudaStream_t aux = nullptr;
@@ -35,7 +36,7 @@ struct DevInfo {
   // device-to-host copies, with their events; pipe_mu makes one pass's enqueue atomic.
   bool pipe_ready = false;
   cudaStream_t cin = nullptr, cout = nullptr;
-  cudaEvent_t p_start = nullptr, p_idx = nullptr, p_done = nullptr;
+  cudaEvent_t p_start = nullptr, p_idx = nullptr, p_done = nullptr, p_lay = nullptr, p_aux = nullptr;
   cudaEvent_t p_in[kMaxHostBatches] = {}, p_dev[kMaxHostBatches] = {};
   std::mutex pipe_mu;
 };
@@ -71,7 +72,7 @@ DevInfo* pipe_for(int dev) {
     auto ev = [](cudaEvent_t* e) { return *e || cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess; };
     if ((!di.cin && cudaStreamCreateWithFlags(&di.cin, cudaStreamNonBlocking) != cudaSuccess) ||
         (!di.cout && cudaStreamCreateWithFlags(&di.cout, cudaStreamNonBlocking) != cudaSuccess) ||
-        !ev(&di.p_start) || !ev(&di.p_idx) || !ev(&di.p_done))
+        !ev(&di.p_start) || !ev(&di.p_idx) || !ev(&di.p_done) || !ev(&di.p_lay) || !ev(&di.p_aux))
       return nullptr;
     for (int i = 0; i < kMaxHostBatches; ++i)
       if (!ev(&di.p_in[i]) || !ev(&di.p_dev[i])) return nullptr;
@@ -130,7 +131,8 @@ moe_status make_ctx(const moe_layout_t* lay, void* stream, Ctx& c) {
     if (di.num_sms == 0) {
       if (cudaDeviceGetAttribute(&di.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
           cudaDeviceGetAttribute(&di.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
-          cudaDeviceGetAttribute(&di.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess) {
+          cudaDeviceGetAttribute(&di.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&di.l2_bytes, cudaDevAttrL2CacheSize, dev) != cudaSuccess) {
         di.num_sms = 0;
         return MOE_ERR_CUDA;
       }
@@ -138,6 +140,7 @@ moe_status make_ctx(const moe_layout_t* lay, void* stream, Ctx& c) {
     c.num_sms = di.num_sms;
     c.smem_optin = di.smem_optin;
     c.smem_per_sm = di.smem_per_sm;
+    c.l2_bytes = di.l2_bytes;
   }
   c.device = dev;
   c.stream = static_cast<cudaStream_t>(stream);
@@ -325,8 +328,14 @@ int host_batch_count(const Geo& g, const moe_layout_t* lay) {
 // buffers; the caller's stream runs the layout once idx is there, then each batch's device
 // work once its rows are there; the output stream copies each finished batch's output rows
 // back. Copy engines move the host bytes, so batch j's copies in and out overlap the device
-// work of its neighbours without taking SMs from it. The caller's stream waits for the last
-// copy before the call returns.
+// work of its neighbours without taking SMs from it. When a batch's combine rows take at
+// most 40% of L2, odd batches run on the library's high-priority stream, so one batch's
+// first kernels fill the SMs its neighbour's last kernels leave idle (the batches touch
+// disjoint rows of every buffer); with larger batches the two would evict each other's
+// rows from L2 between consecutive moves, and one stream measured faster (GB300: 29 and
+// 47 MB batches 8-13% faster on two streams, 59 and 67 MB batches 2.5% slower). The
+// caller's stream waits for the auxiliary stream and for the last copy before the call
+// returns.
 moe_status forward_host_pipelined(const Geo& g, const moe_dims* dims, const moe_layout_t* lay,
                                   const moe_buffers_t* b, const uint16_t* h_x, const int32_t* h_idx,
                                   const float* h_w, uint16_t* h_out, int nb, void* stream) {
@@ -340,7 +349,12 @@ moe_status forward_host_pipelined(const Geo& g, const moe_dims* dims, const moe_
   moe_status st = make_ctx(lay, stream, c);
   if (st != MOE_OK) return st;
   DevInfo* di = pipe_for(c.device);
-  if (!di) return MOE_ERR_CUDA;
+  DevInfo* da = aux_for(c.device);
+  if (!di || !da) return MOE_ERR_CUDA;
+  Ctx ca = c;
+  ca.stream = da->aux;
+  const double batch_rows = (double)g.N * g.T * g.R / nb;   // pairs of one batch
+  const bool two_streams = batch_rows * 2.0 * g.H <= 0.4 * c.l2_bytes;
   const size_t pitch = (size_t)g.T * g.H * 2, pb = (size_t)g.P * 4;
   std::lock_guard<std::mutex> lk(di->pipe_mu);
   // Nothing is overwritten before the caller's earlier work on `stream` is done with it.
@@ -360,16 +374,20 @@ moe_status forward_host_pipelined(const Geo& g, const moe_dims* dims, const moe_
   }
   if (cudaStreamWaitEvent(c.stream, di->p_idx, 0) != cudaSuccess) return MOE_ERR_CUDA;
   if ((st = moe_layout(dims, b->idx, lay, stream)) != MOE_OK) return st;
+  if (cudaEventRecord(di->p_lay, c.stream) != cudaSuccess || cudaStreamWaitEvent(ca.stream, di->p_lay, 0))
+    return MOE_ERR_CUDA;
   for (int j = 0; j < nb; ++j) {
     const int t0 = (int)((int64_t)j * g.T / nb), nt = (int)((int64_t)(j + 1) * g.T / nb) - t0;
-    if (cudaStreamWaitEvent(c.stream, di->p_in[j], 0) != cudaSuccess) return MOE_ERR_CUDA;
-    if (batch_chain(g, lay, b, t0, nt, c) != cudaSuccess) return MOE_ERR_CUDA;
-    if (cudaEventRecord(di->p_dev[j], c.stream) != cudaSuccess || cudaStreamWaitEvent(di->cout, di->p_dev[j], 0) ||
+    Ctx& cj = (two_streams && (j & 1)) ? ca : c;
+    if (cudaStreamWaitEvent(cj.stream, di->p_in[j], 0) != cudaSuccess) return MOE_ERR_CUDA;
+    if (batch_chain(g, lay, b, t0, nt, cj) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaEventRecord(di->p_dev[j], cj.stream) != cudaSuccess || cudaStreamWaitEvent(di->cout, di->p_dev[j], 0) ||
         cudaMemcpy2DAsync(h_out + (size_t)t0 * g.H, pitch, b->out + (size_t)t0 * g.H, pitch, (size_t)nt * g.H * 2,
                           g.N, cudaMemcpyDeviceToHost, di->cout) != cudaSuccess)
       return MOE_ERR_CUDA;
   }
-  if (cudaEventRecord(di->p_done, di->cout) != cudaSuccess || cudaStreamWaitEvent(c.stream, di->p_done, 0))
+  if (cudaEventRecord(di->p_aux, ca.stream) != cudaSuccess || cudaStreamWaitEvent(c.stream, di->p_aux, 0) ||
+      cudaEventRecord(di->p_done, di->cout) != cudaSuccess || cudaStreamWaitEvent(c.stream, di->p_done, 0))
     return MOE_ERR_CUDA;
   return MOE_OK;
 }

@@ -17,6 +17,7 @@ struct Ctx {
   int num_sms;
   int smem_optin;     // max dynamic shared memory per block (opt-in), bytes
   int smem_per_sm;    // shared memory per SM, bytes
+  int l2_bytes;       // L2 cache size, bytes
   uint32_t flags;
   int tma_stages;     // 0 = automatic
   int ctas_per_sm;    // 0 = automatic

@@ -72,7 +72,8 @@ extern "C" moe_status moe_dispatch_send_noalloc(const moe_dims* dims, const moe_
   c.status = lay->status;
   if (cudaDeviceGetAttribute(&c.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&c.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&c.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess)
+      cudaDeviceGetAttribute(&c.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&c.l2_bytes, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
     return MOE_ERR_CUDA;
   Geo g;
   g.N = (int)N;

@@ -564,6 +564,29 @@ def test_forward_host_concurrent_callers(orc):
             np.testing.assert_array_equal(out, o["out"], err_msg=wl.name)
 
 
+def test_forward_host_pipeline_large_batches_one_stream(orc):
+    """Batches whose combine rows exceed 40% of L2 stay on the caller's stream (8 batches of
+    512 tokens' 4096 pairs of 14 KB rows here); the output is still the oracle's."""
+    import ctypes
+    from combine_routing_count_gb300 import MoeEP, lib
+    wl = W("host-large", 8, 512, 7168, 64, 8, "bf16", "uniform", 222)
+    inp = workloads.make_inputs(wl)
+    ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, payload="bf16", alias_buffers=True)
+    assert lib().moe_host_batches(ctypes.byref(ep.dims), ctypes.byref(ep.layout)) == 8
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    assert wl.N * wl.T * wl.R // 8 * 2 * wl.H > 0.4 * l2
+    h_x, h_idx, h_w, h_out = _host_tensors(inp, wl)
+    x = torch.empty_like(h_x, device="cuda")
+    idx = torch.empty_like(h_idx, device="cuda")
+    w = torch.empty_like(h_w, device="cuda")
+    h_out.view(torch.int16).fill_(-1)
+    ep.forward_host(h_x, h_idx, h_w, h_out, x, idx, w)
+    code, _ = ep.status()
+    assert code == 0
+    o = orc.forward(wl.N, wl.T, wl.H, wl.E, wl.R, 0, "bf16", inp["x"], inp["idx"], inp["w"])
+    np.testing.assert_array_equal(u16(h_out), o["out"])
+
+
 @pytest.mark.parametrize("payload", ["bf16", "fp8"])
 def test_forward_host_pipeline_replays_under_cuda_graph(orc, payload):
     """The copy-engine pipeline (its two library streams fork from and join back into the
