@@ -323,19 +323,30 @@ int host_batch_count(const Geo& g, const moe_layout_t* lay) {
   return nb < 1 ? 1 : nb;
 }
 
+// First token of batch j of nb (j = nb gives T): equal batches, or, when `shaped` and there
+// are three or more, a first and a last batch of half the others' tokens (weights 1, 2, ...,
+// 2, 1), since the first batch's copy in and the last batch's copy out are the parts of a
+// one-stream pipeline that no device work hides.
+int batch_start(int T, int nb, int j, bool shaped) {
+  if (!shaped || nb < 3) return (int)((int64_t)j * T / nb);
+  const int64_t wsum = 2 * (int64_t)nb - 2, wj = j == 0 ? 0 : (j == nb ? wsum : 2 * (int64_t)j - 1);
+  return (int)((wj * T + wsum / 2) / wsum);
+}
+
 // The host pass as a pipeline over nb token batches (tokens [t0, t0 + nt) of every rank):
 // the library's input stream copies idx, w and then each batch's token rows into the device
 // buffers; the caller's stream runs the layout once idx is there, then each batch's device
 // work once its rows are there; the output stream copies each finished batch's output rows
 // back. Copy engines move the host bytes, so batch j's copies in and out overlap the device
-// work of its neighbours without taking SMs from it. When a batch's combine rows take at
-// most 40% of L2, odd batches run on the library's high-priority stream, so one batch's
+// work of its neighbours without taking SMs from it. When an average batch's combine rows
+// take at most 40% of L2, odd batches run on the library's high-priority stream, so one batch's
 // first kernels fill the SMs its neighbour's last kernels leave idle (the batches touch
 // disjoint rows of every buffer); with larger batches the two would evict each other's
 // rows from L2 between consecutive moves, and one stream measured faster (GB300: 29 and
-// 47 MB batches 8-13% faster on two streams, 59 and 67 MB batches 2.5% slower). The
-// caller's stream waits for the auxiliary stream and for the last copy before the call
-// returns.
+// 47 MB batches 8-13% faster on two streams, 59 and 67 MB batches 2.5% slower). On one
+// stream the first and last batches are half-size (3-4% faster there; 5% slower on two
+// streams, whose overlapping batches prefer equal sizes). The caller's stream waits for
+// the auxiliary stream and for the last copy before the call returns.
 moe_status forward_host_pipelined(const Geo& g, const moe_dims* dims, const moe_layout_t* lay,
                                   const moe_buffers_t* b, const uint16_t* h_x, const int32_t* h_idx,
                                   const float* h_w, uint16_t* h_out, int nb, void* stream) {
@@ -366,7 +377,8 @@ moe_status forward_host_pipelined(const Geo& g, const moe_dims* dims, const moe_
       cudaMemcpyAsync(b->w, h_w, pb, cudaMemcpyHostToDevice, di->cin) != cudaSuccess)
     return MOE_ERR_CUDA;
   for (int j = 0; j < nb; ++j) {
-    const int t0 = (int)((int64_t)j * g.T / nb), nt = (int)((int64_t)(j + 1) * g.T / nb) - t0;
+    const int t0 = batch_start(g.T, nb, j, !two_streams), nt = batch_start(g.T, nb, j + 1, !two_streams) - t0;
+    if (nt == 0) continue;
     if (cudaMemcpy2DAsync(b->x + (size_t)t0 * g.H, pitch, h_x + (size_t)t0 * g.H, pitch, (size_t)nt * g.H * 2, g.N,
                           cudaMemcpyHostToDevice, di->cin) != cudaSuccess ||
         cudaEventRecord(di->p_in[j], di->cin) != cudaSuccess)
@@ -377,7 +389,8 @@ moe_status forward_host_pipelined(const Geo& g, const moe_dims* dims, const moe_
   if (cudaEventRecord(di->p_lay, c.stream) != cudaSuccess || cudaStreamWaitEvent(ca.stream, di->p_lay, 0))
     return MOE_ERR_CUDA;
   for (int j = 0; j < nb; ++j) {
-    const int t0 = (int)((int64_t)j * g.T / nb), nt = (int)((int64_t)(j + 1) * g.T / nb) - t0;
+    const int t0 = batch_start(g.T, nb, j, !two_streams), nt = batch_start(g.T, nb, j + 1, !two_streams) - t0;
+    if (nt == 0) continue;
     Ctx& cj = (two_streams && (j & 1)) ? ca : c;
     if (cudaStreamWaitEvent(cj.stream, di->p_in[j], 0) != cudaSuccess) return MOE_ERR_CUDA;
     if (batch_chain(g, lay, b, t0, nt, cj) != cudaSuccess) return MOE_ERR_CUDA;
