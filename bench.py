@@ -56,6 +56,8 @@ def parse_args(argv=None):
     p.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     p.add_argument("--staged-quant", action="store_true",
                    help="fp8: quantise into a staging buffer, then pack (two kernels) instead of inside the pack")
+    p.add_argument("--one-batch", action="store_true",
+                   help="run moe_forward (and the host pass) as one token batch instead of micro-batches")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work for the oracle baseline")
     return p.parse_args(argv)
@@ -305,7 +307,7 @@ def run_ours(args):
     inp = workloads.make_inputs(wl)
     ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, wl.payload, alias_buffers=(wl.payload == "bf16"),
                flags={"auto": 0, "ldg": 1, "tma": 4}[args.mover] | (2 if args.no_pdl else 0) |
-               (0x10 if args.staged_quant else 0), tma_stages=args.tma_stages,
+               (0x10 if args.staged_quant else 0) | (0x40 if args.one_batch else 0), tma_stages=args.tma_stages,
                ctas_per_sm=args.ctas_per_sm)
     x = torch.from_numpy(inp["x"]).view(torch.bfloat16).to(device)
     idx = torch.from_numpy(inp["idx"]).to(device)
@@ -413,9 +415,13 @@ def run_ours(args):
 
     def kernel_region(step=step):
         """Timed region: per-kernel CUDA events (the library records one pair around each of
-        its launches on this stream) give each kernel's duration for the roofline."""
+        its launches on this stream) give each kernel's duration for the roofline. The pass
+        runs as one batch here (MOE_FLAG_ONE_BATCH), so every kernel is its whole-pass launch
+        and no two of them overlap; the step region below times the default micro-batches."""
         barrier(dist, device)
         torch.cuda.synchronize()
+        flags0 = ep.layout.flags
+        ep.layout.flags = flags0 | 0x40
         for i in range(K):
             flush_l2()
             pr, _ = profs[i]
@@ -424,6 +430,7 @@ def run_ours(args):
             step()
         torch.cuda.synchronize()
         ep.layout.prof = None
+        ep.layout.flags = flags0
         per_kernel = {}
         for pr, evs in profs:
             for j in range(pr.n):
@@ -463,6 +470,9 @@ def run_ours(args):
             expert_ms = statistics.fmean(ex)
         return statistics.fmean(step_ms), expert_ms, launches
 
+    # micro-batches of the timed step: moe_forward's for bf16; the fp8 step calls the entry
+    # points one by one (to time the identity expert apart) and runs as one batch
+    step_batches = 1 if fp8 else int(lib().moe_batches(ctypes.byref(ep.dims), ctypes.byref(ep.layout), 0))
     sampler.start()
     per_kernel = kernel_region()
     mean_ms, expert_ms, launches = step_region()
@@ -588,13 +598,13 @@ def run_ours(args):
     # Default: the copy-engine pipeline over token batches; then one batch (copies in, the
     # pass, copy out); then the kernels on the pinned host memory itself (NVLink-C2C).
     e2e_ms, e2e_same = e2e_region()
-    e2e_nb = lib().moe_host_batches(ctypes.byref(ep.dims), ctypes.byref(ep.layout))
-    ep.layout.flags |= 0x40
+    e2e_nb = lib().moe_batches(ctypes.byref(ep.dims), ctypes.byref(ep.layout), 1)
+    f0 = ep.layout.flags
+    ep.layout.flags = f0 | 0x40
     e2e_one_ms, _ = e2e_region()
-    ep.layout.flags &= ~0x40
-    ep.layout.flags |= 0x20
+    ep.layout.flags = f0 | 0x20
     e2e_mapped_ms, _ = e2e_region()
-    ep.layout.flags &= ~0x20
+    ep.layout.flags = f0
     h2d = inp["x"].nbytes + inp["idx"].nbytes + inp["w"].nbytes
     d2h = wl.N * wl.T * wl.H * 2
 
@@ -607,6 +617,7 @@ def run_ours(args):
                    "payload": wl.payload, "routing": wl.routing, "seed": wl.seed, "mover": args.mover,
                    "pdl": not args.no_pdl, "fp8_quant": ("staged" if args.staged_quant else "inside the pack") if fp8 else None,
                    "l2": "flushed before every timed step (write of 2x L2, then read of 2x L2)",
+                   "micro_batches": step_batches,
                    "parallelism": f"{ws} independent replica(s) of the {wl.N}-rank group"},
         "hbm_gbs": round(step_bytes / (mean_ms * 1e-3) / 1e9, 1),
         "hbm_frac": round(step_bytes / (mean_ms * 1e-3) / 1e9 / peak, 3),
@@ -643,9 +654,9 @@ def run_ours(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "path": f"moe_forward_host (C ABI): copy engines move each of {e2e_nb} token batches in and "
                         "out of pinned host memory while the device works on the other batches",
-                "host_batches": e2e_nb,
+                "batches": e2e_nb,
                 "one_batch": {"value": round(tokens / (e2e_one_ms * 1e-3), 1), "ms_per_step": round(e2e_one_ms, 4),
-                              "path": "MOE_FLAG_HOST_ONE_BATCH: copies in, the pass, copy out on one stream"},
+                              "path": "MOE_FLAG_ONE_BATCH: copies in, the pass, copy out on one stream"},
                 "out_equals_device_path": e2e_same,
                 "mapped": {"value": round(tokens / (e2e_mapped_ms * 1e-3), 1),
                            "ms_per_step": round(e2e_mapped_ms, 4),

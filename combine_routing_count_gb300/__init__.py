@@ -14,14 +14,14 @@ import ctypes
 import torch
 
 from . import _abi
-from ._abi import (MOE_FLAG_DIRECT_PUSH, MOE_FLAG_HOST_ONE_BATCH, MOE_FLAG_HOST_MAPPED, MOE_FLAG_LDG_MOVER,
+from ._abi import (MOE_FLAG_DIRECT_PUSH, MOE_FLAG_ONE_BATCH, MOE_FLAG_HOST_MAPPED, MOE_FLAG_LDG_MOVER,
                    MOE_FLAG_NO_PDL, MOE_FLAG_STAGED_QUANT,
                    MOE_FLAG_TMA_MOVER, MOE_PAYLOAD_BF16, MOE_PAYLOAD_FP8_E4M3_B128, KERNEL_NAMES, MoeBuffers,
                    MoeDims, MoeError, MoeLayout, MoeProf, check, lib)
 
 __all__ = ["MoeEP", "MoeDims", "MoeLayout", "MoeBuffers", "MoeProf", "MoeError", "lib", "check",
            "MOE_FLAG_LDG_MOVER", "MOE_FLAG_NO_PDL", "MOE_FLAG_TMA_MOVER", "MOE_FLAG_DIRECT_PUSH",
-           "MOE_FLAG_STAGED_QUANT", "MOE_FLAG_HOST_MAPPED", "MOE_FLAG_HOST_ONE_BATCH", "KERNEL_NAMES"]
+           "MOE_FLAG_STAGED_QUANT", "MOE_FLAG_HOST_MAPPED", "MOE_FLAG_ONE_BATCH", "KERNEL_NAMES"]
 
 
 def _ptr(t) -> int | None:
@@ -47,7 +47,7 @@ class MoeEP:
     """
 
     def __init__(self, N, T, H, E, R, cap=0, payload="bf16", *, alias_buffers=False, separate_expert_y=False,
-                 flags=0, tma_stages=0, ctas_per_sm=0, host_batches=0):
+                 flags=0, tma_stages=0, ctas_per_sm=0, batches=0):
         L_ = lib()
         self.payload = payload
         self.fp8 = payload == "fp8"
@@ -67,7 +67,7 @@ class MoeEP:
         self.layout.flags = flags
         self.layout.tma_stages = tma_stages
         self.layout.ctas_per_sm = ctas_per_sm
-        self.layout.host_batches = host_batches
+        self.layout.batches = batches
         L = self.L
         self.xq = torch.empty((N, T, self.B), dtype=u8, device=dev) if self.fp8 else None
         self.send = torch.empty((N, T * R, self.B), dtype=u8, device=dev)

@@ -24,7 +24,7 @@ MOE_FLAG_TMA_MOVER = 0x4
 MOE_FLAG_DIRECT_PUSH = 0x8
 MOE_FLAG_STAGED_QUANT = 0x10
 MOE_FLAG_HOST_MAPPED = 0x20
-MOE_FLAG_HOST_ONE_BATCH = 0x40
+MOE_FLAG_ONE_BATCH = 0x40
 MOE_PROF_MAX = 32
 
 KERNEL_NAMES = ["route_count", "layout_maps", "quant_fp8", "pack", "scatter", "unpack", "expert",
@@ -47,7 +47,7 @@ class MoeProf(ctypes.Structure):
 class MoeLayout(ctypes.Structure):
     _fields_ = [(f, c_void_p) for f in LAYOUT_FIELDS] + [
         ("flags", c_uint32), ("prof", POINTER(MoeProf)), ("tma_stages", c_int32), ("ctas_per_sm", c_int32),
-        ("host_batches", c_int32)]
+        ("batches", c_int32)]
 
 
 BUFFER_FIELDS = ("x", "xq", "idx", "w", "send", "recv", "expert_x", "expert_scale", "expert_y", "csend",
@@ -101,7 +101,7 @@ def lib():
             "moe_combine_recv_partial": (c_int32, [D, Lp, c_void_p, c_void_p, c_void_p]),
             "moe_forward": (c_int32, [D, Lp, B, c_void_p]),
             "moe_forward_host": (c_int32, [D, Lp, B, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
-            "moe_host_batches": (c_int32, [D, Lp]),
+            "moe_batches": (c_int32, [D, Lp, c_int32]),
             "moe_status_sync": (c_int32, [Lp, c_void_p, POINTER(c_uint32)]),
             "moe_status_string": (c_char_p, [c_int32]),
             "moe_launch_count": (c_uint64, []),
@@ -129,5 +129,5 @@ EXPORTED = ("moe_check_dims", "moe_recv_capacity_rows", "moe_row_bytes", "moe_ca
             "moe_dispatch_send", "moe_dispatch_send_noalloc", "moe_quantize_dispatch_send", "moe_dispatch_split",
             "moe_dedicated_exchange_bytes", "moe_dispatch_dedicated", "moe_dispatch_recv",
             "moe_expert_identity", "moe_combine_send", "moe_combine_recv", "moe_combine_send_partial",
-            "moe_combine_recv_partial", "moe_forward", "moe_forward_host", "moe_host_batches", "moe_status_sync",
+            "moe_combine_recv_partial", "moe_forward", "moe_forward_host", "moe_batches", "moe_status_sync",
             "moe_status_string", "moe_launch_count")

@@ -308,16 +308,17 @@ cudaError_t batch_chain(const Geo& g, const moe_layout_t* lay, const moe_buffers
   return e;
 }
 
-// Token batches of the copy-engine pipeline: the caller's choice, else about the square root
-// of the token rows' MB. The first copy in and the last copy out are what no device work
-// hides (X / nb each, X the token bytes), while every batch adds its launches' ramp and
-// tail (about c); X / nb + c * nb is least at nb = sqrt(X / c), and c near 1 MB of link
-// time fitted the measured optimum (4 batches at 14.7 MB, 8 at 59-67 MB) on GB300.
+// Token batches of the copy-engine pipeline: the caller's choice, else about 1.4 times the
+// square root of the token rows' MB. The first copy in and the last copy out are what no
+// device work hides (X / nb each, X the token bytes), while every batch adds its launches'
+// ramp and tail (about c); X / nb + c * nb is least at nb = sqrt(X / c). The factor fitted
+// the measured optimum with batches alternating over two streams on GB300 (5 batches at
+// 14.7 MB, 7-8 at 29 MB, 11 at 59 MB; 16 measured best at 67 MB, 11 gives 6% less).
 int host_batch_count(const Geo& g, const moe_layout_t* lay) {
-  if (lay->flags & MOE_FLAG_HOST_ONE_BATCH) return 1;
+  if (lay->flags & MOE_FLAG_ONE_BATCH) return 1;
   if (g.payload == MOE_PAYLOAD_FP8_E4M3_B128 && (lay->flags & MOE_FLAG_STAGED_QUANT)) return 1;
-  int nb = lay->host_batches;
-  if (nb <= 0) nb = (int)std::lround(std::sqrt((double)g.N * g.T * g.H * 2 / 1e6));
+  int nb = lay->batches;
+  if (nb <= 0) nb = (int)std::lround(1.4 * std::sqrt((double)g.N * g.T * g.H * 2 / 1e6));
   if (nb > kMaxHostBatches) nb = kMaxHostBatches;
   if (nb > g.T) nb = (int)g.T;
   return nb < 1 ? 1 : nb;
@@ -331,6 +332,57 @@ int batch_start(int T, int nb, int j, bool shaped) {
   if (!shaped || nb < 3) return (int)((int64_t)j * T / nb);
   const int64_t wsum = 2 * (int64_t)nb - 2, wj = j == 0 ? 0 : (j == nb ? wsum : 2 * (int64_t)j - 1);
   return (int)((wj * T + wsum / 2) / wsum);
+}
+
+// Micro-batches of moe_forward: the caller's choice, else about one per 256 tokens of all
+// ranks (at most 16 and T); one with MOE_FLAG_ONE_BATCH or staged fp8 quantisation. Measured
+// on GB300 with batches alternating over two streams: 4 batches of 1024 tokens 7.5% faster
+// than one, 4 of 2048 (fp8) 10%, 16 of 4096 15%, 16 of 8192 17%; up to ~400 tokens one
+// batch is fastest.
+int forward_batch_count(const Geo& g, const moe_layout_t* lay) {
+  if (lay->flags & MOE_FLAG_ONE_BATCH) return 1;
+  if (g.payload == MOE_PAYLOAD_FP8_E4M3_B128 && (lay->flags & MOE_FLAG_STAGED_QUANT)) return 1;
+  int nb = lay->batches;
+  if (nb <= 0) nb = (int)std::lround((double)g.N * g.T / 256.0);
+  if (nb > kMaxHostBatches) nb = kMaxHostBatches;
+  if (nb > g.T) nb = (int)g.T;
+  return nb < 1 ? 1 : nb;
+}
+
+// moe_forward as nb micro-batches (tokens [j*T/nb, (j+1)*T/nb) of every rank), each running
+// dispatch, identity expert and combine on its own rows, odd ones on the library's
+// high-priority stream: a micro-batch's rows of each buffer are still in L2 when its next
+// move reads them, and one batch's first kernels fill the SMs its neighbour's last kernels
+// leave idle. The batches touch disjoint rows of every buffer. The caller's stream waits for
+// the auxiliary stream before the call returns.
+moe_status forward_batched(const Geo& g, const moe_dims* dims, const moe_layout_t* lay, const moe_buffers_t* b,
+                           int nb, void* stream) {
+  const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
+  if (!b->x || !b->idx || !b->w || !b->send || !b->recv || !b->expert_x || !b->expert_y || !b->csend ||
+      !b->crecv || !b->out || !aligned16(b->x) || !aligned16(b->send) || !aligned16(b->recv) ||
+      !aligned16(b->expert_x) || !aligned16(b->expert_y) || !aligned16(b->csend) || !aligned16(b->crecv) ||
+      !aligned16(b->out) || (fp8 && (!b->expert_scale || !aligned16(b->expert_scale))))
+    return MOE_ERR_INVALID_ARG;
+  moe_status st = moe_layout(dims, b->idx, lay, stream);
+  if (st != MOE_OK) return st;
+  Ctx c;
+  if ((st = make_ctx(lay, stream, c)) != MOE_OK) return st;
+  DevInfo* di = pipe_for(c.device);
+  DevInfo* da = aux_for(c.device);
+  if (!di || !da) return MOE_ERR_CUDA;
+  Ctx ca = c;
+  ca.stream = da->aux;
+  std::lock_guard<std::mutex> lk(di->pipe_mu);
+  if (cudaEventRecord(di->p_lay, c.stream) != cudaSuccess || cudaStreamWaitEvent(ca.stream, di->p_lay, 0))
+    return MOE_ERR_CUDA;
+  for (int j = 0; j < nb; ++j) {
+    const int t0 = batch_start(g.T, nb, j, false), nt = batch_start(g.T, nb, j + 1, false) - t0;
+    if (nt == 0) continue;
+    if (batch_chain(g, lay, b, t0, nt, (j & 1) ? ca : c) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (cudaEventRecord(di->p_aux, ca.stream) != cudaSuccess || cudaStreamWaitEvent(c.stream, di->p_aux, 0))
+    return MOE_ERR_CUDA;
+  return MOE_OK;
 }
 
 // The host pass as a pipeline over nb token batches (tokens [t0, t0 + nt) of every rank):
@@ -455,7 +507,7 @@ moe_status moe_layout_init(const moe_dims* dims, void* d_ws, size_t ws_bytes, mo
   out->prof = nullptr;
   out->tma_stages = 0;
   out->ctas_per_sm = 0;
-  out->host_batches = 0;
+  out->batches = 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(out->status, 0, 64, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemsetAsync(out->scratch + layout_scratch_done_offset(g), 0, 4 * (size_t)g.N, s) != cudaSuccess)
@@ -669,6 +721,10 @@ moe_status moe_forward(const moe_dims* dims, const moe_layout_t* lay, const moe_
   moe_status st = make_geo(dims, g);
   if (st != MOE_OK) return st;
   const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
+  if (layout_ok(lay)) {
+    const int nb = moe_batches(dims, lay, 0);
+    if (nb > 1) return forward_batched(g, dims, lay, b, nb, stream);
+  }
   if ((st = moe_layout(dims, b->idx, lay, stream)) != MOE_OK) return st;
   if (fp8 && !(lay->flags & MOE_FLAG_STAGED_QUANT)) {
     if ((st = moe_quantize_dispatch_send(dims, lay, b->x, b->send, b->recv, stream)) != MOE_OK) return st;
@@ -705,12 +761,12 @@ moe_status moe_forward_host(const moe_dims* dims, const moe_layout_t* lay, const
       m.idx = static_cast<int32_t*>(didx);
       m.w = static_cast<float*>(dw);
       m.out = static_cast<uint16_t*>(dout);
-      const bool two = g.T >= 2 && !(lay->flags & (MOE_FLAG_HOST_ONE_BATCH | MOE_FLAG_DIRECT_PUSH)) &&
+      const bool two = g.T >= 2 && !(lay->flags & (MOE_FLAG_ONE_BATCH | MOE_FLAG_DIRECT_PUSH)) &&
                        !(g.payload == MOE_PAYLOAD_FP8_E4M3_B128 && (lay->flags & MOE_FLAG_STAGED_QUANT));
       return two ? forward_two_batches(g, dims, lay, &m, stream) : moe_forward(dims, lay, &m, stream);
     }
   }
-  const int nb = moe_host_batches(dims, lay);
+  const int nb = moe_batches(dims, lay, 1);
   if (nb > 1) return forward_host_pipelined(g, dims, lay, b, h_x, h_idx, h_w, h_out, nb, stream);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (xb && cudaMemcpyAsync(b->x, h_x, xb, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -721,10 +777,11 @@ moe_status moe_forward_host(const moe_dims* dims, const moe_layout_t* lay, const
   return MOE_OK;
 }
 
-int32_t moe_host_batches(const moe_dims* dims, const moe_layout_t* lay) {
+int32_t moe_batches(const moe_dims* dims, const moe_layout_t* lay, int32_t host) {
   Geo g;
   if (make_geo(dims, g) != MOE_OK || !lay) return 0;
-  return (int64_t)g.N * g.T > 0 ? host_batch_count(g, lay) : 1;
+  if ((int64_t)g.N * g.T == 0) return 1;
+  return host ? host_batch_count(g, lay) : forward_batch_count(g, lay);
 }
 
 moe_status moe_status_sync(const moe_layout_t* lay, void* stream, uint32_t* bits_out) {

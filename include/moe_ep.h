@@ -126,10 +126,10 @@ typedef struct {
  * itself (the pack reads the tokens and the reduce writes the output over the host link)
  * instead of the default copy-engine pipeline. */
 #define MOE_FLAG_HOST_MAPPED 0x20u
-/* moe_forward_host: run the pass as one token batch on the caller's stream (copies, then
- * the pass, then the copy back; or, with MOE_FLAG_HOST_MAPPED, the pass alone) instead of
- * the default pipeline of token batches. */
-#define MOE_FLAG_HOST_ONE_BATCH 0x40u
+/* moe_forward and moe_forward_host: run the pass as one token batch on the caller's stream
+ * (for moe_forward_host: copies, then the pass, then the copy back; or, with
+ * MOE_FLAG_HOST_MAPPED, the pass alone) instead of the default token batches. */
+#define MOE_FLAG_ONE_BATCH 0x40u
 #define MOE_FLAG_NO_PDL 0x2u    /* launch without programmatic dependent launch (by default
                                    each kernel may be scheduled while its predecessor in the
                                    stream drains; it waits for it before touching memory) */
@@ -163,8 +163,9 @@ typedef struct {
  *            arrival counters [N][N] (+ 2)
  * Host-side fields (set by the caller after moe_layout_init, read at each call):
  *   flags, prof, tma_stages (0 = automatic, else 1..32 stages per TMA mover CTA),
- *   ctas_per_sm (0 = automatic, else mover CTAs per SM), host_batches (token batches of
- *   moe_forward_host's copy-engine pipeline: 0 = automatic, else 1..16).
+ *   ctas_per_sm (0 = automatic, else mover CTAs per SM), batches (token batches of
+ *   moe_forward's micro-batches and of moe_forward_host's copy-engine pipeline:
+ *   0 = automatic, else 1..16; see moe_batches).
  */
 typedef struct {
     int32_t *cnt, *C, *soff, *roff, *rtot, *ecnt, *eoff;
@@ -176,7 +177,7 @@ typedef struct {
     moe_prof_t *prof;
     int32_t tma_stages;
     int32_t ctas_per_sm;
-    int32_t host_batches;
+    int32_t batches;
 } moe_layout_t;
 
 /* Device buffers of one whole pass (moe_forward). Shapes, with B = row bytes,
@@ -382,13 +383,21 @@ moe_status moe_combine_recv_partial(const moe_dims *dims, const moe_layout_t *la
 /* One whole pass: moe_layout, moe_quantize_dispatch_send (fp8; or moe_quantize_fp8_b128 +
  * moe_dispatch_send with MOE_FLAG_STAGED_QUANT) or moe_dispatch_send (bf16),
  * moe_dispatch_recv, moe_expert_identity, moe_combine_send, moe_combine_recv. Returns the
- * first error. bufs->x, idx, w and out may also be device-accessible host memory. */
+ * first error. bufs->x, idx, w and out may also be device-accessible host memory.
+ * After the layout, the pass runs as nb micro-batches (nb = moe_batches(dims, lay, 0):
+ * lay->batches, or automatically about one per 256 tokens of all ranks, at most 16 and T;
+ * one with MOE_FLAG_ONE_BATCH or staged fp8 quantisation). Micro-batch j covers tokens
+ * [j*T/nb, (j+1)*T/nb) of every rank and runs dispatch send and recv, the identity expert
+ * and the combine on only those tokens' rows (the same kernels, restricted to a token
+ * range), odd micro-batches on the library's high-priority stream (created on first use,
+ * kept until exit); the caller's stream waits for it before the call returns. Every
+ * buffer ends up as in one batch, bit for bit. */
 moe_status moe_forward(const moe_dims *dims, const moe_layout_t *lay, const moe_buffers_t *bufs, void *stream);
 
 /* moe_forward with host inputs h_x [N][T][H] bf16, h_idx [N][T][R], h_w [N][T][R] and host
  * output h_out [N][T][H] (pinned for the copies to be asynchronous; pageable works too).
  * Default: a pipeline over nb token batches (tokens [j*T/nb, (j+1)*T/nb) of every rank;
- * nb = lay->host_batches, or automatically about sqrt(token-row MB), at most 16 and T).
+ * nb = lay->batches, or automatically about 1.4 sqrt(token-row MB), at most 16 and T).
  * A copy-engine stream of the library copies h_idx and h_w into bufs->idx/w, then each
  * batch's token rows into bufs->x; the caller's stream runs the layout as soon as idx is
  * there, then each batch's dispatch, identity expert and combine once its rows are there;
@@ -397,12 +406,12 @@ moe_status moe_forward(const moe_dims *dims, const moe_layout_t *lay, const moe_
  * it. The two streams and their events are created on the first such call per device and
  * kept until exit; the caller's stream waits for the last copy before the call returns, so
  * `stream` orders everything as usual (and the pass can be captured into a CUDA graph).
- * With MOE_FLAG_HOST_ONE_BATCH (or fp8 with MOE_FLAG_STAGED_QUANT): copies in, moe_forward,
+ * With MOE_FLAG_ONE_BATCH (or fp8 with MOE_FLAG_STAGED_QUANT): copies in, moe_forward,
  * copy out, all on `stream`.
  * With MOE_FLAG_HOST_MAPPED and all four buffers pinned memory the device can address
  * (cudaHostAlloc / cudaHostRegister; over NVLink-C2C on Grace-Blackwell), the kernels read
  * the inputs and write the output there directly and bufs->x/idx/w/out are not used; with
- * T >= 2 (and neither direct push, staged fp8 quantisation nor MOE_FLAG_HOST_ONE_BATCH)
+ * T >= 2 (and neither direct push, staged fp8 quantisation nor MOE_FLAG_ONE_BATCH)
  * that pass runs in two token batches, the library's high-priority stream taking the
  * scatter and unpack of the first batch and its reduce while the caller's stream packs and
  * sends the second. Asynchronous: the caller synchronises `stream` before reading h_out. */
@@ -410,10 +419,10 @@ moe_status moe_forward_host(const moe_dims *dims, const moe_layout_t *lay, const
                             const uint16_t *h_x, const int32_t *h_idx, const float *h_w, uint16_t *h_out,
                             void *stream);
 
-/* Token batches moe_forward_host's copy-engine pipeline uses for these dims and layout
- * settings (lay->host_batches, lay->flags): 1 means one batch (no pipeline); 0 for bad
- * arguments. Host only, no CUDA call. */
-int32_t moe_host_batches(const moe_dims *dims, const moe_layout_t *lay);
+/* Token batches for these dims and layout settings (lay->batches, lay->flags): of
+ * moe_forward_host's copy-engine pipeline when host != 0, else of moe_forward's
+ * micro-batches. 1 means one batch; 0 for bad arguments. Host only, no CUDA call. */
+int32_t moe_batches(const moe_dims *dims, const moe_layout_t *lay, int32_t host);
 
 /* Synchronises `stream`, reads and clears the device status word. Returns MOE_OK or the
  * lowest-numbered error whose bit is set; *bits_out (may be NULL) receives all bits. */

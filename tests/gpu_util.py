@@ -18,11 +18,12 @@ def to_dev(a: np.ndarray, dtype=None) -> torch.Tensor:
 
 
 def run_gpu(wl: workloads.Workload, inp: dict, flags: int = 0, poison: bool = True, split: bool = False,
-            withhold_slice: int = -1, fused_quant: bool = False, **kw):
+            withhold_slice: int = -1, fused_quant: bool = False, forward: bool = False, **kw):
     """Runs every step separately on the GPU; returns (MoeEP, host copies of every buffer).
     With split, dispatch is the one-launch split-phase dispatch (direct push) instead of
     dispatch send + receive; withhold_slice is passed to it. With fused_quant (fp8), the
-    quantisation runs inside the pack (the quantised token rows are not kept)."""
+    quantisation runs inside the pack (the quantised token rows are not kept). With forward,
+    the whole pass is one moe_forward call (micro-batched as the layout's settings say)."""
     from combine_routing_count_gb300 import MoeEP
     ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, wl.payload, flags=flags, separate_expert_y=True, **kw)
     if poison:
@@ -33,23 +34,26 @@ def run_gpu(wl: workloads.Workload, inp: dict, flags: int = 0, poison: bool = Tr
     x = to_dev(inp["x"]).view(torch.bfloat16) if "x" in inp else None
     idx = to_dev(inp["idx"])
     w = to_dev(inp["w"])
-    ep.layout_step(idx)
     res = {}
-    if fused_quant:
-        ep.quantize_dispatch_send(x)
-        ep.dispatch_recv()
+    if forward:
+        ep.forward(x, idx, w)
     else:
-        if wl.payload == "fp8":
-            ep.quantize(x)
-            x = ep.xq
-        if split:
-            ep.dispatch_split(x, withhold_slice)
-        else:
-            ep.dispatch_send(x)
+        ep.layout_step(idx)
+        if fused_quant:
+            ep.quantize_dispatch_send(x)
             ep.dispatch_recv()
-    ep.expert_identity()
-    ep.combine_send()
-    ep.combine_recv(w)
+        else:
+            if wl.payload == "fp8":
+                ep.quantize(x)
+                x = ep.xq
+            if split:
+                ep.dispatch_split(x, withhold_slice)
+            else:
+                ep.dispatch_send(x)
+                ep.dispatch_recv()
+        ep.expert_identity()
+        ep.combine_send()
+        ep.combine_recv(w)
     code, bits = ep.status()
     torch.cuda.synchronize()
     res["status_code"], res["status_bits"] = code, bits

@@ -126,7 +126,7 @@ def test_invalid_arguments_launch_nothing():
     assert L.moe_launch_count() == n0
 
 
-# mode: (flags, host_batches, capacity, pinned, identity expert by aliasing)
+# mode: (flags, batches, capacity, pinned, identity expert by aliasing)
 HOST_MODES = {
     "pipelined": (0, 0, 0, True, True),              # copy-engine pipeline, automatic batches
     "pipelined-7": (0, 7, 0, True, True),            # 7 uneven batches of 29 tokens
@@ -146,7 +146,7 @@ HOST_MODES = {
 @pytest.mark.parametrize("payload", ["bf16", "fp8"])
 def test_forward_host_matches_device_path(orc, mode, payload):
     """Host inputs and output: copied by the copy-engine pipeline in token batches (default;
-    several batch counts, pageable memory too), in one batch (MOE_FLAG_HOST_ONE_BATCH), or
+    several batch counts, pageable memory too), in one batch (MOE_FLAG_ONE_BATCH), or
     read and written by the kernels directly (MOE_FLAG_HOST_MAPPED); an odd token count,
     with and without capacity drops."""
     flags, nb, cap, pinned, alias = HOST_MODES[mode]
@@ -154,7 +154,7 @@ def test_forward_host_matches_device_path(orc, mode, payload):
     inp = workloads.make_inputs(wl)
     from combine_routing_count_gb300 import MoeEP
     ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, payload=payload, alias_buffers=(payload == "bf16" and alias),
-               separate_expert_y=(payload == "bf16" and not alias), flags=flags, host_batches=nb)
+               separate_expert_y=(payload == "bf16" and not alias), flags=flags, batches=nb)
     pin = (lambda t: t.pin_memory()) if pinned else (lambda t: t)
     h_x = pin(torch.from_numpy(inp["x"]).view(torch.bfloat16))
     h_idx = pin(torch.from_numpy(inp["idx"]))
@@ -377,15 +377,18 @@ def test_forward_variants_agree(orc, payload):
                 np.testing.assert_array_equal(got[k], o["layout"][k], err_msg=f"flags {flags:#x} {k}")
 
 
+@pytest.mark.parametrize("batches", [1, 3])
 @pytest.mark.parametrize("flags", [0, 4, 8], ids=["auto", "tma", "push"])
 @pytest.mark.parametrize("payload", ["bf16", "fp8"])
-def test_forward_replays_under_cuda_graph(orc, flags, payload):
+def test_forward_replays_under_cuda_graph(orc, flags, payload, batches):
     """The whole pass captures into a CUDA graph (no synchronisation or allocation on the
-    path; programmatic dependent launches become graph edges) and replays on new inputs
-    written into the captured tensors."""
+    path; programmatic dependent launches become graph edges; micro-batches on the library's
+    second stream fork from and join back into the captured stream) and replays on new
+    inputs written into the captured tensors."""
     from combine_routing_count_gb300 import MoeEP
     wl = W("graph", 4, 64, 2048, 32, 8, payload, "uniform", 170)
-    ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, payload=payload, alias_buffers=(payload == "bf16"), flags=flags)
+    ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, payload=payload, alias_buffers=(payload == "bf16"), flags=flags,
+               batches=batches)
     inp = workloads.make_inputs(wl)
     x, idx, w = to_dev(inp["x"]).view(torch.bfloat16), to_dev(inp["idx"]), to_dev(inp["w"])
     side = torch.cuda.Stream()
@@ -406,6 +409,28 @@ def test_forward_replays_under_cuda_graph(orc, flags, payload):
         assert code == 0
         o = orc.forward(wl.N, wl.T, wl.H, wl.E, wl.R, 0, payload, inp["x"], inp["idx"], inp["w"])
         np.testing.assert_array_equal(u16(ep.out.cpu()), o["out"], err_msg=f"seed {seed}")
+
+
+MB_CASES = [
+    W("mb-bf16", 8, 40, 2048, 64, 8, "bf16", "uniform", 230),
+    W("mb-fp8", 4, 33, 1024, 32, 6, "fp8", "zipf", 231),
+    W("mb-skew-cap", 4, 24, 1024, 16, 4, "bf16", "skew0", 232, cap=7),   # capacity drops
+    W("mb-fp8-H384", 3, 17, 384, 6, 3, "fp8", "uniform", 233),          # 396-byte fp8 rows
+    W("mb-H136", 2, 21, 136, 8, 3, "bf16", "zipf", 234),                # 272-byte rows
+]
+
+
+@pytest.mark.parametrize("batches", [2, 3, 7])
+@pytest.mark.parametrize("flags", [0, 1, 4, 8], ids=["auto", "ldg", "tma", "push"])
+@pytest.mark.parametrize("wl", MB_CASES, ids=lambda w: w.name)
+def test_forward_micro_batches_match_oracle(orc, wl, flags, batches):
+    """moe_forward in micro-batches (token ranges of every rank; odd ones on the library's
+    second stream): every buffer bit for bit as the oracle's, unused rows untouched, with
+    each mover, direct push, capacity drops and rows that are not 16-byte multiples."""
+    inp = workloads.make_inputs(wl)
+    _, res = run_gpu(wl, inp, flags=flags, forward=True, batches=batches)
+    assert res["status_code"] == (3 if wl.cap else 0)
+    compare_all(orc, wl, inp, res, push=bool(flags & 8), fused_quant=True)
 
 
 LIMIT_CASES = [
@@ -535,7 +560,7 @@ def test_forward_host_concurrent_callers(orc):
             with torch.cuda.stream(stream):
                 inp = workloads.make_inputs(wl)
                 ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, payload=wl.payload, alias_buffers=(wl.payload == "bf16"),
-                           flags=flags, host_batches=nb)
+                           flags=flags, batches=nb)
                 h_x, h_idx, h_w, h_out = _host_tensors(inp, wl)
                 x = torch.empty_like(h_x, device="cuda")
                 idx = torch.empty_like(h_idx, device="cuda")
@@ -565,14 +590,15 @@ def test_forward_host_concurrent_callers(orc):
 
 
 def test_forward_host_pipeline_large_batches_one_stream(orc):
-    """Batches whose combine rows exceed 40% of L2 stay on the caller's stream (8 batches of
-    512 tokens' 4096 pairs of 14 KB rows here); the output is still the oracle's."""
+    """Batches whose combine rows exceed 40% of L2 stay on the caller's stream, with half-size
+    first and last batches (8 batches of about 4096 pairs of 14 KB rows here); the output is
+    still the oracle's."""
     import ctypes
     from combine_routing_count_gb300 import MoeEP, lib
     wl = W("host-large", 8, 512, 7168, 64, 8, "bf16", "uniform", 222)
     inp = workloads.make_inputs(wl)
-    ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, payload="bf16", alias_buffers=True)
-    assert lib().moe_host_batches(ctypes.byref(ep.dims), ctypes.byref(ep.layout)) == 8
+    ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, payload="bf16", alias_buffers=True, batches=8)
+    assert lib().moe_batches(ctypes.byref(ep.dims), ctypes.byref(ep.layout), 1) == 8
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
     assert wl.N * wl.T * wl.R // 8 * 2 * wl.H > 0.4 * l2
     h_x, h_idx, h_w, h_out = _host_tensors(inp, wl)
@@ -594,7 +620,7 @@ def test_forward_host_pipeline_replays_under_cuda_graph(orc, payload):
     the captured pinned tensors."""
     from combine_routing_count_gb300 import MoeEP
     wl = W("hgraph", 4, 24, 2048, 16, 4, payload, "uniform", 217)
-    ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, payload=payload, alias_buffers=(payload == "bf16"), host_batches=3)
+    ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, payload=payload, alias_buffers=(payload == "bf16"), batches=3)
     inp = workloads.make_inputs(wl)
     h_x, h_idx, h_w, h_out = _host_tensors(inp, wl)
     x = torch.empty_like(h_x, device="cuda")
