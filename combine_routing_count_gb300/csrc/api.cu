@@ -18,6 +18,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kMaxHostBatches = 16;
+constexpr int kMaxMicroBatches = 32;
 constexpr int64_t kMaxE = 1536;
 constexpr int64_t kMaxN = 2048;           // ranks: the scan CTAs stage up to 64*33 per-rank values
 constexpr int64_t kI32 = 0x7fffffff;
@@ -334,17 +335,18 @@ int batch_start(int T, int nb, int j, bool shaped) {
   return (int)((wj * T + wsum / 2) / wsum);
 }
 
-// Micro-batches of moe_forward: the caller's choice, else about one per 256 tokens of all
-// ranks (at most 16 and T); one with MOE_FLAG_ONE_BATCH or staged fp8 quantisation. Measured
-// on GB300 with batches alternating over two streams: 4 batches of 1024 tokens 7.5% faster
-// than one, 4 of 2048 (fp8) 10%, 16 of 4096 15%, 16 of 8192 17%; up to ~400 tokens one
-// batch is fastest.
+// Micro-batches of moe_forward: the caller's choice (at most 32 and T), else about one per
+// 256 tokens of all ranks (at most 16 and T); one with MOE_FLAG_ONE_BATCH or staged fp8
+// quantisation. Measured on GB300 with batches alternating over two streams: 4 batches of
+// 1024 tokens 9% faster than one, 4 of 2048 (fp8, expert included) 10%, 16 of 4096 22%,
+// 16 of 8192 17%; up to ~400 tokens one batch is fastest. Even counts keep both streams
+// equally loaded (1024 tokens: 3 and 5 batches lose to 4).
 int forward_batch_count(const Geo& g, const moe_layout_t* lay) {
   if (lay->flags & MOE_FLAG_ONE_BATCH) return 1;
   if (g.payload == MOE_PAYLOAD_FP8_E4M3_B128 && (lay->flags & MOE_FLAG_STAGED_QUANT)) return 1;
   int nb = lay->batches;
-  if (nb <= 0) nb = (int)std::lround((double)g.N * g.T / 256.0);
-  if (nb > kMaxHostBatches) nb = kMaxHostBatches;
+  if (nb <= 0) nb = (int)std::min(16L, std::lround((double)g.N * g.T / 256.0));
+  if (nb > kMaxMicroBatches) nb = kMaxMicroBatches;
   if (nb > g.T) nb = (int)g.T;
   return nb < 1 ? 1 : nb;
 }

@@ -164,8 +164,8 @@ typedef struct {
  * Host-side fields (set by the caller after moe_layout_init, read at each call):
  *   flags, prof, tma_stages (0 = automatic, else 1..32 stages per TMA mover CTA),
  *   ctas_per_sm (0 = automatic, else mover CTAs per SM), batches (token batches of
- *   moe_forward's micro-batches and of moe_forward_host's copy-engine pipeline:
- *   0 = automatic, else 1..16; see moe_batches).
+ *   moe_forward's micro-batches (0 = automatic, else 1..32) and of moe_forward_host's
+ *   copy-engine pipeline (0 = automatic, else 1..16); see moe_batches).
  */
 typedef struct {
     int32_t *cnt, *C, *soff, *roff, *rtot, *ecnt, *eoff;
@@ -385,7 +385,8 @@ moe_status moe_combine_recv_partial(const moe_dims *dims, const moe_layout_t *la
  * moe_dispatch_recv, moe_expert_identity, moe_combine_send, moe_combine_recv. Returns the
  * first error. bufs->x, idx, w and out may also be device-accessible host memory.
  * After the layout, the pass runs as nb micro-batches (nb = moe_batches(dims, lay, 0):
- * lay->batches, or automatically about one per 256 tokens of all ranks, at most 16 and T;
+ * lay->batches (at most 32 and T), or automatically about one per 256 tokens of all ranks,
+ * at most 16 and T;
  * one with MOE_FLAG_ONE_BATCH or staged fp8 quantisation). Micro-batch j covers tokens
  * [j*T/nb, (j+1)*T/nb) of every rank and runs dispatch send and recv, the identity expert
  * and the combine on only those tokens' rows (the same kernels, restricted to a token

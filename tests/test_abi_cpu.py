@@ -131,8 +131,8 @@ def test_host_batch_count_rule(L):
 
 def test_forward_micro_batch_count_rule(L):
     """moe_forward's micro-batches: about one per 256 tokens of all ranks by default (at most
-    16 and T), the caller's count when set, one for the one-batch flag and for the staged fp8
-    quantiser. Host only."""
+    16 and T), the caller's count when set (at most 32 and T), one for the one-batch flag and
+    for the staged fp8 quantiser. Host only."""
     from combine_routing_count_gb300 import MoeLayout
     def nb(N, T, H, E, R, payload=0, flags=0, batches=0):
         lay = MoeLayout()
@@ -146,5 +146,7 @@ def test_forward_micro_batch_count_rule(L):
     assert nb(4, 96, 1024, 16, 4) == 2           # 384 tokens
     assert nb(8, 128, 7168, 256, 8, batches=3) == 3
     assert nb(8, 2, 7168, 256, 8, batches=9) == 2
+    assert nb(16, 512, 4096, 128, 8, batches=20) == 20
+    assert nb(16, 512, 4096, 128, 8, batches=40) == 32
     assert nb(8, 128, 7168, 256, 8, flags=0x40) == 1
     assert nb(64, 32, 7168, 384, 8, 1, flags=0x10) == 1
