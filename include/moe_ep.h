@@ -392,7 +392,11 @@ moe_status moe_combine_recv_partial(const moe_dims *dims, const moe_layout_t *la
  * and the combine on only those tokens' rows (the same kernels, restricted to a token
  * range), odd micro-batches on the library's high-priority stream (created on first use,
  * kept until exit); the caller's stream waits for it before the call returns. Every
- * buffer ends up as in one batch, bit for bit. */
+ * buffer ends up as in one batch, bit for bit.
+ * Graph capture: a captured call forks the library's stream into the capture and joins it
+ * back, so the pass captures like any other stream work; while a capture that holds such
+ * a call is open on a device, no other thread may run a multi-batch moe_forward or
+ * moe_forward_host on that device (its work would land in the open capture). */
 moe_status moe_forward(const moe_dims *dims, const moe_layout_t *lay, const moe_buffers_t *bufs, void *stream);
 
 /* moe_forward with host inputs h_x [N][T][H] bf16, h_idx [N][T][R], h_w [N][T][R] and host
