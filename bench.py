@@ -341,16 +341,19 @@ def run_ours(args):
 
     def step_split(e0, e1, e2, e3):
         """One pass with events around the identity expert (the grouped-GEMM stand-in), so
-        its time can be left out of the step as the scope's tokens/s definition asks."""
+        its time can be left out of the step as the scope's tokens/s definition asks: the
+        layout, moe_dispatch (in its token batches), the expert, moe_combine."""
         e0.record(stream)
         ep.layout_step(idx)
-        quant_dispatch_send()
-        ep.dispatch_recv()
+        if args.staged_quant:
+            quant_dispatch_send()
+            ep.dispatch_recv()
+        else:
+            ep.dispatch(x)
         e1.record(stream)
         ep.expert_identity()
         e2.record(stream)
-        ep.combine_send()
-        ep.combine_recv(w)
+        ep.combine(w)
         e3.record(stream)
 
     for _ in range(args.warmup):
@@ -470,9 +473,9 @@ def run_ours(args):
             expert_ms = statistics.fmean(ex)
         return statistics.fmean(step_ms), expert_ms, launches
 
-    # micro-batches of the timed step: moe_forward's for bf16; the fp8 step calls the entry
-    # points one by one (to time the identity expert apart) and runs as one batch
-    step_batches = 1 if fp8 else int(lib().moe_batches(ctypes.byref(ep.dims), ctypes.byref(ep.layout), 0))
+    # token batches of the timed step: moe_forward's micro-batches for bf16; the fp8 step
+    # (which times the identity expert apart) runs moe_dispatch and moe_combine in theirs
+    step_batches = int(lib().moe_batches(ctypes.byref(ep.dims), ctypes.byref(ep.layout), 2 if fp8 else 0))
     sampler.start()
     per_kernel = kernel_region()
     mean_ms, expert_ms, launches = step_region()

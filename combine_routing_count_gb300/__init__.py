@@ -115,6 +115,22 @@ class MoeEP:
                                                self.send.data_ptr(), self.recv.data_ptr(), _stream(stream)),
               "moe_quantize_dispatch_send")
 
+    def dispatch(self, x: torch.Tensor, stream=None):
+        """Whole dispatch phase (send + recv; fp8: the bf16 token rows x are quantised inside
+        the pack), in token batches when moe_batches(..., 2) says so."""
+        self.x = x
+        check(lib().moe_dispatch(ctypes.byref(self.dims), ctypes.byref(self.layout), x.data_ptr(),
+                                 self.send.data_ptr(), self.recv.data_ptr(), self.expert_x.data_ptr(),
+                                 _ptr(self.expert_scale), _stream(stream)), "moe_dispatch")
+
+    def combine(self, w: torch.Tensor, stream=None) -> torch.Tensor:
+        """Whole combine phase (send + recv) from self.expert_y into self.out."""
+        self.w = w
+        check(lib().moe_combine(ctypes.byref(self.dims), ctypes.byref(self.layout), self.expert_y.data_ptr(),
+                                self.csend.data_ptr(), self.crecv.data_ptr(), w.data_ptr(), self.out.data_ptr(),
+                                _stream(stream)), "moe_combine")
+        return self.out
+
     def dispatch_split(self, x: torch.Tensor, withhold_slice: int = -1, stream=None):
         """Split-phase dispatch: receive rows and grouped expert rows in one launch.
         withhold_slice (tests only) names a slice d*N + s whose arrival signals are not sent."""

@@ -97,6 +97,8 @@ def lib():
             "moe_expert_identity": (c_int32, [D, Lp, c_void_p, c_void_p, c_void_p, c_void_p]),
             "moe_combine_send": (c_int32, [D, Lp, c_void_p, c_void_p, c_void_p, c_void_p]),
             "moe_combine_recv": (c_int32, [D, Lp, c_void_p, c_void_p, c_void_p, c_void_p]),
+            "moe_dispatch": (c_int32, [D, Lp, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+            "moe_combine": (c_int32, [D, Lp, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
             "moe_combine_send_partial": (c_int32, [D, Lp, c_void_p, c_void_p, c_void_p, c_void_p]),
             "moe_combine_recv_partial": (c_int32, [D, Lp, c_void_p, c_void_p, c_void_p]),
             "moe_forward": (c_int32, [D, Lp, B, c_void_p]),
@@ -128,6 +130,7 @@ EXPORTED = ("moe_check_dims", "moe_recv_capacity_rows", "moe_row_bytes", "moe_ca
             "moe_layout_workspace_bytes", "moe_layout_init", "moe_layout", "moe_quantize_fp8_b128",
             "moe_dispatch_send", "moe_dispatch_send_noalloc", "moe_quantize_dispatch_send", "moe_dispatch_split",
             "moe_dedicated_exchange_bytes", "moe_dispatch_dedicated", "moe_dispatch_recv",
-            "moe_expert_identity", "moe_combine_send", "moe_combine_recv", "moe_combine_send_partial",
+            "moe_expert_identity", "moe_combine_send", "moe_combine_recv", "moe_dispatch", "moe_combine",
+            "moe_combine_send_partial",
             "moe_combine_recv_partial", "moe_forward", "moe_forward_host", "moe_batches", "moe_status_sync",
             "moe_status_string", "moe_launch_count")

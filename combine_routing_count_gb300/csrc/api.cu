@@ -274,22 +274,47 @@ moe_status forward_two_batches(const Geo& g, const moe_dims* dims, const moe_lay
   return MOE_OK;
 }
 
+// Dispatch send and recv of the token range [t0, t0 + nt) of every rank: its tokens'
+// rows packed (quantised for fp8) and written to their owners, then shuffled into the
+// grouped rows.
+cudaError_t dispatch_range(const Geo& g, const moe_layout_t* lay, const void* x, void* send, void* recv, void* ex,
+                           float* exs, int t0, int nt, Ctx& c) {
+  const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
+  cudaError_t e;
+  if (c.flags & MOE_FLAG_DIRECT_PUSH) {
+    e = fp8 ? launch_quant_pack(g, lay->grecv, static_cast<const uint16_t*>(x), static_cast<uint8_t*>(recv), c, t0,
+                                nt)
+            : launch_move_range(kMovePackPush, g, lay, x, recv, nullptr, t0, nt, c);
+  } else {
+    e = fp8 ? launch_quant_pack(g, lay->gsend, static_cast<const uint16_t*>(x), static_cast<uint8_t*>(send), c, t0,
+                                nt)
+            : launch_move_range(kMovePack, g, lay, x, send, nullptr, t0, nt, c);
+    if (e == cudaSuccess) e = launch_move_range(kMoveScatter, g, lay, send, recv, nullptr, t0, nt, c);
+  }
+  if (e == cudaSuccess) e = launch_move_range(kMoveUnpack, g, lay, recv, ex, fp8 ? exs : nullptr, t0, nt, c);
+  return e;
+}
+
+// Combine send and recv of the token range [t0, t0 + nt) of every rank: its pairs' expert
+// rows written back to their sources, then each token's weighted sum.
+cudaError_t combine_range(const Geo& g, const moe_layout_t* lay, const uint16_t* ey, uint16_t* csend, uint16_t* crecv,
+                          const float* w, uint16_t* out, int t0, int nt, Ctx& c) {
+  cudaError_t e;
+  if (c.flags & MOE_FLAG_DIRECT_PUSH) {
+    e = launch_move_range(kMoveCPush, g, lay, ey, crecv, nullptr, t0, nt, c);
+  } else {
+    e = launch_move_range(kMoveCPack, g, lay, ey, csend, nullptr, t0, nt, c);
+    if (e == cudaSuccess) e = launch_move_range(kMoveCScatter, g, lay, csend, crecv, nullptr, t0, nt, c);
+  }
+  if (e == cudaSuccess) e = launch_combine_reduce(g, lay, crecv, w, out, c, t0, nt);
+  return e;
+}
+
 // Device work of one token batch [t0, t0 + nt) of every rank: dispatch send and recv, the
 // identity expert and the combine, each on only the batch's tokens or pairs.
 cudaError_t batch_chain(const Geo& g, const moe_layout_t* lay, const moe_buffers_t* b, int t0, int nt, Ctx& c) {
   const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
-  const bool push = (c.flags & MOE_FLAG_DIRECT_PUSH) != 0;
-  cudaError_t e;
-  if (push) {
-    e = fp8 ? launch_quant_pack(g, lay->grecv, b->x, static_cast<uint8_t*>(b->recv), c, t0, nt)
-            : launch_move_range(kMovePackPush, g, lay, b->x, b->recv, nullptr, t0, nt, c);
-  } else {
-    e = fp8 ? launch_quant_pack(g, lay->gsend, b->x, static_cast<uint8_t*>(b->send), c, t0, nt)
-            : launch_move_range(kMovePack, g, lay, b->x, b->send, nullptr, t0, nt, c);
-    if (e == cudaSuccess) e = launch_move_range(kMoveScatter, g, lay, b->send, b->recv, nullptr, t0, nt, c);
-  }
-  if (e == cudaSuccess)
-    e = launch_move_range(kMoveUnpack, g, lay, b->recv, b->expert_x, fp8 ? b->expert_scale : nullptr, t0, nt, c);
+  cudaError_t e = dispatch_range(g, lay, b->x, b->send, b->recv, b->expert_x, b->expert_scale, t0, nt, c);
   if (e == cudaSuccess) {
     if (fp8)
       e = launch_dequant_fp8(g, lay, static_cast<const uint8_t*>(b->expert_x), b->expert_scale, b->expert_y, c, t0,
@@ -297,15 +322,7 @@ cudaError_t batch_chain(const Geo& g, const moe_layout_t* lay, const moe_buffers
     else if (static_cast<const void*>(b->expert_y) != b->expert_x)
       e = launch_move_range(kMoveCopyEx, g, lay, b->expert_x, b->expert_y, nullptr, t0, nt, c);
   }
-  if (e == cudaSuccess) {
-    if (push) {
-      e = launch_move_range(kMoveCPush, g, lay, b->expert_y, b->crecv, nullptr, t0, nt, c);
-    } else {
-      e = launch_move_range(kMoveCPack, g, lay, b->expert_y, b->csend, nullptr, t0, nt, c);
-      if (e == cudaSuccess) e = launch_move_range(kMoveCScatter, g, lay, b->csend, b->crecv, nullptr, t0, nt, c);
-    }
-  }
-  if (e == cudaSuccess) e = launch_combine_reduce(g, lay, b->crecv, b->w, b->out, c, t0, nt);
+  if (e == cudaSuccess) e = combine_range(g, lay, b->expert_y, b->csend, b->crecv, b->w, b->out, t0, nt, c);
   return e;
 }
 
@@ -351,6 +368,45 @@ int forward_batch_count(const Geo& g, const moe_layout_t* lay) {
   return nb < 1 ? 1 : nb;
 }
 
+// Token batches of moe_dispatch and moe_combine (each phase on its own, the expert between
+// them a barrier): the caller's choice (at most 32 and T), else none up to 1024 tokens of
+// all ranks and about one per 8 tokens of a rank beyond (at most 16); one with
+// MOE_FLAG_ONE_BATCH. Measured on GB300 with batches alternating over two streams: 1024
+// tokens never gained; 64 ranks x 32 tokens (fp8) 4% with 4 batches; 32 x 128 and 16 x 512
+// tokens 9% with 16.
+int phase_batch_count(const Geo& g, const moe_layout_t* lay) {
+  if (lay->flags & MOE_FLAG_ONE_BATCH) return 1;
+  int nb = lay->batches;
+  if (nb <= 0) nb = (int64_t)g.N * g.T <= 1024 ? 1 : (int)std::min<int64_t>(16, g.T / 8);
+  if (nb > kMaxMicroBatches) nb = kMaxMicroBatches;
+  if (nb > g.T) nb = (int)g.T;
+  return nb < 1 ? 1 : nb;
+}
+
+// Runs fn(t0, nt, ctx) for nb equal token ranges of every rank, odd ones on the library's
+// high-priority stream (which starts after everything issued so far on the caller's
+// stream); the caller's stream waits for it at the end. One range on the caller's stream
+// when nb is 1.
+template <typename F>
+cudaError_t run_batches(const Geo& g, Ctx& c, int nb, F&& fn) {
+  if (nb <= 1) return fn(0, (int)g.T, c);
+  DevInfo* di = pipe_for(c.device);
+  DevInfo* da = aux_for(c.device);
+  if (!di || !da) return cudaErrorUnknown;
+  Ctx ca = c;
+  ca.stream = da->aux;
+  std::lock_guard<std::mutex> lk(di->pipe_mu);
+  cudaError_t e = cudaEventRecord(di->p_lay, c.stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ca.stream, di->p_lay, 0);
+  for (int j = 0; j < nb && e == cudaSuccess; ++j) {
+    const int t0 = batch_start(g.T, nb, j, false), nt = batch_start(g.T, nb, j + 1, false) - t0;
+    if (nt > 0) e = fn(t0, nt, (j & 1) ? ca : c);
+  }
+  if (e == cudaSuccess) e = cudaEventRecord(di->p_aux, ca.stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(c.stream, di->p_aux, 0);
+  return e;
+}
+
 // moe_forward as nb micro-batches (tokens [j*T/nb, (j+1)*T/nb) of every rank), each running
 // dispatch, identity expert and combine on its own rows, odd ones on the library's
 // high-priority stream: a micro-batch's rows of each buffer are still in L2 when its next
@@ -369,22 +425,8 @@ moe_status forward_batched(const Geo& g, const moe_dims* dims, const moe_layout_
   if (st != MOE_OK) return st;
   Ctx c;
   if ((st = make_ctx(lay, stream, c)) != MOE_OK) return st;
-  DevInfo* di = pipe_for(c.device);
-  DevInfo* da = aux_for(c.device);
-  if (!di || !da) return MOE_ERR_CUDA;
-  Ctx ca = c;
-  ca.stream = da->aux;
-  std::lock_guard<std::mutex> lk(di->pipe_mu);
-  if (cudaEventRecord(di->p_lay, c.stream) != cudaSuccess || cudaStreamWaitEvent(ca.stream, di->p_lay, 0))
-    return MOE_ERR_CUDA;
-  for (int j = 0; j < nb; ++j) {
-    const int t0 = batch_start(g.T, nb, j, false), nt = batch_start(g.T, nb, j + 1, false) - t0;
-    if (nt == 0) continue;
-    if (batch_chain(g, lay, b, t0, nt, (j & 1) ? ca : c) != cudaSuccess) return MOE_ERR_CUDA;
-  }
-  if (cudaEventRecord(di->p_aux, ca.stream) != cudaSuccess || cudaStreamWaitEvent(c.stream, di->p_aux, 0))
-    return MOE_ERR_CUDA;
-  return MOE_OK;
+  return cuda_status(
+      run_batches(g, c, nb, [&](int t0, int nt, Ctx& cj) { return batch_chain(g, lay, b, t0, nt, cj); }));
 }
 
 // The host pass as a pipeline over nb token batches (tokens [t0, t0 + nt) of every rank):
@@ -690,6 +732,42 @@ moe_status moe_combine_recv(const moe_dims* dims, const moe_layout_t* lay, const
   return cuda_status(launch_combine_reduce(g, lay, d_crecv, d_w, d_out, c));
 }
 
+moe_status moe_dispatch(const moe_dims* dims, const moe_layout_t* lay, const void* d_x, void* d_send, void* d_recv,
+                        void* d_expert_x, float* d_expert_scale, void* stream) {
+  Geo g;
+  moe_status st = make_geo(dims, g);
+  if (st != MOE_OK) return st;
+  if ((int64_t)g.N * g.T == 0) return layout_ok(lay) ? MOE_OK : MOE_ERR_INVALID_ARG;  // nothing to move
+  const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
+  const bool push = lay && (lay->flags & MOE_FLAG_DIRECT_PUSH);
+  if (!layout_ok(lay) || !d_x || !d_recv || !d_expert_x || !aligned16(d_x) || !aligned16(d_recv) ||
+      !aligned16(d_expert_x) || (!push && (!d_send || !aligned16(d_send))) ||
+      (fp8 && (!d_expert_scale || !aligned16(d_expert_scale))))
+    return MOE_ERR_INVALID_ARG;
+  Ctx c;
+  if ((st = make_ctx(lay, stream, c)) != MOE_OK) return st;
+  return cuda_status(run_batches(g, c, phase_batch_count(g, lay), [&](int t0, int nt, Ctx& cj) {
+    return dispatch_range(g, lay, d_x, d_send, d_recv, d_expert_x, d_expert_scale, t0, nt, cj);
+  }));
+}
+
+moe_status moe_combine(const moe_dims* dims, const moe_layout_t* lay, const uint16_t* d_expert_y, uint16_t* d_csend,
+                       uint16_t* d_crecv, const float* d_w, uint16_t* d_out, void* stream) {
+  Geo g;
+  moe_status st = make_geo(dims, g);
+  if (st != MOE_OK) return st;
+  if ((int64_t)g.N * g.T == 0) return layout_ok(lay) ? MOE_OK : MOE_ERR_INVALID_ARG;  // nothing to move
+  const bool push = lay && (lay->flags & MOE_FLAG_DIRECT_PUSH);
+  if (!layout_ok(lay) || !d_expert_y || !d_crecv || !d_w || !d_out || !aligned16(d_expert_y) ||
+      !aligned16(d_crecv) || !aligned16(d_out) || (!push && (!d_csend || !aligned16(d_csend))))
+    return MOE_ERR_INVALID_ARG;
+  Ctx c;
+  if ((st = make_ctx(lay, stream, c)) != MOE_OK) return st;
+  return cuda_status(run_batches(g, c, phase_batch_count(g, lay), [&](int t0, int nt, Ctx& cj) {
+    return combine_range(g, lay, d_expert_y, d_csend, d_crecv, d_w, d_out, t0, nt, cj);
+  }));
+}
+
 moe_status moe_combine_send_partial(const moe_dims* dims, const moe_layout_t* lay, const uint16_t* d_expert_y,
                                     const float* d_w, uint16_t* d_cpart, void* stream) {
   Geo g;
@@ -779,11 +857,11 @@ moe_status moe_forward_host(const moe_dims* dims, const moe_layout_t* lay, const
   return MOE_OK;
 }
 
-int32_t moe_batches(const moe_dims* dims, const moe_layout_t* lay, int32_t host) {
+int32_t moe_batches(const moe_dims* dims, const moe_layout_t* lay, int32_t which) {
   Geo g;
-  if (make_geo(dims, g) != MOE_OK || !lay) return 0;
+  if (make_geo(dims, g) != MOE_OK || !lay || which < 0 || which > 2) return 0;
   if ((int64_t)g.N * g.T == 0) return 1;
-  return host ? host_batch_count(g, lay) : forward_batch_count(g, lay);
+  return which == 1 ? host_batch_count(g, lay) : which == 2 ? phase_batch_count(g, lay) : forward_batch_count(g, lay);
 }
 
 moe_status moe_status_sync(const moe_layout_t* lay, void* stream, uint32_t* bits_out) {

@@ -164,8 +164,9 @@ typedef struct {
  * Host-side fields (set by the caller after moe_layout_init, read at each call):
  *   flags, prof, tma_stages (0 = automatic, else 1..32 stages per TMA mover CTA),
  *   ctas_per_sm (0 = automatic, else mover CTAs per SM), batches (token batches of
- *   moe_forward's micro-batches (0 = automatic, else 1..32) and of moe_forward_host's
- *   copy-engine pipeline (0 = automatic, else 1..16); see moe_batches).
+ *   moe_forward's micro-batches and of moe_dispatch / moe_combine (0 = automatic, else
+ *   1..32) and of moe_forward_host's copy-engine pipeline (0 = automatic, else 1..16); see
+ *   moe_batches).
  */
 typedef struct {
     int32_t *cnt, *C, *soff, *roff, *rtot, *ecnt, *eoff;
@@ -362,6 +363,21 @@ moe_status moe_combine_send(const moe_dims *dims, const moe_layout_t *lay, const
 moe_status moe_combine_recv(const moe_dims *dims, const moe_layout_t *lay, const uint16_t *d_crecv,
                             const float *d_w, uint16_t *d_out, void *stream);
 
+/* Whole phases, as the page's dispatch and combine calls (section "Dispatch and combine"):
+ * moe_dispatch is moe_dispatch_send followed by moe_dispatch_recv (fp8: d_x holds the bf16
+ * token rows, quantised inside the pack as moe_quantize_dispatch_send does; d_send unused
+ * with MOE_FLAG_DIRECT_PUSH); moe_combine is moe_combine_send followed by moe_combine_recv.
+ * Arguments as in those calls; the expert work goes between the two. Each phase may run in
+ * nb token batches (nb = moe_batches(dims, lay, 2): lay->batches, else none up to 1024
+ * tokens of all ranks and about T/8 beyond, at most 16; one with MOE_FLAG_ONE_BATCH), batch j
+ * covering tokens [j*T/nb, (j+1)*T/nb) of every rank, odd batches on the library's
+ * high-priority stream, which the caller's stream waits for before the call returns. Every
+ * buffer ends up as with the separate calls, bit for bit. */
+moe_status moe_dispatch(const moe_dims *dims, const moe_layout_t *lay, const void *d_x, void *d_send,
+                        void *d_recv, void *d_expert_x, float *d_expert_scale, void *stream);
+moe_status moe_combine(const moe_dims *dims, const moe_layout_t *lay, const uint16_t *d_expert_y,
+                       uint16_t *d_csend, uint16_t *d_crecv, const float *d_w, uint16_t *d_out, void *stream);
+
 /* Combine with the weighted sum started on the expert side (section "Evaluation": DeepEP
  * accumulates on the sender side to send less data, at some accuracy cost; this library's
  * default combine accumulates on the receiving side only, as the page's kernels do).
@@ -424,10 +440,11 @@ moe_status moe_forward_host(const moe_dims *dims, const moe_layout_t *lay, const
                             const uint16_t *h_x, const int32_t *h_idx, const float *h_w, uint16_t *h_out,
                             void *stream);
 
-/* Token batches for these dims and layout settings (lay->batches, lay->flags): of
- * moe_forward_host's copy-engine pipeline when host != 0, else of moe_forward's
- * micro-batches. 1 means one batch; 0 for bad arguments. Host only, no CUDA call. */
-int32_t moe_batches(const moe_dims *dims, const moe_layout_t *lay, int32_t host);
+/* Token batches for these dims and layout settings (lay->batches, lay->flags): which = 0:
+ * moe_forward's micro-batches; 1: moe_forward_host's copy-engine pipeline; 2: the phases of
+ * moe_dispatch and moe_combine. 1 means one batch; 0 for bad arguments. Host only, no CUDA
+ * call. */
+int32_t moe_batches(const moe_dims *dims, const moe_layout_t *lay, int32_t which);
 
 /* Synchronises `stream`, reads and clears the device status word. Returns MOE_OK or the
  * lowest-numbered error whose bit is set; *bits_out (may be NULL) receives all bits. */

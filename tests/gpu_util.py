@@ -18,12 +18,14 @@ def to_dev(a: np.ndarray, dtype=None) -> torch.Tensor:
 
 
 def run_gpu(wl: workloads.Workload, inp: dict, flags: int = 0, poison: bool = True, split: bool = False,
-            withhold_slice: int = -1, fused_quant: bool = False, forward: bool = False, **kw):
+            withhold_slice: int = -1, fused_quant: bool = False, forward: bool = False, phases: bool = False,
+            **kw):
     """Runs every step separately on the GPU; returns (MoeEP, host copies of every buffer).
     With split, dispatch is the one-launch split-phase dispatch (direct push) instead of
     dispatch send + receive; withhold_slice is passed to it. With fused_quant (fp8), the
     quantisation runs inside the pack (the quantised token rows are not kept). With forward,
-    the whole pass is one moe_forward call (micro-batched as the layout's settings say)."""
+    the whole pass is one moe_forward call (micro-batched as the layout's settings say); with
+    phases, moe_dispatch, the identity expert and moe_combine (fp8 quantised in the pack)."""
     from combine_routing_count_gb300 import MoeEP
     ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, wl.payload, flags=flags, separate_expert_y=True, **kw)
     if poison:
@@ -37,6 +39,11 @@ def run_gpu(wl: workloads.Workload, inp: dict, flags: int = 0, poison: bool = Tr
     res = {}
     if forward:
         ep.forward(x, idx, w)
+    elif phases:
+        ep.layout_step(idx)
+        ep.dispatch(x)
+        ep.expert_identity()
+        ep.combine(w)
     else:
         ep.layout_step(idx)
         if fused_quant:

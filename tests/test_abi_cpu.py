@@ -150,3 +150,21 @@ def test_forward_micro_batch_count_rule(L):
     assert nb(16, 512, 4096, 128, 8, batches=40) == 32
     assert nb(8, 128, 7168, 256, 8, flags=0x40) == 1
     assert nb(64, 32, 7168, 384, 8, 1, flags=0x10) == 1
+
+
+def test_phase_batch_count_rule(L):
+    """moe_dispatch / moe_combine token batches: none up to 1024 tokens of all ranks, about
+    T/8 beyond (at most 16), the caller's count when set (at most 32 and T), one with the
+    one-batch flag. Host only."""
+    from combine_routing_count_gb300 import MoeLayout
+    def nb(N, T, H, E, R, payload=0, flags=0, batches=0):
+        lay = MoeLayout()
+        lay.flags, lay.batches = flags, batches
+        return L.moe_batches(ctypes.byref(_dims(N, T, H, E, R, 0, payload)), ctypes.byref(lay), 2)
+    assert nb(8, 128, 7168, 256, 8) == 1         # 1024 tokens
+    assert nb(64, 32, 7168, 384, 8, 1) == 4      # 2048 tokens, T = 32
+    assert nb(32, 128, 7168, 384, 8) == 16       # T = 128
+    assert nb(16, 512, 4096, 128, 8) == 16       # T = 512: capped
+    assert nb(8, 128, 7168, 256, 8, batches=5) == 5
+    assert nb(16, 512, 4096, 128, 8, flags=0x40) == 1
+    assert L.moe_batches(ctypes.byref(_dims()), ctypes.byref(MoeLayout()), 3) == 0

@@ -433,6 +433,18 @@ def test_forward_micro_batches_match_oracle(orc, wl, flags, batches):
     compare_all(orc, wl, inp, res, push=bool(flags & 8), fused_quant=True)
 
 
+@pytest.mark.parametrize("batches", [1, 2, 3, 7])
+@pytest.mark.parametrize("flags", [0, 1, 4, 8], ids=["auto", "ldg", "tma", "push"])
+@pytest.mark.parametrize("wl", MB_CASES, ids=lambda w: w.name)
+def test_dispatch_and_combine_phases_match_oracle(orc, wl, flags, batches):
+    """moe_dispatch and moe_combine (whole phases, in token batches on two streams when asked)
+    around the identity expert: every buffer bit for bit as the oracle's."""
+    inp = workloads.make_inputs(wl)
+    _, res = run_gpu(wl, inp, flags=flags, phases=True, batches=batches)
+    assert res["status_code"] == (3 if wl.cap else 0)
+    compare_all(orc, wl, inp, res, push=bool(flags & 8), fused_quant=True)
+
+
 LIMIT_CASES = [
     W("E1536-max", 8, 64, 256, 1536, 8, "bf16", "uniform", 180),      # largest E: 48 KB count tables
     W("N1536-L1", 1536, 2, 128, 1536, 2, "bf16", "uniform", 181),     # 1536 ranks, one expert each
