@@ -16,8 +16,10 @@
  * Conventions for every entry point:
  *  - Pointers named d_* are DEVICE pointers, h_* HOST pointers. Every device buffer must be
  *    16-byte aligned; MOE_ERR_INVALID_ARG otherwise.
- *  - The caller allocates and owns all memory and streams. The library never allocates,
- *    frees or synchronises, except moe_status_sync. `stream` is a cudaStream_t (NULL = the
+ *  - The caller allocates and owns all memory. The library never allocates or frees memory
+ *    and never synchronises, except moe_status_sync; the batched passes (moe_forward,
+ *    moe_dispatch, moe_combine, moe_forward_host) create three streams of their own and a
+ *    few events per device on first use and keep them until exit. `stream` is a cudaStream_t (NULL = the
  *    legacy default stream). All calls are asynchronous on that stream; a buffer may be
  *    reused once the stream has passed its consumer (the buffer-reuse barrier between
  *    dispatch and combine of the page's section "Dispatch and combine" is stream order).
