@@ -95,6 +95,16 @@ bool join_from(DevInfo* di, cudaStream_t main) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The device buffers a whole pass uses, present and 16-byte aligned (x, idx, w and out only
+// when `with_io`); send and csend may be NULL with direct push, which never touches them.
+bool pass_buffers_ok(const moe_buffers_t* b, uint32_t flags, bool fp8, bool with_io) {
+  const bool push = (flags & MOE_FLAG_DIRECT_PUSH) != 0;
+  auto ok = [](const void* p) { return p && aligned16(p); };
+  if (with_io && (!ok(b->x) || !b->idx || !b->w || !ok(b->out))) return false;
+  if (!push && (!ok(b->send) || !ok(b->csend))) return false;
+  return ok(b->recv) && ok(b->expert_x) && ok(b->expert_y) && ok(b->crecv) && (!fp8 || ok(b->expert_scale));
+}
+
 moe_status make_geo(const moe_dims* d, Geo& g) {
   if (!d) return MOE_ERR_INVALID_ARG;
   if (d->N < 1 || d->T < 0 || d->E < 1 || d->R < 1 || d->cap < 0 || d->H < 8) return MOE_ERR_INVALID_ARG;
@@ -233,11 +243,7 @@ namespace {
 moe_status forward_two_batches(const Geo& g, const moe_dims* dims, const moe_layout_t* lay, const moe_buffers_t* b,
                                void* stream) {
   const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
-  if (!layout_ok(lay) || !b->x || !b->idx || !b->w || !b->send || !b->recv || !b->expert_x || !b->expert_y ||
-      !b->csend || !b->crecv || !b->out || !aligned16(b->x) || !aligned16(b->send) || !aligned16(b->recv) ||
-      !aligned16(b->expert_x) || !aligned16(b->expert_y) || !aligned16(b->csend) || !aligned16(b->crecv) ||
-      !aligned16(b->out) || (fp8 && (!b->expert_scale || !aligned16(b->expert_scale))))
-    return MOE_ERR_INVALID_ARG;
+  if (!layout_ok(lay) || !pass_buffers_ok(b, lay->flags, fp8, true)) return MOE_ERR_INVALID_ARG;
   moe_status st = moe_layout(dims, b->idx, lay, stream);
   if (st != MOE_OK) return st;
   Ctx c;
@@ -416,11 +422,7 @@ cudaError_t run_batches(const Geo& g, Ctx& c, int nb, F&& fn) {
 moe_status forward_batched(const Geo& g, const moe_dims* dims, const moe_layout_t* lay, const moe_buffers_t* b,
                            int nb, void* stream) {
   const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
-  if (!b->x || !b->idx || !b->w || !b->send || !b->recv || !b->expert_x || !b->expert_y || !b->csend ||
-      !b->crecv || !b->out || !aligned16(b->x) || !aligned16(b->send) || !aligned16(b->recv) ||
-      !aligned16(b->expert_x) || !aligned16(b->expert_y) || !aligned16(b->csend) || !aligned16(b->crecv) ||
-      !aligned16(b->out) || (fp8 && (!b->expert_scale || !aligned16(b->expert_scale))))
-    return MOE_ERR_INVALID_ARG;
+  if (!pass_buffers_ok(b, lay->flags, fp8, true)) return MOE_ERR_INVALID_ARG;
   moe_status st = moe_layout(dims, b->idx, lay, stream);
   if (st != MOE_OK) return st;
   Ctx c;
@@ -447,11 +449,7 @@ moe_status forward_host_pipelined(const Geo& g, const moe_dims* dims, const moe_
                                   const moe_buffers_t* b, const uint16_t* h_x, const int32_t* h_idx,
                                   const float* h_w, uint16_t* h_out, int nb, void* stream) {
   const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
-  if (!b->send || !b->recv || !b->expert_x || !b->expert_y || !b->csend || !b->crecv || !aligned16(b->x) ||
-      !aligned16(b->send) || !aligned16(b->recv) || !aligned16(b->expert_x) || !aligned16(b->expert_y) ||
-      !aligned16(b->csend) || !aligned16(b->crecv) || !aligned16(b->out) ||
-      (fp8 && (!b->expert_scale || !aligned16(b->expert_scale))))
-    return MOE_ERR_INVALID_ARG;
+  if (!pass_buffers_ok(b, lay->flags, fp8, true)) return MOE_ERR_INVALID_ARG;
   Ctx c;
   moe_status st = make_ctx(lay, stream, c);
   if (st != MOE_OK) return st;

@@ -445,6 +445,27 @@ def test_dispatch_and_combine_phases_match_oracle(orc, wl, flags, batches):
     compare_all(orc, wl, inp, res, push=bool(flags & 8), fused_quant=True)
 
 
+@pytest.mark.parametrize("batches", [1, 3])
+@pytest.mark.parametrize("payload", ["bf16", "fp8"])
+def test_forward_direct_push_without_send_buffers(orc, payload, batches):
+    """Direct push never touches the send and combine-send buffers, so moe_forward accepts
+    NULL for both, in one batch and in micro-batches."""
+    import ctypes
+    from combine_routing_count_gb300 import MoeEP, lib
+    wl = W("push-null", 4, 30, 1024, 16, 4, payload, "zipf", 236)
+    inp = workloads.make_inputs(wl)
+    ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, payload=payload, alias_buffers=(payload == "bf16"), flags=0x8,
+               batches=batches)
+    x, idx, w = to_dev(inp["x"]).view(torch.bfloat16), to_dev(inp["idx"]), to_dev(inp["w"])
+    b = ep.buffers(x, idx, w)
+    b.send, b.csend = None, None
+    assert lib().moe_forward(ctypes.byref(ep.dims), ctypes.byref(ep.layout), ctypes.byref(b), None) == 0
+    code, _ = ep.status()
+    assert code == 0
+    o = orc.forward(wl.N, wl.T, wl.H, wl.E, wl.R, 0, payload, inp["x"], inp["idx"], inp["w"])
+    np.testing.assert_array_equal(u16(ep.out.cpu()), o["out"])
+
+
 LIMIT_CASES = [
     W("E1536-max", 8, 64, 256, 1536, 8, "bf16", "uniform", 180),      # largest E: 48 KB count tables
     W("N1536-L1", 1536, 2, 128, 1536, 2, "bf16", "uniform", 181),     # 1536 ranks, one expert each
