@@ -1,6 +1,7 @@
-// C ABI of libmoe_ep (declared in include/moe_ep.h): argument checks, workspace carving and
-// the kernel sequence of each dispatch/combine step. No allocation, no synchronisation
-// (except moe_status_sync), no fallback: every step runs in this library's kernels.
+// C ABI of libmoe_ep (declared in include/moe_ep.h): argument checks, workspace carving, the
+// kernel sequence of each dispatch/combine step and the token batches of the batched passes.
+// No memory allocation, no synchronisation (except moe_status_sync), no fallback: every step
+// runs in this library's kernels.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -28,13 +29,16 @@ struct DevInfo {
   int smem_optin = 0;
   int smem_per_sm = 0;
   int l2_bytes = 0;
-  // The host pass's second stream (highest priority) and its fork and join events, created
-  // on first use and kept until exit; fork_mu makes a fork (record, then wait) atomic.
+  // The library's second stream (highest priority), which takes the odd token batches of
+  // the batched passes, and the mapped host pass's fork and join events; created on first
+  // use and kept until exit. fork_mu makes a fork (record, then wait) atomic.
   cudaStream_t aux = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
   std::mutex fork_mu;
   // The copy-engine pipeline of the host pass: a stream for host-to-device and one for
-  // device-to-host copies, with their events; pipe_mu makes one pass's enqueue atomic.
+  // device-to-host copies, with their events; p_lay and p_aux fork the second stream from
+  // the caller's and join it back in every batched pass. pipe_mu makes one pass's enqueue
+  // atomic.
   bool pipe_ready = false;
   cudaStream_t cin = nullptr, cout = nullptr;
   cudaEvent_t p_start = nullptr, p_idx = nullptr, p_done = nullptr, p_lay = nullptr, p_aux = nullptr;
