@@ -644,7 +644,8 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["gbs"], "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": kernels[dom]["frac"],
                      "bytes_per_launch": ab[dom], "traffic": ncu_traffic(dom, wl.name),
-                     "traffic_warm_l2": ncu_traffic(dom, wl.name, "warm_l2")},
+                     "traffic_warm_l2": ncu_traffic(dom, wl.name, "warm_l2"),
+                     "launch": "whole-pass launch, timed in the per-kernel region (one batch)"},
         "kernels": kernels,
         "direct_push": {"value": round(tokens / (push_ms_all * 1e-3), 1), "unit": "tokens/s",
                         "ms_per_step": round(push_ms_all, 4),
