@@ -426,18 +426,22 @@ moe_status moe_forward(const moe_dims *dims, const moe_layout_t *lay, const moe_
  * there, then each batch's dispatch, identity expert and combine once its rows are there;
  * a second copy-engine stream copies each finished batch's rows of bufs->out into h_out.
  * The copies of one batch overlap the device work of the others without taking SMs from
- * it. The two streams and their events are created on the first such call per device and
- * kept until exit; the caller's stream waits for the last copy before the call returns, so
- * `stream` orders everything as usual (and the pass can be captured into a CUDA graph).
- * With MOE_FLAG_ONE_BATCH (or fp8 with MOE_FLAG_STAGED_QUANT): copies in, moe_forward,
- * copy out, all on `stream`.
+ * it. When an average batch's combine rows (pairs x 2H bytes) take at most 40% of the L2,
+ * odd batches' device work runs on the library's high-priority stream; otherwise all of it
+ * runs on `stream` and the first and last batches are half the size of the others. The
+ * streams and their events are created on the first such call per device and kept until
+ * exit; the caller's stream waits for them before the call returns, so `stream` orders
+ * everything as usual (and the pass can be captured into a CUDA graph).
+ * With MOE_FLAG_ONE_BATCH (or fp8 with MOE_FLAG_STAGED_QUANT): copies in, moe_forward in one
+ * batch, copy out, all on `stream`.
  * With MOE_FLAG_HOST_MAPPED and all four buffers pinned memory the device can address
  * (cudaHostAlloc / cudaHostRegister; over NVLink-C2C on Grace-Blackwell), the kernels read
  * the inputs and write the output there directly and bufs->x/idx/w/out are not used; with
  * T >= 2 (and neither direct push, staged fp8 quantisation nor MOE_FLAG_ONE_BATCH)
  * that pass runs in two token batches, the library's high-priority stream taking the
  * scatter and unpack of the first batch and its reduce while the caller's stream packs and
- * sends the second. Asynchronous: the caller synchronises `stream` before reading h_out. */
+ * sends the second (otherwise it is moe_forward on the mapped memory). Asynchronous: the
+ * caller synchronises `stream` before reading h_out. */
 moe_status moe_forward_host(const moe_dims *dims, const moe_layout_t *lay, const moe_buffers_t *bufs,
                             const uint16_t *h_x, const int32_t *h_idx, const float *h_w, uint16_t *h_out,
                             void *stream);
