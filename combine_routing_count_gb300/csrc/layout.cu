@@ -60,6 +60,12 @@ __device__ __forceinline__ int warp_inclusive_scan(int v, int lane) {
 // Every CTA reads the per-rank totals cnt[][] written by the counting kernel; lanes run
 // along the scanned dimension, so global stores are coalesced.
 constexpr int kScanThreads = 256;
+// Shared staging of the scan CTAs: a 64 x 33 tile (column CTAs), a row of E counts (row
+// CTAs), or E counts plus N sums (destination CTAs). The entry points accept E <= 1536,
+// and N <= E since E is a multiple of N.
+constexpr int kScanMaxE = 1536;
+constexpr int kScanTileInts = 2 * kScanMaxE;
+static_assert(kScanTileInts >= 64 * 33, "the column tile fits");
 
 __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -86,7 +92,7 @@ __device__ __forceinline__ int cnt_at(const LayoutArgs& a, int64_t i) {
 
 __global__ void __launch_bounds__(kScanThreads) k_route_scan(Geo g, LayoutArgs a) {
   __shared__ int warp_tot[kScanThreads / 32 + 1];
-  __shared__ int tile[64 * 33];
+  __shared__ int tile[kScanTileInts];
   const int N = g.N, E = g.E, L = g.L;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n_col = (E + 31) / 32;
@@ -104,8 +110,12 @@ __global__ void __launch_bounds__(kScanThreads) k_route_scan(Geo g, LayoutArgs a
       vals[j] = (j < k && e0 + j < E) ? cnt_at(a, (int64_t)s * E + e0 + j) : 0;
       sum += vals[j];
     }
+    int* row = tile;   // the row's counts (read once, summed from shared memory), E <= kScanMaxE
+#pragma unroll
+    for (int j = 0; j < 6; ++j)
+      if (j < k && e0 + j < E) row[e0 + j] = vals[j];
     int total;
-    int run = block_exclusive_scan(sum, warp_tot, total);
+    int run = block_exclusive_scan(sum, warp_tot, total);   // its barriers also publish row[]
 #pragma unroll
     for (int j = 0; j < 6; ++j)
       if (j < k && e0 + j < E) {
@@ -115,7 +125,7 @@ __global__ void __launch_bounds__(kScanThreads) k_route_scan(Geo g, LayoutArgs a
       }
     for (int d = warp; d < N; d += kScanThreads / 32) {   // C[s][d]: lanes along d's experts
       int c = 0;
-      for (int l = lane; l < L; l += 32) c += cnt_at(a, (int64_t)s * E + d * L + l);
+      for (int l = lane; l < L; l += 32) c += row[d * L + l];
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
       if (lane == 0) a.C[s * N + d] = c;
@@ -157,10 +167,18 @@ __global__ void __launch_bounds__(kScanThreads) k_route_scan(Geo g, LayoutArgs a
   } else {
     // ---- destination CTA: roff[d][.] and rtot[d]
     const int d = b - N - n_col;
-    int* cd = tile;   // cd[s] = C[s][d], N <= 64*33
+    // cnt[s][d*L + l] for every s and l (N * L = E values) in one round of loads, then the
+    // per-source sums from shared memory.
+    int* col = tile;                 // col[s * L + l]: E values
+    int* cd = tile + E;              // cd[s] = C[s][d]: E + N <= 2 * kScanMaxE
+    for (int i = tid; i < E; i += kScanThreads) {
+      const int s = i / L, l = i - s * L;
+      col[i] = cnt_at(a, (int64_t)s * E + d * L + l);
+    }
+    __syncthreads();
     for (int s = warp; s < N; s += kScanThreads / 32) {
       int c = 0;
-      for (int l = lane; l < L; l += 32) c += cnt_at(a, (int64_t)s * E + d * L + l);
+      for (int l = lane; l < L; l += 32) c += col[s * L + l];
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
       if (lane == 0) cd[s] = c;
