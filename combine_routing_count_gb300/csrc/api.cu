@@ -29,7 +29,7 @@ struct DevInfo {
   int smem_optin = 0;
   int smem_per_sm = 0;
   int l2_bytes = 0;
-  // The library's second stream (highest priority), which takes the odd token batches of
+  // The library's second stream (default priority), which takes the odd token batches of
   // the batched passes, and the mapped host pass's fork and join events; created on first
   // use and kept until exit. fork_mu makes a fork (record, then wait) atomic.
   cudaStream_t aux = nullptr;
@@ -52,11 +52,12 @@ DevInfo* aux_for(int dev) {
   std::lock_guard<std::mutex> lk(g_dev_mu);
   DevInfo& di = g_dev[dev];
   if (!di.aux) {
-    int least = 0, greatest = 0;
-    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return nullptr;
+    // Default priority: batches on the two streams interleave their CTAs fairly (measured
+    // with the second stream at the highest priority, its batches ran ahead and the step
+    // was 3-7% slower).
     cudaStream_t s = nullptr;
     cudaEvent_t f = nullptr, j = nullptr;
-    if (cudaStreamCreateWithPriority(&s, cudaStreamNonBlocking, greatest) != cudaSuccess) return nullptr;
+    if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
     if (cudaEventCreateWithFlags(&f, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&j, cudaEventDisableTiming) != cudaSuccess) {
       if (f) cudaEventDestroy(f);
@@ -394,7 +395,7 @@ int phase_batch_count(const Geo& g, const moe_layout_t* lay) {
 }
 
 // Runs fn(t0, nt, ctx) for nb equal token ranges of every rank, odd ones on the library's
-// high-priority stream (which starts after everything issued so far on the caller's
+// second stream (which starts after everything issued so far on the caller's
 // stream); the caller's stream waits for it at the end. One range on the caller's stream
 // when nb is 1.
 template <typename F>
@@ -419,7 +420,7 @@ cudaError_t run_batches(const Geo& g, Ctx& c, int nb, F&& fn) {
 
 // moe_forward as nb micro-batches (tokens [j*T/nb, (j+1)*T/nb) of every rank), each running
 // dispatch, identity expert and combine on its own rows, odd ones on the library's
-// high-priority stream: a micro-batch's rows of each buffer are still in L2 when its next
+// second stream: a micro-batch's rows of each buffer are still in L2 when its next
 // move reads them, and one batch's first kernels fill the SMs its neighbour's last kernels
 // leave idle. The batches touch disjoint rows of every buffer. The caller's stream waits for
 // the auxiliary stream before the call returns.
@@ -441,7 +442,7 @@ moe_status forward_batched(const Geo& g, const moe_dims* dims, const moe_layout_
 // work once its rows are there; the output stream copies each finished batch's output rows
 // back. Copy engines move the host bytes, so batch j's copies in and out overlap the device
 // work of its neighbours without taking SMs from it. When an average batch's combine rows
-// take at most 40% of L2, odd batches run on the library's high-priority stream, so one batch's
+// take at most 40% of L2, odd batches run on the library's second stream, so one batch's
 // first kernels fill the SMs its neighbour's last kernels leave idle (the batches touch
 // disjoint rows of every buffer); with larger batches the two would evict each other's
 // rows from L2 between consecutive moves, and one stream measured faster (GB300: 29 and

@@ -373,7 +373,7 @@ moe_status moe_combine_recv(const moe_dims *dims, const moe_layout_t *lay, const
  * nb token batches (nb = moe_batches(dims, lay, 2): lay->batches, else none up to 1024
  * tokens of all ranks and about T/8 beyond, at most 16; one with MOE_FLAG_ONE_BATCH), batch j
  * covering tokens [j*T/nb, (j+1)*T/nb) of every rank, odd batches on the library's
- * high-priority stream, which the caller's stream waits for before the call returns. Every
+ * second stream, which the caller's stream waits for before the call returns. Every
  * buffer ends up as with the separate calls, bit for bit. */
 moe_status moe_dispatch(const moe_dims *dims, const moe_layout_t *lay, const void *d_x, void *d_send,
                         void *d_recv, void *d_expert_x, float *d_expert_scale, void *stream);
@@ -408,7 +408,7 @@ moe_status moe_combine_recv_partial(const moe_dims *dims, const moe_layout_t *la
  * one with MOE_FLAG_ONE_BATCH or staged fp8 quantisation). Micro-batch j covers tokens
  * [j*T/nb, (j+1)*T/nb) of every rank and runs dispatch send and recv, the identity expert
  * and the combine on only those tokens' rows (the same kernels, restricted to a token
- * range), odd micro-batches on the library's high-priority stream (created on first use,
+ * range), odd micro-batches on the library's second stream (created on first use,
  * kept until exit); the caller's stream waits for it before the call returns. Every
  * buffer ends up as in one batch, bit for bit.
  * Graph capture: a captured call forks the library's stream into the capture and joins it
@@ -427,7 +427,7 @@ moe_status moe_forward(const moe_dims *dims, const moe_layout_t *lay, const moe_
  * a second copy-engine stream copies each finished batch's rows of bufs->out into h_out.
  * The copies of one batch overlap the device work of the others without taking SMs from
  * it. When an average batch's combine rows (pairs x 2H bytes) take at most 40% of the L2,
- * odd batches' device work runs on the library's high-priority stream; otherwise all of it
+ * odd batches' device work runs on the library's second stream; otherwise all of it
  * runs on `stream` and the first and last batches are half the size of the others. The
  * streams and their events are created on the first such call per device and kept until
  * exit; the caller's stream waits for them before the call returns, so `stream` orders
@@ -438,7 +438,7 @@ moe_status moe_forward(const moe_dims *dims, const moe_layout_t *lay, const moe_
  * (cudaHostAlloc / cudaHostRegister; over NVLink-C2C on Grace-Blackwell), the kernels read
  * the inputs and write the output there directly and bufs->x/idx/w/out are not used; with
  * T >= 2 (and neither direct push, staged fp8 quantisation nor MOE_FLAG_ONE_BATCH)
- * that pass runs in two token batches, the library's high-priority stream taking the
+ * that pass runs in two token batches, the library's second stream taking the
  * scatter and unpack of the first batch and its reduce while the caller's stream packs and
  * sends the second (otherwise it is moe_forward on the mapped memory). Asynchronous: the
  * caller synchronises `stream` before reading h_out. */
