@@ -364,16 +364,17 @@ int batch_start(int T, int nb, int j, bool shaped) {
 }
 
 // Micro-batches of moe_forward: the caller's choice (at most 32 and T), else about one per
-// 256 tokens of all ranks (at most 16 and T); one with MOE_FLAG_ONE_BATCH or staged fp8
-// quantisation. Measured on GB300 with batches alternating over two streams: 4 batches of
-// 1024 tokens 9% faster than one, 4 of 2048 (fp8, expert included) 10%, 16 of 4096 22%,
-// 16 of 8192 17%; up to ~400 tokens one batch is fastest. Even counts keep both streams
-// equally loaded (1024 tokens: 3 and 5 batches lose to 4).
+// 60 MB of dispatch and combine rows (pairs x (B + 2H) bytes; at most 16 and T); one with
+// MOE_FLAG_ONE_BATCH or staged fp8 quantisation. Measured on GB300 with batches alternating
+// over two equal-priority streams, each the best of the counts tried: 4 batches of 235 MB
+// of rows (EP8, 18% faster than one), 6 of 356 MB (fp8 EP64, expert included, 16%), 16 of
+// 940 MB and 1074 MB (EP32 28%, EP16 24%); under ~35 MB one batch is fastest. Even counts
+// keep both streams equally loaded (EP8: 3 and 6 batches lose to 4).
 int forward_batch_count(const Geo& g, const moe_layout_t* lay) {
   if (lay->flags & MOE_FLAG_ONE_BATCH) return 1;
   if (g.payload == MOE_PAYLOAD_FP8_E4M3_B128 && (lay->flags & MOE_FLAG_STAGED_QUANT)) return 1;
   int nb = lay->batches;
-  if (nb <= 0) nb = (int)std::min(16L, std::lround((double)g.N * g.T / 256.0));
+  if (nb <= 0) nb = (int)std::min(16L, std::lround((double)g.P * (g.B + 2.0 * g.H) / 60e6));
   if (nb > kMaxMicroBatches) nb = kMaxMicroBatches;
   if (nb > g.T) nb = (int)g.T;
   return nb < 1 ? 1 : nb;

@@ -130,20 +130,20 @@ def test_host_batch_count_rule(L):
 
 
 def test_forward_micro_batch_count_rule(L):
-    """moe_forward's micro-batches: about one per 256 tokens of all ranks by default (at most
-    16 and T), the caller's count when set (at most 32 and T), one for the one-batch flag and
+    """moe_forward's micro-batches: about one per 60 MB of dispatch and combine rows by default
+    (at most 16 and T), the caller's count when set (at most 32 and T), one for the one-batch flag and
     for the staged fp8 quantiser. Host only."""
     from combine_routing_count_gb300 import MoeLayout
     def nb(N, T, H, E, R, payload=0, flags=0, batches=0):
         lay = MoeLayout()
         lay.flags, lay.batches = flags, batches
         return L.moe_batches(ctypes.byref(_dims(N, T, H, E, R, 0, payload)), ctypes.byref(lay), 0)
-    assert nb(8, 128, 7168, 256, 8) == 4         # 1024 tokens
-    assert nb(64, 32, 7168, 384, 8, 1) == 8      # 2048 tokens, fp8
-    assert nb(32, 128, 7168, 384, 8) == 16       # 4096 tokens
-    assert nb(16, 512, 4096, 128, 8) == 16       # 8192 tokens: capped
+    assert nb(8, 128, 7168, 256, 8) == 4         # 235 MB of rows
+    assert nb(64, 32, 7168, 384, 8, 1) == 6      # 356 MB (fp8 rows of 7392 B)
+    assert nb(32, 128, 7168, 384, 8) == 16       # 940 MB
+    assert nb(16, 512, 4096, 128, 8) == 16       # 1074 MB: capped
     assert nb(2, 16, 128, 8, 2) == 1             # 32 tokens
-    assert nb(4, 96, 1024, 16, 4) == 2           # 384 tokens
+    assert nb(8, 64, 7168, 256, 8) == 2          # 117 MB
     assert nb(8, 128, 7168, 256, 8, batches=3) == 3
     assert nb(8, 2, 7168, 256, 8, batches=9) == 2
     assert nb(16, 512, 4096, 128, 8, batches=20) == 20
