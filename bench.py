@@ -56,6 +56,8 @@ def parse_args(argv=None):
     p.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     p.add_argument("--staged-quant", action="store_true",
                    help="fp8: quantise into a staging buffer, then pack (two kernels) instead of inside the pack")
+    p.add_argument("--batches", type=int, default=0,
+                   help="token batches of the batched passes (0: the library's automatic choice)")
     p.add_argument("--one-batch", action="store_true",
                    help="run moe_forward (and the host pass) as one token batch instead of micro-batches")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -308,7 +310,7 @@ def run_ours(args):
     ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, wl.payload, alias_buffers=(wl.payload == "bf16"),
                flags={"auto": 0, "ldg": 1, "tma": 4}[args.mover] | (2 if args.no_pdl else 0) |
                (0x10 if args.staged_quant else 0) | (0x40 if args.one_batch else 0), tma_stages=args.tma_stages,
-               ctas_per_sm=args.ctas_per_sm)
+               ctas_per_sm=args.ctas_per_sm, batches=args.batches)
     x = torch.from_numpy(inp["x"]).view(torch.bfloat16).to(device)
     idx = torch.from_numpy(inp["idx"]).to(device)
     w = torch.from_numpy(inp["w"]).to(device)
