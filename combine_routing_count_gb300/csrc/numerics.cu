@@ -274,6 +274,126 @@ __global__ void __launch_bounds__(256) k_quant_pack(Geo g, const uint16_t* __res
   pdl_trigger();
 }
 
+// The fused quantise-and-pack for rows that are 16-byte multiples: 8 lanes per 128-value
+// block and 16 consecutive values per lane (two 16-byte loads), so that each destination
+// row gets one 16-byte code store per lane and block instead of two 8-byte ones. A warp
+// unit covers blocks 8u .. 8u+7 of a row: lane (q, sub) takes block 8u + q + 4j, j < 2.
+// Same products, conversions, bracket and settling as quant_unit, value for value.
+constexpr int kQ16Blocks = 2;   // blocks per lane and unit
+
+__device__ __forceinline__ void quant_unit16(const uint16_t* xr, int bbase, int nb, int sub,
+                                             uint32_t (&codes)[kQ16Blocks][4], float (&scale)[kQ16Blocks]) {
+  uint4 v[kQ16Blocks][2];
+#pragma unroll
+  for (int j = 0; j < kQ16Blocks; ++j) {
+    const int b = bbase + 4 * j;
+    const uint16_t* p = xr + b * 128 + sub * 16;
+    v[j][0] = b < nb ? ld_stream16(p) : make_uint4(0, 0, 0, 0);
+    v[j][1] = b < nb ? ld_stream16(p + 8) : make_uint4(0, 0, 0, 0);
+  }
+  uint32_t any = 0, pend = 0;   // pend bit 16j + 4i + e: value e of word i of block j to settle
+#pragma unroll
+  for (int j = 0; j < kQ16Blocks; ++j) {
+    const uint32_t u[8] = {v[j][0].x, v[j][0].y, v[j][0].z, v[j][0].w, v[j][1].x, v[j][1].y, v[j][1].z, v[j][1].w};
+    float f[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      f[2 * i] = bf16_lo(u[i]);
+      f[2 * i + 1] = bf16_hi(u[i]);
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+    for (int o = 4; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o, 8));
+    const float sc = block_scale(amax);
+    scale[j] = sc;
+    const bool tiny = sc < 0x1p-90f;
+    float rlo, rhi;
+    bracket_rcp(tiny ? 1.0f : sc, rlo, rhi);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float* fi = f + 4 * i;
+      const uint32_t wl = e4m3x4_rn_sat(__fmul_rn(fi[0], rlo), __fmul_rn(fi[1], rlo), __fmul_rn(fi[2], rlo),
+                                        __fmul_rn(fi[3], rlo));
+      const uint32_t wh = e4m3x4_rn_sat(__fmul_rn(fi[0], rhi), __fmul_rn(fi[1], rhi), __fmul_rn(fi[2], rhi),
+                                        __fmul_rn(fi[3], rhi));
+      codes[j][i] = wl;
+      const uint32_t d = tiny ? 0xffffffffu : (wl ^ wh);
+      any |= d;
+      pend |= nonzero_bytes(d) << (16 * j + 4 * i);
+    }
+  }
+  if (!any) return;
+  while (pend) {
+    const int bit = __ffs(pend) - 1;
+    pend &= pend - 1;
+    const int j = bit >> 4, i = (bit >> 2) & 3, e = bit & 3;
+    const int k = 4 * i + e;            // value of the lane's 16
+    const int h = k >> 3, q = (k & 7) >> 1;
+    float sc = scale[0];
+    uint32_t pair = v[0][0].x;
+#pragma unroll
+    for (int jj = 0; jj < kQ16Blocks; ++jj) {
+      sc = j == jj ? scale[jj] : sc;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const bool at = j == jj && h == hh;
+        pair = (at && q == 0) ? v[jj][hh].x : pair;
+        pair = (at && q == 1) ? v[jj][hh].y : pair;
+        pair = (at && q == 2) ? v[jj][hh].z : pair;
+        pair = (at && q == 3) ? v[jj][hh].w : pair;
+      }
+    }
+    const uint32_t c = e4m3_code_exact((k & 1) ? bf16_hi(pair) : bf16_lo(pair), sc);
+#pragma unroll
+    for (int jj = 0; jj < kQ16Blocks; ++jj)
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii)
+        if (j == jj && i == ii) codes[jj][ii] = (codes[jj][ii] & ~(0xffu << (8 * e))) | (c << (8 * e));
+  }
+}
+
+template <bool RANGED>
+__global__ void __launch_bounds__(256) k_quant_pack16(Geo g, const uint16_t* __restrict__ x,
+                                                      const int32_t* __restrict__ fan, uint8_t* __restrict__ dst,
+                                                      int t0, int nt) {
+  const int nb = g.H / 128;
+  const int upr = (nb + 7) / 8;   // warp units per row
+  const int64_t units = (int64_t)g.N * (RANGED ? nt : g.T) * upr;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane & 7;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  pdl_wait();
+  for (int64_t u = warp; u < units; u += nwarps) {   // warp-uniform
+    const int64_t rv = units <= INT32_MAX ? (int64_t)((uint32_t)u / (uint32_t)upr) : u / upr;
+    const int bbase = (int)(u - rv * upr) * 8 + (lane >> 3);   // block of j = 0
+    const int64_t row = RANGED ? (rv / nt) * g.T + t0 + rv % nt : rv;   // token
+    const int32_t* fr = fan + row * g.R;
+    const int myp = lane < g.R ? __ldg(fr + lane) : -1;   // rows of pairs 0..31 (R > 32: loaded)
+    uint32_t codes[kQ16Blocks][4];
+    float scale[kQ16Blocks];
+    quant_unit16(x + row * g.H, bbase, nb, sub, codes, scale);
+#pragma unroll 1
+    for (int k = 0; k < g.R; ++k) {
+      const int p = k < 32 ? __shfl_sync(kFull, myp, k) : __ldg(fr + k);
+      if (p < 0) continue;
+      uint8_t* dr = dst + (int64_t)p * g.B;
+#pragma unroll
+      for (int j = 0; j < kQ16Blocks; ++j) {
+        const int b = bbase + 4 * j;
+        if (b < nb) {
+          *reinterpret_cast<uint4*>(dr + b * 128 + sub * 16) = make_uint4(codes[j][0], codes[j][1], codes[j][2],
+                                                                          codes[j][3]);
+          if (sub == 0) *reinterpret_cast<float*>(dr + g.H + 4 * b) = scale[j];
+        }
+      }
+    }
+  }
+  pdl_trigger();
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
   const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
@@ -675,6 +795,10 @@ cudaError_t launch_quant_pack(const Geo& g, const int32_t* fan, const uint16_t* 
   if (blocks > maxb) blocks = maxb;
   LaunchScope ls(c, MOE_K_QUANT_PACK);
   const bool ranged = nt != g.T;
+  if (g.B % 16 == 0) {   // 16-byte code stores (same unit count: 8 blocks of a row per warp)
+    auto k16 = ranged ? k_quant_pack16<true> : k_quant_pack16<false>;
+    return launch_kernel(k16, dim3((unsigned)blocks), dim3(256), 0, c, g, x, fan, dst, t0, nt);
+  }
   auto k = g.B % 8 == 0 ? (ranged ? k_quant_pack<true, true> : k_quant_pack<true, false>)
                         : (ranged ? k_quant_pack<false, true> : k_quant_pack<false, false>);
   return launch_kernel(k, dim3((unsigned)blocks), dim3(256), 0, c, g, x, fan, dst, t0, nt);
