@@ -64,6 +64,26 @@ def test_duplicates_and_bad_ids(orc, flags):
     compare_all(orc, wl, inp, res, push=bool(flags & 8))
 
 
+@pytest.mark.parametrize("mode", ["forward", "phases"])
+@pytest.mark.parametrize("flags", [0, 4, 8], ids=["auto", "tma", "push"])
+@pytest.mark.parametrize("payload", ["bf16", "fp8"])
+def test_duplicates_and_bad_ids_in_token_batches(orc, payload, flags, mode):
+    """Duplicate experts in a token and ids outside [0, E), with the pass split into 3 token
+    batches (moe_forward's micro-batches, or moe_dispatch / moe_combine): status bit, no
+    trap, every buffer as the oracle's."""
+    wl = W("dups-mb", 3, 21, 512, 12, 4, payload, "uniform", 111)
+    inp = workloads.make_inputs(wl)
+    rng = np.random.default_rng(1)
+    idx = rng.integers(0, wl.E, size=(wl.N, wl.T, wl.R)).astype(np.int32)   # duplicates allowed
+    idx[0, 3, 1] = -1
+    idx[2, 20, 0] = wl.E
+    idx[1, 9, 3] = 1 << 30
+    inp["idx"] = idx
+    _, res = run_gpu(wl, inp, flags=flags, batches=3, **{mode: True})
+    assert res["status_code"] == 2                      # MOE_ERR_EXPERT_RANGE, no trap
+    compare_all(orc, wl, inp, res, push=bool(flags & 8), fused_quant=True)
+
+
 def test_random_tiny_layouts_bit_exact(orc):
     from combine_routing_count_gb300 import MoeEP
     rng = np.random.default_rng(1234)
