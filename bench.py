@@ -649,6 +649,9 @@ def run_ours(args):
                    "parallelism": f"{ws} independent replica(s) of the {wl.N}-rank group"},
         "hbm_gbs": round(step_bytes / (mean_ms * 1e-3) / 1e9, 1),
         "hbm_frac": round(step_bytes / (mean_ms * 1e-3) / 1e9 / peak, 3),
+        "hbm_note": "step-level algorithmic bytes / step time: above 1.0 because consecutive moves read "
+                    "part of their input from L2 (alternating unit order, token batches); the per-kernel "
+                    "roofline below is of whole-pass launches",
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["gbs"], "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": kernels[dom]["frac"],
                      "bytes_per_launch": ab[dom], "traffic": ncu_traffic(dom, wl.name),
