@@ -5,11 +5,13 @@
  *
  * Reads the bf16 tokens [N][T][H], int32 expert ids [N][T][R] and fp32 weights [N][T][R],
  * allocates every device buffer itself (cudaMalloc: the library allocates nothing), runs
- * moe_layout_init, moe_forward and moe_status_sync on its own stream, and writes the bf16
+ * moe_layout_init, moe_forward (then the same pass through moe_dispatch and moe_combine in
+ * token batches, which must match) and moe_status_sync on its own stream, and writes the bf16
  * output [N][T][H]. Exit status 0 on success, else the step that failed on stderr. */
 #include <stdint.h>
 #include <stdio.h>
 #include <stdlib.h>
+#include <string.h>
 
 #include <cuda_runtime.h>
 
@@ -91,6 +93,22 @@ int main(int argc, char **argv) {
     st = moe_status_sync(&lay, s, &bits);
     CHECK(st == MOE_OK, moe_status_string(st));
     CHECK(cudaMemcpy(hout, b.out, xb, cudaMemcpyDeviceToHost) == cudaSuccess, "copy out");
+
+    /* The same pass through the whole-phase calls, in 3 token batches each: the layout,
+     * moe_dispatch, the identity expert, moe_combine; the output must equal moe_forward's. */
+    lay.batches = 3;
+    CHECK(moe_batches(&d, &lay, 2) == (d.T < 3 ? d.T : 3), "moe_batches");
+    uint16_t *out2 = (uint16_t *)dev(xb), *hout2 = (uint16_t *)malloc(xb);
+    CHECK(out2 && hout2, "second output");
+    st = moe_layout(&d, b.idx, &lay, s);
+    if (st == MOE_OK) st = moe_dispatch(&d, &lay, b.x, b.send, b.recv, b.expert_x, b.expert_scale, s);
+    if (st == MOE_OK) st = moe_expert_identity(&d, &lay, b.expert_x, b.expert_scale, b.expert_y, s);
+    if (st == MOE_OK) st = moe_combine(&d, &lay, b.expert_y, b.csend, b.crecv, b.w, out2, s);
+    CHECK(st == MOE_OK, moe_status_string(st));
+    st = moe_status_sync(&lay, s, &bits);
+    CHECK(st == MOE_OK, moe_status_string(st));
+    CHECK(cudaMemcpy(hout2, out2, xb, cudaMemcpyDeviceToHost) == cudaSuccess, "copy out2");
+    CHECK(memcmp(hout, hout2, xb) == 0, "moe_dispatch + moe_combine differ from moe_forward");
 
     FILE *f = fopen(argv[10], "wb");
     CHECK(f && fwrite(hout, 1, xb, f) == xb, "writing the output");
