@@ -168,3 +168,42 @@ def test_phase_batch_count_rule(L):
     assert nb(8, 128, 7168, 256, 8, batches=5) == 5
     assert nb(16, 512, 4096, 128, 8, flags=0x40) == 1
     assert L.moe_batches(ctypes.byref(_dims()), ctypes.byref(MoeLayout()), 3) == 0
+
+
+def _fake_layout():
+    """A layout whose arrays are non-null placeholders: enough for the host-side argument
+    checks, which return before anything touches device memory."""
+    from combine_routing_count_gb300 import MoeLayout
+    from combine_routing_count_gb300._abi import LAYOUT_FIELDS
+    lay = MoeLayout()
+    for i, f in enumerate(LAYOUT_FIELDS):
+        setattr(lay, f, 0x100000 + 256 * i)
+    return lay
+
+
+def test_batched_entry_points_reject_bad_arguments_without_gpu(L):
+    """moe_dispatch, moe_combine and moe_forward check their arguments on the host and
+    return MOE_ERR_INVALID_ARG (1) before any CUDA call: missing or misaligned buffers, a
+    missing layout. (Runs on a machine without a GPU.)"""
+    d = _dims(4, 8, 256, 16, 4)
+    lay = _fake_layout()
+    A, M = 0x200000, 0x200008            # a 16-byte aligned and a misaligned placeholder
+    # moe_dispatch(dims, lay, x, send, recv, expert_x, expert_scale, stream)
+    assert L.moe_dispatch(ctypes.byref(d), ctypes.byref(lay), None, A, A, A, None, None) == 1
+    assert L.moe_dispatch(ctypes.byref(d), ctypes.byref(lay), M, A, A, A, None, None) == 1
+    assert L.moe_dispatch(ctypes.byref(d), ctypes.byref(lay), A, None, A, A, None, None) == 1   # send needed
+    assert L.moe_dispatch(ctypes.byref(d), None, A, A, A, A, None, None) == 1
+    fp8 = _dims(4, 8, 256, 16, 4, 0, 1)
+    assert L.moe_dispatch(ctypes.byref(fp8), ctypes.byref(lay), A, A, A, A, None, None) == 1   # scales needed
+    # moe_combine(dims, lay, expert_y, csend, crecv, w, out, stream)
+    assert L.moe_combine(ctypes.byref(d), ctypes.byref(lay), A, A, A, None, A, None) == 1
+    assert L.moe_combine(ctypes.byref(d), ctypes.byref(lay), A, None, A, A, A, None) == 1     # csend needed
+    assert L.moe_combine(ctypes.byref(d), ctypes.byref(lay), A, A, M, A, A, None) == 1
+    # moe_forward with a micro-batched pass and a missing receive buffer
+    from combine_routing_count_gb300 import MoeBuffers
+    b = MoeBuffers()
+    for f in ("x", "idx", "w", "send", "expert_x", "expert_y", "csend", "crecv", "out"):
+        setattr(b, f, A)
+    lay.batches = 3
+    assert L.moe_forward(ctypes.byref(d), ctypes.byref(lay), ctypes.byref(b), None) == 1
+    assert L.moe_forward(ctypes.byref(d), ctypes.byref(lay), None, None) == 1
