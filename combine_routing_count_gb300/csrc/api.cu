@@ -805,7 +805,13 @@ moe_status moe_forward(const moe_dims* dims, const moe_layout_t* lay, const moe_
   moe_status st = make_geo(dims, g);
   if (st != MOE_OK) return st;
   const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
-  if (layout_ok(lay)) {
+  // Every buffer is checked before anything is launched (an empty batch needs none).
+  if (!layout_ok(lay)) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)g.N * g.T > 0 &&
+      (!pass_buffers_ok(b, lay->flags, fp8, true) ||
+       (fp8 && (lay->flags & MOE_FLAG_STAGED_QUANT) && (!b->xq || !aligned16(b->xq)))))
+    return MOE_ERR_INVALID_ARG;
+  {
     const int nb = moe_batches(dims, lay, 0);
     if (nb > 1) return forward_batched(g, dims, lay, b, nb, stream);
   }

@@ -207,3 +207,21 @@ def test_batched_entry_points_reject_bad_arguments_without_gpu(L):
     lay.batches = 3
     assert L.moe_forward(ctypes.byref(d), ctypes.byref(lay), ctypes.byref(b), None) == 1
     assert L.moe_forward(ctypes.byref(d), ctypes.byref(lay), None, None) == 1
+
+
+def test_forward_in_one_batch_checks_every_buffer_first(L):
+    """moe_forward in one batch returns MOE_ERR_INVALID_ARG for a missing buffer before the
+    layout is launched (without a GPU, a launch would fail with MOE_ERR_CUDA instead)."""
+    from combine_routing_count_gb300 import MoeBuffers
+    d = _dims(4, 8, 256, 16, 4)
+    lay = _fake_layout()
+    lay.flags = 0x40
+    A = 0x200000
+    b = MoeBuffers()
+    for f in ("x", "idx", "w", "send", "recv", "expert_x", "expert_y", "csend", "crecv"):
+        setattr(b, f, A)
+    assert L.moe_forward(ctypes.byref(d), ctypes.byref(lay), ctypes.byref(b), None) == 1   # out missing
+    fp8 = _dims(4, 8, 256, 16, 4, 0, 1)
+    b.out, b.expert_scale = A, A
+    lay.flags = 0x40 | 0x10                                                                # staged quantiser
+    assert L.moe_forward(ctypes.byref(fp8), ctypes.byref(lay), ctypes.byref(b), None) == 1  # xq missing
