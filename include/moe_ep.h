@@ -367,8 +367,8 @@ moe_status moe_combine_recv(const moe_dims *dims, const moe_layout_t *lay, const
 
 /* Whole phases, as the page's dispatch and combine calls (section "Dispatch and combine"):
  * moe_dispatch is moe_dispatch_send followed by moe_dispatch_recv (fp8: d_x holds the bf16
- * token rows, quantised inside the pack as moe_quantize_dispatch_send does; d_send unused
- * with MOE_FLAG_DIRECT_PUSH); moe_combine is moe_combine_send followed by moe_combine_recv.
+ * token rows, always quantised inside the pack as moe_quantize_dispatch_send does, so
+ * MOE_FLAG_STAGED_QUANT does not apply; d_send unused with MOE_FLAG_DIRECT_PUSH); moe_combine is moe_combine_send followed by moe_combine_recv.
  * Arguments as in those calls; the expert work goes between the two. Each phase may run in
  * nb token batches (nb = moe_batches(dims, lay, 2): lay->batches, else none up to 1024
  * tokens of all ranks and about T/8 beyond, at most 16; one with MOE_FLAG_ONE_BATCH), batch j
