@@ -354,6 +354,38 @@ __device__ __forceinline__ void quant_unit16(const uint16_t* xr, int bbase, int 
   }
 }
 
+// moe_quantize_fp8_b128 for rows that are 16-byte multiples: quant_unit16's lane layout,
+// one 16-byte code store per lane and block.
+__global__ void __launch_bounds__(256) k_quant_fp8_16(Geo g, const uint16_t* __restrict__ x,
+                                                      uint8_t* __restrict__ xq) {
+  const int nb = g.H / 128;
+  const int upr = (nb + 7) / 8;   // warp units per row
+  const int64_t units = (int64_t)g.N * g.T * upr;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane & 7;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  pdl_wait();
+  for (int64_t u = warp; u < units; u += nwarps) {   // warp-uniform
+    const int64_t row = units <= INT32_MAX ? (int64_t)((uint32_t)u / (uint32_t)upr) : u / upr;
+    const int bbase = (int)(u - row * upr) * 8 + (lane >> 3);   // block of j = 0
+    uint32_t codes[kQ16Blocks][4];
+    float scale[kQ16Blocks];
+    quant_unit16(x + row * g.H, bbase, nb, sub, codes, scale);
+    uint8_t* qr = xq + row * g.B;
+#pragma unroll
+    for (int j = 0; j < kQ16Blocks; ++j) {
+      const int b = bbase + 4 * j;
+      if (b < nb) {
+        *reinterpret_cast<uint4*>(qr + b * 128 + sub * 16) = make_uint4(codes[j][0], codes[j][1], codes[j][2],
+                                                                        codes[j][3]);
+        if (sub == 0) *reinterpret_cast<float*>(qr + g.H + 4 * b) = scale[j];
+      }
+    }
+  }
+  pdl_trigger();
+}
+
 template <bool RANGED>
 __global__ void __launch_bounds__(256) k_quant_pack16(Geo g, const uint16_t* __restrict__ x,
                                                       const int32_t* __restrict__ fan, uint8_t* __restrict__ dst,
@@ -781,6 +813,8 @@ cudaError_t launch_quant_fp8(const Geo& g, const uint16_t* x, uint8_t* xq, Ctx& 
   const int64_t maxb = (int64_t)c.num_sms * 8;
   if (blocks > maxb) blocks = maxb;
   LaunchScope ls(c, MOE_K_QUANT_FP8);
+  if (g.B % 16 == 0)   // 16-byte code stores (same unit count: 8 blocks of a row per warp)
+    return launch_kernel(k_quant_fp8_16, dim3((unsigned)blocks), dim3(256), 0, c, g, x, xq);
   return launch_kernel(k_quant_fp8, dim3((unsigned)blocks), dim3(256), 0, c, g, x, xq);
 }
 
