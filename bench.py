@@ -4,7 +4,11 @@
 A step is one whole pass of the path over one batch of N simulated ranks' tokens:
 routing layout (histogram, scans, placements) -> dispatch send (pack + per-peer write) ->
 dispatch recv (grouped expert rows) -> identity expert -> combine send (reverse shuffle +
-per-peer write back) -> combine recv (fp32 weighted sum -> bf16).
+per-peer write back) -> combine recv (fp32 weighted sum -> bf16). The bf16 step is one
+moe_forward call, which runs the pass in the library's token micro-batches; the fp8 step
+calls the layout, moe_dispatch, the identity expert and moe_combine (in token batches) so
+that the expert can be timed apart and left out. The same step in one batch is reported
+beside it (`one_batch`), as are the per-kernel times of whole-pass launches (roofline).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1] [--impl reference]
 
