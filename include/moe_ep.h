@@ -19,8 +19,9 @@
  *  - The caller allocates and owns all memory. The library never allocates or frees memory
  *    and never synchronises, except moe_status_sync; the batched passes (moe_forward,
  *    moe_dispatch, moe_combine, moe_forward_host) create three streams of their own and a
- *    few events per device on first use and keep them until exit. `stream` is a cudaStream_t (NULL = the
- *    legacy default stream). All calls are asynchronous on that stream; a buffer may be
+ *    few events per device on first use and keep them until exit. `stream` is a
+ *    cudaStream_t (NULL = the legacy default stream). All calls are asynchronous on that
+ *    stream; a buffer may be
  *    reused once the stream has passed its consumer (the buffer-reuse barrier between
  *    dispatch and combine of the page's section "Dispatch and combine" is stream order).
  *  - Host-checkable argument errors return MOE_ERR_INVALID_ARG before anything is launched.
@@ -368,11 +369,12 @@ moe_status moe_combine_recv(const moe_dims *dims, const moe_layout_t *lay, const
 /* Whole phases, as the page's dispatch and combine calls (section "Dispatch and combine"):
  * moe_dispatch is moe_dispatch_send followed by moe_dispatch_recv (fp8: d_x holds the bf16
  * token rows, always quantised inside the pack as moe_quantize_dispatch_send does, so
- * MOE_FLAG_STAGED_QUANT does not apply; d_send unused with MOE_FLAG_DIRECT_PUSH); moe_combine is moe_combine_send followed by moe_combine_recv.
- * Arguments as in those calls; the expert work goes between the two. Each phase may run in
- * nb token batches (nb = moe_batches(dims, lay, 2): lay->batches, else none up to 1024
- * tokens of all ranks and about T/8 beyond, at most 16; one with MOE_FLAG_ONE_BATCH), batch j
- * covering tokens [j*T/nb, (j+1)*T/nb) of every rank, odd batches on the library's
+ * MOE_FLAG_STAGED_QUANT does not apply; d_send unused with MOE_FLAG_DIRECT_PUSH);
+ * moe_combine is moe_combine_send followed by moe_combine_recv. Arguments as in those
+ * calls; the expert work goes between the two. Each phase may run in nb token batches
+ * (nb = moe_batches(dims, lay, 2): lay->batches, else none up to 1024 tokens of all ranks
+ * and about T/8 beyond, at most 16; one with MOE_FLAG_ONE_BATCH), batch j covering tokens
+ * [j*T/nb, (j+1)*T/nb) of every rank, odd batches on the library's
  * second stream, which the caller's stream waits for before the call returns. Every
  * buffer ends up as with the separate calls, bit for bit. */
 moe_status moe_dispatch(const moe_dims *dims, const moe_layout_t *lay, const void *d_x, void *d_send,
