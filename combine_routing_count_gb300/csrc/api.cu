@@ -369,12 +369,16 @@ int batch_start(int T, int nb, int j, bool shaped) {
 // over two equal-priority streams, each the best of the counts tried: 4 batches of 235 MB
 // of rows (EP8, 18% faster than one), 6 of 356 MB (fp8 EP64, expert included, 16%), 16 of
 // 940 MB and 1074 MB (EP32 28%, EP16 24%); under ~35 MB one batch is fastest. Even counts
-// keep both streams equally loaded (EP8: 3 and 6 batches lose to 4).
+// keep both streams equally loaded (EP8: 3 and 5 batches lose to 4 and 6), so an odd count
+// of 3 or more rounds up.
 int forward_batch_count(const Geo& g, const moe_layout_t* lay) {
   if (lay->flags & MOE_FLAG_ONE_BATCH) return 1;
   if (g.payload == MOE_PAYLOAD_FP8_E4M3_B128 && (lay->flags & MOE_FLAG_STAGED_QUANT)) return 1;
   int nb = lay->batches;
-  if (nb <= 0) nb = (int)std::min(16L, std::lround((double)g.P * (g.B + 2.0 * g.H) / 60e6));
+  if (nb <= 0) {
+    nb = (int)std::min(16L, std::lround((double)g.P * (g.B + 2.0 * g.H) / 60e6));
+    if (nb >= 3 && (nb & 1)) ++nb;   // even: both streams end together
+  }
   if (nb > kMaxMicroBatches) nb = kMaxMicroBatches;
   if (nb > g.T) nb = (int)g.T;
   return nb < 1 ? 1 : nb;

@@ -406,7 +406,8 @@ moe_status moe_combine_recv_partial(const moe_dims *dims, const moe_layout_t *la
  * first error. bufs->x, idx, w and out may also be device-accessible host memory.
  * After the layout, the pass runs as nb micro-batches (nb = moe_batches(dims, lay, 0):
  * lay->batches (at most 32 and T), or automatically about one per 60 MB of dispatch and
- * combine rows (N*T*R pairs x (row bytes + 2H)), at most 16 and T;
+ * combine rows (N*T*R pairs x (row bytes + 2H)), rounded up to an even count from 3, at most
+ * 16 and T;
  * one with MOE_FLAG_ONE_BATCH or staged fp8 quantisation). Micro-batch j covers tokens
  * [j*T/nb, (j+1)*T/nb) of every rank and runs dispatch send and recv, the identity expert
  * and the combine on only those tokens' rows (the same kernels, restricted to a token

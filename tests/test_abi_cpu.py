@@ -144,6 +144,7 @@ def test_forward_micro_batch_count_rule(L):
     assert nb(16, 512, 4096, 128, 8) == 16       # 1074 MB: capped
     assert nb(2, 16, 128, 8, 2) == 1             # 32 tokens
     assert nb(8, 64, 7168, 256, 8) == 2          # 117 MB
+    assert nb(8, 160, 7168, 256, 8) == 6         # 294 MB: 5 rounded up to an even count
     assert nb(8, 128, 7168, 256, 8, batches=3) == 3
     assert nb(8, 2, 7168, 256, 8, batches=9) == 2
     assert nb(16, 512, 4096, 128, 8, batches=20) == 20
