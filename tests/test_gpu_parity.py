@@ -813,3 +813,24 @@ def test_fuzz_shapes_and_flags(orc, wl, flags):
     inp = workloads.make_inputs(wl)
     _, res = run_gpu(wl, inp, flags=flags)
     compare_all(orc, wl, inp, res, push=bool(flags & 8))
+
+
+def _fuzz_batch_cases(n, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    for wl, flags in _fuzz_cases(n, seed):
+        mode = str(rng.choice(["forward", "phases"]))
+        batches = int(rng.choice([2, 3, 5, 7]))
+        out.append((wl.replace(name=wl.name.replace("fuzz", f"fuzzb-{mode}{batches}-")), flags, mode, batches))
+    return out
+
+
+@pytest.mark.parametrize("wl,flags,mode,batches", _fuzz_batch_cases(80, 37),
+                         ids=lambda v: v.name if hasattr(v, "name") else str(v))
+def test_fuzz_token_batches(orc, wl, flags, mode, batches):
+    """The fuzz shapes and launch options again, with the pass split into 2-7 token batches
+    (moe_forward's micro-batches or the moe_dispatch / moe_combine phases, fp8 quantised in
+    the pack): every buffer bit for bit against the oracle."""
+    inp = workloads.make_inputs(wl)
+    _, res = run_gpu(wl, inp, flags=flags, batches=batches, **{mode: True})
+    compare_all(orc, wl, inp, res, push=bool(flags & 8), fused_quant=True)
