@@ -834,3 +834,34 @@ def test_fuzz_token_batches(orc, wl, flags, mode, batches):
     inp = workloads.make_inputs(wl)
     _, res = run_gpu(wl, inp, flags=flags, batches=batches, **{mode: True})
     compare_all(orc, wl, inp, res, push=bool(flags & 8), fused_quant=True)
+
+
+def _fuzz_host_cases(n, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    for wl, flags in _fuzz_cases(n, seed):
+        if wl.T == 0:
+            continue
+        nb = int(rng.choice([0, 2, 3, 6]))
+        out.append((wl.replace(name=wl.name.replace("fuzz", f"fuzzh{nb}-")), flags & ~0x2, nb))
+    return out
+
+
+@pytest.mark.parametrize("wl,flags,nb", _fuzz_host_cases(40, 41),
+                         ids=lambda v: v.name if hasattr(v, "name") else str(v))
+def test_fuzz_host_pipeline(orc, wl, flags, nb):
+    """Random shapes through moe_forward_host's copy-engine pipeline (automatic, 2, 3 or 6
+    token batches; each mover, direct push): the host output bit for bit the oracle's."""
+    from combine_routing_count_gb300 import MoeEP
+    inp = workloads.make_inputs(wl)
+    ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, payload=wl.payload, alias_buffers=(wl.payload == "bf16"),
+               flags=flags, batches=nb)
+    h_x, h_idx, h_w, h_out = _host_tensors(inp, wl)
+    x = torch.empty_like(h_x, device="cuda")
+    idx = torch.empty_like(h_idx, device="cuda")
+    w = torch.empty_like(h_w, device="cuda")
+    h_out.view(torch.int16).fill_(-1)
+    ep.forward_host(h_x, h_idx, h_w, h_out, x, idx, w)
+    ep.status()
+    o = orc.forward(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, wl.payload, inp["x"], inp["idx"], inp["w"])
+    np.testing.assert_array_equal(u16(h_out), o["out"])
