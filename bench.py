@@ -8,9 +8,17 @@ per-peer write back) -> combine recv (fp32 weighted sum -> bf16). The bf16 step 
 moe_forward call, which runs the pass in the library's token micro-batches; the fp8 step
 calls the layout, moe_dispatch, the identity expert and moe_combine (in token batches) so
 that the expert can be timed apart and left out. The same step in one batch is reported
-beside it (`one_batch`), as are the per-kernel times of whole-pass launches (roofline).
+beside it (`one_batch`), as are the per-kernel times of whole-pass launches (roofline),
+both with L2 carried over from kernel to kernel as in the step and cold (L2 evicted before
+each kernel).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1] [--impl reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl reference]
+
+With no --config the JSON line's top level is the largest workload (EP16, T=512, H=4096,
+every token routed to rank 0's experts: 5.5 GB of algorithmic bytes per step) and
+`per_config` carries the other three full-size workloads measured the same way in the same
+run (EP8 bf16, EP32 zipf bf16, EP64 fp8), each checked against the CPU oracle; --config C
+measures workload C alone.
 
 Prints one JSON line (rank 0). `value` is tokens/s over all GPUs: (N*T tokens per
 simulated group) x (GPUs) / (step time, max over ranks), timed with CUDA events on the
@@ -23,6 +31,7 @@ from __future__ import annotations
 
 import argparse
 import ctypes
+import gc
 import hashlib
 import json
 import os
@@ -43,16 +52,22 @@ METRIC = "dispatch+combine tokens/s and achieved HBM GB/s (% of GB300 peak), 1 G
 KERNELS = ["route_count", "layout_maps", "quant_fp8", "pack", "scatter", "unpack", "expert",
            "combine_pack", "combine_scatter", "combine_reduce", "route_scan", "pack_push", "combine_push",
            "combine_partial", "combine_sum", "dispatch_split", "quant_pack", "dispatch_dedicated"]
+HEADLINE_CONFIG = 4          # the largest workload: the line's top level
+OTHER_CONFIGS = (1, 2, 3)    # measured in the same run, reported under per_config
+L2_NOTE = "flushed before every timed step (write of 2x L2, then read of 2x L2)"
 
 
 def parse_args(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=200)
-    p.add_argument("--warmup", type=int, default=10)
-    p.add_argument("--config", type=int, default=1, help="workload index (1: EP8 T128 H7168 E256 R8 bf16)")
-    p.add_argument("--shape", default="", help="custom workload N,T,H,E,R[,payload[,cap]] (uniform routing, "
-                   "seed 11) instead of --config, e.g. for profiling a smaller footprint")
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--config", type=int, default=None,
+                   help="measure this workload alone (default: workload 4 at the top level and 1, 2, 3 "
+                        "under per_config)")
+    p.add_argument("--shape", default="", help="custom workload N,T,H,E,R[,payload[,cap[,routing]]] (seed 11; "
+                   "routing uniform, zipf or skew0, default uniform) instead of --config, e.g. for profiling "
+                   "a smaller footprint")
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--mover", choices=["auto", "tma", "ldg"], default="auto")
     p.add_argument("--tma-stages", type=int, default=0)
@@ -65,7 +80,14 @@ def parse_args(argv=None):
     p.add_argument("--one-batch", action="store_true",
                    help="run moe_forward (and the host pass) as one token batch instead of micro-batches")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work for the oracle baseline")
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="CPU work for the oracle baseline of the top-level workload (single thread, then "
+                        "all cores)")
+    p.add_argument("--other-cpu-seconds", type=float, default=3.0,
+                   help="CPU work for the single-thread oracle baseline of each per_config workload")
+    p.add_argument("--profile-step", action="store_true",
+                   help="run only W + K one-batch steps of the workload (L2 flushed before each) and print a "
+                        "short summary: the command the ncu captures in profiles/ profile")
     return p.parse_args(argv)
 
 
@@ -73,13 +95,14 @@ def parse_args(argv=None):
 
 def workload_of(args) -> workloads.Workload:
     if not args.shape:
-        return workloads.config(args.config)
+        return workloads.config(HEADLINE_CONFIG if args.config is None else args.config)
     f = args.shape.split(",")
     N, T, H, E, R = (int(v) for v in f[:5])
     payload = f[5] if len(f) > 5 else "bf16"
     cap = int(f[6]) if len(f) > 6 else 0
-    return workloads.Workload(f"custom-N{N}-T{T}-H{H}-E{E}-R{R}-{payload}-cap{cap}", N, T, H, E, R, payload,
-                              "uniform", 11, cap=cap)
+    routing = f[7] if len(f) > 7 else "uniform"
+    return workloads.Workload(f"custom-N{N}-T{T}-H{H}-E{E}-R{R}-{payload}-cap{cap}-{routing}", N, T, H, E, R,
+                              payload, routing, 11, cap=cap)
 
 
 def dist_env():
@@ -217,22 +240,35 @@ def kernel_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str, workload: str, mode: str = "cold"):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on these sources:
-    mode "cold" (ncu's default cache control, L2 flushed before the kernel) or "warm_l2"
-    (L2 carried over from the previous kernel, as in the step)."""
+def dram_table(workload: str):
+    """The committed ncu DRAM capture for this workload (profiles/ncu_traffic.json), if it was
+    taken on these kernel sources: per kernel the DRAM bytes of one whole-pass launch on a
+    smaller case of the same shape family ('cold': L2 flushed before the kernel; 'warm_l2': L2
+    carried over from the previous kernel, as in the step) and the pairs of that case."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(path):
         return None
     d = json.load(open(path))
     if d.get("source_sha") != kernel_source_sha():
         return None
-    return d.get("workloads", {}).get(workload, {}).get(mode, {}).get(kernel)
+    return d.get("workloads", {}).get(workload)
+
+
+def scaled_dram(table, mode: str, kernel: str, pairs: int):
+    """DRAM bytes of one whole-pass launch of `kernel` at `pairs` routed pairs, scaled from the
+    capture by the pairs processed (every data kernel's traffic is per pair or per token, and
+    the captured case has the same R, H and payload); None without a capture."""
+    if not table:
+        return None
+    v = table.get(mode, {}).get(kernel)
+    if v is None or not table.get("pairs"):
+        return None
+    return int(round(v * pairs / table["pairs"]))
 
 
 # ---------------------------------------------------------------------------- CPU oracle baseline
 
-def cpu_baseline(wl, inp, seconds: float) -> dict:
+def cpu_baseline(wl, inp, seconds: float, all_cores: bool = True) -> dict:
     import oracle
     b = oracle.alloc_step(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, wl.payload)
     oracle.run_step(b, inp["x"], inp["idx"], inp["w"])   # first touch of the buffers, untimed
@@ -243,11 +279,13 @@ def cpu_baseline(wl, inp, seconds: float) -> dict:
         oracle.run_step(b, inp["x"], inp["idx"], inp["w"])
         times.append(time.perf_counter() - t0)
     med = statistics.median(times)
-    return {"value": wl.N * wl.T / med, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{len(times)} whole steps of {wl.name} (all {wl.N} simulated ranks), median "
-                      f"{med * 1e3:.1f} ms, single-threaded C",
-            "all_cores": cpu_baseline_all_cores(wl, inp, seconds, b),
-            "out": b["out"]}
+    out = {"value": wl.N * wl.T / med, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+           "sample": f"{len(times)} whole steps of {wl.name} (all {wl.N} simulated ranks), median "
+                     f"{med * 1e3:.1f} ms, single-threaded C"}
+    if all_cores:
+        out["all_cores"] = cpu_baseline_all_cores(wl, inp, seconds, b)
+    out["out"] = b["out"]
+    return out
 
 
 def step_resident_bytes(b: dict) -> int:
@@ -300,16 +338,18 @@ def cpu_baseline_all_cores(wl, inp, seconds: float, b0: dict) -> dict:
 
 # ---------------------------------------------------------------------------- our arm
 
-def run_ours(args):
-    import torch
-    from combine_routing_count_gb300 import KERNEL_NAMES, MoeEP, MoeProf, build, lib
-    build.build()
-    ws, rank, local = dist_env()
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    dist = dist_init("nccl")
+def _kernel_entry(ab: dict, name: str, ts: list, peak: float, K: int) -> dict:
+    us = statistics.fmean(ts) * 1e3
+    gbs = ab[name] / (us * 1e-6) / 1e9
+    return {"us": round(us, 2), "us_median": round(statistics.median(ts) * 1e3, 2),
+            "launches_per_step": len(ts) / K, "bytes": ab[name], "gbs": round(gbs, 1), "frac": round(gbs / peak, 3)}
 
-    wl = workload_of(args)
+
+def measure(wl, args, dist, device, peak: float, peak_kind: str, cpu_seconds: float, all_cores: bool) -> dict:
+    """Times one workload in every mode (see the module docstring) and returns its JSON object."""
+    import torch
+    from combine_routing_count_gb300 import KERNEL_NAMES, MoeEP, MoeProf, lib
+    ws, rank, local = dist_env()
     inp = workloads.make_inputs(wl)
     ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, wl.payload, alias_buffers=(wl.payload == "bf16"),
                flags={"auto": 0, "ldg": 1, "tma": 4}[args.mover] | (2 if args.no_pdl else 0) |
@@ -331,6 +371,7 @@ def run_ours(args):
         torch.sum(flush_r, dim=0, out=flush_sum)
 
     fp8 = wl.payload == "fp8"
+    K = args.steps
 
     def step():
         ep.forward(x, idx, w)
@@ -362,6 +403,15 @@ def run_ours(args):
         ep.combine(w)
         e3.record(stream)
 
+    if args.profile_step:
+        # Only the one-batch pass (whole-pass launches), for ncu: W + K steps, L2 flushed before each.
+        ep.layout.flags |= 0x40
+        for _ in range(args.warmup + K):
+            flush_l2()
+            step()
+        code, bits = ep.status()
+        return {"profile_step": wl.name, "steps": args.warmup + K, "status": code}
+
     for _ in range(args.warmup):
         flush_l2()
         step()
@@ -373,7 +423,6 @@ def run_ours(args):
     Pk = int((lay["slot"] >= 0).sum().item())
 
     # per-step, per-kernel events through the library's profiling hook
-    K = args.steps
     profs = []
     for _ in range(K):
         pr = MoeProf()
@@ -388,6 +437,7 @@ def run_ours(args):
 
     vis = [v.strip() for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
     sampler = ClockSampler(vis[local] if local < len(vis) else local)
+
     def step_partial():
         ep.layout_step(idx)
         if fp8:
@@ -422,11 +472,13 @@ def run_ours(args):
         ep.combine_send()
         ep.combine_recv(w)
 
-    def kernel_region(step=step):
+    def kernel_region(step=step, cold=False):
         """Timed region: per-kernel CUDA events (the library records one pair around each of
         its launches on this stream) give each kernel's duration for the roofline. The pass
         runs as one batch here (MOE_FLAG_ONE_BATCH), so every kernel is its whole-pass launch
-        and no two of them overlap; the step region below times the default micro-batches."""
+        and no two of them overlap; the step region below times the default micro-batches.
+        With cold, the library reads a 2x-L2 buffer before each bracketed launch, so every
+        kernel starts with nothing of the pass in L2 (the profiling hook's flush option)."""
         barrier(dist, device)
         torch.cuda.synchronize()
         flags0 = ep.layout.flags
@@ -435,6 +487,8 @@ def run_ours(args):
             flush_l2()
             pr, _ = profs[i]
             pr.n = 0
+            pr.flush = flush_r.data_ptr() if cold else None
+            pr.flush_bytes = flush_r.numel() * 4 if cold else 0
             ep.layout.prof = ctypes.pointer(pr)
             step()
         torch.cuda.synchronize()
@@ -485,9 +539,9 @@ def run_ours(args):
     step_batches = int(lib().moe_batches(ctypes.byref(ep.dims), ctypes.byref(ep.layout), 2 if fp8 else 0))
     sampler.start()
     per_kernel = kernel_region()
+    per_kernel_cold = kernel_region(cold=True)
     mean_ms, expert_ms, launches = step_region()
     median_ms = step_region.median_ms
-    clocks = sampler.stop()
     # the same step in one token batch (MOE_FLAG_ONE_BATCH), reported beside the default
     flags0 = ep.layout.flags
     ep.layout.flags = flags0 | 0x40
@@ -498,20 +552,25 @@ def run_ours(args):
     tokens = wl.N * wl.T * ws
     value = tokens / (mean_ms_all * 1e-3)
 
-    peak, peak_kind = measured_peak()
     ab = algorithmic_bytes(wl, P, Pk)
+    table = dram_table(wl.name)
     kernels = {}
     for name, ts in per_kernel.items():
         if name == "expert":
             continue  # the identity expert stands in for the grouped GEMM; reported separately
-        us = statistics.fmean(ts) * 1e3 / 1.0
-        launches_per_step = len(ts) / K
-        gbs = ab[name] / (us * 1e-6) / 1e9
-        kernels[name] = {"us": round(us, 2), "us_median": round(statistics.median(ts) * 1e3, 2),
-                         "launches_per_step": launches_per_step, "bytes": ab[name],
-                         "gbs": round(gbs, 1), "frac": round(gbs / peak, 3)}
+        kernels[name] = _kernel_entry(ab, name, ts, peak, K)
+        tc = per_kernel_cold.get(name)
+        if tc:
+            us_c = statistics.fmean(tc) * 1e3
+            kernels[name]["us_cold"] = round(us_c, 2)
+            kernels[name]["frac_cold"] = round(ab[name] / (us_c * 1e-6) / 1e9 / peak, 3)
+            db = scaled_dram(table, "cold", name, P)
+            kernels[name]["dram_bytes"] = db
+            kernels[name]["dram_frac"] = None if db is None else round(db / (us_c * 1e-6) / 1e9 / peak, 3)
     dom = max(kernels, key=lambda k: kernels[k]["us"] * kernels[k]["launches_per_step"])
     step_bytes = sum(ab[k] * kernels[k]["launches_per_step"] for k in kernels)
+    warm_pass = [scaled_dram(table, "warm_l2", k, P) for k in kernels]
+    dram_step = None if (not warm_pass or any(v is None for v in warm_pass)) else sum(warm_pass)
 
     # The same step in direct-push mode (the pack writes into the owners' receive rows and
     # the combine send into the sources' rows, fusing away both per-peer write steps).
@@ -526,9 +585,8 @@ def run_ours(args):
     for name, ts in pk_push.items():
         if name == "expert":
             continue
-        us = statistics.fmean(ts) * 1e3
-        push_kernels[name] = {"us": round(us, 2), "gbs": round(ab[name] / (us * 1e-6) / 1e9, 1),
-                              "frac": round(ab[name] / (us * 1e-6) / 1e9 / peak, 3)}
+        e = _kernel_entry(ab, name, ts, peak, K)
+        push_kernels[name] = {k: e[k] for k in ("us", "gbs", "frac")}
     push_bytes = sum(ab[k] for k in push_kernels)
     push_ms_all = max_over_ranks(push_ms, dist, device)
 
@@ -548,11 +606,9 @@ def run_ours(args):
         part_ms -= expert_ms
     part_kernels = {}
     for name, ts in pk_part.items():
-        if name == "expert":
-            continue
-        us = statistics.fmean(ts) * 1e3
-        part_kernels[name] = {"us": round(us, 2), "gbs": round(ab[name] / (us * 1e-6) / 1e9, 1),
-                              "frac": round(ab[name] / (us * 1e-6) / 1e9 / peak, 3)}
+        if name.startswith("combine_p") or name == "combine_sum":
+            e = _kernel_entry(ab, name, ts, peak, K)
+            part_kernels[name] = {k: e[k] for k in ("us", "gbs", "frac")}
     part_ms_all = max_over_ranks(part_ms, dist, device)
 
     # The direct-push step with dispatch as one split-phase launch: every CTA pushes its
@@ -568,11 +624,9 @@ def run_ours(args):
         sp_ms -= expert_ms
     sp_kernels = {}
     for name, ts in pk_sp.items():
-        if name == "expert":
-            continue
-        us = statistics.fmean(ts) * 1e3
-        sp_kernels[name] = {"us": round(us, 2), "gbs": round(ab[name] / (us * 1e-6) / 1e9, 1),
-                            "frac": round(ab[name] / (us * 1e-6) / 1e9 / peak, 3)}
+        if name == "dispatch_split":
+            e = _kernel_entry(ab, name, ts, peak, K)
+            sp_kernels[name] = {k: e[k] for k in ("us", "gbs", "frac")}
     sp_ms_all = max_over_ranks(sp_ms, dist, device)
 
     # Split-phase dispatch with per-sender dedicated space and piggybacked routing counts.
@@ -588,9 +642,8 @@ def run_ours(args):
     ded_kernels = {}
     for name, ts in pk_ded.items():
         if name == "dispatch_dedicated":
-            us = statistics.fmean(ts) * 1e3
-            ded_kernels[name] = {"us": round(us, 2), "gbs": round(ab[name] / (us * 1e-6) / 1e9, 1),
-                                 "frac": round(ab[name] / (us * 1e-6) / 1e9 / peak, 3)}
+            e = _kernel_entry(ab, name, ts, peak, K)
+            ded_kernels[name] = {k: e[k] for k in ("us", "gbs", "frac")}
     ded_ms_all = max_over_ranks(ded_ms, dist, device)
 
     # fp8: the whole pass through moe_forward in its micro-batches, the identity expert
@@ -611,6 +664,7 @@ def run_ours(args):
     h_idx = torch.from_numpy(inp["idx"]).pin_memory()
     h_w = torch.from_numpy(inp["w"]).pin_memory()
     h_out = torch.empty((wl.N, wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
+
     def e2e_region():
         for _ in range(3):
             ep.forward_host(h_x, h_idx, h_w, h_out, x, idx, w)
@@ -636,9 +690,11 @@ def run_ours(args):
     ep.layout.flags = f0 | 0x20
     e2e_mapped_ms, _ = e2e_region()
     ep.layout.flags = f0
+    clocks = sampler.stop()
     h2d = inp["x"].nbytes + inp["idx"].nbytes + inp["w"].nbytes
     d2h = wl.N * wl.T * wl.H * 2
 
+    eff_gbs = step_bytes / (mean_ms * 1e-3) / 1e9
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(mean_ms_all, 4), "ms_per_step_median": round(median_ms, 4),
@@ -646,37 +702,52 @@ def run_ours(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "fp8+bf16" if wl.payload == "fp8" else "bf16",
         "data": "synthetic (seeded; DeepSeek-V3/Kimi-K2-shaped routing, identity experts)",
         "config": {"workload": wl.name, "N_ranks_simulated": wl.N, "T": wl.T, "H": wl.H, "E": wl.E, "R": wl.R,
-                   "payload": wl.payload, "routing": wl.routing, "seed": wl.seed, "mover": args.mover,
-                   "pdl": not args.no_pdl, "fp8_quant": ("staged" if args.staged_quant else "inside the pack") if fp8 else None,
-                   "l2": "flushed before every timed step (write of 2x L2, then read of 2x L2)",
+                   "payload": wl.payload, "routing": wl.routing, "seed": wl.seed, "l2": L2_NOTE},
+        "launch": {"mover": args.mover, "pdl": not args.no_pdl,
+                   "fp8_quant": ("staged" if args.staged_quant else "inside the pack") if fp8 else None,
                    "micro_batches": step_batches,
                    "parallelism": f"{ws} independent replica(s) of the {wl.N}-rank group"},
-        "hbm_gbs": round(step_bytes / (mean_ms * 1e-3) / 1e9, 1),
-        "hbm_frac": round(step_bytes / (mean_ms * 1e-3) / 1e9 / peak, 3),
-        "hbm_note": "step-level algorithmic bytes / step time: above 1.0 because consecutive moves read "
-                    "part of their input from L2 (alternating unit order, token batches); the per-kernel "
-                    "roofline below is of whole-pass launches",
+        "effective_gbs": round(eff_gbs, 1),
+        "effective_frac": round(eff_gbs / peak, 3),
+        "effective_note": "step-level algorithmic bytes / step time: an effective rate, not HBM throughput; it "
+                          "exceeds the copy bandwidth because consecutive moves read part of their input from "
+                          "L2 (alternating unit order, token batches). HBM figures: dram_* and each kernel's "
+                          "dram_frac",
+        "dram_bytes_per_step": dram_step,
+        "dram_gbs_one_batch": None if dram_step is None else round(dram_step / (one_ms * 1e-3) / 1e9, 1),
+        "dram_note": "DRAM bytes of one whole pass in one batch (sum over its kernels, L2 carried over from "
+                     "kernel to kernel; ncu on a smaller case of the same shape, scaled by pairs: "
+                     "profiles/ncu_traffic.json) / the one-batch step time; the micro-batched step keeps "
+                     "more rows in L2, so it moves at most these bytes",
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["gbs"], "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": kernels[dom]["frac"],
-                     "bytes_per_launch": ab[dom], "traffic": ncu_traffic(dom, wl.name),
-                     "traffic_warm_l2": ncu_traffic(dom, wl.name, "warm_l2"),
-                     "launch": "whole-pass launch, timed in the per-kernel region (one batch)"},
+                     "achieved_cold": (round(ab[dom] / (kernels[dom]["us_cold"] * 1e-6) / 1e9, 1)
+                                       if "us_cold" in kernels[dom] else None),
+                     "frac_cold": kernels[dom].get("frac_cold"),
+                     "dram_frac": kernels[dom].get("dram_frac"),
+                     "bytes_per_launch": ab[dom],
+                     "traffic": scaled_dram(table, "cold", dom, P),
+                     "traffic_warm_l2": scaled_dram(table, "warm_l2", dom, P),
+                     "traffic_source": (None if not table else
+                                        f"ncu capture of {table.get('shape')} ({table.get('pairs')} pairs), "
+                                        f"scaled by pairs x{P / table['pairs']:.3g}"),
+                     "launch": "whole-pass launch, timed in the per-kernel region (one batch): frac with L2 "
+                               "carried over as in the step, frac_cold with L2 evicted before the kernel, "
+                               "dram_frac = DRAM bytes / cold time"},
         "kernels": kernels,
         "direct_push": {"value": round(tokens / (push_ms_all * 1e-3), 1), "unit": "tokens/s",
                         "ms_per_step": round(push_ms_all, 4),
-                        "hbm_gbs": round(push_bytes / (push_ms * 1e-3) / 1e9, 1),
-                        "hbm_frac": round(push_bytes / (push_ms * 1e-3) / 1e9 / peak, 3),
+                        "effective_gbs": round(push_bytes / (push_ms * 1e-3) / 1e9, 1),
                         "kernels": push_kernels,
                         "note": "same results; pack and combine send write straight into the peers' "
                                 "receive regions, so the two per-peer write kernels are fused away"},
         "sender_side_combine": {"value": round(tokens / (part_ms_all * 1e-3), 1), "unit": "tokens/s",
                                 "ms_per_step": round(part_ms_all, 4), "groups": G, "pairs": Pk,
-                                "kernels": {k: v for k, v in part_kernels.items() if k.startswith("combine")},
+                                "kernels": part_kernels,
                                 "note": "combine sums each token's experts per destination rank on the "
                                         "expert side (bf16 partial rows), then over ranks on the source"},
         "split_phase_dispatch": {"value": round(tokens / (sp_ms_all * 1e-3), 1), "unit": "tokens/s",
-                                 "ms_per_step": round(sp_ms_all, 4),
-                                 "kernels": {k: v for k, v in sp_kernels.items() if k == "dispatch_split"},
+                                 "ms_per_step": round(sp_ms_all, 4), "kernels": sp_kernels,
                                  "note": "direct-push step whose dispatch is one cooperative launch: "
                                          "push rows, signal per (destination, source) slice, wait "
                                          "(bounded), shuffle into the grouped rows"},
@@ -713,10 +784,55 @@ def run_ours(args):
         "clocks": clocks,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        cb = cpu_baseline(wl, inp, args.cpu_seconds)
+        cb = cpu_baseline(wl, inp, cpu_seconds, all_cores=all_cores)
         gpu_out = ep.out.cpu().view(torch.int16).numpy().view(np.uint16)
         out["parity"] = {"out_bit_exact_vs_oracle": bool(np.array_equal(gpu_out, cb.pop("out")))}
         out["cpu_baseline"] = cb
+    return out
+
+
+def compact(r: dict) -> dict:
+    """A per_config entry: the workload's headline figures, its roofline, per-kernel table,
+    end-to-end figure, CPU baseline and parity, without the long notes."""
+    keep = ("value", "unit", "ms_per_step", "ms_per_step_median", "dtype", "config", "launch", "effective_gbs",
+            "effective_frac", "dram_bytes_per_step", "dram_gbs_one_batch", "roofline", "kernels", "parity",
+            "cpu_baseline", "gpu_launches", "clocks")
+    c = {k: r[k] for k in keep if k in r}
+    c["roofline"] = {k: v for k, v in r["roofline"].items() if k != "launch"}
+    c["e2e"] = {k: r["e2e"][k] for k in ("value", "unit", "ms_per_step", "h2d_bytes_per_step",
+                                         "d2h_bytes_per_step", "batches", "out_equals_device_path")}
+    for k in ("one_batch", "direct_push", "sender_side_combine", "split_phase_dispatch", "split_phase_dedicated",
+              "forward_with_expert", "identity_expert"):
+        if r.get(k) is not None:
+            c[k] = {kk: vv for kk, vv in r[k].items() if kk not in ("note", "path")}
+    return c
+
+
+def run_ours(args):
+    import torch
+    from combine_routing_count_gb300 import build
+    build.build()
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = dist_init("nccl")
+    peak, peak_kind = measured_peak()
+
+    wl = workload_of(args)
+    if args.profile_step:
+        r = measure(wl, args, dist, device, peak, peak_kind, 0.0, False)
+        if rank == 0:
+            print(json.dumps(r), flush=True)
+        return
+    out = measure(wl, args, dist, device, peak, peak_kind, args.cpu_seconds, True)
+    if args.config is None and not args.shape:
+        out["per_config"] = {}
+        for cfg in OTHER_CONFIGS:
+            gc.collect()
+            torch.cuda.empty_cache()
+            wc = workloads.config(cfg)
+            out["per_config"][wc.name] = compact(
+                measure(wc, args, dist, device, peak, peak_kind, args.other_cpu_seconds, False))
     if dist is not None:
         dist.destroy_process_group()
     if rank == 0:

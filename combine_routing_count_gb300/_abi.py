@@ -41,7 +41,8 @@ class MoeDims(ctypes.Structure):
 
 
 class MoeProf(ctypes.Structure):
-    _fields_ = [("events", c_void_p * (2 * MOE_PROF_MAX)), ("kernel", c_int32 * MOE_PROF_MAX), ("n", c_int32)]
+    _fields_ = [("events", c_void_p * (2 * MOE_PROF_MAX)), ("kernel", c_int32 * MOE_PROF_MAX), ("n", c_int32),
+                ("flush", c_void_p), ("flush_bytes", ctypes.c_size_t)]
 
 
 class MoeLayout(ctypes.Structure):

@@ -17,6 +17,36 @@ std::atomic<uint64_t> g_launches{0};
 
 namespace {
 
+// Reads n16 16-byte words so that whatever L2 held before is evicted (dirty lines are
+// written back during this kernel). The xor of everything read decides a store that never
+// happens in practice, which keeps the loads from being dropped.
+__global__ void __launch_bounds__(256) k_l2_flush(uint4* buf, int64_t n16) {
+  uint4 acc = make_uint4(0, 0, 0, 0);
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) {
+    const uint4 v = buf[i];   // plain load: normal L2 allocation, so it displaces what was cached
+    acc.x ^= v.x;
+    acc.y ^= v.y;
+    acc.z ^= v.z;
+    acc.w ^= v.w;
+  }
+  if (acc.x == 0x6d6f6531u && acc.y == 0x6c326675u && acc.z == 0x73686f6eu && acc.w == 0x21212121u) buf[0] = acc;
+}
+
+}  // namespace
+
+cudaError_t launch_l2_flush(const moe_prof_t* prof, cudaStream_t stream) {
+  if (!prof->flush || prof->flush_bytes < 16 || (prof->flush_bytes & 15u)) return cudaSuccess;
+  const int64_t n16 = (int64_t)(prof->flush_bytes / 16);
+  int64_t blocks = (n16 + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  k_l2_flush<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<uint4*>(prof->flush), n16);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaGetLastError();
+}
+
+namespace {
+
 constexpr int kMaxDevices = 64;
 constexpr int kMaxHostBatches = 16;
 constexpr int kMaxMicroBatches = 32;
@@ -110,6 +140,8 @@ bool pass_buffers_ok(const moe_buffers_t* b, uint32_t flags, bool fp8, bool with
   return ok(b->recv) && ok(b->expert_x) && ok(b->expert_y) && ok(b->crecv) && (!fp8 || ok(b->expert_scale));
 }
 
+}  // namespace
+
 moe_status make_geo(const moe_dims* d, Geo& g) {
   if (!d) return MOE_ERR_INVALID_ARG;
   if (d->N < 1 || d->T < 0 || d->E < 1 || d->R < 1 || d->cap < 0 || d->H < 8) return MOE_ERR_INVALID_ARG;
@@ -177,6 +209,8 @@ bool layout_ok(const moe_layout_t* l) {
     if (!p) return false;
   return true;
 }
+
+namespace {
 
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 

@@ -26,6 +26,9 @@ struct Ctx {
 
 extern std::atomic<uint64_t> g_launches;
 
+// Reads prof->flush (prof->flush_bytes) on `stream`: the cold-cache option of moe_prof_t.
+cudaError_t launch_l2_flush(const moe_prof_t* prof, cudaStream_t stream);
+
 // Launches `kernel` on c.stream, with programmatic stream serialization unless
 // MOE_FLAG_NO_PDL is set (every kernel calls pdl_wait() before touching memory).
 template <typename... KArgs, typename... Args>
@@ -50,6 +53,7 @@ struct LaunchScope {
   int slot = -1;
   LaunchScope(Ctx& ctx, moe_kernel_id id) : c(ctx) {
     if (c.prof && c.prof->n < MOE_PROF_MAX) {
+      launch_l2_flush(c.prof, c.stream);
       slot = c.prof->n++;
       c.prof->kernel[slot] = id;
       cudaEventRecord(static_cast<cudaEvent_t>(c.prof->events[2 * slot]), c.stream);
@@ -75,6 +79,11 @@ inline cudaError_t ensure_dyn_smem(K kernel, int device, size_t bytes, std::atom
   }
   return cudaSuccess;
 }
+
+// api.cu: argument checks shared by every entry point.
+moe_status make_geo(const moe_dims* d, Geo& g);                       // dims -> geometry, or INVALID_ARG
+moe_status make_ctx(const moe_layout_t* lay, void* stream, Ctx& c);   // launch context (device attributes cached)
+bool layout_ok(const moe_layout_t* l);                                // every layout array present
 
 // layout.cu
 cudaError_t launch_layout(const Geo& g, const int32_t* idx, const moe_layout_t* lay, Ctx& c);

@@ -25,7 +25,11 @@ constexpr size_t kNoAllocSendBytes = 64ull << 20;
 
 static __device__ __align__(256) uint8_t g_noalloc_send[kNoAllocSendBytes];
 
-// Device address of g_noalloc_send, looked up once per device with that device current.
+// Device address of g_noalloc_send, looked up once per device with that device current (the
+// set-up step of the first call on each device). The address belongs to the library's module
+// as loaded in the device's primary context: after cudaDeviceReset, or when a caller makes
+// another context of the device current, it is no longer valid, and this entry point must
+// not be used there.
 void* g_send_addr[64];
 std::mutex g_send_mu;
 
@@ -50,44 +54,20 @@ using namespace moe;
 
 extern "C" moe_status moe_dispatch_send_noalloc(const moe_dims* dims, const moe_layout_t* lay, const void* d_x,
                                                 void* d_recv, void* stream) {
-  if (moe_check_dims(dims) != MOE_OK || !lay || !lay->gsend || !lay->grecv || !lay->status)
-    return MOE_ERR_INVALID_ARG;
-  const int64_t N = dims->N, T = dims->T, R = dims->R, E = dims->E, H = dims->H, L = E / N;
-  if (N * T == 0) return MOE_OK;
-  if (!d_x || !d_recv || !aligned16(d_x) || !aligned16(d_recv)) return MOE_ERR_INVALID_ARG;
-  const int64_t B = (int64_t)moe_row_bytes(dims);
-  if ((size_t)(N * T * R * B) > kNoAllocSendBytes) return MOE_ERR_INVALID_ARG;  // beyond the static buffer
-
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
-  void* send = nullptr;
-  if (send_scratch(dev, &send) != cudaSuccess) return MOE_ERR_CUDA;
-  Ctx c;
-  c.device = dev;
-  c.stream = static_cast<cudaStream_t>(stream);
-  c.prof = lay->prof;
-  c.flags = lay->flags;
-  c.tma_stages = lay->tma_stages;
-  c.ctas_per_sm = lay->ctas_per_sm;
-  c.status = lay->status;
-  if (cudaDeviceGetAttribute(&c.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&c.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&c.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&c.l2_bytes, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
-    return MOE_ERR_CUDA;
   Geo g;
-  g.N = (int)N;
-  g.T = (int)T;
-  g.H = (int)H;
-  g.E = (int)E;
-  g.R = (int)R;
-  g.L = (int)L;
-  g.cap = moe_capacity(dims);
-  g.payload = dims->payload;
-  g.TR = T * R;
-  g.RB = (int64_t)moe_recv_capacity_rows(dims);
-  g.P = N * T * R;
-  g.B = B;
+  moe_status st = make_geo(dims, g);
+  if (st != MOE_OK) return st;
+  if (!layout_ok(lay)) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)g.N * g.T == 0) return MOE_OK;   // nothing to move
+  if (!d_x || !d_recv || !aligned16(d_x) || !aligned16(d_recv)) return MOE_ERR_INVALID_ARG;
+  if ((size_t)(g.P * g.B) > kNoAllocSendBytes) return MOE_ERR_INVALID_ARG;   // beyond the static buffer
+  Ctx c;
+  if ((st = make_ctx(lay, stream, c)) != MOE_OK) return st;
+  void* send = nullptr;
+  if (send_scratch(c.device, &send) != cudaSuccess) return MOE_ERR_CUDA;
+  // Always pack then scatter through the array (MOE_FLAG_DIRECT_PUSH, which needs no send
+  // buffer, is what moe_dispatch_send offers without one).
+  c.flags &= ~MOE_FLAG_DIRECT_PUSH;
   cudaError_t e = launch_move(kMovePack, g, lay, d_x, send, nullptr, c);
   if (e == cudaSuccess) e = launch_move(kMoveScatter, g, lay, send, d_recv, nullptr, c);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;

@@ -538,8 +538,8 @@ __device__ __forceinline__ void store_bf16x8(uint16_t* p, const float (&acc)[8])
 // Combine receive. Block (token u, column tile); a thread owns 8 bf16 columns (16 bytes).
 // Lane j of each warp loads pair j's send row and weight and shares them by shuffle; the
 // R rows are gathered with up to 8 loads in flight; fp32 products and sums are rounded
-// separately in slot order (packed f32x2 pairs, each lane rounded as the scalar op);
-// dropped or invalid pairs are skipped.
+// separately with scalar __fmul_rn / __fadd_rn, in slot order; dropped or invalid pairs are
+// skipped.
 // RANGED: block x covers token x of the range [t0, t0 + nt) of every rank, rank-major (else
 // token x; t0, nt unused).
 constexpr int kReduceThreads = 128;

@@ -98,12 +98,20 @@ typedef enum {
  * launches is bracketed by cudaEventRecord(events[2n]) and cudaEventRecord(events[2n+1]) on
  * the call's stream, kernel[n] receives its moe_kernel_id and n is incremented, until n
  * reaches MOE_PROF_MAX. The caller creates the events (cudaEvent_t cast to void*) and
- * resets n. */
+ * resets n.
+ * Cold timing: when `flush` is non-NULL (a device buffer of flush_bytes, a multiple of 16
+ * and best at least twice the L2 size), a kernel of the library reads the whole buffer on
+ * the stream before each bracketed launch's first event, so every timed kernel starts with
+ * the previous kernels' rows evicted from L2 (their dirty lines written back during the
+ * read, outside the bracket). The read kernel is not bracketed; it writes at most 16 bytes
+ * at the start of the buffer. flush_bytes below 16 or not a multiple of 16 turns it off. */
 #define MOE_PROF_MAX 32
 typedef struct {
     void *events[2 * MOE_PROF_MAX];
     int32_t kernel[MOE_PROF_MAX];
     int32_t n;
+    void *flush;
+    size_t flush_bytes;
 } moe_prof_t;
 
 /* moe_layout_t.flags */
@@ -281,7 +289,11 @@ moe_status moe_quantize_dispatch_send(const moe_dims *dims, const moe_layout_t *
  * caller buffer. Arguments are those of moe_dispatch_send without d_send.
  *  - Sizes: N*T*R*B must be at most 64 MiB (B = row bytes), else MOE_ERR_INVALID_ARG.
  *  - The first call on a device looks the array's address up (cudaGetSymbolAddress) with
- *    that device current; make that first call before any stream capture.
+ *    that device current; make that first call before any stream capture. The address is
+ *    the one of the device's primary context: do not call this after cudaDeviceReset or with
+ *    another context of the device current.
+ *  - MOE_FLAG_DIRECT_PUSH is ignored: the rows are always packed into the array, then
+ *    scattered (moe_dispatch_send with that flag needs no send buffer at all).
  *  - The array is shared by every call and keeps the last call's rows; calls that overlap
  *    on the GPU (other streams or threads) race on it. Every GPU that loads the library
  *    holds the 64 MiB until the process exits.

@@ -1,20 +1,24 @@
 """GPU parity at the full sizes of the benchmark workloads, in the launch configuration the
-benchmark times (default mover choice, programmatic dependent launch, and direct push).
+benchmark times (default mover choice, programmatic dependent launch, the micro-batched
+moe_forward, and direct push).
 
-The whole output and every layout array are compared bit for bit with the oracle; the
-receive, grouped and combine rows (hundreds of MB) are compared on a seeded sample of rows.
-A second pass runs with the benchmark's aliased buffers (combine reusing the dispatch
-buffers) and compares the output again."""
+Every buffer is compared with the oracle in full, with no sampling: the layout arrays and
+the output on the host; the send, receive, grouped (codes and scales for fp8), dequantised,
+combine-send and combine rows on the device, each used row against the oracle's row
+(uploaded a rank at a time) and every unused row against the poison it was filled with, so
+a stray write anywhere in the hundreds of MB of padding fails. A second pass runs with the
+benchmark's aliased buffers (combine reusing the dispatch buffers) and compares the output
+again."""
 import numpy as np
 import pytest
 import torch
 
 import workloads
-from tests.gpu_util import to_dev, u8, u16
+from tests.gpu_util import POISON, to_dev, u16
 
 pytestmark = pytest.mark.gpu
 
-SAMPLE = 768
+CHUNK = 1 << 28   # bytes of oracle rows uploaded per comparison
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -24,9 +28,76 @@ def _built():
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
 
 
-def _rows(t: torch.Tensor, index: tuple) -> np.ndarray:
-    """Gathers rows t[index] on the device, then copies only those to the host."""
-    return t[tuple(torch.as_tensor(i, device=t.device, dtype=torch.long) for i in index)].cpu()
+def _bytes(t: torch.Tensor) -> torch.Tensor:
+    """The tensor's rows as a [rows, bytes] uint8 view (first dimension kept)."""
+    return t.contiguous().view(torch.uint8).reshape(t.shape[0], -1)
+
+
+def _same_rows(dev: torch.Tensor, host: np.ndarray, what: str):
+    """dev [n, ...] on the GPU equals host [n, ...] byte for byte (uploaded in chunks)."""
+    d = _bytes(dev)
+    h = np.ascontiguousarray(host).view(np.uint8).reshape(d.shape[0], -1)
+    assert d.shape == h.shape, (what, d.shape, h.shape)
+    if d.shape[0] == 0:
+        return
+    step = max(1, CHUNK // max(1, d.shape[1]))
+    for i in range(0, d.shape[0], step):
+        hc = torch.from_numpy(h[i:i + step]).to(d.device)
+        if not torch.equal(d[i:i + step], hc):
+            bad = (d[i:i + step] != hc).any(dim=1).nonzero()[:5, 0].cpu().numpy() + i
+            raise AssertionError(f"{what}: rows {bad.tolist()} differ from the oracle")
+
+
+def _poisoned(dev: torch.Tensor, what: str):
+    """Every byte of dev still holds the poison (no stray write)."""
+    if dev.numel() == 0:
+        return
+    b = dev.contiguous().view(torch.uint8)
+    assert bool((b == POISON).all()), f"{what}: stray write into unused rows"
+
+
+def _check_buffers(ep, o, wl, push: bool):
+    N, L = wl.N, wl.L
+    lay = o["layout"]
+    rtot, cap = lay["rtot"], lay["cap"]
+    nvalid = (lay["pos"] >= 0).reshape(N, -1).sum(axis=1)
+    ecnt = np.minimum(lay["ecnt"], cap)
+    for s in range(N):
+        nv = int(nvalid[s])
+        if push:
+            _poisoned(ep.send[s], "send (direct push must not write it)")
+        else:
+            _same_rows(ep.send[s, :nv], o["send"][s, :nv], f"send rank {s}")
+            _poisoned(ep.send[s, nv:], f"send rank {s}")
+    for d in range(N):
+        n = int(rtot[d])
+        _same_rows(ep.recv[d, :n], o["recv"][d, :n], f"recv rank {d}")
+        _poisoned(ep.recv[d, n:], f"recv rank {d}")
+    for d in range(N):
+        for l in range(L):
+            n = int(ecnt[d, l])
+            if wl.payload == "fp8":
+                _same_rows(ep.expert_x[d, l, :n], o["exq"][d, l, :n], f"expert codes {d}/{l}")
+                _same_rows(ep.expert_scale[d, l, :n], o["exs"][d, l, :n], f"expert scales {d}/{l}")
+                _poisoned(ep.expert_x[d, l, n:], f"expert codes {d}/{l}")
+                _poisoned(ep.expert_scale[d, l, n:], f"expert scales {d}/{l}")
+                _same_rows(ep.expert_y[d, l, :n], o["ey"][d, l, :n], f"dequantised expert rows {d}/{l}")
+            else:
+                _same_rows(ep.expert_x[d, l, :n], o["ex"][d, l, :n], f"grouped rows {d}/{l}")
+                _poisoned(ep.expert_x[d, l, n:], f"grouped rows {d}/{l}")
+    kept = (lay["slot"] >= 0).reshape(N, -1)
+    assert kept.sum() == (lay["pos"] >= 0).sum(), "full-size workloads drop no pair"
+    for d in range(N):
+        n = int(rtot[d])
+        if push:
+            _poisoned(ep.csend[d], "combine send (direct push must not write it)")
+        else:
+            _same_rows(ep.csend[d, :n], o["csend"][d, :n], f"combine send rank {d}")
+            _poisoned(ep.csend[d, n:], f"combine send rank {d}")
+    for s in range(N):
+        nv = int(nvalid[s])
+        _same_rows(ep.crecv[s, :nv], o["crecv"][s, :nv], f"combine rows rank {s}")
+        _poisoned(ep.crecv[s, nv:], f"combine rows rank {s}")
 
 
 @pytest.mark.parametrize("push", [False, True], ids=["scatter", "push"])
@@ -40,6 +111,10 @@ def test_full_size_matches_oracle(orc, cfg, push):
     x, idx, w = to_dev(inp["x"]).view(torch.bfloat16), to_dev(inp["idx"]), to_dev(inp["w"])
 
     ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, wl.payload, flags=8 if push else 0)
+    for t in (ep.send, ep.recv, ep.expert_x, ep.csend, ep.crecv):
+        t.view(torch.uint8).fill_(POISON)
+    if ep.expert_scale is not None:
+        ep.expert_scale.view(torch.uint8).fill_(POISON)
     ep.forward(x, idx, w)
     code, bits = ep.status()
     assert bits == lay_o["status"] and code == 0
@@ -47,34 +122,12 @@ def test_full_size_matches_oracle(orc, cfg, push):
     got = {k: v.cpu().numpy() for k, v in ep.layout_arrays().items()}
     for k in ("cnt", "C", "soff", "roff", "rtot", "ecnt", "eoff", "pos", "rrow", "slot", "slot_src", "recv_src"):
         np.testing.assert_array_equal(got[k], lay_o[k], err_msg=k)
-
-    rng = np.random.default_rng(1000 + cfg)
-    # receive rows: sampled (d, i) with i < rtot[d]
-    rtot = lay_o["rtot"]
-    ds = rng.choice(np.flatnonzero(rtot > 0), SAMPLE)
-    iis = (rng.random(SAMPLE) * rtot[ds]).astype(np.int64)
-    np.testing.assert_array_equal(u8(_rows(ep.recv, (ds, iis))), o["recv"][ds, iis], err_msg="receive rows")
-    # grouped rows: sampled (d, l, j) with j < min(ecnt, cap)
-    ecnt = np.minimum(lay_o["ecnt"], lay_o["cap"]).reshape(-1)
-    es = rng.choice(np.flatnonzero(ecnt > 0), SAMPLE)
-    js = (rng.random(SAMPLE) * ecnt[es]).astype(np.int64)
-    dd, ll = es // wl.L, es % wl.L
-    if wl.payload == "fp8":
-        np.testing.assert_array_equal(u8(_rows(ep.expert_x, (dd, ll, js))), o["exq"][dd, ll, js], err_msg="codes")
-        exs_o = o["exs"].view(np.uint8).reshape(o["exs"].shape[:3] + (-1,))
-        np.testing.assert_array_equal(u8(_rows(ep.expert_scale, (dd, ll, js))), exs_o[dd, ll, js], err_msg="scales")
-    else:
-        np.testing.assert_array_equal(u16(_rows(ep.expert_x, (dd, ll, js))), o["ex"][dd, ll, js], err_msg="grouped rows")
-    # combine rows back at the sources: sampled kept pairs (s, pos)
-    pos, slot = lay_o["pos"].reshape(wl.N, -1), lay_o["slot"].reshape(wl.N, -1)
-    kept = np.argwhere(slot >= 0)
-    pick = kept[rng.integers(0, len(kept), SAMPLE)]
-    ss, pp = pick[:, 0], pos[pick[:, 0], pick[:, 1]]
-    np.testing.assert_array_equal(u16(_rows(ep.crecv, (ss, pp))), o["crecv"][ss, pp], err_msg="combine rows")
+    _check_buffers(ep, o, wl, push)
 
     # the benchmark's buffer reuse: combine writes into the dispatch buffers
     if wl.payload == "bf16":
         del ep
+        torch.cuda.empty_cache()
         ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, wl.payload, alias_buffers=True, flags=8 if push else 0)
         for _ in range(2):
             ep.forward(x, idx, w)

@@ -206,7 +206,7 @@ def test_launch_counter_counts_kernels():
 
 def test_profiling_events_bracket_each_kernel():
     import ctypes
-    from combine_routing_count_gb300 import MoeEP, MoeProf, KERNEL_NAMES
+    from combine_routing_count_gb300 import KERNEL_NAMES, MoeEP, MoeProf, lib
     wl = W("prof", 4, 16, 1024, 16, 4, "fp8", "uniform", 130)
     inp = workloads.make_inputs(wl)
     ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, payload="fp8")
@@ -222,6 +222,22 @@ def test_profiling_events_bracket_each_kernel():
     names = [KERNEL_NAMES[prof.kernel[i]] for i in range(prof.n)]
     assert names == ["route_count", "route_scan", "layout_maps", "quant_pack", "scatter", "unpack",
                      "expert", "combine_pack", "combine_scatter", "combine_reduce"]
+    for i in range(prof.n):
+        assert evs[2 * i].elapsed_time(evs[2 * i + 1]) >= 0.0
+    out0 = ep.out.clone()
+    # cold timing: the library reads a flush buffer before each bracketed launch; same
+    # brackets, one extra launch per kernel, same results
+    flush = torch.ones(1 << 22, dtype=torch.float32, device="cuda")
+    prof.n = 0
+    prof.flush, prof.flush_bytes = flush.data_ptr(), flush.numel() * 4
+    ep.out.zero_()
+    n0 = lib().moe_launch_count()
+    ep.forward(to_dev(inp["x"]).view(torch.bfloat16), to_dev(inp["idx"]), to_dev(inp["w"]))
+    torch.cuda.synchronize()
+    assert [KERNEL_NAMES[prof.kernel[i]] for i in range(prof.n)] == names
+    assert lib().moe_launch_count() - n0 == 2 * len(names)
+    assert torch.equal(ep.out, out0)
+    assert bool((flush == 1.0).all()), "the flush read must leave its buffer as it was"
     for i in range(prof.n):
         assert evs[2 * i].elapsed_time(evs[2 * i + 1]) >= 0.0
 
@@ -862,6 +878,7 @@ def test_fuzz_host_pipeline(orc, wl, flags, nb):
     w = torch.empty_like(h_w, device="cuda")
     h_out.view(torch.int16).fill_(-1)
     ep.forward_host(h_x, h_idx, h_w, h_out, x, idx, w)
-    ep.status()
+    code, bits = ep.status()
     o = orc.forward(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, wl.payload, inp["x"], inp["idx"], inp["w"])
+    assert bits == o["layout"]["status"], (code, bits, o["layout"]["status"])
     np.testing.assert_array_equal(u16(h_out), o["out"])
