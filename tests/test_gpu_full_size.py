@@ -35,11 +35,12 @@ def _bytes(t: torch.Tensor) -> torch.Tensor:
 
 def _same_rows(dev: torch.Tensor, host: np.ndarray, what: str):
     """dev [n, ...] on the GPU equals host [n, ...] byte for byte (uploaded in chunks)."""
+    assert dev.shape[0] == host.shape[0], (what, dev.shape, host.shape)
+    if dev.shape[0] == 0:
+        return
     d = _bytes(dev)
     h = np.ascontiguousarray(host).view(np.uint8).reshape(d.shape[0], -1)
     assert d.shape == h.shape, (what, d.shape, h.shape)
-    if d.shape[0] == 0:
-        return
     step = max(1, CHUNK // max(1, d.shape[1]))
     for i in range(0, d.shape[0], step):
         hc = torch.from_numpy(h[i:i + step]).to(d.device)
