@@ -131,13 +131,13 @@ class MoeEP:
                                 _stream(stream)), "moe_combine")
         return self.out
 
-    def dispatch_split(self, x: torch.Tensor, withhold_slice: int = -1, stream=None):
+    def dispatch_split(self, x: torch.Tensor, withhold_source: int = -1, stream=None):
         """Split-phase dispatch: receive rows and grouped expert rows in one launch.
-        withhold_slice (tests only) names a slice d*N + s whose arrival signals are not sent."""
+        withhold_source (tests only) names a source rank whose arrival signals are not sent."""
         self.x = x
         check(lib().moe_dispatch_split(ctypes.byref(self.dims), ctypes.byref(self.layout), x.data_ptr(),
                                        self.recv.data_ptr(), self.expert_x.data_ptr(), _ptr(self.expert_scale),
-                                       int(withhold_slice), _stream(stream)), "moe_dispatch_split")
+                                       int(withhold_source), _stream(stream)), "moe_dispatch_split")
 
     def dispatch_dedicated(self, x: torch.Tensor, idx: torch.Tensor, K: int, withhold_slice: int = -1, stream=None):
         """Split-phase dispatch with K dedicated rows per (receiver, sender) and the routing

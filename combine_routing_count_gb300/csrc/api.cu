@@ -241,7 +241,7 @@ WsPlan ws_plan(const Geo& g) {
                           P,               // grecv
                           P,               // gslot
                           16,              // status
-                          (size_t)layout_scratch_arrive_offset(g) + N * N + 16};  // scratch: chunk table,
+                          (size_t)(layout_scratch_arrive_offset(g) + split_arrive_words(g)) + 16};  // scratch: chunk table,
                                                                       // counters, token groups, arrivals
   w.total = 0;
   for (int i = 0; i < 17; ++i) {
@@ -598,7 +598,7 @@ moe_status moe_layout_init(const moe_dims* dims, void* d_ws, size_t ws_bytes, mo
   if (cudaMemsetAsync(out->status, 0, 64, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemsetAsync(out->scratch + layout_scratch_done_offset(g), 0, 4 * (size_t)g.N, s) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if (cudaMemsetAsync(out->scratch + layout_scratch_arrive_offset(g), 0, 4 * ((size_t)g.N * g.N + 2), s) !=
+  if (cudaMemsetAsync(out->scratch + layout_scratch_arrive_offset(g), 0, 4 * ((size_t)split_arrive_words(g) + 2), s) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
@@ -666,11 +666,11 @@ moe_status moe_quantize_dispatch_send(const moe_dims* dims, const moe_layout_t* 
 }
 
 moe_status moe_dispatch_split(const moe_dims* dims, const moe_layout_t* lay, const void* d_x, void* d_recv,
-                              void* d_expert_x, float* d_expert_scale, int32_t withhold_slice, void* stream) {
+                              void* d_expert_x, float* d_expert_scale, int32_t withhold_source, void* stream) {
   Geo g;
   moe_status st = make_geo(dims, g);
   if (st != MOE_OK) return st;
-  if (withhold_slice < -1 || withhold_slice >= (int64_t)g.N * g.N) return MOE_ERR_INVALID_ARG;
+  if (withhold_source < -1 || withhold_source >= g.N) return MOE_ERR_INVALID_ARG;
   if ((int64_t)g.N * g.T == 0) return layout_ok(lay) ? MOE_OK : MOE_ERR_INVALID_ARG;  // nothing to move
   const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
   if (!layout_ok(lay) || !d_x || !d_recv || !d_expert_x || !aligned16(d_x) || !aligned16(d_recv) ||
@@ -680,7 +680,7 @@ moe_status moe_dispatch_split(const moe_dims* dims, const moe_layout_t* lay, con
   Ctx c;
   if ((st = make_ctx(lay, stream, c)) != MOE_OK) return st;
   return cuda_status(launch_dispatch_split(g, lay, d_x, d_recv, d_expert_x, fp8 ? d_expert_scale : nullptr,
-                                           withhold_slice, c));
+                                           withhold_source, c));
 }
 
 size_t moe_dedicated_exchange_bytes(const moe_dims* dims) {

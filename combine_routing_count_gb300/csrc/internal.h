@@ -90,7 +90,16 @@ cudaError_t launch_layout(const Geo& g, const int32_t* idx, const moe_layout_t* 
 int layout_chunks(const Geo& g);
 int64_t layout_scratch_done_offset(const Geo& g);  // ints from the scratch start to the counters
 int64_t layout_scratch_tgroups_offset(const Geo& g);  // ... to the per-token group counts
-int64_t layout_scratch_arrive_offset(const Geo& g);   // ... to the split-dispatch counters [N*N + 2]
+int64_t layout_scratch_arrive_offset(const Geo& g);   // ... to the split-dispatch counters (+ 2)
+
+// split.cu
+constexpr int kMaxSplitBatches = 32;   // token batches of the split-phase dispatch
+// Words of the split-dispatch arrival counters: one per (token batch, source rank).
+inline int64_t split_arrive_words(const Geo& g) {
+  const int64_t a = (int64_t)g.N * g.N, b = (int64_t)kMaxSplitBatches * g.N;
+  return a > b ? a : b;
+}
+int split_batches(const Geo& g);
 
 // dedicated.cu
 size_t dedicated_exchange_bytes(const Geo& g);
@@ -98,9 +107,8 @@ cudaError_t launch_dispatch_dedicated(const Geo& g, const moe_layout_t* lay, con
                                       int K, void* ded, void* xchg, void* main, void* ex, float* exs,
                                       int drop_slice, Ctx& c);
 
-// split.cu
 cudaError_t launch_dispatch_split(const Geo& g, const moe_layout_t* lay, const void* x, void* recv, void* ex,
-                                  float* exs, int drop_slice, Ctx& c);
+                                  float* exs, int drop_source, Ctx& c);
 
 // movers.cu: row movement kernels.
 enum MoveKind : int {

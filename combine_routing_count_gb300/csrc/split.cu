@@ -9,17 +9,24 @@
 //
 // On one GPU the two halves cannot be separate kernels that wait on each other (nothing
 // guarantees they run at the same time), so both run in one cooperative launch, whose
-// CTAs are all resident at once:
-//  1. sender work: every (token, column chunk) unit is pushed into the owners' receive
-//     rows (the direct-push pack); after a row chunk lands, the warp release-increments
-//     the arrival counter of its (destination d, source s) slice;
-//  2. receiver work: each (pair, column chunk) unit waits, with an acquire poll bounded
-//     by kSplitWaitNs, until its slice's counter reaches C[s][d] * chunks, then copies the
-//     row chunk into its expert's grouped row (codes and scales apart for fp8).
-// A CTA finishes all its sender units before it takes receiver units, and no sender ever
-// waits, so every wait ends unless a signal is missing; then the status word gets the
-// timeout bit, later waits give up at once, and the unfinished rows are skipped. The
+// CTAs are all resident at once. The tokens are taken in nb batches (tokens
+// [j*T/nb, (j+1)*T/nb) of every rank), and every CTA has sender warps and receiver warps:
+//  - sender warps push the (token, column chunk) units of batch 0, then batch 1, ... into
+//    the owners' receive rows (the direct-push pack); once a warp's units of a batch have
+//    landed (one fence), it signals each unit on the counter of (batch j, source s);
+//  - receiver warps take the (pair, column chunk) units of batch 0, then batch 1, ...; each
+//    waits, with an acquire poll bounded by kSplitWaitNs, until its source's counter for
+//    the batch reaches the batch's token chunks (every row source s pushed in batch j has
+//    landed), then copies the row chunk into its expert's grouped row (codes and scales
+//    apart for fp8).
+// Receivers trail the senders by about a batch, so a batch's receive rows are still in L2
+// when they are read back. Sender warps never wait, so every wait ends unless a signal is
+// missing; then the status word gets the timeout bit, later waits of the call give up at
+// once (by then every push has long landed), and the unfinished rows are skipped. The
 // counters start at zero (moe_layout_init) and the last CTA of each call zeroes them again.
+// The share of sender warps follows the bytes each half moves: a token row is read once and
+// written R times by the senders, and each of its R pairs is read and written once by the
+// receivers, so senders take (R + 1) / (3R + 1) of the warps (3 of 8 at R = 8).
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -29,23 +36,25 @@ namespace {
 
 constexpr uint64_t kSplitWaitNs = 1000000000ull;   // 1 s
 constexpr int kSplitThreads = 256;
+constexpr int kSplitWarps = kSplitThreads / 32;
+constexpr int64_t kSplitBatchBytes = 16ll << 20;    // pushed rows per token batch (about L2 / 8)
 
 struct SplitArgs {
   const uint8_t* x;     // [N][T][B] token rows
   uint8_t* recv;        // [N][RB][B]
   uint8_t* ex;          // grouped rows: [N][L][cap][B] (bf16) or codes [N][L][cap][H] (fp8)
   uint8_t* exs;         // fp8 scales [N][L][cap][H/128]
-  const int32_t* gsend;
   const int32_t* grecv;
   const int32_t* gslot;
-  const int32_t* C;     // [N][N]: rows s sends to d
-  uint32_t* arrive;     // [N][N]: arrive[d*N + s], row chunks of slice (d, s) landed
+  uint32_t* arrive;     // [nb][N]: arrive[j*N + s], token chunks of source s in batch j landed
   uint32_t* done;       // CTAs finished (the last one resets arrive[], done and abort)
   uint32_t* abort;      // set by the first wait that times out in this call
   int32_t* status;
   int chunks;           // column chunks per row
   int64_t chunk_bytes;
-  int drop_slice;       // failure injection: the slice d*N+s whose signals are withheld, or -1
+  int nb;               // token batches
+  int senders;          // sender warps per CTA (the rest receive)
+  int drop_source;      // failure injection: the source rank whose signals are withheld, or -1
 };
 
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
@@ -68,7 +77,7 @@ __device__ __forceinline__ bool wait_arrival(const uint32_t* ctr, uint32_t targe
       set_status(status, kBitTimeout);
       return false;
     }
-    __nanosleep(256);
+    __nanosleep(128);
   }
 }
 
@@ -101,88 +110,108 @@ __device__ __forceinline__ uint32_t ldv_l2<uint32_t>(const uint8_t* p) {
 __device__ __forceinline__ void stv(uint8_t* p, const uint4& v) { st16(p, v); }
 __device__ __forceinline__ void stv(uint8_t* p, const uint32_t& v) { *reinterpret_cast<uint32_t*>(p) = v; }
 
+__device__ __forceinline__ int batch_lo(const Geo& g, int nb, int j) { return (int)((int64_t)j * g.T / nb); }
+
 template <bool FP8, typename V>
-__global__ void __launch_bounds__(kSplitThreads) k_dispatch_split(Geo g, SplitArgs a) {
+__global__ void __launch_bounds__(kSplitThreads, 3) k_dispatch_split(Geo g, SplitArgs a) {
   constexpr int W = (int)sizeof(V);
   constexpr int U = 8;
-  const int lane = threadIdx.x & 31;
-  const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t nel = a.chunk_bytes / W;
+  const bool sender = warp < a.senders;
 
-  // ---- sender half: push every token chunk into its owners' receive rows, then signal
-  const int64_t send_units = (int64_t)g.N * g.T * a.chunks;
-  for (int64_t u = warp0; u < send_units; u += nwarps) {
-    const int64_t tok = u / a.chunks;
-    const int64_t coff = (u - tok * a.chunks) * a.chunk_bytes;
-    const int s = (int)(tok / g.T);
-    const uint8_t* src = a.x + tok * g.B + coff;
-    const int myr = lane < g.R ? __ldg(a.grecv + tok * g.R + lane) : -1;   // R <= 32
-    // The trip count is the same for every lane: the shuffles below need the whole warp.
-    for (int64_t b0 = 0; b0 < nel; b0 += 32 * U) {
-      const int64_t v0 = b0 + lane;
-      V r[U];
+  if (sender) {
+    // ---- sender warps: push every token chunk of batch j into its owners' receive rows;
+    // once this warp's chunks of the batch have landed, signal them per source
+    const int64_t w0 = (int64_t)blockIdx.x * a.senders + warp;
+    const int64_t nw = (int64_t)gridDim.x * a.senders;
+    for (int j = 0; j < a.nb; ++j) {
+      const int lo = batch_lo(g, a.nb, j), nt = batch_lo(g, a.nb, j + 1) - lo;
+      const int64_t per_rank = (int64_t)nt * a.chunks;
+      const int64_t units = (int64_t)g.N * per_rank;
+      if (w0 >= units) continue;
+      for (int64_t u = w0; u < units; u += nw) {
+        const int s = (int)(u / per_rank);
+        const int64_t r = u - s * per_rank;
+        const int64_t tok = (int64_t)s * g.T + lo + r / a.chunks;
+        const int64_t coff = (r % a.chunks) * a.chunk_bytes;
+        const uint8_t* src = a.x + tok * g.B + coff;
+        const int myr = lane < g.R ? __ldg(a.grecv + tok * g.R + lane) : -1;   // R <= 32
+        // The trip count is the same for every lane: the shuffles below need the whole warp.
+        for (int64_t b0 = 0; b0 < nel; b0 += 32 * U) {
+          const int64_t v0 = b0 + lane;
+          V v[U];
 #pragma unroll
-      for (int j = 0; j < U; ++j)
-        if (v0 + 32 * j < nel) r[j] = ldv<V>(src + (v0 + 32 * j) * W);
+          for (int k = 0; k < U; ++k)
+            if (v0 + 32 * k < nel) v[k] = ldv<V>(src + (v0 + 32 * k) * W);
 #pragma unroll 1
-      for (int k = 0; k < g.R; ++k) {
-        const int gr = __shfl_sync(0xffffffffu, myr, k);
-        if (gr < 0) continue;
-        uint8_t* d = a.recv + (int64_t)gr * g.B + coff;
+          for (int k = 0; k < g.R; ++k) {
+            const int gr = __shfl_sync(0xffffffffu, myr, k);
+            if (gr < 0) continue;
+            uint8_t* d = a.recv + (int64_t)gr * g.B + coff;
 #pragma unroll
-        for (int j = 0; j < U; ++j)
-          if (v0 + 32 * j < nel) stv(d + (v0 + 32 * j) * W, r[j]);
+            for (int i = 0; i < U; ++i)
+              if (v0 + 32 * i < nel) stv(d + (v0 + 32 * i) * W, v[i]);
+          }
+        }
       }
+      // Every lane's stores of the batch, then one increment per unit on its source's counter.
+      __threadfence();
+      __syncwarp();
+      if (lane == 0)
+        for (int64_t u = w0; u < units; u += nw) {
+          const int s = (int)(u / per_rank);
+          if (s != a.drop_source) atomicAdd(a.arrive + (int64_t)j * g.N + s, 1u);
+        }
     }
-    // Every lane's stores of this chunk, then one release increment per destination row.
-    __threadfence();
-    __syncwarp();
-    if (myr >= 0) {
-      const int d = myr / (int)g.RB;
-      const int slice = d * g.N + s;
-      if (slice != a.drop_slice) {
-        __threadfence();
-        atomicAdd(a.arrive + slice, 1u);
-      }
-    }
-  }
-
-  // ---- receiver half: wait for the slice of each pair's row, then shuffle it into place
-  const int64_t recv_units = g.P * a.chunks;
-  for (int64_t u = warp0; u < recv_units; u += nwarps) {
-    const int64_t q = u / a.chunks;
-    const int64_t coff = (u - q * a.chunks) * a.chunk_bytes;
-    const int gl = __ldg(a.gslot + q);
-    if (gl < 0) continue;
-    const int gr = __ldg(a.grecv + q);
-    const int s = (int)(q / g.TR);
-    const int d = gr / (int)g.RB;
-    const uint32_t target = (uint32_t)__ldg(a.C + s * g.N + d) * (uint32_t)a.chunks;
-    bool ready = true;
-    if (lane == 0) ready = wait_arrival(a.arrive + d * g.N + s, target, a.abort, a.status);
-    ready = __shfl_sync(0xffffffffu, ready, 0);
-    __syncwarp();   // orders every lane's loads below after lane 0's acquire
-    if (!ready) continue;
-    const uint8_t* src = a.recv + (int64_t)gr * g.B + coff;
-    for (int64_t b0 = 0; b0 < nel; b0 += 32 * U) {
-      const int64_t v0 = b0 + lane;
-      V r[U];
+  } else {
+    // ---- receiver warps: wait for the source's batch, then shuffle each row chunk into place
+    const int rec = kSplitWarps - a.senders;
+    const int64_t w0 = (int64_t)blockIdx.x * rec + (warp - a.senders);
+    const int64_t nw = (int64_t)gridDim.x * rec;
+    for (int j = 0; j < a.nb; ++j) {
+      const int lo = batch_lo(g, a.nb, j), nt = batch_lo(g, a.nb, j + 1) - lo;
+      const int64_t per_rank = (int64_t)nt * g.R * a.chunks;
+      const int64_t units = (int64_t)g.N * per_rank;
+      const uint32_t target = (uint32_t)nt * (uint32_t)a.chunks;
+      int ready_s = -1;
+      for (int64_t u = w0; u < units; u += nw) {
+        const int s = (int)(u / per_rank);
+        const int64_t r = u - s * per_rank;
+        const int64_t q = ((int64_t)s * g.T + lo) * g.R + r / a.chunks;
+        const int64_t coff = (r % a.chunks) * a.chunk_bytes;
+        const int gl = __ldg(a.gslot + q);
+        if (gl < 0) continue;
+        if (s != ready_s) {
+          bool ok = true;
+          if (lane == 0) ok = wait_arrival(a.arrive + (int64_t)j * g.N + s, target, a.abort, a.status);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          __syncwarp();   // orders every lane's loads below after lane 0's acquire
+          if (!ok) continue;
+          ready_s = s;
+        }
+        const int gr = __ldg(a.grecv + q);
+        const uint8_t* src = a.recv + (int64_t)gr * g.B + coff;
+        for (int64_t b0 = 0; b0 < nel; b0 += 32 * U) {
+          const int64_t v0 = b0 + lane;
+          V v[U];
 #pragma unroll
-      for (int j = 0; j < U; ++j)
-        if (v0 + 32 * j < nel) r[j] = ldv_l2<V>(src + (v0 + 32 * j) * W);
+          for (int k = 0; k < U; ++k)
+            if (v0 + 32 * k < nel) v[k] = ldv_l2<V>(src + (v0 + 32 * k) * W);
 #pragma unroll
-      for (int j = 0; j < U; ++j) {
-        const int64_t v = v0 + 32 * j;
-        if (v >= nel) continue;
-        if (FP8) {   // one chunk per row: codes [0, H), then the scales
-          const int64_t split = g.H / W;
-          if (v < split)
-            stv(a.ex + (int64_t)gl * g.H + v * W, r[j]);
-          else
-            stv(a.exs + (int64_t)gl * (g.H / 32) + (v - split) * W, r[j]);
-        } else {
-          stv(a.ex + (int64_t)gl * g.B + coff + v * W, r[j]);
+          for (int k = 0; k < U; ++k) {
+            const int64_t e = v0 + 32 * k;
+            if (e >= nel) continue;
+            if (FP8) {   // one chunk per row: codes [0, H), then the scales
+              const int64_t split = g.H / W;
+              if (e < split)
+                stv(a.ex + (int64_t)gl * g.H + e * W, v[k]);
+              else
+                stv(a.exs + (int64_t)gl * (g.H / 32) + (e - split) * W, v[k]);
+            } else {
+              stv(a.ex + (int64_t)gl * g.B + coff + e * W, v[k]);
+            }
+          }
         }
       }
     }
@@ -197,7 +226,7 @@ __global__ void __launch_bounds__(kSplitThreads) k_dispatch_split(Geo g, SplitAr
   }
   __syncthreads();
   if (is_last) {
-    for (int i = threadIdx.x; i < g.N * g.N; i += blockDim.x) a.arrive[i] = 0u;
+    for (int i = threadIdx.x; i < a.nb * g.N; i += blockDim.x) a.arrive[i] = 0u;
     if (threadIdx.x == 0) {
       *a.abort = 0u;
       *a.done = 0u;
@@ -225,25 +254,34 @@ cudaError_t run_split(const Geo& g, const SplitArgs& a, Ctx& c) {
 
 }  // namespace
 
+int split_batches(const Geo& g) {
+  int64_t nb = (g.P * g.B + kSplitBatchBytes / 2) / kSplitBatchBytes;
+  if (nb > kMaxSplitBatches) nb = kMaxSplitBatches;
+  if (nb > g.T) nb = g.T;
+  return nb < 1 ? 1 : (int)nb;
+}
+
 cudaError_t launch_dispatch_split(const Geo& g, const moe_layout_t* lay, const void* x, void* recv, void* ex,
-                                  float* exs, int drop_slice, Ctx& c) {
+                                  float* exs, int drop_source, Ctx& c) {
   SplitArgs a;
   a.x = static_cast<const uint8_t*>(x);
   a.recv = static_cast<uint8_t*>(recv);
   a.ex = static_cast<uint8_t*>(ex);
   a.exs = reinterpret_cast<uint8_t*>(exs);
-  a.gsend = lay->gsend;
   a.grecv = lay->grecv;
   a.gslot = lay->gslot;
-  a.C = lay->C;
   a.arrive = reinterpret_cast<uint32_t*>(lay->scratch + layout_scratch_arrive_offset(g));
-  a.done = a.arrive + (int64_t)g.N * g.N;
+  a.done = a.arrive + split_arrive_words(g);
   a.abort = a.done + 1;
   a.status = lay->status;
-  a.drop_slice = drop_slice;
+  a.drop_source = drop_source;
   const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
   a.chunks = (!fp8 && g.B >= 8192 && g.B % 32 == 0) ? 2 : 1;
   a.chunk_bytes = g.B / a.chunks;
+  a.nb = lay->batches > 0 ? (lay->batches < kMaxSplitBatches ? lay->batches : kMaxSplitBatches) : split_batches(g);
+  if (a.nb > g.T) a.nb = g.T < 1 ? 1 : g.T;
+  int senders = (int)((2 * kSplitWarps * ((int64_t)g.R + 1) + (3 * (int64_t)g.R + 1)) / (2 * (3 * (int64_t)g.R + 1)));
+  a.senders = senders < 1 ? 1 : (senders > kSplitWarps - 1 ? kSplitWarps - 1 : senders);
   if ((int64_t)g.N * g.T == 0) return cudaSuccess;
   LaunchScope ls(c, MOE_K_DISPATCH_SPLIT);
   if (g.B % 16 == 0)

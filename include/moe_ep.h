@@ -171,13 +171,13 @@ typedef struct {
  *   status   [1]         sticky error bits, bit (1 << moe_status)
  *   scratch  internal: per-chunk counts [N][ceil(T*R/256)][E], per-rank counters [N],
  *            per-token group counts of the partial combine [N][T] and the split-phase
- *            arrival counters [N][N] (+ 2)
+ *            arrival counters [max(N, 32)][N] (+ 2)
  * Host-side fields (set by the caller after moe_layout_init, read at each call):
  *   flags, prof, tma_stages (0 = automatic, else 1..32 stages per TMA mover CTA),
  *   ctas_per_sm (0 = automatic, else mover CTAs per SM), batches (token batches of
- *   moe_forward's micro-batches and of moe_dispatch / moe_combine (0 = automatic, else
- *   1..32) and of moe_forward_host's copy-engine pipeline (0 = automatic, else 1..16); see
- *   moe_batches).
+ *   moe_forward's micro-batches, of moe_dispatch / moe_combine and of moe_dispatch_split
+ *   (0 = automatic, else 1..32) and of moe_forward_host's copy-engine pipeline (0 =
+ *   automatic, else 1..16); see moe_batches).
  */
 typedef struct {
     int32_t *cnt, *C, *soff, *roff, *rtot, *ecnt, *eoff;
@@ -308,19 +308,23 @@ moe_status moe_dispatch_send_noalloc(const moe_dims *dims, const moe_layout_t *l
  * Results are those of moe_dispatch_send with MOE_FLAG_DIRECT_PUSH followed by
  * moe_dispatch_recv: d_recv [N][RB][B] holds every receive row, d_expert_x / d_expert_scale
  * the grouped rows (same layouts as moe_dispatch_recv).
- * One cooperative launch: every CTA first pushes its share of token rows into the owners'
- * receive rows and increments, per row, the arrival counter of the slice (d, s) it belongs
- * to; it then takes pairs, waits until the counter of the pair's slice reaches C[s][d] row
- * pieces, and copies the row into its expert's slot. Each wait is bounded (1 s): on expiry
- * the status word gets the MOE_ERR_TIMEOUT bit, later waits of the call give up at once,
- * the grouped rows of unfinished slices are left unwritten, and the call still completes.
- * The counters live in the layout workspace, start at zero and are zeroed again by the
- * call; calls that share a layout must not overlap on the GPU.
- * withhold_slice: failure injection for tests; the signals of slice d*N + s are never sent,
- * so its waits time out. Pass -1 in normal use; other negative values and values >= N*N
- * are MOE_ERR_INVALID_ARG, and so is R > 32. */
+ * One cooperative launch over nb token batches (tokens [j*T/nb, (j+1)*T/nb) of every rank;
+ * nb = lay->batches if set, else about one per 16 MB of pushed rows; at most 32 and T).
+ * Sender warps push each batch's
+ * token rows into the owners' receive rows and, once their rows of the batch have landed,
+ * signal the batch on a counter per (batch, source rank); receiver warps take the batch's
+ * pairs, wait until the pair's source has signalled every token of the batch, and copy the
+ * row into its expert's slot, while the batch's rows are still in L2. Each wait is bounded
+ * (1 s): on expiry the status word gets the MOE_ERR_TIMEOUT bit, later waits of the call give
+ * up at once, the grouped rows of unfinished batches are left unwritten, and the call still
+ * completes. The counters live in the layout workspace, start at zero and are zeroed again by
+ * the call; calls that share a layout must not overlap on the GPU.
+ * withhold_source: failure injection for tests; source rank s's signals are never sent, so
+ * the waits for its rows time out (its receive rows are still written, its grouped rows are
+ * not). Pass -1 in normal use; other negative values and values >= N are
+ * MOE_ERR_INVALID_ARG, and so is R > 32. */
 moe_status moe_dispatch_split(const moe_dims *dims, const moe_layout_t *lay, const void *d_x, void *d_recv,
-                              void *d_expert_x, float *d_expert_scale, int32_t withhold_slice, void *stream);
+                              void *d_expert_x, float *d_expert_scale, int32_t withhold_source, void *stream);
 
 /* Split-phase dispatch with per-sender dedicated space and the routing information
  * piggybacked on the first writes (section "Send and receive buffers": each receiver

@@ -18,11 +18,11 @@ def to_dev(a: np.ndarray, dtype=None) -> torch.Tensor:
 
 
 def run_gpu(wl: workloads.Workload, inp: dict, flags: int = 0, poison: bool = True, split: bool = False,
-            withhold_slice: int = -1, fused_quant: bool = False, forward: bool = False, phases: bool = False,
+            withhold_source: int = -1, fused_quant: bool = False, forward: bool = False, phases: bool = False,
             **kw):
     """Runs every step separately on the GPU; returns (MoeEP, host copies of every buffer).
     With split, dispatch is the one-launch split-phase dispatch (direct push) instead of
-    dispatch send + receive; withhold_slice is passed to it. With fused_quant (fp8), the
+    dispatch send + receive; withhold_source is passed to it. With fused_quant (fp8), the
     quantisation runs inside the pack (the quantised token rows are not kept). With forward,
     the whole pass is one moe_forward call (micro-batched as the layout's settings say); with
     phases, moe_dispatch, the identity expert and moe_combine (fp8 quantised in the pack)."""
@@ -54,7 +54,7 @@ def run_gpu(wl: workloads.Workload, inp: dict, flags: int = 0, poison: bool = Tr
                 ep.quantize(x)
                 x = ep.xq
             if split:
-                ep.dispatch_split(x, withhold_slice)
+                ep.dispatch_split(x, withhold_source)
             else:
                 ep.dispatch_send(x)
                 ep.dispatch_recv()

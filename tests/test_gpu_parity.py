@@ -259,32 +259,34 @@ def test_partial_combine_matches_oracle(orc, wl):
     np.testing.assert_array_equal(u16(ep.out.cpu()), out_o)
 
 
+@pytest.mark.parametrize("nb", [0, 3, 7], ids=lambda b: f"batches{b}")
 @pytest.mark.parametrize("wl", CASES + [workloads.config(1).replace(T=16, seed=150)], ids=lambda w: w.name)
-def test_split_dispatch_matches_oracle(orc, wl):
-    """Split-phase dispatch (push, per-slice arrival counters, bounded waits, shuffle in one
-    cooperative launch) leaves exactly the receive and grouped rows of the two-step path."""
+def test_split_dispatch_matches_oracle(orc, wl, nb):
+    """Split-phase dispatch (push, per-(batch, source) arrival counters, bounded waits,
+    shuffle in one cooperative launch over token batches: automatic, 3 and 7) leaves exactly
+    the receive and grouped rows of the two-step path."""
     inp = workloads.make_inputs(wl)
-    _, res = run_gpu(wl, inp, flags=8, split=True)
+    _, res = run_gpu(wl, inp, flags=8, split=True, batches=nb)
     compare_all(orc, wl, inp, res, push=True)
 
 
-def test_split_dispatch_withheld_slice_times_out_and_recovers(orc):
-    """A slice whose arrival signals never come: its waits end after the bound with the
-    timeout status, every other row is still placed, and the next call on the same layout
-    (counters reset by the call itself) is exact again."""
+@pytest.mark.parametrize("nb", [1, 5], ids=lambda b: f"batches{b}")
+def test_split_dispatch_withheld_source_times_out_and_recovers(orc, nb):
+    """A source whose arrival signals never come: the waits for its rows end after the bound
+    with the timeout status, every other row is still placed, and the next call on the same
+    layout (counters reset by the call itself) is exact again."""
     wl = W("split-timeout", 4, 33, 1024, 16, 4, "bf16", "uniform", 151)
     inp = workloads.make_inputs(wl)
     o = orc.forward(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, wl.payload, inp["x"], inp["idx"], inp["w"])
     lay_o = o["layout"]
-    s, d = 1, 2
-    assert lay_o["C"][s, d] > 0
-    ep, res = run_gpu(wl, inp, flags=8, split=True, withhold_slice=d * wl.N + s)
+    s = 1
+    ep, res = run_gpu(wl, inp, flags=8, split=True, withhold_source=s, batches=nb)
     assert res["status_code"] == 6                      # MOE_ERR_TIMEOUT
     recv = u8(res["recv"])
     for dd in range(wl.N):
         n = lay_o["rtot"][dd]
         np.testing.assert_array_equal(recv[dd, :n], o["recv"][dd, :n], err_msg="recv")
-    # grouped rows: those of slice (d, s) are unwritten, every other one is exact
+    # grouped rows: those from source s are unwritten, every other one is exact
     ex = u16(res["expert_x"])
     slot_src = lay_o["slot_src"].reshape(wl.E, -1)
     TR = wl.T * wl.R
@@ -292,7 +294,7 @@ def test_split_dispatch_withheld_slice_times_out_and_recovers(orc):
         dd, l = divmod(e, wl.L)
         for j in range(min(lay_o["ecnt"][dd, l], lay_o["cap"])):
             src = slot_src[e, j] // TR
-            if dd == d and src == s:
+            if src == s:
                 assert (ex[dd, l, j].view(np.uint8) == 0xA5).all(), "withheld row was written"
             else:
                 np.testing.assert_array_equal(ex[dd, l, j], o["ex"][dd, l, j])
@@ -308,13 +310,13 @@ def test_split_dispatch_withheld_slice_times_out_and_recovers(orc):
             np.testing.assert_array_equal(ex[dd, l, :ecnt[dd, l]], o["ex"][dd, l, :ecnt[dd, l]])
 
 
-def test_split_dispatch_rejects_bad_withhold_slice():
+def test_split_dispatch_rejects_bad_withhold_source():
     import ctypes
     from combine_routing_count_gb300 import MoeEP, lib
     ep = MoeEP(2, 4, 128, 4, 2)
     x = torch.zeros((2, 4, 128), dtype=torch.bfloat16, device="cuda")
     n0 = lib().moe_launch_count()
-    for bad in (-2, 4):
+    for bad in (-2, 2):
         rc = lib().moe_dispatch_split(ctypes.byref(ep.dims), ctypes.byref(ep.layout), x.data_ptr(),
                                       ep.recv.data_ptr(), ep.expert_x.data_ptr(), None, bad, None)
         assert rc == 1
