@@ -85,9 +85,11 @@ def parse_args(argv=None):
                         "all cores)")
     p.add_argument("--other-cpu-seconds", type=float, default=3.0,
                    help="CPU work for the single-thread oracle baseline of each per_config workload")
-    p.add_argument("--profile-step", action="store_true",
-                   help="run only W + K one-batch steps of the workload (L2 flushed before each) and print a "
-                        "short summary: the command the ncu captures in profiles/ profile")
+    p.add_argument("--profile-step", choices=["pass", "split", "dedicated"], default=None,
+                   help="run only W + K steps of one kind (L2 flushed before each) and print a short summary, "
+                        "for the ncu captures in profiles/: 'pass' the whole pass in one batch (whole-pass "
+                        "launches), 'split' and 'dedicated' the direct-push step with the split-phase dispatch "
+                        "(without or with dedicated space)")
     return p.parse_args(argv)
 
 
@@ -404,13 +406,29 @@ def measure(wl, args, dist, device, peak: float, peak_kind: str, cpu_seconds: fl
         e3.record(stream)
 
     if args.profile_step:
-        # Only the one-batch pass (whole-pass launches), for ncu: W + K steps, L2 flushed before each.
+        # Only one kind of step, for ncu: W + K steps, L2 flushed before each.
         ep.layout.flags |= 0x40
+        if args.profile_step != "pass":
+            ep.layout.flags |= 8
         for _ in range(args.warmup + K):
             flush_l2()
-            step()
+            if args.profile_step == "pass":
+                step()
+                continue
+            ep.layout_step(idx)
+            xin = x
+            if fp8:
+                ep.quantize(x)
+                xin = ep.xq
+            if args.profile_step == "split":
+                ep.dispatch_split(xin)
+            else:
+                ep.dispatch_dedicated(xin, idx, 16)
+            ep.expert_identity()
+            ep.combine_send()
+            ep.combine_recv(w)
         code, bits = ep.status()
-        return {"profile_step": wl.name, "steps": args.warmup + K, "status": code}
+        return {"profile_step": args.profile_step, "workload": wl.name, "steps": args.warmup + K, "status": code}
 
     for _ in range(args.warmup):
         flush_l2()

@@ -50,8 +50,8 @@ struct SplitArgs {
   uint32_t* done;       // CTAs finished (the last one resets arrive[], done and abort)
   uint32_t* abort;      // set by the first wait that times out in this call
   int32_t* status;
-  int chunks;           // column chunks per row
-  int64_t chunk_bytes;
+  int send_chunks;      // column chunks of a token row per sender unit
+  int recv_chunks;      // column chunks of a receive row per receiver unit
   int nb;               // token batches
   int senders;          // sender warps per CTA (the rest receive)
   int drop_source;      // failure injection: the source rank whose signals are withheld, or -1
@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(kSplitThreads, 3) k_dispatch_split(Geo g, Spli
   constexpr int W = (int)sizeof(V);
   constexpr int U = 8;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t nel = a.chunk_bytes / W;
+  const int64_t nel = g.B / W;                                    // vectors per row
   const bool sender = warp < a.senders;
 
   if (sender) {
@@ -125,33 +125,35 @@ __global__ void __launch_bounds__(kSplitThreads, 3) k_dispatch_split(Geo g, Spli
     // once this warp's chunks of the batch have landed, signal them per source
     const int64_t w0 = (int64_t)blockIdx.x * a.senders + warp;
     const int64_t nw = (int64_t)gridDim.x * a.senders;
+    const int64_t cv = (nel + a.send_chunks - 1) / a.send_chunks;   // vectors per chunk
     for (int j = 0; j < a.nb; ++j) {
       const int lo = batch_lo(g, a.nb, j), nt = batch_lo(g, a.nb, j + 1) - lo;
-      const int64_t per_rank = (int64_t)nt * a.chunks;
+      const int64_t per_rank = (int64_t)nt * a.send_chunks;
       const int64_t units = (int64_t)g.N * per_rank;
       if (w0 >= units) continue;
       for (int64_t u = w0; u < units; u += nw) {
         const int s = (int)(u / per_rank);
         const int64_t r = u - s * per_rank;
-        const int64_t tok = (int64_t)s * g.T + lo + r / a.chunks;
-        const int64_t coff = (r % a.chunks) * a.chunk_bytes;
-        const uint8_t* src = a.x + tok * g.B + coff;
+        const int64_t tok = (int64_t)s * g.T + lo + r / a.send_chunks;
+        const int64_t v_lo = (r % a.send_chunks) * cv;
+        const int64_t v_hi = v_lo + cv < nel ? v_lo + cv : nel;
+        const uint8_t* src = a.x + tok * g.B;
         const int myr = lane < g.R ? __ldg(a.grecv + tok * g.R + lane) : -1;   // R <= 32
         // The trip count is the same for every lane: the shuffles below need the whole warp.
-        for (int64_t b0 = 0; b0 < nel; b0 += 32 * U) {
+        for (int64_t b0 = v_lo; b0 < v_hi; b0 += 32 * U) {
           const int64_t v0 = b0 + lane;
           V v[U];
 #pragma unroll
           for (int k = 0; k < U; ++k)
-            if (v0 + 32 * k < nel) v[k] = ldv<V>(src + (v0 + 32 * k) * W);
+            if (v0 + 32 * k < v_hi) v[k] = ldv<V>(src + (v0 + 32 * k) * W);
 #pragma unroll 1
           for (int k = 0; k < g.R; ++k) {
             const int gr = __shfl_sync(0xffffffffu, myr, k);
             if (gr < 0) continue;
-            uint8_t* d = a.recv + (int64_t)gr * g.B + coff;
+            uint8_t* d = a.recv + (int64_t)gr * g.B;
 #pragma unroll
             for (int i = 0; i < U; ++i)
-              if (v0 + 32 * i < nel) stv(d + (v0 + 32 * i) * W, v[i]);
+              if (v0 + 32 * i < v_hi) stv(d + (v0 + 32 * i) * W, v[i]);
           }
         }
       }
@@ -169,17 +171,20 @@ __global__ void __launch_bounds__(kSplitThreads, 3) k_dispatch_split(Geo g, Spli
     const int rec = kSplitWarps - a.senders;
     const int64_t w0 = (int64_t)blockIdx.x * rec + (warp - a.senders);
     const int64_t nw = (int64_t)gridDim.x * rec;
+    const int64_t cv = (nel + a.recv_chunks - 1) / a.recv_chunks;
+    const int64_t split = g.H / W;   // fp8: codes are vectors [0, split), scales the rest
     for (int j = 0; j < a.nb; ++j) {
       const int lo = batch_lo(g, a.nb, j), nt = batch_lo(g, a.nb, j + 1) - lo;
-      const int64_t per_rank = (int64_t)nt * g.R * a.chunks;
+      const int64_t per_rank = (int64_t)nt * g.R * a.recv_chunks;
       const int64_t units = (int64_t)g.N * per_rank;
-      const uint32_t target = (uint32_t)nt * (uint32_t)a.chunks;
+      const uint32_t target = (uint32_t)nt * (uint32_t)a.send_chunks;
       int ready_s = -1;
       for (int64_t u = w0; u < units; u += nw) {
         const int s = (int)(u / per_rank);
         const int64_t r = u - s * per_rank;
-        const int64_t q = ((int64_t)s * g.T + lo) * g.R + r / a.chunks;
-        const int64_t coff = (r % a.chunks) * a.chunk_bytes;
+        const int64_t q = ((int64_t)s * g.T + lo) * g.R + r / a.recv_chunks;
+        const int64_t v_lo = (r % a.recv_chunks) * cv;
+        const int64_t v_hi = v_lo + cv < nel ? v_lo + cv : nel;
         const int gl = __ldg(a.gslot + q);
         if (gl < 0) continue;
         if (s != ready_s) {
@@ -191,25 +196,24 @@ __global__ void __launch_bounds__(kSplitThreads, 3) k_dispatch_split(Geo g, Spli
           ready_s = s;
         }
         const int gr = __ldg(a.grecv + q);
-        const uint8_t* src = a.recv + (int64_t)gr * g.B + coff;
-        for (int64_t b0 = 0; b0 < nel; b0 += 32 * U) {
+        const uint8_t* src = a.recv + (int64_t)gr * g.B;
+        for (int64_t b0 = v_lo; b0 < v_hi; b0 += 32 * U) {
           const int64_t v0 = b0 + lane;
           V v[U];
 #pragma unroll
           for (int k = 0; k < U; ++k)
-            if (v0 + 32 * k < nel) v[k] = ldv_l2<V>(src + (v0 + 32 * k) * W);
+            if (v0 + 32 * k < v_hi) v[k] = ldv_l2<V>(src + (v0 + 32 * k) * W);
 #pragma unroll
           for (int k = 0; k < U; ++k) {
             const int64_t e = v0 + 32 * k;
-            if (e >= nel) continue;
-            if (FP8) {   // one chunk per row: codes [0, H), then the scales
-              const int64_t split = g.H / W;
+            if (e >= v_hi) continue;
+            if (FP8) {
               if (e < split)
                 stv(a.ex + (int64_t)gl * g.H + e * W, v[k]);
               else
                 stv(a.exs + (int64_t)gl * (g.H / 32) + (e - split) * W, v[k]);
             } else {
-              stv(a.ex + (int64_t)gl * g.B + coff + e * W, v[k]);
+              stv(a.ex + (int64_t)gl * g.B + e * W, v[k]);
             }
           }
         }
@@ -276,8 +280,15 @@ cudaError_t launch_dispatch_split(const Geo& g, const moe_layout_t* lay, const v
   a.status = lay->status;
   a.drop_source = drop_source;
   const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
-  a.chunks = (!fp8 && g.B >= 8192 && g.B % 32 == 0) ? 2 : 1;
-  a.chunk_bytes = g.B / a.chunks;
+  // Receive units are half rows for rows of 8 KB and more (one row otherwise); a send unit
+  // writes its chunk R times, so token rows are cut into about R times as many chunks, which
+  // gives the senders about as many units per batch as the receivers (at least 32 vectors a
+  // chunk: one per lane).
+  const int64_t nvec = g.B / (g.B % 16 == 0 ? 16 : 4);
+  a.recv_chunks = (g.B >= 8192 && nvec >= 64) ? 2 : 1;
+  int64_t sc = (int64_t)a.recv_chunks * g.R;
+  if (sc > nvec / 32) sc = nvec / 32;
+  a.send_chunks = sc < 1 ? 1 : (int)sc;
   a.nb = lay->batches > 0 ? (lay->batches < kMaxSplitBatches ? lay->batches : kMaxSplitBatches) : split_batches(g);
   if (a.nb > g.T) a.nb = g.T < 1 ? 1 : g.T;
   int senders = (int)((2 * kSplitWarps * ((int64_t)g.R + 1) + (3 * (int64_t)g.R + 1)) / (2 * (3 * (int64_t)g.R + 1)));
