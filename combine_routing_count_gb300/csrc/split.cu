@@ -10,23 +10,20 @@
 // On one GPU the two halves cannot be separate kernels that wait on each other (nothing
 // guarantees they run at the same time), so both run in one cooperative launch, whose
 // CTAs are all resident at once. The tokens are taken in nb batches (tokens
-// [j*T/nb, (j+1)*T/nb) of every rank), and every CTA has sender warps and receiver warps:
-//  - sender warps push the (token, column chunk) units of batch 0, then batch 1, ... into
-//    the owners' receive rows (the direct-push pack); once a warp's units of a batch have
-//    landed (one fence), it signals each unit on the counter of (batch j, source s);
-//  - receiver warps take the (pair, column chunk) units of batch 0, then batch 1, ...; each
-//    waits, with an acquire poll bounded by kSplitWaitNs, until its source's counter for
-//    the batch reaches the batch's token chunks (every row source s pushed in batch j has
-//    landed), then copies the row chunk into its expert's grouped row (codes and scales
-//    apart for fp8).
-// Receivers trail the senders by about a batch, so a batch's receive rows are still in L2
-// when they are read back. Sender warps never wait, so every wait ends unless a signal is
-// missing; then the status word gets the timeout bit, later waits of the call give up at
-// once (by then every push has long landed), and the unfinished rows are skipped. The
+// [j*T/nb, (j+1)*T/nb) of every rank), and every warp runs the two halves pipelined: it
+// pushes its (token, column chunk) units of batch j+1 into the owners' receive rows (the
+// direct-push pack) and, once they have landed (one fence), signals each on the counter of
+// (batch j+1, source s); then it takes its (pair, column chunk) units of batch j, waits with
+// an acquire poll until the pair's source has signalled every chunk of batch j, and copies
+// the row chunk into its expert's grouped row (codes and scales apart for fp8). A batch's
+// rows are read back one batch after they were pushed, while they are still in L2.
+// Waits in that loop are short (kSplitQuickNs): one that runs out leaves the rest of the
+// batch's units for later, so a warp's pushes never wait behind a missing signal. After its
+// last push a warp finishes the units it left, each wait now bounded by kSplitWaitNs; every
+// push of the call has landed by then, so a wait that runs out means a signal that will
+// never come: the status word gets the timeout bit, later waits of the call give up at once
+// unless their counter is already complete, and the unfinished rows are skipped. The
 // counters start at zero (moe_layout_init) and the last CTA of each call zeroes them again.
-// The share of sender warps follows the bytes each half moves: a token row is read once and
-// written R times by the senders, and each of its R pairs is read and written once by the
-// receivers, so senders take (R + 1) / (3R + 1) of the warps (3 of 8 at R = 8).
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -34,9 +31,9 @@
 namespace moe {
 namespace {
 
-constexpr uint64_t kSplitWaitNs = 1000000000ull;   // 1 s
+constexpr uint64_t kSplitWaitNs = 1000000000ull;   // 1 s: a signal that will not come
+constexpr uint64_t kSplitQuickNs = 20000ull;         // 20 us: leave the batch for later
 constexpr int kSplitThreads = 256;
-constexpr int kSplitWarps = kSplitThreads / 32;
 constexpr int64_t kSplitBatchBytes = 16ll << 20;    // pushed rows per token batch (about L2 / 8)
 
 struct SplitArgs {
@@ -50,10 +47,8 @@ struct SplitArgs {
   uint32_t* done;       // CTAs finished (the last one resets arrive[], done and abort)
   uint32_t* abort;      // set by the first wait that times out in this call
   int32_t* status;
-  int send_chunks;      // column chunks of a token row per sender unit
-  int recv_chunks;      // column chunks of a receive row per receiver unit
+  int chunks;           // column chunks of a row per unit
   int nb;               // token batches
-  int senders;          // sender warps per CTA (the rest receive)
   int drop_source;      // failure injection: the source rank whose signals are withheld, or -1
 };
 
@@ -63,19 +58,25 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
   return v;
 }
 
-// Waits until *ctr >= target. Gives up at once if a wait of this call already timed out,
-// else after kSplitWaitNs, recording the timeout. Returns whether the target was reached.
+// Waits until *ctr >= target. quick: gives up after kSplitQuickNs and records nothing (the
+// caller retries later). Otherwise gives up at once if a wait of this call already timed
+// out, else after kSplitWaitNs, recording the timeout. Returns whether the target was reached.
 __device__ __forceinline__ bool wait_arrival(const uint32_t* ctr, uint32_t target, uint32_t* abort,
-                                             int32_t* status) {
+                                             int32_t* status, bool quick) {
   if (ld_acquire(ctr) >= target) return true;
   const uint64_t t0 = global_ns();
   while (true) {
     if (ld_acquire(ctr) >= target) return true;
-    if (*reinterpret_cast<volatile uint32_t*>(abort)) return false;
-    if (global_ns() - t0 > kSplitWaitNs) {
-      atomicExch(abort, 1u);
-      set_status(status, kBitTimeout);
-      return false;
+    const uint64_t dt = global_ns() - t0;
+    if (quick) {
+      if (dt > kSplitQuickNs) return false;
+    } else {
+      if (*reinterpret_cast<volatile uint32_t*>(abort)) return false;
+      if (dt > kSplitWaitNs) {
+        atomicExch(abort, 1u);
+        set_status(status, kBitTimeout);
+        return false;
+      }
     }
     __nanosleep(128);
   }
@@ -112,114 +113,139 @@ __device__ __forceinline__ void stv(uint8_t* p, const uint32_t& v) { *reinterpre
 
 __device__ __forceinline__ int batch_lo(const Geo& g, int nb, int j) { return (int)((int64_t)j * g.T / nb); }
 
-template <bool FP8, typename V>
-__global__ void __launch_bounds__(kSplitThreads, 3) k_dispatch_split(Geo g, SplitArgs a) {
+// Pushes this warp's (token, column chunk) units of batch j into the owners' receive rows,
+// then, once they have landed, signals each on its source's counter of the batch.
+template <typename V>
+__device__ __forceinline__ void send_batch(const Geo& g, const SplitArgs& a, int j, int64_t w0, int64_t nw,
+                                           int lane) {
   constexpr int W = (int)sizeof(V);
   constexpr int U = 8;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t nel = g.B / W;                                    // vectors per row
-  const bool sender = warp < a.senders;
-
-  if (sender) {
-    // ---- sender warps: push every token chunk of batch j into its owners' receive rows;
-    // once this warp's chunks of the batch have landed, signal them per source
-    const int64_t w0 = (int64_t)blockIdx.x * a.senders + warp;
-    const int64_t nw = (int64_t)gridDim.x * a.senders;
-    const int64_t cv = (nel + a.send_chunks - 1) / a.send_chunks;   // vectors per chunk
-    for (int j = 0; j < a.nb; ++j) {
-      const int lo = batch_lo(g, a.nb, j), nt = batch_lo(g, a.nb, j + 1) - lo;
-      const int64_t per_rank = (int64_t)nt * a.send_chunks;
-      const int64_t units = (int64_t)g.N * per_rank;
-      if (w0 >= units) continue;
-      for (int64_t u = w0; u < units; u += nw) {
-        const int s = (int)(u / per_rank);
-        const int64_t r = u - s * per_rank;
-        const int64_t tok = (int64_t)s * g.T + lo + r / a.send_chunks;
-        const int64_t v_lo = (r % a.send_chunks) * cv;
-        const int64_t v_hi = v_lo + cv < nel ? v_lo + cv : nel;
-        const uint8_t* src = a.x + tok * g.B;
-        const int myr = lane < g.R ? __ldg(a.grecv + tok * g.R + lane) : -1;   // R <= 32
-        // The trip count is the same for every lane: the shuffles below need the whole warp.
-        for (int64_t b0 = v_lo; b0 < v_hi; b0 += 32 * U) {
-          const int64_t v0 = b0 + lane;
-          V v[U];
+  const int64_t nel = g.B / W;
+  const int64_t cv = (nel + a.chunks - 1) / a.chunks;   // vectors per chunk
+  const int lo = batch_lo(g, a.nb, j), nt = batch_lo(g, a.nb, j + 1) - lo;
+  const int64_t per_rank = (int64_t)nt * a.chunks;
+  const int64_t units = (int64_t)g.N * per_rank;
+  if (w0 >= units) return;
+  for (int64_t u = w0; u < units; u += nw) {
+    const int s = (int)(u / per_rank);
+    const int64_t r = u - s * per_rank;
+    const int64_t tok = (int64_t)s * g.T + lo + r / a.chunks;
+    const int64_t v_lo = (r % a.chunks) * cv;
+    const int64_t v_hi = v_lo + cv < nel ? v_lo + cv : nel;
+    const uint8_t* src = a.x + tok * g.B;
+    const int myr = lane < g.R ? __ldg(a.grecv + tok * g.R + lane) : -1;   // R <= 32
+    // The trip count is the same for every lane: the shuffles below need the whole warp.
+    for (int64_t b0 = v_lo; b0 < v_hi; b0 += 32 * U) {
+      const int64_t v0 = b0 + lane;
+      V v[U];
 #pragma unroll
-          for (int k = 0; k < U; ++k)
-            if (v0 + 32 * k < v_hi) v[k] = ldv<V>(src + (v0 + 32 * k) * W);
+      for (int k = 0; k < U; ++k)
+        if (v0 + 32 * k < v_hi) v[k] = ldv<V>(src + (v0 + 32 * k) * W);
 #pragma unroll 1
-          for (int k = 0; k < g.R; ++k) {
-            const int gr = __shfl_sync(0xffffffffu, myr, k);
-            if (gr < 0) continue;
-            uint8_t* d = a.recv + (int64_t)gr * g.B;
+      for (int k = 0; k < g.R; ++k) {
+        const int gr = __shfl_sync(0xffffffffu, myr, k);
+        if (gr < 0) continue;
+        uint8_t* d = a.recv + (int64_t)gr * g.B;
 #pragma unroll
-            for (int i = 0; i < U; ++i)
-              if (v0 + 32 * i < v_hi) stv(d + (v0 + 32 * i) * W, v[i]);
-          }
-        }
+        for (int i = 0; i < U; ++i)
+          if (v0 + 32 * i < v_hi) stv(d + (v0 + 32 * i) * W, v[i]);
       }
-      // Every lane's stores of the batch, then one increment per unit on its source's counter.
-      __threadfence();
-      __syncwarp();
-      if (lane == 0)
-        for (int64_t u = w0; u < units; u += nw) {
-          const int s = (int)(u / per_rank);
-          if (s != a.drop_source) atomicAdd(a.arrive + (int64_t)j * g.N + s, 1u);
-        }
     }
-  } else {
-    // ---- receiver warps: wait for the source's batch, then shuffle each row chunk into place
-    const int rec = kSplitWarps - a.senders;
-    const int64_t w0 = (int64_t)blockIdx.x * rec + (warp - a.senders);
-    const int64_t nw = (int64_t)gridDim.x * rec;
-    const int64_t cv = (nel + a.recv_chunks - 1) / a.recv_chunks;
-    const int64_t split = g.H / W;   // fp8: codes are vectors [0, split), scales the rest
-    for (int j = 0; j < a.nb; ++j) {
-      const int lo = batch_lo(g, a.nb, j), nt = batch_lo(g, a.nb, j + 1) - lo;
-      const int64_t per_rank = (int64_t)nt * g.R * a.recv_chunks;
-      const int64_t units = (int64_t)g.N * per_rank;
-      const uint32_t target = (uint32_t)nt * (uint32_t)a.send_chunks;
-      int ready_s = -1;
-      for (int64_t u = w0; u < units; u += nw) {
-        const int s = (int)(u / per_rank);
-        const int64_t r = u - s * per_rank;
-        const int64_t q = ((int64_t)s * g.T + lo) * g.R + r / a.recv_chunks;
-        const int64_t v_lo = (r % a.recv_chunks) * cv;
-        const int64_t v_hi = v_lo + cv < nel ? v_lo + cv : nel;
-        const int gl = __ldg(a.gslot + q);
-        if (gl < 0) continue;
-        if (s != ready_s) {
-          bool ok = true;
-          if (lane == 0) ok = wait_arrival(a.arrive + (int64_t)j * g.N + s, target, a.abort, a.status);
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          __syncwarp();   // orders every lane's loads below after lane 0's acquire
-          if (!ok) continue;
-          ready_s = s;
-        }
-        const int gr = __ldg(a.grecv + q);
-        const uint8_t* src = a.recv + (int64_t)gr * g.B;
-        for (int64_t b0 = v_lo; b0 < v_hi; b0 += 32 * U) {
-          const int64_t v0 = b0 + lane;
-          V v[U];
+  }
+  // Every lane's stores of the batch, then one increment per unit on its source's counter.
+  __threadfence();
+  __syncwarp();
+  if (lane == 0)
+    for (int64_t u = w0; u < units; u += nw) {
+      const int s = (int)(u / per_rank);
+      if (s != a.drop_source) atomicAdd(a.arrive + (int64_t)j * g.N + s, 1u);
+    }
+}
+
+// Copies this warp's (pair, column chunk) units of batch j, from unit index `from` on, into
+// the grouped rows once their source's batch has landed. quick: a wait that runs out stops
+// the batch there; returns the unit index to resume from (or a value >= units when done).
+template <bool FP8, typename V>
+__device__ __forceinline__ int64_t recv_batch(const Geo& g, const SplitArgs& a, int j, int64_t from, int64_t nw,
+                                              int lane, bool quick) {
+  constexpr int W = (int)sizeof(V);
+  constexpr int U = 8;
+  const int64_t nel = g.B / W;
+  const int64_t cv = (nel + a.chunks - 1) / a.chunks;
+  const int64_t split = g.H / W;   // fp8: codes are vectors [0, split), scales the rest
+  const int lo = batch_lo(g, a.nb, j), nt = batch_lo(g, a.nb, j + 1) - lo;
+  const int64_t per_rank = (int64_t)nt * g.R * a.chunks;
+  const int64_t units = (int64_t)g.N * per_rank;
+  const uint32_t target = (uint32_t)nt * (uint32_t)a.chunks;
+  int ready_s = -1;
+  for (int64_t u = from; u < units; u += nw) {
+    const int s = (int)(u / per_rank);
+    const int64_t r = u - s * per_rank;
+    const int64_t q = ((int64_t)s * g.T + lo) * g.R + r / a.chunks;
+    const int64_t v_lo = (r % a.chunks) * cv;
+    const int64_t v_hi = v_lo + cv < nel ? v_lo + cv : nel;
+    const int gl = __ldg(a.gslot + q);
+    const int gr = __ldg(a.grecv + q);
+    if (gl < 0) continue;
+    if (s != ready_s) {
+      bool ok = true;
+      if (lane == 0) ok = wait_arrival(a.arrive + (int64_t)j * g.N + s, target, a.abort, a.status, quick);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      __syncwarp();   // orders every lane's loads below after lane 0's acquire
+      if (!ok) {
+        if (quick) return u;   // resume here later
+        continue;              // timed out: the row stays unwritten
+      }
+      ready_s = s;
+    }
+    const uint8_t* src = a.recv + (int64_t)gr * g.B;
+    for (int64_t b0 = v_lo; b0 < v_hi; b0 += 32 * U) {
+      const int64_t v0 = b0 + lane;
+      V v[U];
 #pragma unroll
-          for (int k = 0; k < U; ++k)
-            if (v0 + 32 * k < v_hi) v[k] = ldv_l2<V>(src + (v0 + 32 * k) * W);
+      for (int k = 0; k < U; ++k)
+        if (v0 + 32 * k < v_hi) v[k] = ldv_l2<V>(src + (v0 + 32 * k) * W);
 #pragma unroll
-          for (int k = 0; k < U; ++k) {
-            const int64_t e = v0 + 32 * k;
-            if (e >= v_hi) continue;
-            if (FP8) {
-              if (e < split)
-                stv(a.ex + (int64_t)gl * g.H + e * W, v[k]);
-              else
-                stv(a.exs + (int64_t)gl * (g.H / 32) + (e - split) * W, v[k]);
-            } else {
-              stv(a.ex + (int64_t)gl * g.B + e * W, v[k]);
-            }
-          }
+      for (int k = 0; k < U; ++k) {
+        const int64_t e = v0 + 32 * k;
+        if (e >= v_hi) continue;
+        if (FP8) {
+          if (e < split)
+            stv(a.ex + (int64_t)gl * g.H + e * W, v[k]);
+          else
+            stv(a.exs + (int64_t)gl * (g.H / 32) + (e - split) * W, v[k]);
+        } else {
+          stv(a.ex + (int64_t)gl * g.B + e * W, v[k]);
         }
       }
     }
   }
+  return units;
+}
+
+template <bool FP8, typename V>
+__global__ void __launch_bounds__(kSplitThreads, 2) k_dispatch_split(Geo g, SplitArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  // Units of batch j go to warps from a rotating start, so the pushes of successive batches
+  // fall on different warps.
+  auto mine = [&](int j) { return (w0 + (int64_t)j * 977) % nw; };
+  int64_t resume[kMaxSplitBatches];
+  uint32_t left = 0;   // batches with units left for the second pass
+  send_batch<V>(g, a, 0, mine(0), nw, lane);
+  for (int j = 0; j < a.nb; ++j) {
+    if (j + 1 < a.nb) send_batch<V>(g, a, j + 1, mine(j + 1), nw, lane);
+    const int64_t at = recv_batch<FP8, V>(g, a, j, mine(j), nw, lane, true);
+    const int lo = batch_lo(g, a.nb, j), nt = batch_lo(g, a.nb, j + 1) - lo;
+    if (at < (int64_t)g.N * nt * g.R * a.chunks) {
+      resume[j] = at;
+      left |= 1u << j;
+    }
+  }
+  // Every push of this warp is out; finish what the short waits left.
+  for (int j = 0; j < a.nb; ++j)
+    if (left & (1u << j)) recv_batch<FP8, V>(g, a, j, resume[j], nw, lane, false);
 
   // The last CTA to finish zeroes the arrival counters for the next call.
   __shared__ int is_last;
@@ -280,19 +306,10 @@ cudaError_t launch_dispatch_split(const Geo& g, const moe_layout_t* lay, const v
   a.status = lay->status;
   a.drop_source = drop_source;
   const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
-  // Receive units are half rows for rows of 8 KB and more (one row otherwise); a send unit
-  // writes its chunk R times, so token rows are cut into about R times as many chunks, which
-  // gives the senders about as many units per batch as the receivers (at least 32 vectors a
-  // chunk: one per lane).
-  const int64_t nvec = g.B / (g.B % 16 == 0 ? 16 : 4);
-  a.recv_chunks = (g.B >= 8192 && nvec >= 64) ? 2 : 1;
-  int64_t sc = (int64_t)a.recv_chunks * g.R;
-  if (sc > nvec / 32) sc = nvec / 32;
-  a.send_chunks = sc < 1 ? 1 : (int)sc;
+  // Units are row chunks of about 4 KB: one round of eight vectors per lane.
+  a.chunks = (int)((g.B + 4095) / 4096);
   a.nb = lay->batches > 0 ? (lay->batches < kMaxSplitBatches ? lay->batches : kMaxSplitBatches) : split_batches(g);
   if (a.nb > g.T) a.nb = g.T < 1 ? 1 : g.T;
-  int senders = (int)((2 * kSplitWarps * ((int64_t)g.R + 1) + (3 * (int64_t)g.R + 1)) / (2 * (3 * (int64_t)g.R + 1)));
-  a.senders = senders < 1 ? 1 : (senders > kSplitWarps - 1 ? kSplitWarps - 1 : senders);
   if ((int64_t)g.N * g.T == 0) return cudaSuccess;
   LaunchScope ls(c, MOE_K_DISPATCH_SPLIT);
   if (g.B % 16 == 0)
