@@ -14,21 +14,24 @@
 // launch (all CTAs resident). A sender uses only its own routing (cnt[s][.], soff[s][.] and
 // its pairs' send positions pos); a receiver computes its offsets only from the counts the
 // senders piggybacked. Work items, taken by every warp in this order:
-//  A. for each (receiver d, sender s): the counts of d's experts, meta[d][s][l] =
-//     cnt[s][d*L + l], then mflag[d][s] (release); for each token: its pairs whose place j
-//     in the slice (d, s) is below K go to ded[d][s][j], each row signalled on arrive[d][s];
+//  M. for each (receiver d, sender s): the counts of d's experts, meta[d][s][l] =
+//     cnt[s][d*L + l], then mflag[d][s] (release);
 //  P. for each receiver d: wait for every sender's counts (mflag), then C[s][d], the shared
 //     region's offsets moff[d][s] = sum over s' < s of max(C[s'][d] - K, 0), the grouped
 //     offsets eoffx[d][l][s] = sum over s' < s of meta[d][s'][l] and the slice-local
 //     expert offsets spre[d][s][l]; then pflag[d] (release);
-//  B. for each token: its pairs with j >= K wait for pflag[d] and go to
-//     main[d][moff[d][s] + j - K], each row signalled on arrive[d][s];
-//  C. for each item (groups of 8 places j of a slice (d, s) below its row count C[s][d],
-//     from the reported counts): wait for pflag[d] and the slice's C[s][d] rows, find each row's
-//     expert l from spre (the receiver never reads the senders' routing arrays), and copy
-//     the row from the dedicated or the shared region to grouped row
-//     eoffx[d][l][s] + j - spre[d][s][l] (dropped at or beyond cap).
-// A wait depends only on items of earlier letters, and items of A never wait, so every wait
+//  S. for each (token, column chunk of about 4 KB), one lane per pair: a pair whose place j
+//     in the slice (d, s) is below K goes to ded[d][s][j] at once; the others wait for
+//     pflag[d] and go to main[d][moff[d][s] + j - K]; each chunk is read once and stored R
+//     times; once it has landed (one fence), each lane signals its row chunk on arrive[d][s]
+//     (a slice is complete at C[s][d] x chunks);
+//  C. for each item (a group of 8 places j of a slice (d, s) below its row count C[s][d],
+//     from the reported counts, and a column chunk of about 4 KB): wait for pflag[d] and the
+//     slice's C[s][d] rows; lanes 0..7 find their row's expert l from spre (the receiver
+//     never reads the senders' routing arrays) and its grouped row eoffx[d][l][s] + j -
+//     spre[d][s][l] (dropped at or beyond cap); the warp copies the chunk of each of the 8
+//     rows from the dedicated or the shared region.
+// A wait depends only on items of earlier letters, and items of M never wait, so every wait
 // ends unless a signal is missing (withheld for a test); then the status word gets the
 // timeout bit, later waits of the call give up at once, and their rows are skipped. The
 // flags and counters are zeroed on the stream before each launch.
@@ -42,6 +45,7 @@ namespace {
 constexpr uint64_t kDedWaitNs = 1000000000ull;   // 1 s
 constexpr int kDedThreads = 256;
 constexpr int kRowsPerItem = 8;   // receive rows one warp item handles
+constexpr int64_t kItemBytes = 4096;   // column chunk of a receive item
 
 struct DedArgs {
   const uint8_t* x;       // [N][T][B] token rows
@@ -60,7 +64,7 @@ struct DedArgs {
   int32_t* spre;          // [N][N][L]
   uint32_t* mflag;        // [N][N]
   uint32_t* pflag;        // [N]
-  uint32_t* arrive;       // [N][N]
+  uint32_t* arrive;       // [N][N]: row chunks of slice (d, s) landed, at d*N + s
   uint32_t* abort;        // a wait of this call timed out
   int32_t* status;
   int K;
@@ -77,10 +81,13 @@ __device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Waits until *ctr >= target, bounded like the split-phase waits.
+// Waits until *ctr >= target, bounded like the split-phase waits. The polls back off from
+// 256 ns to 4 us, so that thousands of waiting warps leave the counters' lines to the
+// senders' increments.
 __device__ __forceinline__ bool wait_at_least(const uint32_t* ctr, uint32_t target, uint32_t* abort, int32_t* status) {
   if (ld_acquire(ctr) >= target) return true;
   const uint64_t t0 = global_ns();
+  unsigned nap = 256;
   while (true) {
     if (ld_acquire(ctr) >= target) return true;
     if (*reinterpret_cast<volatile uint32_t*>(abort)) return false;
@@ -89,7 +96,8 @@ __device__ __forceinline__ bool wait_at_least(const uint32_t* ctr, uint32_t targ
       set_status(status, kBitTimeout);
       return false;
     }
-    __nanosleep(256);
+    __nanosleep(nap);
+    if (nap < 4096) nap <<= 1;
   }
 }
 
@@ -121,60 +129,60 @@ __device__ __forceinline__ void st_v(uint8_t* p, const uint4& v) { st16(p, v); }
 __device__ __forceinline__ void st_v(uint8_t* p, const uint32_t& v) { *reinterpret_cast<uint32_t*>(p) = v; }
 
 
-// Sends the pairs of one token that belong to this phase (DEDICATED: slice place j < K, into
-// the dedicated rows; else j >= K, into the shared region once the receiver's offsets are
-// ready), then signals each landed row on its slice. Lane k handles pair k (R <= 32).
-template <typename V, bool DEDICATED>
-__device__ __forceinline__ void send_token(const Geo& g, const DedArgs& a, int64_t tok, int lane) {
+// Sends the column chunk [v_lo, v_hi) (in vectors) of token tok, lane k holding pair k: a
+// place j < K in its slice goes to the dedicated rows, the rest to the shared region once the
+// receiver's offsets are out. The chunk is read once and stored to its pairs' rows; after
+// one fence every lane with a row signals the chunk on its slice.
+template <typename V>
+__device__ __forceinline__ void send_unit(const Geo& g, const DedArgs& a, int64_t tok, int64_t v_lo, int64_t v_hi,
+                                          int lane) {
   constexpr int W = (int)sizeof(V);
   constexpr int U = 8;
-  const int s = (int)(tok / g.T);
   uint8_t* myrow = nullptr;
   int myslice = -1;
   if (lane < g.R) {
+    const int s = (int)(tok / g.T);
     const int64_t q = tok * g.R + lane;
     const int e = __ldg(a.idx + q);
     if (e >= 0 && e < g.E) {
       const int d = e / g.L;
       const int j = __ldg(a.pos + q) - __ldg(a.soff + (int64_t)s * g.E + d * g.L);   // place in the slice
       const int slice = d * g.N + s;
-      if (DEDICATED) {
-        if (j < a.K) {
-          myrow = a.ded + ((int64_t)slice * a.K + j) * g.B;
-          myslice = slice;
-        }
-      } else if (j >= a.K && wait_at_least(a.pflag + d, 1u, a.abort, a.status)) {
+      if (j < a.K) {
+        myrow = a.ded + ((int64_t)slice * a.K + j) * g.B;
+        myslice = slice;
+      } else if (wait_at_least(a.pflag + d, 1u, a.abort, a.status)) {
         myrow = a.main + ((int64_t)d * g.RB + __ldcg(a.moff + slice) + (j - a.K)) * g.B;
         myslice = slice;
       }
     }
   }
   const unsigned any = __ballot_sync(0xffffffffu, myrow != nullptr);
-  if (!any) return;
-  const uint8_t* src = a.x + tok * g.B;
-  const int64_t nel = g.B / W;
-  for (int64_t b0 = 0; b0 < nel; b0 += 32 * U) {   // same trip count on every lane
-    const int64_t v0 = b0 + lane;
-    V r[U];
-#pragma unroll
-    for (int j = 0; j < U; ++j)
-      if (v0 + 32 * j < nel) r[j] = ld_nc<V>(src + (v0 + 32 * j) * W);
-#pragma unroll 1
-    for (int k = 0; k < g.R; ++k) {
-      if (!((any >> k) & 1u)) continue;
-      uint8_t* dst = reinterpret_cast<uint8_t*>(
-          __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(myrow), k));
+  if (any) {
+    const uint8_t* src = a.x + tok * g.B;
+    for (int64_t b0 = v_lo; b0 < v_hi; b0 += 32 * U) {   // same trip count on every lane
+      const int64_t v0 = b0 + lane;
+      V r[U];
 #pragma unroll
       for (int j = 0; j < U; ++j)
-        if (v0 + 32 * j < nel) st_v(dst + (v0 + 32 * j) * W, r[j]);
+        if (v0 + 32 * j < v_hi) r[j] = ld_nc<V>(src + (v0 + 32 * j) * W);
+#pragma unroll 1
+      for (int k = 0; k < g.R; ++k) {
+        if (!((any >> k) & 1u)) continue;
+        uint8_t* dst = reinterpret_cast<uint8_t*>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(myrow), k));
+#pragma unroll
+        for (int j = 0; j < U; ++j)
+          if (v0 + 32 * j < v_hi) st_v(dst + (v0 + 32 * j) * W, r[j]);
+      }
     }
   }
   __threadfence();
   __syncwarp();
-  if (myrow && myslice != a.drop_slice) {
-    __threadfence();
-    atomicAdd(a.arrive + myslice, 1u);
-  }
+  // One increment per slice: lanes whose rows share a slice add their count together.
+  const int key = (myrow && myslice != a.drop_slice) ? myslice : -1;
+  const unsigned same = __match_any_sync(0xffffffffu, key);
+  if (key >= 0 && lane == __ffs(same) - 1) atomicAdd(a.arrive + key, (unsigned)__popc(same));
 }
 
 // Largest i in [0, n) with v[i] <= key (v ascending, v[0] <= key).
@@ -200,7 +208,7 @@ __global__ void __launch_bounds__(kDedThreads) k_dispatch_dedicated(Geo g, DedAr
   const int N = g.N, L = g.L;
   const int64_t tokens = (int64_t)N * g.T;
 
-  // ---- A: the routing information, then the dedicated rows
+  // ---- M: the routing information
   for (int64_t it = warp0; it < (int64_t)N * N; it += nwarps) {   // it = d*N + s
     const int d = (int)(it / N), s = (int)(it - (int64_t)d * N);
     for (int l = lane; l < L; l += 32) a.meta[it * L + l] = __ldg(a.cnt + (int64_t)s * g.E + d * L + l);
@@ -208,7 +216,6 @@ __global__ void __launch_bounds__(kDedThreads) k_dispatch_dedicated(Geo g, DedAr
     __syncwarp();
     if (lane == 0) st_release(a.mflag + it, 1u);
   }
-  for (int64_t tok = warp0; tok < tokens; tok += nwarps) send_token<V, true>(g, a, tok, lane);
 
   // ---- P: each receiver's offsets from the counts its senders reported
   for (int64_t d = warp0; d < N; d += nwarps) {
@@ -255,60 +262,81 @@ __global__ void __launch_bounds__(kDedThreads) k_dispatch_dedicated(Geo g, DedAr
     if (lane == 0) st_release(a.pflag + d, 1u);
   }
 
-  // ---- B: the rows past the dedicated space, into the shared region
-  for (int64_t tok = warp0; tok < tokens; tok += nwarps) send_token<V, false>(g, a, tok, lane);
-
-  // ---- C: receive: items of up to kRowsPerItem rows of one slice (d, s), each into its
-  // expert's grouped row
   const int64_t nel = g.B / W;
-  // Items per slice: enough for an average slice (P / N^2 rows) in groups of kRowsPerItem;
-  // item m of a slice takes the row groups m, m + per_slice, ... so a long (skewed) slice is
-  // still covered.
+  const int chunks = (int)((g.B + kItemBytes - 1) / kItemBytes);   // column chunks of a row
+  const int64_t cv = (nel + chunks - 1) / chunks;
+
+  // ---- S: every token row chunk once, to its dedicated and shared-region rows
+  for (int64_t u = warp0; u < tokens * chunks; u += nwarps) {
+    const int64_t tok = u / chunks, v_lo = (u - tok * chunks) * cv;
+    send_unit<V>(g, a, tok, v_lo, v_lo + cv < nel ? v_lo + cv : nel, lane);
+  }
+
+  // ---- C: receive: items of up to kRowsPerItem places of one slice (d, s) and one column
+  // chunk, each row chunk into its expert's grouped row
+  const int64_t split = g.H / W;   // fp8: codes are vectors [0, split), scales the rest
+  // Row groups per slice: enough for an average slice (P / N^2 rows); group m of a slice
+  // takes the places m, m + per_slice, ... (in steps of kRowsPerItem rows), so a long
+  // (skewed) slice is still covered.
   int64_t per_slice = (g.P + (int64_t)N * N * kRowsPerItem - 1) / ((int64_t)N * N * kRowsPerItem);
   const int64_t most = (g.TR + kRowsPerItem - 1) / kRowsPerItem;   // a slice has <= T*R rows
   per_slice = per_slice < 1 ? 1 : (per_slice > most ? most : per_slice);
-  for (int64_t it = warp0; it < (int64_t)N * N * per_slice; it += nwarps) {
-    const int slice = (int)(it / per_slice);
+  const int64_t items = (int64_t)N * N * per_slice * chunks;
+  for (int64_t it = warp0; it < items; it += nwarps) {
+    const int64_t sg = it / chunks;
+    const int ch = (int)(it - sg * chunks);
+    const int slice = (int)(sg / per_slice);
     const int d = slice / N, s = slice - d * N;
-    const int j0 = (int)(it - (int64_t)slice * per_slice) * kRowsPerItem;
+    const int j0 = (int)(sg - (int64_t)slice * per_slice) * kRowsPerItem;
     bool ok = lane == 0 ? wait_at_least(a.pflag + d, 1u, a.abort, a.status) : false;
     ok = __shfl_sync(0xffffffffu, ok, 0);
     __syncwarp();
     if (!ok) continue;
     const int c = __ldcg(a.cx + slice);   // rows of the slice, from the reported counts
     if (j0 >= c) continue;
-    ok = lane == 0 ? wait_at_least(a.arrive + slice, (uint32_t)c, a.abort, a.status) : false;
+    ok = lane == 0 ? wait_at_least(a.arrive + slice, (uint32_t)c * (uint32_t)chunks, a.abort, a.status) : false;
     ok = __shfl_sync(0xffffffffu, ok, 0);
     __syncwarp();
     if (!ok) continue;
     const int moff = __ldcg(a.moff + slice);
-    for (int jg = j0; jg < c; jg += (int)per_slice * kRowsPerItem)
-    for (int jj = 0; jj < kRowsPerItem && jg + jj < c; ++jj) {
-      const int j = jg + jj;
-      const int l = last_at_most(a.spre + (int64_t)slice * L, L, j);   // the slice is expert-major
-      const int slot = __ldcg(a.eoffx + ((int64_t)d * L + l) * N + s) + j - __ldcg(a.spre + (int64_t)slice * L + l);
-      if (slot >= g.cap) continue;   // dropped for capacity
-      const int64_t gl = ((int64_t)d * L + l) * g.cap + slot;
-      const uint8_t* src = j < a.K ? a.ded + ((int64_t)slice * a.K + j) * g.B
-                                   : a.main + ((int64_t)d * g.RB + moff + (j - a.K)) * g.B;
-      for (int64_t b0 = 0; b0 < nel; b0 += 32 * U) {
-        const int64_t v0 = b0 + lane;
-        V r[U];
+    const int64_t v_lo = ch * cv, v_hi = v_lo + cv < nel ? v_lo + cv : nel;
+    for (int jg = j0; jg < c; jg += (int)per_slice * kRowsPerItem) {
+      // lanes 0 .. kRowsPerItem-1: place jg + lane's expert, grouped row and source row
+      const uint8_t* mysrc = nullptr;
+      int64_t mygl = -1;
+      if (lane < kRowsPerItem && jg + lane < c) {
+        const int j = jg + lane;
+        const int l = last_at_most(a.spre + (int64_t)slice * L, L, j);   // the slice is expert-major
+        const int slot = __ldcg(a.eoffx + ((int64_t)d * L + l) * N + s) + j - __ldcg(a.spre + (int64_t)slice * L + l);
+        if (slot < g.cap) {   // else dropped for capacity
+          mygl = ((int64_t)d * L + l) * g.cap + slot;
+          mysrc = j < a.K ? a.ded + ((int64_t)slice * a.K + j) * g.B
+                          : a.main + ((int64_t)d * g.RB + moff + (j - a.K)) * g.B;
+        }
+      }
+      for (int rr = 0; rr < kRowsPerItem; ++rr) {
+        const int64_t gl = __shfl_sync(0xffffffffu, mygl, rr);
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mysrc), rr));
+        if (gl < 0) continue;
+        for (int64_t b0 = v_lo; b0 < v_hi; b0 += 32 * U) {
+          const int64_t v0 = b0 + lane;
+          V r[U];
 #pragma unroll
-        for (int k = 0; k < U; ++k)
-          if (v0 + 32 * k < nel) r[k] = ld_l2<V>(src + (v0 + 32 * k) * W);
+          for (int k = 0; k < U; ++k)
+            if (v0 + 32 * k < v_hi) r[k] = ld_l2<V>(src + (v0 + 32 * k) * W);
 #pragma unroll
-        for (int k = 0; k < U; ++k) {
-          const int64_t v = v0 + 32 * k;
-          if (v >= nel) continue;
-          if (FP8) {   // codes [0, H), then the scales
-            const int64_t split = g.H / W;
-            if (v < split)
-              st_v(a.ex + gl * g.H + v * W, r[k]);
-            else
-              st_v(a.exs + gl * (g.H / 32) + (v - split) * W, r[k]);
-          } else {
-            st_v(a.ex + gl * g.B + v * W, r[k]);
+          for (int k = 0; k < U; ++k) {
+            const int64_t v = v0 + 32 * k;
+            if (v >= v_hi) continue;
+            if (FP8) {
+              if (v < split)
+                st_v(a.ex + gl * g.H + v * W, r[k]);
+              else
+                st_v(a.exs + gl * (g.H / 32) + (v - split) * W, r[k]);
+            } else {
+              st_v(a.ex + gl * g.B + v * W, r[k]);
+            }
           }
         }
       }
