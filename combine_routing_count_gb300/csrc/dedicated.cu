@@ -44,7 +44,7 @@ namespace {
 
 constexpr uint64_t kDedWaitNs = 1000000000ull;   // 1 s
 constexpr int kDedThreads = 256;
-constexpr int kRowsPerItem = 8;   // receive rows one warp item handles
+constexpr int kRowsPerItem = 4;   // receive rows one warp item handles
 constexpr int64_t kItemBytes = 4096;   // column chunk of a receive item
 
 struct DedArgs {
@@ -199,7 +199,7 @@ __device__ __forceinline__ int last_at_most(const int32_t* v, int n, int key) {
 }
 
 template <bool FP8, typename V>
-__global__ void __launch_bounds__(kDedThreads) k_dispatch_dedicated(Geo g, DedArgs a) {
+__global__ void __launch_bounds__(kDedThreads, 2) k_dispatch_dedicated(Geo g, DedArgs a) {
   constexpr int W = (int)sizeof(V);
   constexpr int U = 8;
   const int lane = threadIdx.x & 31;
