@@ -587,8 +587,10 @@ def measure(wl, args, dist, device, peak: float, peak_kind: str, cpu_seconds: fl
             kernels[name]["dram_frac"] = None if db is None else round(db / (us_c * 1e-6) / 1e9 / peak, 3)
     dom = max(kernels, key=lambda k: kernels[k]["us"] * kernels[k]["launches_per_step"])
     step_bytes = sum(ab[k] * kernels[k]["launches_per_step"] for k in kernels)
-    warm_pass = [scaled_dram(table, "warm_l2", k, P) for k in kernels]
-    dram_step = None if (not warm_pass or any(v is None for v in warm_pass)) else sum(warm_pass)
+    # DRAM bytes of the one-batch pass: its data kernels' captures (the layout kernels move
+    # well under 1 MB and have none)
+    captured = [k for k in kernels if table and k in table.get("warm_l2", {})]
+    dram_step = sum(scaled_dram(table, "warm_l2", k, P) for k in captured) if captured else None
 
     # The same step in direct-push mode (the pack writes into the owners' receive rows and
     # the combine send into the sources' rows, fusing away both per-peer write steps).
