@@ -48,7 +48,7 @@ class MoeProf(ctypes.Structure):
 class MoeLayout(ctypes.Structure):
     _fields_ = [(f, c_void_p) for f in LAYOUT_FIELDS] + [
         ("flags", c_uint32), ("prof", POINTER(MoeProf)), ("tma_stages", c_int32), ("ctas_per_sm", c_int32),
-        ("batches", c_int32)]
+        ("batches", c_int32), ("win_lo", c_int32), ("win_hi", c_int32)]
 
 
 BUFFER_FIELDS = ("x", "xq", "idx", "w", "send", "recv", "expert_x", "expert_scale", "expert_y", "csend",
@@ -57,6 +57,10 @@ BUFFER_FIELDS = ("x", "xq", "idx", "w", "send", "recv", "expert_x", "expert_scal
 
 class MoeBuffers(ctypes.Structure):
     _fields_ = [(f, c_void_p) for f in BUFFER_FIELDS]
+
+
+class MoeSlice(ctypes.Structure):
+    _fields_ = [("peer", c_int32), ("s", c_int32), ("d", c_int32), ("rows", c_int32), ("local_row", ctypes.c_int64)]
 
 
 _lib = None
@@ -105,6 +109,8 @@ def lib():
             "moe_forward": (c_int32, [D, Lp, B, c_void_p]),
             "moe_forward_host": (c_int32, [D, Lp, B, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
             "moe_batches": (c_int32, [D, Lp, c_int32]),
+            "moe_exchange_plan": (ctypes.c_int64, [D, c_void_p, c_void_p, c_void_p, c_int32, c_void_p, c_int32,
+                                                   c_int32, c_int32, POINTER(MoeSlice), ctypes.c_int64]),
             "moe_status_sync": (c_int32, [Lp, c_void_p, POINTER(c_uint32)]),
             "moe_status_string": (c_char_p, [c_int32]),
             "moe_launch_count": (c_uint64, []),
@@ -133,5 +139,6 @@ EXPORTED = ("moe_check_dims", "moe_recv_capacity_rows", "moe_row_bytes", "moe_ca
             "moe_dedicated_exchange_bytes", "moe_dispatch_dedicated", "moe_dispatch_recv",
             "moe_expert_identity", "moe_combine_send", "moe_combine_recv", "moe_dispatch", "moe_combine",
             "moe_combine_send_partial",
-            "moe_combine_recv_partial", "moe_forward", "moe_forward_host", "moe_batches", "moe_status_sync",
+            "moe_combine_recv_partial", "moe_forward", "moe_forward_host", "moe_batches", "moe_exchange_plan",
+            "moe_status_sync",
             "moe_status_string", "moe_launch_count")

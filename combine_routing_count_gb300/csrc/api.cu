@@ -197,6 +197,8 @@ moe_status make_ctx(const moe_layout_t* lay, void* stream, Ctx& c) {
   c.tma_stages = lay->tma_stages;
   c.ctas_per_sm = lay->ctas_per_sm;
   c.status = lay->status;
+  c.win_lo = lay->win_lo;
+  c.win_hi = lay->win_hi;
   return MOE_OK;
 }
 
@@ -213,6 +215,22 @@ bool layout_ok(const moe_layout_t* l) {
 namespace {
 
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// The layout's rank window: valid (0, 0 or 0 <= lo < hi <= N) and whether it is smaller than
+// the group.
+bool window_valid(const Geo& g, const moe_layout_t* l) {
+  if (l->win_lo == 0 && l->win_hi == 0) return true;
+  return l->win_lo >= 0 && l->win_lo < l->win_hi && l->win_hi <= g.N;
+}
+bool window_partial(const Geo& g, const moe_layout_t* l) {
+  return l->win_hi > 0 && !(l->win_lo == 0 && l->win_hi == g.N);
+}
+// Entry points that work on the whole group only.
+bool whole_group(const Geo& g, const moe_layout_t* l) { return l && window_valid(g, l) && !window_partial(g, l); }
+// Entry points that accept a rank window: valid, and no direct push with a partial one.
+bool window_ok(const Geo& g, const moe_layout_t* l) {
+  return l && window_valid(g, l) && !(window_partial(g, l) && (l->flags & MOE_FLAG_DIRECT_PUSH));
+}
 
 // Byte sizes of the workspace arrays, in carving order.
 struct WsPlan {
@@ -594,6 +612,8 @@ moe_status moe_layout_init(const moe_dims* dims, void* d_ws, size_t ws_bytes, mo
   out->tma_stages = 0;
   out->ctas_per_sm = 0;
   out->batches = 0;
+  out->win_lo = 0;
+  out->win_hi = 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(out->status, 0, 64, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemsetAsync(out->scratch + layout_scratch_done_offset(g), 0, 4 * (size_t)g.N, s) != cudaSuccess)
@@ -619,6 +639,7 @@ moe_status moe_quantize_fp8_b128(const moe_dims* dims, const uint16_t* d_x, uint
   Geo g;
   moe_status st = make_geo(dims, g);
   if (st != MOE_OK) return st;
+  if (!window_ok(g, lay)) return MOE_ERR_INVALID_ARG;
   if ((int64_t)g.N * g.T == 0) return layout_ok(lay) ? MOE_OK : MOE_ERR_INVALID_ARG;  // nothing to move
   if (g.payload != MOE_PAYLOAD_FP8_E4M3_B128 || !layout_ok(lay) || !d_x || !d_xq || !aligned16(d_x) ||
       !aligned16(d_xq))
@@ -633,6 +654,7 @@ moe_status moe_dispatch_send(const moe_dims* dims, const moe_layout_t* lay, cons
   Geo g;
   moe_status st = make_geo(dims, g);
   if (st != MOE_OK) return st;
+  if (!window_ok(g, lay)) return MOE_ERR_INVALID_ARG;
   if ((int64_t)g.N * g.T == 0) return layout_ok(lay) ? MOE_OK : MOE_ERR_INVALID_ARG;  // nothing to move
   const bool push = lay && (lay->flags & MOE_FLAG_DIRECT_PUSH);
   if (!layout_ok(lay) || !d_x || !d_recv || !aligned16(d_x) || !aligned16(d_recv) ||
@@ -651,6 +673,7 @@ moe_status moe_quantize_dispatch_send(const moe_dims* dims, const moe_layout_t* 
   Geo g;
   moe_status st = make_geo(dims, g);
   if (st != MOE_OK) return st;
+  if (!window_ok(g, lay)) return MOE_ERR_INVALID_ARG;
   if (g.payload != MOE_PAYLOAD_FP8_E4M3_B128) return MOE_ERR_INVALID_ARG;
   if ((int64_t)g.N * g.T == 0) return layout_ok(lay) ? MOE_OK : MOE_ERR_INVALID_ARG;  // nothing to move
   const bool push = lay && (lay->flags & MOE_FLAG_DIRECT_PUSH);
@@ -670,6 +693,7 @@ moe_status moe_dispatch_split(const moe_dims* dims, const moe_layout_t* lay, con
   Geo g;
   moe_status st = make_geo(dims, g);
   if (st != MOE_OK) return st;
+  if (!whole_group(g, lay)) return MOE_ERR_INVALID_ARG;   // a rank window is not supported here
   if (withhold_source < -1 || withhold_source >= g.N) return MOE_ERR_INVALID_ARG;
   if ((int64_t)g.N * g.T == 0) return layout_ok(lay) ? MOE_OK : MOE_ERR_INVALID_ARG;  // nothing to move
   const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
@@ -695,6 +719,7 @@ moe_status moe_dispatch_dedicated(const moe_dims* dims, const moe_layout_t* lay,
   Geo g;
   moe_status st = make_geo(dims, g);
   if (st != MOE_OK) return st;
+  if (!whole_group(g, lay)) return MOE_ERR_INVALID_ARG;   // a rank window is not supported here
   if (K < 0 || withhold_slice < -1 || withhold_slice >= (int64_t)g.N * g.N || g.R > 32) return MOE_ERR_INVALID_ARG;
   const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
   if (!layout_ok(lay) || !d_xchg || !aligned16(d_xchg)) return MOE_ERR_INVALID_ARG;
@@ -714,6 +739,7 @@ moe_status moe_dispatch_recv(const moe_dims* dims, const moe_layout_t* lay, cons
   Geo g;
   moe_status st = make_geo(dims, g);
   if (st != MOE_OK) return st;
+  if (!window_ok(g, lay)) return MOE_ERR_INVALID_ARG;
   if ((int64_t)g.N * g.T == 0) return layout_ok(lay) ? MOE_OK : MOE_ERR_INVALID_ARG;  // nothing to move
   const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
   if (!layout_ok(lay) || !d_recv || !d_expert_x || !aligned16(d_recv) || !aligned16(d_expert_x))
@@ -729,6 +755,7 @@ moe_status moe_expert_identity(const moe_dims* dims, const moe_layout_t* lay, co
   Geo g;
   moe_status st = make_geo(dims, g);
   if (st != MOE_OK) return st;
+  if (!window_ok(g, lay)) return MOE_ERR_INVALID_ARG;
   if ((int64_t)g.N * g.T == 0) return layout_ok(lay) ? MOE_OK : MOE_ERR_INVALID_ARG;  // nothing to move
   const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
   if (!layout_ok(lay) || !d_expert_x || !d_expert_y || !aligned16(d_expert_x) || !aligned16(d_expert_y))
@@ -748,6 +775,7 @@ moe_status moe_combine_send(const moe_dims* dims, const moe_layout_t* lay, const
   Geo g;
   moe_status st = make_geo(dims, g);
   if (st != MOE_OK) return st;
+  if (!window_ok(g, lay)) return MOE_ERR_INVALID_ARG;
   if ((int64_t)g.N * g.T == 0) return layout_ok(lay) ? MOE_OK : MOE_ERR_INVALID_ARG;  // nothing to move
   const bool push = lay && (lay->flags & MOE_FLAG_DIRECT_PUSH);
   if (!layout_ok(lay) || !d_expert_y || !d_crecv || !aligned16(d_expert_y) || !aligned16(d_crecv) ||
@@ -766,6 +794,7 @@ moe_status moe_combine_recv(const moe_dims* dims, const moe_layout_t* lay, const
   Geo g;
   moe_status st = make_geo(dims, g);
   if (st != MOE_OK) return st;
+  if (!window_ok(g, lay)) return MOE_ERR_INVALID_ARG;
   if ((int64_t)g.N * g.T == 0) return layout_ok(lay) ? MOE_OK : MOE_ERR_INVALID_ARG;  // nothing to move
   if (!layout_ok(lay) || !d_crecv || !d_w || !d_out || !aligned16(d_crecv) || !aligned16(d_out))
     return MOE_ERR_INVALID_ARG;
@@ -779,6 +808,7 @@ moe_status moe_dispatch(const moe_dims* dims, const moe_layout_t* lay, const voi
   Geo g;
   moe_status st = make_geo(dims, g);
   if (st != MOE_OK) return st;
+  if (!whole_group(g, lay)) return MOE_ERR_INVALID_ARG;   // a rank window is not supported here
   if ((int64_t)g.N * g.T == 0) return layout_ok(lay) ? MOE_OK : MOE_ERR_INVALID_ARG;  // nothing to move
   const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
   const bool push = lay && (lay->flags & MOE_FLAG_DIRECT_PUSH);
@@ -798,6 +828,7 @@ moe_status moe_combine(const moe_dims* dims, const moe_layout_t* lay, const uint
   Geo g;
   moe_status st = make_geo(dims, g);
   if (st != MOE_OK) return st;
+  if (!whole_group(g, lay)) return MOE_ERR_INVALID_ARG;   // a rank window is not supported here
   if ((int64_t)g.N * g.T == 0) return layout_ok(lay) ? MOE_OK : MOE_ERR_INVALID_ARG;  // nothing to move
   const bool push = lay && (lay->flags & MOE_FLAG_DIRECT_PUSH);
   if (!layout_ok(lay) || !d_expert_y || !d_crecv || !d_w || !d_out || !aligned16(d_expert_y) ||
@@ -815,6 +846,7 @@ moe_status moe_combine_send_partial(const moe_dims* dims, const moe_layout_t* la
   Geo g;
   moe_status st = make_geo(dims, g);
   if (st != MOE_OK) return st;
+  if (!whole_group(g, lay)) return MOE_ERR_INVALID_ARG;   // a rank window is not supported here
   if ((int64_t)g.N * g.T == 0) return layout_ok(lay) ? MOE_OK : MOE_ERR_INVALID_ARG;  // nothing to move
   if (!layout_ok(lay) || !d_expert_y || !d_w || !d_cpart || !aligned16(d_expert_y) || !aligned16(d_cpart) ||
       g.R > 32)
@@ -829,6 +861,7 @@ moe_status moe_combine_recv_partial(const moe_dims* dims, const moe_layout_t* la
   Geo g;
   moe_status st = make_geo(dims, g);
   if (st != MOE_OK) return st;
+  if (!whole_group(g, lay)) return MOE_ERR_INVALID_ARG;   // a rank window is not supported here
   if ((int64_t)g.N * g.T == 0) return layout_ok(lay) ? MOE_OK : MOE_ERR_INVALID_ARG;  // nothing to move
   if (!layout_ok(lay) || !d_cpart || !d_out || !aligned16(d_cpart) || !aligned16(d_out) || g.R > 32)
     return MOE_ERR_INVALID_ARG;
@@ -844,7 +877,7 @@ moe_status moe_forward(const moe_dims* dims, const moe_layout_t* lay, const moe_
   if (st != MOE_OK) return st;
   const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
   // Every buffer is checked before anything is launched (an empty batch needs none).
-  if (!layout_ok(lay)) return MOE_ERR_INVALID_ARG;
+  if (!layout_ok(lay) || !whole_group(g, lay)) return MOE_ERR_INVALID_ARG;
   if ((int64_t)g.N * g.T > 0 &&
       (!pass_buffers_ok(b, lay->flags, fp8, true) ||
        (fp8 && (lay->flags & MOE_FLAG_STAGED_QUANT) && (!b->xq || !aligned16(b->xq)))))
@@ -879,7 +912,7 @@ moe_status moe_forward_host(const moe_dims* dims, const moe_layout_t* lay, const
   const size_t xb = (size_t)g.N * g.T * g.H * 2, pb = (size_t)g.P * 4;
   if ((xb && (!h_x || !h_out || !b->x || !b->out)) || (pb && (!h_idx || !h_w || !b->idx || !b->w)))
     return MOE_ERR_INVALID_ARG;
-  if (!layout_ok(lay)) return MOE_ERR_INVALID_ARG;
+  if (!layout_ok(lay) || !whole_group(g, lay)) return MOE_ERR_INVALID_ARG;
   if (lay->flags & MOE_FLAG_HOST_MAPPED) {
     // Device-accessible host memory: run the pass on it directly.
     void *dx = nullptr, *didx = nullptr, *dw = nullptr, *dout = nullptr;
@@ -903,6 +936,50 @@ moe_status moe_forward_host(const moe_dims* dims, const moe_layout_t* lay, const
   if ((st = moe_forward(dims, lay, b, stream)) != MOE_OK) return st;
   if (xb && cudaMemcpyAsync(h_out, b->out, xb, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+int64_t moe_exchange_plan(const moe_dims* dims, const int32_t* h_C, const int32_t* h_soff, const int32_t* h_roff,
+                          int32_t nwin, const int32_t* h_bounds, int32_t me, int32_t direction, int32_t sending,
+                          moe_slice_t* out, int64_t max_out) {
+  Geo g;
+  if (make_geo(dims, g) != MOE_OK || !h_bounds || nwin < 1 || me < 0 || me >= nwin || direction < 0 ||
+      direction > 1 || sending < 0 || sending > 1 || max_out < 0)
+    return -1;
+  if (h_bounds[0] != 0 || h_bounds[nwin] != g.N) return -1;
+  for (int w = 0; w < nwin; ++w)
+    if (h_bounds[w] > h_bounds[w + 1]) return -1;
+  const int N = g.N, L = g.L;
+  if ((int64_t)N * g.T > 0 && (!h_C || !h_soff || !h_roff)) return -1;
+  const int lo = h_bounds[me], hi = h_bounds[me + 1];
+  // window of each rank
+  std::vector<int32_t> win(N);
+  for (int w = 0; w < nwin; ++w)
+    for (int r = h_bounds[w]; r < h_bounds[w + 1]; ++r) win[r] = w;
+  int64_t n = 0;
+  if ((int64_t)N * g.T == 0) return 0;
+  for (int s = 0; s < N; ++s)
+    for (int d = 0; d < N; ++d) {
+      const bool s_in = s >= lo && s < hi, d_in = d >= lo && d < hi;
+      if (s_in == d_in) continue;   // inside the window (moved by the kernels) or not ours
+      const int32_t rows = h_C[(int64_t)s * N + d];
+      if (rows <= 0) continue;
+      // Dispatch moves s -> d, combine d -> s: the side that sends is the one holding the
+      // rows before the move.
+      const bool mine_sends = direction == 0 ? s_in : d_in;
+      if ((sending != 0) != mine_sends) continue;
+      if (out && n < max_out) {
+        moe_slice_t& sl = out[n];
+        sl.peer = s_in ? win[d] : win[s];
+        sl.s = s;
+        sl.d = d;
+        sl.rows = rows;
+        const int64_t send_side = (int64_t)(s - lo) * g.TR + h_soff[(int64_t)s * g.E + (int64_t)d * L];
+        const int64_t recv_side = (int64_t)(d - lo) * g.RB + h_roff[(int64_t)d * N + s];
+        sl.local_row = s_in ? send_side : recv_side;
+      }
+      ++n;
+    }
+  return n;
 }
 
 int32_t moe_batches(const moe_dims* dims, const moe_layout_t* lay, int32_t which) {

@@ -22,7 +22,19 @@ struct Ctx {
   int tma_stages;     // 0 = automatic
   int ctas_per_sm;    // 0 = automatic
   int32_t* status;
+  int win_lo, win_hi; // rank window of the layout (0, 0: the whole group)
 };
+
+// True when the call works on a rank window smaller than the group (see moe_layout_t).
+inline bool windowed(const Geo& g, const Ctx& c) { return c.win_hi > 0 && !(c.win_lo == 0 && c.win_hi == g.N); }
+
+// A device pointer moved back by `bytes`: the base of a window-local buffer seen as a whole-
+// group buffer, so that whole-group row indices of the window's ranks land in it. Only rows
+// of the window are ever accessed through it.
+template <typename P>
+inline P rebase(P p, int64_t bytes) {
+  return p ? reinterpret_cast<P>(reinterpret_cast<uintptr_t>(p) - (uintptr_t)bytes) : p;
+}
 
 extern std::atomic<uint64_t> g_launches;
 

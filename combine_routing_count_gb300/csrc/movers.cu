@@ -43,7 +43,16 @@ struct MoveArgs {
   int stages;
   int chunks;             // pack: column chunks per token row (1 elsewhere)
   uint32_t chunk_bytes;   // pack: bytes per chunk (B / chunks)
+  // Rank window filter of the receive-side moves: a pair is moved only when its destination
+  // rank (its global receive row / fd_rows, or for the identity copy its grouped row /
+  // fd_rows) is in [fd_lo, fd_lo + fd_n). fd_rows == 0: no filter.
+  int64_t fd_rows;
+  int fd_lo, fd_n;
 };
+
+__device__ __forceinline__ bool dst_outside(const MoveArgs& a, int64_t row) {
+  return a.fd_rows != 0 && (uint64_t)(row / a.fd_rows - a.fd_lo) >= (uint64_t)a.fd_n;
+}
 
 struct Plan {
   const uint8_t* src;
@@ -94,14 +103,14 @@ __device__ __forceinline__ bool make_plan(const Geo& g, const MoveArgs& a, int64
   if (KIND == kMoveScatter) {
     const int gs = __ldg(a.gsend + u);
     const int gr = __ldg(a.grecv + u);
-    if (gs < 0) return false;
+    if (gs < 0 || dst_outside(a, gr)) return false;
     pl.src = a.src + (int64_t)gs * g.B + coff;
     pl.dst = a.dst + (int64_t)gr * g.B + coff;
     return true;
   }
   if (KIND == kMoveCopyEx) {
     const int gl = __ldg(a.gslot + u);
-    if (gl < 0) return false;
+    if (gl < 0 || dst_outside(a, gl)) return false;
     pl.src = a.src + (int64_t)gl * H2 + coff;
     pl.dst = a.dst + (int64_t)gl * H2 + coff;
     return true;
@@ -109,7 +118,7 @@ __device__ __forceinline__ bool make_plan(const Geo& g, const MoveArgs& a, int64
   const int gl = __ldg(a.gslot + u);
   const int gr = __ldg(a.grecv + u);
   if (KIND == kMoveUnpack) {
-    if (gl < 0) return false;
+    if (gl < 0 || dst_outside(a, gr)) return false;
     pl.src = a.src + (int64_t)gr * g.B + coff;
     if (FP8) {
       pl.dst = a.dst + (int64_t)gl * g.H;
@@ -120,7 +129,7 @@ __device__ __forceinline__ bool make_plan(const Geo& g, const MoveArgs& a, int64
     return true;
   }
   if (KIND == kMoveCPack) {
-    if (gl < 0) return false;
+    if (gl < 0 || dst_outside(a, gr)) return false;
     pl.src = a.src + (int64_t)gl * H2 + coff;
     pl.dst = a.dst + (int64_t)gr * H2 + coff;
     return true;
@@ -134,7 +143,7 @@ __device__ __forceinline__ bool make_plan(const Geo& g, const MoveArgs& a, int64
   }
   // kMoveCScatter
   const int gs = __ldg(a.gsend + u);
-  if (gl < 0) return false;
+  if (gl < 0 || dst_outside(a, gr)) return false;
   pl.src = a.src + (int64_t)gr * H2 + coff;
   pl.dst = a.dst + (int64_t)gs * H2 + coff;
   return true;
@@ -470,6 +479,88 @@ cudaError_t run_move(MoveKind kind, const Geo& g, const MoveArgs& a, Ctx& c, boo
 
 }  // namespace
 
+namespace {
+
+// A move on the rank window [lo, lo + n) of a layout (see moe_layout_t): buffers are
+// window-local. Moves that start from the window's tokens or pairs (pack, scatter, combine
+// scatter) run over the window's contiguous token / pair range as a group of n ranks, their
+// index arrays advanced to it; moves into the window's receive or grouped rows (unpack,
+// combine pack, identity copy) visit every pair and skip those whose destination is outside
+// the window. Scatter and combine scatter move only the pairs whose both ends are in the
+// window; the caller moves the others between windows.
+cudaError_t launch_move_window(MoveKind kind, const Geo& g, const moe_layout_t* lay, MoveArgs a, Ctx& c) {
+  const int64_t lo = c.win_lo, n = (int64_t)c.win_hi - c.win_lo;
+  const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
+  const int64_t H2 = 2 * (int64_t)g.H, LC = (int64_t)g.L * g.cap;
+  const int64_t q0 = lo * g.TR;   // the window's first pair
+  Geo gw = g;                     // the window as a group of n ranks (source-side moves)
+  gw.N = (int)n;
+  gw.P = n * g.TR;
+  const uint8_t* src = a.src;
+  uint8_t* dst = a.dst;
+  uint8_t* dst2 = a.dst2;
+  const Geo* gp = &g;
+  switch (kind) {
+    case kMovePack:   // window tokens -> window send rows
+      gp = &gw;
+      a.fan = lay->gsend + q0;
+      a.dst = rebase(dst, q0 * g.B);
+      break;
+    case kMoveScatter:   // window pairs with a window destination: send rows -> receive rows
+      gp = &gw;
+      a.gsend = lay->gsend + q0;
+      a.grecv = lay->grecv + q0;
+      a.gslot = lay->gslot + q0;
+      a.src = rebase(src, q0 * g.B);
+      a.dst = rebase(dst, lo * g.RB * g.B);
+      a.fd_rows = g.RB;
+      break;
+    case kMoveUnpack:   // every pair with a window destination: receive rows -> grouped rows
+      a.src = rebase(src, lo * g.RB * g.B);
+      a.dst = rebase(dst, lo * LC * (fp8 ? (int64_t)g.H : g.B));
+      a.dst2 = rebase(dst2, lo * LC * (int64_t)(g.H / 32));
+      a.fd_rows = g.RB;
+      break;
+    case kMoveCPack:   // every pair with a window destination: grouped outputs -> receive order
+      a.src = rebase(src, lo * LC * H2);
+      a.dst = rebase(dst, lo * g.RB * H2);
+      a.fd_rows = g.RB;
+      break;
+    case kMoveCScatter:   // window pairs with a window destination: receive order -> sources
+      gp = &gw;
+      a.gsend = lay->gsend + q0;
+      a.grecv = lay->grecv + q0;
+      a.gslot = lay->gslot + q0;
+      a.src = rebase(src, lo * g.RB * H2);
+      a.dst = rebase(dst, q0 * H2);
+      a.fd_rows = g.RB;
+      break;
+    case kMoveCopyEx:   // the window's grouped rows (bf16 identity expert into another buffer)
+      a.src = rebase(src, lo * LC * H2);
+      a.dst = rebase(dst, lo * LC * H2);
+      a.fd_rows = LC;
+      break;
+    default:   // direct push writes other ranks' rows: the whole group only
+      return cudaErrorInvalidValue;
+  }
+  a.fd_lo = (int)lo;
+  a.fd_n = (int)n;
+  const Geo& gg = *gp;
+  if (kind == kMovePack) {
+    a.units = gg.N * (int64_t)gg.T * a.chunks;   // chunks were chosen for the whole group
+  } else {
+    a.units = gg.P * a.chunks;
+  }
+  if (a.units == 0) return cudaSuccess;
+  static const moe_kernel_id ids[] = {MOE_K_PACK,         MOE_K_SCATTER,         MOE_K_UNPACK,
+                                      MOE_K_COMBINE_PACK, MOE_K_COMBINE_SCATTER, MOE_K_EXPERT,
+                                      MOE_K_PACK_PUSH,    MOE_K_COMBINE_PUSH};
+  LaunchScope ls(c, ids[kind]);
+  return run_move<false>(kind, gg, a, c, fp8, (g.B % 16) == 0);
+}
+
+}  // namespace
+
 cudaError_t launch_move(MoveKind kind, const Geo& g, const moe_layout_t* lay, const void* src, void* dst, void* dst2,
                         Ctx& c) {
   return launch_move_range(kind, g, lay, src, dst, dst2, 0, g.T, c);
@@ -492,6 +583,9 @@ cudaError_t launch_move_range(MoveKind kind, const Geo& g, const moe_layout_t* l
   a.stage_bytes = 0;
   a.chunks = 1;
   a.chunk_bytes = (uint32_t)g.B;
+  a.fd_rows = 0;
+  a.fd_lo = 0;
+  a.fd_n = 0;
   const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
   const bool rowB16 = (g.B % 16) == 0;  // bf16 rows always; fp8 rows when H % 512 == 0
   if (kind == kMovePack || kind == kMovePackPush) {
@@ -523,6 +617,7 @@ cudaError_t launch_move_range(MoveKind kind, const Geo& g, const moe_layout_t* l
     a.chunk_bytes = (uint32_t)(rowb / a.chunks);
     a.units = g.P * a.chunks;
   }
+  if (windowed(g, c)) return nt == g.T ? launch_move_window(kind, g, lay, a, c) : cudaErrorInvalidValue;
   if (nt != g.T) {   // a token range of every rank: its tokens, or its pairs
     a.t0 = t0;
     a.nt = nt;

@@ -57,7 +57,8 @@ extern "C" moe_status moe_dispatch_send_noalloc(const moe_dims* dims, const moe_
   Geo g;
   moe_status st = make_geo(dims, g);
   if (st != MOE_OK) return st;
-  if (!layout_ok(lay)) return MOE_ERR_INVALID_ARG;
+  if (!layout_ok(lay) || (lay->win_hi > 0 && !(lay->win_lo == 0 && lay->win_hi == g.N)))
+    return MOE_ERR_INVALID_ARG;   // the whole group only
   if ((int64_t)g.N * g.T == 0) return MOE_OK;   // nothing to move
   if (!d_x || !d_recv || !aligned16(d_x) || !aligned16(d_recv)) return MOE_ERR_INVALID_ARG;
   if ((size_t)(g.P * g.B) > kNoAllocSendBytes) return MOE_ERR_INVALID_ARG;   // beyond the static buffer

@@ -450,7 +450,8 @@ constexpr int kDequantUnroll = 4;
 template <bool REV, bool RANGED>
 __global__ void __launch_bounds__(256) k_dequant_fp8(Geo g, const int32_t* __restrict__ gslot,
                                                      const uint8_t* __restrict__ exq, const float* __restrict__ exs,
-                                                     uint16_t* __restrict__ ey, int t0, int nt, int64_t np) {
+                                                     uint16_t* __restrict__ ey, int t0, int nt, int64_t np,
+                                                     int64_t win_rows, int win_lo, int win_n) {
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int nvec = g.H / 16;
@@ -463,6 +464,8 @@ __global__ void __launch_bounds__(256) k_dequant_fp8(Geo g, const int32_t* __res
     }
     const int gl = __ldg(gslot + q);
     if (gl < 0) continue;
+    // a rank window: only the grouped rows of its ranks (win_rows = L * cap rows a rank)
+    if (win_rows != 0 && (uint64_t)(gl / win_rows - win_lo) >= (uint64_t)win_n) continue;
     const uint8_t* qr = exq + (int64_t)gl * g.H;
     const float* sr = exs + (int64_t)gl * (g.H / 128);
     uint16_t* yr = ey + (int64_t)gl * g.H;
@@ -805,7 +808,9 @@ cudaError_t launch_combine_sum(const Geo& g, const moe_layout_t* lay, const uint
                        (const int32_t*)(lay->scratch + layout_scratch_tgroups_offset(g)), cpart, out);
 }
 
-cudaError_t launch_quant_fp8(const Geo& g, const uint16_t* x, uint8_t* xq, Ctx& c) {
+cudaError_t launch_quant_fp8(const Geo& g0, const uint16_t* x, uint8_t* xq, Ctx& c) {
+  Geo g = g0;
+  if (windowed(g0, c)) g.N = c.win_hi - c.win_lo;   // the window's token rows (window-local buffers)
   const int64_t upr = (g.H / 128 + 2 * kQuantUnroll - 1) / (2 * kQuantUnroll);
   const int64_t units = (int64_t)g.N * g.T * upr;   // one warp unit: 2 x kQuantUnroll blocks of a row
   if (units == 0) return cudaSuccess;
@@ -818,9 +823,18 @@ cudaError_t launch_quant_fp8(const Geo& g, const uint16_t* x, uint8_t* xq, Ctx& 
   return launch_kernel(k_quant_fp8, dim3((unsigned)blocks), dim3(256), 0, c, g, x, xq);
 }
 
-cudaError_t launch_quant_pack(const Geo& g, const int32_t* fan, const uint16_t* x, uint8_t* dst, Ctx& c, int t0,
+cudaError_t launch_quant_pack(const Geo& g0, const int32_t* fan, const uint16_t* x, uint8_t* dst, Ctx& c, int t0,
                               int nt) {
-  if (nt < 0) nt = g.T;
+  if (nt < 0) nt = g0.T;
+  Geo g = g0;
+  if (windowed(g0, c)) {   // the window's tokens into its window-local send rows
+    if (nt != g0.T || (c.flags & MOE_FLAG_DIRECT_PUSH)) return cudaErrorInvalidValue;
+    const int64_t q0 = (int64_t)c.win_lo * g0.TR;
+    g.N = c.win_hi - c.win_lo;
+    g.P = (int64_t)g.N * g0.TR;
+    fan += q0;
+    dst = rebase(dst, q0 * g0.B);
+  }
   const int64_t upr = (g.H / 128 + 2 * kQuantUnroll - 1) / (2 * kQuantUnroll);
   const int64_t units = (int64_t)g.N * nt * upr;
   if (units == 0) return cudaSuccess;
@@ -850,21 +864,43 @@ cudaError_t launch_dequant_fp8(const Geo& g, const moe_layout_t* lay, const uint
   const bool rev = (c.flags & MOE_FLAG_DIRECT_PUSH) != 0, ranged = nt != g.T;
   auto k = rev ? (ranged ? k_dequant_fp8<true, true> : k_dequant_fp8<true, false>)
                : (ranged ? k_dequant_fp8<false, true> : k_dequant_fp8<false, false>);
+  int64_t win_rows = 0;
+  int win_lo = 0, win_n = 0;
+  if (windowed(g, c)) {   // the window's grouped rows, in window-local buffers
+    if (ranged) return cudaErrorInvalidValue;
+    win_rows = (int64_t)g.L * g.cap;
+    win_lo = c.win_lo;
+    win_n = c.win_hi - c.win_lo;
+    exq = rebase(exq, win_lo * win_rows * g.H);
+    exs = rebase(exs, win_lo * win_rows * (int64_t)(g.H / 128) * 4);
+    ey = rebase(ey, win_lo * win_rows * 2 * (int64_t)g.H);
+  }
   return launch_kernel(k, dim3((unsigned)blocks), dim3(256), 0, c, g, (const int32_t*)lay->gslot, exq, exs, ey, t0,
-                       nt, np);
+                       nt, np, win_rows, win_lo, win_n);
 }
 
-cudaError_t launch_combine_reduce(const Geo& g, const moe_layout_t* lay, const uint16_t* crecv, const float* w,
+cudaError_t launch_combine_reduce(const Geo& g0, const moe_layout_t* lay, const uint16_t* crecv, const float* w,
                                   uint16_t* out, Ctx& c, int t0, int nt) {
-  if (nt < 0) nt = g.T;
+  if (nt < 0) nt = g0.T;
+  Geo g = g0;
+  const int32_t* gsend = lay->gsend;
+  const int32_t* gslot = lay->gslot;
+  if (windowed(g0, c)) {   // the window's tokens: window-local weights, combine rows and output
+    if (nt != g0.T) return cudaErrorInvalidValue;
+    const int64_t q0 = (int64_t)c.win_lo * g0.TR;
+    g.N = c.win_hi - c.win_lo;
+    g.P = (int64_t)g.N * g0.TR;
+    gsend += q0;
+    gslot += q0;
+    crecv = rebase(crecv, q0 * 2 * (int64_t)g0.H);
+  }
   const int64_t tokens = (int64_t)g.N * nt;
   if (tokens == 0) return cudaSuccess;
   const int ncol = g.H / 8;
   dim3 grid((unsigned)tokens, (unsigned)((ncol + kReduceThreads - 1) / kReduceThreads));
   LaunchScope ls(c, MOE_K_COMBINE_REDUCE);
   return launch_kernel(nt != g.T ? k_combine_reduce<true> : k_combine_reduce<false>, grid, dim3(kReduceThreads), 0, c,
-                       g, (const int32_t*)lay->gsend,
-                       (const int32_t*)lay->gslot, w, crecv, out, t0, nt);
+                       g, gsend, gslot, w, crecv, out, t0, nt);
 }
 
 }  // namespace moe

@@ -177,7 +177,30 @@ typedef struct {
  *   ctas_per_sm (0 = automatic, else mover CTAs per SM), batches (token batches of
  *   moe_forward's micro-batches, of moe_dispatch / moe_combine and of moe_dispatch_split
  *   (0 = automatic, else 1..32) and of moe_forward_host's copy-engine pipeline (0 =
- *   automatic, else 1..16); see moe_batches).
+ *   automatic, else 1..16); see moe_batches), win_lo / win_hi (the rank window, below).
+ *
+ * Rank window (expert parallelism over several GPUs, one process each; section "Send and
+ * receive buffers": every rank knows where its writes go and where it receives from each
+ * rank; section "MoE all-to-all over EFA": one write per peer). With win_hi > 0 the layout
+ * describes all N ranks (moe_layout reads the routing of every rank, d_idx [N][T][R]) but the
+ * data entry points below work on the ranks [win_lo, win_hi) only, whose buffers are
+ * window-local: rank win_lo + i is row block i of every [N, ...] buffer, which holds
+ * n = win_hi - win_lo blocks (d_x [n][T][H], d_send [n][T*R][B], d_recv [n][RB][B],
+ * d_expert_x [n][L][cap][...], d_csend [n][RB][H], d_crecv [n][T*R][H], d_w [n][T][R],
+ * d_out [n][T][H]). Within the window:
+ *   moe_dispatch_send / moe_quantize_dispatch_send pack the window's tokens and write the
+ *     slices whose destination is in the window (the slices to other ranks stay in d_send
+ *     for the caller to move, at the rows moe_exchange_plan lists);
+ *   moe_dispatch_recv shuffles the receive rows of the window's ranks (the slices from
+ *     other ranks must have been written into d_recv first);
+ *   moe_expert_identity works on the window's experts;
+ *   moe_combine_send writes the window's expert outputs in receive order and writes back
+ *     the slices whose source is in the window (the others stay in d_csend for the caller);
+ *   moe_combine_recv sums the window's tokens (the slices from other ranks must have been
+ *     written into d_crecv first).
+ * moe_quantize_fp8_b128 quantises the window's token rows. Every other data entry point, and
+ * MOE_FLAG_DIRECT_PUSH, needs the whole group (win_lo = win_hi = 0, or 0 and N): otherwise
+ * MOE_ERR_INVALID_ARG. A window runs each call as one token batch.
  */
 typedef struct {
     int32_t *cnt, *C, *soff, *roff, *rtot, *ecnt, *eoff;
@@ -190,6 +213,7 @@ typedef struct {
     int32_t tma_stages;
     int32_t ctas_per_sm;
     int32_t batches;
+    int32_t win_lo, win_hi; /* rank window [win_lo, win_hi); 0, 0: all N ranks */
 } moe_layout_t;
 
 /* Device buffers of one whole pass (moe_forward). Shapes, with B = row bytes,
@@ -464,6 +488,33 @@ moe_status moe_forward(const moe_dims *dims, const moe_layout_t *lay, const moe_
 moe_status moe_forward_host(const moe_dims *dims, const moe_layout_t *lay, const moe_buffers_t *bufs,
                             const uint16_t *h_x, const int32_t *h_idx, const float *h_w, uint16_t *h_out,
                             void *stream);
+
+/* The slices a rank window sends to or receives from the ranks outside it (section "Send
+ * and receive buffers": with the counts known, each rank writes one contiguous slice per
+ * peer at offsets both sides derive from them). The N ranks are split into nwin windows,
+ * window w holding ranks [h_bounds[w], h_bounds[w+1]) (h_bounds ascending, h_bounds[0] = 0,
+ * h_bounds[nwin] = N); `me` is the caller's window. h_C [N][N], h_soff [N][E] and
+ * h_roff [N][N] are host copies of the layout's arrays.
+ *  direction 0 (dispatch): sending = 1 lists, for every source s in the window and
+ *    destination d outside it with C[s][d] > 0, the rows of d_send (window-local row
+ *    (s - lo)*T*R + soff[s][d*L]); sending = 0 lists, for every destination d in the window
+ *    and source s outside it, the rows of d_recv ((d - lo)*RB + roff[d][s]).
+ *  direction 1 (combine): sending = 1 lists the rows of d_csend that go back to sources
+ *    outside the window ((d - lo)*RB + roff[d][s], d in the window); sending = 0 lists the
+ *    rows of d_crecv that arrive from them ((s - lo)*T*R + soff[s][d*L], s in the window).
+ * Each slice is C[s][d] rows; `peer` is the window on the other side. Slices are listed in
+ * ascending (s, d) order, so the k-th slice window p sends to window q is the k-th slice q
+ * receives from p. Writes at most max_out slices to out (may be NULL) and returns how many
+ * there are, or -1 for bad arguments. Host only, no CUDA call. */
+typedef struct {
+    int32_t peer;       /* the other window */
+    int32_t s, d;       /* source and destination rank of the slice */
+    int32_t rows;       /* C[s][d] */
+    int64_t local_row;  /* first row in the caller's window-local buffer */
+} moe_slice_t;
+int64_t moe_exchange_plan(const moe_dims *dims, const int32_t *h_C, const int32_t *h_soff, const int32_t *h_roff,
+                          int32_t nwin, const int32_t *h_bounds, int32_t me, int32_t direction, int32_t sending,
+                          moe_slice_t *out, int64_t max_out);
 
 /* Token batches for these dims and layout settings (lay->batches, lay->flags): which = 0:
  * moe_forward's micro-batches; 1: moe_forward_host's copy-engine pipeline; 2: the phases of
