@@ -24,8 +24,11 @@ Prints one JSON line (rank 0). `value` is tokens/s over all GPUs: (N*T tokens pe
 simulated group) x (GPUs) / (step time, max over ranks), timed with CUDA events on the
 launching stream, inputs resident in HBM, L2 flushed (a write of 2x the L2 size, then a
 read of another 2x, so no dirty flush lines are written back inside the step) before
-every timed step. With --gpus > 1 each GPU runs an independent replica of the whole
-simulated group (the one-GPU path has no cross-GPU exchange).
+every timed step. With --gpus G > 1 (torchrun, one process per GPU) the workload's N
+simulated ranks are split over the G GPUs in rank windows of N/G ranks: the routing is
+all-gathered, each GPU's kernels move the rows inside its window, and the slices between
+windows go over NCCL point-to-point (strong scaling: the job processes N*T tokens per step);
+--replicas runs an independent copy of the whole group on every GPU instead.
 """
 from __future__ import annotations
 
@@ -85,6 +88,11 @@ def parse_args(argv=None):
                         "all cores)")
     p.add_argument("--other-cpu-seconds", type=float, default=3.0,
                    help="CPU work for the single-thread oracle baseline of each per_config workload")
+    p.add_argument("--sharded", action="store_true",
+                   help="the expert-parallel path of --gpus > 1 also on one GPU (one window holding every rank)")
+    p.add_argument("--replicas", action="store_true",
+                   help="with --gpus > 1: an independent replica of the whole group on every GPU instead of "
+                        "expert parallelism over the GPUs")
     p.add_argument("--profile-step", choices=["pass", "split", "dedicated"], default=None,
                    help="run only W + K steps of one kind (L2 flushed before each) and print a short summary, "
                         "for the ncu captures in profiles/: 'pass' the whole pass in one batch (whole-pass "
@@ -828,6 +836,172 @@ def compact(r: dict) -> dict:
     return c
 
 
+def measure_sharded(wl, args, dist, device, peak: float, peak_kind: str) -> dict:
+    """The workload's N simulated ranks split over the GPUs of the job, one rank window per
+    process (combine_routing_count_gb300.sharded): a step gathers the routing, lays it out,
+    plans the slices, dispatches (kernels inside the window, NCCL point-to-point slices
+    between windows), runs the identity expert and combines back. Strong scaling: the whole
+    job processes the workload's N*T tokens per step."""
+    import torch
+    from combine_routing_count_gb300 import KERNEL_NAMES, MoeProf, lib
+    from combine_routing_count_gb300.sharded import DistTransport, ShardedEP, sharded_forward, window_bounds
+    ws, rank, local = dist_env()
+    if wl.N % ws:
+        raise SystemExit(f"{wl.name}: {wl.N} simulated ranks do not split evenly over {ws} GPUs")
+    b = window_bounds(wl.N, ws)
+    lo, hi = b[rank], b[rank + 1]
+    inp = workloads.make_inputs(wl)
+    sh = ShardedEP(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, wl.payload, bounds=b, me=rank)
+    x = torch.from_numpy(inp["x"][lo:hi].copy()).view(torch.bfloat16).to(device)
+    idx = torch.from_numpy(inp["idx"][lo:hi].copy()).to(device)
+    w = torch.from_numpy(inp["w"][lo:hi].copy()).to(device)
+    tr = DistTransport()
+    stream = torch.cuda.current_stream()
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush_w = torch.empty(2 * l2, dtype=torch.uint8, device=device)
+    flush_r = torch.ones(2 * l2 // 4, dtype=torch.float32, device=device)
+    flush_sum = torch.empty((), dtype=torch.float32, device=device)
+
+    def flush_l2():
+        flush_w.zero_()
+        torch.sum(flush_r, dim=0, out=flush_sum)
+
+    def step():
+        sharded_forward([sh], tr, [x], [idx], [w])
+
+    K = args.steps
+    for _ in range(args.warmup):
+        flush_l2()
+        step()
+    code, bits = sh.status()
+    if code != 0:
+        raise RuntimeError(f"device status {code} bits {bits:#x}")
+    vis = [v.strip() for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+    sampler = ClockSampler(vis[local] if local < len(vis) else local)
+    sampler.start()
+    # per-kernel events of this window's launches (one batch)
+    profs = []
+    for _ in range(K):
+        pr = MoeProf()
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(KERNEL_NAMES))]
+        for i, e in enumerate(evs):
+            e.record(stream)
+            pr.events[i] = e.cuda_event
+        profs.append((pr, evs))
+    barrier(dist, device)
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush_l2()
+        pr, _ = profs[i]
+        pr.n = 0
+        sh.layout.prof = ctypes.pointer(pr)
+        step()
+    torch.cuda.synchronize()
+    sh.layout.prof = None
+    per_kernel = {}
+    for pr, evs in profs:
+        for j in range(pr.n):
+            per_kernel.setdefault(KERNEL_NAMES[pr.kernel[j]], []).append(evs[2 * j].elapsed_time(evs[2 * j + 1]))
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    barrier(dist, device)
+    torch.cuda.synchronize()
+    n0 = lib().moe_launch_count()
+    for i in range(K):
+        flush_l2()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(dist, device)
+    launches = lib().moe_launch_count() - n0
+    mean_ms = statistics.fmean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    ms_all = max_over_ranks(mean_ms, dist, device)
+    # end to end: this window's inputs from pinned host memory, its output back
+    h_x = torch.from_numpy(inp["x"][lo:hi].copy()).view(torch.bfloat16).pin_memory()
+    h_idx = torch.from_numpy(inp["idx"][lo:hi].copy()).pin_memory()
+    h_w = torch.from_numpy(inp["w"][lo:hi].copy()).pin_memory()
+    h_out = torch.empty(tuple(sh.out.shape), dtype=torch.bfloat16).pin_memory()
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    barrier(dist, device)
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush_l2()
+        e_s[i].record(stream)
+        x.copy_(h_x, non_blocking=True)
+        idx.copy_(h_idx, non_blocking=True)
+        w.copy_(h_w, non_blocking=True)
+        step()
+        h_out.copy_(sh.out, non_blocking=True)
+        e_e[i].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    e2e_ms = max_over_ranks(statistics.fmean(s.elapsed_time(e) for s, e in zip(e_s, e_e)), dist, device)
+    code, bits = sh.status()
+    # parity: every window checks its output against the oracle's rows of its ranks
+    import oracle
+    o = oracle.forward(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, wl.payload, inp["x"], inp["idx"], inp["w"])
+    ok = bool(np.array_equal(sh.out.cpu().view(torch.int16).numpy().view(np.uint16), o["out"][lo:hi])) and code == 0
+    ok_all = max_over_ranks(0.0 if ok else 1.0, dist, device) == 0.0
+    lay = sh.layout_arrays()
+    P = int(lay["rtot"].sum().item())
+    Pk = int((lay["slot"] >= 0).sum().item())
+    ab = algorithmic_bytes(wl, P, Pk)
+    n = hi - lo
+    frac_w = n / wl.N   # the window's share of the source-side work
+    # the window's algorithmic bytes per kernel (rows it moves; no pair of these workloads is
+    # dropped for capacity, so routed rows are kept rows)
+    C = lay["C"].cpu().numpy().astype(np.int64)
+    B, H2 = wl.row_bytes, 2 * wl.H
+    pw = int(C[lo:hi, :].sum())          # pairs the window's tokens route
+    rw = int(C[:, lo:hi].sum())          # rows the window's ranks receive
+    inner = int(C[lo:hi, lo:hi].sum())   # rows whose both ends are in the window
+    tin = n * wl.T * (2 * wl.H)          # the window's token rows (bf16)
+    wbytes = {"pack": n * wl.T * B + pw * B, "quant_pack": tin + pw * B, "scatter": 2 * inner * B,
+              "unpack": 2 * rw * B, "combine_pack": 2 * rw * H2, "combine_scatter": 2 * inner * H2,
+              "combine_reduce": pw * H2 + n * wl.T * H2}
+    kernels = {}
+    for name, ts in per_kernel.items():
+        if name == "expert":
+            continue
+        us = statistics.fmean(ts) * 1e3
+        kernels[name] = {"us": round(us, 2), "launches_per_step": len(ts) / K}
+        if name in wbytes:
+            gbs = wbytes[name] / (us * 1e-6) / 1e9
+            kernels[name].update({"bytes": wbytes[name], "gbs": round(gbs, 1), "frac": round(gbs / peak, 3)})
+    dom = max((k for k in kernels if "bytes" in kernels[k]), key=lambda k: kernels[k]["us"], default=None)
+    tokens = wl.N * wl.T
+    slices = {k: len(v) for k, v in sh.plans.items()}
+    return {
+        "metric": METRIC, "value": round(tokens / (ms_all * 1e-3), 1), "unit": "tokens/s", "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_all, 4), "higher_is_better": True, "scaling": "strong",
+        "vs_baseline": None, "dtype": "fp8+bf16" if wl.payload == "fp8" else "bf16",
+        "data": "synthetic (seeded; DeepSeek-V3/Kimi-K2-shaped routing, identity experts)",
+        "config": {"workload": wl.name, "N_ranks_simulated": wl.N, "T": wl.T, "H": wl.H, "E": wl.E, "R": wl.R,
+                   "payload": wl.payload, "routing": wl.routing, "seed": wl.seed, "l2": L2_NOTE,
+                   "parallelism": f"expert parallel: {ws} GPUs, {n} of the {wl.N} ranks each (rank windows), "
+                                  "routing all-gathered, slices between windows over NCCL point-to-point"},
+        "roofline": {"bound": "hbm", "kernel": dom, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "achieved": kernels[dom]["gbs"] if dom else None, "frac": kernels[dom]["frac"] if dom else None,
+                     "bytes_per_launch": kernels[dom]["bytes"] if dom else None, "traffic": None,
+                     "launch": "rank 0's window: the rows its kernels move in one step (one batch)"},
+        "kernels_rank0": kernels,
+        "window_share": frac_w,
+        "slices": {"dispatch_send": slices[(0, 1)], "dispatch_recv": slices[(0, 0)],
+                   "combine_send": slices[(1, 1)], "combine_recv": slices[(1, 0)]},
+        "e2e": {"value": round(tokens / (e2e_ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(e2e_ms, 4),
+                "h2d_bytes_per_step": (x.numel() * 2 + idx.numel() * 4 + w.numel() * 4) * ws,
+                "d2h_bytes_per_step": sh.out.numel() * 2 * ws,
+                "path": "each window's inputs copied in from pinned host memory and its output back, inside the step"},
+        "parity": {"out_bit_exact_vs_oracle": ok_all},
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+        "bytes_per_step_algorithmic": sum(ab[k] for k in ("pack", "scatter", "unpack", "combine_pack",
+                                                          "combine_scatter", "combine_reduce")),
+    }
+
+
 def run_ours(args):
     import torch
     from combine_routing_count_gb300 import build
@@ -839,6 +1013,23 @@ def run_ours(args):
     peak, peak_kind = measured_peak()
 
     wl = workload_of(args)
+    if (ws > 1 and not args.replicas) or args.sharded:
+        if dist is None:   # --sharded on one GPU: a one-process group, the same code path
+            import socket
+
+            import torch.distributed as tdist
+            with socket.socket() as sk:
+                sk.bind(("127.0.0.1", 0))
+                port = sk.getsockname()[1]
+            tdist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0, world_size=1,
+                                     device_id=device)
+            dist = tdist
+        out = measure_sharded(wl, args, dist, device, peak, peak_kind)
+        if dist is not None:
+            dist.destroy_process_group()
+        if rank == 0:
+            print(json.dumps(out), flush=True)
+        return
     if args.profile_step:
         r = measure(wl, args, dist, device, peak, peak_kind, 0.0, False)
         if rank == 0:
