@@ -1028,12 +1028,12 @@ def run_ours(args):
         if dist is not None:
             dist.destroy_process_group()
         if rank == 0:
-            print(json.dumps(out), flush=True)
+            print(json.dumps(out), file=_OUT, flush=True)
         return
     if args.profile_step:
         r = measure(wl, args, dist, device, peak, peak_kind, 0.0, False)
         if rank == 0:
-            print(json.dumps(r), flush=True)
+            print(json.dumps(r), file=_OUT, flush=True)
         return
     out = measure(wl, args, dist, device, peak, peak_kind, args.cpu_seconds, True)
     if args.config is None and not args.shape:
@@ -1047,8 +1047,10 @@ def run_ours(args):
     if dist is not None:
         dist.destroy_process_group()
     if rank == 0:
-        print(json.dumps(out), flush=True)
+        print(json.dumps(out), file=_OUT, flush=True)
 
+
+_OUT = sys.stdout   # where the JSON line goes (main() points it at the real stdout)
 
 # ---------------------------------------------------------------------------- reference arm
 
@@ -1084,11 +1086,22 @@ def run_reference(args):
     }), flush=True)
 
 
+def _stdout_for_the_json_line():
+    """The process's stdout for the one JSON line; everything else that writes to file
+    descriptor 1 (NCCL prints its version there, at exit) goes to stderr."""
+    sys.stdout.flush()
+    fd = os.dup(1)
+    os.dup2(2, 1)
+    return os.fdopen(fd, "w")
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
     else:
+        global _OUT
+        _OUT = _stdout_for_the_json_line()
         run_ours(args)
 
 

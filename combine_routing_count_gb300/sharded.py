@@ -141,7 +141,11 @@ class ShardedEP:
         return out
 
     def make_plans(self):
-        """The four slice lists of this window (host; reads C, soff and roff back from the device)."""
+        """The four slice lists of this window (host; reads C, soff and roff back from the device;
+        a single window exchanges nothing and reads nothing)."""
+        if len(self.bounds) == 2:
+            self.plans = {(direction, sending): [] for direction in (0, 1) for sending in (0, 1)}
+            return self.plans
         a = self.layout_arrays()
         C, soff, roff = (a[k].cpu().numpy() for k in ("C", "soff", "roff"))
         self.plans = {(direction, sending): exchange_plan(self.dims, C, soff, roff, self.bounds, self.me, direction,
