@@ -19,7 +19,9 @@
 //    sums that rank's chunk counts into cnt[s][.]; a grid of independent scan CTAs (one
 //    per source row, per 32-expert column tile and per destination) then runs every
 //    scan, and the maps kernel adds a pair's earlier-chunk counts to its chunk-local rank.
-//    The three kernels chain with programmatic dependent launch.
+//    The counting kernel's last CTA per rank also turns the rank's chunk counts into
+//    exclusive prefixes over its chunks. The three kernels chain with programmatic
+//    dependent launch.
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -36,7 +38,7 @@ struct LayoutArgs {
   int32_t *pos, *rrow, *slot, *slot_src, *recv_src;
   int32_t *gsend, *grecv, *gslot;
   int32_t* status;
-  int32_t* ccnt;    // [N][nch][E]: per-chunk counts
+  int32_t* ccnt;    // [N][nch][E]: per-chunk counts, then exclusive prefixes over the chunks
   int32_t* done;    // [N]: chunk CTAs of each rank that have finished (reset by the last one)
   int nch;          // chunks per rank, ceil(T*R / kChunk)
 };
@@ -246,17 +248,27 @@ __global__ void __launch_bounds__(kChunk) k_route_count(Geo g, LayoutArgs a) {
   if (tid == 0) is_last = (atomicAdd(a.done + s, 1) == a.nch - 1);
   __syncthreads();
   if (is_last) {
+    // cnt[s][.] = sum over the chunks; each chunk's row becomes the exclusive prefix over
+    // the rank's earlier chunks, so a pair's rank is its chunk-local rank plus one load.
     __threadfence();
-    const int32_t* base = a.ccnt + (int64_t)s * a.nch * E;
+    int32_t* base = a.ccnt + (int64_t)s * a.nch * E;
     for (int ee = tid; ee < E; ee += kChunk) {
       int r = 0;
       int cc = 0;
       for (; cc + 4 <= a.nch; cc += 4) {   // four independent loads in flight
         const int v0 = __ldcg(base + (int64_t)cc * E + ee), v1 = __ldcg(base + (int64_t)(cc + 1) * E + ee);
         const int v2 = __ldcg(base + (int64_t)(cc + 2) * E + ee), v3 = __ldcg(base + (int64_t)(cc + 3) * E + ee);
+        base[(int64_t)cc * E + ee] = r;
+        base[(int64_t)(cc + 1) * E + ee] = r + v0;
+        base[(int64_t)(cc + 2) * E + ee] = r + v0 + v1;
+        base[(int64_t)(cc + 3) * E + ee] = r + v0 + v1 + v2;
         r += v0 + v1 + v2 + v3;
       }
-      for (; cc < a.nch; ++cc) r += __ldcg(base + (int64_t)cc * E + ee);
+      for (; cc < a.nch; ++cc) {
+        const int v = __ldcg(base + (int64_t)cc * E + ee);
+        base[(int64_t)cc * E + ee] = r;
+        r += v;
+      }
       a.cnt[(int64_t)s * E + ee] = r;
     }
     if (tid == 0) a.done[s] = 0;  // ready for the next call
@@ -287,9 +299,9 @@ __global__ void __launch_bounds__(kMapThreads) k_layout_maps(Geo g, LayoutArgs a
         const int TR = (int)g.TR;
         const int s = q / TR;
         const int c = (q - s * TR) / kChunk;
-        const int32_t* col = a.ccnt + (int64_t)s * a.nch * g.E + e;
-        int rk = a.pos[q];
-        for (int cc = 0; cc < c; ++cc) rk += col[(int64_t)cc * g.E];   // pairs of e in earlier chunks
+        // chunk-local rank + pairs of e in the rank's earlier chunks (the counting kernel
+        // left the chunk table as exclusive prefixes over the chunks)
+        const int rk = a.pos[q] + a.ccnt[((int64_t)s * a.nch + c) * g.E + e];
         const int d = e / g.L;
         const int p = a.soff[s * g.E + e] + rk;
         const int rr = a.roff[d * g.N + s] + p - a.soff[s * g.E + d * g.L];

@@ -43,15 +43,17 @@ struct MoveArgs {
   int stages;
   int chunks;             // pack: column chunks per token row (1 elsewhere)
   uint32_t chunk_bytes;   // pack: bytes per chunk (B / chunks)
-  // Rank window filter of the receive-side moves: a pair is moved only when its destination
-  // rank (its global receive row / fd_rows, or for the identity copy its grouped row /
-  // fd_rows) is in [fd_lo, fd_lo + fd_n). fd_rows == 0: no filter.
+  // Rank window filter of the receive-side moves (mode 2): a pair is moved only when its
+  // destination rank (its global receive row / fd_rows, or for the identity copy its grouped
+  // row / fd_rows) is in [fd_lo, fd_lo + fd_n).
   int64_t fd_rows;
   int fd_lo, fd_n;
 };
 
+template <int MODE>
 __device__ __forceinline__ bool dst_outside(const MoveArgs& a, int64_t row) {
-  return a.fd_rows != 0 && (uint64_t)(row / a.fd_rows - a.fd_lo) >= (uint64_t)a.fd_n;
+  if (MODE != 2) return false;   // only rank-window launches filter (MODE 2)
+  return (uint64_t)(row / a.fd_rows - a.fd_lo) >= (uint64_t)a.fd_n;
 }
 
 struct Plan {
@@ -70,25 +72,29 @@ __host__ __device__ __forceinline__ uint32_t unit_bytes(const Geo& g, const Move
   return a.chunk_bytes;
 }
 
-// Fills `pl` for unit u; false when the unit moves nothing (bad expert id or dropped pair).
-// The global index (token for per = 1, pair for per = R) of item v of the token range
-// [t0, t0 + nt) of every rank, items rank-major. RANGED is a compile-time choice, so moves
-// over all tokens compile to the identity.
-template <bool RANGED>
+// Launch modes, a compile-time choice: 0 the whole pass, 1 a token range [t0, t0 + nt) of
+// every rank (micro-batches), 2 a rank window (buffers window-local; the receive-side moves
+// skip pairs whose destination is outside the window). Modes 0 and 1 compile no filter.
+//
+// The global index (token for per = 1, pair for per = R) of item v: in mode 1, item v of the
+// token range of every rank, items rank-major; otherwise v itself.
+template <int MODE>
 __device__ __forceinline__ int64_t range_item(const Geo& g, const MoveArgs& a, int64_t v, int per) {
-  if (!RANGED) return v;
+  if (MODE != 1) return v;
   const int64_t span = (int64_t)a.nt * per;
   const int64_t s = v / span;
   return (s * g.T + a.t0) * per + (v - s * span);
 }
 
-template <int KIND, bool FP8, bool RANGED, bool REV>
+// Fills `pl` for unit u; false when the unit moves nothing (bad expert id, dropped pair, or a
+// destination outside the rank window).
+template <int KIND, bool FP8, int MODE, bool REV>
 __device__ __forceinline__ bool make_plan(const Geo& g, const MoveArgs& a, int64_t u, Plan& pl) {
   if (REV) u = a.units - 1 - u;
   const int64_t H2 = 2 * (int64_t)g.H;
   if (KIND == kMovePack || KIND == kMovePackPush) {
     const int64_t tv = u / a.chunks;
-    const int64_t tok = range_item<RANGED>(g, a, tv, 1);
+    const int64_t tok = range_item<MODE>(g, a, tv, 1);
     pl.tok = tok;
     pl.coff = (int32_t)((u - tv * a.chunks) * a.chunk_bytes);
     pl.src = a.src + tok * g.B + pl.coff;
@@ -99,18 +105,18 @@ __device__ __forceinline__ bool make_plan(const Geo& g, const MoveArgs& a, int64
   // Non-pack kinds: unit u is column chunk (u % chunks) of pair u / chunks.
   const int64_t cq = u / a.chunks;
   const int64_t coff = (u - cq * a.chunks) * (int64_t)a.chunk_bytes;
-  u = range_item<RANGED>(g, a, cq, g.R);
+  u = range_item<MODE>(g, a, cq, g.R);
   if (KIND == kMoveScatter) {
     const int gs = __ldg(a.gsend + u);
     const int gr = __ldg(a.grecv + u);
-    if (gs < 0 || dst_outside(a, gr)) return false;
+    if (gs < 0 || dst_outside<MODE>(a, gr)) return false;
     pl.src = a.src + (int64_t)gs * g.B + coff;
     pl.dst = a.dst + (int64_t)gr * g.B + coff;
     return true;
   }
   if (KIND == kMoveCopyEx) {
     const int gl = __ldg(a.gslot + u);
-    if (gl < 0 || dst_outside(a, gl)) return false;
+    if (gl < 0 || dst_outside<MODE>(a, gl)) return false;
     pl.src = a.src + (int64_t)gl * H2 + coff;
     pl.dst = a.dst + (int64_t)gl * H2 + coff;
     return true;
@@ -118,7 +124,7 @@ __device__ __forceinline__ bool make_plan(const Geo& g, const MoveArgs& a, int64
   const int gl = __ldg(a.gslot + u);
   const int gr = __ldg(a.grecv + u);
   if (KIND == kMoveUnpack) {
-    if (gl < 0 || dst_outside(a, gr)) return false;
+    if (gl < 0 || dst_outside<MODE>(a, gr)) return false;
     pl.src = a.src + (int64_t)gr * g.B + coff;
     if (FP8) {
       pl.dst = a.dst + (int64_t)gl * g.H;
@@ -129,7 +135,7 @@ __device__ __forceinline__ bool make_plan(const Geo& g, const MoveArgs& a, int64
     return true;
   }
   if (KIND == kMoveCPack) {
-    if (gl < 0 || dst_outside(a, gr)) return false;
+    if (gl < 0 || dst_outside<MODE>(a, gr)) return false;
     pl.src = a.src + (int64_t)gl * H2 + coff;
     pl.dst = a.dst + (int64_t)gr * H2 + coff;
     return true;
@@ -143,7 +149,7 @@ __device__ __forceinline__ bool make_plan(const Geo& g, const MoveArgs& a, int64
   }
   // kMoveCScatter
   const int gs = __ldg(a.gsend + u);
-  if (gl < 0 || dst_outside(a, gr)) return false;
+  if (gl < 0 || dst_outside<MODE>(a, gr)) return false;
   pl.src = a.src + (int64_t)gr * H2 + coff;
   pl.dst = a.dst + (int64_t)gs * H2 + coff;
   return true;
@@ -186,7 +192,7 @@ __device__ __forceinline__ void bulk_wait_read_1() {
   asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 
-template <int KIND, bool FP8, bool RANGED, bool REV>
+template <int KIND, bool FP8, int MODE, bool REV>
 __global__ void __launch_bounds__(kIssuers * 32) k_move_tma(Geo g, MoveArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -206,7 +212,7 @@ __global__ void __launch_bounds__(kIssuers * 32) k_move_tma(Geo g, MoveArgs a) {
     uint32_t vbits = 0, pbits = 0;   // per stage: a load is in flight; the barrier's parity
     Plan pl;
     for (int k = 0; k < S && k < n; ++k) {
-      const bool ok = make_plan<KIND, FP8, RANGED, REV>(g, a, gi + k * G, pl);
+      const bool ok = make_plan<KIND, FP8, MODE, REV>(g, a, gi + k * G, pl);
       sp[k] = StagePlan{pl.dst, pl.dst2, pl.tok, pl.coff, {}};
       if (KIND == kMovePack || KIND == kMovePackPush)
         for (int r = 0; r < kPackPrefetch; ++r) sp[k].p[r] = pl.p[r];
@@ -217,7 +223,7 @@ __global__ void __launch_bounds__(kIssuers * 32) k_move_tma(Geo g, MoveArgs a) {
       }
     }
     Plan nx;
-    bool nx_ok = (S < n) && make_plan<KIND, FP8, RANGED, REV>(g, a, gi + S * G, nx);
+    bool nx_ok = (S < n) && make_plan<KIND, FP8, MODE, REV>(g, a, gi + S * G, nx);
     for (int64_t j = 0; j < n; ++j) {
       const int k = (int)(j % S);
       bool stored = false;
@@ -252,7 +258,7 @@ __global__ void __launch_bounds__(kIssuers * 32) k_move_tma(Geo g, MoveArgs a) {
           bulk_g2s(ring + (size_t)kp * a.stage_bytes, nx.src, bytes, &bar[kp]);
           vbits |= 1u << kp;
         }
-        nx_ok = (jr + 1 < n) && make_plan<KIND, FP8, RANGED, REV>(g, a, gi + (jr + 1) * G, nx);
+        nx_ok = (jr + 1 < n) && make_plan<KIND, FP8, MODE, REV>(g, a, gi + (jr + 1) * G, nx);
       }
     }
     pdl_trigger();
@@ -273,7 +279,7 @@ __device__ __forceinline__ uint32_t ld_vec<uint32_t>(const uint8_t* p) {
 __device__ __forceinline__ void st_vec(uint8_t* p, const uint4& v) { st16(p, v); }
 __device__ __forceinline__ void st_vec(uint8_t* p, const uint32_t& v) { *reinterpret_cast<uint32_t*>(p) = v; }
 
-template <int KIND, bool FP8, typename V, bool RANGED, bool REV>
+template <int KIND, bool FP8, typename V, int MODE, bool REV>
 __global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
   constexpr int U = 8;
   constexpr int W = (int)sizeof(V);
@@ -288,7 +294,7 @@ __global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
     for (int64_t u0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u0 < a.units; u0 += nwarps) {
       const int64_t u = REV ? a.units - 1 - u0 : u0;
       const int64_t tv = u / a.chunks;
-      const int64_t tok = range_item<RANGED>(g, a, tv, 1);
+      const int64_t tok = range_item<MODE>(g, a, tv, 1);
       const int64_t coff = (u - tv * a.chunks) * (int64_t)a.chunk_bytes;
       const uint8_t* src = a.src + tok * g.B + coff;
       uint8_t* dst0 = a.dst + coff;
@@ -321,7 +327,7 @@ __global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
   }
   for (int64_t u = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < a.units; u += nwarps) {
     Plan pl;
-    if (!make_plan<KIND, FP8, RANGED, REV>(g, a, u, pl)) continue;
+    if (!make_plan<KIND, FP8, MODE, REV>(g, a, u, pl)) continue;
     for (int64_t v0 = lane; v0 < nel; v0 += 32 * U) {
       V r[U];
 #pragma unroll
@@ -348,12 +354,12 @@ __global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
 }
 
 // Largest dynamic shared memory limit set so far, per TMA instantiation and device.
-std::atomic<int> g_tma_smem[8][2][2][2][64];
+std::atomic<int> g_tma_smem[8][2][3][2][64];
 
 // Stages per issuer and CTAs per SM: as many CTAs as fit with 3 stages per issuer (at
 // most 8 CTAs), then as many stages as the shared memory of each CTA holds (2..8). Each
 // CTA also pays 1 KB of reserved shared memory and its mbarrier/plan header.
-template <int KIND, bool FP8, bool RANGED, bool REV>
+template <int KIND, bool FP8, int MODE, bool REV>
 cudaError_t run_tma(const Geo& g, MoveArgs a, Ctx& c) {
   const uint32_t bytes = unit_bytes<KIND>(g, a);
   const int stage_bytes = (int)((bytes + 127u) & ~127u);
@@ -373,8 +379,8 @@ cudaError_t run_tma(const Geo& g, MoveArgs a, Ctx& c) {
   if (S < 2) return cudaErrorInvalidValue;
   const size_t smem = kTmaHeader + (size_t)kIssuers * S * stage_bytes;
   {
-    cudaError_t e = ensure_dyn_smem(k_move_tma<KIND, FP8, RANGED, REV>, c.device, smem,
-                                    g_tma_smem[KIND][FP8 ? 1 : 0][RANGED ? 1 : 0][REV ? 1 : 0]);
+    cudaError_t e = ensure_dyn_smem(k_move_tma<KIND, FP8, MODE, REV>, c.device, smem,
+                                    g_tma_smem[KIND][FP8 ? 1 : 0][MODE][REV ? 1 : 0]);
     if (e != cudaSuccess) return e;
   }
   a.stages = S;
@@ -382,17 +388,17 @@ cudaError_t run_tma(const Geo& g, MoveArgs a, Ctx& c) {
   int64_t grid = (int64_t)c.num_sms * cps;
   const int64_t need = (a.units + kIssuers - 1) / kIssuers;
   if (grid > need) grid = need;
-  return launch_kernel(k_move_tma<KIND, FP8, RANGED, REV>, dim3((unsigned)grid), dim3(kIssuers * 32), smem, c, g, a);
+  return launch_kernel(k_move_tma<KIND, FP8, MODE, REV>, dim3((unsigned)grid), dim3(kIssuers * 32), smem, c, g, a);
 }
 
-template <int KIND, bool FP8, typename V, bool RANGED, bool REV>
+template <int KIND, bool FP8, typename V, int MODE, bool REV>
 cudaError_t run_ldg(const Geo& g, const MoveArgs& a, Ctx& c) {
   // Four waves of the CTAs the SMs hold at once (registers decide): warps that finish early
   // take later units, which measured faster on GB300 than one wave of grid-stride loops.
   static std::atomic<int> resident{0};
   int per_sm = resident.load(std::memory_order_relaxed);
   if (per_sm == 0) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_move_ldg<KIND, FP8, V, RANGED, REV>, 256, 0) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_move_ldg<KIND, FP8, V, MODE, REV>, 256, 0) != cudaSuccess ||
         per_sm < 1)
       per_sm = 1;
     resident.store(per_sm, std::memory_order_relaxed);
@@ -401,7 +407,7 @@ cudaError_t run_ldg(const Geo& g, const MoveArgs& a, Ctx& c) {
   int64_t blocks = (a.units + 7) / 8;
   const int64_t maxb = (int64_t)c.num_sms * per_sm;
   if (blocks > maxb) blocks = maxb;
-  return launch_kernel(k_move_ldg<KIND, FP8, V, RANGED, REV>, dim3((unsigned)blocks), dim3(256), 0, c, g, a);
+  return launch_kernel(k_move_ldg<KIND, FP8, V, MODE, REV>, dim3((unsigned)blocks), dim3(256), 0, c, g, a);
 }
 
 // True when two stages per issuer fit in one CTA's shared memory.
@@ -422,14 +428,14 @@ bool tma_default(const MoveArgs& a, const Ctx& c) {
   return a.units / a.chunks >= 40LL * kIssuers * c.num_sms;
 }
 
-template <int KIND, bool FP8, bool RANGED, bool REV>
+template <int KIND, bool FP8, int MODE, bool REV>
 cudaError_t run_kind(const Geo& g, const MoveArgs& a, Ctx& c, bool row16) {
   const bool want_tma = (c.flags & MOE_FLAG_TMA_MOVER) ? true
                         : (c.flags & MOE_FLAG_LDG_MOVER) ? false
                                                           : tma_default<KIND>(a, c);
-  if (row16 && want_tma && tma_fits<KIND>(g, a, c)) return run_tma<KIND, FP8, RANGED, REV>(g, a, c);
-  if (row16) return run_ldg<KIND, FP8, uint4, RANGED, REV>(g, a, c);
-  return run_ldg<KIND, FP8, uint32_t, RANGED, REV>(g, a, c);
+  if (row16 && want_tma && tma_fits<KIND>(g, a, c)) return run_tma<KIND, FP8, MODE, REV>(g, a, c);
+  if (row16) return run_ldg<KIND, FP8, uint4, MODE, REV>(g, a, c);
+  return run_ldg<KIND, FP8, uint32_t, MODE, REV>(g, a, c);
 }
 
 // Traversal direction. Each intermediate buffer of the pass is written by one move and read
@@ -440,13 +446,13 @@ cudaError_t run_kind(const Geo& g, const MoveArgs& a, Ctx& c, bool row16) {
 // backward, combine scatter forward. With direct push the pack writes the receive rows
 // forward, so the unpack and the identity expert run backward and the combine push forward.
 // Only the order in which independent rows are copied changes, never a value.
-template <int KIND, bool FP8, bool RANGED>
+template <int KIND, bool FP8, int MODE>
 cudaError_t run_dir(const Geo& g, const MoveArgs& a, Ctx& c, bool row16) {
   if constexpr (KIND == kMoveUnpack || KIND == kMoveCopyEx) {
-    if (c.flags & MOE_FLAG_DIRECT_PUSH) return run_kind<KIND, FP8, RANGED, true>(g, a, c, row16);
-    return run_kind<KIND, FP8, RANGED, false>(g, a, c, row16);
+    if (c.flags & MOE_FLAG_DIRECT_PUSH) return run_kind<KIND, FP8, MODE, true>(g, a, c, row16);
+    return run_kind<KIND, FP8, MODE, false>(g, a, c, row16);
   } else {
-    return run_kind<KIND, FP8, RANGED, KIND == kMoveScatter || KIND == kMoveCPack>(g, a, c, row16);
+    return run_kind<KIND, FP8, MODE, KIND == kMoveScatter || KIND == kMoveCPack>(g, a, c, row16);
   }
 }
 
@@ -454,7 +460,7 @@ cudaError_t run_dir(const Geo& g, const MoveArgs& a, Ctx& c, bool row16) {
 
 namespace {
 
-template <bool R>
+template <int R>
 cudaError_t run_move(MoveKind kind, const Geo& g, const MoveArgs& a, Ctx& c, bool fp8, bool rowB16) {
   switch (kind) {
     case kMovePack:
@@ -556,7 +562,7 @@ cudaError_t launch_move_window(MoveKind kind, const Geo& g, const moe_layout_t* 
                                       MOE_K_COMBINE_PACK, MOE_K_COMBINE_SCATTER, MOE_K_EXPERT,
                                       MOE_K_PACK_PUSH,    MOE_K_COMBINE_PUSH};
   LaunchScope ls(c, ids[kind]);
-  return run_move<false>(kind, gg, a, c, fp8, (g.B % 16) == 0);
+  return run_move<2>(kind, gg, a, c, fp8, (g.B % 16) == 0);
 }
 
 }  // namespace
@@ -628,7 +634,7 @@ cudaError_t launch_move_range(MoveKind kind, const Geo& g, const moe_layout_t* l
                                       MOE_K_COMBINE_PACK, MOE_K_COMBINE_SCATTER, MOE_K_EXPERT,
                                       MOE_K_PACK_PUSH,    MOE_K_COMBINE_PUSH};
   LaunchScope ls(c, ids[kind]);
-  return nt != g.T ? run_move<true>(kind, g, a, c, fp8, rowB16) : run_move<false>(kind, g, a, c, fp8, rowB16);
+  return nt != g.T ? run_move<1>(kind, g, a, c, fp8, rowB16) : run_move<0>(kind, g, a, c, fp8, rowB16);
 }
 
 }  // namespace moe
