@@ -44,6 +44,10 @@ def test_exchange_plan_against_oracle_buffers(orc, wl, G):
     """Every remote (s, d) slice is listed once by its sender and once by its receiver, with
     C[s][d] rows at the window-local rows where the oracle's send, receive, combine-send and
     combine-receive buffers hold that slice; local slices are listed by no one."""
+    _check_plan(orc, wl, G)
+
+
+def _check_plan(orc, wl, G):
     from combine_routing_count_gb300.sharded import exchange_plan, window_bounds
     inp = workloads.make_inputs(wl)
     o = _oracle(orc, wl, inp)
@@ -147,3 +151,24 @@ def test_sharded_exchange_gloo_two_ranks(wl_i):
     got = sorted(q.get(timeout=10) for _ in range(2))
     assert [g[0] for g in got] == [0, 1] and all(g[1] for g in got)
     assert sum(g[2] for g in got) > 0   # slices crossed windows
+
+
+def _fuzz_plan_cases(n, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        N = int(rng.integers(1, 10))
+        L = int(rng.integers(1, 5))
+        R = int(rng.integers(1, min(6, N * L) + 1))
+        T = int(rng.integers(0, 12))
+        routing = str(rng.choice(["uniform", "zipf"]))
+        G = int(rng.integers(1, N + 1))
+        out.append((workloads.Workload(f"pfuzz{i}-N{N}-G{G}", N, T, 64, N * L, R, "bf16", routing, 800 + i), G))
+    return out
+
+
+@pytest.mark.parametrize("wl,G", _fuzz_plan_cases(40, 91), ids=lambda v: v.name if hasattr(v, "name") else str(v))
+def test_fuzz_exchange_plan(orc, wl, G):
+    """Random shapes and window counts (including empty batches and one-rank windows): the
+    plan's slices are exactly the remote (s, d) pairs with rows, with matching rows and order."""
+    _check_plan(orc, wl, G)
