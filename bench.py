@@ -54,7 +54,8 @@ import workloads  # noqa: E402
 METRIC = "dispatch+combine tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 KERNELS = ["route_count", "layout_maps", "quant_fp8", "pack", "scatter", "unpack", "expert",
            "combine_pack", "combine_scatter", "combine_reduce", "route_scan", "pack_push", "combine_push",
-           "combine_partial", "combine_sum", "dispatch_split", "quant_pack", "dispatch_dedicated"]
+           "combine_partial", "combine_sum", "dispatch_split", "quant_pack", "dispatch_dedicated", "scatter_unpack",
+           "combine_pack_scatter"]
 HEADLINE_CONFIG = 4          # the largest workload: the line's top level
 OTHER_CONFIGS = (1, 2, 3)    # measured in the same run, reported under per_config
 L2_NOTE = "flushed before every timed step (write of 2x L2, then read of 2x L2)"
@@ -82,6 +83,9 @@ def parse_args(argv=None):
                    help="token batches of the batched passes (0: the library's automatic choice)")
     p.add_argument("--one-batch", action="store_true",
                    help="run moe_forward (and the host pass) as one token batch instead of micro-batches")
+    p.add_argument("--separate-moves", action="store_true",
+                   help="run the scatter and unpack, and the combine pack and scatter, as separate kernels "
+                        "(MOE_FLAG_SEPARATE_MOVES) instead of the fused moves")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="CPU work for the oracle baseline of the top-level workload (single thread, then "
@@ -227,6 +231,8 @@ def algorithmic_bytes(wl: workloads.Workload, P: int, Pk: int) -> dict:
         "combine_push": 2 * Pk * 2 * H,
         "dispatch_split": tok * B + P * B + 2 * Pk * B,
         "dispatch_dedicated": tok * B + P * B + 2 * Pk * B,
+        "scatter_unpack": 2 * P * B + Pk * B,
+        "combine_pack_scatter": 3 * Pk * 2 * H,
     }
 
 
@@ -363,7 +369,8 @@ def measure(wl, args, dist, device, peak: float, peak_kind: str, cpu_seconds: fl
     inp = workloads.make_inputs(wl)
     ep = MoeEP(wl.N, wl.T, wl.H, wl.E, wl.R, wl.cap, wl.payload, alias_buffers=(wl.payload == "bf16"),
                flags={"auto": 0, "ldg": 1, "tma": 4}[args.mover] | (2 if args.no_pdl else 0) |
-               (0x10 if args.staged_quant else 0) | (0x40 if args.one_batch else 0), tma_stages=args.tma_stages,
+               (0x10 if args.staged_quant else 0) | (0x40 if args.one_batch else 0) |
+               (0x80 if args.separate_moves else 0), tma_stages=args.tma_stages,
                ctas_per_sm=args.ctas_per_sm, batches=args.batches)
     x = torch.from_numpy(inp["x"]).view(torch.bfloat16).to(device)
     idx = torch.from_numpy(inp["idx"]).to(device)
@@ -572,8 +579,13 @@ def measure(wl, args, dist, device, peak: float, peak_kind: str, cpu_seconds: fl
     flags0 = ep.layout.flags
     ep.layout.flags = flags0 | 0x40
     one_ms, _, _ = step_region()
+    # the same step with the four moves apart (MOE_FLAG_SEPARATE_MOVES, or without it when
+    # the run asked for separate moves), reported beside the default
+    ep.layout.flags = flags0 ^ 0x80
+    other_ms, _, _ = step_region()
     ep.layout.flags = flags0
     one_ms_all = max_over_ranks(one_ms, dist, device)
+    other_ms_all = max_over_ranks(other_ms, dist, device)
     mean_ms_all = max_over_ranks(mean_ms, dist, device)
     tokens = wl.N * wl.T * ws
     value = tokens / (mean_ms_all * 1e-3)
@@ -804,6 +816,11 @@ def measure(wl, args, dist, device, peak: float, peak_kind: str, cpu_seconds: fl
                       "ms_per_step": round(one_ms_all, 4),
                       "note": "the same step as one token batch (MOE_FLAG_ONE_BATCH): identical results; "
                               "the default splits it into token batches over two streams"},
+        ("fused_moves" if args.separate_moves else "separate_moves"): {
+            "value": round(tokens / (other_ms_all * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(other_ms_all, 4),
+            "note": "the same step with the dispatch's scatter and unpack, and the combine's pack and scatter, "
+                    + ("fused (the default)" if args.separate_moves else
+                       "as separate kernels (MOE_FLAG_SEPARATE_MOVES); identical results")},
         "forward_with_expert": None if fwd_ms is None else {
             "value": round(tokens / (fwd_ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(fwd_ms, 4),
             "micro_batches": fwd_batches,
@@ -829,8 +846,8 @@ def compact(r: dict) -> dict:
     c["roofline"] = {k: v for k, v in r["roofline"].items() if k != "launch"}
     c["e2e"] = {k: r["e2e"][k] for k in ("value", "unit", "ms_per_step", "h2d_bytes_per_step",
                                          "d2h_bytes_per_step", "batches", "out_equals_device_path")}
-    for k in ("one_batch", "direct_push", "sender_side_combine", "split_phase_dispatch", "split_phase_dedicated",
-              "forward_with_expert", "identity_expert"):
+    for k in ("one_batch", "separate_moves", "fused_moves", "direct_push", "sender_side_combine",
+              "split_phase_dispatch", "split_phase_dedicated", "forward_with_expert", "identity_expert"):
         if r.get(k) is not None:
             c[k] = {kk: vv for kk, vv in r[k].items() if kk not in ("note", "path")}
     return c

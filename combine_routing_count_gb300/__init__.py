@@ -15,13 +15,14 @@ import torch
 
 from . import _abi
 from ._abi import (MOE_FLAG_DIRECT_PUSH, MOE_FLAG_ONE_BATCH, MOE_FLAG_HOST_MAPPED, MOE_FLAG_LDG_MOVER,
-                   MOE_FLAG_NO_PDL, MOE_FLAG_STAGED_QUANT,
+                   MOE_FLAG_NO_PDL, MOE_FLAG_SEPARATE_MOVES, MOE_FLAG_STAGED_QUANT,
                    MOE_FLAG_TMA_MOVER, MOE_PAYLOAD_BF16, MOE_PAYLOAD_FP8_E4M3_B128, KERNEL_NAMES, MoeBuffers,
                    MoeDims, MoeError, MoeLayout, MoeProf, check, lib)
 
 __all__ = ["MoeEP", "MoeDims", "MoeLayout", "MoeBuffers", "MoeProf", "MoeError", "lib", "check",
            "MOE_FLAG_LDG_MOVER", "MOE_FLAG_NO_PDL", "MOE_FLAG_TMA_MOVER", "MOE_FLAG_DIRECT_PUSH",
-           "MOE_FLAG_STAGED_QUANT", "MOE_FLAG_HOST_MAPPED", "MOE_FLAG_ONE_BATCH", "KERNEL_NAMES"]
+           "MOE_FLAG_STAGED_QUANT", "MOE_FLAG_HOST_MAPPED", "MOE_FLAG_ONE_BATCH", "MOE_FLAG_SEPARATE_MOVES",
+           "KERNEL_NAMES"]
 
 
 def _ptr(t) -> int | None:

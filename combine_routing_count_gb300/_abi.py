@@ -25,11 +25,13 @@ MOE_FLAG_DIRECT_PUSH = 0x8
 MOE_FLAG_STAGED_QUANT = 0x10
 MOE_FLAG_HOST_MAPPED = 0x20
 MOE_FLAG_ONE_BATCH = 0x40
+MOE_FLAG_SEPARATE_MOVES = 0x80
 MOE_PROF_MAX = 32
 
 KERNEL_NAMES = ["route_count", "layout_maps", "quant_fp8", "pack", "scatter", "unpack", "expert",
                 "combine_pack", "combine_scatter", "combine_reduce", "route_scan", "pack_push", "combine_push",
-                "combine_partial", "combine_sum", "dispatch_split", "quant_pack", "dispatch_dedicated"]
+                "combine_partial", "combine_sum", "dispatch_split", "quant_pack", "dispatch_dedicated",
+                "scatter_unpack", "combine_pack_scatter"]
 
 LAYOUT_FIELDS = ("cnt", "C", "soff", "roff", "rtot", "ecnt", "eoff", "pos", "rrow", "slot", "slot_src",
                  "recv_src", "gsend", "grecv", "gslot", "status", "scratch")

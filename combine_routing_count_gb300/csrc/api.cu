@@ -291,6 +291,31 @@ using namespace moe;
 namespace moe {
 namespace {
 
+// Dispatch: the send rows of the token range [t0, t0 + nt) of every rank written to their
+// owners' receive rows and shuffled into the grouped rows, by one fused move (each send row
+// read once) unless MOE_FLAG_SEPARATE_MOVES asks for the scatter and the unpack apart.
+cudaError_t dispatch_recv_range(const Geo& g, const moe_layout_t* lay, const void* send, void* recv, void* ex,
+                                float* exs, int t0, int nt, Ctx& c) {
+  const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
+  if (!(c.flags & MOE_FLAG_SEPARATE_MOVES))
+    return launch_move_range(kMoveScatterUnpack, g, lay, send, recv, ex, t0, nt, c, fp8 ? exs : nullptr);
+  cudaError_t e = launch_move_range(kMoveScatter, g, lay, send, recv, nullptr, t0, nt, c);
+  if (e == cudaSuccess) e = launch_move_range(kMoveUnpack, g, lay, recv, ex, fp8 ? exs : nullptr, t0, nt, c);
+  return e;
+}
+
+// Combine: the expert output rows of the pairs of the token range [t0, t0 + nt) of every
+// rank written in receive order and back to their sources' combine rows, by one fused move
+// unless MOE_FLAG_SEPARATE_MOVES asks for the combine pack and scatter apart.
+cudaError_t combine_send_range(const Geo& g, const moe_layout_t* lay, const uint16_t* ey, uint16_t* csend,
+                               uint16_t* crecv, int t0, int nt, Ctx& c) {
+  if (!(c.flags & MOE_FLAG_SEPARATE_MOVES))
+    return launch_move_range(kMoveCPackScatter, g, lay, ey, csend, crecv, t0, nt, c);
+  cudaError_t e = launch_move_range(kMoveCPack, g, lay, ey, csend, nullptr, t0, nt, c);
+  if (e == cudaSuccess) e = launch_move_range(kMoveCScatter, g, lay, csend, crecv, nullptr, t0, nt, c);
+  return e;
+}
+
 // The whole pass in two token batches (tokens [0, T/2) and [T/2, T) of every rank) so that
 // the host-link-bound kernels of one batch overlap the HBM-bound moves of the other: the
 // pack of batch B (reading tokens over the host link) runs while batch A is scattered and
@@ -315,15 +340,10 @@ moe_status forward_two_batches(const Geo& g, const moe_dims* dims, const moe_lay
                : launch_move_range(kMovePack, g, lay, b->x, b->send, nullptr, t0, nt, c);
   };
   auto recv_half = [&](int t0, int nt, Ctx& cc) {
-    cudaError_t e = launch_move_range(kMoveScatter, g, lay, b->send, b->recv, nullptr, t0, nt, cc);
-    if (e == cudaSuccess)
-      e = launch_move_range(kMoveUnpack, g, lay, b->recv, b->expert_x, fp8 ? b->expert_scale : nullptr, t0, nt, cc);
-    return e;
+    return dispatch_recv_range(g, lay, b->send, b->recv, b->expert_x, b->expert_scale, t0, nt, cc);
   };
   auto combine_send_half = [&](int t0, int nt) {
-    cudaError_t e = launch_move_range(kMoveCPack, g, lay, b->expert_y, b->csend, nullptr, t0, nt, c);
-    if (e == cudaSuccess) e = launch_move_range(kMoveCScatter, g, lay, b->csend, b->crecv, nullptr, t0, nt, c);
-    return e;
+    return combine_send_range(g, lay, b->expert_y, b->csend, b->crecv, t0, nt, c);
   };
   if (pack(0, ta) != cudaSuccess || !fork_to(di, c.stream) || pack(ta, tb) != cudaSuccess ||
       recv_half(0, ta, ca) != cudaSuccess || recv_half(ta, tb, c) != cudaSuccess || !join_from(di, c.stream))
@@ -352,7 +372,8 @@ cudaError_t dispatch_range(const Geo& g, const moe_layout_t* lay, const void* x,
     e = fp8 ? launch_quant_pack(g, lay->gsend, static_cast<const uint16_t*>(x), static_cast<uint8_t*>(send), c, t0,
                                 nt)
             : launch_move_range(kMovePack, g, lay, x, send, nullptr, t0, nt, c);
-    if (e == cudaSuccess) e = launch_move_range(kMoveScatter, g, lay, send, recv, nullptr, t0, nt, c);
+    if (e == cudaSuccess) e = dispatch_recv_range(g, lay, send, recv, ex, exs, t0, nt, c);
+    return e;
   }
   if (e == cudaSuccess) e = launch_move_range(kMoveUnpack, g, lay, recv, ex, fp8 ? exs : nullptr, t0, nt, c);
   return e;
@@ -366,8 +387,7 @@ cudaError_t combine_range(const Geo& g, const moe_layout_t* lay, const uint16_t*
   if (c.flags & MOE_FLAG_DIRECT_PUSH) {
     e = launch_move_range(kMoveCPush, g, lay, ey, crecv, nullptr, t0, nt, c);
   } else {
-    e = launch_move_range(kMoveCPack, g, lay, ey, csend, nullptr, t0, nt, c);
-    if (e == cudaSuccess) e = launch_move_range(kMoveCScatter, g, lay, csend, crecv, nullptr, t0, nt, c);
+    e = combine_send_range(g, lay, ey, csend, crecv, t0, nt, c);
   }
   if (e == cudaSuccess) e = launch_combine_reduce(g, lay, crecv, w, out, c, t0, nt);
   return e;
@@ -883,8 +903,11 @@ moe_status moe_forward(const moe_dims* dims, const moe_layout_t* lay, const moe_
        (fp8 && (lay->flags & MOE_FLAG_STAGED_QUANT) && (!b->xq || !aligned16(b->xq)))))
     return MOE_ERR_INVALID_ARG;
   {
+    // One or more token batches of the whole chain; staged fp8 quantisation runs as a
+    // separate pass over all tokens first, so it takes the phase by phase path below.
     const int nb = moe_batches(dims, lay, 0);
-    if (nb > 1) return forward_batched(g, dims, lay, b, nb, stream);
+    const bool staged = fp8 && (lay->flags & MOE_FLAG_STAGED_QUANT);
+    if (nb > 1 || ((int64_t)g.N * g.T > 0 && !staged)) return forward_batched(g, dims, lay, b, nb, stream);
   }
   if ((st = moe_layout(dims, b->idx, lay, stream)) != MOE_OK) return st;
   if (fp8 && !(lay->flags & MOE_FLAG_STAGED_QUANT)) {

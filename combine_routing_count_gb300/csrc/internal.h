@@ -132,13 +132,17 @@ enum MoveKind : int {
   kMoveCopyEx = 5,    // grouped rows -> grouped rows (bf16 identity expert, distinct output)
   kMovePackPush = 6,  // direct push: token rows -> R receive rows of the owner ranks
   kMoveCPush = 7,     // direct push: grouped expert output rows -> source ranks' combine rows
+  kMoveScatterUnpack = 8,  // scatter and unpack in one move: send row -> receive row and grouped row
+  kMoveCPackScatter = 9,   // combine pack and scatter in one move: grouped output row -> receive-
+                           // order row and the source's combine row
 };
 cudaError_t launch_move(MoveKind kind, const Geo& g, const moe_layout_t* lay, const void* src, void* dst,
-                        void* dst2, Ctx& c);
+                        void* dst2, Ctx& c, void* dst3 = nullptr);
 // The same move over the token range [t0, t0 + nt) of every rank only (its tokens for a
 // pack, its pairs otherwise).
+// dst3: the fp8 scales of kMoveScatterUnpack (dst2 its codes); unused otherwise.
 cudaError_t launch_move_range(MoveKind kind, const Geo& g, const moe_layout_t* lay, const void* src, void* dst,
-                              void* dst2, int t0, int nt, Ctx& c);
+                              void* dst2, int t0, int nt, Ctx& c, void* dst3 = nullptr);
 
 // numerics.cu
 cudaError_t launch_quant_fp8(const Geo& g, const uint16_t* x, uint8_t* xq, Ctx& c);

@@ -32,6 +32,7 @@ struct MoveArgs {
   const uint8_t* src;
   uint8_t* dst;
   uint8_t* dst2;
+  uint8_t* dst3;          // the fp8 scales of the fused scatter-and-unpack
   const int32_t* gsend;   // per pair: global send row, or -1
   const int32_t* grecv;   // per pair: global receive row, or -1
   const int32_t* gslot;   // per pair: global grouped row, or -1
@@ -60,6 +61,7 @@ struct Plan {
   const uint8_t* src;
   uint8_t* dst;
   uint8_t* dst2;
+  uint8_t* dst3;
   int64_t tok;                 // pack: token index s*T+t
   int32_t coff;                // pack: byte offset of the chunk in the row
   int32_t p[kPackPrefetch];    // pack: global send rows of the token's pairs
@@ -112,6 +114,35 @@ __device__ __forceinline__ bool make_plan(const Geo& g, const MoveArgs& a, int64
     if (gs < 0 || dst_outside<MODE>(a, gr)) return false;
     pl.src = a.src + (int64_t)gs * g.B + coff;
     pl.dst = a.dst + (int64_t)gr * g.B + coff;
+    return true;
+  }
+  if (KIND == kMoveScatterUnpack) {   // the receive row, and the grouped row if the pair is kept
+    const int gs = __ldg(a.gsend + u);
+    const int gr = __ldg(a.grecv + u);
+    const int gl = __ldg(a.gslot + u);
+    if (gs < 0) return false;
+    pl.src = a.src + (int64_t)gs * g.B + coff;
+    pl.dst = a.dst + (int64_t)gr * g.B + coff;
+    pl.dst2 = nullptr;
+    pl.dst3 = nullptr;
+    if (gl >= 0) {
+      if (FP8) {   // dst3: the scale row, less the codes' length (the row's offset of the scales)
+        pl.dst2 = a.dst2 + (int64_t)gl * g.H;
+        pl.dst3 = a.dst3 + (int64_t)gl * (g.H / 32) - g.H;
+      } else {
+        pl.dst2 = a.dst2 + (int64_t)gl * g.B + coff;
+      }
+    }
+    return true;
+  }
+  if (KIND == kMoveCPackScatter) {   // receive-order row and the source's combine row
+    const int gl = __ldg(a.gslot + u);
+    const int gr = __ldg(a.grecv + u);
+    const int gs = __ldg(a.gsend + u);
+    if (gl < 0) return false;
+    pl.src = a.src + (int64_t)gl * H2 + coff;
+    pl.dst = a.dst + (int64_t)gr * H2 + coff;
+    pl.dst2 = a.dst2 + (int64_t)gs * H2 + coff;
     return true;
   }
   if (KIND == kMoveCopyEx) {
@@ -170,6 +201,19 @@ __device__ __forceinline__ void issue_stores(const Geo& g, const MoveArgs& a, co
   } else if (KIND == kMoveUnpack && FP8) {
     bulk_s2g(pl.dst, stage, (uint32_t)g.H);
     bulk_s2g(pl.dst2, stage + g.H, (uint32_t)(g.H / 32));
+  } else if (KIND == kMoveScatterUnpack) {
+    bulk_s2g(pl.dst, stage, bytes);
+    if (pl.dst2) {
+      if (FP8) {
+        bulk_s2g(pl.dst2, stage, (uint32_t)g.H);
+        bulk_s2g(pl.dst3 + g.H, stage + g.H, (uint32_t)(g.H / 32));
+      } else {
+        bulk_s2g(pl.dst2, stage, bytes);
+      }
+    }
+  } else if (KIND == kMoveCPackScatter) {
+    bulk_s2g(pl.dst, stage, bytes);
+    bulk_s2g(pl.dst2, stage, bytes);
   } else {
     bulk_s2g(pl.dst, stage, bytes);
   }
@@ -183,6 +227,7 @@ constexpr int kTmaHeader = kIssuers * kMaxStages * (8 + 128);  // mbarriers + pl
 struct StagePlan {
   uint8_t* dst;
   uint8_t* dst2;
+  uint8_t* dst3;
   int64_t tok;
   int32_t coff;
   int32_t p[kPackPrefetch];
@@ -213,7 +258,7 @@ __global__ void __launch_bounds__(kIssuers * 32) k_move_tma(Geo g, MoveArgs a) {
     Plan pl;
     for (int k = 0; k < S && k < n; ++k) {
       const bool ok = make_plan<KIND, FP8, MODE, REV>(g, a, gi + k * G, pl);
-      sp[k] = StagePlan{pl.dst, pl.dst2, pl.tok, pl.coff, {}};
+      sp[k] = StagePlan{pl.dst, pl.dst2, pl.dst3, pl.tok, pl.coff, {}};
       if (KIND == kMovePack || KIND == kMovePackPush)
         for (int r = 0; r < kPackPrefetch; ++r) sp[k].p[r] = pl.p[r];
       if (ok) {
@@ -233,6 +278,7 @@ __global__ void __launch_bounds__(kIssuers * 32) k_move_tma(Geo g, MoveArgs a) {
         Plan cur;
         cur.dst = sp[k].dst;
         cur.dst2 = sp[k].dst2;
+        cur.dst3 = sp[k].dst3;
         cur.tok = sp[k].tok;
         cur.coff = sp[k].coff;
         if (KIND == kMovePack || KIND == kMovePackPush)
@@ -250,7 +296,7 @@ __global__ void __launch_bounds__(kIssuers * 32) k_move_tma(Geo g, MoveArgs a) {
         else
           bulk_wait_read_all();
         vbits &= ~(1u << kp);
-        sp[kp] = StagePlan{nx.dst, nx.dst2, nx.tok, nx.coff, {}};
+        sp[kp] = StagePlan{nx.dst, nx.dst2, nx.dst3, nx.tok, nx.coff, {}};
         if (KIND == kMovePack || KIND == kMovePackPush)
           for (int r = 0; r < kPackPrefetch; ++r) sp[kp].p[r] = nx.p[r];
         if (nx_ok) {
@@ -280,13 +326,13 @@ __device__ __forceinline__ void st_vec(uint8_t* p, const uint4& v) { st16(p, v);
 __device__ __forceinline__ void st_vec(uint8_t* p, const uint32_t& v) { *reinterpret_cast<uint32_t*>(p) = v; }
 
 template <int KIND, bool FP8, typename V, int MODE, bool REV>
-__global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
+__device__ __forceinline__ void move_ldg(const Geo& g, const MoveArgs& a) {
   constexpr int U = 8;
   constexpr int W = (int)sizeof(V);
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int64_t nel = unit_bytes<KIND>(g, a) / W;
-  const int64_t split = (KIND == kMoveUnpack && FP8) ? g.H / W : nel;
+  const int64_t split = ((KIND == kMoveUnpack || KIND == kMoveScatterUnpack) && FP8) ? g.H / W : nel;
   pdl_wait();
   if (KIND == kMovePack || KIND == kMovePackPush) {
     // Pack: lane k holds the destination row of the token's pair k and broadcasts it by
@@ -344,6 +390,14 @@ __global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
             st_vec(pl.dst + v * W, r[j]);
           else
             st_vec(pl.dst2 + (v - split) * W, r[j]);
+        } else if (KIND == kMoveScatterUnpack) {
+          st_vec(pl.dst + v * W, r[j]);
+          // fp8: codes to dst2, the scales that follow them in the row to dst3 (pl.dst3 was
+          // moved back by the codes' length in the plan, so both take offset v * W)
+          if (pl.dst2) st_vec(((!FP8 || v < split) ? pl.dst2 : pl.dst3) + v * W, r[j]);
+        } else if (KIND == kMoveCPackScatter) {
+          st_vec(pl.dst + v * W, r[j]);
+          st_vec(pl.dst2 + v * W, r[j]);
         } else {
           st_vec(pl.dst + v * W, r[j]);
         }
@@ -353,8 +407,29 @@ __global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
   pdl_trigger();
 }
 
+template <int KIND, bool FP8, typename V, int MODE, bool REV>
+__global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
+  move_ldg<KIND, FP8, V, MODE, REV>(g, a);
+}
+
+// The fused kinds hold two or three store pointers per row: without a bound the bf16 ones
+// take 72-76 registers, three CTAs of 256 threads per SM instead of four. The fp8
+// scatter-and-unpack would spill at 64 and keeps three.
+template <int KIND, bool FP8, typename V, int MODE, bool REV>
+__global__ void __launch_bounds__(256, FP8 ? 3 : 4) k_move_ldg_fused(Geo g, MoveArgs a) {
+  move_ldg<KIND, FP8, V, MODE, REV>(g, a);
+}
+
+template <int KIND, bool FP8, typename V, int MODE, bool REV>
+constexpr auto ldg_kernel() {
+  if constexpr (KIND == kMoveScatterUnpack || KIND == kMoveCPackScatter)
+    return k_move_ldg_fused<KIND, FP8, V, MODE, REV>;
+  else
+    return k_move_ldg<KIND, FP8, V, MODE, REV>;
+}
+
 // Largest dynamic shared memory limit set so far, per TMA instantiation and device.
-std::atomic<int> g_tma_smem[8][2][3][2][64];
+std::atomic<int> g_tma_smem[10][2][3][2][64];
 
 // Stages per issuer and CTAs per SM: as many CTAs as fit with 3 stages per issuer (at
 // most 8 CTAs), then as many stages as the shared memory of each CTA holds (2..8). Each
@@ -398,7 +473,8 @@ cudaError_t run_ldg(const Geo& g, const MoveArgs& a, Ctx& c) {
   static std::atomic<int> resident{0};
   int per_sm = resident.load(std::memory_order_relaxed);
   if (per_sm == 0) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_move_ldg<KIND, FP8, V, MODE, REV>, 256, 0) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ldg_kernel<KIND, FP8, V, MODE, REV>(), 256, 0) !=
+            cudaSuccess ||
         per_sm < 1)
       per_sm = 1;
     resident.store(per_sm, std::memory_order_relaxed);
@@ -407,7 +483,7 @@ cudaError_t run_ldg(const Geo& g, const MoveArgs& a, Ctx& c) {
   int64_t blocks = (a.units + 7) / 8;
   const int64_t maxb = (int64_t)c.num_sms * per_sm;
   if (blocks > maxb) blocks = maxb;
-  return launch_kernel(k_move_ldg<KIND, FP8, V, MODE, REV>, dim3((unsigned)blocks), dim3(256), 0, c, g, a);
+  return launch_kernel(ldg_kernel<KIND, FP8, V, MODE, REV>(), dim3((unsigned)blocks), dim3(256), 0, c, g, a);
 }
 
 // True when two stages per issuer fit in one CTA's shared memory.
@@ -443,8 +519,10 @@ cudaError_t run_kind(const Geo& g, const MoveArgs& a, Ctx& c, bool row16) {
 // the rows the producer wrote last, which are still in L2 (at 8K pairs of 14 KB rows,
 // about 117 MB a buffer against 129 MB of L2). Pair-ordered moves therefore alternate:
 // pack forward, scatter backward, unpack forward, identity expert forward, combine pack
-// backward, combine scatter forward. With direct push the pack writes the receive rows
-// forward, so the unpack and the identity expert run backward and the combine push forward.
+// backward, combine scatter forward; the fused scatter-and-unpack and combine pack-and-scatter
+// run backward, as the scatter and the combine pack they stand for. With direct push the pack
+// writes the receive rows forward, so the unpack and the identity expert run backward and the
+// combine push forward.
 // Only the order in which independent rows are copied changes, never a value.
 template <int KIND, bool FP8, int MODE>
 cudaError_t run_dir(const Geo& g, const MoveArgs& a, Ctx& c, bool row16) {
@@ -452,7 +530,9 @@ cudaError_t run_dir(const Geo& g, const MoveArgs& a, Ctx& c, bool row16) {
     if (c.flags & MOE_FLAG_DIRECT_PUSH) return run_kind<KIND, FP8, MODE, true>(g, a, c, row16);
     return run_kind<KIND, FP8, MODE, false>(g, a, c, row16);
   } else {
-    return run_kind<KIND, FP8, MODE, KIND == kMoveScatter || KIND == kMoveCPack>(g, a, c, row16);
+    constexpr bool kRev = KIND == kMoveScatter || KIND == kMoveCPack || KIND == kMoveScatterUnpack ||
+                          KIND == kMoveCPackScatter;
+    return run_kind<KIND, FP8, MODE, kRev>(g, a, c, row16);
   }
 }
 
@@ -462,6 +542,9 @@ namespace {
 
 template <int R>
 cudaError_t run_move(MoveKind kind, const Geo& g, const MoveArgs& a, Ctx& c, bool fp8, bool rowB16) {
+  if constexpr (R == 2) {   // the fused moves are whole-group moves only
+    if (kind == kMoveScatterUnpack || kind == kMoveCPackScatter) return cudaErrorInvalidValue;
+  }
   switch (kind) {
     case kMovePack:
       return run_dir<kMovePack, false, R>(g, a, c, rowB16);
@@ -479,6 +562,14 @@ cudaError_t run_move(MoveKind kind, const Geo& g, const MoveArgs& a, Ctx& c, boo
       return run_dir<kMovePackPush, false, R>(g, a, c, rowB16);
     case kMoveCPush:
       return run_dir<kMoveCPush, false, R>(g, a, c, true);
+    case kMoveScatterUnpack:
+      if constexpr (R != 2)
+        return fp8 ? run_dir<kMoveScatterUnpack, true, R>(g, a, c, rowB16)
+                   : run_dir<kMoveScatterUnpack, false, R>(g, a, c, rowB16);
+      break;
+    case kMoveCPackScatter:
+      if constexpr (R != 2) return run_dir<kMoveCPackScatter, false, R>(g, a, c, true);
+      break;
   }
   return cudaErrorInvalidValue;
 }
@@ -559,8 +650,7 @@ cudaError_t launch_move_window(MoveKind kind, const Geo& g, const moe_layout_t* 
   }
   if (a.units == 0) return cudaSuccess;
   static const moe_kernel_id ids[] = {MOE_K_PACK,         MOE_K_SCATTER,         MOE_K_UNPACK,
-                                      MOE_K_COMBINE_PACK, MOE_K_COMBINE_SCATTER, MOE_K_EXPERT,
-                                      MOE_K_PACK_PUSH,    MOE_K_COMBINE_PUSH};
+                                      MOE_K_COMBINE_PACK, MOE_K_COMBINE_SCATTER, MOE_K_EXPERT};
   LaunchScope ls(c, ids[kind]);
   return run_move<2>(kind, gg, a, c, fp8, (g.B % 16) == 0);
 }
@@ -568,16 +658,17 @@ cudaError_t launch_move_window(MoveKind kind, const Geo& g, const moe_layout_t* 
 }  // namespace
 
 cudaError_t launch_move(MoveKind kind, const Geo& g, const moe_layout_t* lay, const void* src, void* dst, void* dst2,
-                        Ctx& c) {
-  return launch_move_range(kind, g, lay, src, dst, dst2, 0, g.T, c);
+                        Ctx& c, void* dst3) {
+  return launch_move_range(kind, g, lay, src, dst, dst2, 0, g.T, c, dst3);
 }
 
 cudaError_t launch_move_range(MoveKind kind, const Geo& g, const moe_layout_t* lay, const void* src, void* dst,
-                              void* dst2, int t0, int nt, Ctx& c) {
+                              void* dst2, int t0, int nt, Ctx& c, void* dst3) {
   MoveArgs a;
   a.src = static_cast<const uint8_t*>(src);
   a.dst = static_cast<uint8_t*>(dst);
   a.dst2 = static_cast<uint8_t*>(dst2);
+  a.dst3 = static_cast<uint8_t*>(dst3);
   a.gsend = lay->gsend;
   a.grecv = lay->grecv;
   a.gslot = lay->gslot;
@@ -616,8 +707,10 @@ cudaError_t launch_move_range(MoveKind kind, const Geo& g, const moe_layout_t* l
     // issuer slot of the TMA ring, so that each issuer keeps more (smaller) rows in flight
     // (measured on micro-batches of 2048 pairs: 14 KB rows 6% faster halved, 8 KB rows 4.5%
     // slower). The fp8 receive split (codes | scales) is never chunked.
-    const int64_t rowb = (kind == kMoveScatter || kind == kMoveUnpack) ? g.B : 2 * (int64_t)g.H;
-    const bool splittable = !(kind == kMoveUnpack && fp8) && rowb >= 12288 && rowb % 32 == 0;
+    const bool recv_rows = kind == kMoveScatter || kind == kMoveUnpack || kind == kMoveScatterUnpack;
+    const int64_t rowb = recv_rows ? g.B : 2 * (int64_t)g.H;
+    const bool splittable =
+        !((kind == kMoveUnpack || kind == kMoveScatterUnpack) && fp8) && rowb >= 12288 && rowb % 32 == 0;
     const int64_t pairs = nt == g.T ? g.P : (int64_t)g.N * nt * g.R;   // of this launch
     if (splittable && pairs < 32LL * 4 * c.num_sms) a.chunks = 2;
     a.chunk_bytes = (uint32_t)(rowb / a.chunks);
@@ -632,7 +725,8 @@ cudaError_t launch_move_range(MoveKind kind, const Geo& g, const moe_layout_t* l
   if (a.units == 0) return cudaSuccess;
   static const moe_kernel_id ids[] = {MOE_K_PACK,         MOE_K_SCATTER,         MOE_K_UNPACK,
                                       MOE_K_COMBINE_PACK, MOE_K_COMBINE_SCATTER, MOE_K_EXPERT,
-                                      MOE_K_PACK_PUSH,    MOE_K_COMBINE_PUSH};
+                                      MOE_K_PACK_PUSH,    MOE_K_COMBINE_PUSH,    MOE_K_SCATTER_UNPACK,
+                                      MOE_K_COMBINE_PACK_SCATTER};
   LaunchScope ls(c, ids[kind]);
   return nt != g.T ? run_move<1>(kind, g, a, c, fp8, rowB16) : run_move<0>(kind, g, a, c, fp8, rowB16);
 }

@@ -91,7 +91,10 @@ typedef enum {
     MOE_K_DISPATCH_SPLIT = 15, /* split-phase dispatch: push, signal, wait, shuffle in one launch */
     MOE_K_QUANT_PACK = 16,     /* fp8 quantisation fused into the pack */
     MOE_K_DISPATCH_DEDICATED = 17, /* split-phase dispatch with dedicated space and piggybacked routing */
-    MOE_K_NUM = 18
+    MOE_K_SCATTER_UNPACK = 18, /* scatter and unpack fused: send row -> receive row and grouped row */
+    MOE_K_COMBINE_PACK_SCATTER = 19, /* combine pack and scatter fused: output row -> receive-order row
+                                        and the source's combine row */
+    MOE_K_NUM = 20
 } moe_kernel_id;
 
 /* Optional per-kernel timing. When moe_layout_t.prof is non-NULL, every kernel the library
@@ -141,6 +144,13 @@ typedef struct {
  * (for moe_forward_host: copies, then the pass, then the copy back; or, with
  * MOE_FLAG_HOST_MAPPED, the pass alone) instead of the default token batches. */
 #define MOE_FLAG_ONE_BATCH 0x40u
+/* The whole-pass and whole-phase calls (moe_forward, moe_forward_host, moe_dispatch,
+ * moe_combine) read each pair's row once for the per-peer write and the shuffle behind it:
+ * one kernel writes the receive row and the grouped row (dispatch), another the
+ * receive-order row and the source's combine row (combine). Every buffer ends up as with
+ * the separate calls, byte for byte. This flag runs the four moves as separate kernels
+ * instead, as moe_dispatch_send + moe_dispatch_recv and moe_combine_send do. */
+#define MOE_FLAG_SEPARATE_MOVES 0x80u
 #define MOE_FLAG_NO_PDL 0x2u    /* launch without programmatic dependent launch (by default
                                    each kernel may be scheduled while its predecessor in the
                                    stream drains; it waits for it before touching memory) */

@@ -22,6 +22,9 @@ def test_algorithmic_bytes_match_the_scope_table():
     assert ab["scatter"] == ab["unpack"] == 2 * P * 2 * wl.H == 234_881_024
     assert ab["combine_pack"] + ab["combine_scatter"] == 469_762_048
     assert ab["combine_reduce"] == wl.N * wl.T * (wl.R + 1) * 2 * wl.H
+    # the fused moves: one read of each row, every write of the two moves they stand for
+    assert ab["scatter_unpack"] == ab["scatter"] + ab["unpack"] - P * 2 * wl.H
+    assert ab["combine_pack_scatter"] == ab["combine_pack"] + ab["combine_scatter"] - P * 2 * wl.H
     f = workloads.config(3)
     Pf = f.N * f.T * f.R
     abf = bench.algorithmic_bytes(f, Pf, Pf)

@@ -200,7 +200,12 @@ def test_launch_counter_counts_kernels():
     n0 = lib().moe_launch_count()
     ep.forward(to_dev(inp["x"]).view(torch.bfloat16), to_dev(inp["idx"]), to_dev(inp["w"]))
     torch.cuda.synchronize()
-    # layout (3) + pack + scatter + unpack + combine pack + combine scatter + reduce; bf16 identity aliases
+    # layout (3) + pack + scatter-and-unpack + combine pack-and-scatter + reduce; bf16 identity aliases
+    assert lib().moe_launch_count() - n0 == 7
+    ep.layout.flags |= 0x80   # MOE_FLAG_SEPARATE_MOVES: the four moves apart
+    n0 = lib().moe_launch_count()
+    ep.forward(to_dev(inp["x"]).view(torch.bfloat16), to_dev(inp["idx"]), to_dev(inp["w"]))
+    torch.cuda.synchronize()
     assert lib().moe_launch_count() - n0 == 9
 
 
@@ -220,8 +225,8 @@ def test_profiling_events_bracket_each_kernel():
     ep.forward(to_dev(inp["x"]).view(torch.bfloat16), to_dev(inp["idx"]), to_dev(inp["w"]))
     torch.cuda.synchronize()
     names = [KERNEL_NAMES[prof.kernel[i]] for i in range(prof.n)]
-    assert names == ["route_count", "route_scan", "layout_maps", "quant_pack", "scatter", "unpack",
-                     "expert", "combine_pack", "combine_scatter", "combine_reduce"]
+    assert names == ["route_count", "route_scan", "layout_maps", "quant_pack", "scatter_unpack", "expert",
+                     "combine_pack_scatter", "combine_reduce"]
     for i in range(prof.n):
         assert evs[2 * i].elapsed_time(evs[2 * i + 1]) >= 0.0
     out0 = ep.out.clone()
@@ -481,6 +486,20 @@ def test_dispatch_and_combine_phases_match_oracle(orc, wl, flags, batches):
     _, res = run_gpu(wl, inp, flags=flags, phases=True, batches=batches)
     assert res["status_code"] == (3 if wl.cap else 0)
     compare_all(orc, wl, inp, res, push=bool(flags & 8), fused_quant=True)
+
+
+@pytest.mark.parametrize("flags", [0, 1, 4, 0x80, 0x81, 0x84], ids=["fused-auto", "fused-ldg", "fused-tma",
+                                                                   "separate-auto", "separate-ldg", "separate-tma"])
+@pytest.mark.parametrize("wl", CASES + MB_CASES, ids=lambda w: w.name)
+def test_fused_and_separate_moves_match_oracle(orc, wl, flags):
+    """moe_forward in one batch with the fused moves (scatter with unpack, combine pack with
+    combine scatter) and with the four moves apart (MOE_FLAG_SEPARATE_MOVES): in both, every
+    buffer, the receive and combine-send rows included, bit for bit as the oracle's, unused
+    rows untouched; each mover, fp8 rows that are not 16-byte multiples, capacity drops."""
+    inp = workloads.make_inputs(wl)
+    _, res = run_gpu(wl, inp, flags=flags | 0x40, forward=True)
+    assert res["status_code"] == (3 if wl.cap else 0)
+    compare_all(orc, wl, inp, res, fused_quant=True)
 
 
 @pytest.mark.parametrize("batches", [1, 3])
