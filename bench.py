@@ -54,8 +54,8 @@ import workloads  # noqa: E402
 METRIC = "dispatch+combine tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 KERNELS = ["route_count", "layout_maps", "quant_fp8", "pack", "scatter", "unpack", "expert",
            "combine_pack", "combine_scatter", "combine_reduce", "route_scan", "pack_push", "combine_push",
-           "combine_partial", "combine_sum", "dispatch_split", "quant_pack", "dispatch_dedicated", "scatter_unpack",
-           "combine_pack_scatter"]
+           "combine_partial", "combine_sum", "dispatch_split", "quant_pack", "dispatch_dedicated", "dispatch_fused",
+           "quant_dispatch_fused", "combine_fused"]
 HEADLINE_CONFIG = 4          # the largest workload: the line's top level
 OTHER_CONFIGS = (1, 2, 3)    # measured in the same run, reported under per_config
 L2_NOTE = "flushed before every timed step (write of 2x L2, then read of 2x L2)"
@@ -84,8 +84,8 @@ def parse_args(argv=None):
     p.add_argument("--one-batch", action="store_true",
                    help="run moe_forward (and the host pass) as one token batch instead of micro-batches")
     p.add_argument("--separate-moves", action="store_true",
-                   help="run the scatter and unpack, and the combine pack and scatter, as separate kernels "
-                        "(MOE_FLAG_SEPARATE_MOVES) instead of the fused moves")
+                   help="run each phase as separate kernels (pack, write, shuffle; combine pack, write, sum: "
+                        "MOE_FLAG_SEPARATE_MOVES) instead of one kernel per phase and token batch")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="CPU work for the oracle baseline of the top-level workload (single thread, then "
@@ -231,8 +231,9 @@ def algorithmic_bytes(wl: workloads.Workload, P: int, Pk: int) -> dict:
         "combine_push": 2 * Pk * 2 * H,
         "dispatch_split": tok * B + P * B + 2 * Pk * B,
         "dispatch_dedicated": tok * B + P * B + 2 * Pk * B,
-        "scatter_unpack": 2 * P * B + Pk * B,
-        "combine_pack_scatter": 3 * Pk * 2 * H,
+        "dispatch_fused": tok * B + 2 * P * B + Pk * B,
+        "quant_dispatch_fused": tok * 2 * H + 2 * P * B + Pk * B,
+        "combine_fused": Pk * 2 * H + 2 * Pk * 2 * H + tok * 2 * H,
     }
 
 
@@ -818,9 +819,10 @@ def measure(wl, args, dist, device, peak: float, peak_kind: str, cpu_seconds: fl
                               "the default splits it into token batches over two streams"},
         ("fused_moves" if args.separate_moves else "separate_moves"): {
             "value": round(tokens / (other_ms_all * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(other_ms_all, 4),
-            "note": "the same step with the dispatch's scatter and unpack, and the combine's pack and scatter, "
-                    + ("fused (the default)" if args.separate_moves else
-                       "as separate kernels (MOE_FLAG_SEPARATE_MOVES); identical results")},
+            "note": "the same step with each phase "
+                    + ("in one kernel per token batch (the default)" if args.separate_moves else
+                       "as separate kernels (MOE_FLAG_SEPARATE_MOVES: pack, write, shuffle; combine pack, "
+                       "write, sum); identical results")},
         "forward_with_expert": None if fwd_ms is None else {
             "value": round(tokens / (fwd_ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(fwd_ms, 4),
             "micro_batches": fwd_batches,

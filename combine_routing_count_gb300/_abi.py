@@ -31,7 +31,7 @@ MOE_PROF_MAX = 32
 KERNEL_NAMES = ["route_count", "layout_maps", "quant_fp8", "pack", "scatter", "unpack", "expert",
                 "combine_pack", "combine_scatter", "combine_reduce", "route_scan", "pack_push", "combine_push",
                 "combine_partial", "combine_sum", "dispatch_split", "quant_pack", "dispatch_dedicated",
-                "scatter_unpack", "combine_pack_scatter"]
+                "dispatch_fused", "quant_dispatch_fused", "combine_fused"]
 
 LAYOUT_FIELDS = ("cnt", "C", "soff", "roff", "rtot", "ecnt", "eoff", "pos", "rrow", "slot", "slot_src",
                  "recv_src", "gsend", "grecv", "gslot", "status", "scratch")

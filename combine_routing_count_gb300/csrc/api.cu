@@ -292,25 +292,19 @@ namespace moe {
 namespace {
 
 // Dispatch: the send rows of the token range [t0, t0 + nt) of every rank written to their
-// owners' receive rows and shuffled into the grouped rows, by one fused move (each send row
-// read once) unless MOE_FLAG_SEPARATE_MOVES asks for the scatter and the unpack apart.
+// owners' receive rows, then shuffled into the grouped rows.
 cudaError_t dispatch_recv_range(const Geo& g, const moe_layout_t* lay, const void* send, void* recv, void* ex,
                                 float* exs, int t0, int nt, Ctx& c) {
   const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
-  if (!(c.flags & MOE_FLAG_SEPARATE_MOVES))
-    return launch_move_range(kMoveScatterUnpack, g, lay, send, recv, ex, t0, nt, c, fp8 ? exs : nullptr);
   cudaError_t e = launch_move_range(kMoveScatter, g, lay, send, recv, nullptr, t0, nt, c);
   if (e == cudaSuccess) e = launch_move_range(kMoveUnpack, g, lay, recv, ex, fp8 ? exs : nullptr, t0, nt, c);
   return e;
 }
 
 // Combine: the expert output rows of the pairs of the token range [t0, t0 + nt) of every
-// rank written in receive order and back to their sources' combine rows, by one fused move
-// unless MOE_FLAG_SEPARATE_MOVES asks for the combine pack and scatter apart.
+// rank written in receive order, then back to their sources' combine rows.
 cudaError_t combine_send_range(const Geo& g, const moe_layout_t* lay, const uint16_t* ey, uint16_t* csend,
                                uint16_t* crecv, int t0, int nt, Ctx& c) {
-  if (!(c.flags & MOE_FLAG_SEPARATE_MOVES))
-    return launch_move_range(kMoveCPackScatter, g, lay, ey, csend, crecv, t0, nt, c);
   cudaError_t e = launch_move_range(kMoveCPack, g, lay, ey, csend, nullptr, t0, nt, c);
   if (e == cudaSuccess) e = launch_move_range(kMoveCScatter, g, lay, csend, crecv, nullptr, t0, nt, c);
   return e;
@@ -368,6 +362,11 @@ cudaError_t dispatch_range(const Geo& g, const moe_layout_t* lay, const void* x,
     e = fp8 ? launch_quant_pack(g, lay->grecv, static_cast<const uint16_t*>(x), static_cast<uint8_t*>(recv), c, t0,
                                 nt)
             : launch_move_range(kMovePackPush, g, lay, x, recv, nullptr, t0, nt, c);
+  } else if (!(c.flags & MOE_FLAG_SEPARATE_MOVES)) {
+    // pack, write and shuffle in one kernel: each token row read (and quantised) once
+    return fp8 ? launch_quant_dispatch_fused(g, lay, static_cast<const uint16_t*>(x), static_cast<uint8_t*>(send),
+                                             static_cast<uint8_t*>(recv), static_cast<uint8_t*>(ex), exs, c, t0, nt)
+               : launch_move_range(kMovePackAll, g, lay, x, send, recv, t0, nt, c, ex);
   } else {
     e = fp8 ? launch_quant_pack(g, lay->gsend, static_cast<const uint16_t*>(x), static_cast<uint8_t*>(send), c, t0,
                                 nt)
@@ -386,6 +385,9 @@ cudaError_t combine_range(const Geo& g, const moe_layout_t* lay, const uint16_t*
   cudaError_t e;
   if (c.flags & MOE_FLAG_DIRECT_PUSH) {
     e = launch_move_range(kMoveCPush, g, lay, ey, crecv, nullptr, t0, nt, c);
+  } else if (!(c.flags & MOE_FLAG_SEPARATE_MOVES)) {
+    // combine pack, write and weighted sum in one kernel: each expert output row read once
+    return launch_combine_fused(g, lay, ey, csend, crecv, w, out, c, t0, nt);
   } else {
     e = combine_send_range(g, lay, ey, csend, crecv, t0, nt, c);
   }

@@ -32,7 +32,7 @@ struct MoveArgs {
   const uint8_t* src;
   uint8_t* dst;
   uint8_t* dst2;
-  uint8_t* dst3;          // the fp8 scales of the fused scatter-and-unpack
+  uint8_t* dst3;          // pack-all: the grouped rows
   const int32_t* gsend;   // per pair: global send row, or -1
   const int32_t* grecv;   // per pair: global receive row, or -1
   const int32_t* gslot;   // per pair: global grouped row, or -1
@@ -61,7 +61,6 @@ struct Plan {
   const uint8_t* src;
   uint8_t* dst;
   uint8_t* dst2;
-  uint8_t* dst3;
   int64_t tok;                 // pack: token index s*T+t
   int32_t coff;                // pack: byte offset of the chunk in the row
   int32_t p[kPackPrefetch];    // pack: global send rows of the token's pairs
@@ -94,7 +93,7 @@ template <int KIND, bool FP8, int MODE, bool REV>
 __device__ __forceinline__ bool make_plan(const Geo& g, const MoveArgs& a, int64_t u, Plan& pl) {
   if (REV) u = a.units - 1 - u;
   const int64_t H2 = 2 * (int64_t)g.H;
-  if (KIND == kMovePack || KIND == kMovePackPush) {
+  if (is_pack_kind(KIND)) {
     const int64_t tv = u / a.chunks;
     const int64_t tok = range_item<MODE>(g, a, tv, 1);
     pl.tok = tok;
@@ -114,35 +113,6 @@ __device__ __forceinline__ bool make_plan(const Geo& g, const MoveArgs& a, int64
     if (gs < 0 || dst_outside<MODE>(a, gr)) return false;
     pl.src = a.src + (int64_t)gs * g.B + coff;
     pl.dst = a.dst + (int64_t)gr * g.B + coff;
-    return true;
-  }
-  if (KIND == kMoveScatterUnpack) {   // the receive row, and the grouped row if the pair is kept
-    const int gs = __ldg(a.gsend + u);
-    const int gr = __ldg(a.grecv + u);
-    const int gl = __ldg(a.gslot + u);
-    if (gs < 0) return false;
-    pl.src = a.src + (int64_t)gs * g.B + coff;
-    pl.dst = a.dst + (int64_t)gr * g.B + coff;
-    pl.dst2 = nullptr;
-    pl.dst3 = nullptr;
-    if (gl >= 0) {
-      if (FP8) {   // dst3: the scale row, less the codes' length (the row's offset of the scales)
-        pl.dst2 = a.dst2 + (int64_t)gl * g.H;
-        pl.dst3 = a.dst3 + (int64_t)gl * (g.H / 32) - g.H;
-      } else {
-        pl.dst2 = a.dst2 + (int64_t)gl * g.B + coff;
-      }
-    }
-    return true;
-  }
-  if (KIND == kMoveCPackScatter) {   // receive-order row and the source's combine row
-    const int gl = __ldg(a.gslot + u);
-    const int gr = __ldg(a.grecv + u);
-    const int gs = __ldg(a.gsend + u);
-    if (gl < 0) return false;
-    pl.src = a.src + (int64_t)gl * H2 + coff;
-    pl.dst = a.dst + (int64_t)gr * H2 + coff;
-    pl.dst2 = a.dst2 + (int64_t)gs * H2 + coff;
     return true;
   }
   if (KIND == kMoveCopyEx) {
@@ -190,7 +160,7 @@ __device__ __forceinline__ bool make_plan(const Geo& g, const MoveArgs& a, int64
 template <int KIND, bool FP8>
 __device__ __forceinline__ void issue_stores(const Geo& g, const MoveArgs& a, const Plan& pl, const uint8_t* stage,
                                              uint32_t bytes) {
-  if (KIND == kMovePack || KIND == kMovePackPush) {
+  if (is_pack_kind(KIND)) {
 #pragma unroll
     for (int k = 0; k < kPackPrefetch; ++k)
       if (pl.p[k] >= 0) bulk_s2g(a.dst + (int64_t)pl.p[k] * g.B + pl.coff, stage, bytes);
@@ -198,22 +168,18 @@ __device__ __forceinline__ void issue_stores(const Geo& g, const MoveArgs& a, co
       const int p = __ldg(a.fan + pl.tok * g.R + k);
       if (p >= 0) bulk_s2g(a.dst + (int64_t)p * g.B + pl.coff, stage, bytes);
     }
+    if (KIND == kMovePackAll) {   // the receive rows, and the grouped rows of the kept pairs
+      for (int k = 0; k < g.R; ++k) {
+        const int64_t q = pl.tok * g.R + k;
+        if (__ldg(a.gsend + q) < 0) continue;
+        bulk_s2g(a.dst2 + (int64_t)__ldg(a.grecv + q) * g.B + pl.coff, stage, bytes);
+        const int gl = __ldg(a.gslot + q);
+        if (gl >= 0) bulk_s2g(a.dst3 + (int64_t)gl * g.B + pl.coff, stage, bytes);
+      }
+    }
   } else if (KIND == kMoveUnpack && FP8) {
     bulk_s2g(pl.dst, stage, (uint32_t)g.H);
     bulk_s2g(pl.dst2, stage + g.H, (uint32_t)(g.H / 32));
-  } else if (KIND == kMoveScatterUnpack) {
-    bulk_s2g(pl.dst, stage, bytes);
-    if (pl.dst2) {
-      if (FP8) {
-        bulk_s2g(pl.dst2, stage, (uint32_t)g.H);
-        bulk_s2g(pl.dst3 + g.H, stage + g.H, (uint32_t)(g.H / 32));
-      } else {
-        bulk_s2g(pl.dst2, stage, bytes);
-      }
-    }
-  } else if (KIND == kMoveCPackScatter) {
-    bulk_s2g(pl.dst, stage, bytes);
-    bulk_s2g(pl.dst2, stage, bytes);
   } else {
     bulk_s2g(pl.dst, stage, bytes);
   }
@@ -227,7 +193,6 @@ constexpr int kTmaHeader = kIssuers * kMaxStages * (8 + 128);  // mbarriers + pl
 struct StagePlan {
   uint8_t* dst;
   uint8_t* dst2;
-  uint8_t* dst3;
   int64_t tok;
   int32_t coff;
   int32_t p[kPackPrefetch];
@@ -258,8 +223,8 @@ __global__ void __launch_bounds__(kIssuers * 32) k_move_tma(Geo g, MoveArgs a) {
     Plan pl;
     for (int k = 0; k < S && k < n; ++k) {
       const bool ok = make_plan<KIND, FP8, MODE, REV>(g, a, gi + k * G, pl);
-      sp[k] = StagePlan{pl.dst, pl.dst2, pl.dst3, pl.tok, pl.coff, {}};
-      if (KIND == kMovePack || KIND == kMovePackPush)
+      sp[k] = StagePlan{pl.dst, pl.dst2, pl.tok, pl.coff, {}};
+      if (is_pack_kind(KIND))
         for (int r = 0; r < kPackPrefetch; ++r) sp[k].p[r] = pl.p[r];
       if (ok) {
         mbar_arrive_expect_tx(&bar[k], bytes);
@@ -278,10 +243,9 @@ __global__ void __launch_bounds__(kIssuers * 32) k_move_tma(Geo g, MoveArgs a) {
         Plan cur;
         cur.dst = sp[k].dst;
         cur.dst2 = sp[k].dst2;
-        cur.dst3 = sp[k].dst3;
         cur.tok = sp[k].tok;
         cur.coff = sp[k].coff;
-        if (KIND == kMovePack || KIND == kMovePackPush)
+        if (is_pack_kind(KIND))
           for (int r = 0; r < kPackPrefetch; ++r) cur.p[r] = sp[k].p[r];
         issue_stores<KIND, FP8>(g, a, cur, ring + (size_t)k * a.stage_bytes, bytes);
         bulk_commit();
@@ -296,8 +260,8 @@ __global__ void __launch_bounds__(kIssuers * 32) k_move_tma(Geo g, MoveArgs a) {
         else
           bulk_wait_read_all();
         vbits &= ~(1u << kp);
-        sp[kp] = StagePlan{nx.dst, nx.dst2, nx.dst3, nx.tok, nx.coff, {}};
-        if (KIND == kMovePack || KIND == kMovePackPush)
+        sp[kp] = StagePlan{nx.dst, nx.dst2, nx.tok, nx.coff, {}};
+        if (is_pack_kind(KIND))
           for (int r = 0; r < kPackPrefetch; ++r) sp[kp].p[r] = nx.p[r];
         if (nx_ok) {
           mbar_arrive_expect_tx(&bar[kp], bytes);
@@ -332,9 +296,9 @@ __device__ __forceinline__ void move_ldg(const Geo& g, const MoveArgs& a) {
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int64_t nel = unit_bytes<KIND>(g, a) / W;
-  const int64_t split = ((KIND == kMoveUnpack || KIND == kMoveScatterUnpack) && FP8) ? g.H / W : nel;
+  const int64_t split = (KIND == kMoveUnpack && FP8) ? g.H / W : nel;
   pdl_wait();
-  if (KIND == kMovePack || KIND == kMovePackPush) {
+  if (is_pack_kind(KIND)) {
     // Pack: lane k holds the destination row of the token's pair k and broadcasts it by
     // shuffle, so a warp keeps only its U loaded vectors live while it writes R copies.
     for (int64_t u0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u0 < a.units; u0 += nwarps) {
@@ -346,6 +310,9 @@ __device__ __forceinline__ void move_ldg(const Geo& g, const MoveArgs& a) {
       uint8_t* dst0 = a.dst + coff;
       const int32_t* fan = a.fan + tok * g.R;
       const int myp = lane < g.R ? __ldg(fan + lane) : -1;   // pairs 0..31 (R > 32: see below)
+      // pack-all: the pair's receive row and grouped row (-1: dropped) as well
+      const int myr = (KIND == kMovePackAll && lane < g.R) ? __ldg(a.grecv + tok * g.R + lane) : -1;
+      const int myl = (KIND == kMovePackAll && lane < g.R) ? __ldg(a.gslot + tok * g.R + lane) : -1;
       // The trip count is the same for every lane: the shuffles below need the whole warp.
       for (int64_t b0 = 0; b0 < nel; b0 += 32 * U) {
         const int64_t v0 = b0 + lane;
@@ -358,6 +325,24 @@ __device__ __forceinline__ void move_ldg(const Geo& g, const MoveArgs& a) {
 #pragma unroll 1
         for (int k = 0; k < g.R; ++k) {
           const int p = k < 32 ? __shfl_sync(0xffffffffu, myp, k) : __ldg(fan + k);
+          if (KIND == kMovePackAll) {
+            const int rr = k < 32 ? __shfl_sync(0xffffffffu, myr, k) : __ldg(a.grecv + tok * g.R + k);
+            const int rl = k < 32 ? __shfl_sync(0xffffffffu, myl, k) : __ldg(a.gslot + tok * g.R + k);
+            if (p < 0) continue;
+            uint8_t* d = dst0 + (int64_t)p * g.B;
+            uint8_t* d2 = a.dst2 + coff + (int64_t)rr * g.B;
+            uint8_t* d3 = a.dst3 + coff + (int64_t)rl * g.B;
+#pragma unroll
+            for (int j = 0; j < U; ++j) {
+              const int64_t v = v0 + 32 * j;
+              if (v < nel) {
+                st_vec(d + v * W, r[j]);
+                st_vec(d2 + v * W, r[j]);
+                if (rl >= 0) st_vec(d3 + v * W, r[j]);
+              }
+            }
+            continue;
+          }
           if (p < 0) continue;
           uint8_t* d = dst0 + (int64_t)p * g.B;
 #pragma unroll
@@ -390,14 +375,6 @@ __device__ __forceinline__ void move_ldg(const Geo& g, const MoveArgs& a) {
             st_vec(pl.dst + v * W, r[j]);
           else
             st_vec(pl.dst2 + (v - split) * W, r[j]);
-        } else if (KIND == kMoveScatterUnpack) {
-          st_vec(pl.dst + v * W, r[j]);
-          // fp8: codes to dst2, the scales that follow them in the row to dst3 (pl.dst3 was
-          // moved back by the codes' length in the plan, so both take offset v * W)
-          if (pl.dst2) st_vec(((!FP8 || v < split) ? pl.dst2 : pl.dst3) + v * W, r[j]);
-        } else if (KIND == kMoveCPackScatter) {
-          st_vec(pl.dst + v * W, r[j]);
-          st_vec(pl.dst2 + v * W, r[j]);
         } else {
           st_vec(pl.dst + v * W, r[j]);
         }
@@ -412,24 +389,23 @@ __global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
   move_ldg<KIND, FP8, V, MODE, REV>(g, a);
 }
 
-// The fused kinds hold two or three store pointers per row: without a bound the bf16 ones
-// take 72-76 registers, three CTAs of 256 threads per SM instead of four. The fp8
-// scatter-and-unpack would spill at 64 and keeps three.
+// The pack-all move keeps three destination rows per pair: without a bound it takes 89
+// registers, two CTAs of 256 threads per SM; bounded to three.
 template <int KIND, bool FP8, typename V, int MODE, bool REV>
-__global__ void __launch_bounds__(256, FP8 ? 3 : 4) k_move_ldg_fused(Geo g, MoveArgs a) {
+__global__ void __launch_bounds__(256, 3) k_move_ldg_all(Geo g, MoveArgs a) {
   move_ldg<KIND, FP8, V, MODE, REV>(g, a);
 }
 
 template <int KIND, bool FP8, typename V, int MODE, bool REV>
 constexpr auto ldg_kernel() {
-  if constexpr (KIND == kMoveScatterUnpack || KIND == kMoveCPackScatter)
-    return k_move_ldg_fused<KIND, FP8, V, MODE, REV>;
+  if constexpr (KIND == kMovePackAll)
+    return k_move_ldg_all<KIND, FP8, V, MODE, REV>;
   else
     return k_move_ldg<KIND, FP8, V, MODE, REV>;
 }
 
 // Largest dynamic shared memory limit set so far, per TMA instantiation and device.
-std::atomic<int> g_tma_smem[10][2][3][2][64];
+std::atomic<int> g_tma_smem[9][2][3][2][64];
 
 // Stages per issuer and CTAs per SM: as many CTAs as fit with 3 stages per issuer (at
 // most 8 CTAs), then as many stages as the shared memory of each CTA holds (2..8). Each
@@ -500,7 +476,7 @@ bool tma_fits(const Geo& g, const MoveArgs& a, const Ctx& c) {
 // issue, is as fast or faster.
 template <int KIND>
 bool tma_default(const MoveArgs& a, const Ctx& c) {
-  if (KIND == kMovePack || KIND == kMovePackPush) return false;
+  if (is_pack_kind(KIND)) return false;
   return a.units / a.chunks >= 40LL * kIssuers * c.num_sms;
 }
 
@@ -519,10 +495,8 @@ cudaError_t run_kind(const Geo& g, const MoveArgs& a, Ctx& c, bool row16) {
 // the rows the producer wrote last, which are still in L2 (at 8K pairs of 14 KB rows,
 // about 117 MB a buffer against 129 MB of L2). Pair-ordered moves therefore alternate:
 // pack forward, scatter backward, unpack forward, identity expert forward, combine pack
-// backward, combine scatter forward; the fused scatter-and-unpack and combine pack-and-scatter
-// run backward, as the scatter and the combine pack they stand for. With direct push the pack
-// writes the receive rows forward, so the unpack and the identity expert run backward and the
-// combine push forward.
+// backward, combine scatter forward. With direct push the pack writes the receive rows
+// forward, so the unpack and the identity expert run backward and the combine push forward.
 // Only the order in which independent rows are copied changes, never a value.
 template <int KIND, bool FP8, int MODE>
 cudaError_t run_dir(const Geo& g, const MoveArgs& a, Ctx& c, bool row16) {
@@ -530,9 +504,7 @@ cudaError_t run_dir(const Geo& g, const MoveArgs& a, Ctx& c, bool row16) {
     if (c.flags & MOE_FLAG_DIRECT_PUSH) return run_kind<KIND, FP8, MODE, true>(g, a, c, row16);
     return run_kind<KIND, FP8, MODE, false>(g, a, c, row16);
   } else {
-    constexpr bool kRev = KIND == kMoveScatter || KIND == kMoveCPack || KIND == kMoveScatterUnpack ||
-                          KIND == kMoveCPackScatter;
-    return run_kind<KIND, FP8, MODE, kRev>(g, a, c, row16);
+    return run_kind<KIND, FP8, MODE, KIND == kMoveScatter || KIND == kMoveCPack>(g, a, c, row16);
   }
 }
 
@@ -542,8 +514,8 @@ namespace {
 
 template <int R>
 cudaError_t run_move(MoveKind kind, const Geo& g, const MoveArgs& a, Ctx& c, bool fp8, bool rowB16) {
-  if constexpr (R == 2) {   // the fused moves are whole-group moves only
-    if (kind == kMoveScatterUnpack || kind == kMoveCPackScatter) return cudaErrorInvalidValue;
+  if constexpr (R == 2) {   // the pack-all move is a whole-group move only
+    if (kind == kMovePackAll) return cudaErrorInvalidValue;
   }
   switch (kind) {
     case kMovePack:
@@ -562,13 +534,8 @@ cudaError_t run_move(MoveKind kind, const Geo& g, const MoveArgs& a, Ctx& c, boo
       return run_dir<kMovePackPush, false, R>(g, a, c, rowB16);
     case kMoveCPush:
       return run_dir<kMoveCPush, false, R>(g, a, c, true);
-    case kMoveScatterUnpack:
-      if constexpr (R != 2)
-        return fp8 ? run_dir<kMoveScatterUnpack, true, R>(g, a, c, rowB16)
-                   : run_dir<kMoveScatterUnpack, false, R>(g, a, c, rowB16);
-      break;
-    case kMoveCPackScatter:
-      if constexpr (R != 2) return run_dir<kMoveCPackScatter, false, R>(g, a, c, true);
+    case kMovePackAll:
+      if constexpr (R != 2) return run_dir<kMovePackAll, false, R>(g, a, c, rowB16);
       break;
   }
   return cudaErrorInvalidValue;
@@ -685,7 +652,7 @@ cudaError_t launch_move_range(MoveKind kind, const Geo& g, const moe_layout_t* l
   a.fd_n = 0;
   const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
   const bool rowB16 = (g.B % 16) == 0;  // bf16 rows always; fp8 rows when H % 512 == 0
-  if (kind == kMovePack || kind == kMovePackPush) {
+  if (is_pack_kind(kind)) {
     // Split token rows into column chunks (16-byte multiples, at most 8 per row) of at least
     // 2 KB, or 1.5 KB while this launch has fewer than ~16 units per SM: smaller units
     // balance the warps better (measured: 3.5 KB chunks of 14 KB rows and 2 KB chunks of 8 KB
@@ -707,10 +674,8 @@ cudaError_t launch_move_range(MoveKind kind, const Geo& g, const moe_layout_t* l
     // issuer slot of the TMA ring, so that each issuer keeps more (smaller) rows in flight
     // (measured on micro-batches of 2048 pairs: 14 KB rows 6% faster halved, 8 KB rows 4.5%
     // slower). The fp8 receive split (codes | scales) is never chunked.
-    const bool recv_rows = kind == kMoveScatter || kind == kMoveUnpack || kind == kMoveScatterUnpack;
-    const int64_t rowb = recv_rows ? g.B : 2 * (int64_t)g.H;
-    const bool splittable =
-        !((kind == kMoveUnpack || kind == kMoveScatterUnpack) && fp8) && rowb >= 12288 && rowb % 32 == 0;
+    const int64_t rowb = (kind == kMoveScatter || kind == kMoveUnpack) ? g.B : 2 * (int64_t)g.H;
+    const bool splittable = !(kind == kMoveUnpack && fp8) && rowb >= 12288 && rowb % 32 == 0;
     const int64_t pairs = nt == g.T ? g.P : (int64_t)g.N * nt * g.R;   // of this launch
     if (splittable && pairs < 32LL * 4 * c.num_sms) a.chunks = 2;
     a.chunk_bytes = (uint32_t)(rowb / a.chunks);
@@ -720,13 +685,12 @@ cudaError_t launch_move_range(MoveKind kind, const Geo& g, const moe_layout_t* l
   if (nt != g.T) {   // a token range of every rank: its tokens, or its pairs
     a.t0 = t0;
     a.nt = nt;
-    a.units = (int64_t)g.N * nt * (kind == kMovePack || kind == kMovePackPush ? 1 : g.R) * a.chunks;
+    a.units = (int64_t)g.N * nt * (is_pack_kind(kind) ? 1 : g.R) * a.chunks;
   }
   if (a.units == 0) return cudaSuccess;
   static const moe_kernel_id ids[] = {MOE_K_PACK,         MOE_K_SCATTER,         MOE_K_UNPACK,
                                       MOE_K_COMBINE_PACK, MOE_K_COMBINE_SCATTER, MOE_K_EXPERT,
-                                      MOE_K_PACK_PUSH,    MOE_K_COMBINE_PUSH,    MOE_K_SCATTER_UNPACK,
-                                      MOE_K_COMBINE_PACK_SCATTER};
+                                      MOE_K_PACK_PUSH,    MOE_K_COMBINE_PUSH,    MOE_K_DISPATCH_FUSED};
   LaunchScope ls(c, ids[kind]);
   return nt != g.T ? run_move<1>(kind, g, a, c, fp8, rowB16) : run_move<0>(kind, g, a, c, fp8, rowB16);
 }

@@ -229,10 +229,21 @@ __global__ void __launch_bounds__(256) k_quant_fp8(Geo g, const uint16_t* __rest
 // when pushing), so the fp8 rows are never staged in HBM. The bytes each row gets are those
 // moe_quantize_fp8_b128 writes. W8: rows are 8-byte aligned (8-byte code stores).
 // RANGED: only the token range [t0, t0 + nt) of every rank (else every token; t0, nt unused).
-template <bool W8, bool RANGED>
+// ALL: the write and the shuffle as well (pack-all): every pair's codes and scales also go to
+// its receive row (recv at grecv) and, when the pair is kept, to its grouped row (codes at
+// ex + gslot * H, scales at exs + gslot * H / 128), the bytes moe_dispatch_recv writes.
+struct FanAll {
+  const int32_t* grecv;
+  const int32_t* gslot;
+  uint8_t* recv;
+  uint8_t* ex;
+  float* exs;
+};
+
+template <bool W8, bool RANGED, bool ALL>
 __global__ void __launch_bounds__(256) k_quant_pack(Geo g, const uint16_t* __restrict__ x,
                                                     const int32_t* __restrict__ fan, uint8_t* __restrict__ dst,
-                                                    int t0, int nt) {
+                                                    int t0, int nt, FanAll fa) {
   const int nb = g.H / 128;
   const int upr = (nb + 2 * kQuantUnroll - 1) / (2 * kQuantUnroll);
   const int64_t units = (int64_t)g.N * (RANGED ? nt : g.T) * upr;
@@ -247,26 +258,38 @@ __global__ void __launch_bounds__(256) k_quant_pack(Geo g, const uint16_t* __res
     const int64_t row = RANGED ? (rv / nt) * g.T + t0 + rv % nt : rv;   // token
     const int32_t* fr = fan + row * g.R;
     const int myp = lane < g.R ? __ldg(fr + lane) : -1;   // rows of pairs 0..31 (R > 32: loaded)
+    const int myr = (ALL && lane < g.R) ? __ldg(fa.grecv + row * g.R + lane) : -1;
+    const int myl = (ALL && lane < g.R) ? __ldg(fa.gslot + row * g.R + lane) : -1;
     uint32_t codes[kQuantUnroll][2];
     float scale[kQuantUnroll];
     quant_unit(x + row * g.H + sub * 8, bbase, nb, codes, scale);
 #pragma unroll 1
     for (int k = 0; k < g.R; ++k) {
       const int p = k < 32 ? __shfl_sync(kFull, myp, k) : __ldg(fr + k);
+      const int rr = ALL ? (k < 32 ? __shfl_sync(kFull, myr, k) : __ldg(fa.grecv + row * g.R + k)) : -1;
+      const int rl = ALL ? (k < 32 ? __shfl_sync(kFull, myl, k) : __ldg(fa.gslot + row * g.R + k)) : -1;
       if (p < 0) continue;
-      uint8_t* dr = dst + (int64_t)p * g.B;
+#pragma unroll 1
+      for (int dsel = 0; dsel < (ALL ? 3 : 1); ++dsel) {   // send row, receive row, grouped row
+        if (dsel == 2 && rl < 0) break;
+        uint8_t* dr = dsel == 0 ? dst + (int64_t)p * g.B
+                                : dsel == 1 ? fa.recv + (int64_t)rr * g.B : fa.ex + (int64_t)rl * g.H;
 #pragma unroll
-      for (int j = 0; j < kQuantUnroll; ++j) {
-        const int b = bbase + 2 * j;
-        if (b < nb) {
-          uint8_t* c = dr + b * 128 + sub * 8;
-          if (W8) {
-            *reinterpret_cast<uint2*>(c) = make_uint2(codes[j][0], codes[j][1]);
-          } else {
-            reinterpret_cast<uint32_t*>(c)[0] = codes[j][0];
-            reinterpret_cast<uint32_t*>(c)[1] = codes[j][1];
+        for (int j = 0; j < kQuantUnroll; ++j) {
+          const int b = bbase + 2 * j;
+          if (b < nb) {
+            uint8_t* c = dr + b * 128 + sub * 8;
+            if (W8 || dsel == 2) {   // grouped code rows (H bytes) are always 8-byte aligned
+              *reinterpret_cast<uint2*>(c) = make_uint2(codes[j][0], codes[j][1]);
+            } else {
+              reinterpret_cast<uint32_t*>(c)[0] = codes[j][0];
+              reinterpret_cast<uint32_t*>(c)[1] = codes[j][1];
+            }
+            if (sub == 0) {
+              float* sp = dsel < 2 ? reinterpret_cast<float*>(dr + g.H + 4 * b) : fa.exs + (int64_t)rl * nb + b;
+              *sp = scale[j];
+            }
           }
-          if (sub == 0) *reinterpret_cast<float*>(dr + g.H + 4 * b) = scale[j];
         }
       }
     }
@@ -386,10 +409,10 @@ __global__ void __launch_bounds__(256) k_quant_fp8_16(Geo g, const uint16_t* __r
   pdl_trigger();
 }
 
-template <bool RANGED>
+template <bool RANGED, bool ALL>
 __global__ void __launch_bounds__(256) k_quant_pack16(Geo g, const uint16_t* __restrict__ x,
                                                       const int32_t* __restrict__ fan, uint8_t* __restrict__ dst,
-                                                      int t0, int nt) {
+                                                      int t0, int nt, FanAll fa) {
   const int nb = g.H / 128;
   const int upr = (nb + 7) / 8;   // warp units per row
   const int64_t units = (int64_t)g.N * (RANGED ? nt : g.T) * upr;
@@ -404,21 +427,33 @@ __global__ void __launch_bounds__(256) k_quant_pack16(Geo g, const uint16_t* __r
     const int64_t row = RANGED ? (rv / nt) * g.T + t0 + rv % nt : rv;   // token
     const int32_t* fr = fan + row * g.R;
     const int myp = lane < g.R ? __ldg(fr + lane) : -1;   // rows of pairs 0..31 (R > 32: loaded)
+    const int myr = (ALL && lane < g.R) ? __ldg(fa.grecv + row * g.R + lane) : -1;
+    const int myl = (ALL && lane < g.R) ? __ldg(fa.gslot + row * g.R + lane) : -1;
     uint32_t codes[kQ16Blocks][4];
     float scale[kQ16Blocks];
     quant_unit16(x + row * g.H, bbase, nb, sub, codes, scale);
 #pragma unroll 1
     for (int k = 0; k < g.R; ++k) {
       const int p = k < 32 ? __shfl_sync(kFull, myp, k) : __ldg(fr + k);
+      const int rr = ALL ? (k < 32 ? __shfl_sync(kFull, myr, k) : __ldg(fa.grecv + row * g.R + k)) : -1;
+      const int rl = ALL ? (k < 32 ? __shfl_sync(kFull, myl, k) : __ldg(fa.gslot + row * g.R + k)) : -1;
       if (p < 0) continue;
-      uint8_t* dr = dst + (int64_t)p * g.B;
+#pragma unroll 1
+      for (int dsel = 0; dsel < (ALL ? 3 : 1); ++dsel) {   // send row, receive row, grouped row
+        if (dsel == 2 && rl < 0) break;
+        uint8_t* dr = dsel == 0 ? dst + (int64_t)p * g.B
+                                : dsel == 1 ? fa.recv + (int64_t)rr * g.B : fa.ex + (int64_t)rl * g.H;
 #pragma unroll
-      for (int j = 0; j < kQ16Blocks; ++j) {
-        const int b = bbase + 4 * j;
-        if (b < nb) {
-          *reinterpret_cast<uint4*>(dr + b * 128 + sub * 16) = make_uint4(codes[j][0], codes[j][1], codes[j][2],
-                                                                          codes[j][3]);
-          if (sub == 0) *reinterpret_cast<float*>(dr + g.H + 4 * b) = scale[j];
+        for (int j = 0; j < kQ16Blocks; ++j) {
+          const int b = bbase + 4 * j;
+          if (b < nb) {
+            *reinterpret_cast<uint4*>(dr + b * 128 + sub * 16) = make_uint4(codes[j][0], codes[j][1], codes[j][2],
+                                                                            codes[j][3]);
+            if (sub == 0) {
+              float* sp = dsel < 2 ? reinterpret_cast<float*>(dr + g.H + 4 * b) : fa.exs + (int64_t)rl * nb + b;
+              *sp = scale[j];
+            }
+          }
         }
       }
     }
@@ -547,11 +582,18 @@ __device__ __forceinline__ void store_bf16x8(uint16_t* p, const float (&acc)[8])
 // token x; t0, nt unused).
 constexpr int kReduceThreads = 128;
 
-template <bool RANGED>
+// FUSED: the combine pack and write in the same pass. The rows are read from the grouped
+// expert outputs (src = ey, at gslot) instead of the combine rows, and each is also stored to
+// its receive-order row csend[grecv] and its source's combine row crecv[gsend], the rows the
+// combine send writes; the sum is the same, value for value.
+template <bool RANGED, bool FUSED>
 __global__ void __launch_bounds__(kReduceThreads) k_combine_reduce(Geo g, const int32_t* __restrict__ gsend,
                                                                    const int32_t* __restrict__ gslot,
+                                                                   const int32_t* __restrict__ grecv,
                                                                    const float* __restrict__ w,
-                                                                   const uint16_t* __restrict__ crecv,
+                                                                   const uint16_t* __restrict__ src,
+                                                                   uint16_t* __restrict__ csend,
+                                                                   uint16_t* __restrict__ crecv,
                                                                    uint16_t* __restrict__ out, int t0, int nt) {
   const int64_t u = RANGED ? (int64_t)(blockIdx.x / nt) * g.T + t0 + blockIdx.x % nt : (int64_t)blockIdx.x;
   const int col = blockIdx.y * kReduceThreads + threadIdx.x;
@@ -563,14 +605,18 @@ __global__ void __launch_bounds__(kReduceThreads) k_combine_reduce(Geo g, const 
   acc_zero(acc);
   pdl_wait();
   for (int k0 = 0; k0 < g.R; k0 += 32) {
-    int myrow = -1;
+    int myrow = -1, mys = -1, myr = -1;
     float myw = 0.0f;
     if (k0 + lane < g.R) {
       const int gs = __ldg(gsend + q0 + k0 + lane);
       const int gl = __ldg(gslot + q0 + k0 + lane);
       if (gs >= 0 && gl >= 0) {
-        myrow = gs;
+        myrow = FUSED ? gl : gs;
         myw = __ldg(w + q0 + k0 + lane);
+        if (FUSED) {
+          mys = gs;
+          myr = __ldg(grecv + q0 + k0 + lane);
+        }
       }
     }
     const int kn = min(32, g.R - k0);
@@ -587,7 +633,18 @@ __global__ void __launch_bounds__(kReduceThreads) k_combine_reduce(Geo g, const 
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         v[j] = make_uint4(0, 0, 0, 0);
-        if (act && rk[j] >= 0) v[j] = ld_stream16(crecv + (int64_t)rk[j] * g.H + col * 8);
+        if (act && rk[j] >= 0) v[j] = ld_stream16(src + (int64_t)rk[j] * g.H + col * 8);
+      }
+      if (FUSED) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int rs = __shfl_sync(kFull, mys, (j0 + j) & 31);
+          const int rr = __shfl_sync(kFull, myr, (j0 + j) & 31);
+          if (act && rk[j] >= 0) {
+            st16(csend + (int64_t)rr * g.H + col * 8, v[j]);
+            st16(crecv + (int64_t)rs * g.H + col * 8, v[j]);
+          }
+        }
       }
 #pragma unroll
       for (int j = 0; j < 8; ++j)
@@ -823,6 +880,19 @@ cudaError_t launch_quant_fp8(const Geo& g0, const uint16_t* x, uint8_t* xq, Ctx&
   return launch_kernel(k_quant_fp8, dim3((unsigned)blocks), dim3(256), 0, c, g, x, xq);
 }
 
+template <bool ALL>
+cudaError_t run_quant_pack(const Geo& g, const uint16_t* x, const int32_t* fan, uint8_t* dst, Ctx& c, int t0, int nt,
+                           const FanAll& fa, int64_t blocks) {
+  const bool ranged = nt != g.T;
+  if (g.B % 16 == 0) {   // 16-byte code stores (same unit count: 8 blocks of a row per warp)
+    auto k16 = ranged ? k_quant_pack16<true, ALL> : k_quant_pack16<false, ALL>;
+    return launch_kernel(k16, dim3((unsigned)blocks), dim3(256), 0, c, g, x, fan, dst, t0, nt, fa);
+  }
+  auto k = g.B % 8 == 0 ? (ranged ? k_quant_pack<true, true, ALL> : k_quant_pack<true, false, ALL>)
+                        : (ranged ? k_quant_pack<false, true, ALL> : k_quant_pack<false, false, ALL>);
+  return launch_kernel(k, dim3((unsigned)blocks), dim3(256), 0, c, g, x, fan, dst, t0, nt, fa);
+}
+
 cudaError_t launch_quant_pack(const Geo& g0, const int32_t* fan, const uint16_t* x, uint8_t* dst, Ctx& c, int t0,
                               int nt) {
   if (nt < 0) nt = g0.T;
@@ -842,14 +912,22 @@ cudaError_t launch_quant_pack(const Geo& g0, const int32_t* fan, const uint16_t*
   const int64_t maxb = (int64_t)c.num_sms * 8;
   if (blocks > maxb) blocks = maxb;
   LaunchScope ls(c, MOE_K_QUANT_PACK);
-  const bool ranged = nt != g.T;
-  if (g.B % 16 == 0) {   // 16-byte code stores (same unit count: 8 blocks of a row per warp)
-    auto k16 = ranged ? k_quant_pack16<true> : k_quant_pack16<false>;
-    return launch_kernel(k16, dim3((unsigned)blocks), dim3(256), 0, c, g, x, fan, dst, t0, nt);
-  }
-  auto k = g.B % 8 == 0 ? (ranged ? k_quant_pack<true, true> : k_quant_pack<true, false>)
-                        : (ranged ? k_quant_pack<false, true> : k_quant_pack<false, false>);
-  return launch_kernel(k, dim3((unsigned)blocks), dim3(256), 0, c, g, x, fan, dst, t0, nt);
+  return run_quant_pack<false>(g, x, fan, dst, c, t0, nt, FanAll{}, blocks);
+}
+
+cudaError_t launch_quant_dispatch_fused(const Geo& g, const moe_layout_t* lay, const uint16_t* x, uint8_t* send,
+                                        uint8_t* recv, uint8_t* ex, float* exs, Ctx& c, int t0, int nt) {
+  if (nt < 0) nt = g.T;
+  if (windowed(g, c)) return cudaErrorInvalidValue;
+  const int64_t upr = (g.H / 128 + 2 * kQuantUnroll - 1) / (2 * kQuantUnroll);
+  const int64_t units = (int64_t)g.N * nt * upr;
+  if (units == 0) return cudaSuccess;
+  int64_t blocks = (units + 7) / 8;
+  const int64_t maxb = (int64_t)c.num_sms * 8;
+  if (blocks > maxb) blocks = maxb;
+  LaunchScope ls(c, MOE_K_QUANT_DISPATCH_FUSED);
+  return run_quant_pack<true>(g, x, lay->gsend, send, c, t0, nt, FanAll{lay->grecv, lay->gslot, recv, ex, exs},
+                              blocks);
 }
 
 cudaError_t launch_dequant_fp8(const Geo& g, const moe_layout_t* lay, const uint8_t* exq, const float* exs,
@@ -899,8 +977,23 @@ cudaError_t launch_combine_reduce(const Geo& g0, const moe_layout_t* lay, const 
   const int ncol = g.H / 8;
   dim3 grid((unsigned)tokens, (unsigned)((ncol + kReduceThreads - 1) / kReduceThreads));
   LaunchScope ls(c, MOE_K_COMBINE_REDUCE);
-  return launch_kernel(nt != g.T ? k_combine_reduce<true> : k_combine_reduce<false>, grid, dim3(kReduceThreads), 0, c,
-                       g, gsend, gslot, w, crecv, out, t0, nt);
+  return launch_kernel(nt != g.T ? k_combine_reduce<true, false> : k_combine_reduce<false, false>, grid,
+                       dim3(kReduceThreads), 0, c, g, gsend, gslot, (const int32_t*)nullptr, w, crecv,
+                       (uint16_t*)nullptr, (uint16_t*)nullptr, out, t0, nt);
+}
+
+cudaError_t launch_combine_fused(const Geo& g, const moe_layout_t* lay, const uint16_t* ey, uint16_t* csend,
+                                 uint16_t* crecv, const float* w, uint16_t* out, Ctx& c, int t0, int nt) {
+  if (nt < 0) nt = g.T;
+  if (windowed(g, c)) return cudaErrorInvalidValue;
+  const int64_t tokens = (int64_t)g.N * nt;
+  if (tokens == 0) return cudaSuccess;
+  const int ncol = g.H / 8;
+  dim3 grid((unsigned)tokens, (unsigned)((ncol + kReduceThreads - 1) / kReduceThreads));
+  LaunchScope ls(c, MOE_K_COMBINE_FUSED);
+  return launch_kernel(nt != g.T ? k_combine_reduce<true, true> : k_combine_reduce<false, true>, grid,
+                       dim3(kReduceThreads), 0, c, g, (const int32_t*)lay->gsend, (const int32_t*)lay->gslot,
+                       (const int32_t*)lay->grecv, w, ey, csend, crecv, out, t0, nt);
 }
 
 }  // namespace moe

@@ -91,10 +91,10 @@ typedef enum {
     MOE_K_DISPATCH_SPLIT = 15, /* split-phase dispatch: push, signal, wait, shuffle in one launch */
     MOE_K_QUANT_PACK = 16,     /* fp8 quantisation fused into the pack */
     MOE_K_DISPATCH_DEDICATED = 17, /* split-phase dispatch with dedicated space and piggybacked routing */
-    MOE_K_SCATTER_UNPACK = 18, /* scatter and unpack fused: send row -> receive row and grouped row */
-    MOE_K_COMBINE_PACK_SCATTER = 19, /* combine pack and scatter fused: output row -> receive-order row
-                                        and the source's combine row */
-    MOE_K_NUM = 20
+    MOE_K_DISPATCH_FUSED = 18, /* pack, write and shuffle in one kernel (bf16) */
+    MOE_K_QUANT_DISPATCH_FUSED = 19, /* fp8 quantisation, pack, write and shuffle in one kernel */
+    MOE_K_COMBINE_FUSED = 20,  /* combine pack, write and weighted sum in one kernel */
+    MOE_K_NUM = 21
 } moe_kernel_id;
 
 /* Optional per-kernel timing. When moe_layout_t.prof is non-NULL, every kernel the library
@@ -144,12 +144,14 @@ typedef struct {
  * (for moe_forward_host: copies, then the pass, then the copy back; or, with
  * MOE_FLAG_HOST_MAPPED, the pass alone) instead of the default token batches. */
 #define MOE_FLAG_ONE_BATCH 0x40u
-/* The whole-pass and whole-phase calls (moe_forward, moe_forward_host, moe_dispatch,
- * moe_combine) read each pair's row once for the per-peer write and the shuffle behind it:
- * one kernel writes the receive row and the grouped row (dispatch), another the
- * receive-order row and the source's combine row (combine). Every buffer ends up as with
- * the separate calls, byte for byte. This flag runs the four moves as separate kernels
- * instead, as moe_dispatch_send + moe_dispatch_recv and moe_combine_send do. */
+/* The whole-pass and whole-phase calls (moe_forward, moe_dispatch, moe_combine and the
+ * copy-engine pipeline of moe_forward_host) run each phase of a token batch as one kernel:
+ * dispatch reads (and, for fp8, quantises) each token row once and stores it to its send
+ * rows, the owners' receive rows and the grouped rows; combine reads each kept pair's expert
+ * output row once, stores it to its receive-order row and its source's combine row, and sums
+ * the token's rows into its output. Every buffer ends up as with the separate calls, byte for
+ * byte, and so does the output. This flag runs the phases as the separate calls do instead
+ * (pack, write, shuffle; combine pack, write, sum). Direct push is unaffected. */
 #define MOE_FLAG_SEPARATE_MOVES 0x80u
 #define MOE_FLAG_NO_PDL 0x2u    /* launch without programmatic dependent launch (by default
                                    each kernel may be scheduled while its predecessor in the

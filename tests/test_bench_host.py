@@ -22,14 +22,16 @@ def test_algorithmic_bytes_match_the_scope_table():
     assert ab["scatter"] == ab["unpack"] == 2 * P * 2 * wl.H == 234_881_024
     assert ab["combine_pack"] + ab["combine_scatter"] == 469_762_048
     assert ab["combine_reduce"] == wl.N * wl.T * (wl.R + 1) * 2 * wl.H
-    # the fused moves: one read of each row, every write of the two moves they stand for
-    assert ab["scatter_unpack"] == ab["scatter"] + ab["unpack"] - P * 2 * wl.H
-    assert ab["combine_pack_scatter"] == ab["combine_pack"] + ab["combine_scatter"] - P * 2 * wl.H
+    # the one-kernel phases: one read of each row, every write of the kernels they stand for
+    assert ab["dispatch_fused"] == ab["pack"] + ab["scatter"] + ab["unpack"] - 2 * P * 2 * wl.H
+    assert ab["combine_fused"] == (ab["combine_pack"] + ab["combine_scatter"] + ab["combine_reduce"]
+                                   - 2 * P * 2 * wl.H)
     f = workloads.config(3)
     Pf = f.N * f.T * f.R
     abf = bench.algorithmic_bytes(f, Pf, Pf)
     assert abf["pack"] == f.N * f.T * (1 + f.R) * 7392 == 136_249_344
     assert abf["combine_reduce"] == f.N * f.T * (f.R + 1) * 2 * f.H == 264_241_152
+    assert abf["quant_dispatch_fused"] == abf["quant_pack"] + 2 * Pf * 7392
 
 
 def _worker(rank, port, q):

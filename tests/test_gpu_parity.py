@@ -200,8 +200,8 @@ def test_launch_counter_counts_kernels():
     n0 = lib().moe_launch_count()
     ep.forward(to_dev(inp["x"]).view(torch.bfloat16), to_dev(inp["idx"]), to_dev(inp["w"]))
     torch.cuda.synchronize()
-    # layout (3) + pack + scatter-and-unpack + combine pack-and-scatter + reduce; bf16 identity aliases
-    assert lib().moe_launch_count() - n0 == 7
+    # layout (3) + dispatch (pack, write, shuffle) + combine (pack, write, sum); bf16 identity aliases
+    assert lib().moe_launch_count() - n0 == 5
     ep.layout.flags |= 0x80   # MOE_FLAG_SEPARATE_MOVES: the four moves apart
     n0 = lib().moe_launch_count()
     ep.forward(to_dev(inp["x"]).view(torch.bfloat16), to_dev(inp["idx"]), to_dev(inp["w"]))
@@ -225,8 +225,7 @@ def test_profiling_events_bracket_each_kernel():
     ep.forward(to_dev(inp["x"]).view(torch.bfloat16), to_dev(inp["idx"]), to_dev(inp["w"]))
     torch.cuda.synchronize()
     names = [KERNEL_NAMES[prof.kernel[i]] for i in range(prof.n)]
-    assert names == ["route_count", "route_scan", "layout_maps", "quant_pack", "scatter_unpack", "expert",
-                     "combine_pack_scatter", "combine_reduce"]
+    assert names == ["route_count", "route_scan", "layout_maps", "quant_dispatch_fused", "expert", "combine_fused"]
     for i in range(prof.n):
         assert evs[2 * i].elapsed_time(evs[2 * i + 1]) >= 0.0
     out0 = ep.out.clone()
@@ -492,10 +491,11 @@ def test_dispatch_and_combine_phases_match_oracle(orc, wl, flags, batches):
                                                                    "separate-auto", "separate-ldg", "separate-tma"])
 @pytest.mark.parametrize("wl", CASES + MB_CASES, ids=lambda w: w.name)
 def test_fused_and_separate_moves_match_oracle(orc, wl, flags):
-    """moe_forward in one batch with the fused moves (scatter with unpack, combine pack with
-    combine scatter) and with the four moves apart (MOE_FLAG_SEPARATE_MOVES): in both, every
-    buffer, the receive and combine-send rows included, bit for bit as the oracle's, unused
-    rows untouched; each mover, fp8 rows that are not 16-byte multiples, capacity drops."""
+    """moe_forward in one batch with one kernel per phase (pack, write and shuffle; combine
+    pack, write and sum) and with the phases' kernels apart (MOE_FLAG_SEPARATE_MOVES): in
+    both, every buffer, the send, receive and combine-send rows included, bit for bit as the
+    oracle's, unused rows untouched; each mover, fp8 rows that are not 16-byte multiples,
+    capacity drops."""
     inp = workloads.make_inputs(wl)
     _, res = run_gpu(wl, inp, flags=flags | 0x40, forward=True)
     assert res["status_code"] == (3 if wl.cap else 0)
