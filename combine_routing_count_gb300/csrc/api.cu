@@ -437,20 +437,27 @@ int batch_start(int T, int nb, int j, bool shaped) {
   return (int)((wj * T + wsum / 2) / wsum);
 }
 
-// Micro-batches of moe_forward: the caller's choice (at most 32 and T), else about one per
-// 60 MB of dispatch and combine rows (pairs x (B + 2H) bytes; at most 16 and T); one with
+// Micro-batches of moe_forward: the caller's choice (at most 32 and T), else, for bf16 rows,
+// about one per 32 MB of dispatch and combine rows (pairs x (B + 2H) bytes; at most 24 and
+// T), and one per 60 MB (at most 16) for fp8 rows or with MOE_FLAG_SEPARATE_MOVES; one with
 // MOE_FLAG_ONE_BATCH or staged fp8 quantisation. Measured on GB300 with batches alternating
-// over two equal-priority streams, each the best of the counts tried: 4 batches of 235 MB
-// of rows (EP8, 18% faster than one), 6 of 356 MB (fp8 EP64, expert included, 16%), 16 of
-// 940 MB and 1074 MB (EP32 28%, EP16 24%); under ~35 MB one batch is fastest. Even counts
-// keep both streams equally loaded (EP8: 3 and 5 batches lose to 4 and 6), so an odd count
-// of 3 or more rounds up.
+// over two equal-priority streams, each the best of the counts tried. One kernel per phase:
+// 8 batches of 235 MB of rows (EP8, 10% faster than one), 24 of 940 MB and 1074 MB (EP32 9%
+// and EP16 6% faster than 8; 32 no better): while a batch's rows stay in L2, its combine
+// rewrites the send and receive rows its dispatch wrote before they reach DRAM (the combine
+// buffers may alias them). fp8, whose identity expert writes a bf16 row per pair inside the
+// chain: 6 of 356 MB (10% faster than one; 12 no faster than one). Separate kernels: 4
+// batches of 235 MB (EP8, 18% faster than one), 6 of 356 MB (fp8 EP64, expert included,
+// 16%), 16 of 940 MB and 1074 MB (EP32 28%, EP16 24%). Under ~35 MB one batch is fastest.
+// Even counts keep both streams equally loaded (EP8: 3 and 5 batches lose to 4 and 6), so an
+// odd count of 3 or more rounds up.
 int forward_batch_count(const Geo& g, const moe_layout_t* lay) {
   if (lay->flags & MOE_FLAG_ONE_BATCH) return 1;
   if (g.payload == MOE_PAYLOAD_FP8_E4M3_B128 && (lay->flags & MOE_FLAG_STAGED_QUANT)) return 1;
   int nb = lay->batches;
   if (nb <= 0) {
-    nb = (int)std::min(16L, std::lround((double)g.P * (g.B + 2.0 * g.H) / 60e6));
+    const bool fine = !(lay->flags & MOE_FLAG_SEPARATE_MOVES) && g.payload != MOE_PAYLOAD_FP8_E4M3_B128;
+    nb = (int)std::min(fine ? 24L : 16L, std::lround((double)g.P * (g.B + 2.0 * g.H) / (fine ? 32e6 : 60e6)));
     if (nb >= 3 && (nb & 1)) ++nb;   // even: both streams end together
   }
   if (nb > kMaxMicroBatches) nb = kMaxMicroBatches;
@@ -459,15 +466,15 @@ int forward_batch_count(const Geo& g, const moe_layout_t* lay) {
 }
 
 // Token batches of moe_dispatch and moe_combine (each phase on its own, the expert between
-// them a barrier): the caller's choice (at most 32 and T), else none up to 1024 tokens of
+// them a barrier): the caller's choice (at most 32 and T), else none up to 2048 tokens of
 // all ranks and about one per 8 tokens of a rank beyond (at most 16); one with
-// MOE_FLAG_ONE_BATCH. Measured on GB300 with batches alternating over two streams: 1024
-// tokens never gained; 64 ranks x 32 tokens (fp8) 4% with 4 batches; 32 x 128 and 16 x 512
-// tokens 9% with 16.
+// MOE_FLAG_ONE_BATCH. Measured on GB300 with batches alternating over two streams and one
+// kernel per phase: 1024 tokens never gained; 64 ranks x 32 tokens (fp8) 2.5% faster in one
+// batch than in 4; 16 x 512 tokens 1.5% faster in 16 than in one, slower in 24.
 int phase_batch_count(const Geo& g, const moe_layout_t* lay) {
   if (lay->flags & MOE_FLAG_ONE_BATCH) return 1;
   int nb = lay->batches;
-  if (nb <= 0) nb = (int64_t)g.N * g.T <= 1024 ? 1 : (int)std::min<int64_t>(16, g.T / 8);
+  if (nb <= 0) nb = (int64_t)g.N * g.T <= 2048 ? 1 : (int)std::min<int64_t>(16, g.T / 8);
   if (nb > kMaxMicroBatches) nb = kMaxMicroBatches;
   if (nb > g.T) nb = (int)g.T;
   return nb < 1 ? 1 : nb;

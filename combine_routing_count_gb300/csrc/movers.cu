@@ -289,8 +289,11 @@ __device__ __forceinline__ uint32_t ld_vec<uint32_t>(const uint8_t* p) {
 __device__ __forceinline__ void st_vec(uint8_t* p, const uint4& v) { st16(p, v); }
 __device__ __forceinline__ void st_vec(uint8_t* p, const uint32_t& v) { *reinterpret_cast<uint32_t*>(p) = v; }
 
+// The pack-all move keeps three destination rows per pair and takes 89 registers (two CTAs
+// of 256 threads per SM): measured on GB300, bounding it to three CTAs per SM (79 registers)
+// was 1-3% slower on every workload, and finer column chunks changed nothing.
 template <int KIND, bool FP8, typename V, int MODE, bool REV>
-__device__ __forceinline__ void move_ldg(const Geo& g, const MoveArgs& a) {
+__global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
   constexpr int U = 8;
   constexpr int W = (int)sizeof(V);
   const int lane = threadIdx.x & 31;
@@ -384,26 +387,6 @@ __device__ __forceinline__ void move_ldg(const Geo& g, const MoveArgs& a) {
   pdl_trigger();
 }
 
-template <int KIND, bool FP8, typename V, int MODE, bool REV>
-__global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
-  move_ldg<KIND, FP8, V, MODE, REV>(g, a);
-}
-
-// The pack-all move keeps three destination rows per pair: without a bound it takes 89
-// registers, two CTAs of 256 threads per SM; bounded to three.
-template <int KIND, bool FP8, typename V, int MODE, bool REV>
-__global__ void __launch_bounds__(256, 3) k_move_ldg_all(Geo g, MoveArgs a) {
-  move_ldg<KIND, FP8, V, MODE, REV>(g, a);
-}
-
-template <int KIND, bool FP8, typename V, int MODE, bool REV>
-constexpr auto ldg_kernel() {
-  if constexpr (KIND == kMovePackAll)
-    return k_move_ldg_all<KIND, FP8, V, MODE, REV>;
-  else
-    return k_move_ldg<KIND, FP8, V, MODE, REV>;
-}
-
 // Largest dynamic shared memory limit set so far, per TMA instantiation and device.
 std::atomic<int> g_tma_smem[9][2][3][2][64];
 
@@ -449,7 +432,7 @@ cudaError_t run_ldg(const Geo& g, const MoveArgs& a, Ctx& c) {
   static std::atomic<int> resident{0};
   int per_sm = resident.load(std::memory_order_relaxed);
   if (per_sm == 0) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ldg_kernel<KIND, FP8, V, MODE, REV>(), 256, 0) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_move_ldg<KIND, FP8, V, MODE, REV>, 256, 0) !=
             cudaSuccess ||
         per_sm < 1)
       per_sm = 1;
@@ -459,7 +442,7 @@ cudaError_t run_ldg(const Geo& g, const MoveArgs& a, Ctx& c) {
   int64_t blocks = (a.units + 7) / 8;
   const int64_t maxb = (int64_t)c.num_sms * per_sm;
   if (blocks > maxb) blocks = maxb;
-  return launch_kernel(ldg_kernel<KIND, FP8, V, MODE, REV>(), dim3((unsigned)blocks), dim3(256), 0, c, g, a);
+  return launch_kernel(k_move_ldg<KIND, FP8, V, MODE, REV>, dim3((unsigned)blocks), dim3(256), 0, c, g, a);
 }
 
 // True when two stages per issuer fit in one CTA's shared memory.

@@ -419,12 +419,13 @@ moe_status moe_combine_recv(const moe_dims *dims, const moe_layout_t *lay, const
                             const float *d_w, uint16_t *d_out, void *stream);
 
 /* Whole phases, as the page's dispatch and combine calls (section "Dispatch and combine"):
- * moe_dispatch is moe_dispatch_send followed by moe_dispatch_recv (fp8: d_x holds the bf16
- * token rows, always quantised inside the pack as moe_quantize_dispatch_send does, so
- * MOE_FLAG_STAGED_QUANT does not apply; d_send unused with MOE_FLAG_DIRECT_PUSH);
- * moe_combine is moe_combine_send followed by moe_combine_recv. Arguments as in those
- * calls; the expert work goes between the two. Each phase may run in nb token batches
- * (nb = moe_batches(dims, lay, 2): lay->batches, else none up to 1024 tokens of all ranks
+ * moe_dispatch leaves what moe_dispatch_send followed by moe_dispatch_recv leaves (fp8: d_x
+ * holds the bf16 token rows, always quantised inside the pack as moe_quantize_dispatch_send
+ * does, so MOE_FLAG_STAGED_QUANT does not apply; d_send unused with MOE_FLAG_DIRECT_PUSH);
+ * moe_combine leaves what moe_combine_send followed by moe_combine_recv leaves. One kernel
+ * per phase and token batch unless MOE_FLAG_SEPARATE_MOVES or MOE_FLAG_DIRECT_PUSH. Arguments
+ * as in those calls; the expert work goes between the two. Each phase may run in nb token batches
+ * (nb = moe_batches(dims, lay, 2): lay->batches, else none up to 2048 tokens of all ranks
  * and about T/8 beyond, at most 16; one with MOE_FLAG_ONE_BATCH), batch j covering tokens
  * [j*T/nb, (j+1)*T/nb) of every rank, odd batches on the library's
  * second stream, which the caller's stream waits for before the call returns. Every
@@ -452,20 +453,22 @@ moe_status moe_combine_send_partial(const moe_dims *dims, const moe_layout_t *la
 moe_status moe_combine_recv_partial(const moe_dims *dims, const moe_layout_t *lay, const uint16_t *d_cpart,
                                     uint16_t *d_out, void *stream);
 
-/* One whole pass: moe_layout, moe_quantize_dispatch_send (fp8; or moe_quantize_fp8_b128 +
- * moe_dispatch_send with MOE_FLAG_STAGED_QUANT) or moe_dispatch_send (bf16),
- * moe_dispatch_recv, moe_expert_identity, moe_combine_send, moe_combine_recv. Returns the
- * first error. bufs->x, idx, w and out may also be device-accessible host memory.
+/* One whole pass, with the results of moe_layout, moe_quantize_dispatch_send (fp8; or
+ * moe_quantize_fp8_b128 + moe_dispatch_send with MOE_FLAG_STAGED_QUANT) or moe_dispatch_send
+ * (bf16), moe_dispatch_recv, moe_expert_identity, moe_combine_send and moe_combine_recv in
+ * every buffer, bit for bit (each phase one kernel per token batch unless
+ * MOE_FLAG_SEPARATE_MOVES; staged fp8 quantisation runs those calls). Returns the first
+ * error. bufs->x, idx, w and out may also be device-accessible host memory.
  * After the layout, the pass runs as nb micro-batches (nb = moe_batches(dims, lay, 0):
- * lay->batches (at most 32 and T), or automatically about one per 60 MB of dispatch and
+ * lay->batches (at most 32 and T), or automatically about one per 32 MB of dispatch and
  * combine rows (N*T*R pairs x (row bytes + 2H)), rounded up to an even count from 3, at most
- * 16 and T;
+ * 24 and T (fp8 rows, or MOE_FLAG_SEPARATE_MOVES: one per 60 MB, at most 16);
  * one with MOE_FLAG_ONE_BATCH or staged fp8 quantisation). Micro-batch j covers tokens
- * [j*T/nb, (j+1)*T/nb) of every rank and runs dispatch send and recv, the identity expert
- * and the combine on only those tokens' rows (the same kernels, restricted to a token
- * range), odd micro-batches on the library's second stream (created on first use,
- * kept until exit); the caller's stream waits for it before the call returns. Every
- * buffer ends up as in one batch, bit for bit.
+ * [j*T/nb, (j+1)*T/nb) of every rank and runs the dispatch, the identity expert and the
+ * combine on only those tokens' rows (the same kernels, restricted to a token range), odd
+ * micro-batches on the library's second stream (created on first use, kept until exit);
+ * the caller's stream waits for it before the call returns. Every buffer ends up as in one
+ * batch, bit for bit.
  * Graph capture: a captured call forks the library's stream into the capture and joins it
  * back, so the pass captures like any other stream work; while a capture that holds such
  * a call is open on a device, no other thread may run a multi-batch moe_forward or

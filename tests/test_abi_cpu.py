@@ -130,21 +130,25 @@ def test_host_batch_count_rule(L):
 
 
 def test_forward_micro_batch_count_rule(L):
-    """moe_forward's micro-batches: about one per 60 MB of dispatch and combine rows by default
-    (at most 16 and T), the caller's count when set (at most 32 and T), one for the one-batch flag and
-    for the staged fp8 quantiser. Host only."""
+    """moe_forward's micro-batches: about one per 32 MB of dispatch and combine rows for bf16
+    (at most 24 and T), one per 60 MB for fp8 or with separate kernels (at most 16), the
+    caller's count when set (at most 32 and T), one for the one-batch flag and for the staged
+    fp8 quantiser. Host only."""
     from combine_routing_count_gb300 import MoeLayout
     def nb(N, T, H, E, R, payload=0, flags=0, batches=0):
         lay = MoeLayout()
         lay.flags, lay.batches = flags, batches
         return L.moe_batches(ctypes.byref(_dims(N, T, H, E, R, 0, payload)), ctypes.byref(lay), 0)
-    assert nb(8, 128, 7168, 256, 8) == 4         # 235 MB of rows
-    assert nb(64, 32, 7168, 384, 8, 1) == 6      # 356 MB (fp8 rows of 7392 B)
-    assert nb(32, 128, 7168, 384, 8) == 16       # 940 MB
-    assert nb(16, 512, 4096, 128, 8) == 16       # 1074 MB: capped
+    assert nb(8, 128, 7168, 256, 8) == 8         # 235 MB of rows: 7, rounded up to an even count
+    assert nb(64, 32, 7168, 384, 8, 1) == 6      # 356 MB (fp8 rows of 7392 B): one per 60 MB
+    assert nb(32, 128, 7168, 384, 8) == 24       # 940 MB: capped
+    assert nb(16, 512, 4096, 128, 8) == 24       # 1074 MB: capped
     assert nb(2, 16, 128, 8, 2) == 1             # 32 tokens
-    assert nb(8, 64, 7168, 256, 8) == 2          # 117 MB
-    assert nb(8, 160, 7168, 256, 8) == 6         # 294 MB: 5 rounded up to an even count
+    assert nb(8, 32, 7168, 256, 8) == 2          # 59 MB
+    assert nb(8, 64, 7168, 256, 8) == 4          # 117 MB
+    assert nb(8, 128, 7168, 256, 8, flags=0x80) == 4    # separate kernels: one per 60 MB
+    assert nb(32, 128, 7168, 384, 8, flags=0x80) == 16  # capped at 16
+    assert nb(8, 160, 7168, 256, 8, flags=0x80) == 6    # 294 MB: 5 rounded up to an even count
     assert nb(8, 128, 7168, 256, 8, batches=3) == 3
     assert nb(8, 2, 7168, 256, 8, batches=9) == 2
     assert nb(16, 512, 4096, 128, 8, batches=20) == 20
@@ -154,7 +158,7 @@ def test_forward_micro_batch_count_rule(L):
 
 
 def test_phase_batch_count_rule(L):
-    """moe_dispatch / moe_combine token batches: none up to 1024 tokens of all ranks, about
+    """moe_dispatch / moe_combine token batches: none up to 2048 tokens of all ranks, about
     T/8 beyond (at most 16), the caller's count when set (at most 32 and T), one with the
     one-batch flag. Host only."""
     from combine_routing_count_gb300 import MoeLayout
@@ -163,7 +167,8 @@ def test_phase_batch_count_rule(L):
         lay.flags, lay.batches = flags, batches
         return L.moe_batches(ctypes.byref(_dims(N, T, H, E, R, 0, payload)), ctypes.byref(lay), 2)
     assert nb(8, 128, 7168, 256, 8) == 1         # 1024 tokens
-    assert nb(64, 32, 7168, 384, 8, 1) == 4      # 2048 tokens, T = 32
+    assert nb(64, 32, 7168, 384, 8, 1) == 1      # 2048 tokens
+    assert nb(64, 64, 7168, 384, 8, 1) == 8      # 4096 tokens, T = 64
     assert nb(32, 128, 7168, 384, 8) == 16       # T = 128
     assert nb(16, 512, 4096, 128, 8) == 16       # T = 512: capped
     assert nb(8, 128, 7168, 256, 8, batches=5) == 5
