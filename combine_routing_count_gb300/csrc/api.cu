@@ -358,15 +358,19 @@ cudaError_t dispatch_range(const Geo& g, const moe_layout_t* lay, const void* x,
                            float* exs, int t0, int nt, Ctx& c) {
   const bool fp8 = g.payload == MOE_PAYLOAD_FP8_E4M3_B128;
   cudaError_t e;
-  if (c.flags & MOE_FLAG_DIRECT_PUSH) {
+  const bool push = (c.flags & MOE_FLAG_DIRECT_PUSH) != 0;
+  if (!(c.flags & MOE_FLAG_SEPARATE_MOVES)) {
+    // pack, write and shuffle in one kernel: each token row read (and quantised) once; direct
+    // push writes no send rows
+    void* snd = push ? nullptr : send;
+    return fp8 ? launch_quant_dispatch_fused(g, lay, static_cast<const uint16_t*>(x), static_cast<uint8_t*>(snd),
+                                             static_cast<uint8_t*>(recv), static_cast<uint8_t*>(ex), exs, c, t0, nt)
+               : launch_move_range(kMovePackAll, g, lay, x, snd, recv, t0, nt, c, ex);
+  }
+  if (push) {
     e = fp8 ? launch_quant_pack(g, lay->grecv, static_cast<const uint16_t*>(x), static_cast<uint8_t*>(recv), c, t0,
                                 nt)
             : launch_move_range(kMovePackPush, g, lay, x, recv, nullptr, t0, nt, c);
-  } else if (!(c.flags & MOE_FLAG_SEPARATE_MOVES)) {
-    // pack, write and shuffle in one kernel: each token row read (and quantised) once
-    return fp8 ? launch_quant_dispatch_fused(g, lay, static_cast<const uint16_t*>(x), static_cast<uint8_t*>(send),
-                                             static_cast<uint8_t*>(recv), static_cast<uint8_t*>(ex), exs, c, t0, nt)
-               : launch_move_range(kMovePackAll, g, lay, x, send, recv, t0, nt, c, ex);
   } else {
     e = fp8 ? launch_quant_pack(g, lay->gsend, static_cast<const uint16_t*>(x), static_cast<uint8_t*>(send), c, t0,
                                 nt)
@@ -383,11 +387,14 @@ cudaError_t dispatch_range(const Geo& g, const moe_layout_t* lay, const void* x,
 cudaError_t combine_range(const Geo& g, const moe_layout_t* lay, const uint16_t* ey, uint16_t* csend, uint16_t* crecv,
                           const float* w, uint16_t* out, int t0, int nt, Ctx& c) {
   cudaError_t e;
-  if (c.flags & MOE_FLAG_DIRECT_PUSH) {
+  const bool push = (c.flags & MOE_FLAG_DIRECT_PUSH) != 0;
+  if (!(c.flags & MOE_FLAG_SEPARATE_MOVES)) {
+    // combine pack, write and weighted sum in one kernel: each expert output row read once;
+    // direct push writes no receive-order rows
+    return launch_combine_fused(g, lay, ey, push ? nullptr : csend, crecv, w, out, c, t0, nt);
+  }
+  if (push) {
     e = launch_move_range(kMoveCPush, g, lay, ey, crecv, nullptr, t0, nt, c);
-  } else if (!(c.flags & MOE_FLAG_SEPARATE_MOVES)) {
-    // combine pack, write and weighted sum in one kernel: each expert output row read once
-    return launch_combine_fused(g, lay, ey, csend, crecv, w, out, c, t0, nt);
   } else {
     e = combine_send_range(g, lay, ey, csend, crecv, t0, nt, c);
   }
@@ -439,14 +446,16 @@ int batch_start(int T, int nb, int j, bool shaped) {
 
 // Micro-batches of moe_forward: the caller's choice (at most 32 and T), else, for bf16 rows,
 // about one per 32 MB of dispatch and combine rows (pairs x (B + 2H) bytes; at most 24 and
-// T), and one per 60 MB (at most 16) for fp8 rows or with MOE_FLAG_SEPARATE_MOVES; one with
-// MOE_FLAG_ONE_BATCH or staged fp8 quantisation. Measured on GB300 with batches alternating
-// over two equal-priority streams, each the best of the counts tried. One kernel per phase:
-// 8 batches of 235 MB of rows (EP8, 10% faster than one), 24 of 940 MB and 1074 MB (EP32 9%
-// and EP16 6% faster than 8; 32 no better): while a batch's rows stay in L2, its combine
-// rewrites the send and receive rows its dispatch wrote before they reach DRAM (the combine
-// buffers may alias them). fp8, whose identity expert writes a bf16 row per pair inside the
-// chain: 6 of 356 MB (10% faster than one; 12 no faster than one). Separate kernels: 4
+// T), and one per 60 MB (at most 16) for fp8 rows, with direct push or with
+// MOE_FLAG_SEPARATE_MOVES; one with MOE_FLAG_ONE_BATCH or staged fp8 quantisation. Measured
+// on GB300 with batches alternating over two equal-priority streams, each the best of the
+// counts tried. One kernel per phase: 8 batches of 235 MB of rows (EP8, 10% faster than
+// one), 24 of 940 MB and 1074 MB (EP32 9% and EP16 6% faster than 8; 32 no better): while a
+// batch's rows stay in L2, its combine rewrites the send and receive rows its dispatch wrote
+// before they reach DRAM (the combine buffers may alias them). With direct push, which writes
+// neither, 4 of 235 MB and 16 of 940 MB and 1074 MB (EP8 10%, EP32 6%, EP16 5% faster than 8,
+// 24 and 24). fp8, whose identity expert writes a bf16 row per pair inside the chain: 6 of
+// 356 MB (10% faster than one; 12 no faster than one). Separate kernels: 4
 // batches of 235 MB (EP8, 18% faster than one), 6 of 356 MB (fp8 EP64, expert included,
 // 16%), 16 of 940 MB and 1074 MB (EP32 28%, EP16 24%). Under ~35 MB one batch is fastest.
 // Even counts keep both streams equally loaded (EP8: 3 and 5 batches lose to 4 and 6), so an
@@ -456,7 +465,8 @@ int forward_batch_count(const Geo& g, const moe_layout_t* lay) {
   if (g.payload == MOE_PAYLOAD_FP8_E4M3_B128 && (lay->flags & MOE_FLAG_STAGED_QUANT)) return 1;
   int nb = lay->batches;
   if (nb <= 0) {
-    const bool fine = !(lay->flags & MOE_FLAG_SEPARATE_MOVES) && g.payload != MOE_PAYLOAD_FP8_E4M3_B128;
+    const bool fine = !(lay->flags & (MOE_FLAG_SEPARATE_MOVES | MOE_FLAG_DIRECT_PUSH)) &&
+                      g.payload != MOE_PAYLOAD_FP8_E4M3_B128;
     nb = (int)std::min(fine ? 24L : 16L, std::lround((double)g.P * (g.B + 2.0 * g.H) / (fine ? 32e6 : 60e6)));
     if (nb >= 3 && (nb & 1)) ++nb;   // even: both streams end together
   }

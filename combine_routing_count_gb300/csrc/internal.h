@@ -132,8 +132,9 @@ enum MoveKind : int {
   kMoveCopyEx = 5,    // grouped rows -> grouped rows (bf16 identity expert, distinct output)
   kMovePackPush = 6,  // direct push: token rows -> R receive rows of the owner ranks
   kMoveCPush = 7,     // direct push: grouped expert output rows -> source ranks' combine rows
-  kMovePackAll = 8,   // pack, write and shuffle in one move: token row -> its R send rows (dst), the
-                      // owners' receive rows (dst2) and the kept pairs' grouped rows (dst3), bf16
+  kMovePackAll = 8,   // pack, write and shuffle in one move: token row -> its R send rows (dst; none
+                      // when dst is null, direct push), the owners' receive rows (dst2) and the
+                      // kept pairs' grouped rows (dst3), bf16
 };
 
 // Moves whose unit is a (token, column chunk) that fans out to the token's R pairs.
@@ -161,13 +162,14 @@ cudaError_t launch_combine_sum(const Geo& g, const moe_layout_t* lay, const uint
 cudaError_t launch_combine_reduce(const Geo& g, const moe_layout_t* lay, const uint16_t* crecv, const float* w,
                                   uint16_t* out, Ctx& c, int t0 = 0, int nt = -1);   // t0, nt as launch_quant_pack
 // fp8 quantisation, pack, write and shuffle in one kernel: each token row quantised once and
-// stored to its R send rows, the owners' receive rows and the kept pairs' grouped codes and
-// scales (whole group only).
+// stored to its R send rows (none when send is null: direct push), the owners' receive rows
+// and the kept pairs' grouped codes and scales (whole group only).
 cudaError_t launch_quant_dispatch_fused(const Geo& g, const moe_layout_t* lay, const uint16_t* x, uint8_t* send,
                                         uint8_t* recv, uint8_t* ex, float* exs, Ctx& c, int t0 = 0, int nt = -1);
 // Combine pack, write and weighted sum in one kernel: each kept pair's expert output row read
-// once, stored to its receive-order row (csend) and its source's combine row (crecv), and
-// summed into the token's output as launch_combine_reduce does (whole group only).
+// once, stored to its receive-order row (csend; none when csend is null: direct push) and its
+// source's combine row (crecv), and summed into the token's output as launch_combine_reduce
+// does (whole group only).
 cudaError_t launch_combine_fused(const Geo& g, const moe_layout_t* lay, const uint16_t* ey, uint16_t* csend,
                                  uint16_t* crecv, const float* w, uint16_t* out, Ctx& c, int t0 = 0, int nt = -1);
 

@@ -161,12 +161,14 @@ template <int KIND, bool FP8>
 __device__ __forceinline__ void issue_stores(const Geo& g, const MoveArgs& a, const Plan& pl, const uint8_t* stage,
                                              uint32_t bytes) {
   if (is_pack_kind(KIND)) {
+    if (KIND != kMovePackAll || a.dst) {   // pack-all with direct push has no send rows
 #pragma unroll
-    for (int k = 0; k < kPackPrefetch; ++k)
-      if (pl.p[k] >= 0) bulk_s2g(a.dst + (int64_t)pl.p[k] * g.B + pl.coff, stage, bytes);
-    for (int k = kPackPrefetch; k < g.R; ++k) {
-      const int p = __ldg(a.fan + pl.tok * g.R + k);
-      if (p >= 0) bulk_s2g(a.dst + (int64_t)p * g.B + pl.coff, stage, bytes);
+      for (int k = 0; k < kPackPrefetch; ++k)
+        if (pl.p[k] >= 0) bulk_s2g(a.dst + (int64_t)pl.p[k] * g.B + pl.coff, stage, bytes);
+      for (int k = kPackPrefetch; k < g.R; ++k) {
+        const int p = __ldg(a.fan + pl.tok * g.R + k);
+        if (p >= 0) bulk_s2g(a.dst + (int64_t)p * g.B + pl.coff, stage, bytes);
+      }
     }
     if (KIND == kMovePackAll) {   // the receive rows, and the grouped rows of the kept pairs
       for (int k = 0; k < g.R; ++k) {
@@ -310,7 +312,7 @@ __global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
       const int64_t tok = range_item<MODE>(g, a, tv, 1);
       const int64_t coff = (u - tv * a.chunks) * (int64_t)a.chunk_bytes;
       const uint8_t* src = a.src + tok * g.B + coff;
-      uint8_t* dst0 = a.dst + coff;
+      uint8_t* dst0 = a.dst ? a.dst + coff : nullptr;
       const int32_t* fan = a.fan + tok * g.R;
       const int myp = lane < g.R ? __ldg(fan + lane) : -1;   // pairs 0..31 (R > 32: see below)
       // pack-all: the pair's receive row and grouped row (-1: dropped) as well
@@ -332,14 +334,14 @@ __global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
             const int rr = k < 32 ? __shfl_sync(0xffffffffu, myr, k) : __ldg(a.grecv + tok * g.R + k);
             const int rl = k < 32 ? __shfl_sync(0xffffffffu, myl, k) : __ldg(a.gslot + tok * g.R + k);
             if (p < 0) continue;
-            uint8_t* d = dst0 + (int64_t)p * g.B;
+            uint8_t* d = a.dst ? dst0 + (int64_t)p * g.B : nullptr;   // none with direct push
             uint8_t* d2 = a.dst2 + coff + (int64_t)rr * g.B;
             uint8_t* d3 = a.dst3 + coff + (int64_t)rl * g.B;
 #pragma unroll
             for (int j = 0; j < U; ++j) {
               const int64_t v = v0 + 32 * j;
               if (v < nel) {
-                st_vec(d + v * W, r[j]);
+                if (d) st_vec(d + v * W, r[j]);
                 st_vec(d2 + v * W, r[j]);
                 if (rl >= 0) st_vec(d3 + v * W, r[j]);
               }

@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(256) k_quant_pack(Geo g, const uint16_t* __res
       const int rl = ALL ? (k < 32 ? __shfl_sync(kFull, myl, k) : __ldg(fa.gslot + row * g.R + k)) : -1;
       if (p < 0) continue;
 #pragma unroll 1
-      for (int dsel = 0; dsel < (ALL ? 3 : 1); ++dsel) {   // send row, receive row, grouped row
+      for (int dsel = dst ? 0 : 1; dsel < (ALL ? 3 : 1); ++dsel) {   // send (none with direct push), receive, grouped
         if (dsel == 2 && rl < 0) break;
         uint8_t* dr = dsel == 0 ? dst + (int64_t)p * g.B
                                 : dsel == 1 ? fa.recv + (int64_t)rr * g.B : fa.ex + (int64_t)rl * g.H;
@@ -439,7 +439,7 @@ __global__ void __launch_bounds__(256) k_quant_pack16(Geo g, const uint16_t* __r
       const int rl = ALL ? (k < 32 ? __shfl_sync(kFull, myl, k) : __ldg(fa.gslot + row * g.R + k)) : -1;
       if (p < 0) continue;
 #pragma unroll 1
-      for (int dsel = 0; dsel < (ALL ? 3 : 1); ++dsel) {   // send row, receive row, grouped row
+      for (int dsel = dst ? 0 : 1; dsel < (ALL ? 3 : 1); ++dsel) {   // send (none with direct push), receive, grouped
         if (dsel == 2 && rl < 0) break;
         uint8_t* dr = dsel == 0 ? dst + (int64_t)p * g.B
                                 : dsel == 1 ? fa.recv + (int64_t)rr * g.B : fa.ex + (int64_t)rl * g.H;
@@ -584,8 +584,9 @@ constexpr int kReduceThreads = 128;
 
 // FUSED: the combine pack and write in the same pass. The rows are read from the grouped
 // expert outputs (src = ey, at gslot) instead of the combine rows, and each is also stored to
-// its receive-order row csend[grecv] and its source's combine row crecv[gsend], the rows the
-// combine send writes; the sum is the same, value for value.
+// its receive-order row csend[grecv] (unless csend is null: direct push) and its source's
+// combine row crecv[gsend], the rows the combine send writes; the sum is the same, value for
+// value.
 template <bool RANGED, bool FUSED>
 __global__ void __launch_bounds__(kReduceThreads) k_combine_reduce(Geo g, const int32_t* __restrict__ gsend,
                                                                    const int32_t* __restrict__ gslot,
@@ -641,7 +642,7 @@ __global__ void __launch_bounds__(kReduceThreads) k_combine_reduce(Geo g, const 
           const int rs = __shfl_sync(kFull, mys, (j0 + j) & 31);
           const int rr = __shfl_sync(kFull, myr, (j0 + j) & 31);
           if (act && rk[j] >= 0) {
-            st16(csend + (int64_t)rr * g.H + col * 8, v[j]);
+            if (csend) st16(csend + (int64_t)rr * g.H + col * 8, v[j]);   // none with direct push
             st16(crecv + (int64_t)rs * g.H + col * 8, v[j]);
           }
         }

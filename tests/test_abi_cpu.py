@@ -131,7 +131,7 @@ def test_host_batch_count_rule(L):
 
 def test_forward_micro_batch_count_rule(L):
     """moe_forward's micro-batches: about one per 32 MB of dispatch and combine rows for bf16
-    (at most 24 and T), one per 60 MB for fp8 or with separate kernels (at most 16), the
+    (at most 24 and T), one per 60 MB for fp8, direct push or separate kernels (at most 16), the
     caller's count when set (at most 32 and T), one for the one-batch flag and for the staged
     fp8 quantiser. Host only."""
     from combine_routing_count_gb300 import MoeLayout
@@ -147,6 +147,7 @@ def test_forward_micro_batch_count_rule(L):
     assert nb(8, 32, 7168, 256, 8) == 2          # 59 MB
     assert nb(8, 64, 7168, 256, 8) == 4          # 117 MB
     assert nb(8, 128, 7168, 256, 8, flags=0x80) == 4    # separate kernels: one per 60 MB
+    assert nb(16, 512, 4096, 128, 8, flags=0x8) == 16   # direct push: one per 60 MB, capped at 16
     assert nb(32, 128, 7168, 384, 8, flags=0x80) == 16  # capped at 16
     assert nb(8, 160, 7168, 256, 8, flags=0x80) == 6    # 294 MB: 5 rounded up to an even count
     assert nb(8, 128, 7168, 256, 8, batches=3) == 3
