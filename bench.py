@@ -472,13 +472,11 @@ def measure(wl, args, dist, device, peak: float, peak_kind: str, cpu_seconds: fl
     vis = [v.strip() for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
     sampler = ClockSampler(vis[local] if local < len(vis) else local)
 
+    # The variant steps below differ from the default step in one phase only: the other phase
+    # is the same whole-phase call (moe_dispatch / moe_combine).
     def step_partial():
         ep.layout_step(idx)
-        if fp8:
-            quant_dispatch_send()
-        else:
-            ep.dispatch_send(x)
-        ep.dispatch_recv()
+        ep.dispatch(x)
         ep.expert_identity()
         ep.combine_partial(w)
 
@@ -490,8 +488,7 @@ def measure(wl, args, dist, device, peak: float, peak_kind: str, cpu_seconds: fl
         else:
             ep.dispatch_split(x)
         ep.expert_identity()
-        ep.combine_send()
-        ep.combine_recv(w)
+        ep.combine(w)
 
     DED_K = 16   # dedicated rows per (receiver, sender)
 
@@ -503,8 +500,7 @@ def measure(wl, args, dist, device, peak: float, peak_kind: str, cpu_seconds: fl
         else:
             ep.dispatch_dedicated(x, idx, DED_K)
         ep.expert_identity()
-        ep.combine_send()
-        ep.combine_recv(w)
+        ep.combine(w)
 
     def kernel_region(step=step, cold=False):
         """Timed region: per-kernel CUDA events (the library records one pair around each of
