@@ -365,7 +365,7 @@ cudaError_t dispatch_range(const Geo& g, const moe_layout_t* lay, const void* x,
     void* snd = push ? nullptr : send;
     return fp8 ? launch_quant_dispatch_fused(g, lay, static_cast<const uint16_t*>(x), static_cast<uint8_t*>(snd),
                                              static_cast<uint8_t*>(recv), static_cast<uint8_t*>(ex), exs, c, t0, nt)
-               : launch_move_range(kMovePackAll, g, lay, x, snd, recv, t0, nt, c, ex);
+               : launch_move_range(push ? kMovePackAllPush : kMovePackAll, g, lay, x, snd, recv, t0, nt, c, ex);
   }
   if (push) {
     e = fp8 ? launch_quant_pack(g, lay->grecv, static_cast<const uint16_t*>(x), static_cast<uint8_t*>(recv), c, t0,

@@ -132,13 +132,16 @@ enum MoveKind : int {
   kMoveCopyEx = 5,    // grouped rows -> grouped rows (bf16 identity expert, distinct output)
   kMovePackPush = 6,  // direct push: token rows -> R receive rows of the owner ranks
   kMoveCPush = 7,     // direct push: grouped expert output rows -> source ranks' combine rows
-  kMovePackAll = 8,   // pack, write and shuffle in one move: token row -> its R send rows (dst; none
-                      // when dst is null, direct push), the owners' receive rows (dst2) and the
-                      // kept pairs' grouped rows (dst3), bf16
+  kMovePackAll = 8,   // pack, write and shuffle in one move: token row -> its R send rows (dst), the
+                      // owners' receive rows (dst2) and the kept pairs' grouped rows (dst3), bf16
+  kMovePackAllPush = 9,  // the same with direct push: no send rows (dst unused)
 };
 
 // Moves whose unit is a (token, column chunk) that fans out to the token's R pairs.
-constexpr bool is_pack_kind(int kind) { return kind == kMovePack || kind == kMovePackPush || kind == kMovePackAll; }
+constexpr bool is_pack_kind(int kind) {
+  return kind == kMovePack || kind == kMovePackPush || kind == kMovePackAll || kind == kMovePackAllPush;
+}
+constexpr bool is_pack_all_kind(int kind) { return kind == kMovePackAll || kind == kMovePackAllPush; }
 cudaError_t launch_move(MoveKind kind, const Geo& g, const moe_layout_t* lay, const void* src, void* dst,
                         void* dst2, Ctx& c, void* dst3 = nullptr);
 // The same move over the token range [t0, t0 + nt) of every rank only (its tokens for a

@@ -161,7 +161,7 @@ template <int KIND, bool FP8>
 __device__ __forceinline__ void issue_stores(const Geo& g, const MoveArgs& a, const Plan& pl, const uint8_t* stage,
                                              uint32_t bytes) {
   if (is_pack_kind(KIND)) {
-    if (KIND != kMovePackAll || a.dst) {   // pack-all with direct push has no send rows
+    if (KIND != kMovePackAllPush) {   // pack-all with direct push has no send rows
 #pragma unroll
       for (int k = 0; k < kPackPrefetch; ++k)
         if (pl.p[k] >= 0) bulk_s2g(a.dst + (int64_t)pl.p[k] * g.B + pl.coff, stage, bytes);
@@ -170,7 +170,7 @@ __device__ __forceinline__ void issue_stores(const Geo& g, const MoveArgs& a, co
         if (p >= 0) bulk_s2g(a.dst + (int64_t)p * g.B + pl.coff, stage, bytes);
       }
     }
-    if (KIND == kMovePackAll) {   // the receive rows, and the grouped rows of the kept pairs
+    if (is_pack_all_kind(KIND)) {   // the receive rows, and the grouped rows of the kept pairs
       for (int k = 0; k < g.R; ++k) {
         const int64_t q = pl.tok * g.R + k;
         if (__ldg(a.gsend + q) < 0) continue;
@@ -295,7 +295,7 @@ __device__ __forceinline__ void st_vec(uint8_t* p, const uint32_t& v) { *reinter
 // of 256 threads per SM): measured on GB300, bounding it to three CTAs per SM (79 registers)
 // was 1-3% slower on every workload, and finer column chunks changed nothing.
 template <int KIND, bool FP8, typename V, int MODE, bool REV>
-__global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
+__device__ __forceinline__ void move_ldg(const Geo& g, const MoveArgs& a) {
   constexpr int U = 8;
   constexpr int W = (int)sizeof(V);
   const int lane = threadIdx.x & 31;
@@ -312,12 +312,12 @@ __global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
       const int64_t tok = range_item<MODE>(g, a, tv, 1);
       const int64_t coff = (u - tv * a.chunks) * (int64_t)a.chunk_bytes;
       const uint8_t* src = a.src + tok * g.B + coff;
-      uint8_t* dst0 = a.dst ? a.dst + coff : nullptr;
+      uint8_t* dst0 = a.dst + coff;
       const int32_t* fan = a.fan + tok * g.R;
       const int myp = lane < g.R ? __ldg(fan + lane) : -1;   // pairs 0..31 (R > 32: see below)
       // pack-all: the pair's receive row and grouped row (-1: dropped) as well
-      const int myr = (KIND == kMovePackAll && lane < g.R) ? __ldg(a.grecv + tok * g.R + lane) : -1;
-      const int myl = (KIND == kMovePackAll && lane < g.R) ? __ldg(a.gslot + tok * g.R + lane) : -1;
+      const int myr = (is_pack_all_kind(KIND) && lane < g.R) ? __ldg(a.grecv + tok * g.R + lane) : -1;
+      const int myl = (is_pack_all_kind(KIND) && lane < g.R) ? __ldg(a.gslot + tok * g.R + lane) : -1;
       // The trip count is the same for every lane: the shuffles below need the whole warp.
       for (int64_t b0 = 0; b0 < nel; b0 += 32 * U) {
         const int64_t v0 = b0 + lane;
@@ -330,18 +330,18 @@ __global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
 #pragma unroll 1
         for (int k = 0; k < g.R; ++k) {
           const int p = k < 32 ? __shfl_sync(0xffffffffu, myp, k) : __ldg(fan + k);
-          if (KIND == kMovePackAll) {
+          if (is_pack_all_kind(KIND)) {
             const int rr = k < 32 ? __shfl_sync(0xffffffffu, myr, k) : __ldg(a.grecv + tok * g.R + k);
             const int rl = k < 32 ? __shfl_sync(0xffffffffu, myl, k) : __ldg(a.gslot + tok * g.R + k);
             if (p < 0) continue;
-            uint8_t* d = a.dst ? dst0 + (int64_t)p * g.B : nullptr;   // none with direct push
+            uint8_t* d = dst0 + (int64_t)p * g.B;
             uint8_t* d2 = a.dst2 + coff + (int64_t)rr * g.B;
             uint8_t* d3 = a.dst3 + coff + (int64_t)rl * g.B;
 #pragma unroll
             for (int j = 0; j < U; ++j) {
               const int64_t v = v0 + 32 * j;
               if (v < nel) {
-                if (d) st_vec(d + v * W, r[j]);
+                if (KIND == kMovePackAll) st_vec(d + v * W, r[j]);   // no send rows with direct push
                 st_vec(d2 + v * W, r[j]);
                 if (rl >= 0) st_vec(d3 + v * W, r[j]);
               }
@@ -389,8 +389,28 @@ __global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
   pdl_trigger();
 }
 
+template <int KIND, bool FP8, typename V, int MODE, bool REV>
+__global__ void __launch_bounds__(256) k_move_ldg(Geo g, MoveArgs a) {
+  move_ldg<KIND, FP8, V, MODE, REV>(g, a);
+}
+
+// Direct-push pack-all held to two CTAs per SM: left to itself it takes 80 registers and
+// three, and then leaves the concurrent combine of the previous micro-batch no room.
+template <int KIND, bool FP8, typename V, int MODE, bool REV>
+__global__ void __launch_bounds__(256, 2) k_move_ldg_b2(Geo g, MoveArgs a) {
+  move_ldg<KIND, FP8, V, MODE, REV>(g, a);
+}
+
+template <int KIND, bool FP8, typename V, int MODE, bool REV>
+constexpr auto ldg_kernel() {
+  if constexpr (KIND == kMovePackAllPush)
+    return k_move_ldg_b2<KIND, FP8, V, MODE, REV>;
+  else
+    return k_move_ldg<KIND, FP8, V, MODE, REV>;
+}
+
 // Largest dynamic shared memory limit set so far, per TMA instantiation and device.
-std::atomic<int> g_tma_smem[9][2][3][2][64];
+std::atomic<int> g_tma_smem[10][2][3][2][64];
 
 // Stages per issuer and CTAs per SM: as many CTAs as fit with 3 stages per issuer (at
 // most 8 CTAs), then as many stages as the shared memory of each CTA holds (2..8). Each
@@ -434,7 +454,7 @@ cudaError_t run_ldg(const Geo& g, const MoveArgs& a, Ctx& c) {
   static std::atomic<int> resident{0};
   int per_sm = resident.load(std::memory_order_relaxed);
   if (per_sm == 0) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_move_ldg<KIND, FP8, V, MODE, REV>, 256, 0) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ldg_kernel<KIND, FP8, V, MODE, REV>(), 256, 0) !=
             cudaSuccess ||
         per_sm < 1)
       per_sm = 1;
@@ -444,7 +464,7 @@ cudaError_t run_ldg(const Geo& g, const MoveArgs& a, Ctx& c) {
   int64_t blocks = (a.units + 7) / 8;
   const int64_t maxb = (int64_t)c.num_sms * per_sm;
   if (blocks > maxb) blocks = maxb;
-  return launch_kernel(k_move_ldg<KIND, FP8, V, MODE, REV>, dim3((unsigned)blocks), dim3(256), 0, c, g, a);
+  return launch_kernel(ldg_kernel<KIND, FP8, V, MODE, REV>(), dim3((unsigned)blocks), dim3(256), 0, c, g, a);
 }
 
 // True when two stages per issuer fit in one CTA's shared memory.
@@ -499,8 +519,8 @@ namespace {
 
 template <int R>
 cudaError_t run_move(MoveKind kind, const Geo& g, const MoveArgs& a, Ctx& c, bool fp8, bool rowB16) {
-  if constexpr (R == 2) {   // the pack-all move is a whole-group move only
-    if (kind == kMovePackAll) return cudaErrorInvalidValue;
+  if constexpr (R == 2) {   // the pack-all moves are whole-group moves only
+    if (is_pack_all_kind(kind)) return cudaErrorInvalidValue;
   }
   switch (kind) {
     case kMovePack:
@@ -521,6 +541,9 @@ cudaError_t run_move(MoveKind kind, const Geo& g, const MoveArgs& a, Ctx& c, boo
       return run_dir<kMoveCPush, false, R>(g, a, c, true);
     case kMovePackAll:
       if constexpr (R != 2) return run_dir<kMovePackAll, false, R>(g, a, c, rowB16);
+      break;
+    case kMovePackAllPush:
+      if constexpr (R != 2) return run_dir<kMovePackAllPush, false, R>(g, a, c, rowB16);
       break;
   }
   return cudaErrorInvalidValue;
@@ -675,7 +698,8 @@ cudaError_t launch_move_range(MoveKind kind, const Geo& g, const moe_layout_t* l
   if (a.units == 0) return cudaSuccess;
   static const moe_kernel_id ids[] = {MOE_K_PACK,         MOE_K_SCATTER,         MOE_K_UNPACK,
                                       MOE_K_COMBINE_PACK, MOE_K_COMBINE_SCATTER, MOE_K_EXPERT,
-                                      MOE_K_PACK_PUSH,    MOE_K_COMBINE_PUSH,    MOE_K_DISPATCH_FUSED};
+                                      MOE_K_PACK_PUSH,    MOE_K_COMBINE_PUSH,    MOE_K_DISPATCH_FUSED,
+                                      MOE_K_DISPATCH_FUSED};
   LaunchScope ls(c, ids[kind]);
   return nt != g.T ? run_move<1>(kind, g, a, c, fp8, rowB16) : run_move<0>(kind, g, a, c, fp8, rowB16);
 }

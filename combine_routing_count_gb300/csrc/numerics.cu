@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(256) k_quant_pack(Geo g, const uint16_t* __res
       const int rl = ALL ? (k < 32 ? __shfl_sync(kFull, myl, k) : __ldg(fa.gslot + row * g.R + k)) : -1;
       if (p < 0) continue;
 #pragma unroll 1
-      for (int dsel = dst ? 0 : 1; dsel < (ALL ? 3 : 1); ++dsel) {   // send (none with direct push), receive, grouped
+      for (int dsel = (ALL && !dst) ? 1 : 0; dsel < (ALL ? 3 : 1); ++dsel) {   // send (none with direct push), receive, grouped
         if (dsel == 2 && rl < 0) break;
         uint8_t* dr = dsel == 0 ? dst + (int64_t)p * g.B
                                 : dsel == 1 ? fa.recv + (int64_t)rr * g.B : fa.ex + (int64_t)rl * g.H;
@@ -439,7 +439,7 @@ __global__ void __launch_bounds__(256) k_quant_pack16(Geo g, const uint16_t* __r
       const int rl = ALL ? (k < 32 ? __shfl_sync(kFull, myl, k) : __ldg(fa.gslot + row * g.R + k)) : -1;
       if (p < 0) continue;
 #pragma unroll 1
-      for (int dsel = dst ? 0 : 1; dsel < (ALL ? 3 : 1); ++dsel) {   // send (none with direct push), receive, grouped
+      for (int dsel = (ALL && !dst) ? 1 : 0; dsel < (ALL ? 3 : 1); ++dsel) {   // send (none with direct push), receive, grouped
         if (dsel == 2 && rl < 0) break;
         uint8_t* dr = dsel == 0 ? dst + (int64_t)p * g.B
                                 : dsel == 1 ? fa.recv + (int64_t)rr * g.B : fa.ex + (int64_t)rl * g.H;
@@ -582,12 +582,14 @@ __device__ __forceinline__ void store_bf16x8(uint16_t* p, const float (&acc)[8])
 // token x; t0, nt unused).
 constexpr int kReduceThreads = 128;
 
-// FUSED: the combine pack and write in the same pass. The rows are read from the grouped
+// FUSE 1: the combine pack and write in the same pass. The rows are read from the grouped
 // expert outputs (src = ey, at gslot) instead of the combine rows, and each is also stored to
-// its receive-order row csend[grecv] (unless csend is null: direct push) and its source's
-// combine row crecv[gsend], the rows the combine send writes; the sum is the same, value for
-// value.
-template <bool RANGED, bool FUSED>
+// its receive-order row csend[grecv] and its source's combine row crecv[gsend], the rows the
+// combine send writes; the sum is the same, value for value. FUSE 2: the same with direct
+// push, which has no receive-order rows (csend unused). A compile-time choice: a null check
+// in the store loop cost the kernel registers and, next to the concurrent dispatch of the
+// next micro-batch, 10% of the step (GB300).
+template <bool RANGED, int FUSE>
 __global__ void __launch_bounds__(kReduceThreads) k_combine_reduce(Geo g, const int32_t* __restrict__ gsend,
                                                                    const int32_t* __restrict__ gslot,
                                                                    const int32_t* __restrict__ grecv,
@@ -612,9 +614,9 @@ __global__ void __launch_bounds__(kReduceThreads) k_combine_reduce(Geo g, const 
       const int gs = __ldg(gsend + q0 + k0 + lane);
       const int gl = __ldg(gslot + q0 + k0 + lane);
       if (gs >= 0 && gl >= 0) {
-        myrow = FUSED ? gl : gs;
+        myrow = FUSE ? gl : gs;
         myw = __ldg(w + q0 + k0 + lane);
-        if (FUSED) {
+        if (FUSE) {
           mys = gs;
           myr = __ldg(grecv + q0 + k0 + lane);
         }
@@ -636,13 +638,13 @@ __global__ void __launch_bounds__(kReduceThreads) k_combine_reduce(Geo g, const 
         v[j] = make_uint4(0, 0, 0, 0);
         if (act && rk[j] >= 0) v[j] = ld_stream16(src + (int64_t)rk[j] * g.H + col * 8);
       }
-      if (FUSED) {
+      if (FUSE) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const int rs = __shfl_sync(kFull, mys, (j0 + j) & 31);
           const int rr = __shfl_sync(kFull, myr, (j0 + j) & 31);
           if (act && rk[j] >= 0) {
-            if (csend) st16(csend + (int64_t)rr * g.H + col * 8, v[j]);   // none with direct push
+            if (FUSE == 1) st16(csend + (int64_t)rr * g.H + col * 8, v[j]);
             st16(crecv + (int64_t)rs * g.H + col * 8, v[j]);
           }
         }
@@ -978,7 +980,7 @@ cudaError_t launch_combine_reduce(const Geo& g0, const moe_layout_t* lay, const 
   const int ncol = g.H / 8;
   dim3 grid((unsigned)tokens, (unsigned)((ncol + kReduceThreads - 1) / kReduceThreads));
   LaunchScope ls(c, MOE_K_COMBINE_REDUCE);
-  return launch_kernel(nt != g.T ? k_combine_reduce<true, false> : k_combine_reduce<false, false>, grid,
+  return launch_kernel(nt != g.T ? k_combine_reduce<true, 0> : k_combine_reduce<false, 0>, grid,
                        dim3(kReduceThreads), 0, c, g, gsend, gslot, (const int32_t*)nullptr, w, crecv,
                        (uint16_t*)nullptr, (uint16_t*)nullptr, out, t0, nt);
 }
@@ -992,8 +994,9 @@ cudaError_t launch_combine_fused(const Geo& g, const moe_layout_t* lay, const ui
   const int ncol = g.H / 8;
   dim3 grid((unsigned)tokens, (unsigned)((ncol + kReduceThreads - 1) / kReduceThreads));
   LaunchScope ls(c, MOE_K_COMBINE_FUSED);
-  return launch_kernel(nt != g.T ? k_combine_reduce<true, true> : k_combine_reduce<false, true>, grid,
-                       dim3(kReduceThreads), 0, c, g, (const int32_t*)lay->gsend, (const int32_t*)lay->gslot,
+  auto k = csend ? (nt != g.T ? k_combine_reduce<true, 1> : k_combine_reduce<false, 1>)
+                 : (nt != g.T ? k_combine_reduce<true, 2> : k_combine_reduce<false, 2>);
+  return launch_kernel(k, grid, dim3(kReduceThreads), 0, c, g, (const int32_t*)lay->gsend, (const int32_t*)lay->gslot,
                        (const int32_t*)lay->grecv, w, ey, csend, crecv, out, t0, nt);
 }
 
