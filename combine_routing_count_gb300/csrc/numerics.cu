@@ -588,7 +588,10 @@ constexpr int kReduceThreads = 128;
 // combine send writes; the sum is the same, value for value. FUSE 2: the same with direct
 // push, which has no receive-order rows (csend unused). A compile-time choice: a null check
 // in the store loop cost the kernel registers and, next to the concurrent dispatch of the
-// next micro-batch, 10% of the step (GB300).
+// next micro-batch, 10% of the step (GB300). The fused kernels read the expert outputs and
+// write the two copies for the last time in the pass, so both go through L2 marked evict-first:
+// the next micro-batch's dispatch, running beside them, keeps its rows in L2 (measured on
+// GB300: micro-batched steps 1.3-5.5% faster for bf16, 9% for fp8 with the expert).
 template <bool RANGED, int FUSE>
 __global__ void __launch_bounds__(kReduceThreads) k_combine_reduce(Geo g, const int32_t* __restrict__ gsend,
                                                                    const int32_t* __restrict__ gslot,
@@ -606,6 +609,7 @@ __global__ void __launch_bounds__(kReduceThreads) k_combine_reduce(Geo g, const 
   const int64_t q0 = u * g.R;
   float acc[8];
   acc_zero(acc);
+  const uint64_t pol = FUSE ? l2_evict_first_policy() : 0;
   pdl_wait();
   for (int k0 = 0; k0 < g.R; k0 += 32) {
     int myrow = -1, mys = -1, myr = -1;
@@ -636,7 +640,10 @@ __global__ void __launch_bounds__(kReduceThreads) k_combine_reduce(Geo g, const 
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         v[j] = make_uint4(0, 0, 0, 0);
-        if (act && rk[j] >= 0) v[j] = ld_stream16(src + (int64_t)rk[j] * g.H + col * 8);
+        if (act && rk[j] >= 0) {
+          const uint16_t* p = src + (int64_t)rk[j] * g.H + col * 8;
+          v[j] = FUSE ? ld_stream16_hint(p, pol) : ld_stream16(p);
+        }
       }
       if (FUSE) {
 #pragma unroll
@@ -644,8 +651,8 @@ __global__ void __launch_bounds__(kReduceThreads) k_combine_reduce(Geo g, const 
           const int rs = __shfl_sync(kFull, mys, (j0 + j) & 31);
           const int rr = __shfl_sync(kFull, myr, (j0 + j) & 31);
           if (act && rk[j] >= 0) {
-            if (FUSE == 1) st16(csend + (int64_t)rr * g.H + col * 8, v[j]);
-            st16(crecv + (int64_t)rs * g.H + col * 8, v[j]);
+            if (FUSE == 1) st16_hint(csend + (int64_t)rr * g.H + col * 8, v[j], pol);
+            st16_hint(crecv + (int64_t)rs * g.H + col * 8, v[j], pol);
           }
         }
       }
