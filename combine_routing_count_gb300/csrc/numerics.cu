@@ -447,8 +447,11 @@ __global__ void __launch_bounds__(256) k_quant_pack16(Geo g, const uint16_t* __r
         for (int j = 0; j < kQ16Blocks; ++j) {
           const int b = bbase + 4 * j;
           if (b < nb) {
-            *reinterpret_cast<uint4*>(dr + b * 128 + sub * 16) = make_uint4(codes[j][0], codes[j][1], codes[j][2],
-                                                                            codes[j][3]);
+            const uint4 cw = make_uint4(codes[j][0], codes[j][1], codes[j][2], codes[j][3]);
+            if (ALL && !dst && dsel == 1)   // direct push: no kernel of the pass reads the receive rows
+              st16_hint(dr + b * 128 + sub * 16, cw, l2_evict_first_policy());
+            else
+              *reinterpret_cast<uint4*>(dr + b * 128 + sub * 16) = cw;
             if (sub == 0) {
               float* sp = dsel < 2 ? reinterpret_cast<float*>(dr + g.H + 4 * b) : fa.exs + (int64_t)rl * nb + b;
               *sp = scale[j];
