@@ -315,12 +315,12 @@ __device__ __forceinline__ void move_ldg(const Geo& g, const MoveArgs& a) {
       uint8_t* dst0 = a.dst + coff;
       const int32_t* fan = a.fan + tok * g.R;
       const int myp = lane < g.R ? __ldg(fan + lane) : -1;   // pairs 0..31 (R > 32: see below)
-      // pack-all: the pair's receive row and grouped row (-1: dropped) as well. With direct
-      // push no later kernel of the pass reads the receive rows (the combine writes the
-      // sources' rows straight from the grouped rows), so they go through L2 marked
-      // evict-first, which keeps the grouped rows and the next micro-batch's rows there
-      // (GB300: direct-push steps 9-11% faster on the bf16 workloads).
-      const uint64_t pol = KIND == kMovePackAllPush ? l2_evict_first_policy() : 0;
+      // pack-all: the pair's receive row and grouped row (-1: dropped) as well. No later
+      // kernel of the pass reads the receive rows (the combine gathers from the grouped
+      // rows), so they go through L2 marked evict-first, which keeps the grouped rows and the
+      // next micro-batch's rows there. Measured on GB300: direct-push steps 9-11% faster on
+      // the bf16 workloads, default steps 1-4% (the send rows instead: the same; both: less).
+      const uint64_t pol = is_pack_all_kind(KIND) ? l2_evict_first_policy() : 0;
       const int myr = (is_pack_all_kind(KIND) && lane < g.R) ? __ldg(a.grecv + tok * g.R + lane) : -1;
       const int myl = (is_pack_all_kind(KIND) && lane < g.R) ? __ldg(a.gslot + tok * g.R + lane) : -1;
       // The trip count is the same for every lane: the shuffles below need the whole warp.
@@ -347,7 +347,7 @@ __device__ __forceinline__ void move_ldg(const Geo& g, const MoveArgs& a) {
               const int64_t v = v0 + 32 * j;
               if (v < nel) {
                 if (KIND == kMovePackAll) st_vec(d + v * W, r[j]);   // no send rows with direct push
-                if constexpr (KIND == kMovePackAllPush && sizeof(V) == 16)
+                if constexpr (sizeof(V) == 16)
                   st16_hint(d2 + v * W, r[j], pol);   // receive rows: nothing in the pass reads them
                 else
                   st_vec(d2 + v * W, r[j]);
