@@ -229,9 +229,12 @@ __global__ void __launch_bounds__(256) k_quant_fp8(Geo g, const uint16_t* __rest
 // when pushing), so the fp8 rows are never staged in HBM. The bytes each row gets are those
 // moe_quantize_fp8_b128 writes. W8: rows are 8-byte aligned (8-byte code stores).
 // RANGED: only the token range [t0, t0 + nt) of every rank (else every token; t0, nt unused).
-// ALL: the write and the shuffle as well (pack-all): every pair's codes and scales also go to
+// ALL 1: the write and the shuffle as well (pack-all): every pair's codes and scales also go to
 // its receive row (recv at grecv) and, when the pair is kept, to its grouped row (codes at
 // ex + gslot * H, scales at exs + gslot * H / 128), the bytes moe_dispatch_recv writes.
+// ALL 2: the same with direct push: no send rows (dst unused), and the receive rows, which no
+// later kernel of the pass reads, go through L2 marked evict-first. A compile-time choice, as
+// a run-time test of dst measured 20% more instructions in the default kernel.
 struct FanAll {
   const int32_t* grecv;
   const int32_t* gslot;
@@ -240,7 +243,7 @@ struct FanAll {
   float* exs;
 };
 
-template <bool W8, bool RANGED, bool ALL>
+template <bool W8, bool RANGED, int ALL>
 __global__ void __launch_bounds__(256) k_quant_pack(Geo g, const uint16_t* __restrict__ x,
                                                     const int32_t* __restrict__ fan, uint8_t* __restrict__ dst,
                                                     int t0, int nt, FanAll fa) {
@@ -270,7 +273,7 @@ __global__ void __launch_bounds__(256) k_quant_pack(Geo g, const uint16_t* __res
       const int rl = ALL ? (k < 32 ? __shfl_sync(kFull, myl, k) : __ldg(fa.gslot + row * g.R + k)) : -1;
       if (p < 0) continue;
 #pragma unroll 1
-      for (int dsel = (ALL && !dst) ? 1 : 0; dsel < (ALL ? 3 : 1); ++dsel) {   // send (none with direct push), receive, grouped
+      for (int dsel = ALL == 2 ? 1 : 0; dsel < (ALL ? 3 : 1); ++dsel) {   // send (none with direct push), receive, grouped
         if (dsel == 2 && rl < 0) break;
         uint8_t* dr = dsel == 0 ? dst + (int64_t)p * g.B
                                 : dsel == 1 ? fa.recv + (int64_t)rr * g.B : fa.ex + (int64_t)rl * g.H;
@@ -409,7 +412,7 @@ __global__ void __launch_bounds__(256) k_quant_fp8_16(Geo g, const uint16_t* __r
   pdl_trigger();
 }
 
-template <bool RANGED, bool ALL>
+template <bool RANGED, int ALL>
 __global__ void __launch_bounds__(256) k_quant_pack16(Geo g, const uint16_t* __restrict__ x,
                                                       const int32_t* __restrict__ fan, uint8_t* __restrict__ dst,
                                                       int t0, int nt, FanAll fa) {
@@ -439,7 +442,7 @@ __global__ void __launch_bounds__(256) k_quant_pack16(Geo g, const uint16_t* __r
       const int rl = ALL ? (k < 32 ? __shfl_sync(kFull, myl, k) : __ldg(fa.gslot + row * g.R + k)) : -1;
       if (p < 0) continue;
 #pragma unroll 1
-      for (int dsel = (ALL && !dst) ? 1 : 0; dsel < (ALL ? 3 : 1); ++dsel) {   // send (none with direct push), receive, grouped
+      for (int dsel = ALL == 2 ? 1 : 0; dsel < (ALL ? 3 : 1); ++dsel) {   // send (none with direct push), receive, grouped
         if (dsel == 2 && rl < 0) break;
         uint8_t* dr = dsel == 0 ? dst + (int64_t)p * g.B
                                 : dsel == 1 ? fa.recv + (int64_t)rr * g.B : fa.ex + (int64_t)rl * g.H;
@@ -448,7 +451,7 @@ __global__ void __launch_bounds__(256) k_quant_pack16(Geo g, const uint16_t* __r
           const int b = bbase + 4 * j;
           if (b < nb) {
             const uint4 cw = make_uint4(codes[j][0], codes[j][1], codes[j][2], codes[j][3]);
-            if (ALL && !dst && dsel == 1)   // direct push: no kernel of the pass reads the receive rows
+            if (ALL == 2 && dsel == 1)   // direct push: no kernel of the pass reads the receive rows
               st16_hint(dr + b * 128 + sub * 16, cw, l2_evict_first_policy());
             else
               *reinterpret_cast<uint4*>(dr + b * 128 + sub * 16) = cw;
@@ -893,7 +896,7 @@ cudaError_t launch_quant_fp8(const Geo& g0, const uint16_t* x, uint8_t* xq, Ctx&
   return launch_kernel(k_quant_fp8, dim3((unsigned)blocks), dim3(256), 0, c, g, x, xq);
 }
 
-template <bool ALL>
+template <int ALL>
 cudaError_t run_quant_pack(const Geo& g, const uint16_t* x, const int32_t* fan, uint8_t* dst, Ctx& c, int t0, int nt,
                            const FanAll& fa, int64_t blocks) {
   const bool ranged = nt != g.T;
@@ -925,7 +928,7 @@ cudaError_t launch_quant_pack(const Geo& g0, const int32_t* fan, const uint16_t*
   const int64_t maxb = (int64_t)c.num_sms * 8;
   if (blocks > maxb) blocks = maxb;
   LaunchScope ls(c, MOE_K_QUANT_PACK);
-  return run_quant_pack<false>(g, x, fan, dst, c, t0, nt, FanAll{}, blocks);
+  return run_quant_pack<0>(g, x, fan, dst, c, t0, nt, FanAll{}, blocks);
 }
 
 cudaError_t launch_quant_dispatch_fused(const Geo& g, const moe_layout_t* lay, const uint16_t* x, uint8_t* send,
@@ -939,8 +942,9 @@ cudaError_t launch_quant_dispatch_fused(const Geo& g, const moe_layout_t* lay, c
   const int64_t maxb = (int64_t)c.num_sms * 8;
   if (blocks > maxb) blocks = maxb;
   LaunchScope ls(c, MOE_K_QUANT_DISPATCH_FUSED);
-  return run_quant_pack<true>(g, x, lay->gsend, send, c, t0, nt, FanAll{lay->grecv, lay->gslot, recv, ex, exs},
-                              blocks);
+  const FanAll fa{lay->grecv, lay->gslot, recv, ex, exs};
+  return send ? run_quant_pack<1>(g, x, lay->gsend, send, c, t0, nt, fa, blocks)
+              : run_quant_pack<2>(g, x, lay->gsend, send, c, t0, nt, fa, blocks);
 }
 
 cudaError_t launch_dequant_fp8(const Geo& g, const moe_layout_t* lay, const uint8_t* exq, const float* exs,
