@@ -445,17 +445,17 @@ int batch_start(int T, int nb, int j, bool shaped) {
 }
 
 // Micro-batches of moe_forward: the caller's choice (at most 32 and T), else, for bf16 rows,
-// about one per 32 MB of dispatch and combine rows (pairs x (B + 2H) bytes; at most 24 and
+// about one per 55 MB of dispatch and combine rows (pairs x (B + 2H) bytes; at most 20 and
 // T), and one per 60 MB (at most 16) for fp8 rows, with direct push or with
 // MOE_FLAG_SEPARATE_MOVES; one with MOE_FLAG_ONE_BATCH or staged fp8 quantisation. Measured
 // on GB300 with batches alternating over two equal-priority streams, each the best of the
-// counts tried. One kernel per phase: 8 batches of 235 MB of rows (EP8, 10% faster than
-// one), 24 of 940 MB and 1074 MB (EP32 9% and EP16 6% faster than 8; 32 no better): while a
-// batch's rows stay in L2, its combine rewrites the send and receive rows its dispatch wrote
-// before they reach DRAM (the combine buffers may alias them). With direct push, which writes
-// neither, 4 of 235 MB and 16 of 940 MB and 1074 MB (EP8 10%, EP32 6%, EP16 5% faster than 8,
-// 24 and 24). fp8, whose identity expert writes a bf16 row per pair inside the chain: 6 of
-// 356 MB (10% faster than one; 12 no faster than one). Separate kernels: 4
+// counts tried. One kernel per phase with its L2 policies: 4 batches of 235 MB of rows (EP8,
+// 4% faster than 8), 20 of 940 MB and 1074 MB (EP32 and EP16 1.5-2% faster than 16 and 24,
+// 7% faster than 12 and 32): while a batch's rows stay in L2, its combine reads the grouped
+// rows the dispatch wrote, and rewrites its send and receive rows, before they reach DRAM (the
+// combine buffers may alias them). With direct push 4 of 235 MB and 16 of 940 MB and 1074 MB
+// (3-7% faster than 12 and 20). fp8, whose identity expert writes a bf16 row per pair inside
+// the chain: 6 of 356 MB (10% faster than one; 12 no faster than one). Separate kernels: 4
 // batches of 235 MB (EP8, 18% faster than one), 6 of 356 MB (fp8 EP64, expert included,
 // 16%), 16 of 940 MB and 1074 MB (EP32 28%, EP16 24%). Under ~35 MB one batch is fastest.
 // Even counts keep both streams equally loaded (EP8: 3 and 5 batches lose to 4 and 6), so an
@@ -467,7 +467,7 @@ int forward_batch_count(const Geo& g, const moe_layout_t* lay) {
   if (nb <= 0) {
     const bool fine = !(lay->flags & (MOE_FLAG_SEPARATE_MOVES | MOE_FLAG_DIRECT_PUSH)) &&
                       g.payload != MOE_PAYLOAD_FP8_E4M3_B128;
-    nb = (int)std::min(fine ? 24L : 16L, std::lround((double)g.P * (g.B + 2.0 * g.H) / (fine ? 32e6 : 60e6)));
+    nb = (int)std::min(fine ? 20L : 16L, std::lround((double)g.P * (g.B + 2.0 * g.H) / (fine ? 55e6 : 60e6)));
     if (nb >= 3 && (nb & 1)) ++nb;   // even: both streams end together
   }
   if (nb > kMaxMicroBatches) nb = kMaxMicroBatches;

@@ -460,9 +460,9 @@ moe_status moe_combine_recv_partial(const moe_dims *dims, const moe_layout_t *la
  * MOE_FLAG_SEPARATE_MOVES; staged fp8 quantisation runs those calls). Returns the first
  * error. bufs->x, idx, w and out may also be device-accessible host memory.
  * After the layout, the pass runs as nb micro-batches (nb = moe_batches(dims, lay, 0):
- * lay->batches (at most 32 and T), or automatically about one per 32 MB of dispatch and
+ * lay->batches (at most 32 and T), or automatically about one per 55 MB of dispatch and
  * combine rows (N*T*R pairs x (row bytes + 2H)), rounded up to an even count from 3, at most
- * 24 and T (fp8 rows, MOE_FLAG_DIRECT_PUSH or MOE_FLAG_SEPARATE_MOVES: one per 60 MB, at
+ * 20 and T (fp8 rows, MOE_FLAG_DIRECT_PUSH or MOE_FLAG_SEPARATE_MOVES: one per 60 MB, at
  * most 16);
  * one with MOE_FLAG_ONE_BATCH or staged fp8 quantisation). Micro-batch j covers tokens
  * [j*T/nb, (j+1)*T/nb) of every rank and runs the dispatch, the identity expert and the

@@ -130,8 +130,8 @@ def test_host_batch_count_rule(L):
 
 
 def test_forward_micro_batch_count_rule(L):
-    """moe_forward's micro-batches: about one per 32 MB of dispatch and combine rows for bf16
-    (at most 24 and T), one per 60 MB for fp8, direct push or separate kernels (at most 16), the
+    """moe_forward's micro-batches: about one per 55 MB of dispatch and combine rows for bf16
+    (at most 20 and T), one per 60 MB for fp8, direct push or separate kernels (at most 16), the
     caller's count when set (at most 32 and T), one for the one-batch flag and for the staged
     fp8 quantiser. Host only."""
     from combine_routing_count_gb300 import MoeLayout
@@ -139,13 +139,14 @@ def test_forward_micro_batch_count_rule(L):
         lay = MoeLayout()
         lay.flags, lay.batches = flags, batches
         return L.moe_batches(ctypes.byref(_dims(N, T, H, E, R, 0, payload)), ctypes.byref(lay), 0)
-    assert nb(8, 128, 7168, 256, 8) == 8         # 235 MB of rows: 7, rounded up to an even count
+    assert nb(8, 128, 7168, 256, 8) == 4         # 235 MB of rows
     assert nb(64, 32, 7168, 384, 8, 1) == 6      # 356 MB (fp8 rows of 7392 B): one per 60 MB
-    assert nb(32, 128, 7168, 384, 8) == 24       # 940 MB: capped
-    assert nb(16, 512, 4096, 128, 8) == 24       # 1074 MB: capped
+    assert nb(32, 128, 7168, 384, 8) == 18       # 940 MB: 17, rounded up to an even count
+    assert nb(16, 512, 4096, 128, 8) == 20       # 1074 MB: 20
+    assert nb(16, 1024, 4096, 128, 8) == 20      # 2147 MB: capped
     assert nb(2, 16, 128, 8, 2) == 1             # 32 tokens
-    assert nb(8, 32, 7168, 256, 8) == 2          # 59 MB
-    assert nb(8, 64, 7168, 256, 8) == 4          # 117 MB
+    assert nb(8, 32, 7168, 256, 8) == 1          # 59 MB
+    assert nb(8, 64, 7168, 256, 8) == 2          # 117 MB
     assert nb(8, 128, 7168, 256, 8, flags=0x80) == 4    # separate kernels: one per 60 MB
     assert nb(16, 512, 4096, 128, 8, flags=0x8) == 16   # direct push: one per 60 MB, capped at 16
     assert nb(32, 128, 7168, 384, 8, flags=0x80) == 16  # capped at 16
