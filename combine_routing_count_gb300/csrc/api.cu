@@ -48,7 +48,7 @@ cudaError_t launch_l2_flush(const moe_prof_t* prof, cudaStream_t stream) {
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kMaxHostBatches = 16;
+constexpr int kMaxHostBatches = 24;
 constexpr int kMaxMicroBatches = 32;
 constexpr int64_t kMaxE = 1536;
 constexpr int64_t kMaxN = 2048;           // ranks: the scan CTAs stage up to 64*33 per-rank values
@@ -418,17 +418,17 @@ cudaError_t batch_chain(const Geo& g, const moe_layout_t* lay, const moe_buffers
   return e;
 }
 
-// Token batches of the copy-engine pipeline: the caller's choice, else about 1.4 times the
+// Token batches of the copy-engine pipeline: the caller's choice, else about twice the
 // square root of the token rows' MB. The first copy in and the last copy out are what no
 // device work hides (X / nb each, X the token bytes), while every batch adds its launches'
 // ramp and tail (about c); X / nb + c * nb is least at nb = sqrt(X / c). The factor fitted
-// the measured optimum with batches alternating over two streams on GB300 (5 batches at
-// 14.7 MB, 7-8 at 29 MB, 11 at 59 MB; 16 measured best at 67 MB, 11 gives 6% less).
+// the measured optimum with batches alternating over two streams on GB300 and one kernel per
+// phase (7 batches at 14.7 MB, 16 at 59 and 67 MB, 3.6-4.2% faster than 11).
 int host_batch_count(const Geo& g, const moe_layout_t* lay) {
   if (lay->flags & MOE_FLAG_ONE_BATCH) return 1;
   if (g.payload == MOE_PAYLOAD_FP8_E4M3_B128 && (lay->flags & MOE_FLAG_STAGED_QUANT)) return 1;
   int nb = lay->batches;
-  if (nb <= 0) nb = (int)std::lround(1.4 * std::sqrt((double)g.N * g.T * g.H * 2 / 1e6));
+  if (nb <= 0) nb = (int)std::lround(2.0 * std::sqrt((double)g.N * g.T * g.H * 2 / 1e6));
   if (nb > kMaxHostBatches) nb = kMaxHostBatches;
   if (nb > g.T) nb = (int)g.T;
   return nb < 1 ? 1 : nb;

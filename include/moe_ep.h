@@ -189,7 +189,7 @@ typedef struct {
  *   ctas_per_sm (0 = automatic, else mover CTAs per SM), batches (token batches of
  *   moe_forward's micro-batches, of moe_dispatch / moe_combine and of moe_dispatch_split
  *   (0 = automatic, else 1..32) and of moe_forward_host's copy-engine pipeline (0 =
- *   automatic, else 1..16); see moe_batches), win_lo / win_hi (the rank window, below).
+ *   automatic, else 1..24); see moe_batches), win_lo / win_hi (the rank window, below).
  *
  * Rank window (expert parallelism over several GPUs, one process each; section "Send and
  * receive buffers": every rank knows where its writes go and where it receives from each
@@ -479,7 +479,7 @@ moe_status moe_forward(const moe_dims *dims, const moe_layout_t *lay, const moe_
 /* moe_forward with host inputs h_x [N][T][H] bf16, h_idx [N][T][R], h_w [N][T][R] and host
  * output h_out [N][T][H] (pinned for the copies to be asynchronous; pageable works too).
  * Default: a pipeline over nb token batches (tokens [j*T/nb, (j+1)*T/nb) of every rank;
- * nb = lay->batches, or automatically about 1.4 sqrt(token-row MB), at most 16 and T).
+ * nb = lay->batches, or automatically about 2 sqrt(token-row MB), at most 24 and T).
  * A copy-engine stream of the library copies h_idx and h_w into bufs->idx/w, then each
  * batch's token rows into bufs->x; the caller's stream runs the layout as soon as idx is
  * there, then each batch's dispatch, identity expert and combine once its rows are there;

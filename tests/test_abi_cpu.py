@@ -106,22 +106,23 @@ def test_library_exports_only_the_abi(L):
 
 
 def test_host_batch_count_rule(L):
-    """The copy-engine pipeline's token batches: about 1.4 sqrt(token-row MB) by default, the
-    caller's count when set (capped at 16 and at T), one for the one-batch flag and for the
+    """The copy-engine pipeline's token batches: about 2 sqrt(token-row MB) by default, the
+    caller's count when set (capped at 24 and at T), one for the one-batch flag and for the
     staged fp8 quantiser; 0 for bad dims. Host only."""
     from combine_routing_count_gb300 import MoeLayout
     def nb(N, T, H, E, R, payload=0, flags=0, batches=0, host=1):
         lay = MoeLayout()
         lay.flags, lay.batches = flags, batches
         return L.moe_batches(ctypes.byref(_dims(N, T, H, E, R, 0, payload)), ctypes.byref(lay), host)
-    assert nb(8, 128, 7168, 256, 8) == 5        # 14.7 MB of token rows
-    assert nb(32, 128, 7168, 384, 8) == 11      # 58.7 MB
-    assert nb(16, 512, 4096, 128, 8) == 11      # 67.1 MB
-    assert nb(64, 32, 7168, 384, 8, 1) == 8     # 29.4 MB (fp8 payload, bf16 tokens)
+    assert nb(8, 128, 7168, 256, 8) == 8        # 14.7 MB of token rows
+    assert nb(32, 128, 7168, 384, 8) == 15      # 58.7 MB
+    assert nb(16, 512, 4096, 128, 8) == 16      # 67.1 MB
+    assert nb(64, 32, 7168, 384, 8, 1) == 11    # 29.4 MB (fp8 payload, bf16 tokens)
+    assert nb(64, 256, 7168, 384, 8) == 24      # 235 MB: capped
     assert nb(2, 16, 128, 8, 2) == 1            # 8 KB: no pipeline
     assert nb(8, 128, 7168, 256, 8, batches=7) == 7
     assert nb(8, 3, 7168, 256, 8, batches=16) == 3
-    assert nb(8, 128, 7168, 256, 8, batches=40) == 16
+    assert nb(8, 128, 7168, 256, 8, batches=40) == 24
     assert nb(8, 128, 7168, 256, 8, flags=0x40) == 1
     assert nb(64, 32, 7168, 384, 8, 1, flags=0x10) == 1
     assert nb(8, 0, 7168, 256, 8) == 1
