@@ -531,6 +531,20 @@ LIMIT_CASES = [
 ]
 
 
+@pytest.mark.parametrize("mode", ["forward", "phases"])
+@pytest.mark.parametrize("flags", [0, 8], ids=["auto", "push"])
+@pytest.mark.parametrize("wl", LIMIT_CASES + [W("fp8-R36", 4, 12, 512, 64, 36, "fp8", "uniform", 184)],
+                         ids=lambda w: w.name)
+def test_limits_one_kernel_phases_match_oracle(orc, wl, flags, mode):
+    """The one-kernel dispatch and combine (and their direct-push instances) at the limits: the
+    largest E, 1536 ranks, R > 32 (pair rows held past one warp's lanes, bf16 and fp8): every
+    buffer bit for bit as the oracle's."""
+    inp = workloads.make_inputs(wl)
+    _, res = run_gpu(wl, inp, flags=flags, forward=(mode == "forward"), phases=(mode == "phases"))
+    assert res["status_code"] == 0
+    compare_all(orc, wl, inp, res, push=bool(flags & 8), fused_quant=True)
+
+
 @pytest.mark.parametrize("flags", [0, 8], ids=["auto", "push"])
 @pytest.mark.parametrize("wl", LIMIT_CASES, ids=lambda w: w.name)
 def test_limits_match_oracle(orc, wl, flags):
