@@ -4,7 +4,10 @@
 A step is one whole pass of the path over one batch of N simulated ranks' tokens:
 routing layout (histogram, scans, placements) -> dispatch send (pack + per-peer write) ->
 dispatch recv (grouped expert rows) -> identity expert -> combine send (reverse shuffle +
-per-peer write back) -> combine recv (fp32 weighted sum -> bf16). The bf16 step is one
+per-peer write back) -> combine recv (fp32 weighted sum -> bf16). The library runs each
+phase as one kernel per token batch (dispatch: pack, write and shuffle; combine: reverse
+shuffle, write back and sum), every buffer as the separate steps leave it; the same step
+with the separate kernels is reported beside it (`separate_moves`). The bf16 step is one
 moe_forward call, which runs the pass in the library's token micro-batches; the fp8 step
 calls the layout, moe_dispatch, the identity expert and moe_combine (in token batches) so
 that the expert can be timed apart and left out. The same step in one batch is reported
@@ -15,7 +18,7 @@ each kernel).
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl reference]
 
 With no --config the JSON line's top level is the largest workload (EP16, T=512, H=4096,
-every token routed to rank 0's experts: 5.5 GB of algorithmic bytes per step) and
+every token routed to rank 0's experts: 3.4 GB of algorithmic bytes per step) and
 `per_config` carries the other three full-size workloads measured the same way in the same
 run (EP8 bf16, EP32 zipf bf16, EP64 fp8), each checked against the CPU oracle; --config C
 measures workload C alone.
