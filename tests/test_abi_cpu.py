@@ -31,6 +31,22 @@ def test_every_declared_symbol_is_exported(L):
     assert set(names) == set(_abi.EXPORTED)
 
 
+def test_binding_constants_match_the_header():
+    """The binding's kernel names follow the header's moe_kernel_id order, and its flag values
+    are the header's."""
+    from combine_routing_count_gb300 import _abi
+    src = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "moe_ep.h")).read(), flags=re.S)
+    ids = {m.group(1): int(m.group(2)) for m in re.finditer(r"\bMOE_K_([A-Z0-9_]+)\s*=\s*(\d+)", src)}
+    num = ids.pop("NUM")
+    assert sorted(ids.values()) == list(range(num)) and len(_abi.KERNEL_NAMES) == num
+    for name, i in ids.items():
+        assert _abi.KERNEL_NAMES[i] == name.lower(), (name, i)
+    flags = {m.group(1): int(m.group(2), 16) for m in re.finditer(r"#define\s+(MOE_FLAG_[A-Z_]+)\s+0x([0-9a-fA-F]+)u", src)}
+    assert len(flags) >= 8
+    for name, v in flags.items():
+        assert getattr(_abi, name) == v, name
+
+
 def _dims(N=8, T=128, H=7168, E=256, R=8, cap=0, payload=0):
     from combine_routing_count_gb300 import MoeDims
     return MoeDims(N, T, H, E, R, cap, payload)
