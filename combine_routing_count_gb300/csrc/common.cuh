@@ -150,6 +150,13 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   return pol;
 }
 
+// The opposite: lines to be kept over others, for data a later kernel of the pass reads.
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 // ld_stream16 and st16 under an L2 access policy.
 __device__ __forceinline__ uint4 ld_stream16_hint(const void* p, uint64_t pol) {
   uint4 v;

@@ -321,6 +321,10 @@ __device__ __forceinline__ void move_ldg(const Geo& g, const MoveArgs& a) {
       // next micro-batch's rows there. Measured on GB300: direct-push steps 9-11% faster on
       // the bf16 workloads, default steps 1-4% (the send rows instead: the same; both: less).
       const uint64_t pol = is_pack_all_kind(KIND) ? l2_evict_first_policy() : 0;
+      // Without direct push the grouped rows, which the combine of the same micro-batch reads,
+      // are kept over other lines (1-1.5% faster default steps on GB300; with direct push,
+      // where the combine runs from them alone, 2% slower, so not there).
+      const uint64_t keep = KIND == kMovePackAll ? l2_evict_last_policy() : 0;
       const int myr = (is_pack_all_kind(KIND) && lane < g.R) ? __ldg(a.grecv + tok * g.R + lane) : -1;
       const int myl = (is_pack_all_kind(KIND) && lane < g.R) ? __ldg(a.gslot + tok * g.R + lane) : -1;
       // The trip count is the same for every lane: the shuffles below need the whole warp.
@@ -351,7 +355,11 @@ __device__ __forceinline__ void move_ldg(const Geo& g, const MoveArgs& a) {
                   st16_hint(d2 + v * W, r[j], pol);   // receive rows: nothing in the pass reads them
                 else
                   st_vec(d2 + v * W, r[j]);
-                if (rl >= 0) st_vec(d3 + v * W, r[j]);
+                if constexpr (KIND == kMovePackAll && sizeof(V) == 16) {
+                  if (rl >= 0) st16_hint(d3 + v * W, r[j], keep);
+                } else if (rl >= 0) {
+                  st_vec(d3 + v * W, r[j]);
+                }
               }
             }
             continue;
