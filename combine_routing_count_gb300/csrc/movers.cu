@@ -312,7 +312,7 @@ __device__ __forceinline__ void move_ldg(const Geo& g, const MoveArgs& a) {
       const int64_t tok = range_item<MODE>(g, a, tv, 1);
       const int64_t coff = (u - tv * a.chunks) * (int64_t)a.chunk_bytes;
       const uint8_t* src = a.src + tok * g.B + coff;
-      uint8_t* dst0 = a.dst + coff;
+      uint8_t* dst0 = KIND == kMovePackAllPush ? nullptr : a.dst + coff;
       const int32_t* fan = a.fan + tok * g.R;
       const int myp = lane < g.R ? __ldg(fan + lane) : -1;   // pairs 0..31 (R > 32: see below)
       // pack-all: the pair's receive row and grouped row (-1: dropped) as well. No later
@@ -343,7 +343,7 @@ __device__ __forceinline__ void move_ldg(const Geo& g, const MoveArgs& a) {
             const int rr = k < 32 ? __shfl_sync(0xffffffffu, myr, k) : __ldg(a.grecv + tok * g.R + k);
             const int rl = k < 32 ? __shfl_sync(0xffffffffu, myl, k) : __ldg(a.gslot + tok * g.R + k);
             if (p < 0) continue;
-            uint8_t* d = dst0 + (int64_t)p * g.B;
+            uint8_t* d = KIND == kMovePackAll ? dst0 + (int64_t)p * g.B : nullptr;   // no send rows with push
             uint8_t* d2 = a.dst2 + coff + (int64_t)rr * g.B;
             uint8_t* d3 = a.dst3 + coff + (int64_t)rl * g.B;
 #pragma unroll
