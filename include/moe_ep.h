@@ -345,7 +345,7 @@ moe_status moe_dispatch_send_noalloc(const moe_dims *dims, const moe_layout_t *l
  * moe_dispatch_recv: d_recv [N][RB][B] holds every receive row, d_expert_x / d_expert_scale
  * the grouped rows (same layouts as moe_dispatch_recv).
  * One cooperative launch over nb token batches (tokens [j*T/nb, (j+1)*T/nb) of every rank;
- * nb = lay->batches if set, else about one per 16 MB of pushed rows; at most 32 and T).
+ * nb = lay->batches if set, else about one per 32 MB of pushed rows; at most 32 and T).
  * Sender warps push each batch's
  * token rows into the owners' receive rows and, once their rows of the batch have landed,
  * signal the batch on a counter per (batch, source rank); receiver warps take the batch's
