@@ -150,8 +150,9 @@ typedef struct {
  * rows, the owners' receive rows and the grouped rows; combine reads each kept pair's expert
  * output row once, stores it to its receive-order row and its source's combine row, and sums
  * the token's rows into its output. Every buffer ends up as with the separate calls, byte for
- * byte, and so does the output. This flag runs the phases as the separate calls do instead
- * (pack, write, shuffle; combine pack, write, sum). Direct push is unaffected. */
+ * byte, and so does the output. With MOE_FLAG_DIRECT_PUSH the same two kernels write no send
+ * rows and no receive-order rows, as the direct-push calls do not. This flag runs the phases as
+ * the separate calls do instead (pack, write, shuffle; combine pack, write, sum). */
 #define MOE_FLAG_SEPARATE_MOVES 0x80u
 #define MOE_FLAG_NO_PDL 0x2u    /* launch without programmatic dependent launch (by default
                                    each kernel may be scheduled while its predecessor in the
@@ -423,7 +424,8 @@ moe_status moe_combine_recv(const moe_dims *dims, const moe_layout_t *lay, const
  * holds the bf16 token rows, always quantised inside the pack as moe_quantize_dispatch_send
  * does, so MOE_FLAG_STAGED_QUANT does not apply; d_send unused with MOE_FLAG_DIRECT_PUSH);
  * moe_combine leaves what moe_combine_send followed by moe_combine_recv leaves. One kernel
- * per phase and token batch unless MOE_FLAG_SEPARATE_MOVES or MOE_FLAG_DIRECT_PUSH. Arguments
+ * per phase and token batch (with or without MOE_FLAG_DIRECT_PUSH) unless
+ * MOE_FLAG_SEPARATE_MOVES. Arguments
  * as in those calls; the expert work goes between the two. Each phase may run in nb token batches
  * (nb = moe_batches(dims, lay, 2): lay->batches, else none up to 2048 tokens of all ranks
  * and about T/8 beyond, at most 16; one with MOE_FLAG_ONE_BATCH), batch j covering tokens
