@@ -583,6 +583,9 @@ def measure(wl, args, dist, device, peak: float, peak_kind: str, cpu_seconds: fl
     # the run asked for separate moves), reported beside the default
     ep.layout.flags = flags0 ^ 0x80
     other_ms, _, _ = step_region()
+    # and the separate kernels' whole-pass launches, each with its own roofline fraction
+    ep.layout.flags = flags0 | 0x80
+    pk_sep = kernel_region() if not args.separate_moves else {}
     ep.layout.flags = flags0
     one_ms_all = max_over_ranks(one_ms, dist, device)
     other_ms_all = max_over_ranks(other_ms, dist, device)
@@ -621,6 +624,12 @@ def measure(wl, args, dist, device, peak: float, peak_kind: str, cpu_seconds: fl
     pk_push = kernel_region()
     push_ms, _, _ = step_region()
     ep.layout.flags &= ~8
+    sep_kernels = {}
+    for name, ts in pk_sep.items():
+        if name == "expert":
+            continue
+        e = _kernel_entry(ab, name, ts, peak, K)
+        sep_kernels[name] = {k: e[k] for k in ("us", "gbs", "frac")}
     push_kernels = {}
     # with direct push the one-kernel phases write no send and no receive-order rows
     tokB, H2 = wl.N * wl.T * wl.row_bytes, 2 * wl.H
@@ -824,6 +833,7 @@ def measure(wl, args, dist, device, peak: float, peak_kind: str, cpu_seconds: fl
                               "the default splits it into token batches over two streams"},
         ("fused_moves" if args.separate_moves else "separate_moves"): {
             "value": round(tokens / (other_ms_all * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(other_ms_all, 4),
+            **({"kernels": sep_kernels} if sep_kernels else {}),
             "note": "the same step with each phase "
                     + ("in one kernel per token batch (the default)" if args.separate_moves else
                        "as separate kernels (MOE_FLAG_SEPARATE_MOVES: pack, write, shuffle; combine pack, "
