@@ -502,6 +502,19 @@ def test_fused_and_separate_moves_match_oracle(orc, wl, flags):
     compare_all(orc, wl, inp, res, fused_quant=True)
 
 
+@pytest.mark.parametrize("mode", ["forward", "phases"])
+@pytest.mark.parametrize("flags", [0x80, 0x88], ids=["separate", "separate-push"])
+@pytest.mark.parametrize("wl", MB_CASES, ids=lambda w: w.name)
+def test_separate_kernels_in_token_batches_match_oracle(orc, wl, flags, mode):
+    """MOE_FLAG_SEPARATE_MOVES in token batches (moe_forward's micro-batches and the
+    moe_dispatch / moe_combine phases, 3 batches), with and without direct push: every buffer
+    bit for bit as the oracle's."""
+    inp = workloads.make_inputs(wl)
+    _, res = run_gpu(wl, inp, flags=flags, batches=3, **{mode: True})
+    assert res["status_code"] == (3 if wl.cap else 0)
+    compare_all(orc, wl, inp, res, push=bool(flags & 8), fused_quant=True)
+
+
 @pytest.mark.parametrize("batches", [1, 3])
 @pytest.mark.parametrize("payload", ["bf16", "fp8"])
 def test_forward_direct_push_without_send_buffers(orc, payload, batches):
